@@ -1,0 +1,477 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+Closed forms, a library routine (torch's float32 -> bfloat16 rounding), an independent
+high-precision brute force (mpmath at 200 bits), and invariants the pages fix. The
+`planted` tests substitute a plausible mistake into the oracle (on the CPU) and show
+that one of the pins catches it.
+"""
+import math
+
+import mpmath
+import numpy as np
+import pytest
+import torch
+
+from oracle import ga_oracle as O
+from verify_gated_gqa_gb300 import synth
+
+mpmath.mp.prec = 200
+
+
+# ---------------------------------------------------------------- bf16 rounding
+def test_bf16_matches_torch_rne():
+    """Library routine: torch rounds float32 -> bfloat16 to nearest even."""
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(200000).astype(np.float32)
+    x = np.concatenate([x, (x * np.float32(1e-38)), (x * np.float32(1e30)),
+                        np.float32([3.3e38, -3.3e38, 0.0, -0.0])]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    got = O.bf16(x.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def test_bf16_ties_and_overflow():
+    assert O.bf16(1 + 2.0 ** -8) == 1.0                       # tie -> even (down)
+    assert O.bf16(1 + 3 * 2.0 ** -8) == 1 + 2.0 ** -6          # tie -> even (up)
+    assert O.bf16(-(1 + 3 * 2.0 ** -8)) == -(1 + 2.0 ** -6)
+    assert O.bf16(1 + 2.0 ** -8 + 2.0 ** -30) == 1 + 2.0 ** -7  # just above the tie
+    assert np.isinf(O.bf16(3.4e38))
+    assert O.bf16(2.0 ** -133) == 2.0 ** -133                  # smallest subnormal
+    # double rounding through float32 would give a different answer here:
+    x = 1 + 2.0 ** -8 + 2.0 ** -40   # float32(x) is the tie 1 + 2^-8 -> 1.0
+    assert O.bf16(x) == 1 + 2.0 ** -7
+
+
+def test_bf16_sig_unbounded_exponent():
+    x = 2.0 ** -140 * (1 + 2.0 ** -7 + 2.0 ** -12)
+    assert O.bf16_sig(x) == 2.0 ** -140 * (1 + 2.0 ** -7)
+    x = np.random.default_rng(2).standard_normal(1000) * 10
+    assert np.array_equal(O.bf16_sig(x), O.bf16(x))
+
+
+def test_ulp_closed_forms():
+    assert O.ulp_bf16(1.0) == 2.0 ** -7
+    assert O.ulp_bf16(1.99) == 2.0 ** -7
+    assert O.ulp_bf16(2.0) == 2.0 ** -6
+    assert O.ulp_bf16(0.0018157959) == 2.0 ** -17
+    assert O.ulp_bf16(-3.0) == 2.0 ** -6
+
+
+# ---------------------------------------------------------------- RoPE table
+def test_rope_table_position_zero_and_frequencies():
+    c, s = O.rope_tables(70000, rounded=False)
+    assert np.all(c[0] == 1.0) and np.all(s[0] == 0.0)
+    # angle of pair i at position 1 is 10^(-7 i / 32) (closed form of 1e7^(-2i/64))
+    theta = np.arctan2(s[1], c[1])
+    want = np.array([10.0 ** (-7.0 * i / 32.0) for i in range(32)])
+    assert np.allclose(theta, want, rtol=1e-12, atol=0)
+    # the angle grows linearly in the position (pair 31 never wraps before 70000)
+    p = np.array([1, 777, 65551])
+    assert np.allclose(np.arctan2(s[p, 31], c[p, 31]), p * want[31], rtol=1e-10)
+    assert np.allclose(c ** 2 + s ** 2, 1.0, atol=1e-15)
+
+
+def test_rope_table_rounded_once():
+    cu, su = O.rope_tables(4096, rounded=False)
+    cr, sr = O.rope_tables(4096, rounded=True)
+    assert np.array_equal(cr, O.bf16(cu)) and np.array_equal(sr, O.bf16(su))
+    # against mpmath at 200 bits, rounded once to bf16 with Python's own float rounding
+    for p, i in [(1, 0), (2054, 5), (4095, 31), (3000, 17)]:
+        ang = mpmath.mpf(p) * mpmath.power(mpmath.mpf(10) ** 7, -mpmath.mpf(2 * i) / 64)
+        want_c = _rne_bf16_mp(mpmath.cos(ang))
+        want_s = _rne_bf16_mp(mpmath.sin(ang))
+        assert cr[p, i] == want_c and sr[p, i] == want_s
+
+
+def _rne_bf16_mp(x):
+    """Independent RNE to bf16 from an mpmath value (exact rational arithmetic)."""
+    from fractions import Fraction
+    if x == 0:
+        return 0.0
+    f = Fraction(int(mpmath.floor(x * 2 ** 300)), 2 ** 300) if x > 0 else \
+        -Fraction(int(mpmath.floor(-x * 2 ** 300)), 2 ** 300)
+    sign = 1 if f > 0 else -1
+    a = abs(f)
+    e = math.floor(math.log2(float(a))) if float(a) > 0 else -200
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    q = Fraction(2) ** (max(e, -126) - 7)
+    n = a / q
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * float(fl * q)
+
+
+# ---------------------------------------------------------------- (1+w) RMSNorm
+def test_norm_constant_vector_closed_form():
+    for c in [1.0, -3.0, 0.015625, 40.0, 2.0 ** -10]:
+        for w in [0.0, 0.5, -0.25]:
+            x = np.full(256, c)
+            want = O.bf16(np.sign(c) * (1 + w) / math.sqrt(1 + O.EPS / (c * c)))
+            assert np.all(O.rms_norm_1pw(x, np.full(256, w)) == want)
+    assert np.all(O.rms_norm_1pw(np.zeros(256), np.zeros(256)) == 0.0)
+
+
+def test_norm_against_mpmath():
+    rng = np.random.default_rng(3)
+    x = O.bf16(rng.standard_normal((4, 256)))
+    w = O.bf16(0.1 * rng.standard_normal(256))
+    got = O.rms_norm_1pw(x, w)
+    for r in range(4):
+        ms = mpmath.fsum([mpmath.mpf(float(v)) ** 2 for v in x[r]]) / 256
+        inv = 1 / mpmath.sqrt(ms + mpmath.mpf(O.EPS))
+        for d in range(256):
+            want = _rne_bf16_mp(mpmath.mpf(float(x[r, d])) * inv * (1 + mpmath.mpf(float(w[d]))))
+            assert got[r, d] == want
+
+
+def test_norm_scale_invariance_without_eps():
+    x = O.bf16(np.random.default_rng(4).standard_normal(256))
+    w = np.zeros(256)
+    assert np.array_equal(O.rms_norm_1pw(4 * x, w, eps=0.0), O.rms_norm_1pw(x, w, eps=0.0))
+
+
+# ---------------------------------------------------------------- partial RoPE
+def test_rope_pairing_closed_form():
+    """A unit vector on dim i (i < 32) rotates into dims i and i+32 by angle i."""
+    c, s = O.rope_tables(100, rounded=False)
+    p = 37
+    for i in [0, 9, 31]:
+        x = np.zeros(256)
+        x[i] = 1.0
+        y = O.rope_partial(x, c[p], s[p], rounded=False)
+        want = np.zeros(256)
+        want[i], want[i + 32] = c[p, i], s[p, i]
+        assert np.array_equal(y, want)
+    x = np.zeros(256)
+    x[100] = 2.0
+    assert np.array_equal(O.rope_partial(x, c[p], s[p]), x)     # dims >= 64 pass through
+
+
+def test_rope_identity_norm_and_inverse():
+    rng = np.random.default_rng(5)
+    x = O.bf16(rng.standard_normal((3, 256)))
+    cr, sr = O.rope_tables(9000)
+    assert np.array_equal(O.rope_partial(x, cr[0], sr[0]), x)     # position 0 is the identity
+    c, s = O.rope_tables(9000, rounded=False)
+    p = 8191
+    y = O.rope_partial(x, c[p], s[p], rounded=False)
+    pair = lambda z: z[:, :32] ** 2 + z[:, 32:64] ** 2
+    assert np.allclose(pair(y), pair(x), rtol=1e-13)
+    back = O.rope_partial(y, c[p], -s[p], rounded=False)         # rotate by -angle
+    assert np.allclose(back, x, atol=1e-12)
+
+
+# ---------------------------------------------------------------- brute force attention
+def _mp_attention(qg, k, v, w_q, w_k, q_base, T, kind, mask=None, heads=(0, 12)):
+    """Textbook gated GQA attention at 200 bits, written directly from the pages'
+    description (no oracle code): split, (1+w) norm, partial RoPE at the exact angle,
+    score q.k/16, softmax over visible keys, P.V, times sigmoid(gate)."""
+    R = qg.shape[0]
+    eps = mpmath.mpf(O.EPS)
+
+    def norm(vec, w):
+        vec = [mpmath.mpf(float(a)) for a in vec]
+        ms = mpmath.fsum([a * a for a in vec]) / len(vec)
+        inv = 1 / mpmath.sqrt(ms + eps)
+        return [a * inv * (1 + mpmath.mpf(float(b))) for a, b in zip(vec, w)]
+
+    def rope(vec, pos):
+        out = list(vec)
+        for i in range(32):
+            ang = mpmath.mpf(pos) * mpmath.power(mpmath.mpf(10) ** 7, -mpmath.mpf(2 * i) / 64)
+            cs, sn = mpmath.cos(ang), mpmath.sin(ang)
+            out[i] = vec[i] * cs - vec[i + 32] * sn
+            out[i + 32] = vec[i + 32] * cs + vec[i] * sn
+        return out
+
+    keys = {kv: [rope(norm(k[j, kv], w_k), j) for j in range(T)] for kv in (0, 1)}
+    res = {}
+    for h in heads:
+        kv = h * 2 // 24
+        for r in range(R):
+            pos = q_base + r
+            q = rope(norm(qg[r, h, :256], w_q), pos)
+            vis = [j for j in range(T) if (j <= pos if kind == "causal" else
+                                           (True if kind == "bidirectional" else mask[r, j] != 0))]
+            sc = [mpmath.fsum([a * b for a, b in zip(q, keys[kv][j])]) / 16 for j in vis]
+            m = max(sc)
+            e = [mpmath.exp(x - m) for x in sc]
+            z = mpmath.fsum(e)
+            o = [mpmath.fsum([e[n] * mpmath.mpf(float(v[j, kv, d])) for n, j in enumerate(vis)]) / z
+                 for d in range(256)]
+            g = [1 / (1 + mpmath.exp(-mpmath.mpf(float(a)))) for a in qg[r, h, 256:]]
+            res[(r, h)] = np.array([float(a * b) for a, b in zip(o, g)])
+    return res
+
+
+def _small_case(S=6, seed=11):
+    qg, k, v, w_q, w_k = synth.attention_inputs(seed, S, S)
+    f = lambda t: t.double().numpy()
+    return f(qg), f(k), f(v), f(w_q), f(w_k)
+
+
+@pytest.mark.parametrize("kind,q_base", [("causal", 0), ("bidirectional", 0), ("causal", 3)])
+def test_f64_mode_equals_mp_bruteforce(kind, q_base):
+    qg, k, v, w_q, w_k = _small_case(S=6)
+    T = 6
+    rows = qg[: T - q_base]
+    ref = _mp_attention(rows, k, v, w_q, w_k, q_base, T, kind)
+    c, s = O.rope_tables(T, rounded=False)
+    kp = O.prep_keys(k, w_k, c, s, mode="F64")
+    out = O.prefill(rows, kp, v, w_q, c, s, q_base, T, causal=(kind == "causal"), mode="F64")
+    for (r, h), want in ref.items():
+        assert np.allclose(out[r, h * 256:(h + 1) * 256], want, rtol=1e-12, atol=1e-14)
+
+
+def test_r1_within_float64_bound_of_bruteforce():
+    """[WIDE] review §Kernel change: the flash kernel is checked against a float64
+    reference with a 1.6e-2 relative tolerance."""
+    qg, k, v, w_q, w_k = _small_case(S=8, seed=12)
+    ref = _mp_attention(qg, k, v, w_q, w_k, 0, 8, "causal")
+    c, s = O.rope_tables(8)
+    kp = O.prep_keys(k, w_k, c, s)
+    out = O.prefill(qg, kp, v, w_q, c, s, 0, 8)
+    for (r, h), want in ref.items():
+        got = out[r, h * 256:(h + 1) * 256]
+        assert np.linalg.norm(got - want) <= 1.6e-2 * np.linalg.norm(want)
+
+
+def test_masked_f64_equals_mp_bruteforce():
+    qg, k, v, w_q, w_k = _small_case(S=7, seed=13)
+    mask = (np.random.default_rng(6).random((7, 7)) < 0.5).astype(np.uint8)
+    mask[np.arange(7), np.arange(7)] = 1
+    ref = _mp_attention(qg, k, v, w_q, w_k, 0, 7, "mask", mask)
+    c, s = O.rope_tables(7, rounded=False)
+    kp = O.prep_keys(k, w_k, c, s, mode="F64")
+    out, _, _ = O.masked(qg, kp, v, w_q, c, s, 0, 7, mask, mode="F64")
+    for (r, h), want in ref.items():
+        assert np.allclose(out[r, h * 256:(h + 1) * 256], want, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- R1 = flash with integer max
+def _flash_integer_max(q_hat, k_hat, v, vis, tile):
+    """A flash pass in the kernels' recurrence: running max snapped to an integer in
+    log2 units, P = bf16(2^(t - M)), lazy power-of-two rescale of O and l."""
+    n, T = vis.shape
+    out = np.zeros((n, v.shape[1]))
+    for i in range(n):
+        M, l, o = None, 0.0, np.zeros(v.shape[1])
+        for j0 in range(0, T, tile):
+            idx = [j for j in range(j0, min(T, j0 + tile)) if vis[i, j]]
+            if not idx:
+                continue
+            t = np.array([O.bf16(q_hat[i] @ k_hat[j]) / 16.0 * math.log2(math.e) for j in idx])
+            need = math.ceil(t.max())
+            if M is None:
+                M = need
+            elif need > M + 8:
+                o *= 2.0 ** (M - need)
+                l *= 2.0 ** (M - need)
+                M = need
+            p = O.bf16(2.0 ** (t - M))
+            l += p.sum()
+            o += p @ v[idx]
+        out[i] = o / l
+    return O.bf16(out)
+
+
+def test_r1_is_flash_with_integer_max_any_tile():
+    rng = np.random.default_rng(7)
+    n, T = 5, 40
+    q = O.bf16(3 * rng.standard_normal((n, 256)))
+    k = O.bf16(rng.standard_normal((T, 256)))
+    v = O.bf16(rng.standard_normal((T, 256)))
+    vis = O.visibility("causal", np.arange(n) + 30, T)
+    g = np.full((n, 256), 30.0)                       # sigmoid rounds to exactly 1.0
+    want, _, _ = O.attend_head(q, g, k, v, vis)
+    for tile in (3, 8, 16):
+        got = _flash_integer_max(q, k, v, vis, tile)
+        assert np.allclose(got, want, rtol=0, atol=0) or \
+            np.all(O.within_tolerance(got, want, 1.0, 0.0))
+
+
+# ---------------------------------------------------------------- closed forms and invariants
+def _prepared(S=16, seed=21, T=None):
+    T = T or S
+    qg, k, v, w_q, w_k = synth.attention_inputs(seed, S, T)
+    f = lambda t: t.double().numpy()
+    qg, k, v, w_q, w_k = f(qg), f(k), f(v), f(w_q), f(w_k)
+    c, s = O.rope_tables(max(S, T))
+    return qg, O.prep_keys(k, w_k, c, s), v, w_q, c, s
+
+
+def test_zero_query_gives_mean_of_visible_values():
+    qg, kp, v, w_q, c, s = _prepared()
+    qg[:, :, :256] = 0.0                          # q = 0: every score is 0, every w_hat 1
+    out = O.prefill(qg, kp, v, w_q, c, s, 0, 16)
+    for r in [0, 5, 15]:
+        for h in [0, 13]:
+            kv = h // 12
+            o = O.bf16(v[: r + 1, kv].mean(axis=0))
+            want = O.bf16(o * O.bf16(1 / (1 + np.exp(-qg[r, h, 256:]))))
+            assert np.array_equal(out[r, h * 256:(h + 1) * 256], want)
+
+
+def test_constant_values_pass_through():
+    qg, kp, v, w_q, c, s = _prepared()
+    v[:, 0] = v[3, 0]
+    v[:, 1] = v[7, 1]
+    qg[:, :, 256:] = 30.0                          # sigmoid(30) rounds to 1.0
+    out = O.prefill(qg, kp, v, w_q, c, s, 0, 16)
+    for h in range(24):
+        assert np.all(out[:, h * 256:(h + 1) * 256] == v[3 if h < 12 else 7, h // 12])
+
+
+def test_single_visible_key_outputs_gated_value():
+    """The first causal row sees only key 0: out = bf16(v_0 * bf16(sigmoid(g)))."""
+    qg, kp, v, w_q, c, s = _prepared()
+    out = O.prefill(qg, kp, v, w_q, c, s, 0, 16)
+    for h in range(24):
+        g = qg[0, h, 256:]
+        want = O.bf16(v[0, h // 12] * O.bf16(1 / (1 + np.exp(-g))))
+        assert np.array_equal(out[0, h * 256:(h + 1) * 256], want)
+
+
+def test_gate_zero_halves_saturated_gate():
+    qg, kp, v, w_q, c, s = _prepared()
+    qg[:, :, 256:] = 0.0
+    half = O.prefill(qg, kp, v, w_q, c, s, 0, 16)
+    qg[:, :, 256:] = 30.0
+    full = O.prefill(qg, kp, v, w_q, c, s, 0, 16)
+    assert np.array_equal(half, full / 2)
+
+
+def test_future_and_masked_keys_do_not_matter():
+    qg, kp, v, w_q, c, s = _prepared()
+    base = O.prefill(qg, kp, v, w_q, c, s, 0, 16)
+    kp2, v2 = kp.copy(), v.copy()
+    kp2[10:] += 3.0
+    v2[10:] = -v2[10:]
+    pert = O.prefill(qg, kp2, v2, w_q, c, s, 0, 16)
+    assert np.array_equal(base[:10], pert[:10]) and not np.array_equal(base[10:], pert[10:])
+    mask = (np.random.default_rng(8).random((16, 16)) < 0.4).astype(np.uint8)
+    mask[np.arange(16), np.arange(16)] = 1
+    m1, _, _ = O.masked(qg, kp, v, w_q, c, s, 0, 16, mask)
+    kp3, v3 = kp.copy(), v.copy()
+    hid = np.nonzero(mask[5] == 0)[0]
+    kp3[hid] += 5.0
+    v3[hid] *= 3.0
+    m2, _, _ = O.masked(qg, kp3, v3, w_q, c, s, 0, 16, mask)
+    assert np.array_equal(m1[5], m2[5])
+
+
+def test_windows_equal_full_pass_rows():
+    """[WIDE] §Test Plan: prefix windows at q_base 64/128/1,024 match the full pass."""
+    S = 1088
+    qg, kp, v, w_q, c, s = _prepared(S=S, seed=22)
+    rows = np.array([0, 1, 63, 64, 127, 128, 500, 1023, 1024, 1087])
+    full = O.prefill(qg, kp, v, w_q, c, s, 0, S, rows=rows, heads=[0, 23])
+    for qb in (64, 128, 1024):
+        sel = rows[rows >= qb]
+        win = O.prefill(qg[qb:], kp, v, w_q, c, s, qb, S, rows=sel - qb, heads=[0, 23])
+        assert np.array_equal(win, full[rows >= qb])
+
+
+def test_bidirectional_and_causal_equal_masked():
+    qg, kp, v, w_q, c, s = _prepared()
+    bi = O.prefill(qg, kp, v, w_q, c, s, 0, 16, causal=False)
+    mb, _, _ = O.masked(qg, kp, v, w_q, c, s, 0, 16, np.ones((16, 16), np.uint8))
+    assert np.array_equal(bi, mb)
+    ca = O.prefill(qg, kp, v, w_q, c, s, 0, 16)
+    mc, _, _ = O.masked(qg, kp, v, w_q, c, s, 0, 16, np.tril(np.ones((16, 16), np.uint8)))
+    assert np.array_equal(ca, mc)
+
+
+def test_weights_rows_sum_to_one_and_hidden_are_zero():
+    """[QSA] review F2: each head's weights sum to 1 within 2e-3; blocked positions carry
+    exactly zero mass (the dump script's zero-mass assertion)."""
+    qg, kp, v, w_q, c, s = _prepared(S=64, seed=23)
+    mask = (np.random.default_rng(9).random((64, 64)) < 0.3).astype(np.uint8)
+    mask[np.arange(64), np.arange(64)] = 1
+    mask[7] = 0                                     # a fully hidden row
+    out, w, hid = O.masked(qg, kp, v, w_q, c, s, 0, 64, mask, want_weights=True)
+    assert hid[7] and hid.sum() == 1 and np.all(out[7] == 0) and np.all(w[:, 7] == 0)
+    vis = mask != 0
+    assert np.all(w[:, ~vis] == 0)
+    # each weight is bf16(w_hat / L) and sum_j w_hat_j / L = 1, so a row misses 1 by at
+    # most half an ulp per visible weight
+    sums = w.sum(axis=2)[:, ~hid]
+    bound = 0.5 * np.where(vis[None], O.ulp_bf16(w), 0.0).sum(axis=2)[:, ~hid]
+    assert np.all(np.abs(sums - 1) <= bound + 1e-12)
+
+
+def test_token_cap_row_weights_sum_to_one():
+    """[QSA] review F2: one query row over exactly 8192 all-visible keys; every head's
+    8192 weights are finite and sum to 1 within 2e-3."""
+    S = 8192
+    qg, k, v, w_q, w_k = synth.attention_inputs(25, 1, S)
+    f = lambda t: t.double().numpy()
+    qg, k, v, w_q, w_k = f(qg), f(k), f(v), f(w_q), f(w_k)
+    c, s = O.rope_tables(S)
+    kp = O.prep_keys(k, w_k, c, s)
+    out, w, hid = O.masked(qg, kp, v, w_q, c, s, S - 1, S, np.ones((1, S), np.uint8),
+                           want_weights=True)
+    assert np.all(np.isfinite(w)) and not hid.any()
+    assert np.all(np.abs(w.sum(axis=2) - 1) <= 2e-3)
+
+
+def test_verify_equals_prefill_rows():
+    L, R = 40, 4
+    qg_all, kp, v, w_q, c, s = _prepared(S=L + R, seed=24)
+    qg = qg_all[L:][None]
+    out = O.verify(qg, kp[None], v[None], [L], w_q, c, s)
+    full = O.prefill(qg_all, kp, v, w_q, c, s, 0, L + R)
+    assert np.array_equal(out[0], full[L:])
+
+
+# ---------------------------------------------------------------- planted mistakes
+def test_planted_unrounded_sigmoid_is_caught(monkeypatch):
+    """[QSA] §Validation, mutation calibration: dropping the sigmoid's bf16 rounding
+    must break an exact check."""
+    monkeypatch.setattr(O, "sigmoid_gate", lambda g, mode="R1": 1.0 / (1.0 + np.exp(-g)))
+    with pytest.raises(AssertionError):
+        test_single_visible_key_outputs_gated_value()
+
+
+def test_planted_kv_swap_is_caught(monkeypatch):
+    """[QSA] §Validation: exchanging the two KV heads must fail."""
+    monkeypatch.setattr(O, "GROUP", 1000)        # every head reads KV head 0
+    with pytest.raises(AssertionError):
+        test_f64_mode_equals_mp_bruteforce("causal", 0)
+
+
+def test_planted_interleaved_rope_is_caught(monkeypatch):
+    def interleaved(x, cos_rows, sin_rows, rounded=True):
+        x = np.asarray(x, dtype=np.float64)
+        y = x.copy()
+        a, b = x[..., 0:64:2], x[..., 1:64:2]
+        y[..., 0:64:2] = a * cos_rows - b * sin_rows
+        y[..., 1:64:2] = b * cos_rows + a * sin_rows
+        return y
+    monkeypatch.setattr(O, "rope_partial", interleaved)
+    with pytest.raises(AssertionError):
+        test_rope_pairing_closed_form()
+
+
+def test_planted_causal_for_sparse_mask_is_caught(monkeypatch):
+    """[QSA] §Validation: replacing the stored mask with plain causality must fail."""
+    real = O.visibility
+    monkeypatch.setattr(O, "visibility",
+                        lambda kind, rows, T, q_base=0, mask=None: real("causal", rows, T, q_base))
+    with pytest.raises(AssertionError):
+        test_masked_f64_equals_mp_bruteforce()
+
+
+def test_planted_eps_outside_sqrt_is_caught(monkeypatch):
+    def wrong(x, w, eps=O.EPS, rounded=True):
+        x = np.asarray(x, dtype=np.float64)
+        y = x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps) * (1.0 + w)
+        return O.bf16(y) if rounded else y
+    monkeypatch.setattr(O, "rms_norm_1pw", wrong)
+    with pytest.raises(AssertionError):
+        test_norm_constant_vector_closed_form()
