@@ -1,0 +1,375 @@
+"""Benchmark of the gated GQA attention hot path on GB300.
+
+Workload (one step): long causal prefill at S = 8192, batch 1, 24 query heads over 2 KV
+heads, head_dim 256, 64-dim partial RoPE, (1+w) RMSNorm: the K prologue over all 8192
+keys, then the full causal pass (Q prep, Q.K^T, online softmax, P.V, gated epilogue).
+Inputs are seeded synthetic bf16 N(0,1) activations and N(0,0.1) norm weights.
+
+Metric: algorithmic TFLOP/s, 4 * head_dim * heads per visible (query, key) pair (the
+convention under which pegainfer PR #1151's 2048 x 2048 table gives 0.93 TFLOP/s);
+tokens/s is reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs one independent sequence per GPU (weak scaling; no data-path collective:
+the process group only carries the barrier and the max-over-ranks time).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+S = 8192
+HEADS, KV_HEADS, DIM = 24, 2, 256
+SEED = 20261101 + 3
+METRIC = "causal prefill attention TFLOP/s at S=8192 (tokens/s beside)"
+UNIT = "TFLOP/s"
+WORKLOAD = "causal gated GQA prefill, batch 1, S=8192, 24q/2kv heads, d=256, rope 64/256"
+
+
+def visible_pairs_causal(rows: int, T: int, q_base: int = 0) -> int:
+    """Sum over rows of the keys a causal row sees (row r sees q_base + r + 1 keys)."""
+    first = q_base + 1
+    last = q_base + rows
+    return (first + last) * rows // 2
+
+
+def attention_flops(pairs: int) -> float:
+    return 4.0 * DIM * HEADS * pairs
+
+
+FLOPS_STEP = attention_flops(visible_pairs_causal(S, S))  # 824.73 GFLOP
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops"), d.get("hbm_gbs"), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, max clock, throttle reasons)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names[1:], r[5:9]):
+                if v.strip().lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        loaded = [x for x in sm if mx and x > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the GPU arm
+def make_inputs(device, seed):
+    from verify_gated_gqa_gb300 import synth
+    return synth.attention_inputs(seed, S, S, device=device)
+
+
+def run_gpu(args, world, rank, local):
+    from verify_gated_gqa_gb300 import binding as B
+    from verify_gated_gqa_gb300.build import build
+
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    qg, k, v, w_q, w_k = make_inputs(dev, SEED + rank)
+    c, s = B.ga_rope_table_host(S)
+    cos, sin = c.to(dev), s.to(dev)
+    k_prep = torch.empty_like(k)
+    out = torch.empty(S, HEADS * DIM, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        B.ga_k_prologue(k, w_k, cos, sin, k_prep=k_prep)
+        B.ga_attn_prefill(qg, k_prep, v, w_q, cos, sin, 0, S, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # device-timed region: K back-to-back steps; per-kernel events on the same stream
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        B.ga_k_prologue(k, w_k, cos, sin, k_prep=k_prep)
+        ev[i][1].record(stream)
+        B.ga_attn_prefill(qg, k_prep, v, w_q, cos, sin, 0, S, out=out)
+        ev[i][2].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    ms_step = total_ms / args.steps
+    attn_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps))
+    pro_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
+    status = B.ga_device_status()
+
+    # end to end through the C ABI with host buffers: H2D of the step's inputs, the two
+    # calls, D2H of the output, every step
+    host_in = [t.cpu().pin_memory() for t in (qg, k, v, w_q, w_k, cos, sin)]
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        qg_d, k_d, v_d, wq_d, wk_d, cos_d, sin_d = dev_in
+        B.ga_k_prologue(k_d, wk_d, cos_d, sin_d, k_prep=k_prep)
+        B.ga_attn_prefill(qg_d, k_prep, v_d, wq_d, cos_d, sin_d, 0, S, out=out)
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    if rank != 0:
+        return None
+    peak_tf, peak_hbm, peak_src = measured_peaks()
+    achieved = FLOPS_STEP / (attn_ms * 1e-3) / 1e12
+    value = world * FLOPS_STEP / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.1) norm weights)",
+        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": S,
+                   "parallelism": f"independent sequence per GPU x{world}",
+                   "l2": "inputs larger than L2 (qg 192 MiB read + out 96 MiB written per step)",
+                   "step": "ga_k_prologue (8192 keys) + ga_attn_prefill (8192 rows, causal)"},
+        "tokens_per_s": round(world * S / (ms_step * 1e-3), 1),
+        "kernel_ms": {"attn_kernel": round(attn_ms, 4), "k_prologue_kernel": round(pro_ms, 4)},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
+                     "traffic": ATTN_TRAFFIC_BYTES,
+                     "peak_kind": f"dense bf16 burst ({peak_src})",
+                     "kernel": "attn_kernel", "algorithmic_flops": FLOPS_STEP},
+        "e2e": {"value": round(world * FLOPS_STEP / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "device_status": status,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+# Per-launch DRAM bytes of attn_kernel (dram__bytes_read.sum + dram__bytes_write.sum) from
+# the ncu capture summarised in profiles/; None until a capture of the current kernel.
+ATTN_TRAFFIC_BYTES = None
+
+
+# ---------------------------------------------------------------- the oracle as baseline
+def oracle_sample_step(qg, kraw, v, w_q, w_k, cos, sin, rows):
+    """One bounded sample of the workload in the CPU oracle: the K prologue over all keys
+    and the causal attention of the listed query rows (all 24 heads)."""
+    from oracle import ga_oracle as O
+    kp = O.prep_keys(kraw, w_k, cos, sin)
+    return O.prefill(qg, kp, v, w_q, cos, sin, 0, S, True, "R1", rows=rows)
+
+
+def _oracle_inputs():
+    import numpy as np  # noqa: F401
+    from oracle import ga_oracle as O
+    from verify_gated_gqa_gb300 import synth
+    qg, k, v, w_q, w_k = synth.attention_inputs(SEED, S, S)
+    f = lambda t: t.double().numpy()
+    cos, sin = O.rope_tables(S)
+    return f(qg), f(k), f(v), f(w_q), f(w_k), cos, sin
+
+
+def _threads_used():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((p.get("num_threads", 1) for p in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(seconds: float):
+    import numpy as np
+    data = _oracle_inputs()
+    rng = np.random.default_rng(0)
+    pairs = 0
+    t0 = time.perf_counter()
+    n_rows = 0
+    while time.perf_counter() - t0 < seconds:
+        rows = np.sort(rng.choice(S, 16, replace=False))
+        oracle_sample_step(*data, rows)
+        pairs += int((rows + 1).sum())
+        n_rows += 16
+    dt = time.perf_counter() - t0
+    return {"value": round(attention_flops(pairs) / dt / 1e12, 6), "unit": UNIT,
+            "cores": _threads_used(), "kind": "oracle",
+            "sample": f"{n_rows} random query rows x 24 heads of the S=8192 causal pass, each "
+                      f"16-row batch with the K prologue over all 8192 keys; {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle, as it stands, on this machine's host cores."""
+    if rank != 0:
+        return None
+    import numpy as np
+    data = _oracle_inputs()
+    rng = np.random.default_rng(1)
+    per_step_rows = 2
+
+    def one():
+        rows = np.sort(rng.choice(S, per_step_rows, replace=False))
+        oracle_sample_step(*data, rows)
+        return int((rows + 1).sum())
+
+    for _ in range(args.warmup):
+        one()
+    pairs = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        pairs += one()
+    dt = time.perf_counter() - t0
+    value = attention_flops(pairs) / dt / 1e12
+    sample = (f"{per_step_rows} random query rows x 24 heads of the S=8192 causal pass per "
+              f"step, with the K prologue over all 8192 keys")
+    return {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.1) norm weights)",
+        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": S,
+                   "parallelism": "none (CPU oracle)"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": _threads_used(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_gpu(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * ga_attn.h -- C ABI of the GB300 (sm_103a) gated grouped-query attention library
+ * (libga_attn.so).
+ *
+ * The operation (pegainfer PR #1151, "feat(qwen4): add the QSA sparse-attention kernel
+ * and its golden", §Semantics): split each fused q|gate row, apply (1+w) RMSNorm to q
+ * and k (eps 1e-6), rotate dims 0..63 of q and k (rotate-half partial RoPE) from a
+ * shared bf16 cos/sin table, score s = bf16(q.k) / 16 over GQA groups of 12 (query
+ * head h reads KV head h / 12), softmax in fp32 over the visible keys with the weights
+ * rounded to bf16 before the context reduction, reduce P.V, and multiply by
+ * bf16(sigmoid(gate)). Output columns are head-major (h * 256 + d).
+ *
+ * Geometry is compiled in: 24 query heads, 2 KV heads, head_dim 256, 64 rotary dims,
+ * eps 1e-6, RoPE base 1e7 (the same page, the commit that replaces the proxy geometry).
+ *
+ * Conventions for every entry point below:
+ *  - Tensor pointers are DEVICE pointers owned by the caller, unless a comment says
+ *    HOST. The library never allocates device memory on a call path, and keeps no
+ *    pointer after the call returns. bf16 values are passed as their 16-bit patterns
+ *    (ga_bf16). All tensors are dense, row-major, without padding unless a leading
+ *    dimension argument says otherwise.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *    and is asynchronous: the return value reports argument validation and launch
+ *    errors, not the kernels' completion. Calls on different streams are re-entrant.
+ *  - Every argument is validated BEFORE any CUDA call (system1-omni PR #99, "run
+ *    prompts that share prefixes once per prefix": refusals happen before any
+ *    allocation or CUDA call). A zero-row call returns GA_OK without touching the GPU
+ *    (pegainfer PR #1151, §What changed: an empty launch is a no-op).
+ *  - There is no fallback path: a launch failure is returned as GA_ERR_CUDA with the
+ *    CUDA error kept for ga_last_cuda_error() (system1-omni PR #202, "cuda: widen the
+ *    attention query tile on sm_89 and sm_120", review §Dispatch/guard: no silent
+ *    fallback).
+ *  - Kernels never trap. A bounded device-side wait that gives up records an error in
+ *    the library's device status word (ga_device_status).
+ *  - Pointers that the kernels read or write with 16-byte vector or TMA accesses must be
+ *    16-byte aligned (GA_ERR_ALIGN otherwise).
+ */
+#ifndef GA_ATTN_H
+#define GA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GA_ABI_VERSION 1
+
+#define GA_N_Q_HEADS 24
+#define GA_N_KV_HEADS 2
+#define GA_HEAD_DIM 256
+#define GA_ROPE_DIMS 64
+#define GA_MASKED_MAX_TOKENS 8192 /* pegainfer PR #1151, §Summary: the 8192-token cap */
+#define GA_MAX_TOKENS (1 << 20)   /* index-arithmetic limit of this build */
+
+typedef uint16_t ga_bf16; /* bfloat16 bit pattern */
+typedef void* ga_stream;  /* cudaStream_t */
+
+enum ga_status {
+  GA_OK = 0,
+  GA_ERR_NULL = -1,      /* a required pointer is NULL */
+  GA_ERR_SHAPE = -2,     /* a size is negative or zero where it must be positive */
+  GA_ERR_ALIGN = -3,     /* a pointer or leading dimension breaks 16-byte alignment */
+  GA_ERR_RANGE = -4,     /* a window, position or size is outside what the call allows */
+  GA_ERR_TABLE = -5,     /* the cos/sin table is shorter than the largest position + 1 */
+  GA_ERR_WORKSPACE = -6, /* workspace missing, misaligned or smaller than required */
+  GA_ERR_DEVICE = -7,    /* current device is not sm_103 or refused the smem opt-in */
+  GA_ERR_CUDA = -8,      /* a CUDA call failed; see ga_last_cuda_error() */
+  GA_ERR_GEOMETRY = -9   /* ga_check_geometry: not this build's compiled geometry */
+};
+
+/* Geometry a caller expects; ga_check_geometry compares it with the compiled constants
+ * (pegainfer PR #1151, §What changed: the wrapper validates its geometry against the
+ * compiled constants before sizing any buffer). */
+typedef struct ga_geometry {
+  int n_q_heads;    /* 24 */
+  int n_kv_heads;   /* 2 */
+  int head_dim;     /* 256 */
+  int rope_dims;    /* 64 */
+  float eps;        /* 1e-6 */
+  double rope_base; /* 1e7 */
+} ga_geometry;
+
+/* GA_ABI_VERSION of the loaded library. */
+int ga_abi_version(void);
+
+/* GA_OK if *g equals the compiled geometry, GA_ERR_GEOMETRY if not, GA_ERR_NULL for NULL. */
+int ga_check_geometry(const ga_geometry* g);
+
+/* Static English text for a status code (never NULL). */
+const char* ga_status_string(int status);
+
+/* The cudaError_t value behind the calling thread's last GA_ERR_CUDA (0 if none). */
+int ga_last_cuda_error(void);
+
+/* Number of CUDA runtime calls this library has made in this process (diagnostic: a
+ * refused call must not change it). Makes no CUDA call itself. */
+unsigned long long ga_debug_cuda_calls(void);
+
+/* Reads the current device's status word, written by kernels whose bounded waits gave
+ * up (0 = no error, 1 = wait timeout). Synchronises the device. clear != 0 resets the
+ * word afterwards. */
+int ga_device_status(int* status_out, int clear);
+
+/* HOST helper. Fills cos_out and sin_out (HOST arrays of n_pos * 32 values each,
+ * [position][pair]) with cos and sin of p * 1e7^(-2i/64) for positions p < n_pos and
+ * pairs i < 32, each computed in double and rounded once to bf16 (pegainfer PR #1151,
+ * review F4: a double pow, rounded once; §What changed: one shared table, no device
+ * trigonometry). Pair i rotates dims i and i + 32. Makes no CUDA call. */
+int ga_rope_table_host(int n_pos, ga_bf16* cos_out, ga_bf16* sin_out);
+
+/* K prologue (pegainfer PR #1151, §What changed: one key pass (1+w)-norms and partially
+ * rotates every token's two key heads once, because all twelve query heads of a KV head
+ * read the same prepared key).
+ *   k_raw  [n_tok][2][256]  raw keys of tokens at positions pos_base .. pos_base+n_tok-1
+ *   w_k    [256]            key norm weight w (applied as 1 + w)
+ *   cos_tab, sin_tab [table_rows][32]; table_rows >= pos_base + n_tok
+ *   k_prep [n_tok][2][256]  output: bf16(rope(norm(k))); may not alias k_raw
+ * Errors: NULL, SHAPE (n_tok < 0), RANGE (pos_base < 0 or n_tok > GA_MAX_TOKENS), TABLE,
+ * ALIGN (k_raw, k_prep, cos_tab, sin_tab, w_k), DEVICE, CUDA. */
+int ga_k_prologue(const ga_bf16* k_raw, const ga_bf16* w_k, const ga_bf16* cos_tab,
+                  const ga_bf16* sin_tab, int table_rows, int n_tok, int pos_base,
+                  ga_bf16* k_prep, ga_stream stream);
+
+/* Causal / prefix-window / bidirectional gated GQA attention (system1-omni PR #202,
+ * §Scope: full pass, causal or bidirectional, and causal prefix windows at q_base).
+ *   qg      [rows][24][512]  fused rows of query positions q_base .. q_base+rows-1; per
+ *                            head the first 256 values are q, the last 256 the gate
+ *   k_prep  [T][2][256]      prepared keys (ga_k_prologue) of positions 0 .. T-1
+ *   v       [T][2][256]      values
+ *   w_q     [256]            query norm weight w (applied as 1 + w)
+ *   cos_tab, sin_tab [table_rows][32]; table_rows >= q_base + rows
+ *   causal  1: row r sees keys j <= q_base + r;  0: bidirectional, every key j < T
+ *           (q_base must then be 0)
+ *   out     [rows][24 * 256] bf16, head-major columns
+ *   row_stats NULL or [24][rows][2] float: per (head, row) the final running maximum M
+ *           (an integer, base-2 units) and the sum l of the rounded weights relative to
+ *           2^M, so that the row's weights are bf16(2^(t - M)) / l with t = s * log2(e).
+ * Rules (review §Dispatch/guard of the same page): q_base % 64 == 0, q_base >= 0,
+ * q_base + rows <= T <= GA_MAX_TOKENS.
+ * Errors: NULL, SHAPE, RANGE, TABLE, ALIGN (qg, k_prep, v, out, w_q, tables, row_stats),
+ * DEVICE, CUDA. */
+int ga_attn_prefill(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                    const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                    int table_rows, int rows, int T, int q_base, int causal, ga_bf16* out,
+                    float* row_stats, ga_stream stream);
+
+/* Bytes of workspace ga_attn_masked needs for (rows, T); 0 for invalid sizes. */
+size_t ga_masked_workspace_bytes(int rows, int T);
+
+/* Stored-mask gated GQA attention (pegainfer PR #1151, §Semantics: the kernel consumes
+ * the selection mask as given, non-zero = visible; it is not ANDed with causality here).
+ *   qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, q_base: as in ga_attn_prefill
+ *   mask    [rows][ld_mask] uint8; row r is query position q_base + r, column j key j
+ *   out     [rows][24 * 256]
+ *   weights NULL or [24][rows][T] bf16: the normalised weights bf16(w_hat / L), exactly
+ *           0 where a key is hidden
+ *   hidden_rows NULL or one device int; receives the number of rows with no visible key
+ *           (their outputs and weights are 0; the page leaves such rows outside its
+ *           contract)
+ *   workspace >= ga_masked_workspace_bytes(rows, T) bytes of device memory, 256-byte
+ *           aligned, owned by the caller, not shared with a concurrent call
+ * Rules: T <= GA_MASKED_MAX_TOKENS, ld_mask >= T, ld_mask % 16 == 0, q_base % 64 == 0,
+ * q_base + rows <= T.
+ * Errors: NULL, SHAPE, RANGE, TABLE, ALIGN (mask also), WORKSPACE, DEVICE, CUDA. */
+int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                   const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                   int table_rows, int rows, int T, int q_base, const uint8_t* mask,
+                   long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
+                   void* workspace, size_t ws_bytes, ga_stream stream);
+
+/* Bytes of workspace ga_attn_verify needs; max_len is the largest L over the sequences. */
+size_t ga_verify_workspace_bytes(int n_seq, int rows, int max_len);
+
+/* Few-row verify windows over long caches, split over key chunks with a log-sum-exp
+ * combine (TensorFold PR #1080, "qwen CUDA: long-prompt prefill 5.4x faster", the
+ * attn_partial commit: keys split into chunks, partial rows combined afterwards).
+ *   qg       [n_seq][rows][24][512] fused rows; sequence b's row r is position L_b + r
+ *   k_cache  [n_seq][cap][2][256] PREPARED keys of positions 0 .. L_b+rows-1 (the
+ *            window's own keys included; fill with ga_k_prologue)
+ *   v_cache  [n_seq][cap][2][256] values
+ *   seq_len  HOST array of n_seq ints: L_b, with L_b >= 0 and L_b + rows <= cap
+ *   out      [n_seq][rows][24 * 256]
+ *   workspace >= ga_verify_workspace_bytes(n_seq, rows, max L_b), 256-byte aligned
+ * Row r of sequence b sees keys 0 .. L_b + r.
+ * Rules: 1 <= rows <= 16, cap <= GA_MAX_TOKENS, table_rows >= max L_b + rows.
+ * Errors: NULL, SHAPE, RANGE, TABLE, ALIGN, WORKSPACE, DEVICE, CUDA. */
+int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_cache,
+                   int cap, const int* seq_len, int n_seq, int rows, const ga_bf16* w_q,
+                   const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
+                   ga_bf16* out, void* workspace, size_t ws_bytes, ga_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GA_ATTN_H */

@@ -212,17 +212,22 @@ def sigmoid_gate(g, mode="R1"):
     return s if mode == "F64" else bf16(s)
 
 
-def attend_head(q_hat, gate, k_hat, v, vis, mode="R1", want_weights=False):
-    """One query head over its KV head.
-
-    q_hat, gate: [n, 256]; k_hat, v: [T, 256]; vis: bool [n, T].
-    Returns (out [n, 256], weights [n, T] or None, hidden bool [n]).
-    Score s = bf16(q.k) * 2^-4 (the exact 1/sqrt(256) after the bf16 rounding of the dot
-    product). A row with no visible key outputs zeros (the pages leave it outside the
-    contract; it is flagged in `hidden`).
-    """
+def scores(q_hat, k_hat, mode="R1"):
+    """s_ij = bf16(q_i . k_j) * 2^-4: the bf16 rounding of the dot product, then the exact
+    1/sqrt(256) ([QSA] attention-reader commit: "the score is the bf16 GEMM result rounded
+    before the exact 1/16 scale"). The dot product is formed in float64 (exact for these
+    bf16 inputs up to float64 rounding of the running sum)."""
     dot = q_hat @ k_hat.T
-    s = dot / 16.0 if mode == "F64" else bf16(dot) / 16.0
+    return dot / 16.0 if mode == "F64" else bf16(dot) / 16.0
+
+
+def attend_scores(s, gate, v, vis, mode="R1", want_weights=False):
+    """Softmax over the visible scores, P.V and the gate for one query head.
+
+    s: [n, T] scores; gate: [n, 256]; v: [T, 256]; vis: bool [n, T].
+    Returns (out [n, 256], weights [n, T] or None, hidden bool [n]). A row with no visible
+    key outputs zeros (the pages leave it outside the contract; it is flagged in `hidden`).
+    """
     hidden = ~vis.any(axis=1)
     weights = None
     if mode == "R1":
@@ -249,6 +254,11 @@ def attend_head(q_hat, gate, k_hat, v, vis, mode="R1", want_weights=False):
     out = o * sig if mode == "F64" else bf16(o * sig)
     out = np.where(hidden[:, None], 0.0, out)
     return out, weights, hidden
+
+
+def attend_head(q_hat, gate, k_hat, v, vis, mode="R1", want_weights=False):
+    """One query head over its KV head: q_hat, gate [n, 256]; k_hat, v [T, 256]; vis [n, T]."""
+    return attend_scores(scores(q_hat, k_hat, mode), gate, v, vis, mode, want_weights)
 
 
 def attention(q_hat, gate, k_hat, v, vis, mode="R1", heads=None, want_weights=False):

@@ -1,0 +1,173 @@
+"""The C ABI without a GPU: the library loads, exports every symbol include/ga_attn.h
+declares, validates every argument before any CUDA call, and its host-side RoPE table is
+bit-identical to the oracle's.
+
+Refusal tests pass fake pointer values: a refused call never dereferences them (it
+returns before any device work), and the library's CUDA-call counter proves it made no
+CUDA call at all (system1-omni PR #99: refusals happen before any allocation or CUDA
+call; pegainfer PR #1151 review F11: 9 geometry/range refusals, 5 null pointers and 2
+zero-length positive controls, device-free).
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import ga_oracle as O
+from verify_gated_gqa_gb300 import binding as B
+from verify_gated_gqa_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return B.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    header = open(os.path.join(ROOT, "include", "ga_attn.h")).read()
+    names = set(re.findall(r"^\s*(?:int|size_t|const char\*|unsigned long long)\s+(ga_\w+)\s*\(",
+                           header, re.M))
+    assert names, "no declarations found"
+    for n in sorted(names):
+        assert hasattr(L, n), n
+    assert names == set(B.exported_symbols())
+
+
+def test_version_geometry_status(L):
+    assert B.ga_abi_version() == 1
+    assert B.ga_check_geometry() == 0
+    assert B.ga_check_geometry(head_dim=128) == -9
+    assert B.ga_check_geometry(n_kv_heads=4) == -9
+    assert B.ga_check_geometry(rope_base=1e6) == -9
+    assert L.ga_check_geometry(None) == -1
+    for st in range(-9, 1):
+        assert B.ga_status_string(st)
+    assert "unknown" in B.ga_status_string(-100)
+
+
+def test_rope_table_matches_oracle_bit_for_bit(L):
+    n = 65552
+    c, s = B.ga_rope_table_host(n)
+    oc, os_ = O.rope_tables(n)
+    assert np.array_equal(c.double().numpy(), oc)
+    assert np.array_equal(s.double().numpy(), os_)
+
+
+# ------------------------------------------------------------------ refusals
+A = 0x10000        # a 16-byte-aligned fake device address (never dereferenced)
+MIS = 0x10002      # misaligned
+S = None           # stream
+
+
+def _prefill(L, **kw):
+    args = dict(qg=A, k=A, v=A, wq=A, cos=A, sin=A, table=8192, rows=128, T=8192, q_base=0,
+                causal=1, out=A, stats=None)
+    args.update(kw)
+    return L.ga_attn_prefill(args["qg"], args["k"], args["v"], args["wq"], args["cos"],
+                             args["sin"], args["table"], args["rows"], args["T"],
+                             args["q_base"], args["causal"], args["out"], args["stats"], S)
+
+
+def _masked(L, **kw):
+    ws_need = L.ga_masked_workspace_bytes(128, 1024)
+    args = dict(qg=A, k=A, v=A, wq=A, cos=A, sin=A, table=1024, rows=128, T=1024, q_base=0,
+                mask=A, ld=1024, out=A, w=None, hid=None, ws=0x100000, wsb=ws_need)
+    args.update(kw)
+    return L.ga_attn_masked(args["qg"], args["k"], args["v"], args["wq"], args["cos"],
+                            args["sin"], args["table"], args["rows"], args["T"], args["q_base"],
+                            args["mask"], args["ld"], args["out"], args["w"], args["hid"],
+                            args["ws"], args["wsb"], S)
+
+
+def _verify(L, lens=(1000, 2000), **kw):
+    n = len(lens)
+    arr = (ctypes.c_int * n)(*lens)
+    wsb = L.ga_verify_workspace_bytes(n, 16, max(lens))
+    args = dict(qg=A, k=A, v=A, cap=4096, arr=arr, n=n, rows=16, wq=A, cos=A, sin=A,
+                table=4096, out=A, ws=0x100000, wsb=wsb)
+    args.update(kw)
+    return L.ga_attn_verify(args["qg"], args["k"], args["v"], args["cap"], args["arr"],
+                            args["n"], args["rows"], args["wq"], args["cos"], args["sin"],
+                            args["table"], args["out"], args["ws"], args["wsb"], S)
+
+
+PREFILL_REFUSALS = [
+    (dict(qg=None), -1), (dict(k=None), -1), (dict(v=None), -1), (dict(wq=None), -1),
+    (dict(cos=None), -1), (dict(sin=None), -1), (dict(out=None), -1),
+    (dict(rows=-1), -2), (dict(T=0), -2), (dict(table=-1), -2),
+    (dict(q_base=32, rows=64), -4), (dict(q_base=-64), -4),
+    (dict(q_base=8192 - 64, rows=128), -4), (dict(T=(1 << 20) + 1, table=(1 << 20) + 1), -4),
+    (dict(causal=0, q_base=64, rows=64), -4), (dict(causal=2), -4),
+    (dict(table=127), -5), (dict(q_base=4096, table=4096 + 127), -5),
+    (dict(qg=MIS), -3), (dict(k=MIS), -3), (dict(out=MIS), -3), (dict(cos=MIS), -3),
+    (dict(stats=MIS + 1), -3),
+]
+
+
+@pytest.mark.parametrize("kw,want", PREFILL_REFUSALS)
+def test_prefill_refusals_make_no_cuda_call(L, kw, want):
+    before = L.ga_debug_cuda_calls()
+    assert _prefill(L, **kw) == want
+    assert L.ga_debug_cuda_calls() == before
+
+
+MASKED_REFUSALS = [
+    (dict(mask=None), -1), (dict(T=8193, ld=8208, table=8193), -4), (dict(ld=1000), -4),
+    (dict(ld=1036), -3), (dict(mask=MIS), -3), (dict(w=MIS), -3),
+    (dict(ws=None), -6), (dict(wsb=100), -6), (dict(ws=0x100010), -6),
+    (dict(q_base=64, rows=1024), -4),
+]
+
+
+@pytest.mark.parametrize("kw,want", MASKED_REFUSALS)
+def test_masked_refusals_make_no_cuda_call(L, kw, want):
+    before = L.ga_debug_cuda_calls()
+    assert _masked(L, **kw) == want
+    assert L.ga_debug_cuda_calls() == before
+
+
+def test_verify_refusals_make_no_cuda_call(L):
+    cases = [
+        (dict(rows=17), -4), (dict(cap=0), -2), (dict(qg=None), -1), (dict(arr=None), -1),
+        (dict(table=1000), -5), (dict(ws=None), -6), (dict(wsb=0), -6), (dict(k=MIS), -3),
+    ]
+    for kw, want in cases:
+        before = L.ga_debug_cuda_calls()
+        assert _verify(L, **kw) == want, kw
+        assert L.ga_debug_cuda_calls() == before
+    before = L.ga_debug_cuda_calls()
+    assert _verify(L, lens=(1000, 4090)) == -4        # L + rows beyond the cache
+    assert _verify(L, lens=(-1, 5)) == -4
+    assert L.ga_debug_cuda_calls() == before
+
+
+def test_k_prologue_refusals(L):
+    before = L.ga_debug_cuda_calls()
+    assert L.ga_k_prologue(None, A, A, A, 100, 10, 0, A, S) == -1
+    assert L.ga_k_prologue(A, A, A, A, 100, -1, 0, A, S) == -2
+    assert L.ga_k_prologue(A, A, A, A, 100, 10, -1, A, S) == -4
+    assert L.ga_k_prologue(A, A, A, A, 100, 10, 95, A, S) == -5
+    assert L.ga_k_prologue(A, A, A, A, 100, 10, 0, MIS, S) == -3
+    assert L.ga_debug_cuda_calls() == before
+
+
+def test_empty_calls_are_noops_without_cuda(L):
+    before = L.ga_debug_cuda_calls()
+    assert _prefill(L, rows=0) == 0
+    assert _masked(L, rows=0, wsb=L.ga_masked_workspace_bytes(0, 1024)) == 0
+    assert _verify(L, rows=0, wsb=256) == 0
+    assert L.ga_k_prologue(A, A, A, A, 100, 0, 0, A, S) == 0
+    assert L.ga_debug_cuda_calls() == before
+
+
+def test_workspace_sizes(L):
+    assert L.ga_masked_workspace_bytes(8192, 8192) >= 8192 * 256 * 4 + 64 * 64 + 24 * 8192 * 8
+    assert L.ga_masked_workspace_bytes(1, 8193) == 0
+    assert L.ga_masked_workspace_bytes(-1, 10) == 0
+    assert L.ga_verify_workspace_bytes(0, 16, 10) == 0

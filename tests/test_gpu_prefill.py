@@ -1,0 +1,167 @@
+"""GPU parity of the K prologue and the causal / window / bidirectional attention against
+the CPU oracle, through the C ABI (ctypes binding)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import ga_oracle as O
+from tests.parity import SEED, Inputs, compare, np64
+from verify_gated_gqa_gb300 import binding as B
+from verify_gated_gqa_gb300 import build as build_mod
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build_mod.build()
+    B.lib()
+    assert torch.cuda.is_available()
+    yield
+    assert B.ga_device_status() == 0
+
+
+def _oracle_prefill(inp, q_base, T, causal, rows=None, heads=None, mode="R1", qg=None):
+    c, s = inp.oracle_tables(mode)
+    kp = O.prep_keys(inp.np["k"], inp.np["w_k"], c, s, mode=mode)
+    qg = inp.np["qg"] if qg is None else qg
+    return O.prefill(qg, kp, inp.np["v"], inp.np["w_q"], c, s, q_base, T, causal, mode,
+                     rows=rows, heads=heads)
+
+
+# ------------------------------------------------------------------ K prologue
+@pytest.mark.parametrize("T,pos_base", [(2048, 0), (333, 777)])
+def test_k_prologue_bit_exact(T, pos_base):
+    inp = Inputs(SEED + 7, 1, T)
+    c, s = B.ga_rope_table_host(pos_base + T)
+    d = inp.dev()
+    got = B.ga_k_prologue(d["k"], d["w_k"], c.cuda(), s.cuda(), pos_base=pos_base)
+    oc, os_ = O.rope_tables(pos_base + T)
+    want = O.prep_keys(inp.np["k"], inp.np["w_k"], oc, os_, pos0=pos_base)
+    g = np64(got)
+    assert np.array_equal(g, want), f"{int((g != want).sum())} of {g.size} differ"
+
+
+# ------------------------------------------------------------------ tiny and S=2048
+def test_prefill_tiny_s64_all_heads():
+    inp = Inputs(SEED + 1, 64, 64)
+    d = inp.dev()
+    got = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, 64)
+    inp.ref(0, 64, "causal").check(got, what="S=64 causal")
+    for mode in ("R2", "F64"):   # information: the other readings of the rounding point
+        print(f"[info] S=64 GPU vs {mode}:", compare(got, _oracle_prefill(inp, 0, 64, True, mode=mode)))
+
+
+def test_prefill_causal_s2048_all_heads():
+    inp = Inputs(SEED + 2, 2048, 2048)
+    d = inp.dev()
+    got = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, 2048)
+    inp.ref(0, 2048, "causal").check(got, what="S=2048 causal, all rows and heads")
+
+
+def test_prefill_bidirectional_s2048():
+    inp = Inputs(SEED + 2, 2048, 2048)
+    d = inp.dev()
+    got = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, 2048,
+                            causal=False)
+    heads = [0, 7, 11, 12, 18, 23]
+    inp.ref(0, 2048, "bidirectional", heads=heads).check(
+        got, what="S=2048 bidirectional (6 heads, all rows)")
+    rows = np.array([0, 1, 127, 128, 1000, 2047])
+    inp.ref(0, 2048, "bidirectional", rows=rows).check(
+        got[torch.as_tensor(rows)], what="S=2048 bidirectional (all heads, 6 rows)")
+
+
+# ------------------------------------------------------------------ ragged and windows
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_ragged_rows_and_keys(causal):
+    S = 333
+    inp = Inputs(SEED + 3, S, S)
+    d = inp.dev()
+    got = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, S,
+                            causal=causal)
+    inp.ref(0, S, "causal" if causal else "bidirectional").check(got, what=f"S=333 causal={causal}")
+
+
+@pytest.mark.parametrize("q_base", [64, 128, 192])
+def test_prefix_window_ragged(q_base):
+    S = 333
+    inp = Inputs(SEED + 3, S, S)
+    d = inp.dev()
+    got = B.ga_attn_prefill(d["qg"][q_base:], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"],
+                            q_base, S)
+    inp.ref(q_base, S, "causal", qg=inp.np["qg"][q_base:]).check(got, what=f"window q_base={q_base}")
+
+
+def test_windows_bit_identical_to_full_pass():
+    """system1-omni PR #202 §Test Plan: prefix windows at q_base 64/128/1,024 match the
+    full pass bit for bit."""
+    S = 1280
+    inp = Inputs(SEED + 4, S, S)
+    d = inp.dev()
+    full = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, S)
+    for qb in (64, 128, 1024):
+        win = B.ga_attn_prefill(d["qg"][qb:], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"],
+                                qb, S)
+        assert torch.equal(win, full[qb:]), f"q_base={qb}"
+    # a window over a prefix of the keys (T < S) equals the full pass of that prefix
+    T = 640
+    part = B.ga_attn_prefill(d["qg"][512:640], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"],
+                             512, T)
+    assert torch.equal(part, full[512:640])
+
+
+# ------------------------------------------------------------------ edge cases
+def test_single_key_and_single_row():
+    inp = Inputs(SEED + 5, 1, 1)
+    d = inp.dev()
+    got = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, 1)
+    g = inp.np["qg"][0, :, 256:]
+    v = inp.np["v"][0]
+    want = np.concatenate([O.bf16(v[h // 12] * O.bf16(1 / (1 + np.exp(-g[h])))) for h in range(24)])
+    assert np.array_equal(np64(got)[0], want)
+
+
+def test_row_stats_and_hidden_free_causal():
+    inp = Inputs(SEED + 6, 256, 256)
+    d = inp.dev()
+    stats = torch.full((24, 256, 2), float("nan"), device="cuda")
+    B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, 256,
+                      row_stats=stats)
+    st = stats.cpu().numpy()
+    # M is ceil(max t) when first set and the row's largest weight is at least 2^-1
+    assert np.all(np.isfinite(st)) and np.all(st[..., 1] >= 0.5)
+    assert np.all(st[..., 0] == np.round(st[..., 0]))
+
+
+# ------------------------------------------------------------------ S = 8192
+def test_prefill_s8192_full_and_chunks():
+    """Long causal prefill at S=8192: the full pass against the oracle on sampled rows,
+    and two 4096-row chunks (q_base 0, then 4096 over the accumulated keys) bit-identical
+    to the full pass's rows."""
+    S = 8192
+    inp = Inputs(SEED + 8, S, S)
+    d = inp.dev()
+    full = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, S)
+    c1 = B.ga_attn_prefill(d["qg"][:4096], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"],
+                           0, 4096)
+    c2 = B.ga_attn_prefill(d["qg"][4096:], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"],
+                           4096, S)
+    assert torch.equal(c1, full[:4096])
+    assert torch.equal(c2, full[4096:])
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 4095, 4096, 4097, 8063, 8064, 8191],
+                                     rng.integers(0, S, 22)]))
+    inp.ref(0, S, "causal", rows=rows).check(full[torch.as_tensor(rows)],
+                                              what=f"S=8192 causal, {len(rows)} sampled rows")
+
+
+# ------------------------------------------------------------------ negative controls
+def test_negative_control_kv_swap_fails():
+    """pegainfer PR #1151 §Validation: exchanging the two KV heads must fail the gate."""
+    inp = Inputs(SEED + 1, 64, 64)
+    d = inp.dev()
+    swapped = d["k_prep"].flip(1).contiguous()
+    got = B.ga_attn_prefill(d["qg"], swapped, d["v"], d["w_q"], d["cos"], d["sin"], 0, 64)
+    with pytest.raises(AssertionError):
+        inp.ref(0, 64, "causal").check(got, what="KV heads swapped (must fail)")

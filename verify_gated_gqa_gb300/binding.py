@@ -1,0 +1,223 @@
+"""ctypes binding of libga_attn.so (the C ABI in include/ga_attn.h).
+
+Argument marshalling only: every step of the attention runs in the library's CUDA
+kernels. Tensors are torch tensors on the current CUDA device; the work goes on torch's
+current stream. There is no CPU fallback: if the library is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libga_attn.so")
+
+N_Q_HEADS, N_KV_HEADS, HEAD_DIM, ROPE_DIMS = 24, 2, 256, 64
+MASKED_MAX_TOKENS = 8192
+
+STATUS = {0: "GA_OK", -1: "GA_ERR_NULL", -2: "GA_ERR_SHAPE", -3: "GA_ERR_ALIGN",
+          -4: "GA_ERR_RANGE", -5: "GA_ERR_TABLE", -6: "GA_ERR_WORKSPACE",
+          -7: "GA_ERR_DEVICE", -8: "GA_ERR_CUDA", -9: "GA_ERR_GEOMETRY"}
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_LL = ctypes.c_longlong
+_SZ = ctypes.c_size_t
+
+# name: (restype, argtypes)
+_SIGS = {
+    "ga_abi_version": (_I, []),
+    "ga_check_geometry": (_I, [_P]),
+    "ga_status_string": (ctypes.c_char_p, [_I]),
+    "ga_last_cuda_error": (_I, []),
+    "ga_debug_cuda_calls": (ctypes.c_ulonglong, []),
+    "ga_device_status": (_I, [_P, _I]),
+    "ga_rope_table_host": (_I, [_I, _P, _P]),
+    "ga_k_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "ga_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "ga_masked_workspace_bytes": (_SZ, [_I, _I]),
+    "ga_attn_masked": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _LL, _P, _P, _P, _P,
+                            _SZ, _P]),
+    "ga_verify_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "ga_attn_verify": (_I, [_P, _P, _P, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P, _SZ, _P]),
+}
+
+
+class GaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        extra = ""
+        if status == -8 and _lib is not None:
+            extra = f" (cudaError {_lib.ga_last_cuda_error()})"
+        super().__init__(f"{where}: {STATUS.get(status, status)}{extra}")
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("rope_dims", ctypes.c_int),
+                ("eps", ctypes.c_float), ("rope_base", ctypes.c_double)]
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run verify_gated_gqa_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise GaError(st, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _bf16_cuda(name, t, shape=None):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+# ------------------------------------------------------------------ host helpers
+def ga_abi_version() -> int:
+    return lib().ga_abi_version()
+
+
+def ga_check_geometry(n_q_heads=24, n_kv_heads=2, head_dim=256, rope_dims=64, eps=1e-6,
+                      rope_base=1e7) -> int:
+    g = Geometry(n_q_heads, n_kv_heads, head_dim, rope_dims, eps, rope_base)
+    return lib().ga_check_geometry(ctypes.byref(g))
+
+
+def ga_status_string(status: int) -> str:
+    return lib().ga_status_string(status).decode()
+
+
+def ga_debug_cuda_calls() -> int:
+    return lib().ga_debug_cuda_calls()
+
+
+def ga_device_status(clear: bool = True) -> int:
+    v = ctypes.c_int(0)
+    _check(lib().ga_device_status(ctypes.byref(v), 1 if clear else 0), "ga_device_status")
+    return v.value
+
+
+def ga_rope_table_host(n_pos: int):
+    """(cos, sin) bf16 CPU tensors [n_pos, 32] built by the library's host helper."""
+    c = torch.empty(n_pos, ROPE_DIMS // 2, dtype=torch.int16)
+    s = torch.empty(n_pos, ROPE_DIMS // 2, dtype=torch.int16)
+    _check(lib().ga_rope_table_host(n_pos, _ptr(c), _ptr(s)), "ga_rope_table_host")
+    return c.view(torch.bfloat16), s.view(torch.bfloat16)
+
+
+# ------------------------------------------------------------------ device entry points
+def ga_k_prologue(k_raw, w_k, cos_tab, sin_tab, pos_base=0, k_prep=None):
+    _bf16_cuda("k_raw", k_raw)
+    n_tok = k_raw.shape[0]
+    if k_prep is None:
+        k_prep = torch.empty_like(k_raw)
+    for n, t in (("w_k", w_k), ("cos_tab", cos_tab), ("sin_tab", sin_tab), ("k_prep", k_prep)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_k_prologue(_ptr(k_raw), _ptr(w_k), _ptr(cos_tab), _ptr(sin_tab),
+                               cos_tab.shape[0], n_tok, pos_base, _ptr(k_prep), _stream()),
+           "ga_k_prologue")
+    return k_prep
+
+
+def ga_attn_prefill(qg, k_prep, v, w_q, cos_tab, sin_tab, q_base=0, T=None, causal=True,
+                    out=None, row_stats=None):
+    rows = qg.shape[0]
+    T = k_prep.shape[0] if T is None else T
+    if out is None:
+        out = torch.empty(rows, N_Q_HEADS * HEAD_DIM, dtype=torch.bfloat16, device=qg.device)
+    for n, t in (("qg", qg), ("k_prep", k_prep), ("v", v), ("w_q", w_q), ("cos_tab", cos_tab),
+                 ("sin_tab", sin_tab), ("out", out)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_attn_prefill(_ptr(qg), _ptr(k_prep), _ptr(v), _ptr(w_q), _ptr(cos_tab),
+                                 _ptr(sin_tab), cos_tab.shape[0], rows, T, q_base,
+                                 1 if causal else 0, _ptr(out), _ptr(row_stats), _stream()),
+           "ga_attn_prefill")
+    return out
+
+
+def ga_masked_workspace_bytes(rows: int, T: int) -> int:
+    return lib().ga_masked_workspace_bytes(rows, T)
+
+
+def ga_attn_masked(qg, k_prep, v, w_q, cos_tab, sin_tab, mask, q_base=0, T=None,
+                   want_weights=False, out=None, weights=None, hidden_rows=None,
+                   workspace=None):
+    """Returns (out, weights or None, hidden_rows int32 device tensor [1])."""
+    rows = qg.shape[0]
+    T = k_prep.shape[0] if T is None else T
+    dev = qg.device
+    if out is None:
+        out = torch.empty(rows, N_Q_HEADS * HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    if want_weights and weights is None:
+        weights = torch.empty(N_Q_HEADS, rows, T, dtype=torch.bfloat16, device=dev)
+    if hidden_rows is None:
+        hidden_rows = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_bytes = ga_masked_workspace_bytes(rows, T)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    if mask.dtype != torch.uint8 or not mask.is_cuda or mask.stride(1) != 1:
+        raise ValueError("mask must be a uint8 CUDA tensor with unit column stride")
+    for n, t in (("qg", qg), ("k_prep", k_prep), ("v", v), ("w_q", w_q), ("cos_tab", cos_tab),
+                 ("sin_tab", sin_tab), ("out", out)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_attn_masked(_ptr(qg), _ptr(k_prep), _ptr(v), _ptr(w_q), _ptr(cos_tab),
+                                _ptr(sin_tab), cos_tab.shape[0], rows, T, q_base, _ptr(mask),
+                                mask.stride(0), _ptr(out), _ptr(weights), _ptr(hidden_rows),
+                                _ptr(workspace), workspace.numel(), _stream()),
+           "ga_attn_masked")
+    return out, weights, hidden_rows
+
+
+def ga_verify_workspace_bytes(n_seq: int, rows: int, max_len: int) -> int:
+    return lib().ga_verify_workspace_bytes(n_seq, rows, max_len)
+
+
+def ga_attn_verify(qg, k_cache, v_cache, seq_len, w_q, cos_tab, sin_tab, out=None,
+                   workspace=None):
+    """qg [n_seq, rows, 24, 512]; k_cache, v_cache [n_seq, cap, 2, 256]; seq_len: ints."""
+    n_seq, rows = qg.shape[0], qg.shape[1]
+    cap = k_cache.shape[1]
+    lens = (ctypes.c_int * n_seq)(*[int(x) for x in seq_len])
+    dev = qg.device
+    if out is None:
+        out = torch.empty(n_seq, rows, N_Q_HEADS * HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    ws_bytes = ga_verify_workspace_bytes(n_seq, rows, max(int(x) for x in seq_len))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    for n, t in (("qg", qg), ("k_cache", k_cache), ("v_cache", v_cache), ("w_q", w_q),
+                 ("cos_tab", cos_tab), ("sin_tab", sin_tab), ("out", out)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_attn_verify(_ptr(qg), _ptr(k_cache), _ptr(v_cache), cap, lens, n_seq, rows,
+                                _ptr(w_q), _ptr(cos_tab), _ptr(sin_tab), cos_tab.shape[0],
+                                _ptr(out), _ptr(workspace), workspace.numel(), _stream()),
+           "ga_attn_verify")
+    return out

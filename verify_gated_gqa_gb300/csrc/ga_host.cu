@@ -1,0 +1,384 @@
+// Host side of libga_attn.so: argument validation (before any CUDA call), per-device
+// set-up, TMA descriptor encoding, launches, status codes.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "ga_internal.h"
+
+namespace ga {
+namespace {
+
+std::atomic<unsigned long long> g_cuda_calls{0};
+thread_local int t_last_cuda_error = 0;
+
+// Every CUDA runtime or driver call of the library goes through here (so that tests can
+// prove a refused call made none).
+template <typename T>
+inline T counted(T r) {
+  return r;
+}
+#define GA_CUDA(expr) (g_cuda_calls.fetch_add(1, std::memory_order_relaxed), counted(expr))
+
+__device__ int g_device_status;  // written by kernels whose bounded waits gave up
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  bool ready = false;
+  int status = GA_OK;  // GA_OK or GA_ERR_DEVICE / GA_ERR_CUDA from set-up
+  int sm_count = 0;
+  int* status_word = nullptr;
+};
+DeviceState g_devices[kMaxDevices];
+std::mutex g_device_mutex;
+
+int fail_cuda(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return GA_ERR_CUDA;
+}
+
+// Capability check, shared-memory opt-in and status-word address, once per device
+// (system1-omni PR #202, "cuda: widen the attention query tile on sm_89 and sm_120",
+// second review and the author's fix: the decision and the opt-in are kept per device).
+int current_device(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = GA_CUDA(cudaGetDevice(&dev));
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return GA_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_device_mutex);
+  DeviceState& d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = GA_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev))) != cudaSuccess ||
+        (e = GA_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev))) != cudaSuccess ||
+        (e = GA_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) != cudaSuccess)
+      return fail_cuda(e);
+    if (major != 10 || minor != 3) {
+      d.ready = true;
+      d.status = GA_ERR_DEVICE;
+    } else {
+      void* sw = nullptr;
+      if ((e = GA_CUDA(attn_set_smem_attribute())) != cudaSuccess) return fail_cuda(e);
+      if ((e = GA_CUDA(cudaGetSymbolAddress(&sw, g_device_status))) != cudaSuccess) return fail_cuda(e);
+      d.status_word = static_cast<int*>(sw);
+      d.sm_count = sms;
+      d.status = GA_OK;
+      d.ready = true;
+    }
+  }
+  *out = &d;
+  return d.status;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int get_encode(EncodeTiledFn* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (GA_CUDA(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                 cudaEnableDefault, &q)) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  *fn = g_encode;
+  return g_encode ? GA_OK : GA_ERR_DEVICE;
+}
+
+// [n_outer][n_tok][2][256] bf16 keys or values as a TMA tensor: box = 64 dims x 1 head x
+// 128 tokens, 128-byte swizzle; tokens past the end read as zeros.
+int encode_kv_map(CUtensorMap* map, const void* base, long long n_tok, long long n_outer) {
+  EncodeTiledFn enc;
+  int st = get_encode(&enc);
+  if (st != GA_OK) return st;
+  cuuint64_t dims[4] = {(cuuint64_t)kDim, (cuuint64_t)kKvHeads, (cuuint64_t)n_tok, (cuuint64_t)n_outer};
+  cuuint64_t strides[3] = {(cuuint64_t)kDim * 2, (cuuint64_t)kKvHeads * kDim * 2,
+                           (cuuint64_t)n_tok * kKvHeads * kDim * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTileN, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  const cuuint32_t rank = n_outer > 1 ? 4 : 3;
+  CUresult r = GA_CUDA(enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
+                           dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = (int)r;
+    return GA_ERR_CUDA;
+  }
+  return GA_OK;
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// bf16 (nearest, ties to even) of a double.
+uint16_t bf16_rne(double x) {
+  if (x == 0.0) return std::signbit(x) ? 0x8000u : 0u;
+  int e = 0;
+  std::frexp(x, &e);
+  if (e < -125) e = -125;
+  const double q = std::ldexp(std::nearbyint(std::ldexp(x, 8 - e)), e - 8);
+  const float f = (float)q;  // exact: q holds a bf16 value
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  return (uint16_t)(u >> 16);
+}
+
+// Shared checks of the attention entry points (no CUDA call).
+int check_attention_args(const void* qg, const void* k_prep, const void* v, const void* w_q,
+                         const void* cos_tab, const void* sin_tab, int table_rows, int rows,
+                         int T, int q_base, const void* out) {
+  if (!qg || !k_prep || !v || !w_q || !cos_tab || !sin_tab || !out) return GA_ERR_NULL;
+  if (rows < 0 || T < 1 || table_rows < 0) return GA_ERR_SHAPE;
+  if (T > GA_MAX_TOKENS || q_base < 0 || q_base % 64 != 0 || (long long)q_base + rows > T)
+    return GA_ERR_RANGE;
+  if ((long long)table_rows < (long long)q_base + rows) return GA_ERR_TABLE;
+  if (!aligned(qg, 16) || !aligned(k_prep, 16) || !aligned(v, 16) || !aligned(w_q, 16) ||
+      !aligned(cos_tab, 16) || !aligned(sin_tab, 16) || !aligned(out, 16))
+    return GA_ERR_ALIGN;
+  return GA_OK;
+}
+
+struct MaskedLayout {
+  size_t bits_off, flags_off, stats_off, total;
+  int row_tiles, key_tiles, mask_words;
+};
+MaskedLayout masked_layout(int rows, int T) {
+  MaskedLayout L;
+  L.row_tiles = (rows + kTileM - 1) / kTileM;
+  L.key_tiles = (T + kTileN - 1) / kTileN;
+  L.mask_words = L.key_tiles * 4;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  L.bits_off = 0;
+  L.flags_off = up(L.bits_off + (size_t)L.row_tiles * kTileM * L.mask_words * 4);
+  L.stats_off = up(L.flags_off + (size_t)L.row_tiles * L.key_tiles);
+  L.total = up(L.stats_off + (size_t)kHeads * rows * 2 * sizeof(float));
+  return L;
+}
+
+int launch_attention(const AttnArgs& a0, const void* k_prep, const void* v, long long n_tok,
+                     DeviceState* dev, cudaStream_t s) {
+  CUtensorMap tm_k, tm_v;
+  int st = encode_kv_map(&tm_k, k_prep, n_tok, 1);
+  if (st != GA_OK) return st;
+  st = encode_kv_map(&tm_v, v, n_tok, 1);
+  if (st != GA_OK) return st;
+  AttnArgs a = a0;
+  a.status = dev->status_word;
+  a.row_tiles = (a.rows + kTileM - 1) / kTileM;
+  a.n_items = a.row_tiles * kHeads;
+  const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
+  cudaError_t e = GA_CUDA(launch_attn(tm_k, tm_v, a, grid, s));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return GA_OK;
+}
+
+}  // namespace
+}  // namespace ga
+
+using namespace ga;
+
+extern "C" {
+
+int ga_abi_version(void) { return GA_ABI_VERSION; }
+
+int ga_check_geometry(const ga_geometry* g) {
+  if (!g) return GA_ERR_NULL;
+  if (g->n_q_heads != GA_N_Q_HEADS || g->n_kv_heads != GA_N_KV_HEADS ||
+      g->head_dim != GA_HEAD_DIM || g->rope_dims != GA_ROPE_DIMS || g->eps != 1e-6f ||
+      g->rope_base != 1e7)
+    return GA_ERR_GEOMETRY;
+  return GA_OK;
+}
+
+const char* ga_status_string(int status) {
+  switch (status) {
+    case GA_OK: return "ok";
+    case GA_ERR_NULL: return "a required pointer is NULL";
+    case GA_ERR_SHAPE: return "a size is negative or zero where it must be positive";
+    case GA_ERR_ALIGN: return "a pointer or leading dimension is not 16-byte aligned";
+    case GA_ERR_RANGE: return "a window, position or size is out of range";
+    case GA_ERR_TABLE: return "the cos/sin table is shorter than the largest position + 1";
+    case GA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case GA_ERR_DEVICE: return "the current device is not sm_103 or refused set-up";
+    case GA_ERR_CUDA: return "a CUDA call failed (see ga_last_cuda_error)";
+    case GA_ERR_GEOMETRY: return "geometry differs from the compiled 24/2/256/64/1e-6/1e7";
+    default: return "unknown status";
+  }
+}
+
+int ga_last_cuda_error(void) { return t_last_cuda_error; }
+
+unsigned long long ga_debug_cuda_calls(void) { return g_cuda_calls.load(); }
+
+int ga_device_status(int* status_out, int clear) {
+  if (!status_out) return GA_ERR_NULL;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaError_t e = GA_CUDA(cudaDeviceSynchronize());
+  if (e != cudaSuccess) return fail_cuda(e);
+  if ((e = GA_CUDA(cudaMemcpy(status_out, dev->status_word, sizeof(int), cudaMemcpyDeviceToHost))) != cudaSuccess)
+    return fail_cuda(e);
+  if (clear && (e = GA_CUDA(cudaMemset(dev->status_word, 0, sizeof(int)))) != cudaSuccess)
+    return fail_cuda(e);
+  return GA_OK;
+}
+
+int ga_rope_table_host(int n_pos, ga_bf16* cos_out, ga_bf16* sin_out) {
+  if (!cos_out || !sin_out) return GA_ERR_NULL;
+  if (n_pos < 0) return GA_ERR_SHAPE;
+  if (n_pos > GA_MAX_TOKENS) return GA_ERR_RANGE;
+  double inv_freq[kHalfRot];
+  for (int i = 0; i < kHalfRot; ++i) inv_freq[i] = std::pow(kRopeBase, -(2.0 * i) / 64.0);
+  for (int p = 0; p < n_pos; ++p)
+    for (int i = 0; i < kHalfRot; ++i) {
+      const double ang = (double)p * inv_freq[i];
+      cos_out[(size_t)p * kHalfRot + i] = bf16_rne(std::cos(ang));
+      sin_out[(size_t)p * kHalfRot + i] = bf16_rne(std::sin(ang));
+    }
+  return GA_OK;
+}
+
+int ga_k_prologue(const ga_bf16* k_raw, const ga_bf16* w_k, const ga_bf16* cos_tab,
+                  const ga_bf16* sin_tab, int table_rows, int n_tok, int pos_base,
+                  ga_bf16* k_prep, ga_stream stream) {
+  if (!k_raw || !w_k || !cos_tab || !sin_tab || !k_prep) return GA_ERR_NULL;
+  if (n_tok < 0 || table_rows < 0) return GA_ERR_SHAPE;
+  if (pos_base < 0 || n_tok > GA_MAX_TOKENS || pos_base > GA_MAX_TOKENS) return GA_ERR_RANGE;
+  if ((long long)table_rows < (long long)pos_base + n_tok) return GA_ERR_TABLE;
+  if (!aligned(k_raw, 16) || !aligned(k_prep, 16) || !aligned(w_k, 16) || !aligned(cos_tab, 16) ||
+      !aligned(sin_tab, 16))
+    return GA_ERR_ALIGN;
+  if (n_tok == 0) return GA_OK;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaError_t e = GA_CUDA(launch_k_prologue(k_raw, w_k, cos_tab, sin_tab, n_tok, pos_base, k_prep,
+                                            dev->status_word, (cudaStream_t)stream));
+  return e == cudaSuccess ? GA_OK : fail_cuda(e);
+}
+
+int ga_attn_prefill(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                    const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                    int table_rows, int rows, int T, int q_base, int causal, ga_bf16* out,
+                    float* row_stats, ga_stream stream) {
+  int st = check_attention_args(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T,
+                                q_base, out);
+  if (st != GA_OK) return st;
+  if (causal != 0 && causal != 1) return GA_ERR_RANGE;
+  if (!causal && q_base != 0) return GA_ERR_RANGE;  // bidirectional passes start at 0
+  if (row_stats && !aligned(row_stats, 4)) return GA_ERR_ALIGN;
+  if (rows == 0) return GA_OK;
+  DeviceState* dev = nullptr;
+  st = current_device(&dev);
+  if (st != GA_OK) return st;
+  AttnArgs a{};
+  a.qg = qg; a.w_q = w_q; a.cos_tab = cos_tab; a.sin_tab = sin_tab;
+  a.out = out; a.row_stats = row_stats;
+  a.rows = rows; a.T = T; a.q_base = q_base;
+  a.mode = causal ? kModeCausal : kModeBidir;
+  return launch_attention(a, k_prep, v, T, dev, (cudaStream_t)stream);
+}
+
+size_t ga_masked_workspace_bytes(int rows, int T) {
+  if (rows < 0 || T < 1 || T > GA_MASKED_MAX_TOKENS) return 0;
+  return masked_layout(rows, T).total;
+}
+
+int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                   const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                   int table_rows, int rows, int T, int q_base, const uint8_t* mask,
+                   long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
+                   void* workspace, size_t ws_bytes, ga_stream stream) {
+  int st = check_attention_args(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T,
+                                q_base, out);
+  if (st != GA_OK) return st;
+  if (!mask) return GA_ERR_NULL;
+  if (T > GA_MASKED_MAX_TOKENS || ld_mask < T) return GA_ERR_RANGE;
+  if (!aligned(mask, 16) || ld_mask % 16 != 0) return GA_ERR_ALIGN;
+  if ((weights && !aligned(weights, 16)) || (hidden_rows && !aligned(hidden_rows, 4)))
+    return GA_ERR_ALIGN;
+  const MaskedLayout L = masked_layout(rows, T);
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return GA_ERR_WORKSPACE;
+  if (rows == 0) return GA_OK;
+  DeviceState* dev = nullptr;
+  st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(ws + L.bits_off);
+  uint8_t* flags = ws + L.flags_off;
+  float* stats = reinterpret_cast<float*>(ws + L.stats_off);
+  cudaError_t e;
+  if (hidden_rows && (e = GA_CUDA(cudaMemsetAsync(hidden_rows, 0, sizeof(int), s))) != cudaSuccess)
+    return fail_cuda(e);
+  if ((e = GA_CUDA(launch_mask_prepass(mask, ld_mask, rows, T, bits, L.mask_words, flags,
+                                       L.key_tiles, s))) != cudaSuccess)
+    return fail_cuda(e);
+  AttnArgs a{};
+  a.qg = qg; a.w_q = w_q; a.cos_tab = cos_tab; a.sin_tab = sin_tab;
+  a.out = out; a.row_stats = stats; a.hidden_rows = hidden_rows;
+  a.mask_bits = bits; a.tile_flags = flags;
+  a.key_tiles = L.key_tiles; a.mask_words = L.mask_words;
+  a.rows = rows; a.T = T; a.q_base = q_base; a.mode = kModeMask;
+  st = launch_attention(a, k_prep, v, T, dev, s);
+  if (st != GA_OK || !weights) return st;
+  if ((e = GA_CUDA(cudaMemsetAsync(weights, 0, (size_t)kHeads * rows * T * sizeof(uint16_t), s))) != cudaSuccess)
+    return fail_cuda(e);
+  a.weights = weights;
+  a.weights_pass = 1;
+  a.hidden_rows = nullptr;
+  return launch_attention(a, k_prep, v, T, dev, s);
+}
+
+size_t ga_verify_workspace_bytes(int n_seq, int rows, int max_len) {
+  if (n_seq < 1 || rows < 1 || rows > 16 || max_len < 0) return 0;
+  return 256;  // reserved for the split-key partials
+}
+
+int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_cache, int cap,
+                   const int* seq_len, int n_seq, int rows, const ga_bf16* w_q,
+                   const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
+                   ga_bf16* out, void* workspace, size_t ws_bytes, ga_stream stream) {
+  if (!qg || !k_cache || !v_cache || !seq_len || !w_q || !cos_tab || !sin_tab || !out)
+    return GA_ERR_NULL;
+  if (n_seq < 0 || rows < 0 || cap < 1 || table_rows < 0) return GA_ERR_SHAPE;
+  if (rows > 16 || cap > GA_MAX_TOKENS) return GA_ERR_RANGE;
+  int max_len = 0;
+  for (int b = 0; b < n_seq; ++b) {
+    if (seq_len[b] < 0 || (long long)seq_len[b] + rows > cap) return GA_ERR_RANGE;
+    if (seq_len[b] > max_len) max_len = seq_len[b];
+  }
+  if ((long long)table_rows < (long long)max_len + rows) return GA_ERR_TABLE;
+  if (!aligned(qg, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(w_q, 16) ||
+      !aligned(cos_tab, 16) || !aligned(sin_tab, 16) || !aligned(out, 16))
+    return GA_ERR_ALIGN;
+  if (n_seq == 0 || rows == 0) return GA_OK;
+  if (!workspace || !aligned(workspace, 256) ||
+      ws_bytes < ga_verify_workspace_bytes(n_seq, rows, max_len))
+    return GA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  const size_t seq_elems = (size_t)cap * kKvHeads * kDim;
+  for (int b = 0; b < n_seq; ++b) {
+    AttnArgs a{};
+    a.qg = qg + (size_t)b * rows * kRowElems;
+    a.w_q = w_q; a.cos_tab = cos_tab; a.sin_tab = sin_tab;
+    a.out = out + (size_t)b * rows * kOutRow;
+    a.rows = rows; a.T = seq_len[b] + rows; a.q_base = seq_len[b]; a.mode = kModeCausal;
+    st = launch_attention(a, k_cache + b * seq_elems, v_cache + b * seq_elems, a.T, dev,
+                          (cudaStream_t)stream);
+    if (st != GA_OK) return st;
+  }
+  return GA_OK;
+}
+
+}  // extern "C"

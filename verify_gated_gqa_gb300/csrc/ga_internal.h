@@ -1,0 +1,63 @@
+// Internal definitions shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ga_attn.h"
+
+namespace ga {
+
+constexpr int kHeads = GA_N_Q_HEADS;          // 24
+constexpr int kKvHeads = GA_N_KV_HEADS;       // 2
+constexpr int kGroup = kHeads / kKvHeads;     // 12
+constexpr int kDim = GA_HEAD_DIM;             // 256
+constexpr int kQgStride = 2 * kDim;           // 512: q then gate, per head
+constexpr int kRowElems = kHeads * kQgStride; // 12288 bf16 per fused row
+constexpr int kOutRow = kHeads * kDim;        // 6144 bf16 per output row
+constexpr int kHalfRot = GA_ROPE_DIMS / 2;    // 32
+constexpr float kEps = 1e-6f;
+constexpr double kEpsD = 1e-6;
+constexpr double kRopeBase = 1e7;
+
+constexpr int kTileM = 128;  // query rows per attention tile
+constexpr int kTileN = 128;  // keys per attention tile
+
+// Attention kernel variants.
+enum AttnMode : int {
+  kModeCausal = 0,   // key j visible iff j <= q_base + r
+  kModeBidir = 1,    // every key j < T
+  kModeMask = 2,     // stored bit mask (from the mask prepass)
+};
+
+struct AttnArgs {
+  const uint16_t* qg;       // [rows][24][512]
+  const uint16_t* w_q;      // [256]
+  const uint16_t* cos_tab;  // [table_rows][32]
+  const uint16_t* sin_tab;
+  uint16_t* out;            // [rows][6144]
+  float* row_stats;         // nullable [24][rows][2]
+  uint16_t* weights;        // weights pass: [24][rows][T]
+  int* hidden_rows;         // nullable
+  const uint32_t* mask_bits;  // [rows_pad][mask_words], bit j of word w <-> key 32w + j
+  const uint8_t* tile_flags;  // [row_tiles][key_tiles], 1 = tile has a visible key
+  int* status;              // device status word
+  int rows, T, q_base, mode, weights_pass;
+  int row_tiles, key_tiles, mask_words;
+  int n_items;
+};
+
+// Launchers (defined next to their kernels). Return a cudaError_t.
+cudaError_t launch_k_prologue(const uint16_t* k_raw, const uint16_t* w_k, const uint16_t* cos_tab,
+                              const uint16_t* sin_tab, int n_tok, int pos_base, uint16_t* k_prep,
+                              int* status, cudaStream_t s);
+cudaError_t attn_set_smem_attribute();
+size_t attn_smem_bytes();
+cudaError_t launch_attn(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
+                        int grid, cudaStream_t s);
+cudaError_t launch_mask_prepass(const uint8_t* mask, long long ld_mask, int rows, int T,
+                                uint32_t* bits, int mask_words, uint8_t* flags, int key_tiles,
+                                cudaStream_t s);
+
+}  // namespace ga
