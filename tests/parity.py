@@ -97,6 +97,7 @@ class Inputs:
 # outputs, and the weights when given) within the same tolerance.
 TC_BAND_ULP32 = 16.0
 MAX_ALTERNATIVES = 10
+MAX_OFF_ROWS = 256     # beyond this many (row, head) pairs off the oracle, fail without search
 
 
 def _ulp32(x):
@@ -202,6 +203,11 @@ class AttnRef:
                 bad_pairs.add((int(i), self.heads[hh]))
             st["weights"] = stw
         unexplained = []
+        if len(bad_pairs) > MAX_OFF_ROWS:
+            # far more rows off than rounding ties produce: a real error, report it at once
+            st["rows_off_oracle"] = len(bad_pairs)
+            print(f"[parity] {what}: {st}")
+            raise AssertionError(f"{what}: {len(bad_pairs)} (row, head) pairs off the oracle: {st}")
         for i, h in sorted(bad_pairs):
             go = np64(got_out)[i, h * 256:(h + 1) * 256]
             gwr = None if gw is None else gw[h, i]

@@ -235,13 +235,13 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 
 // Normalise one 16-byte chunk (8 dims) of a row: bf16((x * r) * (1 + w)).
 __device__ __forceinline__ void norm_chunk(const uint4& xv, const uint4& wv, float r32,
-                                           const SumSq& ss, double* r64, float (&y)[8]) {
+                                           const SumSq& ss, float (&y)[8]) {
   const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
   const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    y[2 * k] = norm_elem(lo_f(xw[k]), lo_f(ww[k]), r32, ss, r64);
-    y[2 * k + 1] = norm_elem(hi_f(xw[k]), hi_f(ww[k]), r32, ss, r64);
+    y[2 * k] = norm_elem(lo_f(xw[k]), lo_f(ww[k]), r32, ss);
+    y[2 * k + 1] = norm_elem(hi_f(xw[k]), hi_f(ww[k]), r32, ss);
   }
 }
 
@@ -277,7 +277,6 @@ __device__ __noinline__ void prep_q_row(AttnSmem& sm, const AttnArgs& a, int h, 
   acc[0].merge(acc[2]);
   const SumSq ss = acc[0];
   const float r32 = inv_rms_f32(ss);
-  double r64 = -1.0;
   const int pos = a.q_base + row;
   const uint4* cp = reinterpret_cast<const uint4*>(a.cos_tab + (size_t)pos * kHalfRot);
   const uint4* sp = reinterpret_cast<const uint4*>(a.sin_tab + (size_t)pos * kHalfRot);
@@ -285,8 +284,8 @@ __device__ __noinline__ void prep_q_row(AttnSmem& sm, const AttnArgs& a, int h, 
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     float ya[8], yb[8];
-    norm_chunk(__ldg(src + c), __ldg(wq + c), r32, ss, &r64, ya);
-    norm_chunk(__ldg(src + c + 4), __ldg(wq + c + 4), r32, ss, &r64, yb);
+    norm_chunk(__ldg(src + c), __ldg(wq + c), r32, ss, ya);
+    norm_chunk(__ldg(src + c + 4), __ldg(wq + c + 4), r32, ss, yb);
     const uint4 cv = __ldg(cp + c), sv = __ldg(sp + c);
     const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
     const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
@@ -305,34 +304,74 @@ __device__ __noinline__ void prep_q_row(AttnSmem& sm, const AttnArgs& a, int h, 
 #pragma unroll 1
   for (int cd = 8; cd < 32; ++cd) {
     float y[8];
-    norm_chunk(__ldg(src + cd), __ldg(wq + cd), r32, ss, &r64, y);
+    norm_chunk(__ldg(src + cd), __ldg(wq + cd), r32, ss, y);
     store_q_chunk(sm, r, cd, y);
   }
 }
 
-// 128-bit visibility of one (row, key tile): bit c <-> key kt*128 + c.
-__device__ __forceinline__ void tile_visibility(const AttnArgs& a, int row, int kt, bool valid,
-                                                uint32_t (&vis)[4], bool& all) {
-  int n_vis;  // number of leading visible columns (causal / bidirectional)
-  if (a.mode == kModeMask) {
-    if (valid) {
-      const uint4 m = __ldg(reinterpret_cast<const uint4*>(a.mask_bits + (size_t)row * a.mask_words) + kt);
-      vis[0] = m.x; vis[1] = m.y; vis[2] = m.z; vis[3] = m.w;
-    } else {
-      vis[0] = vis[1] = vis[2] = vis[3] = 0u;
-    }
-    all = (vis[0] & vis[1] & vis[2] & vis[3]) == 0xFFFFFFFFu;
-    return;
-  }
-  if (a.mode == kModeCausal) n_vis = a.q_base + row - kt * kTileN + 1;
-  else n_vis = a.T - kt * kTileN;
-  n_vis = max(0, min(kTileN, n_vis));
-  all = n_vis == kTileN;
+// Visibility of the 32 keys kt*128 + 32*ch .. +31 for one row: bit k <-> key +k.
+__device__ __forceinline__ uint32_t chunk_visibility(const AttnArgs& a, int row, int kt, int ch,
+                                                     bool valid) {
+  if (!valid) return 0u;
+  if (a.mode == kModeMask)
+    return __ldg(a.mask_bits + (size_t)row * a.mask_words + kt * 4 + ch);
+  const int first = kt * kTileN + ch * 32;
+  int n = (a.mode == kModeCausal) ? (a.q_base + row - first + 1) : (a.T - first);
+  n = max(0, min(32, n));
+  return n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
+}
+
+// Hidden keys read as -inf: their weight is exactly 0 and they never raise the maximum.
+__device__ __forceinline__ void mask_chunk(uint32_t (&s)[32], uint32_t vis) {
+  if (vis != 0xFFFFFFFFu) {
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const int nb = n_vis - 32 * w;
-    vis[w] = nb >= 32 ? 0xFFFFFFFFu : (nb <= 0 ? 0u : ((1u << nb) - 1u));
+    for (int k = 0; k < 32; ++k)
+      if (!((vis >> k) & 1u)) s[k] = 0xFF800000u;
   }
+}
+
+// Weights pass: bf16(bf16(2^(t - M)) / l) for visible keys, with the main pass's final M
+// and l, written to weights[h][row][kt*128 ..]. Every lane of the warp runs it (the TMEM
+// loads are warp-collective); only lanes with `active` compute and store.
+__device__ void weights_tile(const AttnArgs& a, uint32_t s_tmem, int h, int row, int kt, int M,
+                             float l_final, bool active) {
+  const float mf = (float)M;
+  uint16_t* wrow = a.weights + ((size_t)h * a.rows + row) * (size_t)a.T + (size_t)kt * kTileN;
+  const int ncol = min(kTileN, a.T - kt * kTileN);
+  const bool vec = (ncol == kTileN) && ((a.T & 7) == 0);
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t s[32];
+    tmem_ld32(s_tmem + ch * 32, s);
+    tmem_wait_ld(s);
+    if (!active) continue;
+    mask_chunk(s, chunk_visibility(a, row, kt, ch, true));
+    uint32_t pk[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t sb = pack_bf16x2(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]));
+      const float p0 = bf16_round(ex2_approx(fmaf(lo_f(sb), kLog2eOver16, -mf)));
+      const float p1 = bf16_round(ex2_approx(fmaf(hi_f(sb), kLog2eOver16, -mf)));
+      pk[k] = pack2(p0 / l_final, p1 / l_final);
+    }
+    if (vec) {
+      uint4* dst = reinterpret_cast<uint4*>(wrow + ch * 32);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (ch * 32 + k < ncol)
+          wrow[ch * 32 + k] = (uint16_t)((k & 1) ? (pk[k >> 1] >> 16) : (pk[k >> 1] & 0xFFFFu));
+    }
+  }
+}
+
+// Wait in all 32 lanes and agree on the outcome, so that the warp-collective TMEM loads and
+// stores that follow always run with the whole warp (or the whole warp leaves).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
 }
 
 __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
@@ -365,7 +404,7 @@ __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volat
     }
 
     // ---- Q tile (wait until the previous item's last S = Q K^T has read it)
-    if (it_done > 0 && !mbar_wait(&sm.q_empty, (it_done - 1) & 1, abort)) return;
+    if (it_done > 0 && !warp_wait(&sm.q_empty, (it_done - 1) & 1, abort)) return;
     prep_q_row(sm, a, h, row, r, valid);
     fence_async_smem();
     mbar_arrive(&sm.q_full);
@@ -384,62 +423,32 @@ __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volat
       const int kt = next_key_tile(it, j, cursor);
       const uint32_t b = g & 1;
       const uint32_t s_tmem = tmem + kTmemS + b * 128 + lane_off;
-      if (!mbar_wait(&sm.s_full[b], (g >> 1) & 1, abort)) return;
+      if (!warp_wait(&sm.s_full[b], (g >> 1) & 1, abort)) return;
       tc_fence_after();
-      uint32_t s[128];
-      {
-        uint32_t* s0 = s;
-        tmem_ld32(s_tmem + 0, *reinterpret_cast<uint32_t(*)[32]>(s0));
-        tmem_ld32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(s0 + 32));
-        tmem_ld32(s_tmem + 64, *reinterpret_cast<uint32_t(*)[32]>(s0 + 64));
-        tmem_ld32(s_tmem + 96, *reinterpret_cast<uint32_t(*)[32]>(s0 + 96));
-        tmem_wait_ld(s);
-      }
-      uint32_t vis[4];
-      bool all;
-      tile_visibility(a, row, kt, valid, vis, all);
-      if (!all) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (!((vis[c >> 5] >> (c & 31)) & 1u)) s[c] = 0xFF800000u;  // -inf
-      }
-      // running maximum over the raw fp32 scores: bf16 rounding is monotone, so the
-      // rounded maximum is the maximum of the rounded scores
-      float mx = -INFINITY;
-      if (!a.weights_pass) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
-      }
-      // bf16 scores packed in pairs, in place (s[c] <- s[2c], s[2c+1]); the 1/16 scale
-      // is folded into log2(e)/16 below
-#pragma unroll
-      for (int c = 0; c < 64; ++c) s[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-
       if (a.weights_pass) {
-        // weights = bf16(bf16(2^(t - M)) / l) for visible keys, with the final M and l
-        if (valid && hasM) {
-          const float mf = (float)M;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float p0 = bf16_round(ex2_approx(fmaf(lo_f(s[c]), kLog2eOver16, -mf)));
-            const float p1 = bf16_round(ex2_approx(fmaf(hi_f(s[c]), kLog2eOver16, -mf)));
-            s[c] = pack2(p0 / l_final, p1 / l_final);
-          }
-          uint16_t* wrow = a.weights + ((size_t)h * a.rows + row) * (size_t)a.T + (size_t)kt * kTileN;
-          const int ncol = min(kTileN, a.T - kt * kTileN);
-          if (ncol == kTileN && (a.T & 7) == 0) {
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-              reinterpret_cast<uint4*>(wrow)[c] = make_uint4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < kTileN; ++c)
-              if (c < ncol) wrow[c] = (uint16_t)((c & 1) ? (s[c >> 1] >> 16) : (s[c >> 1] & 0xFFFFu));
-          }
-        }
+        weights_tile(a, s_tmem, h, row, kt, M, l_final, valid && hasM);
         tc_fence_before();
         mbar_arrive(&sm.p_full[b]);
         continue;
+      }
+      // pass 1: the tile maximum over the visible raw fp32 scores (bf16 rounding is
+      // monotone, so the rounded maximum is the maximum of the rounded scores)
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t s[32];
+        tmem_ld32(s_tmem + ch * 32, s);
+        tmem_wait_ld(s);
+        mask_chunk(s, chunk_visibility(a, row, kt, ch, valid));
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          m0 = fmaxf(m0, __uint_as_float(s[k]));
+          m1 = fmaxf(m1, __uint_as_float(s[k + 1]));
+          m2 = fmaxf(m2, __uint_as_float(s[k + 2]));
+          m3 = fmaxf(m3, __uint_as_float(s[k + 3]));
+        }
+        mx = fmaxf(mx, fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
       }
 
       bool rescale = false;
@@ -456,7 +465,7 @@ __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volat
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O must hold every earlier P.V before it is scaled (PV of global tile g-1)
-        if (!mbar_wait(&sm.o_ready, (g - 1) & 1, abort)) return;
+        if (!warp_wait(&sm.o_ready, (g - 1) & 1, abort)) return;
         tc_fence_after();
         const float f = rescale ? exp2f((float)(M - newM)) : 1.0f;
 #pragma unroll 1
@@ -473,19 +482,28 @@ __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volat
       }
       M = newM;
       const float mf = hasM ? (float)M : 0.f;
-      float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+      // pass 2: P = bf16(2^(t - M)), t = bf16(s) * log2(e) / 16, written back as bf16 pairs
+      // over the S columns this pass has already read; l sums the rounded P
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t s[32];
+        tmem_ld32(s_tmem + ch * 32, s);
+        tmem_wait_ld(s);
+        mask_chunk(s, chunk_visibility(a, row, kt, ch, valid));
+        uint32_t pk[16];
+        float la = 0.f, lb = 0.f;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(fmaf(lo_f(s[c]), kLog2eOver16, -mf));
-        const float p1 = ex2_approx(fmaf(hi_f(s[c]), kLog2eOver16, -mf));
-        const uint32_t pk = pack_bf16x2(p0, p1);
-        s[c] = pk;
-        if (c & 1) { ls2 += lo_f(pk); ls3 += hi_f(pk); }
-        else { ls0 += lo_f(pk); ls1 += hi_f(pk); }
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t sb = pack_bf16x2(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]));
+          const float p0 = ex2_approx(fmaf(lo_f(sb), kLog2eOver16, -mf));
+          const float p1 = ex2_approx(fmaf(hi_f(sb), kLog2eOver16, -mf));
+          pk[k] = pack_bf16x2(p0, p1);
+          la += lo_f(pk[k]);
+          lb += hi_f(pk[k]);
+        }
+        l += la + lb;
+        tmem_st16(s_tmem + ch * 16, pk);
       }
-      l += (ls0 + ls1) + (ls2 + ls3);
-      tmem_st32(s_tmem + 0, *reinterpret_cast<uint32_t(*)[32]>(s));
-      tmem_st32(s_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&sm.p_full[b]);
@@ -496,7 +514,7 @@ __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volat
     }
 
     // ---- gated epilogue: out = bf16(bf16(O / l) * bf16(sigmoid(gate)))
-    if (!mbar_wait(&sm.o_done, it_done & 1, abort)) return;
+    if (!warp_wait(&sm.o_done, it_done & 1, abort)) return;
     tc_fence_after();
     const float inv = l > 0.f ? 1.0f / l : 0.f;
     const uint4* gp = reinterpret_cast<const uint4*>(a.qg + ((size_t)(valid ? row : 0) * kHeads + h) * kQgStride + kDim);

@@ -71,14 +71,23 @@ __device__ __forceinline__ double inv_rms_f64(const SumSq& s) {
   return 1.0 / sqrt(((double)s.hi + (double)s.lo) / 256.0 + 1e-6);
 }
 
+// Out-of-line double-precision recomputation (rare): kept out of the hot loops so that
+// they stay small.
+static __device__ __noinline__ float norm_elem_slow(float x, float w, float hi, float lo) {
+  SumSq ss;
+  ss.hi = hi;
+  ss.lo = lo;
+  return bf16_of_double(((double)x * inv_rms_f64(ss)) * (1.0 + (double)w));
+}
+static __device__ __noinline__ float sigmoid_slow(float g) {
+  return bf16_of_double(1.0 / (1.0 + exp(-(double)g)));
+}
+
 // bf16 of x * inv_rms * (1 + w) for a bf16 x and a bf16 weight w.
-// r64 is computed on first need (rare) into *r64 (initialise it to a negative value).
-__device__ __forceinline__ float norm_elem(float x, float w, float r32, const SumSq& ss,
-                                           double* r64) {
+__device__ __forceinline__ float norm_elem(float x, float w, float r32, const SumSq& ss) {
   const float y = (x * r32) * (1.0f + w);
   if (!near_bf16_midpoint(y)) return bf16_round(y);
-  if (*r64 < 0.0) *r64 = inv_rms_f64(ss);
-  return bf16_of_double(((double)x * *r64) * (1.0 + (double)w));
+  return norm_elem_slow(x, w, ss.hi, ss.lo);
 }
 
 // Rotate-half RoPE of one pair with bf16 rounding after each product and after the sum;
@@ -93,7 +102,7 @@ __device__ __forceinline__ void rope_pair(float a, float b, float c, float s, fl
 __device__ __forceinline__ float sigmoid_bf16(float g) {
   const float y = 1.0f / (1.0f + expf(-g));
   if (!near_bf16_midpoint(y)) return bf16_round(y);
-  return bf16_of_double(1.0 / (1.0 + exp(-(double)g)));
+  return sigmoid_slow(g);
 }
 
 }  // namespace ga

@@ -59,10 +59,9 @@ __global__ void __launch_bounds__(256) k_prologue_kernel(const uint16_t* __restr
     }
   }
   const float r32 = inv_rms_f32(ss);
-  double r64 = -1.0;
   float y[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = norm_elem(x[i], w[i], r32, ss, &r64);
+  for (int i = 0; i < 8; ++i) y[i] = norm_elem(x[i], w[i], r32, ss);
 
   // Partial RoPE: dims 0..31 (lanes 0..3) pair with dims 32..63 (lanes 4..7).
   float partner[8];
