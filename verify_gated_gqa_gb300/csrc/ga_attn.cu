@@ -18,14 +18,20 @@
 // not depend on which tile or window computes it.
 //
 // Structure (one CTA per SM, persistent, 192 threads):
-//   warp 0     TMA producer: K and V tiles in 16 KiB chunks (128 keys x 64 dims,
-//              128-byte swizzle) through a ring of shared-memory slots;
+//   warp 0     TMA producer: K and V tiles of 64 keys in 8 KiB chunks (64 keys x 64 dims,
+//              128-byte swizzle) through a 28-slot ring (224 KiB) of shared memory;
 //   warp 1     allocates the 512 TMEM columns and issues every tcgen05.mma:
-//              S = Q K^T (M=128, N=128, K=256) into one of two TMEM S buffers, then
-//              O += P V (P read from TMEM, V MN-major from shared memory, N=64 per chunk);
-//   warps 2-5  one query row per thread: Q prep into swizzled shared memory, the
+//              S = Q K^T (M=128, N=64, K=256; Q read from TMEM) into one of two TMEM S
+//              buffers, then O += P V (P read from TMEM over S, V MN-major, N=64 a chunk);
+//   warps 2-5  one query row per thread: Q prep (norm, RoPE) straight into TMEM, the
 //              softmax over each S tile (P written back over S in TMEM), the rare O
-//              rescale, and the gated epilogue with 16-byte bf16 stores.
+//              rescale, and the gated epilogue with 16-byte bf16 stores. The next work
+//              item's Q is prepared before the current item's epilogue, so the tensor
+//              core starts the next item's S = Q K^T while O is drained.
+// Tensor memory (512 columns x 128 lanes, lane = query row): O [0, 256) fp32, Q
+// [256, 384) bf16 pairs, S0 [384, 448) and S1 [448, 512) fp32 with P as bf16 pairs over
+// their first 32 columns. Keeping Q in TMEM leaves shared memory to the K/V ring, which
+// is what keeps enough loads in flight to cover the L2 latency.
 // Work items are (query head, 128-row tile), longest first, dealt to the CTAs in a
 // serpentine order so each CTA's total work evens out.
 #include "ga_internal.h"
@@ -35,17 +41,18 @@
 namespace ga {
 namespace {
 
-constexpr int kSlots = 10;
-constexpr int kChunkBytes = 16384;  // 128 rows x 64 bf16 (one 128-byte-swizzle column)
+constexpr int kSlots = 28;
+constexpr int kChunkBytes = kTileN * 128;  // 64 keys x 64 bf16 (one 128-byte-swizzle column)
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;      // O accumulator: 256 columns (fp32, 128 lanes)
-constexpr uint32_t kTmemS = 256;    // S buffers: 2 x 128 columns; P (bf16 pairs) over S
+constexpr uint32_t kTmemO = 0;      // O accumulator: 256 columns (fp32)
+constexpr uint32_t kTmemQ = 256;    // Q: 128 columns of bf16 pairs (A operand of Q K^T)
+constexpr uint32_t kTmemS = 384;    // S buffers: 2 x 64 columns; P (bf16 pairs) over S
+constexpr uint32_t kSCols = kTileN; // fp32 columns of one S buffer
 constexpr float kLog2eOver16 = 1.4426950408889634f / 16.0f;
 constexpr int kLazyRescale = 8;     // rescale when the tile maximum exceeds M by > 2^8
 
 struct alignas(1024) AttnSmem {
-  uint8_t q[4][kChunkBytes];
   uint8_t ring[kSlots][kChunkBytes];
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
@@ -60,7 +67,8 @@ struct alignas(1024) AttnSmem {
 struct Item {
   int h, mt;          // query head, 128-row tile
   int n;              // key tiles to visit
-  uint64_t tiles;     // mask mode: bit kt set for every key tile with a visible key
+  bool masked;        // mask mode: visit only the key tiles listed in `tiles`
+  uint64_t tiles[2];  // mask mode: bit kt set for every key tile with a visible key
 };
 
 __device__ __forceinline__ int item_index(int round, int cta, int G) {
@@ -71,7 +79,8 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
   Item it;
   it.mt = a.row_tiles - 1 - idx / kHeads;  // later row tiles see more keys: longest first
   it.h = idx % kHeads;
-  it.tiles = 0;
+  it.masked = a.mode == kModeMask;
+  it.tiles[0] = it.tiles[1] = 0;
   if (a.mode == kModeCausal) {
     const int last_row = min(a.rows, (it.mt + 1) * kTileM) - 1;
     const int key_end = min(a.T, a.q_base + last_row + 1);
@@ -81,19 +90,28 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
   } else {
     const uint8_t* f = a.tile_flags + (size_t)it.mt * a.key_tiles;
     for (int kt = 0; kt < a.key_tiles; ++kt)
-      if (f[kt]) it.tiles |= (1ull << kt);
-    it.n = __popcll(it.tiles);
+      if (f[kt]) it.tiles[kt >> 6] |= (1ull << (kt & 63));
+    it.n = __popcll(it.tiles[0]) + __popcll(it.tiles[1]);
   }
   return it;
 }
 
-// Key tile of the j-th visit; `cursor` walks the set bits of a mask-mode item in order.
-__device__ __forceinline__ int next_key_tile(const Item& it, int j, uint64_t& cursor) {
-  if (it.tiles == 0) return j;
-  const int kt = __ffsll((long long)cursor) - 1;
-  cursor &= cursor - 1;
-  return kt;
-}
+// Walks the key tiles of an item in order: 0 .. n-1, or the set bits of a mask-mode item.
+struct TileCursor {
+  uint64_t w0, w1;
+  __device__ __forceinline__ explicit TileCursor(const Item& it) : w0(it.tiles[0]), w1(it.tiles[1]) {}
+  __device__ __forceinline__ int next(const Item& it, int j) {
+    if (!it.masked) return j;
+    if (w0) {
+      const int kt = __ffsll((long long)w0) - 1;
+      w0 &= w0 - 1;
+      return kt;
+    }
+    const int kt = 64 + __ffsll((long long)w1) - 1;
+    w1 &= w1 - 1;
+    return kt;
+  }
+};
 
 __device__ __forceinline__ void record_abort(int* status, int code) {
   if (code) atomicCAS(status, 0, code);
@@ -120,14 +138,14 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_k, const CUten
     const Item it = make_item(a, idx);
     if (it.n == 0) continue;
     const int kvh = it.h / kGroup;
-    uint64_t ck = it.tiles, cv = it.tiles;
+    TileCursor ck(it), cv(it);
     // Ring order = MMA order: K0, then (K_j, V_{j-1}) for j >= 1, then V_{n-1}.
-    if (!load_tile(tm_k, kvh, next_key_tile(it, 0, ck))) return;
+    if (!load_tile(tm_k, kvh, ck.next(it, 0))) return;
     for (int j = 1; j < it.n; ++j) {
-      if (!load_tile(tm_k, kvh, next_key_tile(it, j, ck))) return;
-      if (!a.weights_pass && !load_tile(tm_v, kvh, next_key_tile(it, j - 1, cv))) return;
+      if (!load_tile(tm_k, kvh, ck.next(it, j))) return;
+      if (!a.weights_pass && !load_tile(tm_v, kvh, cv.next(it, j - 1))) return;
     }
-    if (!a.weights_pass && !load_tile(tm_v, kvh, next_key_tile(it, it.n - 1, cv))) return;
+    if (!a.weights_pass && !load_tile(tm_v, kvh, cv.next(it, it.n - 1))) return;
   }
 }
 
@@ -146,9 +164,8 @@ __device__ void producer(AttnSmem& sm, const CUtensorMap* tm_k, const CUtensorMa
 // ------------------------------------------------------------------ warp 1: MMA issuer
 __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
                          volatile int* abort) {
-  constexpr uint32_t kIdQK = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t kIdQK = idesc_bf16(128, kTileN, false, false);
   constexpr uint32_t kIdPV = idesc_bf16(128, 64, false, true);
-  const uint32_t q_addr = smem_u32(sm.q[0]);
   uint32_t chunk = 0;
   uint32_t g = 0;   // global tile counter (selects the S buffer and its phase)
   uint32_t it_done = 0;
@@ -165,12 +182,12 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
     if (j == 0 && it_done > 0 && !mbar_wait(&sm.o_free, (it_done - 1) & 1, abort)) return false;
     if (!mbar_wait(&sm.p_full[b], u & 1, abort)) return false;
     tc_fence_after();
-    const uint32_t p_tmem = tmem + kTmemS + b * 128;
+    const uint32_t p_tmem = tmem + kTmemS + b * kSCols;
     for (int c = 0; c < 4; ++c) {
       uint32_t slot;
       if (!take_chunk(slot)) return false;
       const uint32_t v_addr = smem_u32(sm.ring[slot]);
-      for (int kk = 0; kk < 8; ++kk) {
+      for (int kk = 0; kk < kTileN / 16; ++kk) {
         const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, kChunkBytes, 1024);
         umma_ts(tmem + kTmemO + c * 64, p_tmem + kk * 8, bd, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
       }
@@ -194,15 +211,14 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
         // S buffer b is free once the rows have read tile g-2 from it
         if (!mbar_wait(&sm.p_full[b], ((g >> 1) - 1) & 1, abort)) return;
       }
-      const uint32_t s_tmem = tmem + kTmemS + b * 128;
+      const uint32_t s_tmem = tmem + kTmemS + b * kSCols;
       for (int c = 0; c < 4; ++c) {
         uint32_t slot;
         if (!take_chunk(slot)) return;
         const uint32_t k_addr = smem_u32(sm.ring[slot]);
         for (int k4 = 0; k4 < 4; ++k4) {
-          const uint64_t ad = sdesc_sw128(q_addr + c * kChunkBytes + k4 * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(k_addr + k4 * 32, 16, 1024);
-          umma_ss(s_tmem, ad, bd, kIdQK, (c | k4) ? 1u : 0u);
+          umma_ts(s_tmem, tmem + kTmemQ + (c * 4 + k4) * 8, bd, kIdQK, (c | k4) ? 1u : 0u);
         }
         umma_commit(&sm.empty[slot]);
       }
@@ -245,76 +261,105 @@ __device__ __forceinline__ void norm_chunk(const uint4& xv, const uint4& wv, flo
   }
 }
 
-__device__ __forceinline__ void store_q_chunk(AttnSmem& sm, int r, int cd, const float (&y)[8]) {
-  uint8_t* dst = sm.q[cd >> 3] + sw128_offset((uint32_t)r, (uint32_t)(cd & 7));
-  *reinterpret_cast<uint4*>(dst) =
-      make_uint4(pack2(y[0], y[1]), pack2(y[2], y[3]), pack2(y[4], y[5]), pack2(y[6], y[7]));
-}
-
-// (1+w) RMSNorm and partial RoPE of one query row; writes row r of the 128x256 Q tile
-// into the four 128-byte-swizzled column blocks. Streams the row in 16-byte chunks.
-__device__ __noinline__ void prep_q_row(AttnSmem& sm, const AttnArgs& a, int h, int row, int r,
-                                        bool valid) {
-  if (!valid) {
-    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-    for (int cd = 0; cd < 32; ++cd) store_q_chunk(sm, r, cd, z);
-    return;
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(a.qg + ((size_t)row * kHeads + h) * kQgStride);
+// (1+w) RMSNorm and partial RoPE of one query row, written as bf16 pairs into this
+// thread's TMEM lane at Q (column c holds dims 2c and 2c+1). Every lane of the warp runs
+// it (the stores are warp-collective); lanes of rows past the end store zeros.
+__device__ __noinline__ void prep_q_tmem(const AttnArgs& a, int h, int row, bool valid,
+                                         uint32_t q_taddr) {
+  const uint4* src = reinterpret_cast<const uint4*>(a.qg + ((size_t)(valid ? row : 0) * kHeads + h) * kQgStride);
   const uint4* wq = reinterpret_cast<const uint4*>(a.w_q);
-  SumSq acc[4];
+  SumSq ss;
+  float r32 = 0.f;
+  if (valid) {
+    SumSq acc[4];
 #pragma unroll 4
-  for (int i = 0; i < 32; ++i) {
-    const uint4 v = __ldg(src + i);
-    acc[i & 3].add(lo_f(v.x)); acc[i & 3].add(hi_f(v.x));
-    acc[i & 3].add(lo_f(v.y)); acc[i & 3].add(hi_f(v.y));
-    acc[i & 3].add(lo_f(v.z)); acc[i & 3].add(hi_f(v.z));
-    acc[i & 3].add(lo_f(v.w)); acc[i & 3].add(hi_f(v.w));
-  }
-  acc[0].merge(acc[1]);
-  acc[2].merge(acc[3]);
-  acc[0].merge(acc[2]);
-  const SumSq ss = acc[0];
-  const float r32 = inv_rms_f32(ss);
-  const int pos = a.q_base + row;
-  const uint4* cp = reinterpret_cast<const uint4*>(a.cos_tab + (size_t)pos * kHalfRot);
-  const uint4* sp = reinterpret_cast<const uint4*>(a.sin_tab + (size_t)pos * kHalfRot);
-  // rotary dims: chunk c (dims 8c..8c+7) pairs with chunk c + 4 (dims 8c+32..)
-#pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    float ya[8], yb[8];
-    norm_chunk(__ldg(src + c), __ldg(wq + c), r32, ss, ya);
-    norm_chunk(__ldg(src + c + 4), __ldg(wq + c + 4), r32, ss, yb);
-    const uint4 cv = __ldg(cp + c), sv = __ldg(sp + c);
-    const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float cs = (e & 1) ? hi_f(cw[e >> 1]) : lo_f(cw[e >> 1]);
-      const float sn = (e & 1) ? hi_f(sw[e >> 1]) : lo_f(sw[e >> 1]);
-      float ra, rb;
-      rope_pair(ya[e], yb[e], cs, sn, ra, rb);
-      ya[e] = ra;
-      yb[e] = rb;
+    for (int i = 0; i < 32; ++i) {
+      const uint4 v = __ldg(src + i);
+      acc[i & 3].add(lo_f(v.x)); acc[i & 3].add(hi_f(v.x));
+      acc[i & 3].add(lo_f(v.y)); acc[i & 3].add(hi_f(v.y));
+      acc[i & 3].add(lo_f(v.z)); acc[i & 3].add(hi_f(v.z));
+      acc[i & 3].add(lo_f(v.w)); acc[i & 3].add(hi_f(v.w));
     }
-    store_q_chunk(sm, r, c, ya);
-    store_q_chunk(sm, r, c + 4, yb);
+    acc[0].merge(acc[1]);
+    acc[2].merge(acc[3]);
+    acc[0].merge(acc[2]);
+    ss = acc[0];
+    r32 = inv_rms_f32(ss);
   }
+  uint32_t w[32];
+  // dims 0..63: chunk c (dims 8c..8c+7) pairs with chunk c + 4 (dims 8c+32..)
+  if (valid) {
+    const int pos = a.q_base + row;
+    const uint4* cp = reinterpret_cast<const uint4*>(a.cos_tab + (size_t)pos * kHalfRot);
+    const uint4* sp = reinterpret_cast<const uint4*>(a.sin_tab + (size_t)pos * kHalfRot);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float ya[8], yb[8];
+      norm_chunk(__ldg(src + c), __ldg(wq + c), r32, ss, ya);
+      norm_chunk(__ldg(src + c + 4), __ldg(wq + c + 4), r32, ss, yb);
+      const uint4 cv = __ldg(cp + c), sv = __ldg(sp + c);
+      const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float cs = (e & 1) ? hi_f(cw[e >> 1]) : lo_f(cw[e >> 1]);
+        const float sn = (e & 1) ? hi_f(sw[e >> 1]) : lo_f(sw[e >> 1]);
+        float ra, rb;
+        rope_pair(ya[e], yb[e], cs, sn, ra, rb);
+        ya[e] = ra;
+        yb[e] = rb;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        w[4 * c + k] = pack2(ya[2 * k], ya[2 * k + 1]);
+        w[16 + 4 * c + k] = pack2(yb[2 * k], yb[2 * k + 1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) w[k] = 0u;
+  }
+  tmem_st32(q_taddr, w);
+  // dims 64..255 pass through the rotation
 #pragma unroll 1
-  for (int cd = 8; cd < 32; ++cd) {
-    float y[8];
-    norm_chunk(__ldg(src + cd), __ldg(wq + cd), r32, ss, y);
-    store_q_chunk(sm, r, cd, y);
+  for (int grp = 1; grp < 4; ++grp) {
+    if (valid) {
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        float y[8];
+        norm_chunk(__ldg(src + 8 * grp + cc), __ldg(wq + 8 * grp + cc), r32, ss, y);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[4 * cc + k] = pack2(y[2 * k], y[2 * k + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) w[k] = 0u;
+    }
+    tmem_st32(q_taddr + 32 * grp, w);
   }
+  tmem_wait_st();
 }
 
-// Visibility of the 32 keys kt*128 + 32*ch .. +31 for one row: bit k <-> key +k.
+// Outputs of a work item none of whose key tiles is visible (mask mode): every row is
+// hidden, its output row and statistics are zero.
+__device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r) {
+  const int row = it.mt * kTileM + r;
+  if (row >= a.rows || a.weights_pass) return;
+  uint4* o = reinterpret_cast<uint4*>(a.out + (size_t)row * kOutRow + it.h * kDim);
+  for (int i = 0; i < 32; ++i) o[i] = make_uint4(0, 0, 0, 0);
+  if (a.row_stats) {
+    a.row_stats[((size_t)it.h * a.rows + row) * 2] = 0.f;
+    a.row_stats[((size_t)it.h * a.rows + row) * 2 + 1] = 0.f;
+  }
+  if (a.hidden_rows && it.h == 0) atomicAdd(a.hidden_rows, 1);
+}
+
+// Visibility of the 32 keys kt*64 + 32*ch .. +31 for one row: bit k <-> key +k.
 __device__ __forceinline__ uint32_t chunk_visibility(const AttnArgs& a, int row, int kt, int ch,
                                                      bool valid) {
   if (!valid) return 0u;
   if (a.mode == kModeMask)
-    return __ldg(a.mask_bits + (size_t)row * a.mask_words + kt * 4 + ch);
+    return __ldg(a.mask_bits + (size_t)row * a.mask_words + kt * (kTileN / 32) + ch);
   const int first = kt * kTileN + ch * 32;
   int n = (a.mode == kModeCausal) ? (a.q_base + row - first + 1) : (a.T - first);
   n = max(0, min(32, n));
@@ -331,7 +376,7 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&s)[32], uint32_t vis) {
 }
 
 // Weights pass: bf16(bf16(2^(t - M)) / l) for visible keys, with the main pass's final M
-// and l, written to weights[h][row][kt*128 ..]. Every lane of the warp runs it (the TMEM
+// and l, written to weights[h][row][kt*64 ..]. Every lane of the warp runs it (the TMEM
 // loads are warp-collective); only lanes with `active` compute and store.
 __device__ void weights_tile(const AttnArgs& a, uint32_t s_tmem, int h, int row, int kt, int M,
                              float l_final, bool active) {
@@ -340,7 +385,7 @@ __device__ void weights_tile(const AttnArgs& a, uint32_t s_tmem, int h, int row,
   const int ncol = min(kTileN, a.T - kt * kTileN);
   const bool vec = (ncol == kTileN) && ((a.T & 7) == 0);
 #pragma unroll 1
-  for (int ch = 0; ch < 4; ++ch) {
+  for (int ch = 0; ch < kTileN / 32; ++ch) {
     uint32_t s[32];
     tmem_ld32(s_tmem + ch * 32, s);
     tmem_wait_ld(s);
@@ -379,36 +424,35 @@ __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volat
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+  const uint32_t q_taddr = tmem + kTmemQ + lane_off;
   uint32_t g = 0, it_done = 0;
-
   const int G = gridDim.x;
-  for (int round = 0;; ++round) {
-    const int idx = item_index(round, blockIdx.x, G);
-    if (idx >= a.n_items) break;
-    const Item it = make_item(a, idx);
+  int round = 0;
+
+  // This CTA's next work item that has key tiles; items without any (mask mode) are
+  // answered on the way.
+  auto next_item = [&](Item& out) -> bool {
+    for (;; ++round) {
+      const int idx = item_index(round, blockIdx.x, G);
+      if (idx >= a.n_items) return false;
+      out = make_item(a, idx);
+      if (out.n > 0) {
+        ++round;
+        return true;
+      }
+      write_hidden_rows(a, out, r);
+    }
+  };
+
+  Item it;
+  if (!next_item(it)) return;
+  prep_q_tmem(a, it.h, it.mt * kTileM + r, it.mt * kTileM + r < a.rows, q_taddr);
+  tc_fence_before();
+  mbar_arrive(&sm.q_full);
+  while (true) {
     const int row = it.mt * kTileM + r;
     const bool valid = row < a.rows;
     const int h = it.h;
-    if (it.n == 0) {
-      // mask mode: no key tile of this row tile is visible; every row is hidden
-      if (valid && !a.weights_pass) {
-        uint4* o = reinterpret_cast<uint4*>(a.out + (size_t)row * kOutRow + h * kDim);
-        for (int i = 0; i < 32; ++i) o[i] = make_uint4(0, 0, 0, 0);
-        if (a.row_stats) {
-          a.row_stats[((size_t)h * a.rows + row) * 2] = 0.f;
-          a.row_stats[((size_t)h * a.rows + row) * 2 + 1] = 0.f;
-        }
-        if (a.hidden_rows && h == 0) atomicAdd(a.hidden_rows, 1);
-      }
-      continue;
-    }
-
-    // ---- Q tile (wait until the previous item's last S = Q K^T has read it)
-    if (it_done > 0 && !warp_wait(&sm.q_empty, (it_done - 1) & 1, abort)) return;
-    prep_q_row(sm, a, h, row, r, valid);
-    fence_async_smem();
-    mbar_arrive(&sm.q_full);
-
     int M = 0;
     bool hasM = false;
     float l = 0.f;
@@ -418,11 +462,11 @@ __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volat
       l_final = a.row_stats[((size_t)h * a.rows + row) * 2 + 1];
       hasM = l_final > 0.f;
     }
-    uint64_t cursor = it.tiles;
+    TileCursor cursor(it);
     for (int j = 0; j < it.n; ++j, ++g) {
-      const int kt = next_key_tile(it, j, cursor);
+      const int kt = cursor.next(it, j);
       const uint32_t b = g & 1;
-      const uint32_t s_tmem = tmem + kTmemS + b * 128 + lane_off;
+      const uint32_t s_tmem = tmem + kTmemS + b * kSCols + lane_off;
       if (!warp_wait(&sm.s_full[b], (g >> 1) & 1, abort)) return;
       tc_fence_after();
       if (a.weights_pass) {
@@ -435,7 +479,7 @@ __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volat
       // monotone, so the rounded maximum is the maximum of the rounded scores)
       float mx = -INFINITY;
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < kTileN / 32; ++ch) {
         uint32_t s[32];
         tmem_ld32(s_tmem + ch * 32, s);
         tmem_wait_ld(s);
@@ -485,7 +529,7 @@ __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volat
       // pass 2: P = bf16(2^(t - M)), t = bf16(s) * log2(e) / 16, written back as bf16 pairs
       // over the S columns this pass has already read; l sums the rounded P
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < kTileN / 32; ++ch) {
         uint32_t s[32];
         tmem_ld32(s_tmem + ch * 32, s);
         tmem_wait_ld(s);
@@ -508,51 +552,61 @@ __device__ void row_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volat
       tc_fence_before();
       mbar_arrive(&sm.p_full[b]);
     }
-    if (a.weights_pass) {
-      ++it_done;
-      continue;
-    }
 
-    // ---- gated epilogue: out = bf16(bf16(O / l) * bf16(sigmoid(gate)))
-    if (!warp_wait(&sm.o_done, it_done & 1, abort)) return;
-    tc_fence_after();
-    const float inv = l > 0.f ? 1.0f / l : 0.f;
-    const uint4* gp = reinterpret_cast<const uint4*>(a.qg + ((size_t)(valid ? row : 0) * kHeads + h) * kQgStride + kDim);
-    uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)(valid ? row : 0) * kOutRow + h * kDim);
-#pragma unroll 1
-    for (int c0 = 0; c0 < 256; c0 += 32) {
-      uint32_t o[32];
-      tmem_ld32(tmem + kTmemO + lane_off + c0, o);
-      tmem_wait_ld(o);
-      if (valid) {
-        uint32_t res[16];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 gv = __ldg(gp + (c0 >> 3) + q4);
-          const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int e = q4 * 8 + 2 * k;
-            const float o0 = bf16_round(__uint_as_float(o[e]) * inv);
-            const float o1 = bf16_round(__uint_as_float(o[e + 1]) * inv);
-            res[q4 * 4 + k] = pack2(o0 * sigmoid_bf16(lo_f(gw[k])), o1 * sigmoid_bf16(hi_f(gw[k])));
+    // ---- the next item's Q, as soon as this item's last S = Q K^T has read Q
+    Item nxt;
+    const bool more = next_item(nxt);
+    if (more) {
+      if (!warp_wait(&sm.q_empty, it_done & 1, abort)) return;
+      tc_fence_after();
+      prep_q_tmem(a, nxt.h, nxt.mt * kTileM + r, nxt.mt * kTileM + r < a.rows, q_taddr);
+      tc_fence_before();
+      mbar_arrive(&sm.q_full);
+    }
+    if (!a.weights_pass) {
+      // ---- gated epilogue: out = bf16(bf16(O / l) * bf16(sigmoid(gate)))
+      if (!warp_wait(&sm.o_done, it_done & 1, abort)) return;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      const uint4* gp = reinterpret_cast<const uint4*>(a.qg + ((size_t)(valid ? row : 0) * kHeads + h) * kQgStride + kDim);
+      uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)(valid ? row : 0) * kOutRow + h * kDim);
+  #pragma unroll 1
+      for (int c0 = 0; c0 < 256; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem + kTmemO + lane_off + c0, o);
+        tmem_wait_ld(o);
+        if (valid) {
+          uint32_t res[16];
+  #pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const uint4 gv = __ldg(gp + (c0 >> 3) + q4);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+  #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int e = q4 * 8 + 2 * k;
+              const float o0 = bf16_round(__uint_as_float(o[e]) * inv);
+              const float o1 = bf16_round(__uint_as_float(o[e + 1]) * inv);
+              res[q4 * 4 + k] = pack2(o0 * sigmoid_bf16(lo_f(gw[k])), o1 * sigmoid_bf16(hi_f(gw[k])));
+            }
           }
+  #pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            op[(c0 >> 3) + q4] = make_uint4(res[4 * q4], res[4 * q4 + 1], res[4 * q4 + 2], res[4 * q4 + 3]);
         }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          op[(c0 >> 3) + q4] = make_uint4(res[4 * q4], res[4 * q4 + 1], res[4 * q4 + 2], res[4 * q4 + 3]);
       }
-    }
-    if (valid) {
-      if (a.row_stats) {
-        a.row_stats[((size_t)h * a.rows + row) * 2] = (float)M;
-        a.row_stats[((size_t)h * a.rows + row) * 2 + 1] = l;
+      if (valid) {
+        if (a.row_stats) {
+          a.row_stats[((size_t)h * a.rows + row) * 2] = (float)M;
+          a.row_stats[((size_t)h * a.rows + row) * 2 + 1] = l;
+        }
+        if (a.hidden_rows && h == 0 && l == 0.f) atomicAdd(a.hidden_rows, 1);
       }
-      if (a.hidden_rows && h == 0 && l == 0.f) atomicAdd(a.hidden_rows, 1);
+      tc_fence_before();
+      mbar_arrive(&sm.o_free);
     }
-    tc_fence_before();
-    mbar_arrive(&sm.o_free);
     ++it_done;
+    if (!more) break;
+    it = nxt;
   }
 }
 

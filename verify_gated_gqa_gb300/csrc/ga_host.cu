@@ -153,7 +153,7 @@ MaskedLayout masked_layout(int rows, int T) {
   MaskedLayout L;
   L.row_tiles = (rows + kTileM - 1) / kTileM;
   L.key_tiles = (T + kTileN - 1) / kTileN;
-  L.mask_words = L.key_tiles * 4;
+  L.mask_words = L.key_tiles * (kTileN / 32);
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   L.bits_off = 0;
   L.flags_off = up(L.bits_off + (size_t)L.row_tiles * kTileM * L.mask_words * 4);
