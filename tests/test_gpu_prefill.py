@@ -122,6 +122,32 @@ def test_single_key_and_single_row():
     assert np.array_equal(np64(got)[0], want)
 
 
+def test_gate_every_bf16_value():
+    """Every bf16 gate value but NaN (one per output element across 11 rows) with V = 1, so
+    that o = 1 and out = bf16(sigmoid(g)) itself: the gate's fast path and its exact
+    fallback, bit for bit against the oracle, including +-inf, subnormal gates and the
+    gates whose sigmoid is a bf16 subnormal."""
+    bits = np.arange(65536, dtype=np.uint32)
+    is_nan = (((bits >> 7) & 0xFF) == 0xFF) & ((bits & 0x7F) != 0)
+    vals = (bits[~is_nan] << 16).view(np.float32).astype(np.float64)
+    rows = -(-vals.size // 6144)
+    inp = Inputs(SEED + 11, rows, rows)
+    g = np.zeros(rows * 6144)
+    g[:vals.size] = vals
+    qg = inp.cpu["qg"].clone()
+    qg[:, :, 256:] = torch.from_numpy(g.reshape(rows, 24, 256)).to(torch.bfloat16)
+    inp.cpu["qg"], inp.np["qg"] = qg, np64(qg)
+    inp.cpu["v"] = torch.ones_like(inp.cpu["v"])
+    inp.np["v"] = np64(inp.cpu["v"])
+    d = inp.dev()
+    got = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, rows)
+    want = inp.ref(0, rows, "causal").out
+    assert np.array_equal(want.reshape(-1)[:vals.size], O.sigmoid_gate(vals))
+    g_np = np64(got)
+    diff = np.flatnonzero(g_np.reshape(-1) != want.reshape(-1))
+    assert diff.size == 0, f"{diff.size} gates differ, e.g. g={g[diff[:5]]}"
+
+
 def test_row_stats_and_hidden_free_causal():
     inp = Inputs(SEED + 6, 256, 256)
     d = inp.dev()

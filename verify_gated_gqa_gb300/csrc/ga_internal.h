@@ -22,7 +22,7 @@ constexpr double kEpsD = 1e-6;
 constexpr double kRopeBase = 1e7;
 
 constexpr int kTileM = 128;  // query rows per attention tile
-constexpr int kTileN = 64;   // keys per attention tile
+constexpr int kTileN = 128;  // keys per attention tile
 
 // Attention kernel variants.
 enum AttnMode : int {
@@ -41,7 +41,7 @@ struct AttnArgs {
   uint16_t* weights;        // weights pass: [24][rows][T]
   int* hidden_rows;         // nullable
   const uint32_t* mask_bits;  // [rows_pad][mask_words], bit j of word w <-> key 32w + j
-  const uint8_t* tile_flags;  // [row_tiles][key_tiles] (128 rows x 64 keys), 1 = a visible key
+  const uint8_t* tile_flags;  // [row_tiles][key_tiles] (128 rows x 128 keys), 1 = a visible key
   int* status;              // device status word
   int rows, T, q_base, mode, weights_pass;
   int row_tiles, key_tiles, mask_words;

@@ -3,7 +3,7 @@
 // mask as given, non-zero = visible).
 //
 // Reads the uint8 mask once and writes (a) one bit per (row, key) -- bit j of word w is
-// key 32w + j -- and (b) one flag per (128-row tile, 64-key tile) that says whether any
+// key 32w + j -- and (b) one flag per (128-row tile, 128-key tile) that says whether any
 // key of the tile is visible to any row of the tile, so the attention kernel skips
 // all-hidden tiles without loading them. Rows >= rows and keys >= T read as hidden.
 #include "ga_internal.h"
@@ -21,11 +21,14 @@ __global__ void __launch_bounds__(128) mask_prepass_kernel(const uint8_t* __rest
   const int r = threadIdx.x;
   const int row = mt * kTileM + r;
   const int k0 = kt * kTileN;
-  uint32_t w[2] = {0u, 0u};
+  constexpr int kWords = kTileN / 32;
+  uint32_t w[kWords];
+#pragma unroll
+  for (int i = 0; i < kWords; ++i) w[i] = 0u;
   if (row < rows) {
     const uint8_t* src = mask + (long long)row * ld_mask + k0;
 #pragma unroll
-    for (int c = 0; c < kTileN / 16; ++c) {  // 16-byte chunks of the row's 64 keys
+    for (int c = 0; c < kTileN / 16; ++c) {  // 16-byte chunks of the row's keys
       const int j0 = k0 + 16 * c;
       uint8_t b[16];
       if (j0 + 16 <= T) {
@@ -41,8 +44,14 @@ __global__ void __launch_bounds__(128) mask_prepass_kernel(const uint8_t* __rest
       w[c >> 1] |= m << (16 * (c & 1));
     }
   }
-  reinterpret_cast<uint2*>(bits + (size_t)row * mask_words)[kt] = make_uint2(w[0], w[1]);
-  const int any = __syncthreads_or((w[0] | w[1]) != 0u);
+  uint32_t any_bit = 0u;
+  uint32_t* dst = bits + (size_t)row * mask_words + (size_t)kt * kWords;
+#pragma unroll
+  for (int i = 0; i < kWords; ++i) {
+    dst[i] = w[i];
+    any_bit |= w[i];
+  }
+  const int any = __syncthreads_or(any_bit != 0u);
   if (r == 0) flags[(size_t)mt * key_tiles + kt] = any ? 1 : 0;
 }
 

@@ -17,13 +17,15 @@ namespace ga {
 // kMidMargin fp32 ulps away from a bf16 midpoint (the lower 16 bits equal 0x8000 there).
 constexpr int kMidMargin = 8;
 
-__device__ __forceinline__ bool near_bf16_midpoint(float y) {
+__device__ __forceinline__ bool near_bf16_midpoint(float y, int margin = kMidMargin) {
   const int lo = (int)(__float_as_uint(y) & 0xFFFFu) - 0x8000;
-  return lo <= kMidMargin && lo >= -kMidMargin;
+  return lo <= margin && lo >= -margin;
 }
 
-// bf16 (nearest, ties to even) of a finite double in bf16's normal range, as a float.
+// bf16 (nearest, ties to even) of a finite double within bf16's range, as a float. Below
+// 2^-126 bf16 is subnormal, a multiple of 2^-133.
 __device__ __forceinline__ float bf16_of_double(double x) {
+  if (fabs(x) < 0x1p-126) return (float)(rint(x * 0x1p133) * 0x1p-133);
   unsigned long long u = (unsigned long long)__double_as_longlong(x);
   u += 0x00000FFFFFFFFFFFull + ((u >> 45) & 1ull);
   u &= ~0x00001FFFFFFFFFFFull;
@@ -81,6 +83,54 @@ static __device__ __noinline__ float norm_elem_slow(float x, float w, float hi, 
 }
 static __device__ __noinline__ float sigmoid_slow(float g) {
   return bf16_of_double(1.0 / (1.0 + exp(-(double)g)));
+}
+
+// Fast path of norm_elem: the fp32 value before its bf16 rounding. When
+// near_bf16_midpoint() of it holds, the element needs norm_elem_slow.
+__device__ __forceinline__ float norm_elem_f32(float x, float w, float r32) {
+  return (x * r32) * (1.0f + w);
+}
+// Fast sigmoid of a bf16 g for the epilogue: 1 / (1 + 2^(-g log2 e)) with the exponent
+// split exactly (g has 8 significant bits, kL2eHi 16, so -g * kL2eHi is exact in fp32; the
+// small remainder -g * kL2eLo is applied as a first-order factor), ex2.approx and
+// rcp.approx. Over every bf16 g whose sigmoid is a normal fp32 number the result is within
+// a few fp32 ulps (checked exhaustively on the device against the double definition); the
+// caller rounds it to bf16 unless it lies within kSigmoidMargin ulps of a bf16 midpoint,
+// or g is outside that range, and then sigmoid_slow is the answer: returns false for those.
+// Where 2^-g*log2e is below 2^-32 the sum 1 + e is exactly 1 and so is the bf16 result.
+constexpr int kSigmoidMargin = 12;
+constexpr float kL2eHi = 1.44268798828125f;          // 47274 / 2^15: log2(e) to 16 bits
+constexpr float kL2eLo = 7.05260771340736e-06f;      // log2(e) - kL2eHi
+__device__ __forceinline__ bool sigmoid_fast(float g, float& y) {
+  const float th = -g * kL2eHi;
+  // the remainder from a clamped g, so that an infinite g gives 0 * finite, not 0 * inf
+  // (a NaN g still gives NaN through th)
+  const float tl = -fminf(fmaxf(g, -256.0f), 256.0f) * kL2eLo;
+  float e0, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(th));
+  const float e = fmaf(e0, tl * 0.6931471805599453f, e0);
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  y = r;
+  return th <= 120.0f && !near_bf16_midpoint(r, kSigmoidMargin);
+}
+
+// Norm of one element with a double-float product, good to about 2^-46 relative: y =
+// bf16(x * (1 + w) * r64), where r64 = rh + rl is the row's double inverse RMS. x * w is
+// exact in fp32 (8 x 8 significant bits) and TwoSum makes x + x*w exact; the product with
+// rh + rl is carried as an unevaluated sum, renormalised to s + t with |t| <= half an
+// ulp of s. An s that is not a bf16 midpoint rounds like s + t (a midpoint is at least
+// one ulp away); an s on a midpoint is nudged one ulp toward t before the rounding.
+__device__ __forceinline__ float norm_elem_exact(float x, float w, float rh, float rl) {
+  const float xw = x * w;
+  float ph, pl;
+  two_sum(x, xw, ph, pl);
+  const float yh = ph * rh;
+  const float yl = fmaf(ph, rh, -yh) + fmaf(ph, rl, pl * rh);
+  const float s = yh + yl;
+  const float t = yl - (s - yh);
+  uint32_t u = __float_as_uint(s);
+  if ((u & 0xFFFFu) == 0x8000u && t != 0.0f) u += ((t > 0.0f) == (s > 0.0f)) ? 1u : 0xFFFFFFFFu;
+  return bf16_round(__uint_as_float(u));
 }
 
 // bf16 of x * inv_rms * (1 + w) for a bf16 x and a bf16 weight w.
