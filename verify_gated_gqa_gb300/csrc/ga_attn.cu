@@ -26,14 +26,19 @@
 //   warps 4-7  softmax, one query row per thread: S is copied to registers and its TMEM
 //              columns released at once (so the next S = Q K^T overlaps this softmax),
 //              P = bf16(2^(t - M)) goes to shared memory, the rare O rescale;
-//   warps 8-11 the edge of each work item, off the critical path: the next item's Q
-//              (norm, RoPE) into TMEM, and the gated epilogue (O drained to bf16
-//              registers first so the next item's P V can start, then the gate and
-//              16-byte stores). Rows of upcoming items are prefetched into L2.
+//   warps 8-11 the edge of each work item: the next item's Q (norm, RoPE) into TMEM as
+//              soon as the current item's last S = Q K^T has read Q (its sum of squares
+//              is taken earlier, off that path), then the gated epilogue of the current
+//              item (O drained to the output rows first, so the next item's P V can start,
+//              then the gate applied in place).
+// The edge code is kept in short loops: the four roles run different code at once and
+// share the SM's instruction cache, which long unrolled sequences would overflow.
 // Tensor memory (512 columns x 128 lanes, lane = query row): O [0, 256) fp32, Q
 // [256, 384) bf16 pairs, S [384, 512) fp32.
 // Work items are (query head, 128-row tile), longest first, dealt to the CTAs in a
-// serpentine order so each CTA's total work evens out.
+// serpentine order so each CTA's total work evens out. The kernel is compiled once per
+// visibility mode (causal, bidirectional, stored mask) and for the weights pass, so each
+// variant carries only its own code.
 #include "ga_internal.h"
 #include "ga_numerics.cuh"
 #include "ga_sm100.cuh"
@@ -79,7 +84,6 @@ struct AttnSmem {
 struct Item {
   int h, mt;          // query head, 128-row tile
   int n;              // key tiles to visit
-  bool masked;        // mask mode: visit only the key tiles listed in `tiles`
   uint64_t tiles[2];  // mask mode: bit kt set for every key tile with a visible key
 };
 
@@ -87,17 +91,17 @@ __device__ __forceinline__ int item_index(int round, int cta, int G) {
   return round * G + ((round & 1) ? (G - 1 - cta) : cta);
 }
 
+template <int kMode>
 __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
   Item it;
   it.mt = a.row_tiles - 1 - idx / kHeads;  // later row tiles see more keys: longest first
   it.h = idx % kHeads;
-  it.masked = a.mode == kModeMask;
   it.tiles[0] = it.tiles[1] = 0;
-  if (a.mode == kModeCausal) {
+  if (kMode == kModeCausal) {
     const int last_row = min(a.rows, (it.mt + 1) * kTileM) - 1;
     const int key_end = min(a.T, a.q_base + last_row + 1);
     it.n = (key_end + kTileN - 1) / kTileN;
-  } else if (a.mode == kModeBidir) {
+  } else if (kMode == kModeBidir) {
     it.n = (a.T + kTileN - 1) / kTileN;
   } else {
     const uint8_t* f = a.tile_flags + (size_t)it.mt * a.key_tiles;
@@ -109,11 +113,12 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
 }
 
 // Walks the key tiles of an item in order: 0 .. n-1, or the set bits of a mask-mode item.
+template <int kMode>
 struct TileCursor {
   uint64_t w0, w1;
   __device__ __forceinline__ explicit TileCursor(const Item& it) : w0(it.tiles[0]), w1(it.tiles[1]) {}
-  __device__ __forceinline__ int next(const Item& it, int j) {
-    if (!it.masked) return j;
+  __device__ __forceinline__ int next(int j) {
+    if (kMode != kModeMask) return j;
     if (w0) {
       const int kt = __ffsll((long long)w0) - 1;
       w0 &= w0 - 1;
@@ -127,6 +132,7 @@ struct TileCursor {
 
 // The CTA's sequence of work items that have key tiles (items without any, in mask
 // mode, are skipped here and answered by the edge warps).
+template <int kMode>
 struct ItemWalk {
   int round = 0;
   __device__ __forceinline__ bool next(const AttnArgs& a, Item& out) {
@@ -134,7 +140,7 @@ struct ItemWalk {
     for (;; ++round) {
       const int idx = item_index(round, blockIdx.x, G);
       if (idx >= a.n_items) return false;
-      out = make_item(a, idx);
+      out = make_item<kMode>(a, idx);
       if (out.n > 0) {
         ++round;
         return true;
@@ -148,6 +154,7 @@ __device__ __forceinline__ void record_abort(int* status, int code) {
 }
 
 // ------------------------------------------------------------------ warp 0: producer
+template <int kMode, bool kW>
 __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                               const AttnArgs& a, volatile int* abort, uint32_t& cnt) {
   auto load_tile = [&](const CUtensorMap* map, int kvh, int kt) -> bool {
@@ -159,25 +166,26 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_k, const CUten
     ++cnt;
     return true;
   };
-  ItemWalk walk;
+  ItemWalk<kMode> walk;
   Item it;
   while (walk.next(a, it)) {
     const int kvh = it.h / kGroup;
-    TileCursor ck(it), cv(it);
+    TileCursor<kMode> ck(it), cv(it);
     // Ring order = MMA order: K0, then (K_j, V_{j-1}) for j >= 1, then V_{n-1}.
-    if (!load_tile(tm_k, kvh, ck.next(it, 0))) return;
+    if (!load_tile(tm_k, kvh, ck.next(0))) return;
     for (int j = 1; j < it.n; ++j) {
-      if (!load_tile(tm_k, kvh, ck.next(it, j))) return;
-      if (!a.weights_pass && !load_tile(tm_v, kvh, cv.next(it, j - 1))) return;
+      if (!load_tile(tm_k, kvh, ck.next(j))) return;
+      if (!kW && !load_tile(tm_v, kvh, cv.next(j - 1))) return;
     }
-    if (!a.weights_pass && !load_tile(tm_v, kvh, cv.next(it, it.n - 1))) return;
+    if (!kW && !load_tile(tm_v, kvh, cv.next(it.n - 1))) return;
   }
 }
 
+template <int kMode, bool kW>
 __device__ void producer(AttnSmem& sm, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                          const AttnArgs& a, volatile int* abort) {
   uint32_t cnt = 0;
-  producer_loop(sm, tm_k, tm_v, a, abort, cnt);
+  producer_loop<kMode, kW>(sm, tm_k, tm_v, a, abort, cnt);
   if (*abort) {
     // let the loads already issued into the slots land before exit
     const uint32_t first = cnt > (uint32_t)kSlots ? cnt - kSlots : 0;
@@ -187,6 +195,7 @@ __device__ void producer(AttnSmem& sm, const CUtensorMap* tm_k, const CUtensorMa
 }
 
 // ------------------------------------------------------------------ warp 1: MMA issuer
+template <int kMode, bool kW>
 __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
   constexpr uint32_t kIdQK = idesc_bf16(128, kTileN, false, false);
   constexpr uint32_t kIdPV = idesc_bf16(128, kDim, false, true);
@@ -221,7 +230,7 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
     return true;
   };
 
-  ItemWalk walk;
+  ItemWalk<kMode> walk;
   Item it;
   while (walk.next(a, it)) {
     if (!mbar_wait(&sm.q_full, it_done & 1, abort)) return;
@@ -241,9 +250,9 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
       umma_commit(&sm.empty[slot]);
       umma_commit(&sm.s_full);
       if (j == it.n - 1) umma_commit(&sm.q_empty);
-      if (!a.weights_pass && j >= 1 && !issue_pv(j - 1, g - 1)) return;
+      if (!kW && j >= 1 && !issue_pv(j - 1, g - 1)) return;
     }
-    if (!a.weights_pass) {
+    if (!kW) {
       if (!issue_pv(it.n - 1, g - 1)) return;
       umma_commit(&sm.o_done);
     }
@@ -253,8 +262,9 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
 
 // Issue every MMA, then wait (bounded) until all of them completed, so that tensor
 // memory is never released under an MMA in flight.
+template <int kMode, bool kW>
 __device__ void mma_issuer(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
-  mma_loop(sm, a, tmem, abort);
+  mma_loop<kMode, kW>(sm, a, tmem, abort);
   umma_commit(&sm.drain);
   mbar_wait_quiet(&sm.drain, 0, 100000000LL);
 }
@@ -274,15 +284,25 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // Visibility of the 32 keys kt*128 + 32*ch .. +31 for one row: bit k <-> key +k.
+template <int kMode>
 __device__ __forceinline__ uint32_t chunk_visibility(const AttnArgs& a, int row, int kt, int ch,
                                                      bool valid) {
   if (!valid) return 0u;
-  if (a.mode == kModeMask)
+  if (kMode == kModeMask)
     return __ldg(a.mask_bits + (size_t)row * a.mask_words + kt * (kTileN / 32) + ch);
   const int first = kt * kTileN + ch * 32;
-  int n = (a.mode == kModeCausal) ? (a.q_base + row - first + 1) : (a.T - first);
+  int n = (kMode == kModeCausal) ? (a.q_base + row - first + 1) : (a.T - first);
   n = max(0, min(32, n));
   return n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
+}
+
+// Every key of tile kt visible to every row of row tile mt (no per-key selects needed).
+template <int kMode>
+__device__ __forceinline__ bool tile_full(const AttnArgs& a, int mt, int kt) {
+  if (kMode == kModeMask) return false;
+  if ((mt + 1) * kTileM > a.rows || (kt + 1) * kTileN > a.T) return false;
+  if (kMode == kModeCausal) return (kt + 1) * kTileN - 1 <= a.q_base + mt * kTileM;
+  return true;
 }
 
 // ------------------------------------------------------------------ warps 4-7: softmax
@@ -318,6 +338,7 @@ __device__ __forceinline__ void weights_tile(const AttnArgs& a, const uint32_t (
   }
 }
 
+template <int kMode, bool kW>
 __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
                                volatile int* abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -326,7 +347,7 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const uint32_t s_taddr = tmem + kTmemS + lane_off;
   uint32_t g = 0, it_done = 0;
-  ItemWalk walk;
+  ItemWalk<kMode> walk;
   Item it;
   while (walk.next(a, it)) {
     const int row = it.mt * kTileM + r;
@@ -336,14 +357,14 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
     bool hasM = false;
     float l = 0.f;
     float l_final = 0.f;  // weights pass: the main pass's l (relative to its final M)
-    if (a.weights_pass && valid) {
+    if (kW && valid) {
       M = (int)a.row_stats[((size_t)h * a.rows + row) * 2];
       l_final = a.row_stats[((size_t)h * a.rows + row) * 2 + 1];
       hasM = l_final > 0.f;
     }
-    TileCursor cursor(it);
+    TileCursor<kMode> cursor(it);
     for (int j = 0; j < it.n; ++j, ++g) {
-      const int kt = cursor.next(it, j);
+      const int kt = cursor.next(j);
       if (!warp_wait(&sm.s_full, g & 1, abort)) return;
       tc_fence_after();
       // S -> registers (four loads, one wait), packed in place as bf16 pairs (the score's
@@ -356,33 +377,40 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
       tmem_wait_ld(sb);
       tc_fence_before();
       mbar_arrive(&sm.s_free);   // the next S = Q K^T may overwrite these columns now
+      if (tile_full<kMode>(a, it.mt, kt)) {
 #pragma unroll
-      for (int ch = 0; ch < kTileN / 32; ++ch) {
-        const uint32_t vis = chunk_visibility(a, row, kt, ch, valid);
+        for (int k = 0; k < kTileN / 2; ++k)
+          sb[k] = pack_bf16x2(__uint_as_float(sb[2 * k]), __uint_as_float(sb[2 * k + 1]));
+      } else {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          // hidden keys read as -inf: weight exactly 0, never the maximum
-          const int e = ch * 32 + 2 * k;
-          const float s0 = ((vis >> (2 * k)) & 1u) ? __uint_as_float(sb[e]) : -INFINITY;
-          const float s1 = ((vis >> (2 * k + 1)) & 1u) ? __uint_as_float(sb[e + 1]) : -INFINITY;
-          sb[ch * 16 + k] = pack_bf16x2(s0, s1);   // writes an index already read
+        for (int ch = 0; ch < kTileN / 32; ++ch) {
+          const uint32_t vis = chunk_visibility<kMode>(a, row, kt, ch, valid);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            // hidden keys read as -inf: weight exactly 0, never the maximum
+            const int e = ch * 32 + 2 * k;
+            const float s0 = ((vis >> (2 * k)) & 1u) ? __uint_as_float(sb[e]) : -INFINITY;
+            const float s1 = ((vis >> (2 * k + 1)) & 1u) ? __uint_as_float(sb[e + 1]) : -INFINITY;
+            sb[ch * 16 + k] = pack_bf16x2(s0, s1);   // writes an index already read
+          }
         }
       }
 
-      if (a.weights_pass) {
+      if (kW) {
         if (valid && hasM) weights_tile(a, sb, h, row, kt, M, l_final);
         continue;
       }
-      // tile maximum of the bf16 scores
-      float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+      // tile maximum of the bf16 scores (four independent chains of pair maxima)
+      uint32_t m0 = sb[0], m1 = sb[1], m2 = sb[2], m3 = sb[3];
 #pragma unroll
-      for (int k = 0; k < kTileN / 2; k += 2) {
-        m0 = fmaxf(m0, lo_f(sb[k]));
-        m1 = fmaxf(m1, hi_f(sb[k]));
-        m2 = fmaxf(m2, lo_f(sb[k + 1]));
-        m3 = fmaxf(m3, hi_f(sb[k + 1]));
+      for (int k = 4; k < kTileN / 2; k += 4) {
+        m0 = max_bf16x2(m0, sb[k]);
+        m1 = max_bf16x2(m1, sb[k + 1]);
+        m2 = max_bf16x2(m2, sb[k + 2]);
+        m3 = max_bf16x2(m3, sb[k + 3]);
       }
-      const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+      const uint32_t mm = max_bf16x2(max_bf16x2(m0, m1), max_bf16x2(m2, m3));
+      const float mx = fmaxf(lo_f(mm), hi_f(mm));
       bool rescale = false;
       int newM = M;
       if (mx != -INFINITY) {
@@ -417,27 +445,27 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
       // P = bf16(2^(t - M)), t = bf16(s) * log2(e) / 16, into shared memory once the
       // previous P.V has read the buffer; l sums the rounded P
       if (g > 0 && !warp_wait(&sm.p_empty, (g - 1) & 1, abort)) return;
-      float la = 0.f, lb = 0.f;
+      const float2 c2 = make_float2(kLog2eOver16, kLog2eOver16);
+      const float2 nm = make_float2(-mf, -mf);
+      float2 la = make_float2(0.f, 0.f), lb = la;
 #pragma unroll
       for (int cd = 0; cd < kTileN / 8; ++cd) {
         uint32_t pk[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint32_t w = sb[cd * 4 + k];
-          const float p0 = ex2_approx(fmaf(lo_f(w), kLog2eOver16, -mf));
-          const float p1 = ex2_approx(fmaf(hi_f(w), kLog2eOver16, -mf));
-          pk[k] = pack_bf16x2(p0, p1);
-          la += lo_f(pk[k]);
-          lb += hi_f(pk[k]);
+          const float2 t = fma2(bf16x2_to_f32x2(sb[cd * 4 + k]), c2, nm);
+          pk[k] = pack_bf16x2(ex2_approx(t.x), ex2_approx(t.y));
+          if (k & 1) lb = add2(lb, bf16x2_to_f32x2(pk[k]));
+          else la = add2(la, bf16x2_to_f32x2(pk[k]));
         }
         uint8_t* dst = sm.p[cd >> 3] + sw128_offset((uint32_t)r, (uint32_t)(cd & 7));
         *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      l += la + lb;
+      l += (la.x + lb.x) + (la.y + lb.y);
       fence_async_smem();
       mbar_arrive(&sm.p_full);
     }
-    if (!a.weights_pass) {
+    if (!kW) {
       // hand l and M of this item to the edge warps
       if (it_done > 0 && !warp_wait(&sm.st_empty, (it_done - 1) & 1, abort)) return;
       sm.stat_l[r] = l;
@@ -449,96 +477,226 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
 }
 
 // ------------------------------------------------------------------ warps 8-11: edge
-// Norm of 8 dims (4 words of bf16 pairs, weights wv) with the row's double inverse RMS
-// rh + rl: exact bf16 values in y.
-__device__ __forceinline__ void norm8_exact(const uint4& xv, const uint4& wv, float rh, float rl,
-                                            float (&y)[8]) {
+// Query norm, fast path: y = (x r) (1 + w) as fma(x r, w, x r), with r the row's inverse
+// RMS rounded to fp32 (from its double-float value). Three roundings of at most half an
+// ulp each (r, x r, the fma) keep y within 3 ulps of the exact value, so y rounds to the
+// exact bf16 unless its lower 16 bits lie within 3 of 0x8000 (a bf16 midpoint). The
+// test key below is under kNearKey exactly for those values (within 4, to be safe).
+constexpr uint32_t kNearKey = 9u << 16;
+__device__ __forceinline__ uint32_t near_key(float y) {
+  return __float_as_uint(y) * 65536u + 0x80040000u;
+}
+
+// Norm of 8 dims (x: 4 words of bf16 pairs, w: their weights); tmin collects the
+// smallest midpoint key.
+__device__ __forceinline__ void norm8(const uint4& xv, const uint4& wv, float rf, float (&y)[8],
+                                      uint32_t& tmin) {
   const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-  const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+  const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+  const float2 r2 = make_float2(rf, rf);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    y[2 * k] = norm_elem_exact(lo_f(xs[k]), lo_f(ww[k]), rh, rl);
-    y[2 * k + 1] = norm_elem_exact(hi_f(xs[k]), hi_f(ww[k]), rh, rl);
+    const float2 xr = mul2(bf16x2_to_f32x2(xs[k]), r2);
+    const float2 yy = fma2(xr, bf16x2_to_f32x2(ws[k]), xr);
+    tmin = min(tmin, min(near_key(yy.x), near_key(yy.y)));
+    y[2 * k] = yy.x;
+    y[2 * k + 1] = yy.y;
   }
 }
 
-// (1+w) RMSNorm and partial RoPE of one query row into registers, as the bf16 pairs of
-// its TMEM lane (word c holds dims 2c and 2c+1); rows past the end give zeros. The sum
-// of squares is carried as hi + lo, the inverse RMS taken in double once per row, and
-// every element's product is formed in double-float, so no element needs a second pass.
-__device__ __forceinline__ void prep_q_compute(const AttnSmem& sm, const AttnArgs& a, int h,
-                                               int row, bool valid, uint32_t (&q)[kDim / 2]) {
-  if (!valid) {
+// The row's inverse RMS, 1 / sqrt(sum / 256 + 1e-6): f its fp32 value, h + l good to
+// about 2^-46 relative. From rsqrt's estimate r0, one Newton step carried in double-float:
+// with a r0^2 = 1 - e (e about 2^-22, formed exactly up to 2^-46), r = r0 (1 + e/2 + 3e^2/8).
+struct InvRms {
+  float f, h, l;
+};
+__device__ __forceinline__ InvRms inv_rms_df(const SumSq& s) {
+  constexpr float kEpsHi = 1e-6f;
+  constexpr float kEpsLo = 2.5247573e-15f;  // 1e-6 - kEpsHi
+  float ah, al;
+  two_sum(s.hi * (1.0f / 256.0f), kEpsHi, ah, al);
+  al += s.lo * (1.0f / 256.0f) + kEpsLo;
+  const float r0 = rsqrtf(ah);
+  const float sq = r0 * r0;
+  const float sqe = fmaf(r0, r0, -sq);          // r0^2 = sq + sqe exactly
+  const float th = ah * sq;
+  float te = fmaf(ah, sq, -th);                 // ah sq = th + te exactly
+  te = fmaf(ah, sqe, te);
+  te = fmaf(al, sq, te);
+  const float e = (1.0f - th) - te;             // 1 - th is exact (th within 2^-20 of 1)
+  const float c = r0 * fmaf(0.375f * e, e, 0.5f * e);
+  InvRms r;
+  r.h = r0;
+  r.l = c;
+  r.f = r0 + c;
+  return r;
+}
+
+// Pass 1 of the query norm: the row's sum of squares (off the tensor cores' critical
+// path: it needs no tensor memory).
+__device__ SumSq q_sumsq(const AttnArgs& a, int h, int row, bool valid) {
+  SumSq s0, s1;
+  if (valid) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.qg + ((size_t)row * kHeads + h) * kQgStride);
+#pragma unroll 1
+    for (int i0 = 0; i0 < kDim / 8; i0 += 8) {
+      uint4 v[8];
 #pragma unroll
-    for (int k = 0; k < kDim / 2; ++k) q[k] = 0u;
-    return;
-  }
-  const uint4* src = reinterpret_cast<const uint4*>(a.qg + ((size_t)row * kHeads + h) * kQgStride);
-  const uint4* wq = sm.w_q;
-  // pass 1: the sum of squares over the row (32 loads in flight, consumed as they land)
-  SumSq acc[4];
-  {
-    uint4 v[32];
+      for (int i = 0; i < 8; ++i) v[i] = __ldg(src + i0 + i);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __ldg(src + i);
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t ws[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      acc[i & 3].add(lo_f(v[i].x)); acc[i & 3].add(hi_f(v[i].x));
-      acc[i & 3].add(lo_f(v[i].y)); acc[i & 3].add(hi_f(v[i].y));
-      acc[i & 3].add(lo_f(v[i].z)); acc[i & 3].add(hi_f(v[i].z));
-      acc[i & 3].add(lo_f(v[i].w)); acc[i & 3].add(hi_f(v[i].w));
+        for (int k = 0; k < 4; ++k) {
+          s0.add(lo_f(ws[k]));
+          s1.add(hi_f(ws[k]));
+        }
+      }
     }
   }
-  acc[0].merge(acc[1]);
-  acc[2].merge(acc[3]);
-  acc[0].merge(acc[2]);
-  const double r64 = inv_rms_f64(acc[0]);
-  const float rh = (float)r64;
-  const float rl = (float)(r64 - (double)rh);
-  // pass 2 (the row is in L1 now). Dims 0..63 with the rotation: dims 8c..8c+7 pair
-  // with dims 8c+32..8c+39.
+  s0.merge(s1);
+  return s0;
+}
+
+__device__ __forceinline__ float bf_at(const uint16_t* p, int i) {
+  return __uint_as_float((uint32_t)p[i] << 16);
+}
+__device__ __forceinline__ void set_half(uint32_t* w, int d, float v) {
+  const uint32_t b = (uint32_t)bf16_bits(v);
+  w[d >> 1] = (d & 1) ? ((w[d >> 1] & 0xFFFFu) | (b << 16)) : ((w[d >> 1] & 0xFFFF0000u) | b);
+}
+
+// Rare path: a lane of this warp has, in group grp (dims 64 grp .. +63) of its row, a fast
+// norm value within the error bound of a bf16 midpoint. Every lane re-derives which of its
+// dims those are and replaces them (and, in the rotated dims, the rotation partners) by
+// exact values, patching its TMEM lane (warp-collective load and store).
+__device__ __noinline__ void q_fixup(const AttnArgs& a, const uint16_t* wq, int h, int row,
+                                     bool valid, int grp, InvRms r, uint32_t taddr) {
+  uint32_t w[32];
+  tmem_wait_st();
+  tmem_ld32(taddr, w);
+  tmem_wait_ld(w);
+  if (valid) {
+    const uint16_t* x = a.qg + ((size_t)row * kHeads + h) * kQgStride;
+    const int pos = a.q_base + row;
+#pragma unroll 1
+    for (int k = 0; k < 64; ++k) {
+      const int d = 64 * grp + k;
+      const float xr = bf_at(x, d) * r.f;
+      if (near_key(fmaf(xr, bf_at(wq, d), xr)) >= kNearKey) continue;
+      if (grp == 0) {
+        const int i = d & 31;
+        const float ya = norm_elem_exact(bf_at(x, i), bf_at(wq, i), r.h, r.l);
+        const float yb = norm_elem_exact(bf_at(x, i + 32), bf_at(wq, i + 32), r.h, r.l);
+        float ra, rb;
+        rope_pair(ya, yb, bf_at(a.cos_tab, pos * kHalfRot + i), bf_at(a.sin_tab, pos * kHalfRot + i),
+                  ra, rb);
+        set_half(w, i, ra);
+        set_half(w, i + 32, rb);
+      } else {
+        set_half(w, k, norm_elem_exact(bf_at(x, d), bf_at(wq, d), r.h, r.l));
+      }
+    }
+  }
+  __syncwarp();
+  tmem_st32(taddr, w);
+  tmem_wait_st();
+}
+
+// Pass 2 of the query norm and the partial RoPE: the row as bf16 pairs into this thread's
+// TMEM lane at Q (column c holds dims 2c and 2c+1); rows past the end store zeros. Every
+// lane of the warp runs it (the stores are warp-collective). The words of dims 0..63 and
+// their cos/sin are loaded by the caller before it waits for Q's columns.
+struct QGroup0 {
+  uint4 xa[4], xb[4], cv[4], sv[4];
+};
+__device__ __forceinline__ void q_load_group0(const AttnArgs& a, int h, int row, bool valid,
+                                              QGroup0& g) {
+  if (!valid) return;
+  const uint4* src = reinterpret_cast<const uint4*>(a.qg + ((size_t)row * kHeads + h) * kQgStride);
   const int pos = a.q_base + row;
   const uint4* cp = reinterpret_cast<const uint4*>(a.cos_tab + (size_t)pos * kHalfRot);
   const uint4* sp = reinterpret_cast<const uint4*>(a.sin_tab + (size_t)pos * kHalfRot);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    float ya[8], yb[8];
-    norm8_exact(__ldg(src + c), wq[c], rh, rl, ya);
-    norm8_exact(__ldg(src + c + 4), wq[c + 4], rh, rl, yb);
-    const uint4 cv = __ldg(cp + c), sv = __ldg(sp + c);
-    const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float cs = (e & 1) ? hi_f(cw[e >> 1]) : lo_f(cw[e >> 1]);
-      const float sn = (e & 1) ? hi_f(sw[e >> 1]) : lo_f(sw[e >> 1]);
-      float ra, rb;
-      rope_pair(ya[e], yb[e], cs, sn, ra, rb);
-      ya[e] = ra;
-      yb[e] = rb;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      q[4 * c + k] = pack2(ya[2 * k], ya[2 * k + 1]);
-      q[16 + 4 * c + k] = pack2(yb[2 * k], yb[2 * k + 1]);
-    }
-  }
-  // dims 64..255 pass through the rotation
-#pragma unroll
-  for (int c = 8; c < 32; ++c) {
-    float y[8];
-    norm8_exact(__ldg(src + c), wq[c], rh, rl, y);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) q[4 * c + k] = pack2(y[2 * k], y[2 * k + 1]);
+    g.xa[c] = __ldg(src + c);
+    g.xb[c] = __ldg(src + c + 4);
+    g.cv[c] = __ldg(cp + c);
+    g.sv[c] = __ldg(sp + c);
   }
 }
 
-// The prepared row into this thread's TMEM lane at Q. Every lane of the warp runs it
-// (the stores are warp-collective).
-__device__ __forceinline__ void store_q_tmem(const uint32_t (&q)[kDim / 2], uint32_t q_taddr) {
+__device__ void q_pass2(const AttnSmem& sm, const AttnArgs& a, int h, int row, bool valid,
+                        const QGroup0& g0, InvRms rr, uint32_t q_taddr) {
+  const uint4* src = reinterpret_cast<const uint4*>(a.qg + ((size_t)(valid ? row : 0) * kHeads + h) * kQgStride);
+  const uint16_t* wq16 = reinterpret_cast<const uint16_t*>(sm.w_q);
+  uint4 cur[8];
+  if (valid) {
 #pragma unroll
-  for (int grp = 0; grp < 4; ++grp)
-    tmem_st32(q_taddr + 32 * grp, *reinterpret_cast<const uint32_t(*)[32]>(q + 32 * grp));
+    for (int i = 0; i < 8; ++i) cur[i] = __ldg(src + 8 + i);   // group 1, in flight meanwhile
+  }
+  {
+    // dims 0..63 with the rotation: dims 8c..8c+7 pair with dims 8c+32..8c+39
+    uint32_t w[32];
+    uint32_t tmin = 0xFFFFFFFFu;
+    if (valid) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float ya[8], yb[8];
+        norm8(g0.xa[c], sm.w_q[c], rr.f, ya, tmin);
+        norm8(g0.xb[c], sm.w_q[c + 4], rr.f, yb, tmin);
+        const uint32_t cw[4] = {g0.cv[c].x, g0.cv[c].y, g0.cv[c].z, g0.cv[c].w};
+        const uint32_t sw[4] = {g0.sv[c].x, g0.sv[c].y, g0.sv[c].z, g0.sv[c].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float cs = (e & 1) ? hi_f(cw[e >> 1]) : lo_f(cw[e >> 1]);
+          const float sn = (e & 1) ? hi_f(sw[e >> 1]) : lo_f(sw[e >> 1]);
+          float ra, rb;
+          rope_pair(bf16_round(ya[e]), bf16_round(yb[e]), cs, sn, ra, rb);
+          ya[e] = ra;
+          yb[e] = rb;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          w[4 * c + k] = pack_bf16x2(ya[2 * k], ya[2 * k + 1]);
+          w[16 + 4 * c + k] = pack_bf16x2(yb[2 * k], yb[2 * k + 1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) w[k] = 0u;
+    }
+    tmem_st32(q_taddr, w);
+    if (__any_sync(0xffffffffu, tmin < kNearKey)) q_fixup(a, wq16, h, row, valid, 0, rr, q_taddr);
+  }
+  // dims 64..255 pass through the rotation; the next group's loads are issued first
+#pragma unroll 1
+  for (int grp = 1; grp < 4; ++grp) {
+    uint4 nxt[8];
+    if (valid && grp < 3) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nxt[i] = __ldg(src + 8 * (grp + 1) + i);
+    }
+    uint32_t w[32];
+    uint32_t tmin = 0xFFFFFFFFu;
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float y[8];
+        norm8(cur[i], sm.w_q[8 * grp + i], rr.f, y, tmin);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[4 * i + k] = pack_bf16x2(y[2 * k], y[2 * k + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) w[k] = 0u;
+    }
+    tmem_st32(q_taddr + 32 * grp, w);
+    if (__any_sync(0xffffffffu, tmin < kNearKey))
+      q_fixup(a, wq16, h, row, valid, grp, rr, q_taddr + 32 * grp);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+  }
   tmem_wait_st();
 }
 
@@ -556,9 +714,9 @@ __device__ __forceinline__ void prefetch_row(const AttnArgs& a, const Item& it, 
 
 // Outputs of a work item none of whose key tiles is visible (mask mode): every row is
 // hidden, its output row and statistics are zero.
-__device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r) {
+__device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r, bool weights_pass) {
   const int row = it.mt * kTileM + r;
-  if (row >= a.rows || a.weights_pass) return;
+  if (row >= a.rows || weights_pass) return;
   uint4* o = reinterpret_cast<uint4*>(a.out + (size_t)row * kOutRow + it.h * kDim);
   for (int i = 0; i < 32; ++i) o[i] = make_uint4(0, 0, 0, 0);
   if (a.row_stats) {
@@ -570,14 +728,15 @@ __device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r) {
 
 // One 32-dim batch of the gate with the exact sigmoid wherever the fast one is not
 // certified (rare: a gate whose sigmoid lies near a bf16 midpoint, or a very negative gate).
-// o0..o3 are the batch's bf16 pairs of O / l; the batch's 4 output words are rewritten.
-__device__ __noinline__ void gate_batch_slow(const uint4* gp, uint4* op, uint4 o0, uint4 o1,
-                                             uint4 o2, uint4 o3) {
+// o0..o3 are the batch's bf16 pairs of O / l, g0..g3 its gates; the batch's 4 output
+// words are rewritten.
+__device__ __noinline__ void gate_batch_slow(uint4* op, uint4 o0, uint4 o1, uint4 o2, uint4 o3,
+                                             uint4 g0, uint4 g1, uint4 g2, uint4 g3) {
   const uint4 ov[4] = {o0, o1, o2, o3};
+  const uint4 gv[4] = {g0, g1, g2, g3};
 #pragma unroll 1
   for (int i = 0; i < 4; ++i) {
-    const uint4 gv = gp[i];
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t gw[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
     const uint32_t ow[4] = {ov[i].x, ov[i].y, ov[i].z, ov[i].w};
     uint32_t res[4];
     for (int k = 0; k < 4; ++k) {
@@ -591,8 +750,9 @@ __device__ __noinline__ void gate_batch_slow(const uint4* gp, uint4* op, uint4 o
 }
 
 // Gated epilogue of one finished item: out = bf16(bf16(O / l) * bf16(sigmoid(gate))).
-// O is drained to bf16 registers first and released, then the gate is applied.
-__device__ __forceinline__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32_t tmem,
+// O / l is drained to the output row first and O released; then the gate is applied in
+// place (this thread re-reads the words it has just written).
+__device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32_t tmem,
                          uint32_t lane_off, int r, uint32_t it_done, volatile int* abort) {
   const int row = it.mt * kTileM + r;
   const bool valid = row < a.rows;
@@ -603,48 +763,71 @@ __device__ __forceinline__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const 
   if (!warp_wait(&sm.o_done, it_done & 1, abort)) return false;
   tc_fence_after();
   const float inv = l > 0.f ? 1.0f / l : 0.f;
-  uint32_t ob[kDim / 2];
-#pragma unroll
+  uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)(valid ? row : 0) * kOutRow + h * kDim);
+#pragma unroll 1
   for (int c = 0; c < kDim / 32; ++c) {
     uint32_t o[32];
     tmem_ld32(tmem + kTmemO + lane_off + c * 32, o);
     tmem_wait_ld(o);
+    uint32_t pk[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k)
-      ob[c * 16 + k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+      pk[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+    if (valid) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        op[4 * c + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
   }
   tc_fence_before();
   mbar_arrive(&sm.o_free);
   mbar_arrive(&sm.st_empty);
   if (!valid) return true;
   const uint4* gp = reinterpret_cast<const uint4*>(a.qg + ((size_t)row * kHeads + h) * kQgStride + kDim);
-  uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)row * kOutRow + h * kDim);
+  // 32 dims at a time; the next batch's loads are issued before this one is computed
+  uint4 ov[4], gv[4];
 #pragma unroll
-  for (int q4 = 0; q4 < 8; ++q4) {       // 32 dims at a time, 4 loads in flight
-    uint4 gv[4];
+  for (int i = 0; i < 4; ++i) {
+    ov[i] = op[i];
+    gv[i] = __ldg(gp + i);
+  }
+#pragma unroll 1
+  for (int b = 0; b < 8; ++b) {
+    uint4 on[4], gn[4];
+    if (b < 7) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) gv[i] = __ldg(gp + q4 * 4 + i);
+      for (int i = 0; i < 4; ++i) {
+        on[i] = op[4 * (b + 1) + i];
+        gn[i] = __ldg(gp + 4 * (b + 1) + i);
+      }
+    }
     bool ok = true;
+    uint4 res[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t gw[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
-      uint32_t res[4];
+      const uint32_t ow[4] = {ov[i].x, ov[i].y, ov[i].z, ov[i].w};
+      uint32_t rw[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t ow = ob[(q4 * 4 + i) * 4 + k];
         float s0, s1;
         ok &= sigmoid_fast(lo_f(gw[k]), s0);
         ok &= sigmoid_fast(hi_f(gw[k]), s1);
-        res[k] = pack2(lo_f(ow) * bf16_round(s0), hi_f(ow) * bf16_round(s1));
+        const float2 prod = mul2(bf16x2_to_f32x2(ow[k]), bf16x2_to_f32x2(pack_bf16x2(s0, s1)));
+        rw[k] = pack_bf16x2(prod.x, prod.y);
       }
-      op[q4 * 4 + i] = make_uint4(res[0], res[1], res[2], res[3]);
+      res[i] = make_uint4(rw[0], rw[1], rw[2], rw[3]);
     }
-    if (!ok) {
-      const int b = q4 * 16;
-      gate_batch_slow(gp + q4 * 4, op + q4 * 4, make_uint4(ob[b], ob[b + 1], ob[b + 2], ob[b + 3]),
-                      make_uint4(ob[b + 4], ob[b + 5], ob[b + 6], ob[b + 7]),
-                      make_uint4(ob[b + 8], ob[b + 9], ob[b + 10], ob[b + 11]),
-                      make_uint4(ob[b + 12], ob[b + 13], ob[b + 14], ob[b + 15]));
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) op[4 * b + i] = res[i];
+    } else {
+      gate_batch_slow(op + 4 * b, ov[0], ov[1], ov[2], ov[3], gv[0], gv[1], gv[2], gv[3]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ov[i] = on[i];
+      gv[i] = gn[i];
     }
   }
   if (a.row_stats) {
@@ -655,6 +838,7 @@ __device__ __forceinline__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const 
   return true;
 }
 
+template <int kMode, bool kW>
 __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -668,43 +852,52 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
     for (;; ++round) {
       const int idx = item_index(round, blockIdx.x, G);
       if (idx >= a.n_items) return false;
-      out = make_item(a, idx);
+      out = make_item<kMode>(a, idx);
       if (out.n > 0) {
         ++round;
         return true;
       }
-      write_hidden_rows(a, out, r);
+      write_hidden_rows(a, out, r, kW);
     }
   };
-  // Q of the next item is computed into registers while the tensor cores work on the
-  // current one, and stored into TMEM as soon as the current item's last S = Q K^T has
-  // read Q; then the current item's epilogue runs once its last P V is done.
-  uint32_t q[kDim / 2];
+  // Item i+1's Q goes into TMEM as soon as item i's last S = Q K^T has read Q (its sum
+  // of squares and first loads are done before that); then item i's epilogue runs once
+  // its last P V is done.
   Item cur, nxt;
   if (!next_item(cur)) return;
-  prep_q_compute(sm, a, cur.h, cur.mt * kTileM + r, cur.mt * kTileM + r < a.rows, q);
-  store_q_tmem(q, q_taddr);
-  tc_fence_before();
-  mbar_arrive(&sm.q_full);
+  QGroup0 g0;
+  {
+    const int row = cur.mt * kTileM + r;
+    const bool valid = row < a.rows;
+    const InvRms rr = inv_rms_df(q_sumsq(a, cur.h, row, valid));
+    q_load_group0(a, cur.h, row, valid, g0);
+    q_pass2(sm, a, cur.h, row, valid, g0, rr, q_taddr);
+    tc_fence_before();
+    mbar_arrive(&sm.q_full);
+  }
   uint32_t it_done = 0;
   while (true) {
     const bool have_next = next_item(nxt);
-    if (!a.weights_pass) prefetch_row(a, cur, r, 512);   // the current item's gates
+    if (!kW) prefetch_row(a, cur, r, 512);   // the current item's gates
     if (have_next) {
-      prep_q_compute(sm, a, nxt.h, nxt.mt * kTileM + r, nxt.mt * kTileM + r < a.rows, q);
+      const int row = nxt.mt * kTileM + r;
+      const bool valid = row < a.rows;
+      const InvRms rr = inv_rms_df(q_sumsq(a, nxt.h, row, valid));
+      q_load_group0(a, nxt.h, row, valid, g0);
       if (!warp_wait(&sm.q_empty, it_done & 1, abort)) return;
       tc_fence_after();
-      store_q_tmem(q, q_taddr);
+      q_pass2(sm, a, nxt.h, row, valid, g0, rr, q_taddr);
       tc_fence_before();
       mbar_arrive(&sm.q_full);
     }
-    if (!a.weights_pass && !epilogue(sm, a, cur, tmem, lane_off, r, it_done, abort)) return;
+    if (!kW && !epilogue(sm, a, cur, tmem, lane_off, r, it_done, abort)) return;
     ++it_done;
     if (!have_next) break;
     cur = nxt;
   }
 }
 
+template <int kMode, bool kW>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ AttnArgs a) {
@@ -749,12 +942,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
-    if (warp == 0 && lane == 0) producer(sm, &tm_k, &tm_v, a, abort);
-    if (warp == 1 && lane == 0) mma_issuer(sm, a, tmem, abort);
+    if (warp == 0 && lane == 0) producer<kMode, kW>(sm, &tm_k, &tm_v, a, abort);
+    if (warp == 1 && lane == 0) mma_issuer<kMode, kW>(sm, a, tmem, abort);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
-    if (warp < 8) softmax_worker(sm, a, tmem, abort);
-    else edge_worker(sm, a, tmem, abort);
+    if (warp < 8) softmax_worker<kMode, kW>(sm, a, tmem, abort);
+    else edge_worker<kMode, kW>(sm, a, tmem, abort);
   }
   tc_fence_before();
   __syncthreads();
@@ -771,13 +964,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t attn_smem_bytes() { return sizeof(AttnSmem) + 1024; }
 
 cudaError_t attn_set_smem_attribute() {
-  return cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)attn_smem_bytes());
+  const int bytes = (int)attn_smem_bytes();
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(attn_kernel<kModeCausal, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn_kernel<kModeBidir, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attn_kernel<kModeMask, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(attn_kernel<kModeMask, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 cudaError_t launch_attn(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
                         int grid, cudaStream_t s) {
-  attn_kernel<<<grid, kThreads, attn_smem_bytes(), s>>>(tm_k, tm_v, a);
+  const size_t smem = attn_smem_bytes();
+  if (a.weights_pass) {
+    if (a.mode != kModeMask) return cudaErrorInvalidValue;
+    attn_kernel<kModeMask, true><<<grid, kThreads, smem, s>>>(tm_k, tm_v, a);
+  } else if (a.mode == kModeCausal) {
+    attn_kernel<kModeCausal, false><<<grid, kThreads, smem, s>>>(tm_k, tm_v, a);
+  } else if (a.mode == kModeBidir) {
+    attn_kernel<kModeBidir, false><<<grid, kThreads, smem, s>>>(tm_k, tm_v, a);
+  } else {
+    attn_kernel<kModeMask, false><<<grid, kThreads, smem, s>>>(tm_k, tm_v, a);
+  }
   return cudaGetLastError();
 }
 
