@@ -133,7 +133,10 @@ int ga_k_prologue(const ga_bf16* k_raw, const ga_bf16* w_k, const ga_bf16* cos_t
  *   cos_tab, sin_tab [table_rows][32]; table_rows >= q_base + rows
  *   causal  1: row r sees keys j <= q_base + r;  0: bidirectional, every key j < T
  *           (q_base must then be 0)
- *   out     [rows][24 * 256] bf16, head-major columns
+ *   out     [rows][24 * 256] bf16, head-major columns. It may not overlap any input;
+ *           the call also uses it as scratch (each (row, head) slot holds that row's
+ *           prepared query before its output), so its contents are unspecified until
+ *           the call has completed on the stream.
  *   row_stats NULL or [24][rows][2] float: per (head, row) the final running maximum M
  *           (an integer, base-2 units) and the sum l of the rounded weights relative to
  *           2^M, so that the row's weights are bf16(2^(t - M)) / l with t = s * log2(e).
@@ -153,7 +156,7 @@ size_t ga_masked_workspace_bytes(int rows, int T);
  * the selection mask as given, non-zero = visible; it is not ANDed with causality here).
  *   qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, q_base: as in ga_attn_prefill
  *   mask    [rows][ld_mask] uint8; row r is query position q_base + r, column j key j
- *   out     [rows][24 * 256]
+ *   out     [rows][24 * 256] (scratch during the call, as in ga_attn_prefill)
  *   weights NULL or [24][rows][T] bf16: the normalised weights bf16(w_hat / L), exactly
  *           0 where a key is hidden
  *   hidden_rows NULL or one device int; receives the number of rows with no visible key
@@ -181,7 +184,7 @@ size_t ga_verify_workspace_bytes(int n_seq, int rows, int max_len);
  *            window's own keys included; fill with ga_k_prologue)
  *   v_cache  [n_seq][cap][2][256] values
  *   seq_len  HOST array of n_seq ints: L_b, with L_b >= 0 and L_b + rows <= cap
- *   out      [n_seq][rows][24 * 256]
+ *   out      [n_seq][rows][24 * 256] (scratch during the call, as in ga_attn_prefill)
  *   workspace >= ga_verify_workspace_bytes(n_seq, rows, max L_b), 256-byte aligned
  * Row r of sequence b sees keys 0 .. L_b + r.
  * Rules: 1 <= rows <= 16, cap <= GA_MAX_TOKENS, table_rows >= max L_b + rows.

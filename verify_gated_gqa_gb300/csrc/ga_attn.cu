@@ -75,7 +75,7 @@ struct AttnSmem {
   uint4 w_q[kDim / 8];                // the query norm weight, staged once
   uint64_t full[kSlots], empty[kSlots];
   uint64_t q_full, q_empty, s_full, s_free, p_full, p_empty;
-  uint64_t o_ready, o_done, o_free, st_full, st_empty, drain;
+  uint64_t o_ready, o_done, o_free, st_full, st_empty, drain, q_read;
   uint32_t tmem_base;
   int abort;
 };
@@ -155,14 +155,16 @@ __device__ __forceinline__ void record_abort(int* status, int code) {
 
 // ------------------------------------------------------------------ warp 0: producer
 template <int kMode, bool kW>
-__device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                              const AttnArgs& a, volatile int* abort, uint32_t& cnt) {
-  auto load_tile = [&](const CUtensorMap* map, int kvh, int kt) -> bool {
+__device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                              const CUtensorMap* tm_v, const AttnArgs& a, volatile int* abort,
+                              uint32_t& cnt) {
+  // one 128 x 256 tile (four 64-dim boxes) at coordinates (head, row/key 0) into the next slot
+  auto load_tile = [&](const CUtensorMap* map, int head, int r0) -> bool {
     const uint32_t slot = cnt % kSlots;
     if (!mbar_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
     mbar_expect_tx(&sm.full[slot], kTileBytes);
     for (int c = 0; c < 4; ++c)
-      tma_load_3d(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, kvh, kt * kTileN);
+      tma_load_3d(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0);
     ++cnt;
     return true;
   };
@@ -171,21 +173,23 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_k, const CUten
   while (walk.next(a, it)) {
     const int kvh = it.h / kGroup;
     TileCursor<kMode> ck(it), cv(it);
-    // Ring order = MMA order: K0, then (K_j, V_{j-1}) for j >= 1, then V_{n-1}.
-    if (!load_tile(tm_k, kvh, ck.next(0))) return;
+    // Ring order: the item's prepared Q (for the edge warps), then in MMA order K0,
+    // (K_j, V_{j-1}) for j >= 1, V_{n-1}.
+    if (!load_tile(tm_q, it.h, it.mt * kTileM)) return;
+    if (!load_tile(tm_k, kvh, ck.next(0) * kTileN)) return;
     for (int j = 1; j < it.n; ++j) {
-      if (!load_tile(tm_k, kvh, ck.next(j))) return;
-      if (!kW && !load_tile(tm_v, kvh, cv.next(j - 1))) return;
+      if (!load_tile(tm_k, kvh, ck.next(j) * kTileN)) return;
+      if (!kW && !load_tile(tm_v, kvh, cv.next(j - 1) * kTileN)) return;
     }
-    if (!kW && !load_tile(tm_v, kvh, cv.next(it.n - 1))) return;
+    if (!kW && !load_tile(tm_v, kvh, cv.next(it.n - 1) * kTileN)) return;
   }
 }
 
 template <int kMode, bool kW>
-__device__ void producer(AttnSmem& sm, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                         const AttnArgs& a, volatile int* abort) {
+__device__ void producer(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                         const CUtensorMap* tm_v, const AttnArgs& a, volatile int* abort) {
   uint32_t cnt = 0;
-  producer_loop<kMode, kW>(sm, tm_k, tm_v, a, abort, cnt);
+  producer_loop<kMode, kW>(sm, tm_q, tm_k, tm_v, a, abort, cnt);
   if (*abort) {
     // let the loads already issued into the slots land before exit
     const uint32_t first = cnt > (uint32_t)kSlots ? cnt - kSlots : 0;
@@ -233,6 +237,7 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
   ItemWalk<kMode> walk;
   Item it;
   while (walk.next(a, it)) {
+    ++cnt;   // the item's Q tile: consumed by the edge warps
     if (!mbar_wait(&sm.q_full, it_done & 1, abort)) return;
     tc_fence_after();
     for (int j = 0; j < it.n; ++j, ++g) {
@@ -445,23 +450,23 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
       // P = bf16(2^(t - M)), t = bf16(s) * log2(e) / 16, into shared memory once the
       // previous P.V has read the buffer; l sums the rounded P
       if (g > 0 && !warp_wait(&sm.p_empty, (g - 1) & 1, abort)) return;
-      const float2 c2 = make_float2(kLog2eOver16, kLog2eOver16);
-      const float2 nm = make_float2(-mf, -mf);
-      float2 la = make_float2(0.f, 0.f), lb = la;
+      float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
       for (int cd = 0; cd < kTileN / 8; ++cd) {
         uint32_t pk[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float2 t = fma2(bf16x2_to_f32x2(sb[cd * 4 + k]), c2, nm);
-          pk[k] = pack_bf16x2(ex2_approx(t.x), ex2_approx(t.y));
-          if (k & 1) lb = add2(lb, bf16x2_to_f32x2(pk[k]));
-          else la = add2(la, bf16x2_to_f32x2(pk[k]));
+          const uint32_t w = sb[cd * 4 + k];
+          const float t0 = fmaf(lo_f(w), kLog2eOver16, -mf);
+          const float t1 = fmaf(hi_f(w), kLog2eOver16, -mf);
+          pk[k] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
+          if (k & 1) add_bf16x2(l2, l3, pk[k]);
+          else add_bf16x2(l0, l1, pk[k]);
         }
         uint8_t* dst = sm.p[cd >> 3] + sw128_offset((uint32_t)r, (uint32_t)(cd & 7));
         *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      l += (la.x + lb.x) + (la.y + lb.y);
+      l += (l0 + l2) + (l1 + l3);
       fence_async_smem();
       mbar_arrive(&sm.p_full);
     }
@@ -477,239 +482,91 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
 }
 
 // ------------------------------------------------------------------ warps 8-11: edge
-// Query norm, fast path: y = (x r) (1 + w) as fma(x r, w, x r), with r the row's inverse
-// RMS rounded to fp32 (from its double-float value). Three roundings of at most half an
-// ulp each (r, x r, the fma) keep y within 3 ulps of the exact value, so y rounds to the
-// exact bf16 unless its lower 16 bits lie within 3 of 0x8000 (a bf16 midpoint). The
-// test key below is under kNearKey exactly for those values (within 4, to be safe).
-constexpr uint32_t kNearKey = 9u << 16;
-__device__ __forceinline__ uint32_t near_key(float y) {
-  return __float_as_uint(y) * 65536u + 0x80040000u;
-}
-
-// Norm of 8 dims (x: 4 words of bf16 pairs, w: their weights); tmin collects the
-// smallest midpoint key.
-__device__ __forceinline__ void norm8(const uint4& xv, const uint4& wv, float rf, float (&y)[8],
-                                      uint32_t& tmin) {
-  const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-  const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-  const float2 r2 = make_float2(rf, rf);
+// The item's prepared Q tile (a ring slot: four 128-row x 64-dim blocks, 128-byte
+// swizzled) into this thread's TMEM lane at Q: row r, dims 2c and 2c+1 in column c.
+// Every lane of the warp runs it (warp-collective stores).
+__device__ __forceinline__ void q_copy_tmem(const uint8_t* tile, int r, uint32_t q_taddr) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 xr = mul2(bf16x2_to_f32x2(xs[k]), r2);
-    const float2 yy = fma2(xr, bf16x2_to_f32x2(ws[k]), xr);
-    tmin = min(tmin, min(near_key(yy.x), near_key(yy.y)));
-    y[2 * k] = yy.x;
-    y[2 * k + 1] = yy.y;
-  }
-}
-
-// The row's inverse RMS, 1 / sqrt(sum / 256 + 1e-6): f its fp32 value, h + l good to
-// about 2^-46 relative. From rsqrt's estimate r0, one Newton step carried in double-float:
-// with a r0^2 = 1 - e (e about 2^-22, formed exactly up to 2^-46), r = r0 (1 + e/2 + 3e^2/8).
-struct InvRms {
-  float f, h, l;
-};
-__device__ __forceinline__ InvRms inv_rms_df(const SumSq& s) {
-  constexpr float kEpsHi = 1e-6f;
-  constexpr float kEpsLo = 2.5247573e-15f;  // 1e-6 - kEpsHi
-  float ah, al;
-  two_sum(s.hi * (1.0f / 256.0f), kEpsHi, ah, al);
-  al += s.lo * (1.0f / 256.0f) + kEpsLo;
-  const float r0 = rsqrtf(ah);
-  const float sq = r0 * r0;
-  const float sqe = fmaf(r0, r0, -sq);          // r0^2 = sq + sqe exactly
-  const float th = ah * sq;
-  float te = fmaf(ah, sq, -th);                 // ah sq = th + te exactly
-  te = fmaf(ah, sqe, te);
-  te = fmaf(al, sq, te);
-  const float e = (1.0f - th) - te;             // 1 - th is exact (th within 2^-20 of 1)
-  const float c = r0 * fmaf(0.375f * e, e, 0.5f * e);
-  InvRms r;
-  r.h = r0;
-  r.l = c;
-  r.f = r0 + c;
-  return r;
-}
-
-// Pass 1 of the query norm: the row's sum of squares (off the tensor cores' critical
-// path: it needs no tensor memory).
-__device__ SumSq q_sumsq(const AttnArgs& a, int h, int row, bool valid) {
-  SumSq s0, s1;
-  if (valid) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.qg + ((size_t)row * kHeads + h) * kQgStride);
-#pragma unroll 1
-    for (int i0 = 0; i0 < kDim / 8; i0 += 8) {
-      uint4 v[8];
+  for (int grp = 0; grp < 4; ++grp) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __ldg(src + i0 + i);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t ws[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          s0.add(lo_f(ws[k]));
-          s1.add(hi_f(ws[k]));
-        }
-      }
+    for (int j = 0; j < 8; j += 2) {
+      const uint8_t* base = tile + grp * kChunkBytes;
+      const uint4 v0 = *reinterpret_cast<const uint4*>(base + sw128_offset((uint32_t)r, (uint32_t)j));
+      const uint4 v1 = *reinterpret_cast<const uint4*>(base + sw128_offset((uint32_t)r, (uint32_t)j + 1));
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      tmem_st8(q_taddr + 32 * grp + 4 * j, w);
     }
-  }
-  s0.merge(s1);
-  return s0;
-}
-
-__device__ __forceinline__ float bf_at(const uint16_t* p, int i) {
-  return __uint_as_float((uint32_t)p[i] << 16);
-}
-__device__ __forceinline__ void set_half(uint32_t* w, int d, float v) {
-  const uint32_t b = (uint32_t)bf16_bits(v);
-  w[d >> 1] = (d & 1) ? ((w[d >> 1] & 0xFFFFu) | (b << 16)) : ((w[d >> 1] & 0xFFFF0000u) | b);
-}
-
-// Rare path: a lane of this warp has, in group grp (dims 64 grp .. +63) of its row, a fast
-// norm value within the error bound of a bf16 midpoint. Every lane re-derives which of its
-// dims those are and replaces them (and, in the rotated dims, the rotation partners) by
-// exact values, patching its TMEM lane (warp-collective load and store).
-__device__ __noinline__ void q_fixup(const AttnArgs& a, const uint16_t* wq, int h, int row,
-                                     bool valid, int grp, InvRms r, uint32_t taddr) {
-  uint32_t w[32];
-  tmem_wait_st();
-  tmem_ld32(taddr, w);
-  tmem_wait_ld(w);
-  if (valid) {
-    const uint16_t* x = a.qg + ((size_t)row * kHeads + h) * kQgStride;
-    const int pos = a.q_base + row;
-#pragma unroll 1
-    for (int k = 0; k < 64; ++k) {
-      const int d = 64 * grp + k;
-      const float xr = bf_at(x, d) * r.f;
-      if (near_key(fmaf(xr, bf_at(wq, d), xr)) >= kNearKey) continue;
-      if (grp == 0) {
-        const int i = d & 31;
-        const float ya = norm_elem_exact(bf_at(x, i), bf_at(wq, i), r.h, r.l);
-        const float yb = norm_elem_exact(bf_at(x, i + 32), bf_at(wq, i + 32), r.h, r.l);
-        float ra, rb;
-        rope_pair(ya, yb, bf_at(a.cos_tab, pos * kHalfRot + i), bf_at(a.sin_tab, pos * kHalfRot + i),
-                  ra, rb);
-        set_half(w, i, ra);
-        set_half(w, i + 32, rb);
-      } else {
-        set_half(w, k, norm_elem_exact(bf_at(x, d), bf_at(wq, d), r.h, r.l));
-      }
-    }
-  }
-  __syncwarp();
-  tmem_st32(taddr, w);
-  tmem_wait_st();
-}
-
-// Pass 2 of the query norm and the partial RoPE: the row as bf16 pairs into this thread's
-// TMEM lane at Q (column c holds dims 2c and 2c+1); rows past the end store zeros. Every
-// lane of the warp runs it (the stores are warp-collective). The words of dims 0..63 and
-// their cos/sin are loaded by the caller before it waits for Q's columns.
-struct QGroup0 {
-  uint4 xa[4], xb[4], cv[4], sv[4];
-};
-__device__ __forceinline__ void q_load_group0(const AttnArgs& a, int h, int row, bool valid,
-                                              QGroup0& g) {
-  if (!valid) return;
-  const uint4* src = reinterpret_cast<const uint4*>(a.qg + ((size_t)row * kHeads + h) * kQgStride);
-  const int pos = a.q_base + row;
-  const uint4* cp = reinterpret_cast<const uint4*>(a.cos_tab + (size_t)pos * kHalfRot);
-  const uint4* sp = reinterpret_cast<const uint4*>(a.sin_tab + (size_t)pos * kHalfRot);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    g.xa[c] = __ldg(src + c);
-    g.xb[c] = __ldg(src + c + 4);
-    g.cv[c] = __ldg(cp + c);
-    g.sv[c] = __ldg(sp + c);
-  }
-}
-
-__device__ void q_pass2(const AttnSmem& sm, const AttnArgs& a, int h, int row, bool valid,
-                        const QGroup0& g0, InvRms rr, uint32_t q_taddr) {
-  const uint4* src = reinterpret_cast<const uint4*>(a.qg + ((size_t)(valid ? row : 0) * kHeads + h) * kQgStride);
-  const uint16_t* wq16 = reinterpret_cast<const uint16_t*>(sm.w_q);
-  uint4 cur[8];
-  if (valid) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) cur[i] = __ldg(src + 8 + i);   // group 1, in flight meanwhile
-  }
-  {
-    // dims 0..63 with the rotation: dims 8c..8c+7 pair with dims 8c+32..8c+39
-    uint32_t w[32];
-    uint32_t tmin = 0xFFFFFFFFu;
-    if (valid) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float ya[8], yb[8];
-        norm8(g0.xa[c], sm.w_q[c], rr.f, ya, tmin);
-        norm8(g0.xb[c], sm.w_q[c + 4], rr.f, yb, tmin);
-        const uint32_t cw[4] = {g0.cv[c].x, g0.cv[c].y, g0.cv[c].z, g0.cv[c].w};
-        const uint32_t sw[4] = {g0.sv[c].x, g0.sv[c].y, g0.sv[c].z, g0.sv[c].w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float cs = (e & 1) ? hi_f(cw[e >> 1]) : lo_f(cw[e >> 1]);
-          const float sn = (e & 1) ? hi_f(sw[e >> 1]) : lo_f(sw[e >> 1]);
-          float ra, rb;
-          rope_pair(bf16_round(ya[e]), bf16_round(yb[e]), cs, sn, ra, rb);
-          ya[e] = ra;
-          yb[e] = rb;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          w[4 * c + k] = pack_bf16x2(ya[2 * k], ya[2 * k + 1]);
-          w[16 + 4 * c + k] = pack_bf16x2(yb[2 * k], yb[2 * k + 1]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 32; ++k) w[k] = 0u;
-    }
-    tmem_st32(q_taddr, w);
-    if (__any_sync(0xffffffffu, tmin < kNearKey)) q_fixup(a, wq16, h, row, valid, 0, rr, q_taddr);
-  }
-  // dims 64..255 pass through the rotation; the next group's loads are issued first
-#pragma unroll 1
-  for (int grp = 1; grp < 4; ++grp) {
-    uint4 nxt[8];
-    if (valid && grp < 3) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) nxt[i] = __ldg(src + 8 * (grp + 1) + i);
-    }
-    uint32_t w[32];
-    uint32_t tmin = 0xFFFFFFFFu;
-    if (valid) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float y[8];
-        norm8(cur[i], sm.w_q[8 * grp + i], rr.f, y, tmin);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) w[4 * i + k] = pack_bf16x2(y[2 * k], y[2 * k + 1]);
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 32; ++k) w[k] = 0u;
-    }
-    tmem_st32(q_taddr + 32 * grp, w);
-    if (__any_sync(0xffffffffu, tmin < kNearKey))
-      q_fixup(a, wq16, h, row, valid, grp, rr, q_taddr + 32 * grp);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
   }
   tmem_wait_st();
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+// Moves the 32-entry register queue on by 8: entries 8..31 to the front, `in` at the end.
+__device__ __forceinline__ void rotate8(uint4 (&q)[kDim / 8], const uint4 (&in)[8]) {
+#pragma unroll
+  for (int i = 0; i < kDim / 8 - 8; ++i) q[i] = q[i + 8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) q[kDim / 8 - 8 + i] = in[i];
 }
-// The 512 bytes at byte offset `half` (0: q, 512: gate) of this thread's fused row.
-__device__ __forceinline__ void prefetch_row(const AttnArgs& a, const Item& it, int r, int half) {
+
+// Rare path (this lane only): the sigmoids of the 64 gates g[] (8 words of bf16 pairs) that
+// the fast path did not certify, exactly, into the matching halves of sg[].
+__device__ __noinline__ void sigmoid_patch(const uint4* g, uint4* sg) {
+  const uint32_t* gw = reinterpret_cast<const uint32_t*>(g);
+  uint32_t* sw = reinterpret_cast<uint32_t*>(sg);
+#pragma unroll 1
+  for (int k = 0; k < 64; ++k) {
+    const float gk = (k & 1) ? hi_f(gw[k >> 1]) : lo_f(gw[k >> 1]);
+    float y;
+    if (sigmoid_fast(gk, y)) continue;
+    const uint32_t b = (uint32_t)bf16_bits(sigmoid_slow(gk));
+    sw[k >> 1] = (k & 1) ? ((sw[k >> 1] & 0xFFFFu) | (b << 16)) : ((sw[k >> 1] & 0xFFFF0000u) | b);
+  }
+}
+
+// bf16(sigmoid(g)) of this thread's 256 gates, as bf16 pairs in registers (word c holds
+// dims 2c and 2c+1); zeros for rows past the end. The gates are read once and processed
+// 64 at a time through a rotating register queue, so the loop stays short without
+// indexing registers.
+__device__ void gate_sigmoid(const AttnArgs& a, const Item& it, int r, uint4 (&sg)[kDim / 8]) {
   const int row = it.mt * kTileM + r;
-  if (row >= a.rows) return;
-  const uint8_t* p = reinterpret_cast<const uint8_t*>(a.qg + ((size_t)row * kHeads + it.h) * kQgStride) + half;
+  if (row >= a.rows) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) prefetch_l2(p + 128 * i);
+    for (int i = 0; i < kDim / 8; ++i) sg[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const uint4* gp = reinterpret_cast<const uint4*>(a.qg + ((size_t)row * kHeads + it.h) * kQgStride + kDim);
+#pragma unroll
+  for (int i = 0; i < kDim / 8; ++i) sg[i] = __ldg(gp + i);
+#pragma unroll 1
+  for (int step = 0; step < 4; ++step) {
+    uint4 o[8];
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t gw[4] = {sg[i].x, sg[i].y, sg[i].z, sg[i].w};
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float s0, s1;
+        ok &= sigmoid_fast(lo_f(gw[k]), s0);
+        ok &= sigmoid_fast(hi_f(gw[k]), s1);
+        w[k] = pack_bf16x2(s0, s1);
+      }
+      o[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (!ok) {
+      uint4 g[8], t[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        g[i] = sg[i];
+        t[i] = o[i];
+      }
+      sigmoid_patch(g, t);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = t[i];
+    }
+    rotate8(sg, o);
+  }
 }
 
 // Outputs of a work item none of whose key tiles is visible (mask mode): every row is
@@ -726,34 +583,11 @@ __device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r, bool
   if (a.hidden_rows && it.h == 0) atomicAdd(a.hidden_rows, 1);
 }
 
-// One 32-dim batch of the gate with the exact sigmoid wherever the fast one is not
-// certified (rare: a gate whose sigmoid lies near a bf16 midpoint, or a very negative gate).
-// o0..o3 are the batch's bf16 pairs of O / l, g0..g3 its gates; the batch's 4 output
-// words are rewritten.
-__device__ __noinline__ void gate_batch_slow(uint4* op, uint4 o0, uint4 o1, uint4 o2, uint4 o3,
-                                             uint4 g0, uint4 g1, uint4 g2, uint4 g3) {
-  const uint4 ov[4] = {o0, o1, o2, o3};
-  const uint4 gv[4] = {g0, g1, g2, g3};
-#pragma unroll 1
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t gw[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
-    const uint32_t ow[4] = {ov[i].x, ov[i].y, ov[i].z, ov[i].w};
-    uint32_t res[4];
-    for (int k = 0; k < 4; ++k) {
-      float s0, s1;
-      if (!sigmoid_fast(lo_f(gw[k]), s0)) s0 = sigmoid_slow(lo_f(gw[k]));
-      if (!sigmoid_fast(hi_f(gw[k]), s1)) s1 = sigmoid_slow(hi_f(gw[k]));
-      res[k] = pack2(lo_f(ow[k]) * bf16_round(s0), hi_f(ow[k]) * bf16_round(s1));
-    }
-    op[i] = make_uint4(res[0], res[1], res[2], res[3]);
-  }
-}
-
-// Gated epilogue of one finished item: out = bf16(bf16(O / l) * bf16(sigmoid(gate))).
-// O / l is drained to the output row first and O released; then the gate is applied in
-// place (this thread re-reads the words it has just written).
+// Gated epilogue of one finished item: out = bf16(bf16(O / l) * s) with s = bf16(sigmoid(
+// gate)) already in registers; O is read 32 columns at a time and released at the end.
 __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32_t tmem,
-                         uint32_t lane_off, int r, uint32_t it_done, volatile int* abort) {
+                         uint32_t lane_off, int r, uint32_t it_done, uint4 (&sg)[kDim / 8],
+                         volatile int* abort) {
   const int row = it.mt * kTileM + r;
   const bool valid = row < a.rows;
   const int h = it.h;
@@ -765,71 +599,35 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
   const float inv = l > 0.f ? 1.0f / l : 0.f;
   uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)(valid ? row : 0) * kOutRow + h * kDim);
 #pragma unroll 1
-  for (int c = 0; c < kDim / 32; ++c) {
-    uint32_t o[32];
-    tmem_ld32(tmem + kTmemO + lane_off + c * 32, o);
-    tmem_wait_ld(o);
-    uint32_t pk[16];
+  for (int c = 0; c < kDim / 64; ++c) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-      pk[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
-    if (valid) {
+    for (int half = 0; half < 2; ++half) {
+      uint32_t o[32];
+      tmem_ld32(tmem + kTmemO + lane_off + c * 64 + 32 * half, o);
+      tmem_wait_ld(o);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        op[4 * c + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t sw[4] = {sg[4 * half + i].x, sg[4 * half + i].y, sg[4 * half + i].z,
+                                sg[4 * half + i].w};
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t ob = pack_bf16x2(__uint_as_float(o[8 * i + 2 * k]) * inv,
+                                          __uint_as_float(o[8 * i + 2 * k + 1]) * inv);
+          w[k] = pack_bf16x2(lo_f(ob) * lo_f(sw[k]), hi_f(ob) * hi_f(sw[k]));
+        }
+        if (valid) op[8 * c + 4 * half + i] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
+    uint4 none[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) none[i] = make_uint4(0, 0, 0, 0);
+    rotate8(sg, none);
   }
   tc_fence_before();
   mbar_arrive(&sm.o_free);
   mbar_arrive(&sm.st_empty);
   if (!valid) return true;
-  const uint4* gp = reinterpret_cast<const uint4*>(a.qg + ((size_t)row * kHeads + h) * kQgStride + kDim);
-  // 32 dims at a time; the next batch's loads are issued before this one is computed
-  uint4 ov[4], gv[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    ov[i] = op[i];
-    gv[i] = __ldg(gp + i);
-  }
-#pragma unroll 1
-  for (int b = 0; b < 8; ++b) {
-    uint4 on[4], gn[4];
-    if (b < 7) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        on[i] = op[4 * (b + 1) + i];
-        gn[i] = __ldg(gp + 4 * (b + 1) + i);
-      }
-    }
-    bool ok = true;
-    uint4 res[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t gw[4] = {gv[i].x, gv[i].y, gv[i].z, gv[i].w};
-      const uint32_t ow[4] = {ov[i].x, ov[i].y, ov[i].z, ov[i].w};
-      uint32_t rw[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float s0, s1;
-        ok &= sigmoid_fast(lo_f(gw[k]), s0);
-        ok &= sigmoid_fast(hi_f(gw[k]), s1);
-        const float2 prod = mul2(bf16x2_to_f32x2(ow[k]), bf16x2_to_f32x2(pack_bf16x2(s0, s1)));
-        rw[k] = pack_bf16x2(prod.x, prod.y);
-      }
-      res[i] = make_uint4(rw[0], rw[1], rw[2], rw[3]);
-    }
-    if (ok) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) op[4 * b + i] = res[i];
-    } else {
-      gate_batch_slow(op + 4 * b, ov[0], ov[1], ov[2], ov[3], gv[0], gv[1], gv[2], gv[3]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      ov[i] = on[i];
-      gv[i] = gn[i];
-    }
-  }
   if (a.row_stats) {
     a.row_stats[((size_t)h * a.rows + row) * 2] = M;
     a.row_stats[((size_t)h * a.rows + row) * 2 + 1] = l;
@@ -860,37 +658,42 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
       write_hidden_rows(a, out, r, kW);
     }
   };
-  // Item i+1's Q goes into TMEM as soon as item i's last S = Q K^T has read Q (its sum
-  // of squares and first loads are done before that); then item i's epilogue runs once
-  // its last P V is done.
-  Item cur, nxt;
-  if (!next_item(cur)) return;
-  QGroup0 g0;
-  {
-    const int row = cur.mt * kTileM + r;
-    const bool valid = row < a.rows;
-    const InvRms rr = inv_rms_df(q_sumsq(a, cur.h, row, valid));
-    q_load_group0(a, cur.h, row, valid, g0);
-    q_pass2(sm, a, cur.h, row, valid, g0, rr, q_taddr);
+  // Ring position of each item's Q tile: the producer loads Q, then the item's K and V tiles.
+  // The slot is handed back once all 128 edge threads have read it (bounded waits only).
+  // q_empty(i) comes first: it means the tensor cores have used item i's last K tile, the
+  // slot's previous fill, so the slot's full barrier is at most one phase behind the
+  // awaited one (a parity wait cannot tell a phase from the one two before it).
+  uint32_t q_pos = 0, q_takes = 0;
+  auto take_q = [&](const Item& it, bool wait_empty, uint32_t it_done) -> bool {
+    const uint32_t slot = q_pos % kSlots;
+    if (wait_empty && !warp_wait(&sm.q_empty, it_done & 1, abort)) return false;
+    if (!warp_wait(&sm.full[slot], (q_pos / kSlots) & 1, abort)) return false;
+    tc_fence_after();
+    q_copy_tmem(sm.tile[slot], r, q_taddr);
     tc_fence_before();
     mbar_arrive(&sm.q_full);
-  }
+    mbar_arrive(&sm.q_read);
+    if (threadIdx.x == 256) {
+      if (!mbar_wait(&sm.q_read, q_takes & 1, abort)) return false;
+      mbar_arrive(&sm.empty[slot]);
+    }
+    ++q_takes;
+    q_pos += 1 + (kW ? 1 : 2) * it.n;
+    return true;
+  };
+  // Item i+1's Q goes into TMEM as soon as item i's last S = Q K^T has read Q; item i's
+  // gate sigmoids are computed while its tiles run, and its epilogue once its last P V
+  // is done.
+  Item cur, nxt;
+  if (!next_item(cur)) return;
+  if (!take_q(cur, false, 0)) return;
+  uint4 sg[kDim / 8];
   uint32_t it_done = 0;
   while (true) {
+    if (!kW) gate_sigmoid(a, cur, r, sg);
     const bool have_next = next_item(nxt);
-    if (!kW) prefetch_row(a, cur, r, 512);   // the current item's gates
-    if (have_next) {
-      const int row = nxt.mt * kTileM + r;
-      const bool valid = row < a.rows;
-      const InvRms rr = inv_rms_df(q_sumsq(a, nxt.h, row, valid));
-      q_load_group0(a, nxt.h, row, valid, g0);
-      if (!warp_wait(&sm.q_empty, it_done & 1, abort)) return;
-      tc_fence_after();
-      q_pass2(sm, a, nxt.h, row, valid, g0, rr, q_taddr);
-      tc_fence_before();
-      mbar_arrive(&sm.q_full);
-    }
-    if (!kW && !epilogue(sm, a, cur, tmem, lane_off, r, it_done, abort)) return;
+    if (have_next && !take_q(nxt, true, it_done)) return;
+    if (!kW && !epilogue(sm, a, cur, tmem, lane_off, r, it_done, sg, abort)) return;
     ++it_done;
     if (!have_next) break;
     cur = nxt;
@@ -899,8 +702,8 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
 
 template <int kMode, bool kW>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                const __grid_constant__ AttnArgs a) {
+    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -924,9 +727,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.st_full, 128);
     mbar_init(&sm.st_empty, 128);
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.q_read, 128);
     mbar_fence_init();
   }
   if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
@@ -942,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
-    if (warp == 0 && lane == 0) producer<kMode, kW>(sm, &tm_k, &tm_v, a, abort);
+    if (warp == 0 && lane == 0) producer<kMode, kW>(sm, &tm_q, &tm_k, &tm_v, a, abort);
     if (warp == 1 && lane == 0) mma_issuer<kMode, kW>(sm, a, tmem, abort);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
@@ -979,18 +784,18 @@ cudaError_t attn_set_smem_attribute() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-cudaError_t launch_attn(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
-                        int grid, cudaStream_t s) {
+cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                        const AttnArgs& a, int grid, cudaStream_t s) {
   const size_t smem = attn_smem_bytes();
   if (a.weights_pass) {
     if (a.mode != kModeMask) return cudaErrorInvalidValue;
-    attn_kernel<kModeMask, true><<<grid, kThreads, smem, s>>>(tm_k, tm_v, a);
+    attn_kernel<kModeMask, true><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
   } else if (a.mode == kModeCausal) {
-    attn_kernel<kModeCausal, false><<<grid, kThreads, smem, s>>>(tm_k, tm_v, a);
+    attn_kernel<kModeCausal, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
   } else if (a.mode == kModeBidir) {
-    attn_kernel<kModeBidir, false><<<grid, kThreads, smem, s>>>(tm_k, tm_v, a);
+    attn_kernel<kModeBidir, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
   } else {
-    attn_kernel<kModeMask, false><<<grid, kThreads, smem, s>>>(tm_k, tm_v, a);
+    attn_kernel<kModeMask, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
   }
   return cudaGetLastError();
 }

@@ -115,6 +115,27 @@ int encode_kv_map(CUtensorMap* map, const void* base, long long n_tok, long long
   return GA_OK;
 }
 
+// [rows][24][256] bf16 prepared queries as a TMA tensor: box = 64 dims x 1 head x 128 rows,
+// 128-byte swizzle; rows past the end read as zeros.
+int encode_q_map(CUtensorMap* map, const void* base, long long rows) {
+  EncodeTiledFn enc;
+  int st = get_encode(&enc);
+  if (st != GA_OK) return st;
+  cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)kHeads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)kOutRow * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kTileM};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = GA_CUDA(enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = (int)r;
+    return GA_ERR_CUDA;
+  }
+  return GA_OK;
+}
+
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // bf16 (nearest, ties to even) of a double.
@@ -146,7 +167,7 @@ int check_attention_args(const void* qg, const void* k_prep, const void* v, cons
 }
 
 struct MaskedLayout {
-  size_t bits_off, flags_off, stats_off, total;
+  size_t bits_off, flags_off, stats_off, q_off, total;
   int row_tiles, key_tiles, mask_words;
 };
 MaskedLayout masked_layout(int rows, int T) {
@@ -158,14 +179,20 @@ MaskedLayout masked_layout(int rows, int T) {
   L.bits_off = 0;
   L.flags_off = up(L.bits_off + (size_t)L.row_tiles * kTileM * L.mask_words * 4);
   L.stats_off = up(L.flags_off + (size_t)L.row_tiles * L.key_tiles);
-  L.total = up(L.stats_off + (size_t)kHeads * rows * 2 * sizeof(float));
+  L.q_off = up(L.stats_off + (size_t)kHeads * rows * 2 * sizeof(float));
+  L.total = up(L.q_off + (size_t)rows * kOutRow * sizeof(uint16_t));
   return L;
 }
 
-int launch_attention(const AttnArgs& a0, const void* k_prep, const void* v, long long n_tok,
-                     DeviceState* dev, cudaStream_t s) {
-  CUtensorMap tm_k, tm_v;
-  int st = encode_kv_map(&tm_k, k_prep, n_tok, 1);
+// The query prologue (unless q_ready: q_prep already holds this call's prepared queries)
+// and the attention kernel. q_prep [rows][24][256] may be the output buffer itself: each
+// (row, head) slot is read by the work item that later writes its output there.
+int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const void* k_prep,
+                     const void* v, long long n_tok, DeviceState* dev, cudaStream_t s) {
+  CUtensorMap tm_q, tm_k, tm_v;
+  int st = encode_q_map(&tm_q, q_prep, a0.rows);
+  if (st != GA_OK) return st;
+  st = encode_kv_map(&tm_k, k_prep, n_tok, 1);
   if (st != GA_OK) return st;
   st = encode_kv_map(&tm_v, v, n_tok, 1);
   if (st != GA_OK) return st;
@@ -173,8 +200,13 @@ int launch_attention(const AttnArgs& a0, const void* k_prep, const void* v, long
   a.status = dev->status_word;
   a.row_tiles = (a.rows + kTileM - 1) / kTileM;
   a.n_items = a.row_tiles * kHeads;
+  cudaError_t e;
+  if (!q_ready &&
+      (e = GA_CUDA(launch_q_prologue(a.qg, a.w_q, a.cos_tab, a.sin_tab, a.rows, a.q_base, q_prep,
+                                     s))) != cudaSuccess)
+    return fail_cuda(e);
   const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
-  cudaError_t e = GA_CUDA(launch_attn(tm_k, tm_v, a, grid, s));
+  e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, a, grid, s));
   if (e != cudaSuccess) return fail_cuda(e);
   return GA_OK;
 }
@@ -284,7 +316,7 @@ int ga_attn_prefill(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
   a.out = out; a.row_stats = row_stats;
   a.rows = rows; a.T = T; a.q_base = q_base;
   a.mode = causal ? kModeCausal : kModeBidir;
-  return launch_attention(a, k_prep, v, T, dev, (cudaStream_t)stream);
+  return launch_attention(a, out, false, k_prep, v, T, dev, (cudaStream_t)stream);
 }
 
 size_t ga_masked_workspace_bytes(int rows, int T) {
@@ -316,6 +348,7 @@ int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws + L.bits_off);
   uint8_t* flags = ws + L.flags_off;
   float* stats = reinterpret_cast<float*>(ws + L.stats_off);
+  uint16_t* q_prep = reinterpret_cast<uint16_t*>(ws + L.q_off);
   cudaError_t e;
   if (hidden_rows && (e = GA_CUDA(cudaMemsetAsync(hidden_rows, 0, sizeof(int), s))) != cudaSuccess)
     return fail_cuda(e);
@@ -328,14 +361,14 @@ int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
   a.mask_bits = bits; a.tile_flags = flags;
   a.key_tiles = L.key_tiles; a.mask_words = L.mask_words;
   a.rows = rows; a.T = T; a.q_base = q_base; a.mode = kModeMask;
-  st = launch_attention(a, k_prep, v, T, dev, s);
+  st = launch_attention(a, q_prep, false, k_prep, v, T, dev, s);
   if (st != GA_OK || !weights) return st;
   if ((e = GA_CUDA(cudaMemsetAsync(weights, 0, (size_t)kHeads * rows * T * sizeof(uint16_t), s))) != cudaSuccess)
     return fail_cuda(e);
   a.weights = weights;
   a.weights_pass = 1;
   a.hidden_rows = nullptr;
-  return launch_attention(a, k_prep, v, T, dev, s);
+  return launch_attention(a, q_prep, true, k_prep, v, T, dev, s);
 }
 
 size_t ga_verify_workspace_bytes(int n_seq, int rows, int max_len) {
@@ -374,8 +407,8 @@ int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_c
     a.w_q = w_q; a.cos_tab = cos_tab; a.sin_tab = sin_tab;
     a.out = out + (size_t)b * rows * kOutRow;
     a.rows = rows; a.T = seq_len[b] + rows; a.q_base = seq_len[b]; a.mode = kModeCausal;
-    st = launch_attention(a, k_cache + b * seq_elems, v_cache + b * seq_elems, a.T, dev,
-                          (cudaStream_t)stream);
+    st = launch_attention(a, a.out, false, k_cache + b * seq_elems, v_cache + b * seq_elems, a.T,
+                          dev, (cudaStream_t)stream);
     if (st != GA_OK) return st;
   }
   return GA_OK;

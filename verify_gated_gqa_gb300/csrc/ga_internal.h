@@ -52,10 +52,15 @@ struct AttnArgs {
 cudaError_t launch_k_prologue(const uint16_t* k_raw, const uint16_t* w_k, const uint16_t* cos_tab,
                               const uint16_t* sin_tab, int n_tok, int pos_base, uint16_t* k_prep,
                               int* status, cudaStream_t s);
+// Prepared query rows: q_prep[r][h][0..255] = rope(norm(qg[r][h][0..255])) at q_base + r.
+cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
+                              const uint16_t* sin_tab, int rows, int q_base, uint16_t* q_prep,
+                              cudaStream_t s);
 cudaError_t attn_set_smem_attribute();
 size_t attn_smem_bytes();
-cudaError_t launch_attn(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const AttnArgs& a,
-                        int grid, cudaStream_t s);
+// tm_q: the prepared queries [rows][24][256] (box 64 dims x 1 head x 128 rows).
+cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                        const AttnArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_mask_prepass(const uint8_t* mask, long long ld_mask, int rows, int T,
                                 uint32_t* bits, int mask_words, uint8_t* flags, int key_tiles,
                                 cudaStream_t s);

@@ -1,9 +1,12 @@
-// K prologue: (1+w) RMSNorm and partial RoPE of every key head, once per key
-// (pegainfer PR #1151, "feat(qwen4): add the QSA sparse-attention kernel and its golden",
-// §What changed: all twelve query heads of a KV head read the same prepared key).
+// Prologue: (1+w) RMSNorm and partial RoPE of head rows, once per row (pegainfer PR
+// #1151, "feat(qwen4): add the QSA sparse-attention kernel and its golden", §What changed:
+// all twelve query heads of a KV head read the same prepared key; the query rows take
+// the same norm with w_q at their own positions).
 //
-// One warp per (token, KV head) row of 256 bf16: lane l holds dims 8l .. 8l+7 (one
-// 16-byte load and store). Memory-bound: 1 KiB in and out per token.
+// One warp per (token, head) row of 256 bf16: lane l holds dims 8l .. 8l+7 (one 16-byte
+// load and store, so a warp reads and writes 512 contiguous bytes). Memory-bound. Keys:
+// [T][2][256] -> [T][2][256]. Queries: the q halves of the fused rows [rows][24][512] ->
+// [rows][24][256].
 #include "ga_internal.h"
 #include "ga_numerics.cuh"
 #include "ga_sm100.cuh"
@@ -17,20 +20,23 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return (uint32_t)bf16_bits(a) | ((uint32_t)bf16_bits(b) << 16);
 }
 
-__global__ void __launch_bounds__(256) k_prologue_kernel(const uint16_t* __restrict__ k_raw,
-                                                         const uint16_t* __restrict__ w_k,
-                                                         const uint16_t* __restrict__ cos_tab,
-                                                         const uint16_t* __restrict__ sin_tab,
-                                                         int n_rows, int pos_base,
-                                                         uint16_t* __restrict__ k_prep) {
+// rows are (token, head) pairs, heads_per_tok heads per token; row `row` reads 256 values
+// at src + row * src_stride and writes 256 at dst + row * 256.
+__global__ void __launch_bounds__(256) prologue_kernel(const uint16_t* __restrict__ src,
+                                                       int src_stride, int heads_per_tok,
+                                                       const uint16_t* __restrict__ w_norm,
+                                                       const uint16_t* __restrict__ cos_tab,
+                                                       const uint16_t* __restrict__ sin_tab,
+                                                       long long n_rows, int pos_base,
+                                                       uint16_t* __restrict__ dst) {
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= n_rows) return;
-  const long long tok = row >> 1;  // rows are (token, KV head) pairs
+  const long long tok = row / heads_per_tok;
   const int pos = pos_base + (int)tok;
 
-  const uint4 xv = __ldg(reinterpret_cast<const uint4*>(k_raw + row * kDim) + lane);
-  const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_k) + lane);
+  const uint4 xv = __ldg(reinterpret_cast<const uint4*>(src + row * src_stride) + lane);
+  const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_norm) + lane);
   const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
   const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
   float x[8], w[8];
@@ -92,7 +98,7 @@ __global__ void __launch_bounds__(256) k_prologue_kernel(const uint16_t* __restr
   o.y = pack2(y[2], y[3]);
   o.z = pack2(y[4], y[5]);
   o.w = pack2(y[6], y[7]);
-  reinterpret_cast<uint4*>(k_prep + row * kDim)[lane] = o;
+  reinterpret_cast<uint4*>(dst + row * kDim)[lane] = o;
 }
 
 }  // namespace
@@ -103,8 +109,18 @@ cudaError_t launch_k_prologue(const uint16_t* k_raw, const uint16_t* w_k, const 
   (void)status;
   const long long n_rows = (long long)n_tok * kKvHeads;
   const unsigned grid = (unsigned)((n_rows + 7) / 8);
-  k_prologue_kernel<<<grid, 256, 0, s>>>(k_raw, w_k, cos_tab, sin_tab, (int)n_rows, pos_base,
-                                          k_prep);
+  prologue_kernel<<<grid, 256, 0, s>>>(k_raw, kDim, kKvHeads, w_k, cos_tab, sin_tab, n_rows,
+                                       pos_base, k_prep);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
+                              const uint16_t* sin_tab, int rows, int q_base, uint16_t* q_prep,
+                              cudaStream_t s) {
+  const long long n_rows = (long long)rows * kHeads;
+  const unsigned grid = (unsigned)((n_rows + 7) / 8);
+  prologue_kernel<<<grid, 256, 0, s>>>(qg, kQgStride, kHeads, w_q, cos_tab, sin_tab, n_rows,
+                                       q_base, q_prep);
   return cudaGetLastError();
 }
 
