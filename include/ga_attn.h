@@ -123,6 +123,20 @@ int ga_k_prologue(const ga_bf16* k_raw, const ga_bf16* w_k, const ga_bf16* cos_t
                   const ga_bf16* sin_tab, int table_rows, int n_tok, int pos_base,
                   ga_bf16* k_prep, ga_stream stream);
 
+/* Query prologue: the same (1+w) RMSNorm and partial RoPE for the q half of every fused
+ * row and head (pegainfer PR #1151, §Semantics: q is split from the fused q|gate row,
+ * normed and rotated at its own position). ga_attn_prefill runs it itself; it is exposed
+ * so that a caller can time or reuse the prepared queries (ga_attn_prefill_prepared).
+ *   qg      [rows][24][512]  fused rows of positions q_base .. q_base+rows-1
+ *   w_q     [256]            query norm weight w (applied as 1 + w)
+ *   cos_tab, sin_tab [table_rows][32]; table_rows >= q_base + rows
+ *   q_prep  [rows][24][256]  output: bf16(rope(norm(q))); may not overlap qg
+ * Errors: NULL, SHAPE (rows < 0), RANGE (q_base < 0 or rows > GA_MAX_TOKENS), TABLE,
+ * ALIGN (qg, w_q, cos_tab, sin_tab, q_prep), DEVICE, CUDA. */
+int ga_q_prologue(const ga_bf16* qg, const ga_bf16* w_q, const ga_bf16* cos_tab,
+                  const ga_bf16* sin_tab, int table_rows, int rows, int q_base,
+                  ga_bf16* q_prep, ga_stream stream);
+
 /* Causal / prefix-window / bidirectional gated GQA attention (system1-omni PR #202,
  * §Scope: full pass, causal or bidirectional, and causal prefix windows at q_base).
  *   qg      [rows][24][512]  fused rows of query positions q_base .. q_base+rows-1; per
@@ -148,6 +162,16 @@ int ga_attn_prefill(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
                     const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
                     int table_rows, int rows, int T, int q_base, int causal, ga_bf16* out,
                     float* row_stats, ga_stream stream);
+
+/* ga_attn_prefill from prepared queries (ga_q_prologue's output): the attention kernel
+ * alone. qg still supplies the gates (its last 256 values per head).
+ *   q_prep  [rows][24][256]  prepared queries; may be the same buffer as out (each
+ *                            (row, head) slot is read before its output is written there)
+ *   qg, k_prep, v, rows, T, q_base, causal, out, row_stats: as in ga_attn_prefill
+ * Errors: NULL, SHAPE, RANGE, ALIGN (q_prep, qg, k_prep, v, out, row_stats), DEVICE, CUDA. */
+int ga_attn_prefill_prepared(const ga_bf16* q_prep, const ga_bf16* qg, const ga_bf16* k_prep,
+                             const ga_bf16* v, int rows, int T, int q_base, int causal,
+                             ga_bf16* out, float* row_stats, ga_stream stream);
 
 /* Bytes of workspace ga_attn_masked needs for (rows, T); 0 for invalid sizes. */
 size_t ga_masked_workspace_bytes(int rows, int T);

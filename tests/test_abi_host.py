@@ -157,17 +157,40 @@ def test_k_prologue_refusals(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def test_q_prologue_and_prepared_refusals(L):
+    before = L.ga_debug_cuda_calls()
+    assert L.ga_q_prologue(None, A, A, A, 100, 10, 0, A, S) == -1
+    assert L.ga_q_prologue(A, A, A, A, 100, -1, 0, A, S) == -2
+    assert L.ga_q_prologue(A, A, A, A, 100, 10, -1, A, S) == -4
+    assert L.ga_q_prologue(A, A, A, A, 100, 10, 95, A, S) == -5
+    assert L.ga_q_prologue(A, A, A, A, 100, 10, 0, MIS, S) == -3
+    P = L.ga_attn_prefill_prepared
+    assert P(None, A, A, A, 10, 100, 0, 1, A, None, S) == -1
+    assert P(A, A, A, A, -1, 100, 0, 1, A, None, S) == -2
+    assert P(A, A, A, A, 10, 100, 32, 1, A, None, S) == -4      # q_base not a multiple of 64
+    assert P(A, A, A, A, 10, 100, 64, 0, A, None, S) == -4      # bidirectional window
+    assert P(A, A, A, A, 200, 100, 0, 1, A, None, S) == -4      # rows beyond T
+    assert P(A, A, A, A, 10, 100, 0, 2, A, None, S) == -4
+    assert P(MIS, A, A, A, 10, 100, 0, 1, A, None, S) == -3
+    assert P(A, A, A, A, 10, 100, 0, 1, A, MIS + 1, S) == -3
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_empty_calls_are_noops_without_cuda(L):
     before = L.ga_debug_cuda_calls()
     assert _prefill(L, rows=0) == 0
     assert _masked(L, rows=0, wsb=L.ga_masked_workspace_bytes(0, 1024)) == 0
     assert _verify(L, rows=0, wsb=256) == 0
     assert L.ga_k_prologue(A, A, A, A, 100, 0, 0, A, S) == 0
+    assert L.ga_q_prologue(A, A, A, A, 100, 0, 0, A, S) == 0
+    assert L.ga_attn_prefill_prepared(A, A, A, A, 0, 100, 0, 1, A, None, S) == 0
     assert L.ga_debug_cuda_calls() == before
 
 
 def test_workspace_sizes(L):
-    assert L.ga_masked_workspace_bytes(8192, 8192) >= 8192 * 256 * 4 + 64 * 64 + 24 * 8192 * 8
+    # bit mask, tile flags, row statistics and the prepared queries
+    assert L.ga_masked_workspace_bytes(8192, 8192) >= (8192 * 256 * 4 + 64 * 64 + 24 * 8192 * 8
+                                                       + 8192 * 6144 * 2)
     assert L.ga_masked_workspace_bytes(1, 8193) == 0
     assert L.ga_masked_workspace_bytes(-1, 10) == 0
     assert L.ga_verify_workspace_bytes(0, 16, 10) == 0

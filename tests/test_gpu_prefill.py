@@ -42,6 +42,34 @@ def test_k_prologue_bit_exact(T, pos_base):
     assert np.array_equal(g, want), f"{int((g != want).sum())} of {g.size} differ"
 
 
+# ------------------------------------------------------------------ Q prologue
+@pytest.mark.parametrize("rows,q_base", [(333, 0), (200, 704)])
+def test_q_prologue_bit_exact(rows, q_base):
+    inp = Inputs(SEED + 9, rows, q_base + rows)
+    d = inp.dev()
+    got = B.ga_q_prologue(d["qg"], d["w_q"], d["cos"], d["sin"], q_base=q_base)
+    c, s = inp.oracle_tables()
+    want, _ = O.prep_queries(inp.np["qg"], inp.np["w_q"], c, s, q_base)
+    g = np64(got)
+    assert np.array_equal(g, want), f"{int((g != want).sum())} of {g.size} differ"
+
+
+def test_prepared_path_matches_fused_call():
+    """ga_q_prologue + ga_attn_prefill_prepared equals ga_attn_prefill bit for bit, with the
+    prepared queries in their own buffer and in the output buffer itself."""
+    S = 1000
+    inp = Inputs(SEED + 10, S, S)
+    d = inp.dev()
+    full = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, S)
+    qp = B.ga_q_prologue(d["qg"], d["w_q"], d["cos"], d["sin"])
+    sep = B.ga_attn_prefill_prepared(qp, d["qg"], d["k_prep"], d["v"])
+    assert torch.equal(sep, full)
+    out = torch.empty_like(full)
+    B.ga_q_prologue(d["qg"], d["w_q"], d["cos"], d["sin"], q_prep=out.view(S, 24, 256))
+    B.ga_attn_prefill_prepared(out, d["qg"], d["k_prep"], d["v"], out=out)
+    assert torch.equal(out, full)
+
+
 # ------------------------------------------------------------------ tiny and S=2048
 def test_prefill_tiny_s64_all_heads():
     inp = Inputs(SEED + 1, 64, 64)

@@ -38,7 +38,9 @@ _SIGS = {
     "ga_device_status": (_I, [_P, _I]),
     "ga_rope_table_host": (_I, [_I, _P, _P]),
     "ga_k_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "ga_q_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "ga_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "ga_attn_prefill_prepared": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "ga_masked_workspace_bytes": (_SZ, [_I, _I]),
     "ga_attn_masked": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _LL, _P, _P, _P, _P,
                             _SZ, _P]),
@@ -146,6 +148,35 @@ def ga_k_prologue(k_raw, w_k, cos_tab, sin_tab, pos_base=0, k_prep=None):
                                cos_tab.shape[0], n_tok, pos_base, _ptr(k_prep), _stream()),
            "ga_k_prologue")
     return k_prep
+
+
+def ga_q_prologue(qg, w_q, cos_tab, sin_tab, q_base=0, q_prep=None):
+    """Prepared queries [rows, 24, 256] (bf16(rope(norm(q)))) of the fused rows qg."""
+    _bf16_cuda("qg", qg)
+    rows = qg.shape[0]
+    if q_prep is None:
+        q_prep = torch.empty(rows, N_Q_HEADS, HEAD_DIM, dtype=torch.bfloat16, device=qg.device)
+    for n, t in (("w_q", w_q), ("cos_tab", cos_tab), ("sin_tab", sin_tab), ("q_prep", q_prep)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_q_prologue(_ptr(qg), _ptr(w_q), _ptr(cos_tab), _ptr(sin_tab),
+                               cos_tab.shape[0], rows, q_base, _ptr(q_prep), _stream()),
+           "ga_q_prologue")
+    return q_prep
+
+
+def ga_attn_prefill_prepared(q_prep, qg, k_prep, v, q_base=0, T=None, causal=True, out=None,
+                             row_stats=None):
+    rows = qg.shape[0]
+    T = k_prep.shape[0] if T is None else T
+    if out is None:
+        out = torch.empty(rows, N_Q_HEADS * HEAD_DIM, dtype=torch.bfloat16, device=qg.device)
+    for n, t in (("q_prep", q_prep), ("qg", qg), ("k_prep", k_prep), ("v", v), ("out", out)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_attn_prefill_prepared(_ptr(q_prep), _ptr(qg), _ptr(k_prep), _ptr(v), rows, T,
+                                          q_base, 1 if causal else 0, _ptr(out), _ptr(row_stats),
+                                          _stream()),
+           "ga_attn_prefill_prepared")
+    return out
 
 
 def ga_attn_prefill(qg, k_prep, v, w_q, cos_tab, sin_tab, q_base=0, T=None, causal=True,

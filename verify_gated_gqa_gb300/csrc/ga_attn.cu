@@ -72,7 +72,6 @@ struct AttnSmem {
   uint8_t p[2][kChunkBytes];          // P: 128 rows x 128 keys, two swizzled 64-key columns
   float stat_l[kTileM];               // softmax -> edge: the row sum l of the finished item
   float stat_m[kTileM];               // and its running maximum M
-  uint4 w_q[kDim / 8];                // the query norm weight, staged once
   uint64_t full[kSlots], empty[kSlots];
   uint64_t q_full, q_empty, s_full, s_free, p_full, p_empty;
   uint64_t o_ready, o_done, o_free, st_full, st_empty, drain, q_read;
@@ -735,7 +734,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  if (threadIdx.x < kDim / 8) sm.w_q[threadIdx.x] = __ldg(reinterpret_cast<const uint4*>(a.w_q) + threadIdx.x);
   if (warp == 1) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();

@@ -297,6 +297,50 @@ int ga_k_prologue(const ga_bf16* k_raw, const ga_bf16* w_k, const ga_bf16* cos_t
   return e == cudaSuccess ? GA_OK : fail_cuda(e);
 }
 
+int ga_q_prologue(const ga_bf16* qg, const ga_bf16* w_q, const ga_bf16* cos_tab,
+                  const ga_bf16* sin_tab, int table_rows, int rows, int q_base,
+                  ga_bf16* q_prep, ga_stream stream) {
+  if (!qg || !w_q || !cos_tab || !sin_tab || !q_prep) return GA_ERR_NULL;
+  if (rows < 0 || table_rows < 0) return GA_ERR_SHAPE;
+  if (q_base < 0 || rows > GA_MAX_TOKENS || q_base > GA_MAX_TOKENS) return GA_ERR_RANGE;
+  if ((long long)table_rows < (long long)q_base + rows) return GA_ERR_TABLE;
+  if (!aligned(qg, 16) || !aligned(q_prep, 16) || !aligned(w_q, 16) || !aligned(cos_tab, 16) ||
+      !aligned(sin_tab, 16))
+    return GA_ERR_ALIGN;
+  if (rows == 0) return GA_OK;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaError_t e = GA_CUDA(launch_q_prologue(qg, w_q, cos_tab, sin_tab, rows, q_base, q_prep,
+                                            (cudaStream_t)stream));
+  return e == cudaSuccess ? GA_OK : fail_cuda(e);
+}
+
+int ga_attn_prefill_prepared(const ga_bf16* q_prep, const ga_bf16* qg, const ga_bf16* k_prep,
+                             const ga_bf16* v, int rows, int T, int q_base, int causal,
+                             ga_bf16* out, float* row_stats, ga_stream stream) {
+  if (!q_prep || !qg || !k_prep || !v || !out) return GA_ERR_NULL;
+  if (rows < 0 || T < 1) return GA_ERR_SHAPE;
+  if (T > GA_MAX_TOKENS || q_base < 0 || q_base % 64 != 0 || (long long)q_base + rows > T)
+    return GA_ERR_RANGE;
+  if (causal != 0 && causal != 1) return GA_ERR_RANGE;
+  if (!causal && q_base != 0) return GA_ERR_RANGE;
+  if (!aligned(q_prep, 16) || !aligned(qg, 16) || !aligned(k_prep, 16) || !aligned(v, 16) ||
+      !aligned(out, 16) || (row_stats && !aligned(row_stats, 4)))
+    return GA_ERR_ALIGN;
+  if (rows == 0) return GA_OK;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  AttnArgs a{};
+  a.qg = qg;
+  a.out = out; a.row_stats = row_stats;
+  a.rows = rows; a.T = T; a.q_base = q_base;
+  a.mode = causal ? kModeCausal : kModeBidir;
+  return launch_attention(a, const_cast<uint16_t*>(q_prep), true, k_prep, v, T, dev,
+                          (cudaStream_t)stream);
+}
+
 int ga_attn_prefill(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
                     const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
                     int table_rows, int rows, int T, int q_base, int causal, ga_bf16* out,
