@@ -507,17 +507,21 @@ __device__ __forceinline__ void rotate8(uint4 (&q)[kDim / 8], const uint4 (&in)[
   for (int i = 0; i < 8; ++i) q[kDim / 8 - 8 + i] = in[i];
 }
 
+// bf16(sigmoid(g)) for every bf16 g (index: g's bits), exact from the double definition;
+// filled once per device from the host. The gate's rare exact path reads it.
+__device__ uint16_t g_sigmoid_bf16[1 << 16];
+
 // Rare path (this lane only): the sigmoids of the 64 gates g[] (8 words of bf16 pairs) that
-// the fast path did not certify, exactly, into the matching halves of sg[].
+// the fast path did not certify, from the exact table, into the matching halves of sg[].
 __device__ __noinline__ void sigmoid_patch(const uint4* g, uint4* sg) {
   const uint32_t* gw = reinterpret_cast<const uint32_t*>(g);
   uint32_t* sw = reinterpret_cast<uint32_t*>(sg);
 #pragma unroll 1
   for (int k = 0; k < 64; ++k) {
-    const float gk = (k & 1) ? hi_f(gw[k >> 1]) : lo_f(gw[k >> 1]);
+    const uint32_t gb = (k & 1) ? (gw[k >> 1] >> 16) : (gw[k >> 1] & 0xFFFFu);
     float y;
-    if (sigmoid_fast(gk, y)) continue;
-    const uint32_t b = (uint32_t)bf16_bits(sigmoid_slow(gk));
+    if (sigmoid_fast(__uint_as_float(gb << 16), y)) continue;
+    const uint32_t b = g_sigmoid_bf16[gb];
     sw[k >> 1] = (k & 1) ? ((sw[k >> 1] & 0xFFFFu) | (b << 16)) : ((sw[k >> 1] & 0xFFFF0000u) | b);
   }
 }
@@ -765,6 +769,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 size_t attn_smem_bytes() { return sizeof(AttnSmem) + 1024; }
+
+cudaError_t attn_upload_sigmoid_table(const uint16_t* host_table) {
+  return cudaMemcpyToSymbol(g_sigmoid_bf16, host_table, sizeof(g_sigmoid_bf16));
+}
 
 cudaError_t attn_set_smem_attribute() {
   const int bytes = (int)attn_smem_bytes();

@@ -38,7 +38,31 @@ int fail_cuda(cudaError_t e) {
   return GA_ERR_CUDA;
 }
 
-// Capability check, shared-memory opt-in and status-word address, once per device
+uint16_t bf16_rne(double x);
+
+// bf16(1 / (1 + e^-g)) for every bf16 g, indexed by g's bits, from the definition in double
+// (pegainfer PR #1151, §Semantics: the gate's sigmoid is rounded to bf16 before the final
+// product). NaN gates give a quiet NaN.
+const uint16_t* sigmoid_table() {
+  static uint16_t table[1 << 16];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    for (uint32_t b = 0; b < (1u << 16); ++b) {
+      const uint32_t bits = b << 16;
+      float g;
+      std::memcpy(&g, &bits, 4);
+      if (std::isnan(g)) {
+        table[b] = 0x7FC0u;
+        continue;
+      }
+      table[b] = bf16_rne(1.0 / (1.0 + std::exp(-(double)g)));
+    }
+  });
+  return table;
+}
+
+// Capability check, shared-memory opt-in, sigmoid table and status-word address, once
+// per device
 // (system1-omni PR #202, "cuda: widen the attention query tile on sm_89 and sm_120",
 // second review and the author's fix: the decision and the opt-in are kept per device).
 int current_device(DeviceState** out) {
@@ -60,6 +84,8 @@ int current_device(DeviceState** out) {
     } else {
       void* sw = nullptr;
       if ((e = GA_CUDA(attn_set_smem_attribute())) != cudaSuccess) return fail_cuda(e);
+      if ((e = GA_CUDA(attn_upload_sigmoid_table(sigmoid_table()))) != cudaSuccess)
+        return fail_cuda(e);
       if ((e = GA_CUDA(cudaGetSymbolAddress(&sw, g_device_status))) != cudaSuccess) return fail_cuda(e);
       d.status_word = static_cast<int*>(sw);
       d.sm_count = sms;

@@ -57,6 +57,8 @@ cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uin
                               const uint16_t* sin_tab, int rows, int q_base, uint16_t* q_prep,
                               cudaStream_t s);
 cudaError_t attn_set_smem_attribute();
+// Fills the device's table of bf16(sigmoid(g)) for every bf16 g (65536 entries, by bits).
+cudaError_t attn_upload_sigmoid_table(const uint16_t* host_table);
 size_t attn_smem_bytes();
 // tm_q: the prepared queries [rows][24][256] (box 64 dims x 1 head x 128 rows).
 cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,

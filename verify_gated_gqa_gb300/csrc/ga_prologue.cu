@@ -64,10 +64,10 @@ __global__ void __launch_bounds__(256) prologue_kernel(const uint16_t* __restric
       ss.merge(o);
     }
   }
-  const float r32 = inv_rms_f32(ss);
+  const InvRms r = inv_rms_df(ss);
   float y[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = norm_elem(x[i], w[i], r32, ss);
+  for (int i = 0; i < 8; ++i) y[i] = norm_elem(x[i], w[i], r);
 
   // Partial RoPE: dims 0..31 (lanes 0..3) pair with dims 32..63 (lanes 4..7).
   float partner[8];
