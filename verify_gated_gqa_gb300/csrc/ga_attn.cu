@@ -511,25 +511,27 @@ __device__ __forceinline__ void rotate8(uint4 (&q)[kDim / 8], const uint4 (&in)[
 // filled once per device from the host. The gate's rare exact path reads it.
 __device__ uint16_t g_sigmoid_bf16[1 << 16];
 
-// Rare path (this lane only): the sigmoids of the 64 gates g[] (8 words of bf16 pairs) that
-// the fast path did not certify, from the exact table, into the matching halves of sg[].
-__device__ __noinline__ void sigmoid_patch(const uint4* g, uint4* sg) {
-  const uint32_t* gw = reinterpret_cast<const uint32_t*>(g);
-  uint32_t* sw = reinterpret_cast<uint32_t*>(sg);
+// Rare path (this lane only): the 8 gates of g (bf16 pairs) whose fast sigmoid was not
+// certified take the exact table value, in the matching halves of o.
+__device__ __noinline__ uint4 sigmoid_patch8(uint4 g, uint4 o) {
+  uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+  uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll 1
-  for (int k = 0; k < 64; ++k) {
+  for (int k = 0; k < 8; ++k) {
     const uint32_t gb = (k & 1) ? (gw[k >> 1] >> 16) : (gw[k >> 1] & 0xFFFFu);
     float y;
     if (sigmoid_fast(__uint_as_float(gb << 16), y)) continue;
     const uint32_t b = g_sigmoid_bf16[gb];
-    sw[k >> 1] = (k & 1) ? ((sw[k >> 1] & 0xFFFFu) | (b << 16)) : ((sw[k >> 1] & 0xFFFF0000u) | b);
+    ow[k >> 1] = (k & 1) ? ((ow[k >> 1] & 0xFFFFu) | (b << 16)) : ((ow[k >> 1] & 0xFFFF0000u) | b);
   }
+  return make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
 
 // bf16(sigmoid(g)) of this thread's 256 gates, as bf16 pairs in registers (word c holds
 // dims 2c and 2c+1); zeros for rows past the end. The gates are read once and processed
-// 64 at a time through a rotating register queue, so the loop stays short without
-// indexing registers.
+// 8 at a time through a rotating register queue: the loop body stays small, because this
+// code shares the instruction cache with the softmax loop running on the same SM
+// sub-partition, and a long unrolled body evicts it.
 __device__ void gate_sigmoid(const AttnArgs& a, const Item& it, int r, uint4 (&sg)[kDim / 8]) {
   const int row = it.mt * kTileM + r;
   if (row >= a.rows) {
@@ -541,34 +543,23 @@ __device__ void gate_sigmoid(const AttnArgs& a, const Item& it, int r, uint4 (&s
 #pragma unroll
   for (int i = 0; i < kDim / 8; ++i) sg[i] = __ldg(gp + i);
 #pragma unroll 1
-  for (int step = 0; step < 4; ++step) {
-    uint4 o[8];
+  for (int step = 0; step < kDim / 8; ++step) {
+    const uint4 g = sg[0];
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t w[4];
     bool ok = true;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t gw[4] = {sg[i].x, sg[i].y, sg[i].z, sg[i].w};
-      uint32_t w[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float s0, s1;
-        ok &= sigmoid_fast(lo_f(gw[k]), s0);
-        ok &= sigmoid_fast(hi_f(gw[k]), s1);
-        w[k] = pack_bf16x2(s0, s1);
-      }
-      o[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int k = 0; k < 4; ++k) {
+      float s0, s1;
+      ok &= sigmoid_fast(lo_f(gw[k]), s0);
+      ok &= sigmoid_fast(hi_f(gw[k]), s1);
+      w[k] = pack_bf16x2(s0, s1);
     }
-    if (!ok) {
-      uint4 g[8], t[8];
+    uint4 o = make_uint4(w[0], w[1], w[2], w[3]);
+    if (!ok) o = sigmoid_patch8(g, o);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        g[i] = sg[i];
-        t[i] = o[i];
-      }
-      sigmoid_patch(g, t);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = t[i];
-    }
-    rotate8(sg, o);
+    for (int i = 0; i < kDim / 8 - 1; ++i) sg[i] = sg[i + 1];
+    sg[kDim / 8 - 1] = o;
   }
 }
 
