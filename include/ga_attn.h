@@ -197,6 +197,31 @@ int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
                    long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
                    void* workspace, size_t ws_bytes, ga_stream stream);
 
+/* Allocation-free variant of ga_attn_masked. The pages have no counterpart: this is an
+ * addition of the library for callers that may not allocate device memory at call time,
+ * such as a server step that runs under a fixed memory budget, or a framework that
+ * forbids allocation inside a step (an allocation can synchronise the device, and can
+ * fail when memory is fragmented). The scratch that ga_attn_masked takes as `workspace`
+ * comes instead from one static device array of GA_STATIC_SCRATCH_BYTES per device,
+ * reserved when the library is loaded; nothing is allocated by the call.
+ *   Arguments, layouts and results: as in ga_attn_masked, without workspace/ws_bytes.
+ *   Limit: ga_masked_workspace_bytes(rows, T) <= GA_STATIC_SCRATCH_BYTES (about 1,100
+ *           rows at T = 8192); larger calls are refused with GA_ERR_WORKSPACE before any
+ *           CUDA call.
+ *   The first call on a device looks up the array's address (one CUDA runtime query,
+ *           once per device, with that device current); make a first call before any
+ *           stream capture.
+ *   The scratch needs no initial contents (every call writes all of it that it reads).
+ *   The array is shared by all calls on a device: calls that may overlap in time (other
+ *           streams, other host threads) race on it and must be serialised by the caller.
+ * Errors: as ga_attn_masked. */
+#define GA_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+int ga_attn_masked_static(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                          const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                          int table_rows, int rows, int T, int q_base, const uint8_t* mask,
+                          long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
+                          ga_stream stream);
+
 /* Bytes of workspace ga_attn_verify needs; max_len is the largest L over the sequences. */
 size_t ga_verify_workspace_bytes(int n_seq, int rows, int max_len);
 

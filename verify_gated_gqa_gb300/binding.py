@@ -41,6 +41,8 @@ _SIGS = {
     "ga_q_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "ga_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "ga_attn_prefill_prepared": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "ga_attn_masked_static": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _LL, _P, _P, _P,
+                                   _P]),
     "ga_masked_workspace_bytes": (_SZ, [_I, _I]),
     "ga_attn_masked": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _LL, _P, _P, _P, _P,
                             _SZ, _P]),
@@ -225,6 +227,25 @@ def ga_attn_masked(qg, k_prep, v, w_q, cos_tab, sin_tab, mask, q_base=0, T=None,
                                 mask.stride(0), _ptr(out), _ptr(weights), _ptr(hidden_rows),
                                 _ptr(workspace), workspace.numel(), _stream()),
            "ga_attn_masked")
+    return out, weights, hidden_rows
+
+
+def ga_attn_masked_static(qg, k_prep, v, w_q, cos_tab, sin_tab, mask, out, hidden_rows,
+                          weights=None, q_base=0, T=None):
+    """The allocation-free masked call: the caller passes every output buffer (out,
+    hidden_rows and, when weights are wanted, weights); the library uses its static scratch."""
+    rows = qg.shape[0]
+    T = k_prep.shape[0] if T is None else T
+    if mask.dtype != torch.uint8 or not mask.is_cuda or mask.stride(1) != 1:
+        raise ValueError("mask must be a uint8 CUDA tensor with unit column stride")
+    for n, t in (("qg", qg), ("k_prep", k_prep), ("v", v), ("w_q", w_q), ("cos_tab", cos_tab),
+                 ("sin_tab", sin_tab), ("out", out)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_attn_masked_static(_ptr(qg), _ptr(k_prep), _ptr(v), _ptr(w_q), _ptr(cos_tab),
+                                       _ptr(sin_tab), cos_tab.shape[0], rows, T, q_base,
+                                       _ptr(mask), mask.stride(0), _ptr(out), _ptr(weights),
+                                       _ptr(hidden_rows), _stream()),
+           "ga_attn_masked_static")
     return out, weights, hidden_rows
 
 

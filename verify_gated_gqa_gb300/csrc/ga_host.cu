@@ -484,4 +484,53 @@ int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_c
   return GA_OK;
 }
 
+// ------------------------------------------------------------------ allocation-free masked call
+// The scratch of ga_attn_masked_static: one static array per device, reserved at module
+// load, its address looked up once per device on the first call (with that device current).
+}  // extern "C"
+
+namespace ga {
+namespace {
+__device__ __align__(256) uint8_t g_static_scratch[GA_STATIC_SCRATCH_BYTES];
+void* g_static_scratch_ptr[kMaxDevices];
+std::mutex g_static_mutex;
+}  // namespace
+}  // namespace ga
+
+extern "C" {
+
+int ga_attn_masked_static(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                          const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                          int table_rows, int rows, int T, int q_base, const uint8_t* mask,
+                          long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
+                          ga_stream stream) {
+  // Every argument check first, with no CUDA call: ga_attn_masked validates all arguments
+  // before it looks at the workspace, and a valid call with an empty (never dereferenced)
+  // workspace answers GA_ERR_WORKSPACE, or GA_OK when there is nothing to do.
+  void* const probe = reinterpret_cast<void*>(uintptr_t(256));
+  int st = ga_attn_masked(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base,
+                          mask, ld_mask, out, weights, hidden_rows, probe, 0, stream);
+  if (st != GA_ERR_WORKSPACE) return st;
+  const size_t need = masked_layout(rows, T).total;
+  if (need > GA_STATIC_SCRATCH_BYTES) return GA_ERR_WORKSPACE;
+  int dev = 0;
+  cudaError_t e = GA_CUDA(cudaGetDevice(&dev));
+  if (e != cudaSuccess) return fail_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return GA_ERR_DEVICE;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!g_static_scratch_ptr[dev]) {
+      void* p = nullptr;
+      if ((e = GA_CUDA(cudaGetSymbolAddress(&p, g_static_scratch))) != cudaSuccess)
+        return fail_cuda(e);
+      g_static_scratch_ptr[dev] = p;
+    }
+    scratch = g_static_scratch_ptr[dev];
+  }
+  return ga_attn_masked(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base, mask,
+                        ld_mask, out, weights, hidden_rows, scratch, GA_STATIC_SCRATCH_BYTES,
+                        stream);
+}
+
 }  // extern "C"
