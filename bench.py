@@ -270,9 +270,10 @@ def run_gpu(args, world, rank, local):
     return line
 
 
-# Per-launch DRAM bytes of attn_kernel (dram__bytes_read.sum + dram__bytes_write.sum) from
-# the ncu capture summarised in profiles/; None until a capture of the current kernel.
-ATTN_TRAFFIC_BYTES = None
+# Per-launch DRAM bytes of attn_kernel (dram__bytes_read.sum + dram__bytes_write.sum: 218.61
+# + 57.80 MB) from the ncu capture summarised in profiles/attn_kernel_causal_s8192.md; to be
+# set to None whenever the kernel changes until it is captured again.
+ATTN_TRAFFIC_BYTES = 276_409_856
 
 
 # ---------------------------------------------------------------- the oracle as baseline
