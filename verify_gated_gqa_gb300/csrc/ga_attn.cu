@@ -81,8 +81,9 @@ struct AttnSmem {
 
 // ------------------------------------------------------------------ work items
 struct Item {
-  int h, mt;          // query head, 128-row tile
+  int h, mt;          // query head (verify: the first query head of the half), 128-row tile
   int n;              // key tiles to visit
+  int seq, half, kt0; // verify: sequence, half of the query group, first key tile of the chunk
   uint64_t tiles[2];  // mask mode: bit kt set for every key tile with a visible key
 };
 
@@ -93,9 +94,25 @@ __device__ __forceinline__ int item_index(int round, int cta, int G) {
 template <int kMode>
 __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
   Item it;
+  it.seq = it.half = it.kt0 = 0;
+  it.tiles[0] = it.tiles[1] = 0;
+  if (kMode == kModeVerify) {
+    // (chunk, sequence, KV head, half): the two halves of a query group are neighbours, so
+    // the CTAs that run them read each K/V tile at about the same time (the second from L2)
+    it.half = idx & 1;
+    const int kvh = (idx >> 1) & 1;
+    const int rest = idx >> 2;
+    it.seq = rest % a.n_seq;
+    const int c = rest / a.n_seq;
+    it.h = kvh * kGroup + kVerifyHeadsPerTile * it.half;
+    it.mt = 0;
+    it.kt0 = c * a.chunk_tiles;
+    const int tiles = (a.seq_len[it.seq] + a.vrows + kTileN - 1) / kTileN;
+    it.n = max(0, min(a.chunk_tiles, tiles - it.kt0));
+    return it;
+  }
   it.mt = a.row_tiles - 1 - idx / kHeads;  // later row tiles see more keys: longest first
   it.h = idx % kHeads;
-  it.tiles[0] = it.tiles[1] = 0;
   if (kMode == kModeCausal) {
     const int last_row = min(a.rows, (it.mt + 1) * kTileM) - 1;
     const int key_end = min(a.T, a.q_base + last_row + 1);
@@ -115,9 +132,11 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
 template <int kMode>
 struct TileCursor {
   uint64_t w0, w1;
-  __device__ __forceinline__ explicit TileCursor(const Item& it) : w0(it.tiles[0]), w1(it.tiles[1]) {}
+  int base;
+  __device__ __forceinline__ explicit TileCursor(const Item& it)
+      : w0(it.tiles[0]), w1(it.tiles[1]), base(it.kt0) {}
   __device__ __forceinline__ int next(int j) {
-    if (kMode != kModeMask) return j;
+    if (kMode != kModeMask) return base + j;
     if (w0) {
       const int kt = __ffsll((long long)w0) - 1;
       w0 &= w0 - 1;
@@ -157,13 +176,18 @@ template <int kMode, bool kW>
 __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, const AttnArgs& a, volatile int* abort,
                               uint32_t& cnt) {
-  // one 128 x 256 tile (four 64-dim boxes) at coordinates (head, row/key 0) into the next slot
-  auto load_tile = [&](const CUtensorMap* map, int head, int r0) -> bool {
+  // one tile (four 64-dim boxes) at coordinates (head, row/key r0[, sequence]) into the
+  // next slot; a verify Q tile holds 6 heads x vrows rows
+  auto load_tile = [&](const CUtensorMap* map, int head, int r0, int seq, uint32_t bytes) -> bool {
     const uint32_t slot = cnt % kSlots;
     if (!mbar_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
-    mbar_expect_tx(&sm.full[slot], kTileBytes);
-    for (int c = 0; c < 4; ++c)
-      tma_load_3d(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0);
+    mbar_expect_tx(&sm.full[slot], bytes);
+    for (int c = 0; c < 4; ++c) {
+      if (seq < 0)
+        tma_load_3d(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0);
+      else
+        tma_load_4d(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0, seq);
+    }
     ++cnt;
     return true;
   };
@@ -174,13 +198,19 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
     TileCursor<kMode> ck(it), cv(it);
     // Ring order: the item's prepared Q (for the edge warps), then in MMA order K0,
     // (K_j, V_{j-1}) for j >= 1, V_{n-1}.
-    if (!load_tile(tm_q, it.h, it.mt * kTileM)) return;
-    if (!load_tile(tm_k, kvh, ck.next(0) * kTileN)) return;
-    for (int j = 1; j < it.n; ++j) {
-      if (!load_tile(tm_k, kvh, ck.next(j) * kTileN)) return;
-      if (!kW && !load_tile(tm_v, kvh, cv.next(j - 1) * kTileN)) return;
+    const int kv_seq = kMode == kModeVerify ? it.seq : -1;
+    if (kMode == kModeVerify) {
+      if (!load_tile(tm_q, it.h, it.seq * a.vrows, -1,
+                     4u * kVerifyHeadsPerTile * a.vrows * 128u)) return;
+    } else {
+      if (!load_tile(tm_q, it.h, it.mt * kTileM, -1, kTileBytes)) return;
     }
-    if (!kW && !load_tile(tm_v, kvh, cv.next(it.n - 1) * kTileN)) return;
+    if (!load_tile(tm_k, kvh, ck.next(0) * kTileN, kv_seq, kTileBytes)) return;
+    for (int j = 1; j < it.n; ++j) {
+      if (!load_tile(tm_k, kvh, ck.next(j) * kTileN, kv_seq, kTileBytes)) return;
+      if (!kW && !load_tile(tm_v, kvh, cv.next(j - 1) * kTileN, kv_seq, kTileBytes)) return;
+    }
+    if (!kW && !load_tile(tm_v, kvh, cv.next(it.n - 1) * kTileN, kv_seq, kTileBytes)) return;
   }
 }
 
@@ -287,25 +317,29 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-// Visibility of the 32 keys kt*128 + 32*ch .. +31 for one row: bit k <-> key +k.
+// Visibility of the 32 keys kt*128 + 32*ch .. +31 for one row: bit k <-> key +k. `limit`
+// is the row's last visible key (causal and verify modes).
 template <int kMode>
-__device__ __forceinline__ uint32_t chunk_visibility(const AttnArgs& a, int row, int kt, int ch,
-                                                     bool valid) {
+__device__ __forceinline__ uint32_t chunk_visibility(const AttnArgs& a, int row, int limit, int kt,
+                                                     int ch, bool valid) {
   if (!valid) return 0u;
   if (kMode == kModeMask)
     return __ldg(a.mask_bits + (size_t)row * a.mask_words + kt * (kTileN / 32) + ch);
   const int first = kt * kTileN + ch * 32;
-  int n = (kMode == kModeCausal) ? (a.q_base + row - first + 1) : (a.T - first);
+  int n = (kMode == kModeBidir) ? (a.T - first) : (limit - first + 1);
   n = max(0, min(32, n));
   return n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
 }
 
 // Every key of tile kt visible to every row of row tile mt (no per-key selects needed).
+// (Verify: every key visible to every row of the item; the padding lanes past 6 vrows see
+// zero queries and are never written out.)
 template <int kMode>
-__device__ __forceinline__ bool tile_full(const AttnArgs& a, int mt, int kt) {
+__device__ __forceinline__ bool tile_full(const AttnArgs& a, const Item& it, int kt) {
   if (kMode == kModeMask) return false;
-  if ((mt + 1) * kTileM > a.rows || (kt + 1) * kTileN > a.T) return false;
-  if (kMode == kModeCausal) return (kt + 1) * kTileN - 1 <= a.q_base + mt * kTileM;
+  if (kMode == kModeVerify) return (kt + 1) * kTileN - 1 <= a.seq_len[it.seq];
+  if ((it.mt + 1) * kTileM > a.rows || (kt + 1) * kTileN > a.T) return false;
+  if (kMode == kModeCausal) return (kt + 1) * kTileN - 1 <= a.q_base + it.mt * kTileM;
   return true;
 }
 
@@ -355,7 +389,9 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
   Item it;
   while (walk.next(a, it)) {
     const int row = it.mt * kTileM + r;
-    const bool valid = row < a.rows;
+    const bool valid = kMode == kModeVerify ? r < kVerifyHeadsPerTile * a.vrows : row < a.rows;
+    const int limit = kMode == kModeVerify ? a.seq_len[it.seq] + r / kVerifyHeadsPerTile
+                                           : a.q_base + row;
     const int h = it.h;
     int M = 0;
     bool hasM = false;
@@ -381,14 +417,14 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
       tmem_wait_ld(sb);
       tc_fence_before();
       mbar_arrive(&sm.s_free);   // the next S = Q K^T may overwrite these columns now
-      if (tile_full<kMode>(a, it.mt, kt)) {
+      if (tile_full<kMode>(a, it, kt)) {
 #pragma unroll
         for (int k = 0; k < kTileN / 2; ++k)
           sb[k] = pack_bf16x2(__uint_as_float(sb[2 * k]), __uint_as_float(sb[2 * k + 1]));
       } else {
 #pragma unroll
         for (int ch = 0; ch < kTileN / 32; ++ch) {
-          const uint32_t vis = chunk_visibility<kMode>(a, row, kt, ch, valid);
+          const uint32_t vis = chunk_visibility<kMode>(a, row, limit, kt, ch, valid);
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             // hidden keys read as -inf: weight exactly 0, never the maximum
@@ -484,14 +520,18 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
 // The item's prepared Q tile (a ring slot: four 128-row x 64-dim blocks, 128-byte
 // swizzled) into this thread's TMEM lane at Q: row r, dims 2c and 2c+1 in column c.
 // Every lane of the warp runs it (warp-collective stores).
-__device__ __forceinline__ void q_copy_tmem(const uint8_t* tile, int r, uint32_t q_taddr) {
+// Lanes with `have` false (verify padding) store zeros.
+__device__ __forceinline__ void q_copy_tmem(const uint8_t* tile, int r, bool have, uint32_t q_taddr) {
 #pragma unroll
   for (int grp = 0; grp < 4; ++grp) {
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
       const uint8_t* base = tile + grp * kChunkBytes;
-      const uint4 v0 = *reinterpret_cast<const uint4*>(base + sw128_offset((uint32_t)r, (uint32_t)j));
-      const uint4 v1 = *reinterpret_cast<const uint4*>(base + sw128_offset((uint32_t)r, (uint32_t)j + 1));
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+      if (have) {
+        v0 = *reinterpret_cast<const uint4*>(base + sw128_offset((uint32_t)r, (uint32_t)j));
+        v1 = *reinterpret_cast<const uint4*>(base + sw128_offset((uint32_t)r, (uint32_t)j + 1));
+      }
       const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
       tmem_st8(q_taddr + 32 * grp + 4 * j, w);
     }
@@ -630,6 +670,39 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
   return true;
 }
 
+// Verify epilogue of one item: the unnormalised O (fp32, relative to 2^M) and M, l of each
+// lane's packed row, for the combine kernel; O is released after the copy.
+__device__ bool epilogue_partial(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32_t tmem,
+                                 uint32_t lane_off, int r, uint32_t it_done, volatile int* abort) {
+  const bool valid = r < kVerifyHeadsPerTile * a.vrows;
+  if (!warp_wait(&sm.st_full, it_done & 1, abort)) return false;
+  const float l = sm.stat_l[r];
+  const float M = sm.stat_m[r];
+  if (!warp_wait(&sm.o_done, it_done & 1, abort)) return false;
+  tc_fence_after();
+  const int chunk = it.kt0 / a.chunk_tiles;
+  const size_t slot = (((size_t)it.seq * kKvHeads + it.h / kGroup) * 2 + it.half) * a.n_chunks + chunk;
+  const size_t prow = slot * kVerifyLanes + (valid ? r : 0);
+  float4* op = reinterpret_cast<float4*>(a.part_o + prow * kDim);
+#pragma unroll 1
+  for (int c = 0; c < kDim / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tmem + kTmemO + lane_off + c * 32, o);
+    tmem_wait_ld(o);
+    if (valid) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        op[8 * c + q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                    __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+    }
+  }
+  tc_fence_before();
+  mbar_arrive(&sm.o_free);
+  mbar_arrive(&sm.st_empty);
+  if (valid) reinterpret_cast<float2*>(a.part_ml)[prow] = make_float2(M, l);
+  return true;
+}
+
 template <int kMode, bool kW>
 __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -649,7 +722,7 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
         ++round;
         return true;
       }
-      write_hidden_rows(a, out, r, kW);
+      if (kMode != kModeVerify) write_hidden_rows(a, out, r, kW);
     }
   };
   // Ring position of each item's Q tile: the producer loads Q, then the item's K and V tiles.
@@ -663,7 +736,8 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
     if (wait_empty && !warp_wait(&sm.q_empty, it_done & 1, abort)) return false;
     if (!warp_wait(&sm.full[slot], (q_pos / kSlots) & 1, abort)) return false;
     tc_fence_after();
-    q_copy_tmem(sm.tile[slot], r, q_taddr);
+    q_copy_tmem(sm.tile[slot], r, kMode != kModeVerify || r < kVerifyHeadsPerTile * a.vrows,
+                q_taddr);
     tc_fence_before();
     mbar_arrive(&sm.q_full);
     mbar_arrive(&sm.q_read);
@@ -684,10 +758,14 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
   uint4 sg[kDim / 8];
   uint32_t it_done = 0;
   while (true) {
-    if (!kW) gate_sigmoid(a, cur, r, sg);
+    if (!kW && kMode != kModeVerify) gate_sigmoid(a, cur, r, sg);
     const bool have_next = next_item(nxt);
     if (have_next && !take_q(nxt, true, it_done)) return;
-    if (!kW && !epilogue(sm, a, cur, tmem, lane_off, r, it_done, sg, abort)) return;
+    if (kMode == kModeVerify) {
+      if (!epilogue_partial(sm, a, cur, tmem, lane_off, r, it_done, abort)) return;
+    } else if (!kW && !epilogue(sm, a, cur, tmem, lane_off, r, it_done, sg, abort)) {
+      return;
+    }
     ++it_done;
     if (!have_next) break;
     cur = nxt;
@@ -757,9 +835,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && sm.abort) record_abort(a.status, sm.abort);
 }
 
+// Verify combine (TensorFold PR #1080, "qwen CUDA: long-prompt prefill 5.4x faster", the
+// attn_partial commit: key chunks processed apart, then merged per row). One warp per
+// (sequence, query head, row); lane l holds dims 8l .. 8l+7. With M = max_c M_c over the
+// chunks the row saw keys in, O = sum_c 2^(M_c - M) O_c and L = sum_c 2^(M_c - M) l_c (exact
+// power-of-two scales, chunks in order), o = bf16(O / L), out = bf16(o * bf16(sigmoid(g))).
+__global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_constant__ AttnArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (w >= a.n_seq * kHeads * a.vrows) return;
+  const int rr = w % a.vrows;
+  const int h = (w / a.vrows) % kHeads;
+  const int b = w / (a.vrows * kHeads);
+  const int kvh = h / kGroup, half = (h % kGroup) / kVerifyHeadsPerTile;
+  const int lanep = rr * kVerifyHeadsPerTile + h % kVerifyHeadsPerTile;
+  const int tiles = (a.seq_len[b] + a.vrows + kTileN - 1) / kTileN;
+  const int chunks = (tiles + a.chunk_tiles - 1) / a.chunk_tiles;
+  const size_t slot0 = (((size_t)b * kKvHeads + kvh) * 2 + half) * a.n_chunks;
+  const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+  float M = -INFINITY;
+  for (int c = 0; c < chunks; ++c) {
+    const float2 v = ml[(slot0 + c) * kVerifyLanes + lanep];
+    if (v.y > 0.f) M = fmaxf(M, v.x);
+  }
+  float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float L = 0.f;
+  for (int c = 0; c < chunks; ++c) {
+    const size_t prow = (slot0 + c) * kVerifyLanes + lanep;
+    const float2 v = ml[prow];
+    if (!(v.y > 0.f)) continue;
+    const float f = ldexpf(1.0f, (int)(v.x - M));   // an exact power of two
+    L = fmaf(f, v.y, L);
+    const float4* op = reinterpret_cast<const float4*>(a.part_o + prow * kDim) + 2 * lane;
+    const float4 p0 = op[0], p1 = op[1];
+    o[0] = fmaf(f, p0.x, o[0]); o[1] = fmaf(f, p0.y, o[1]); o[2] = fmaf(f, p0.z, o[2]);
+    o[3] = fmaf(f, p0.w, o[3]); o[4] = fmaf(f, p1.x, o[4]); o[5] = fmaf(f, p1.y, o[5]);
+    o[6] = fmaf(f, p1.z, o[6]); o[7] = fmaf(f, p1.w, o[7]);
+  }
+  const float inv = L > 0.f ? 1.0f / L : 0.f;
+  const size_t row = (size_t)b * a.vrows + rr;
+  const uint4 gv = __ldg(reinterpret_cast<const uint4*>(a.qg + (row * kHeads + h) * kQgStride + kDim) + lane);
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+  uint32_t res[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float s0, s1;
+    if (!sigmoid_fast(lo_f(gw[k]), s0)) s0 = __uint_as_float((uint32_t)g_sigmoid_bf16[gw[k] & 0xFFFFu] << 16);
+    if (!sigmoid_fast(hi_f(gw[k]), s1)) s1 = __uint_as_float((uint32_t)g_sigmoid_bf16[gw[k] >> 16] << 16);
+    const uint32_t ob = pack_bf16x2(o[2 * k] * inv, o[2 * k + 1] * inv);
+    const uint32_t sp = pack_bf16x2(s0, s1);
+    res[k] = pack_bf16x2(lo_f(ob) * lo_f(sp), hi_f(ob) * hi_f(sp));
+  }
+  reinterpret_cast<uint4*>(a.out + row * kOutRow + h * kDim)[lane] = make_uint4(res[0], res[1], res[2], res[3]);
+}
+
 }  // namespace
 
 size_t attn_smem_bytes() { return sizeof(AttnSmem) + 1024; }
+
+cudaError_t launch_verify_combine(const AttnArgs& a, cudaStream_t s) {
+  const int warps = a.n_seq * kHeads * a.vrows;
+  verify_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t attn_upload_sigmoid_table(const uint16_t* host_table) {
   return cudaMemcpyToSymbol(g_sigmoid_bf16, host_table, sizeof(g_sigmoid_bf16));
@@ -777,6 +915,9 @@ cudaError_t attn_set_smem_attribute() {
   if ((e = cudaFuncSetAttribute(attn_kernel<kModeMask, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
+  if ((e = cudaFuncSetAttribute(attn_kernel<kModeVerify, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+    return e;
   return cudaFuncSetAttribute(attn_kernel<kModeMask, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
@@ -791,6 +932,8 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
     attn_kernel<kModeCausal, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
   } else if (a.mode == kModeBidir) {
     attn_kernel<kModeBidir, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
+  } else if (a.mode == kModeVerify) {
+    attn_kernel<kModeVerify, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
   } else {
     attn_kernel<kModeMask, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
   }

@@ -141,15 +141,17 @@ int encode_kv_map(CUtensorMap* map, const void* base, long long n_tok, long long
   return GA_OK;
 }
 
-// [rows][24][256] bf16 prepared queries as a TMA tensor: box = 64 dims x 1 head x 128 rows,
-// 128-byte swizzle; rows past the end read as zeros.
-int encode_q_map(CUtensorMap* map, const void* base, long long rows) {
+// [rows][24][256] bf16 prepared queries as a TMA tensor: box = 64 dims x box_heads heads x
+// box_rows rows (1 x 128 for the prefill row tiles, 6 x rows for a verify tile), 128-byte
+// swizzle; rows past the end read as zeros.
+int encode_q_map(CUtensorMap* map, const void* base, long long rows, int box_heads = 1,
+                 int box_rows = kTileM) {
   EncodeTiledFn enc;
   int st = get_encode(&enc);
   if (st != GA_OK) return st;
   cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)kHeads, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)kOutRow * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)kTileM};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = GA_CUDA(enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -208,6 +210,31 @@ MaskedLayout masked_layout(int rows, int T) {
   L.q_off = up(L.stats_off + (size_t)kHeads * rows * 2 * sizeof(float));
   L.total = up(L.q_off + (size_t)rows * kOutRow * sizeof(uint16_t));
   return L;
+}
+
+// Verify split: sequences in groups of up to kVerifyMaxSeq per launch; per group, the keys
+// of each sequence in n_chunks chunks of chunk_tiles 128-key tiles, with about two work
+// items (chunk x sequence x KV head x half group) per SM. The workspace holds one group's
+// partials; its size does not depend on the device (at most kVerifyChunkCap / n_seq chunks).
+constexpr int kVerifyChunkCap = 320;
+struct VerifyPlan {
+  int n_seq_group, n_tiles_max, n_chunks_cap;
+};
+VerifyPlan verify_plan(int n_seq, int rows, int max_len) {
+  VerifyPlan p;
+  p.n_seq_group = n_seq < kVerifyMaxSeq ? n_seq : kVerifyMaxSeq;
+  p.n_tiles_max = (max_len + rows + kTileN - 1) / kTileN;
+  const int by_items = kVerifyChunkCap / (4 * (p.n_seq_group > 0 ? p.n_seq_group : 1));
+  p.n_chunks_cap = by_items < 1 ? 1 : by_items;
+  if (p.n_chunks_cap > p.n_tiles_max) p.n_chunks_cap = p.n_tiles_max > 0 ? p.n_tiles_max : 1;
+  return p;
+}
+size_t verify_part_o_bytes(const VerifyPlan& p) {
+  return (size_t)p.n_seq_group * 4 * p.n_chunks_cap * kVerifyLanes * kDim * sizeof(float);
+}
+size_t verify_ws_bytes(const VerifyPlan& p) {
+  return verify_part_o_bytes(p) +
+         (size_t)p.n_seq_group * 4 * p.n_chunks_cap * kVerifyLanes * 2 * sizeof(float);
 }
 
 // The query prologue (unless q_ready: q_prep already holds this call's prepared queries)
@@ -442,8 +469,9 @@ int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
 }
 
 size_t ga_verify_workspace_bytes(int n_seq, int rows, int max_len) {
-  if (n_seq < 1 || rows < 1 || rows > 16 || max_len < 0) return 0;
-  return 256;  // reserved for the split-key partials
+  if (n_seq < 1 || rows < 1 || rows > kVerifyMaxRows || max_len < 0 || max_len > GA_MAX_TOKENS)
+    return 0;
+  return verify_ws_bytes(verify_plan(n_seq, rows, max_len));
 }
 
 int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_cache, int cap,
@@ -470,16 +498,53 @@ int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_c
   DeviceState* dev = nullptr;
   int st = current_device(&dev);
   if (st != GA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const VerifyPlan plan = verify_plan(n_seq, rows, max_len);
   const size_t seq_elems = (size_t)cap * kKvHeads * kDim;
-  for (int b = 0; b < n_seq; ++b) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  for (int g0 = 0; g0 < n_seq; g0 += kVerifyMaxSeq) {
+    const int n = n_seq - g0 < kVerifyMaxSeq ? n_seq - g0 : kVerifyMaxSeq;
     AttnArgs a{};
-    a.qg = qg + (size_t)b * rows * kRowElems;
-    a.w_q = w_q; a.cos_tab = cos_tab; a.sin_tab = sin_tab;
-    a.out = out + (size_t)b * rows * kOutRow;
-    a.rows = rows; a.T = seq_len[b] + rows; a.q_base = seq_len[b]; a.mode = kModeCausal;
-    st = launch_attention(a, a.out, false, k_cache + b * seq_elems, v_cache + b * seq_elems, a.T,
-                          dev, (cudaStream_t)stream);
+    a.qg = qg + (size_t)g0 * rows * kRowElems;
+    a.out = out + (size_t)g0 * rows * kOutRow;
+    a.mode = kModeVerify;
+    a.n_seq = n;
+    a.vrows = rows;
+    SeqPositions sp{};
+    sp.rows_per_seq = rows;
+    int tiles_max = 1;
+    for (int b = 0; b < n; ++b) {
+      a.seq_len[b] = seq_len[g0 + b];
+      sp.seq_base[b] = seq_len[g0 + b];
+      const int t = (seq_len[g0 + b] + rows + kTileN - 1) / kTileN;
+      if (t > tiles_max) tiles_max = t;
+    }
+    // about two items per SM, at most the workspace's chunk count
+    int n_chunks = (2 * dev->sm_count) / (4 * n);
+    if (n_chunks < 1) n_chunks = 1;
+    if (n_chunks > plan.n_chunks_cap) n_chunks = plan.n_chunks_cap;
+    if (n_chunks > tiles_max) n_chunks = tiles_max;
+    a.chunk_tiles = (tiles_max + n_chunks - 1) / n_chunks;
+    a.n_chunks = (tiles_max + a.chunk_tiles - 1) / a.chunk_tiles;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_ml = reinterpret_cast<float*>(ws + verify_part_o_bytes(plan));
+    a.n_items = a.n_chunks * n * 4;
+    a.status = dev->status_word;
+    a.rows = n * rows;
+    cudaError_t e;
+    if ((e = GA_CUDA(launch_q_prologue_seq(a.qg, w_q, cos_tab, sin_tab, n * rows, sp, a.out, s))) !=
+        cudaSuccess)
+      return fail_cuda(e);
+    CUtensorMap tm_q, tm_k, tm_v;
+    st = encode_q_map(&tm_q, a.out, (long long)n * rows, kVerifyHeadsPerTile, rows);
     if (st != GA_OK) return st;
+    st = encode_kv_map(&tm_k, k_cache + (size_t)g0 * seq_elems, cap, n);
+    if (st != GA_OK) return st;
+    st = encode_kv_map(&tm_v, v_cache + (size_t)g0 * seq_elems, cap, n);
+    if (st != GA_OK) return st;
+    const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
+    if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, a, grid, s))) != cudaSuccess) return fail_cuda(e);
+    if ((e = GA_CUDA(launch_verify_combine(a, s))) != cudaSuccess) return fail_cuda(e);
   }
   return GA_OK;
 }

@@ -29,7 +29,17 @@ enum AttnMode : int {
   kModeCausal = 0,   // key j visible iff j <= q_base + r
   kModeBidir = 1,    // every key j < T
   kModeMask = 2,     // stored bit mask (from the mask prepass)
+  kModeVerify = 3,   // few-row windows over long caches: split-key partials (see below)
 };
+
+// Verify mode: a work item is (sequence, KV head, half of the query group, key chunk). Its
+// 128-lane row tile packs 6 query heads x vrows rows of one sequence (lane 6 rr + hh for
+// row rr, head 12 kvh + 6 half + hh; lanes past 6 vrows are padding). The item writes the
+// unnormalised partial O (fp32) and its M, l per lane; a combine kernel merges the chunks.
+constexpr int kVerifyHeadsPerTile = 6;
+constexpr int kVerifyMaxRows = 16;
+constexpr int kVerifyLanes = kVerifyHeadsPerTile * kVerifyMaxRows;   // 96
+constexpr int kVerifyMaxSeq = 64;       // sequences per launch (the host loops over groups)
 
 struct AttnArgs {
   const uint16_t* qg;       // [rows][24][512]
@@ -46,12 +56,28 @@ struct AttnArgs {
   int rows, T, q_base, mode, weights_pass;
   int row_tiles, key_tiles, mask_words;
   int n_items;
+  // verify mode
+  int n_seq, vrows, chunk_tiles, n_chunks;
+  int seq_len[kVerifyMaxSeq];   // L per sequence: row rr sits at position L + rr
+  float* part_o;                // [n_seq][2][2][n_chunks][96][256]
+  float* part_ml;               // [n_seq][2][2][n_chunks][96][2]: M, l
 };
 
 // Launchers (defined next to their kernels). Return a cudaError_t.
 cudaError_t launch_k_prologue(const uint16_t* k_raw, const uint16_t* w_k, const uint16_t* cos_tab,
                               const uint16_t* sin_tab, int n_tok, int pos_base, uint16_t* k_prep,
                               int* status, cudaStream_t s);
+// Prepared query rows of several sequences: token t of sequence t / rows_per_seq sits at
+// position seq_base[t / rows_per_seq] + t % rows_per_seq.
+struct SeqPositions {
+  int rows_per_seq;
+  int seq_base[kVerifyMaxSeq];
+};
+cudaError_t launch_q_prologue_seq(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
+                                  const uint16_t* sin_tab, int n_tok, const SeqPositions& sp,
+                                  uint16_t* q_prep, cudaStream_t s);
+// Merges the verify partials and applies the gate: out[b][rr][h*256 ..].
+cudaError_t launch_verify_combine(const AttnArgs& a, cudaStream_t s);
 // Prepared query rows: q_prep[r][h][0..255] = rope(norm(qg[r][h][0..255])) at q_base + r.
 cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
                               const uint16_t* sin_tab, int rows, int q_base, uint16_t* q_prep,

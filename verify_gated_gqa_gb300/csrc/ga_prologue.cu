@@ -21,19 +21,23 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 }
 
 // rows are (token, head) pairs, heads_per_tok heads per token; row `row` reads 256 values
-// at src + row * src_stride and writes 256 at dst + row * 256.
+// at src + row * src_stride and writes 256 at dst + row * 256. Token t sits at position
+// pos_base + t, or, with kSeq, at sp.seq_base[t / sp.rows_per_seq] + t % sp.rows_per_seq.
+template <bool kSeq>
 __global__ void __launch_bounds__(256) prologue_kernel(const uint16_t* __restrict__ src,
                                                        int src_stride, int heads_per_tok,
                                                        const uint16_t* __restrict__ w_norm,
                                                        const uint16_t* __restrict__ cos_tab,
                                                        const uint16_t* __restrict__ sin_tab,
                                                        long long n_rows, int pos_base,
+                                                       const __grid_constant__ SeqPositions sp,
                                                        uint16_t* __restrict__ dst) {
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= n_rows) return;
   const long long tok = row / heads_per_tok;
-  const int pos = pos_base + (int)tok;
+  const int pos = kSeq ? sp.seq_base[tok / sp.rows_per_seq] + (int)(tok % sp.rows_per_seq)
+                       : pos_base + (int)tok;
 
   const uint4 xv = __ldg(reinterpret_cast<const uint4*>(src + row * src_stride) + lane);
   const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_norm) + lane);
@@ -109,8 +113,8 @@ cudaError_t launch_k_prologue(const uint16_t* k_raw, const uint16_t* w_k, const 
   (void)status;
   const long long n_rows = (long long)n_tok * kKvHeads;
   const unsigned grid = (unsigned)((n_rows + 7) / 8);
-  prologue_kernel<<<grid, 256, 0, s>>>(k_raw, kDim, kKvHeads, w_k, cos_tab, sin_tab, n_rows,
-                                       pos_base, k_prep);
+  prologue_kernel<false><<<grid, 256, 0, s>>>(k_raw, kDim, kKvHeads, w_k, cos_tab, sin_tab,
+                                              n_rows, pos_base, SeqPositions{}, k_prep);
   return cudaGetLastError();
 }
 
@@ -119,8 +123,18 @@ cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uin
                               cudaStream_t s) {
   const long long n_rows = (long long)rows * kHeads;
   const unsigned grid = (unsigned)((n_rows + 7) / 8);
-  prologue_kernel<<<grid, 256, 0, s>>>(qg, kQgStride, kHeads, w_q, cos_tab, sin_tab, n_rows,
-                                       q_base, q_prep);
+  prologue_kernel<false><<<grid, 256, 0, s>>>(qg, kQgStride, kHeads, w_q, cos_tab, sin_tab,
+                                              n_rows, q_base, SeqPositions{}, q_prep);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q_prologue_seq(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
+                                  const uint16_t* sin_tab, int n_tok, const SeqPositions& sp,
+                                  uint16_t* q_prep, cudaStream_t s) {
+  const long long n_rows = (long long)n_tok * kHeads;
+  const unsigned grid = (unsigned)((n_rows + 7) / 8);
+  prologue_kernel<true><<<grid, 256, 0, s>>>(qg, kQgStride, kHeads, w_q, cos_tab, sin_tab, n_rows,
+                                             0, sp, q_prep);
   return cudaGetLastError();
 }
 
