@@ -270,6 +270,94 @@ def run_gpu(args, world, rank, local):
     return line
 
 
+# ---------------------------------------------------------------- verify windows (config 5)
+V_ROWS, V_L = 16, 65536
+V_CAP = V_L + V_ROWS
+
+
+def verify_bytes(n_seq):
+    return (2 * n_seq * V_CAP * KV_HEADS * DIM * 2       # K and V caches, read once
+            + n_seq * V_ROWS * HEADS * 2 * DIM * 2     # fused q|gate rows
+            + n_seq * V_ROWS * HEADS * DIM * 2)        # output rows
+
+
+def run_verify(args, world, rank, local):
+    """Config 5 on one GPU (per rank): ga_attn_verify over prepared caches resident in HBM
+    (--verify-seqs sequences; 8 is the configuration, fewer only for profiling)."""
+    V_SEQ = args.verify_seqs
+    V_METRIC = f"verify windows: HBM GB/s ({V_SEQ} sequences x 16 rows over L=65536 cached keys)"
+    V_BYTES = verify_bytes(V_SEQ)
+    from verify_gated_gqa_gb300 import binding as B
+    from verify_gated_gqa_gb300 import synth
+    from verify_gated_gqa_gb300.build import build
+
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    seed = SEED + 5 + rank
+    c, s = B.ga_rope_table_host(V_CAP)
+    cos, sin = c.to(dev), s.to(dev)
+    w_q = synth.normal_bf16(seed, "w_q", (DIM,), sigma=0.1, device=dev)
+    w_k = synth.normal_bf16(seed, "w_k", (DIM,), sigma=0.1, device=dev)
+    k_cache = torch.empty(V_SEQ, V_CAP, KV_HEADS, DIM, dtype=torch.bfloat16, device=dev)
+    v_cache = torch.empty_like(k_cache)
+    for b in range(V_SEQ):
+        k_raw = synth.normal_bf16(seed, "k", (V_CAP, KV_HEADS, DIM), sub=b, device=dev)
+        B.ga_k_prologue(k_raw, w_k, cos, sin, k_prep=k_cache[b])
+        v_cache[b] = synth.normal_bf16(seed, "v", (V_CAP, KV_HEADS, DIM), sub=b, device=dev)
+        del k_raw
+    qg = torch.stack([synth.normal_bf16(seed, "qg", (V_ROWS, HEADS, 2 * DIM), sub=b, device=dev)
+                      for b in range(V_SEQ)])
+    lens = [V_L] * V_SEQ
+    out = torch.empty(V_SEQ, V_ROWS, HEADS * DIM, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(B.ga_verify_workspace_bytes(V_SEQ, V_ROWS, V_L), dtype=torch.uint8, device=dev)
+
+    def step():
+        B.ga_attn_verify(qg, k_cache, v_cache, lens, w_q, cos, sin, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / args.steps
+    if rank != 0:
+        return None
+    _, peak_hbm, peak_src = measured_peaks()
+    gbs = V_BYTES / (ms * 1e-3) / 1e9
+    return {
+        "metric": V_METRIC, "value": round(world * gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.1) norm weights)",
+        "config": {"workload": f"verify: {V_SEQ} sequences x 16 rows at positions 65536..65551 over "
+                               "prepared K/V caches [65552, 2, 256] bf16, split-key partials "
+                               "and combine",
+                   "l2": f"K/V caches {2 * V_SEQ * V_CAP * KV_HEADS * DIM * 2 / 1e9:.2f} GB"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                     "frac": round(gbs / peak_hbm, 4), "traffic": None,
+                     "peak_kind": f"HBM copy ({peak_src})",
+                     "kernel": "ga_attn_verify (Q prologue + attn_kernel<verify> + combine)",
+                     "algorithmic_bytes": V_BYTES},
+        "gpu_launches": 3 * args.steps, "clocks": clk, "device_status": B.ga_device_status(),
+    }
+
+
 # Per-launch DRAM bytes of attn_kernel (dram__bytes_read.sum + dram__bytes_write.sum: 218.61
 # + 57.80 MB) from the ncu capture summarised in profiles/attn_kernel_causal_s8192.md; to be
 # set to None whenever the kernel changes until it is captured again.
@@ -370,10 +458,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", default="prefill", choices=["prefill", "verify"],
+                    help="prefill: the headline S=8192 causal step; verify: config 5")
+    ap.add_argument("--verify-seqs", type=int, default=8)
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, world, rank)
+    elif args.workload == "verify":
+        line = run_verify(args, world, rank, local)
     else:
         line = run_gpu(args, world, rank, local)
     if line is not None:

@@ -519,12 +519,20 @@ int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_c
       const int t = (seq_len[g0 + b] + rows + kTileN - 1) / kTileN;
       if (t > tiles_max) tiles_max = t;
     }
-    // about two items per SM, at most the workspace's chunk count
-    int n_chunks = (2 * dev->sm_count) / (4 * n);
-    if (n_chunks < 1) n_chunks = 1;
-    if (n_chunks > plan.n_chunks_cap) n_chunks = plan.n_chunks_cap;
-    if (n_chunks > tiles_max) n_chunks = tiles_max;
-    a.chunk_tiles = (tiles_max + n_chunks - 1) / n_chunks;
+    // The chunk count (at most the workspace's) that minimises the busiest SM's key tiles:
+    // ceil(items / SMs) items of chunk_tiles tiles each, ties to fewer chunks (fewer partials).
+    int best_nc = 1;
+    long long best_cost = -1;
+    for (int nc = 1; nc <= plan.n_chunks_cap && nc <= tiles_max; ++nc) {
+      const int ct = (tiles_max + nc - 1) / nc;
+      const long long items = 4LL * n * ((tiles_max + ct - 1) / ct);
+      const long long cost = (items + dev->sm_count - 1) / dev->sm_count * ct;
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_nc = nc;
+      }
+    }
+    a.chunk_tiles = (tiles_max + best_nc - 1) / best_nc;
     a.n_chunks = (tiles_max + a.chunk_tiles - 1) / a.chunk_tiles;
     a.part_o = reinterpret_cast<float*>(ws);
     a.part_ml = reinterpret_cast<float*>(ws + verify_part_o_bytes(plan));
