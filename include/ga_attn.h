@@ -103,6 +103,14 @@ unsigned long long ga_debug_cuda_calls(void);
  * word afterwards. */
 int ga_device_status(int* status_out, int clear);
 
+/* Test hook for failure detection (no counterpart in the pages): launches a one-thread
+ * kernel that waits, bounded by limit_cycles SM clock cycles (1 .. 2e9), on an mbarrier
+ * that nothing arrives on. The wait gives up, the kernel records the wait-timeout status
+ * (1) in the device status word and returns: the same bounded wait and recording every
+ * kernel of the library uses, without a fault, a trap or a hang. Read the result with
+ * ga_device_status. Errors: RANGE, DEVICE, CUDA. */
+int ga_debug_wait_timeout(long long limit_cycles, ga_stream stream);
+
 /* HOST helper. Fills cos_out and sin_out (HOST arrays of n_pos * 32 values each,
  * [position][pair]) with cos and sin of p * 1e7^(-2i/64) for positions p < n_pos and
  * pairs i < 32, each computed in double and rounded once to bf16 (pegainfer PR #1151,

@@ -176,6 +176,13 @@ def test_q_prologue_and_prepared_refusals(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def test_wait_timeout_hook_refuses_bad_limits(L):
+    before = L.ga_debug_cuda_calls()
+    assert L.ga_debug_wait_timeout(0, S) == -4
+    assert L.ga_debug_wait_timeout(3_000_000_000, S) == -4
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_empty_calls_are_noops_without_cuda(L):
     before = L.ga_debug_cuda_calls()
     assert _prefill(L, rows=0) == 0

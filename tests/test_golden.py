@@ -1,0 +1,34 @@
+"""Values the pages print, kept as small text fixtures under tests/golden/ with their
+citations, checked against this build's conventions."""
+import os
+
+import pytest
+
+import bench
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line.split()
+
+
+@pytest.mark.parametrize("row", list(_rows("qsa_performance_table.txt")))
+def test_flop_convention_reproduces_the_printed_table(row):
+    """The bench counts 4 * head_dim * heads flops per visible (query, key) pair; with every
+    pair visible this reproduces the TFLOP/s the page prints for its own timings to within
+    0.01 (the 2048 x 2048 row computes to 0.924 where the page prints 0.93; a factor-two
+    convention would give 0.46 or 1.85 and fail every row)."""
+    rows, tokens, ms, printed = int(row[0]), int(row[1]), float(row[2]), float(row[3])
+    tflops = bench.attention_flops(rows * tokens) / (ms * 1e-3) / 1e12
+    assert abs(tflops - printed) <= 0.01, (rows, tokens, tflops, printed)
+
+
+def test_causal_pair_count():
+    """The causal pass at S = 8192 has S (S + 1) / 2 visible pairs per head."""
+    assert bench.visible_pairs_causal(8192, 8192) == 8192 * 8193 // 2
+    assert bench.FLOPS_STEP == 4.0 * 256 * 24 * 33_558_528

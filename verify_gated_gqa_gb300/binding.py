@@ -39,6 +39,7 @@ _SIGS = {
     "ga_rope_table_host": (_I, [_I, _P, _P]),
     "ga_k_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "ga_q_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "ga_debug_wait_timeout": (_I, [_LL, _P]),
     "ga_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "ga_attn_prefill_prepared": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "ga_attn_masked_static": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _LL, _P, _P, _P,

@@ -889,7 +889,25 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_consta
   reinterpret_cast<uint4*>(a.out + row * kOutRow + h * kDim)[lane] = make_uint4(res[0], res[1], res[2], res[3]);
 }
 
+// Test hook: one thread waits, with a bound of `limit` cycles, on an mbarrier that nothing
+// arrives on, through the same bounded wait and status recording every kernel here uses.
+__global__ void wait_timeout_kernel(long long limit, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x != 0) return;
+  abort = 0;
+  mbar_init(&bar, 1);
+  mbar_fence_init();
+  volatile int* ab = &abort;
+  if (!mbar_wait(&bar, 0, ab, limit)) record_abort(status, abort);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout(long long limit, int* status, cudaStream_t s) {
+  wait_timeout_kernel<<<1, 32, 0, s>>>(limit, status);
+  return cudaGetLastError();
+}
 
 size_t attn_smem_bytes() { return sizeof(AttnSmem) + 1024; }
 

@@ -316,6 +316,15 @@ int ga_device_status(int* status_out, int clear) {
   return GA_OK;
 }
 
+int ga_debug_wait_timeout(long long limit_cycles, ga_stream stream) {
+  if (limit_cycles < 1 || limit_cycles > 2000000000LL) return GA_ERR_RANGE;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaError_t e = GA_CUDA(launch_wait_timeout(limit_cycles, dev->status_word, (cudaStream_t)stream));
+  return e == cudaSuccess ? GA_OK : fail_cuda(e);
+}
+
 int ga_rope_table_host(int n_pos, ga_bf16* cos_out, ga_bf16* sin_out) {
   if (!cos_out || !sin_out) return GA_ERR_NULL;
   if (n_pos < 0) return GA_ERR_SHAPE;

@@ -83,6 +83,8 @@ cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uin
                               const uint16_t* sin_tab, int rows, int q_base, uint16_t* q_prep,
                               cudaStream_t s);
 cudaError_t attn_set_smem_attribute();
+// Test hook: a bounded wait on a barrier nothing arrives on (records a wait timeout).
+cudaError_t launch_wait_timeout(long long limit, int* status, cudaStream_t s);
 // Fills the device's table of bf16(sigmoid(g)) for every bf16 g (65536 entries, by bits).
 cudaError_t attn_upload_sigmoid_table(const uint16_t* host_table);
 size_t attn_smem_bytes();
