@@ -74,7 +74,7 @@ struct AttnSmem {
   float stat_m[kTileM];               // and its running maximum M
   uint64_t full[kSlots], empty[kSlots];
   uint64_t q_full, q_empty, s_full, s_free, p_full, p_empty;
-  uint64_t o_ready, o_done, o_free, st_full, st_empty, drain, q_read;
+  uint64_t o_done, o_free, st_full, st_empty, drain, q_read;
   uint32_t tmem_base;
   int abort;
 };
@@ -233,6 +233,9 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
   constexpr uint32_t kIdQK = idesc_bf16(128, kTileN, false, false);
   constexpr uint32_t kIdPV = idesc_bf16(128, kDim, false, true);
   const uint32_t p_addr = smem_u32(sm.p[0]);
+  const uint64_t p_desc0 = sdesc_sw128(p_addr, 16, 1024);
+  const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), kChunkBytes, 1024);
+  const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), 16, 1024);
   uint32_t cnt = 0;       // tile-slot sequence (same order as the producer)
   uint32_t g = 0;         // global key-tile counter: S, P and PV phases
   uint32_t it_done = 0;
@@ -250,16 +253,17 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
     if (j == 0 && it_done > 0 && !mbar_wait(&sm.o_free, (it_done - 1) & 1, abort)) return false;
     if (!mbar_wait(&sm.p_full, gj & 1, abort)) return false;
     tc_fence_after();
-    const uint32_t v_addr = smem_u32(sm.tile[slot]);
+    // descriptors advance by constants (addresses in 16-byte units in the low field):
+    // P by 32 bytes per k-step inside a 64-key block and 16 KiB per block, V by 2 KiB
+    const uint64_t bd0 = v_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
-      const uint64_t ad = sdesc_sw128(p_addr + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
-      const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, kChunkBytes, 1024);
-      umma_ss(tmem + kTmemO, ad, bd, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+      const uint64_t ad = p_desc0 + (uint64_t)((kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2);
+      umma_ss(tmem + kTmemO, ad, bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
+              (j > 0 || kk > 0) ? 1u : 0u);
     }
     umma_commit(&sm.empty[slot]);
-    umma_commit(&sm.p_empty);
-    umma_commit(&sm.o_ready);
+    umma_commit(&sm.p_empty);   // also tells the softmax that O holds every P V so far
     return true;
   };
 
@@ -275,10 +279,10 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
       // S is free once the softmax warps have copied the previous tile's S out
       if (g > 0 && !mbar_wait(&sm.s_free, (g - 1) & 1, abort)) return;
       tc_fence_after();
-      const uint32_t k_addr = smem_u32(sm.tile[slot]);
+      const uint64_t kd0 = k_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
 #pragma unroll
       for (int kk = 0; kk < kDim / 16; ++kk) {
-        const uint64_t bd = sdesc_sw128(k_addr + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = kd0 + (uint64_t)((kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2);
         umma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, kIdQK, kk > 0 ? 1u : 0u);
       }
       umma_commit(&sm.empty[slot]);
@@ -464,8 +468,9 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
         }
       }
       if (__any_sync(0xffffffffu, rescale)) {
-        // O must hold every earlier P.V before it is scaled (the PV of global tile g-1)
-        if (!warp_wait(&sm.o_ready, (g - 1) & 1, abort)) return;
+        // O must hold every earlier P.V before it is scaled (the PV of global tile g-1, whose
+        // completion p_empty marks; the P buffer wait below then passes at once)
+        if (!warp_wait(&sm.p_empty, (g - 1) & 1, abort)) return;
         tc_fence_after();
         const float f = rescale ? exp2f((float)(M - newM)) : 1.0f;
 #pragma unroll 1
@@ -793,7 +798,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.s_free, 128);
     mbar_init(&sm.p_full, 128);
     mbar_init(&sm.p_empty, 1);
-    mbar_init(&sm.o_ready, 1);
     mbar_init(&sm.o_done, 1);
     mbar_init(&sm.o_free, 128);
     mbar_init(&sm.st_full, 128);
