@@ -22,15 +22,17 @@
 //              128-byte-swizzled column blocks) through three tile slots;
 //   warp 1     allocates the 512 TMEM columns and issues every tcgen05.mma, all at full
 //              rate (N >= 128): S = Q K^T (M=128, N=128, K=256; Q read from TMEM), then
-//              O += P V (M=128, N=256, K=128; P from shared memory, V MN-major);
+//              O += P V (M=128, N=256, K=128; P from shared memory, V MN-major). The
+//              whole warp runs the issue loop and one elected lane issues: a lone lane in
+//              a divergent branch issued too slowly to keep the N=128 MMAs back to back;
 //   warps 4-7  softmax, one query row per thread: S is copied to registers and its TMEM
 //              columns released at once (so the next S = Q K^T overlaps this softmax),
 //              P = bf16(2^(t - M)) goes to shared memory, the rare O rescale;
-//   warps 8-11 the edge of each work item: the next item's Q (norm, RoPE) into TMEM as
-//              soon as the current item's last S = Q K^T has read Q (its sum of squares
-//              is taken earlier, off that path), then the gated epilogue of the current
-//              item (O drained to the output rows first, so the next item's P V can start,
-//              then the gate applied in place).
+//   warps 8-11 the edge of each work item: the gate sigmoids of the current item while
+//              its tiles run, the next item's prepared Q tile (normed and rotated by the
+//              query prologue, delivered through the tile ring) into TMEM as soon as the
+//              current item's last S = Q K^T has read Q, then the gated epilogue of the
+//              current item.
 // The edge code is kept in short loops: the four roles run different code at once and
 // share the SM's instruction cache, which long unrolled sequences would overflow.
 // Tensor memory (512 columns x 128 lanes, lane = query row): O [0, 256) fp32, Q
@@ -171,6 +173,13 @@ __device__ __forceinline__ void record_abort(int* status, int code) {
   if (code) atomicCAS(status, 0, code);
 }
 
+// Wait in all 32 lanes and agree on the outcome, so that the warp-collective TMEM loads and
+// stores (and elected MMA issues) that follow always run with the whole warp (or the whole warp leaves).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ------------------------------------------------------------------ warp 0: producer
 template <int kMode, bool kW>
 __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
@@ -242,7 +251,7 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
 
   auto take = [&](uint32_t& slot) -> bool {
     slot = cnt % kSlots;
-    if (!mbar_wait(&sm.full[slot], (cnt / kSlots) & 1, abort)) return false;
+    if (!warp_wait(&sm.full[slot], (cnt / kSlots) & 1, abort)) return false;
     tc_fence_after();
     ++cnt;
     return true;
@@ -250,8 +259,8 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
   auto issue_pv = [&](int j, uint32_t gj) -> bool {
     uint32_t slot;
     if (!take(slot)) return false;
-    if (j == 0 && it_done > 0 && !mbar_wait(&sm.o_free, (it_done - 1) & 1, abort)) return false;
-    if (!mbar_wait(&sm.p_full, gj & 1, abort)) return false;
+    if (j == 0 && it_done > 0 && !warp_wait(&sm.o_free, (it_done - 1) & 1, abort)) return false;
+    if (!warp_wait(&sm.p_full, gj & 1, abort)) return false;
     tc_fence_after();
     // descriptors advance by constants (addresses in 16-byte units in the low field):
     // P by 32 bytes per k-step inside a 64-key block and 16 KiB per block, V by 2 KiB
@@ -259,11 +268,11 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
       const uint64_t ad = p_desc0 + (uint64_t)((kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2);
-      umma_ss(tmem + kTmemO, ad, bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
+      umma_ss_warp(tmem + kTmemO, ad, bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
               (j > 0 || kk > 0) ? 1u : 0u);
     }
-    umma_commit(&sm.empty[slot]);
-    umma_commit(&sm.p_empty);   // also tells the softmax that O holds every P V so far
+    umma_commit_warp(&sm.empty[slot]);
+    umma_commit_warp(&sm.p_empty);   // also tells the softmax that O holds every P V so far
     return true;
   };
 
@@ -271,28 +280,28 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
   Item it;
   while (walk.next(a, it)) {
     ++cnt;   // the item's Q tile: consumed by the edge warps
-    if (!mbar_wait(&sm.q_full, it_done & 1, abort)) return;
+    if (!warp_wait(&sm.q_full, it_done & 1, abort)) return;
     tc_fence_after();
     for (int j = 0; j < it.n; ++j, ++g) {
       uint32_t slot;
       if (!take(slot)) return;
       // S is free once the softmax warps have copied the previous tile's S out
-      if (g > 0 && !mbar_wait(&sm.s_free, (g - 1) & 1, abort)) return;
+      if (g > 0 && !warp_wait(&sm.s_free, (g - 1) & 1, abort)) return;
       tc_fence_after();
       const uint64_t kd0 = k_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
 #pragma unroll
       for (int kk = 0; kk < kDim / 16; ++kk) {
         const uint64_t bd = kd0 + (uint64_t)((kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2);
-        umma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, kIdQK, kk > 0 ? 1u : 0u);
+        umma_ts_warp(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, kIdQK, kk > 0 ? 1u : 0u);
       }
-      umma_commit(&sm.empty[slot]);
-      umma_commit(&sm.s_full);
-      if (j == it.n - 1) umma_commit(&sm.q_empty);
+      umma_commit_warp(&sm.empty[slot]);
+      umma_commit_warp(&sm.s_full);
+      if (j == it.n - 1) umma_commit_warp(&sm.q_empty);
       if (!kW && j >= 1 && !issue_pv(j - 1, g - 1)) return;
     }
     if (!kW) {
       if (!issue_pv(it.n - 1, g - 1)) return;
-      umma_commit(&sm.o_done);
+      umma_commit_warp(&sm.o_done);
     }
     ++it_done;
   }
@@ -303,7 +312,7 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
 template <int kMode, bool kW>
 __device__ void mma_issuer(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
   mma_loop<kMode, kW>(sm, a, tmem, abort);
-  umma_commit(&sm.drain);
+  umma_commit_warp(&sm.drain);
   mbar_wait_quiet(&sm.drain, 0, 100000000LL);
 }
 
@@ -312,13 +321,6 @@ __device__ __forceinline__ float lo_f(uint32_t u) { return __uint_as_float(u << 
 __device__ __forceinline__ float hi_f(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return (uint32_t)bf16_bits(a) | ((uint32_t)bf16_bits(b) << 16);
-}
-
-// Wait in all 32 lanes and agree on the outcome, so that the warp-collective TMEM loads and
-// stores that follow always run with the whole warp (or the whole warp leaves).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  const bool ok = mbar_wait(bar, parity, abort);
-  return __all_sync(0xffffffffu, ok);
 }
 
 // Visibility of the 32 keys kt*128 + 32*ch .. +31 for one row: bit k <-> key +k. `limit`
@@ -823,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
     if (warp == 0 && lane == 0) producer<kMode, kW>(sm, &tm_q, &tm_k, &tm_v, a, abort);
-    if (warp == 1 && lane == 0) mma_issuer<kMode, kW>(sm, a, tmem, abort);
+    if (warp == 1) mma_issuer<kMode, kW>(sm, a, tmem, abort);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
     if (warp < 8) softmax_worker<kMode, kW>(sm, a, tmem, abort);
