@@ -75,7 +75,8 @@ struct AttnSmem {
   float stat_l[kTileM];               // softmax -> edge: the row sum l of the finished item
   float stat_m[kTileM];               // and its running maximum M
   uint64_t full[kSlots], empty[kSlots];
-  uint64_t q_full, q_empty, s_full, s_free, p_full, p_empty;
+  uint64_t q_full, q_empty, s_full, s_free;
+  uint64_t p_full[2], p_empty[2];     // per 64-key half of P
   uint64_t o_done, o_free, st_full, st_empty, drain, q_read;
   uint32_t tmem_base;
   int abort;
@@ -260,19 +261,26 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
     uint32_t slot;
     if (!take(slot)) return false;
     if (j == 0 && it_done > 0 && !warp_wait(&sm.o_free, (it_done - 1) & 1, abort)) return false;
-    if (!warp_wait(&sm.p_full, gj & 1, abort)) return false;
-    tc_fence_after();
     // descriptors advance by constants (addresses in 16-byte units in the low field):
-    // P by 32 bytes per k-step inside a 64-key block and 16 KiB per block, V by 2 KiB
+    // P by 32 bytes per k-step inside a 64-key block and 16 KiB per block, V by 2 KiB.
+    // The two 64-key halves of P go separately: the softmax writes the next tile's first
+    // half while this tile's second half is still being read.
     const uint64_t bd0 = v_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
 #pragma unroll
-    for (int kk = 0; kk < kTileN / 16; ++kk) {
-      const uint64_t ad = p_desc0 + (uint64_t)((kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2);
-      umma_ss_warp(tmem + kTmemO, ad, bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
-              (j > 0 || kk > 0) ? 1u : 0u);
+    for (int hb = 0; hb < 2; ++hb) {
+      if (!warp_wait(&sm.p_full[hb], gj & 1, abort)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const int kk = 4 * hb + k4;
+        const uint64_t ad = p_desc0 + (uint64_t)(hb * (kChunkBytes >> 4) + k4 * 2);
+        umma_ss_warp(tmem + kTmemO, ad, bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      // p_empty[1] also tells the softmax that O holds every P V so far
+      umma_commit_warp(&sm.p_empty[hb]);
     }
     umma_commit_warp(&sm.empty[slot]);
-    umma_commit_warp(&sm.p_empty);   // also tells the softmax that O holds every P V so far
     return true;
   };
 
@@ -471,8 +479,8 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O must hold every earlier P.V before it is scaled (the PV of global tile g-1, whose
-        // completion p_empty marks; the P buffer wait below then passes at once)
-        if (!warp_wait(&sm.p_empty, (g - 1) & 1, abort)) return;
+        // completion p_empty[1] marks; the P buffer waits below then pass at once)
+        if (!warp_wait(&sm.p_empty[1], (g - 1) & 1, abort)) return;
         tc_fence_after();
         const float f = rescale ? exp2f((float)(M - newM)) : 1.0f;
 #pragma unroll 1
@@ -489,28 +497,32 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
       }
       M = newM;
       const float mf = hasM ? (float)M : 0.f;
-      // P = bf16(2^(t - M)), t = bf16(s) * log2(e) / 16, into shared memory once the
-      // previous P.V has read the buffer; l sums the rounded P
-      if (g > 0 && !warp_wait(&sm.p_empty, (g - 1) & 1, abort)) return;
+      // P = bf16(2^(t - M)), t = bf16(s) * log2(e) / 16, into shared memory, each 64-key
+      // half once the previous P.V has read that half; l sums the rounded P
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
-      for (int cd = 0; cd < kTileN / 8; ++cd) {
-        uint32_t pk[4];
+      for (int hb = 0; hb < 2; ++hb) {
+        if (g > 0 && !warp_wait(&sm.p_empty[hb], (g - 1) & 1, abort)) return;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t w = sb[cd * 4 + k];
-          const float t0 = fmaf(lo_f(w), kLog2eOver16, -mf);
-          const float t1 = fmaf(hi_f(w), kLog2eOver16, -mf);
-          pk[k] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
-          if (k & 1) add_bf16x2(l2, l3, pk[k]);
-          else add_bf16x2(l0, l1, pk[k]);
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const int cd = 8 * hb + c8;
+          uint32_t pk[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t w = sb[cd * 4 + k];
+            const float t0 = fmaf(lo_f(w), kLog2eOver16, -mf);
+            const float t1 = fmaf(hi_f(w), kLog2eOver16, -mf);
+            pk[k] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
+            if (k & 1) add_bf16x2(l2, l3, pk[k]);
+            else add_bf16x2(l0, l1, pk[k]);
+          }
+          uint8_t* dst = sm.p[hb] + sw128_offset((uint32_t)r, (uint32_t)c8);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        uint8_t* dst = sm.p[cd >> 3] + sw128_offset((uint32_t)r, (uint32_t)(cd & 7));
-        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        fence_async_smem();
+        mbar_arrive(&sm.p_full[hb]);
       }
       l += (l0 + l2) + (l1 + l3);
-      fence_async_smem();
-      mbar_arrive(&sm.p_full);
     }
     if (!kW) {
       // hand l and M of this item to the edge warps
@@ -798,8 +810,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.q_empty, 1);
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.s_free, 128);
-    mbar_init(&sm.p_full, 128);
-    mbar_init(&sm.p_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.p_full[i], 128);
+      mbar_init(&sm.p_empty[i], 1);
+    }
     mbar_init(&sm.o_done, 1);
     mbar_init(&sm.o_free, 128);
     mbar_init(&sm.st_full, 128);
