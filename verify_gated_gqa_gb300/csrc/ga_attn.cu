@@ -17,7 +17,7 @@
 // bf16(e^s) up to a common power of two, whatever the tile schedule: a row's bits do
 // not depend on which tile or window computes it.
 //
-// Structure (one CTA per SM, persistent, 384 threads in three warpgroups):
+// Structure (one CTA per SM, persistent, 512 threads in four warpgroups):
 //   warp 0     TMA producer: K and V tiles of 128 keys x 256 dims (64 KiB, four 16 KiB
 //              128-byte-swizzled column blocks) through three tile slots;
 //   warp 1     allocates the 512 TMEM columns and issues every tcgen05.mma, all at full
@@ -25,10 +25,14 @@
 //              O += P V (M=128, N=256, K=128; P from shared memory, V MN-major). The
 //              whole warp runs the issue loop and one elected lane issues: a lone lane in
 //              a divergent branch issued too slowly to keep the N=128 MMAs back to back;
-//   warps 4-7  softmax, one query row per thread: S is copied to registers and its TMEM
-//              columns released at once (so the next S = Q K^T overlaps this softmax),
-//              P = bf16(2^(t - M)) goes to shared memory, the rare O rescale;
-//   warps 8-11 the edge of each work item: the gate sigmoids of the current item while
+//   warps 4-11 softmax, two warpgroups, one per 64-key half of each S tile, one query row
+//              per thread: S is copied to registers and its TMEM columns released at once
+//              (so the next S = Q K^T overlaps this softmax); the two halves exchange their
+//              row maxima through shared memory and take the same M; P = bf16(2^(t - M))
+//              goes to shared memory, each half its own 64 keys (and the tensor cores read
+//              each half as soon as it is written), and each half rescales its half of O
+//              when needed;
+//   warps 12-15 the edge of each work item: the gate sigmoids of the current item while
 //              its tiles run, the next item's prepared Q tile (normed and rotated by the
 //              query prologue, delivered through the tile ring) into TMEM as soon as the
 //              current item's last S = Q K^T has read Q, then the gated epilogue of the
@@ -51,15 +55,19 @@ namespace {
 constexpr int kSlots = 3;
 constexpr int kChunkBytes = kTileN * 128;     // 128 keys x 64 dims of bf16
 constexpr int kTileBytes = 4 * kChunkBytes;   // 128 keys x 256 dims
-constexpr int kThreads = 384;     // three warpgroups
+constexpr int kThreads = 512;     // four warpgroups
+constexpr int kEdgeThread0 = 384; // first thread of the edge warpgroup (warps 12-15)
 // Register split (setmaxnreg): the kernel is launched at kLaunchRegs per thread; the
-// producer/MMA warpgroup gives registers back and the softmax and edge warpgroups take
-// them. The shares add up to the launch total: 128*56 + 2*128*224 = 384*168, and on each
-// SM sub-partition (one warp of each warpgroup) 32*(56 + 224 + 224) <= 16384.
-constexpr int kLaunchRegs = 168;
-constexpr int kRegsIssue = 56;
-constexpr int kRegsWork = 224;
-static_assert(128 * kRegsIssue + 2 * 128 * kRegsWork == kThreads * kLaunchRegs, "register split");
+// producer/MMA and softmax warpgroups give registers back and the edge warpgroup takes
+// them. The shares add up to the launch total: 128*(64 + 2*112 + 224) = 512*128, and on
+// each SM sub-partition (one warp of each warpgroup) 32*(64 + 2*112 + 224) = 16384.
+constexpr int kLaunchRegs = 128;
+constexpr int kRegsIssue = 64;
+constexpr int kRegsSoftmax = 112;
+constexpr int kRegsEdge = 224;
+static_assert(128 * (kRegsIssue + 2 * kRegsSoftmax + kRegsEdge) == kThreads * kLaunchRegs,
+              "register split");
+constexpr int kHalfKeys = kTileN / 2;   // keys per softmax warpgroup in a tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;      // O accumulator: 256 columns (fp32)
 constexpr uint32_t kTmemQ = 256;    // Q: 128 columns of bf16 pairs (A operand of Q K^T)
@@ -72,12 +80,13 @@ static_assert(kTileN == 128, "this kernel is laid out for 128-key tiles");
 struct AttnSmem {
   uint8_t tile[kSlots][kTileBytes];   // K or V tiles (1024-byte aligned)
   uint8_t p[2][kChunkBytes];          // P: 128 rows x 128 keys, two swizzled 64-key columns
-  float stat_l[kTileM];               // softmax -> edge: the row sum l of the finished item
-  float stat_m[kTileM];               // and its running maximum M
+  float stat_l[2][kTileM];            // softmax -> edge: each half's row sum l of the item
+  float stat_m[kTileM];               // and the running maximum M
+  uint16_t mx[2][2][kTileM];          // tile g: each half's row maximum (bf16 bits), by g % 2
   uint64_t full[kSlots], empty[kSlots];
   uint64_t q_full, q_empty, s_full, s_free;
   uint64_t p_full[2], p_empty[2];     // per 64-key half of P
-  uint64_t o_done, o_free, st_full, st_empty, drain, q_read;
+  uint64_t o_done, o_free, st_full, st_empty, drain, q_read, mx_bar;
   uint32_t tmem_base;
   int abort;
 };
@@ -357,18 +366,18 @@ __device__ __forceinline__ bool tile_full(const AttnArgs& a, const Item& it, int
   return true;
 }
 
-// ------------------------------------------------------------------ warps 4-7: softmax
-// Weights pass: bf16(bf16(2^(t - M)) / l) for the keys of one tile (bf16 score pairs in
-// sb[0 .. 63], hidden ones -inf), with the main pass's final M and l, written to
-// weights[h][row][kt*128 ..].
-__device__ __forceinline__ void weights_tile(const AttnArgs& a, const uint32_t (&sb)[kTileN],
-                                             int h, int row, int kt, int M, float l_final) {
+// ------------------------------------------------------------------ warps 4-11: softmax
+// Weights pass: bf16(bf16(2^(t - M)) / l) for the 64 keys of one half tile (bf16 score pairs
+// in sb[0 .. 31], hidden ones -inf), with the main pass's final M and l, written to
+// weights[h][row][key0 ..].
+__device__ __forceinline__ void weights_half(const AttnArgs& a, const uint32_t (&sb)[kHalfKeys],
+                                             int h, int row, int key0, int M, float l_final) {
   const float mf = (float)M;
-  uint16_t* wrow = a.weights + ((size_t)h * a.rows + row) * (size_t)a.T + (size_t)kt * kTileN;
-  const int ncol = min(kTileN, a.T - kt * kTileN);
-  const bool vec = (ncol == kTileN) && ((a.T & 7) == 0);
+  uint16_t* wrow = a.weights + ((size_t)h * a.rows + row) * (size_t)a.T + (size_t)key0;
+  const int ncol = min(kHalfKeys, a.T - key0);
+  const bool vec = (ncol == kHalfKeys) && ((a.T & 7) == 0);
 #pragma unroll
-  for (int ch = 0; ch < kTileN / 32; ++ch) {
+  for (int ch = 0; ch < kHalfKeys / 32; ++ch) {
     uint32_t pk[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
@@ -390,14 +399,15 @@ __device__ __forceinline__ void weights_tile(const AttnArgs& a, const uint32_t (
   }
 }
 
+// Softmax of one 64-key half (hf) of every S tile, one query row per thread.
 template <int kMode, bool kW>
-__device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
+__device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, int hf,
                                volatile int* abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-  const uint32_t s_taddr = tmem + kTmemS + lane_off;
+  const uint32_t s_taddr = tmem + kTmemS + lane_off + kHalfKeys * hf;
   uint32_t g = 0, it_done = 0;
   ItemWalk<kMode> walk;
   Item it;
@@ -409,7 +419,7 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
     const int h = it.h;
     int M = 0;
     bool hasM = false;
-    float l = 0.f;
+    float l = 0.f;        // this half's sum of the rounded weights
     float l_final = 0.f;  // weights pass: the main pass's l (relative to its final M)
     if (kW && valid) {
       M = (int)a.row_stats[((size_t)h * a.rows + row) * 2];
@@ -421,24 +431,22 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
       const int kt = cursor.next(j);
       if (!warp_wait(&sm.s_full, g & 1, abort)) return;
       tc_fence_after();
-      // S -> registers (four loads, one wait), packed in place as bf16 pairs (the score's
+      // this half's 64 S columns -> registers, packed in place as bf16 pairs (the score's
       // own rounding); then the columns are released
-      uint32_t sb[kTileN];
+      uint32_t sb[kHalfKeys];
       tmem_ld32(s_taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(sb));
       tmem_ld32(s_taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(sb + 32));
-      tmem_ld32(s_taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(sb + 64));
-      tmem_ld32(s_taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(sb + 96));
       tmem_wait_ld(sb);
       tc_fence_before();
-      mbar_arrive(&sm.s_free);   // the next S = Q K^T may overwrite these columns now
+      mbar_arrive(&sm.s_free);   // the next S = Q K^T may overwrite S once both halves are out
       if (tile_full<kMode>(a, it, kt)) {
 #pragma unroll
-        for (int k = 0; k < kTileN / 2; ++k)
+        for (int k = 0; k < kHalfKeys / 2; ++k)
           sb[k] = pack_bf16x2(__uint_as_float(sb[2 * k]), __uint_as_float(sb[2 * k + 1]));
       } else {
 #pragma unroll
-        for (int ch = 0; ch < kTileN / 32; ++ch) {
-          const uint32_t vis = chunk_visibility<kMode>(a, row, limit, kt, ch, valid);
+        for (int ch = 0; ch < kHalfKeys / 32; ++ch) {
+          const uint32_t vis = chunk_visibility<kMode>(a, row, limit, kt, 2 * hf + ch, valid);
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             // hidden keys read as -inf: weight exactly 0, never the maximum
@@ -451,20 +459,26 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
       }
 
       if (kW) {
-        if (valid && hasM) weights_tile(a, sb, h, row, kt, M, l_final);
+        if (valid && hasM) weights_half(a, sb, h, row, kt * kTileN + kHalfKeys * hf, M, l_final);
         continue;
       }
-      // tile maximum of the bf16 scores (four independent chains of pair maxima)
+      // this half's maximum of the bf16 scores, exchanged with the other half's: both halves
+      // then take the same decisions on M
       uint32_t m0 = sb[0], m1 = sb[1], m2 = sb[2], m3 = sb[3];
 #pragma unroll
-      for (int k = 4; k < kTileN / 2; k += 4) {
+      for (int k = 4; k < kHalfKeys / 2; k += 4) {
         m0 = max_bf16x2(m0, sb[k]);
         m1 = max_bf16x2(m1, sb[k + 1]);
         m2 = max_bf16x2(m2, sb[k + 2]);
         m3 = max_bf16x2(m3, sb[k + 3]);
       }
       const uint32_t mm = max_bf16x2(max_bf16x2(m0, m1), max_bf16x2(m2, m3));
-      const float mx = fmaxf(lo_f(mm), hi_f(mm));
+      const uint32_t mine = max_bf16x2(mm, mm >> 16) & 0xFFFFu;   // low half: max of both
+      sm.mx[g & 1][hf][r] = (uint16_t)mine;
+      mbar_arrive(&sm.mx_bar);
+      if (!warp_wait(&sm.mx_bar, g & 1, abort)) return;
+      const uint32_t other = sm.mx[g & 1][hf ^ 1][r];
+      const float mx = fmaxf(__uint_as_float(mine << 16), __uint_as_float(other << 16));
       bool rescale = false;
       int newM = M;
       if (mx != -INFINITY) {
@@ -479,63 +493,61 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem,
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O must hold every earlier P.V before it is scaled (the PV of global tile g-1, whose
-        // completion p_empty[1] marks; the P buffer waits below then pass at once)
+        // completion p_empty[1] marks; the P buffer wait below then passes at once). Each
+        // half scales its own 128 of O's 256 columns.
         if (!warp_wait(&sm.p_empty[1], (g - 1) & 1, abort)) return;
         tc_fence_after();
         const float f = rescale ? exp2f((float)(M - newM)) : 1.0f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kDim; c0 += 32) {
+        for (int c0 = 0; c0 < kDim / 2; c0 += 32) {
+          const uint32_t ta = tmem + kTmemO + lane_off + (kDim / 2) * hf + c0;
           uint32_t o[32];
-          tmem_ld32(tmem + kTmemO + lane_off + c0, o);
+          tmem_ld32(ta, o);
           tmem_wait_ld(o);
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-          tmem_st32(tmem + kTmemO + lane_off + c0, o);
+          tmem_st32(ta, o);
         }
         tmem_wait_st();
         l *= f;
       }
       M = newM;
       const float mf = hasM ? (float)M : 0.f;
-      // P = bf16(2^(t - M)), t = bf16(s) * log2(e) / 16, into shared memory, each 64-key
-      // half once the previous P.V has read that half; l sums the rounded P
+      // P = bf16(2^(t - M)), t = bf16(s) * log2(e) / 16, into this half's 64-key block of
+      // shared memory once the previous P.V has read it; l sums the rounded P
+      if (g > 0 && !warp_wait(&sm.p_empty[hf], (g - 1) & 1, abort)) return;
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        if (g > 0 && !warp_wait(&sm.p_empty[hb], (g - 1) & 1, abort)) return;
+      for (int cd = 0; cd < kHalfKeys / 8; ++cd) {
+        uint32_t pk[4];
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          const int cd = 8 * hb + c8;
-          uint32_t pk[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t w = sb[cd * 4 + k];
-            const float t0 = fmaf(lo_f(w), kLog2eOver16, -mf);
-            const float t1 = fmaf(hi_f(w), kLog2eOver16, -mf);
-            pk[k] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
-            if (k & 1) add_bf16x2(l2, l3, pk[k]);
-            else add_bf16x2(l0, l1, pk[k]);
-          }
-          uint8_t* dst = sm.p[hb] + sw128_offset((uint32_t)r, (uint32_t)c8);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t w = sb[cd * 4 + k];
+          const float t0 = fmaf(lo_f(w), kLog2eOver16, -mf);
+          const float t1 = fmaf(hi_f(w), kLog2eOver16, -mf);
+          pk[k] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
+          if (k & 1) add_bf16x2(l2, l3, pk[k]);
+          else add_bf16x2(l0, l1, pk[k]);
         }
-        fence_async_smem();
-        mbar_arrive(&sm.p_full[hb]);
+        uint8_t* dst = sm.p[hf] + sw128_offset((uint32_t)r, (uint32_t)cd);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       l += (l0 + l2) + (l1 + l3);
+      fence_async_smem();
+      mbar_arrive(&sm.p_full[hf]);
     }
     if (!kW) {
-      // hand l and M of this item to the edge warps
+      // hand this half's l (and M) of the item to the edge warps
       if (it_done > 0 && !warp_wait(&sm.st_empty, (it_done - 1) & 1, abort)) return;
-      sm.stat_l[r] = l;
-      sm.stat_m[r] = hasM ? (float)M : 0.f;
+      sm.stat_l[hf][r] = l;
+      if (hf == 0) sm.stat_m[r] = hasM ? (float)M : 0.f;
       mbar_arrive(&sm.st_full);
     }
     ++it_done;
   }
 }
 
-// ------------------------------------------------------------------ warps 8-11: edge
+// ------------------------------------------------------------------ warps 12-15: edge
 // The item's prepared Q tile (a ring slot: four 128-row x 64-dim blocks, 128-byte
 // swizzled) into this thread's TMEM lane at Q: row r, dims 2c and 2c+1 in column c.
 // Every lane of the warp runs it (warp-collective stores).
@@ -645,7 +657,7 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
   const bool valid = row < a.rows;
   const int h = it.h;
   if (!warp_wait(&sm.st_full, it_done & 1, abort)) return false;
-  const float l = sm.stat_l[r];
+  const float l = sm.stat_l[0][r] + sm.stat_l[1][r];
   const float M = sm.stat_m[r];
   if (!warp_wait(&sm.o_done, it_done & 1, abort)) return false;
   tc_fence_after();
@@ -695,7 +707,7 @@ __device__ bool epilogue_partial(AttnSmem& sm, const AttnArgs& a, const Item& it
                                  uint32_t lane_off, int r, uint32_t it_done, volatile int* abort) {
   const bool valid = r < kVerifyHeadsPerTile * a.vrows;
   if (!warp_wait(&sm.st_full, it_done & 1, abort)) return false;
-  const float l = sm.stat_l[r];
+  const float l = sm.stat_l[0][r] + sm.stat_l[1][r];
   const float M = sm.stat_m[r];
   if (!warp_wait(&sm.o_done, it_done & 1, abort)) return false;
   tc_fence_after();
@@ -760,7 +772,7 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
     tc_fence_before();
     mbar_arrive(&sm.q_full);
     mbar_arrive(&sm.q_read);
-    if (threadIdx.x == 256) {
+    if (threadIdx.x == kEdgeThread0) {
       if (!mbar_wait(&sm.q_read, q_takes & 1, abort)) return false;
       mbar_arrive(&sm.empty[slot]);
     }
@@ -795,9 +807,14 @@ template <int kMode, bool kW>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  AttnSmem& sm = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~uintptr_t(1023));
+  // The dynamic shared memory is declared 1024-byte aligned (the 128-byte swizzle of TMA
+  // and the MMA descriptors needs it); every thread checks it before using any of it.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_u32(smem_raw) & 1023u) != 0u) {
+    if (threadIdx.x == 0) record_abort(a.status, kDevBadLaunch);
+    return;
+  }
+  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &sm.abort;
   if (threadIdx.x == 0) {
@@ -809,17 +826,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.q_full, 128);
     mbar_init(&sm.q_empty, 1);
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, 128);
+    mbar_init(&sm.s_free, 256);       // both softmax warpgroups
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.p_full[i], 128);
       mbar_init(&sm.p_empty[i], 1);
     }
     mbar_init(&sm.o_done, 1);
     mbar_init(&sm.o_free, 128);
-    mbar_init(&sm.st_full, 128);
+    mbar_init(&sm.st_full, 256);
     mbar_init(&sm.st_empty, 128);
     mbar_init(&sm.drain, 1);
     mbar_init(&sm.q_read, 128);
+    mbar_init(&sm.mx_bar, 256);
     mbar_fence_init();
   }
   if (warp == 0 && lane == 0) {
@@ -840,10 +858,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
     if (warp == 0 && lane == 0) producer<kMode, kW>(sm, &tm_q, &tm_k, &tm_v, a, abort);
     if (warp == 1) mma_issuer<kMode, kW>(sm, a, tmem, abort);
+  } else if (warp < 12) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    softmax_worker<kMode, kW>(sm, a, tmem, (warp - 4) >> 2, abort);
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWork));
-    if (warp < 8) softmax_worker<kMode, kW>(sm, a, tmem, abort);
-    else edge_worker<kMode, kW>(sm, a, tmem, abort);
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEdge));
+    edge_worker<kMode, kW>(sm, a, tmem, abort);
   }
   tc_fence_before();
   __syncthreads();
@@ -929,7 +949,7 @@ cudaError_t launch_wait_timeout(long long limit, int* status, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-size_t attn_smem_bytes() { return sizeof(AttnSmem) + 1024; }
+size_t attn_smem_bytes() { return sizeof(AttnSmem); }
 
 cudaError_t launch_verify_combine(const AttnArgs& a, cudaStream_t s) {
   const int warps = a.n_seq * kHeads * a.vrows;
