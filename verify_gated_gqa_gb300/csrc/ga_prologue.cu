@@ -3,10 +3,12 @@
 // all twelve query heads of a KV head read the same prepared key; the query rows take
 // the same norm with w_q at their own positions).
 //
-// One warp per (token, head) row of 256 bf16: lane l holds dims 8l .. 8l+7 (one 16-byte
-// load and store, so a warp reads and writes 512 contiguous bytes). Memory-bound. Keys:
-// [T][2][256] -> [T][2][256]. Queries: the q halves of the fused rows [rows][24][512] ->
-// [rows][24][256].
+// Eight lanes per (token, head) row of 256 bf16, four rows per warp. Lane j of a row holds
+// dims 32k + 4j .. 32k + 4j + 3 for k = 0..7 (eight 8-byte loads and stores; the eight
+// lanes of a row read 64 contiguous bytes per k). The rotated pairs (d, d + 32), d < 32,
+// then sit in one lane (k = 0 and k = 1), so every lane takes part in the rotation and the
+// row's sum of squares needs three shuffle steps. Keys: [T][2][256] -> [T][2][256].
+// Queries: the q halves of the fused rows [rows][24][512] -> [rows][24][256].
 #include "ga_internal.h"
 #include "ga_numerics.cuh"
 #include "ga_sm100.cuh"
@@ -23,6 +25,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 // rows are (token, head) pairs, heads_per_tok heads per token; row `row` reads 256 values
 // at src + row * src_stride and writes 256 at dst + row * 256. Token t sits at position
 // pos_base + t, or, with kSeq, at sp.seq_base[t / sp.rows_per_seq] + t % sp.rows_per_seq.
+constexpr int kRowsPerBlock = 32;   // 8 warps x 4 rows
 template <bool kSeq>
 __global__ void __launch_bounds__(256) prologue_kernel(const uint16_t* __restrict__ src,
                                                        int src_stride, int heads_per_tok,
@@ -33,34 +36,41 @@ __global__ void __launch_bounds__(256) prologue_kernel(const uint16_t* __restric
                                                        const __grid_constant__ SeqPositions sp,
                                                        uint16_t* __restrict__ dst) {
   const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int j = lane & 7;
+  const long long row = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 3);
+  // whole row groups leave together: the shuffles below stay within a group of 8 lanes
   if (row >= n_rows) return;
+  const unsigned gmask = 0xFFu << (lane & 24);
   const long long tok = row / heads_per_tok;
   const int pos = kSeq ? sp.seq_base[tok / sp.rows_per_seq] + (int)(tok % sp.rows_per_seq)
                        : pos_base + (int)tok;
 
-  const uint4 xv = __ldg(reinterpret_cast<const uint4*>(src + row * src_stride) + lane);
-  const uint4 wv = __ldg(reinterpret_cast<const uint4*>(w_norm) + lane);
-  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-  const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-  float x[8], w[8];
+  const uint2* xs = reinterpret_cast<const uint2*>(src + row * src_stride) + j;
+  const uint2* ws = reinterpret_cast<const uint2*>(w_norm) + j;
+  uint2 xv[8], wv[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = lo_f(xw[i]);
-    x[2 * i + 1] = hi_f(xw[i]);
-    w[2 * i] = lo_f(ww[i]);
-    w[2 * i + 1] = hi_f(ww[i]);
+  for (int k = 0; k < 8; ++k) {
+    xv[k] = __ldg(xs + 8 * k);
+    wv[k] = __ldg(ws + 8 * k);
   }
-  SumSq ss;
+  // sum of squares: two independent TwoSum chains per lane, then the row's 8 lanes in a
+  // fixed order (lower lane first) so every lane of the row holds the same pair
+  SumSq s0, s1;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) ss.add(x[i]);
+  for (int k = 0; k < 8; ++k) {
+    s0.add(lo_f(xv[k].x));
+    s1.add(hi_f(xv[k].x));
+    s0.add(lo_f(xv[k].y));
+    s1.add(hi_f(xv[k].y));
+  }
+  s0.merge(s1);
+  SumSq ss = s0;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
+  for (int off = 1; off < 8; off <<= 1) {
     SumSq o;
-    o.hi = __shfl_xor_sync(0xffffffffu, ss.hi, off);
-    o.lo = __shfl_xor_sync(0xffffffffu, ss.lo, off);
-    // merge in a fixed order (lower lane first) so every lane holds the same pair
-    if (lane & off) {
+    o.hi = __shfl_xor_sync(gmask, ss.hi, off, 8);
+    o.lo = __shfl_xor_sync(gmask, ss.lo, off, 8);
+    if (j & off) {
       SumSq t = o;
       t.merge(ss);
       ss = t;
@@ -69,40 +79,44 @@ __global__ void __launch_bounds__(256) prologue_kernel(const uint16_t* __restric
     }
   }
   const InvRms r = inv_rms_df(ss);
-  float y[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = norm_elem(x[i], w[i], r);
 
-  // Partial RoPE: dims 0..31 (lanes 0..3) pair with dims 32..63 (lanes 4..7).
-  float partner[8];
+  // normed values (fp32 values whose bf16 rounding is the exact one: the fast result when
+  // it is clear of a bf16 midpoint, else the exact bf16 value itself)
+  auto norm4 = [&](int k, float (&y)[4]) {
+    const float xk[4] = {lo_f(xv[k].x), hi_f(xv[k].x), lo_f(xv[k].y), hi_f(xv[k].y)};
+    const float wk[4] = {lo_f(wv[k].x), hi_f(wv[k].x), lo_f(wv[k].y), hi_f(wv[k].y)};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) partner[i] = __shfl_xor_sync(0xffffffffu, y[i], 4);
-  if (lane < 8) {
-    const int pair0 = (lane & 3) * 8;  // pair index of this lane's first dim
-    const uint4 cv = __ldg(reinterpret_cast<const uint4*>(cos_tab + (long long)pos * kHalfRot + pair0));
-    const uint4 sv = __ldg(reinterpret_cast<const uint4*>(sin_tab + (long long)pos * kHalfRot + pair0));
-    const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float c = (i & 1) ? hi_f(cw[i >> 1]) : lo_f(cw[i >> 1]);
-      const float s = (i & 1) ? hi_f(sw[i >> 1]) : lo_f(sw[i >> 1]);
-      float ya, yb;
-      if (lane < 4) {
-        rope_pair(y[i], partner[i], c, s, ya, yb);
-        y[i] = ya;
-      } else {
-        rope_pair(partner[i], y[i], c, s, ya, yb);
-        y[i] = yb;
-      }
+    for (int i = 0; i < 4; ++i) {
+      y[i] = norm_fast(xk[i], wk[i], r);
+      if (near_bf16_midpoint(y[i], 3)) y[i] = norm_elem_exact(xk[i], wk[i], r.h, r.l);
     }
+  };
+  uint2* out = reinterpret_cast<uint2*>(dst + row * kDim) + j;
+  {
+    // Partial RoPE on dims 0..63: pair p = 4j + i is (dim p, dim p + 32), both in this lane.
+    float ya[4], yb[4];
+    norm4(0, ya);
+    norm4(1, yb);
+    const uint2 cv = __ldg(reinterpret_cast<const uint2*>(cos_tab + (long long)pos * kHalfRot) + j);
+    const uint2 sv = __ldg(reinterpret_cast<const uint2*>(sin_tab + (long long)pos * kHalfRot) + j);
+    const float c[4] = {lo_f(cv.x), hi_f(cv.x), lo_f(cv.y), hi_f(cv.y)};
+    const float sn[4] = {lo_f(sv.x), hi_f(sv.x), lo_f(sv.y), hi_f(sv.y)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float oa, ob;
+      rope_pair(bf16_round(ya[i]), bf16_round(yb[i]), c[i], sn[i], oa, ob);
+      ya[i] = oa;
+      yb[i] = ob;
+    }
+    out[0] = make_uint2(pack2(ya[0], ya[1]), pack2(ya[2], ya[3]));
+    out[8] = make_uint2(pack2(yb[0], yb[1]), pack2(yb[2], yb[3]));
   }
-  uint4 o;
-  o.x = pack2(y[0], y[1]);
-  o.y = pack2(y[2], y[3]);
-  o.z = pack2(y[4], y[5]);
-  o.w = pack2(y[6], y[7]);
-  reinterpret_cast<uint4*>(dst + row * kDim)[lane] = o;
+#pragma unroll
+  for (int k = 2; k < 8; ++k) {
+    float y[4];
+    norm4(k, y);
+    out[8 * k] = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+  }
 }
 
 }  // namespace
@@ -112,7 +126,7 @@ cudaError_t launch_k_prologue(const uint16_t* k_raw, const uint16_t* w_k, const 
                               int* status, cudaStream_t s) {
   (void)status;
   const long long n_rows = (long long)n_tok * kKvHeads;
-  const unsigned grid = (unsigned)((n_rows + 7) / 8);
+  const unsigned grid = (unsigned)((n_rows + kRowsPerBlock - 1) / kRowsPerBlock);
   prologue_kernel<false><<<grid, 256, 0, s>>>(k_raw, kDim, kKvHeads, w_k, cos_tab, sin_tab,
                                               n_rows, pos_base, SeqPositions{}, k_prep);
   return cudaGetLastError();
@@ -122,7 +136,7 @@ cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uin
                               const uint16_t* sin_tab, int rows, int q_base, uint16_t* q_prep,
                               cudaStream_t s) {
   const long long n_rows = (long long)rows * kHeads;
-  const unsigned grid = (unsigned)((n_rows + 7) / 8);
+  const unsigned grid = (unsigned)((n_rows + kRowsPerBlock - 1) / kRowsPerBlock);
   prologue_kernel<false><<<grid, 256, 0, s>>>(qg, kQgStride, kHeads, w_q, cos_tab, sin_tab,
                                               n_rows, q_base, SeqPositions{}, q_prep);
   return cudaGetLastError();
@@ -132,7 +146,7 @@ cudaError_t launch_q_prologue_seq(const uint16_t* qg, const uint16_t* w_q, const
                                   const uint16_t* sin_tab, int n_tok, const SeqPositions& sp,
                                   uint16_t* q_prep, cudaStream_t s) {
   const long long n_rows = (long long)n_tok * kHeads;
-  const unsigned grid = (unsigned)((n_rows + 7) / 8);
+  const unsigned grid = (unsigned)((n_rows + kRowsPerBlock - 1) / kRowsPerBlock);
   prologue_kernel<true><<<grid, 256, 0, s>>>(qg, kQgStride, kHeads, w_q, cos_tab, sin_tab, n_rows,
                                              0, sp, q_prep);
   return cudaGetLastError();
