@@ -350,7 +350,9 @@ def run_verify(args, world, rank, local):
                                "and combine",
                    "l2": f"K/V caches {2 * V_SEQ * V_CAP * KV_HEADS * DIM * 2 / 1e9:.2f} GB"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
-                     "frac": round(gbs / peak_hbm, 4), "traffic": None,
+                     "frac": round(gbs / peak_hbm, 4),
+                     "traffic": VERIFY_ATTN_TRAFFIC_BYTES if V_SEQ == 8 else None,
+                     "traffic_kernel": "attn_kernel (verify variant), the call's dominant launch",
                      "peak_kind": f"HBM copy ({peak_src})",
                      "kernel": "ga_attn_verify (Q prologue + attn_kernel<verify> + combine)",
                      "algorithmic_bytes": V_BYTES},
@@ -358,10 +360,13 @@ def run_verify(args, world, rank, local):
     }
 
 
-# Per-launch DRAM bytes of attn_kernel (dram__bytes_read.sum + dram__bytes_write.sum: 218.61
-# + 57.80 MB) from the ncu capture summarised in profiles/attn_kernel_causal_s8192.md; to be
-# set to None whenever the kernel changes until it is captured again.
-ATTN_TRAFFIC_BYTES = 276_409_856
+# Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
+# summarised in profiles/attn_kernel_causal_s8192.md (218,586,880 + 57,809,920) and
+# profiles/attn_kernel_verify_8x16_l65536.md (1,077,402,880 + 18,394,112, the verify
+# variant of attn_kernel); each is to be set to None whenever its kernel changes until it is
+# captured again.
+ATTN_TRAFFIC_BYTES = 276_396_800
+VERIFY_ATTN_TRAFFIC_BYTES = 1_095_796_992
 
 
 # ---------------------------------------------------------------- the oracle as baseline
