@@ -206,34 +206,56 @@ def run_gpu(args, world, rank, local):
     attn_ms = statistics.mean(ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps))
     status = B.ga_device_status()
 
-    # end to end through the C ABI with host buffers: H2D of the step's inputs, the two
-    # public calls (ga_k_prologue, ga_attn_prefill), D2H of the output, every step
+    # end to end through the C ABI with host buffers: every step copies its inputs from
+    # pinned host memory (H2D), runs the two public calls (ga_k_prologue, ga_attn_prefill)
+    # and reads its output back into pinned host memory (D2H). Steps are pipelined on three
+    # streams with double-buffered device inputs and outputs, as a serving loop would run
+    # them: step i+1's inputs travel while step i computes and step i-1's output returns.
     host_in = [t.cpu().pin_memory() for t in (qg, k, v, w_q, w_k, cos, sin)]
-    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dev_in = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(2)]
+    outs = [out, torch.empty_like(out)]
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     e2e_steps = max(3, min(args.steps, 20))
+    h_stream, c_stream, d_stream = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_step():
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
-        qg_d, k_d, v_d, wq_d, wk_d, cos_d, sin_d = dev_in
-        B.ga_k_prologue(k_d, wk_d, cos_d, sin_d, k_prep=k_prep)
-        B.ga_attn_prefill(qg_d, k_prep, v_d, wq_d, cos_d, sin_d, 0, S, out=out)
-        host_out.copy_(out, non_blocking=True)
+    def e2e_run(n):
+        h_done = [torch.cuda.Event() for _ in range(n)]
+        c_done = [torch.cuda.Event() for _ in range(n)]
+        d_done = [torch.cuda.Event() for _ in range(n)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        h_stream.wait_event(start)
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(h_stream):
+                if i >= 2:
+                    h_stream.wait_event(c_done[i - 2])   # buffer b's inputs are consumed
+                for h, d in zip(host_in, dev_in[b]):
+                    d.copy_(h, non_blocking=True)
+                h_done[i].record(h_stream)
+            with torch.cuda.stream(c_stream):
+                c_stream.wait_event(h_done[i])
+                if i >= 2:
+                    c_stream.wait_event(d_done[i - 2])   # buffer b's output was read back
+                qg_d, k_d, v_d, wq_d, wk_d, cos_d, sin_d = dev_in[b]
+                B.ga_k_prologue(k_d, wk_d, cos_d, sin_d, k_prep=k_prep)
+                B.ga_attn_prefill(qg_d, k_prep, v_d, wq_d, cos_d, sin_d, 0, S, out=outs[b])
+                c_done[i].record(c_stream)
+            with torch.cuda.stream(d_stream):
+                d_stream.wait_event(c_done[i])
+                host_out[b].copy_(outs[b], non_blocking=True)
+                d_done[i].record(d_stream)
+        stream.wait_event(d_done[n - 1])
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
 
-    e2e_step()
-    torch.cuda.synchronize()
+    e2e_run(2)
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
+    e2e_ms = max_over_ranks(e2e_run(e2e_steps), world, dev) / e2e_steps
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
 
     if rank != 0:
         return None
@@ -260,7 +282,9 @@ def run_gpu(args, world, rank, local):
                      "kernel": "attn_kernel", "algorithmic_flops": FLOPS_STEP},
         "e2e": {"value": round(world * FLOPS_STEP / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4)},
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "schedule": "H2D, compute (ga_k_prologue + ga_attn_prefill) and D2H on three "
+                            "streams, device inputs and outputs double-buffered"},
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "device_status": status,
