@@ -679,7 +679,7 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
         for (int k = 0; k < 4; ++k) {
           const uint32_t ob = pack_bf16x2(__uint_as_float(o[8 * i + 2 * k]) * inv,
                                           __uint_as_float(o[8 * i + 2 * k + 1]) * inv);
-          w[k] = pack_bf16x2(lo_f(ob) * lo_f(sw[k]), hi_f(ob) * hi_f(sw[k]));
+          w[k] = mul_bf16x2(ob, sw[k]);   // bf16(o * s), o and s already bf16
         }
         if (valid) op[8 * c + 4 * half + i] = make_uint4(w[0], w[1], w[2], w[3]);
       }
@@ -924,7 +924,7 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_consta
     if (!sigmoid_fast(hi_f(gw[k]), s1)) s1 = __uint_as_float((uint32_t)g_sigmoid_bf16[gw[k] >> 16] << 16);
     const uint32_t ob = pack_bf16x2(o[2 * k] * inv, o[2 * k + 1] * inv);
     const uint32_t sp = pack_bf16x2(s0, s1);
-    res[k] = pack_bf16x2(lo_f(ob) * lo_f(sp), hi_f(ob) * hi_f(sp));
+    res[k] = mul_bf16x2(ob, sp);
   }
   reinterpret_cast<uint4*>(a.out + row * kOutRow + h * kDim)[lane] = make_uint4(res[0], res[1], res[2], res[3]);
 }

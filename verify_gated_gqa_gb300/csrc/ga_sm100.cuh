@@ -284,6 +284,14 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // ------------------------------------------------------------------ small helpers
 // Pack two floats into bf16x2 (round to nearest even): lo -> bits 0..15, hi -> 16..31.
+// Two bf16 products, each the exact product rounded once to bf16: the same bits as the
+// fp32 product (exact for two bf16 values) converted to bf16 (checked on the device over
+// every pair of non-NaN bf16 values).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
