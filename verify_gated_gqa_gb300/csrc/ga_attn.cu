@@ -20,11 +20,13 @@
 // Structure (one CTA per SM, persistent, 512 threads in four warpgroups):
 //   warp 0     TMA producer: K and V tiles of 128 keys x 256 dims (64 KiB, four 16 KiB
 //              128-byte-swizzled column blocks) through three tile slots;
-//   warp 1     allocates the 512 TMEM columns and issues every tcgen05.mma, all at full
-//              rate (N >= 128): S = Q K^T (M=128, N=128, K=256; Q read from TMEM), then
-//              O += P V (M=128, N=256, K=128; P from shared memory, V MN-major). The
-//              whole warp runs the issue loop and one elected lane issues: a lone lane in
-//              a divergent branch issued too slowly to keep the N=128 MMAs back to back;
+//   warp 1     allocates the 512 TMEM columns and issues every S = Q K^T (M=128, N=128,
+//              K=256; Q read from TMEM);
+//   warp 2     issues every O += P V (M=128, N=256, K=128; P from shared memory, V
+//              MN-major), so a tile's P V need not wait behind the next tile's Q K^T
+//              issue. Both at full rate (N >= 128); in each, the whole warp runs the issue
+//              loop and one elected lane issues (a lone lane in a divergent branch issued
+//              too slowly to keep the N=128 MMAs back to back);
 //   warps 4-11 softmax, two warpgroups, one per 64-key half of each S tile, one query row
 //              per thread: S is copied to registers and its TMEM columns released at once
 //              (so the next S = Q K^T overlaps this softmax); the two halves exchange their
@@ -86,7 +88,7 @@ struct AttnSmem {
   uint64_t full[kSlots], empty[kSlots];
   uint64_t q_full, q_empty, s_full, s_free;
   uint64_t p_full[2], p_empty[2];     // per 64-key half of P
-  uint64_t o_done, o_free, st_full, st_empty, drain, q_read, mx_bar;
+  uint64_t o_done, o_free, st_full, st_empty, drain, drain_pv, q_read, mx_bar;
   uint32_t tmem_base;
   int abort;
 };
@@ -246,62 +248,49 @@ __device__ void producer(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMa
   }
 }
 
-// ------------------------------------------------------------------ warp 1: MMA issuer
-template <int kMode, bool kW>
-__device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
-  constexpr uint32_t kIdQK = idesc_bf16(128, kTileN, false, false);
-  constexpr uint32_t kIdPV = idesc_bf16(128, kDim, false, true);
-  const uint32_t p_addr = smem_u32(sm.p[0]);
-  const uint64_t p_desc0 = sdesc_sw128(p_addr, 16, 1024);
-  const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), kChunkBytes, 1024);
-  const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), 16, 1024);
-  uint32_t cnt = 0;       // tile-slot sequence (same order as the producer)
-  uint32_t g = 0;         // global key-tile counter: S, P and PV phases
-  uint32_t it_done = 0;
-
-  auto take = [&](uint32_t& slot) -> bool {
+// ------------------------------------------------------------------ warps 1-2: MMA issuers
+// Two issuing warps share the tensor pipe: warp 1 issues every S = Q K^T and warp 2 every
+// O += P V, so a tile's P V enters the pipe as soon as its P is written even while the next
+// tile's Q K^T is still being issued. Each warp walks the whole tile ring in order, waiting
+// for every fill (also those it does not use): a parity wait is only safe when the slot's
+// previous fill is known to have landed, and walking in order guarantees it. A slot is
+// refilled only when every walker has passed it (each arrives on the slot's empty barrier
+// once it has seen the fill) and its consumer has released it (tcgen05.commit for K and V,
+// the edge warps for Q), so no walker can miss a fill. A warp's commits track only its own
+// MMAs (a commit covers the MMAs its thread issued).
+// Ring order per item: Q, K0, then K_j, V_{j-1} for j >= 1, then V_{n-1} (Q and K only in
+// the weights pass).
+struct RingWalk {
+  uint32_t cnt = 0;
+  // wait for the next fill in ring order (its slot in `slot`) and count this warp as past it
+  __device__ __forceinline__ bool next(AttnSmem& sm, volatile int* abort, uint32_t& slot) {
     slot = cnt % kSlots;
-    if (!warp_wait(&sm.full[slot], (cnt / kSlots) & 1, abort)) return false;
-    tc_fence_after();
+    const bool ok = warp_wait(&sm.full[slot], (cnt / kSlots) & 1, abort);
     ++cnt;
-    return true;
-  };
-  auto issue_pv = [&](int j, uint32_t gj) -> bool {
-    uint32_t slot;
-    if (!take(slot)) return false;
-    if (j == 0 && it_done > 0 && !warp_wait(&sm.o_free, (it_done - 1) & 1, abort)) return false;
-    // descriptors advance by constants (addresses in 16-byte units in the low field):
-    // P by 32 bytes per k-step inside a 64-key block and 16 KiB per block, V by 2 KiB.
-    // The two 64-key halves of P go separately: the softmax writes the next tile's first
-    // half while this tile's second half is still being read.
-    const uint64_t bd0 = v_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
-#pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-      if (!warp_wait(&sm.p_full[hb], gj & 1, abort)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const int kk = 4 * hb + k4;
-        const uint64_t ad = p_desc0 + (uint64_t)(hb * (kChunkBytes >> 4) + k4 * 2);
-        umma_ss_warp(tmem + kTmemO, ad, bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      // p_empty[1] also tells the softmax that O holds every P V so far
-      umma_commit_warp(&sm.p_empty[hb]);
-    }
-    umma_commit_warp(&sm.empty[slot]);
-    return true;
-  };
+    if (ok && (threadIdx.x & 31) == 0) mbar_arrive(&sm.empty[slot]);
+    return ok;
+  }
+};
 
+// descriptors advance by constants (addresses in 16-byte units in the low field): K by
+// 32 bytes per k-step inside a 64-dim block and 16 KiB per block; P by 32 bytes per k-step
+// inside a 64-key block and 16 KiB per block; V by 2 KiB per k-step; a slot is 64 KiB.
+template <int kMode, bool kW>
+__device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
+  constexpr uint32_t kIdQK = idesc_bf16(128, kTileN, false, false);
+  const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), 16, 1024);
+  RingWalk ring;
+  uint32_t g = 0;         // global key-tile counter: S phases
+  uint32_t it_done = 0;
+  uint32_t slot;
   ItemWalk<kMode> walk;
   Item it;
   while (walk.next(a, it)) {
-    ++cnt;   // the item's Q tile: consumed by the edge warps
+    if (!ring.next(sm, abort, slot)) return;            // the item's Q tile (edge warps)
     if (!warp_wait(&sm.q_full, it_done & 1, abort)) return;
-    tc_fence_after();
     for (int j = 0; j < it.n; ++j, ++g) {
-      uint32_t slot;
-      if (!take(slot)) return;
+      if (!kW && j >= 2 && !ring.next(sm, abort, slot)) return;   // V_{j-2}
+      if (!ring.next(sm, abort, slot)) return;          // K_j
       // S is free once the softmax warps have copied the previous tile's S out
       if (g > 0 && !warp_wait(&sm.s_free, (g - 1) & 1, abort)) return;
       tc_fence_after();
@@ -314,12 +303,53 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
       umma_commit_warp(&sm.empty[slot]);
       umma_commit_warp(&sm.s_full);
       if (j == it.n - 1) umma_commit_warp(&sm.q_empty);
-      if (!kW && j >= 1 && !issue_pv(j - 1, g - 1)) return;
     }
     if (!kW) {
-      if (!issue_pv(it.n - 1, g - 1)) return;
-      umma_commit_warp(&sm.o_done);
+      if (it.n >= 2 && !ring.next(sm, abort, slot)) return;   // V_{n-2}
+      if (!ring.next(sm, abort, slot)) return;                // V_{n-1}
     }
+    ++it_done;
+  }
+}
+
+template <int kMode>
+__device__ void pv_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
+  constexpr uint32_t kIdPV = idesc_bf16(128, kDim, false, true);
+  const uint64_t p_desc0 = sdesc_sw128(smem_u32(sm.p[0]), 16, 1024);
+  const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), kChunkBytes, 1024);
+  RingWalk ring;
+  uint32_t g = 0;         // global key-tile counter: P and P V phases
+  uint32_t it_done = 0;
+  uint32_t slot;
+  ItemWalk<kMode> walk;
+  Item it;
+  while (walk.next(a, it)) {
+    if (!ring.next(sm, abort, slot)) return;            // Q
+    if (!ring.next(sm, abort, slot)) return;            // K0
+    for (int j = 0; j < it.n; ++j, ++g) {
+      if (j + 1 < it.n && !ring.next(sm, abort, slot)) return;   // K_{j+1}
+      if (!ring.next(sm, abort, slot)) return;                   // V_j
+      if (j == 0 && it_done > 0 && !warp_wait(&sm.o_free, (it_done - 1) & 1, abort)) return;
+      const uint64_t bd0 = v_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
+      // The two 64-key halves of P go separately: each softmax warpgroup writes its half
+      // of the next tile as soon as this tile's P V has read that half.
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        if (!warp_wait(&sm.p_full[hb], g & 1, abort)) return;
+        tc_fence_after();
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * hb + k4;
+          const uint64_t ad = p_desc0 + (uint64_t)(hb * (kChunkBytes >> 4) + k4 * 2);
+          umma_ss_warp(tmem + kTmemO, ad, bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        // p_empty[1] also tells the softmax that O holds every P V so far
+        umma_commit_warp(&sm.p_empty[hb]);
+      }
+      umma_commit_warp(&sm.empty[slot]);
+    }
+    umma_commit_warp(&sm.o_done);
     ++it_done;
   }
 }
@@ -327,10 +357,17 @@ __device__ void mma_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatil
 // Issue every MMA, then wait (bounded) until all of them completed, so that tensor
 // memory is never released under an MMA in flight.
 template <int kMode, bool kW>
-__device__ void mma_issuer(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
-  mma_loop<kMode, kW>(sm, a, tmem, abort);
-  umma_commit_warp(&sm.drain);
-  mbar_wait_quiet(&sm.drain, 0, 100000000LL);
+__device__ void mma_issuer(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort,
+                           bool pv_warp) {
+  uint64_t* drain = pv_warp ? &sm.drain_pv : &sm.drain;
+  if (pv_warp) {
+    if (kW) return;   // the weights pass has no P V
+    pv_loop<kMode>(sm, a, tmem, abort);
+  } else {
+    qk_loop<kMode, kW>(sm, a, tmem, abort);
+  }
+  umma_commit_warp(drain);
+  mbar_wait_quiet(drain, 0, 100000000LL);
 }
 
 // ------------------------------------------------------------------ shared helpers
@@ -821,7 +858,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.abort = 0;
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], 1);
+      // refilled once both MMA warps have passed the fill and its consumer released it
+      // (weights pass: the score warp alone walks the ring)
+      mbar_init(&sm.empty[i], kW ? 2 : 3);
     }
     mbar_init(&sm.q_full, 128);
     mbar_init(&sm.q_empty, 1);
@@ -836,6 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.st_full, 256);
     mbar_init(&sm.st_empty, 128);
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.drain_pv, 1);
     mbar_init(&sm.q_read, 128);
     mbar_init(&sm.mx_bar, 256);
     mbar_fence_init();
@@ -857,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
     if (warp == 0 && lane == 0) producer<kMode, kW>(sm, &tm_q, &tm_k, &tm_v, a, abort);
-    if (warp == 1) mma_issuer<kMode, kW>(sm, a, tmem, abort);
+    if (warp == 1 || warp == 2) mma_issuer<kMode, kW>(sm, a, tmem, abort, warp == 2);
   } else if (warp < 12) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     softmax_worker<kMode, kW>(sm, a, tmem, (warp - 4) >> 2, abort);
