@@ -19,7 +19,8 @@
 //
 // Structure (one CTA per SM, persistent, 512 threads in four warpgroups):
 //   warp 0     TMA producer: K and V tiles of 128 keys x 256 dims (64 KiB, four 16 KiB
-//              128-byte-swizzled column blocks) through three tile slots;
+//              128-byte-swizzled column blocks) through three tile slots (the whole warp
+//              runs the loop, one elected lane issues the copies);
 //   warp 1     allocates the 512 TMEM columns and issues every S = Q K^T (M=128, N=128,
 //              K=256; Q read from TMEM);
 //   warp 2     issues every O += P V (M=128, N=256, K=128; P from shared memory, V
@@ -201,13 +202,15 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
   // next slot; a verify Q tile holds 6 heads x vrows rows
   auto load_tile = [&](const CUtensorMap* map, int head, int r0, int seq, uint32_t bytes) -> bool {
     const uint32_t slot = cnt % kSlots;
-    if (!mbar_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
-    mbar_expect_tx(&sm.full[slot], bytes);
+    if (!warp_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
+    mbar_expect_tx_warp(&sm.full[slot], bytes);
+#pragma unroll
     for (int c = 0; c < 4; ++c) {
       if (seq < 0)
-        tma_load_3d(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0);
+        tma_load_3d_warp(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0);
       else
-        tma_load_4d(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0, seq);
+        tma_load_4d_warp(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0,
+                         seq);
     }
     ++cnt;
     return true;
@@ -896,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
-    if (warp == 0 && lane == 0) producer<kMode, kW>(sm, &tm_q, &tm_k, &tm_v, a, abort);
+    if (warp == 0) producer<kMode, kW>(sm, &tm_q, &tm_k, &tm_v, a, abort);
     if (warp == 1 || warp == 2) mma_issuer<kMode, kW>(sm, a, tmem, abort, warp == 2);
   } else if (warp < 12) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
