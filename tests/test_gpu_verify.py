@@ -91,3 +91,24 @@ def test_verify_long_cache_sampled():
     refs = _refs(data, lens, cap, heads=heads)
     for b in range(2):
         refs[b].check(out[b], what=f"verify L=65536 seq {b} heads {heads}")
+
+
+def test_verify_single_sequence():
+    """One sequence per call, 7 rows (the key/value map keeps its sequence dimension)."""
+    lens, rows, cap = [900], 7, 912
+    out, data, kd, _ = _run(SEED + 33, lens, rows, cap)
+    _refs(data, lens, cap)[0].check(out[0], what="verify, one sequence of 7 rows")
+
+
+def test_verify_65_sequences_two_groups():
+    """65 sequences of 4 rows: one launch for the first 64 sequences and one for the last
+    alone; ragged lengths from 0 to 299 (including L = 0)."""
+    n = 65
+    rng = np.random.default_rng(34)
+    lens = [int(x) for x in rng.integers(0, 300, n)]
+    lens[5] = 0
+    rows, cap = 4, 320
+    out, data, kd, _ = _run(SEED + 34, lens, rows, cap)
+    for b in (0, 5, 31, 63, 64):
+        sub = tuple(x[b:b + 1] for x in data[:3]) + tuple(data[3:])
+        _refs(sub, [lens[b]], cap)[0].check(out[b], what=f"verify, 65 sequences, seq {b}")

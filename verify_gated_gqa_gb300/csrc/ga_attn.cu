@@ -198,19 +198,24 @@ template <int kMode, bool kW>
 __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, const AttnArgs& a, volatile int* abort,
                               uint32_t& cnt) {
-  // one tile (four 64-dim boxes) at coordinates (head, row/key r0[, sequence]) into the
-  // next slot; a verify Q tile holds 6 heads x vrows rows
-  auto load_tile = [&](const CUtensorMap* map, int head, int r0, int seq, uint32_t bytes) -> bool {
+  // One tile into the next slot. A Q tile is four 64-dim boxes at (dim, head, row r0), a
+  // verify Q tile 6 heads x vrows rows per box; a K or V tile is one copy of all four
+  // 64-dim blocks (the key/value map lists the block index as its outermost dimension, so
+  // the box lands as four consecutive 16 KiB blocks) at (0, key r0, head, 0[, sequence]).
+  auto load_tile = [&](const CUtensorMap* map, bool kv, int head, int r0, int seq,
+                       uint32_t bytes) -> bool {
     const uint32_t slot = cnt % kSlots;
     if (!warp_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
     mbar_expect_tx_warp(&sm.full[slot], bytes);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    if (kv) {
       if (seq < 0)
-        tma_load_3d_warp(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0);
+        tma_load_4d_warp(sm.tile[slot], map, &sm.full[slot], 0, r0, head, 0);
       else
-        tma_load_4d_warp(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0,
-                         seq);
+        tma_load_5d_warp(sm.tile[slot], map, &sm.full[slot], 0, r0, head, 0, seq);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tma_load_3d_warp(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0);
     }
     ++cnt;
     return true;
@@ -224,17 +229,17 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
     // (K_j, V_{j-1}) for j >= 1, V_{n-1}.
     const int kv_seq = kMode == kModeVerify ? it.seq : -1;
     if (kMode == kModeVerify) {
-      if (!load_tile(tm_q, it.h, it.seq * a.vrows, -1,
+      if (!load_tile(tm_q, false, it.h, it.seq * a.vrows, -1,
                      4u * kVerifyHeadsPerTile * a.vrows * 128u)) return;
     } else {
-      if (!load_tile(tm_q, it.h, it.mt * kTileM, -1, kTileBytes)) return;
+      if (!load_tile(tm_q, false, it.h, it.mt * kTileM, -1, kTileBytes)) return;
     }
-    if (!load_tile(tm_k, kvh, ck.next(0) * kTileN, kv_seq, kTileBytes)) return;
+    if (!load_tile(tm_k, true, kvh, ck.next(0) * kTileN, kv_seq, kTileBytes)) return;
     for (int j = 1; j < it.n; ++j) {
-      if (!load_tile(tm_k, kvh, ck.next(j) * kTileN, kv_seq, kTileBytes)) return;
-      if (!kW && !load_tile(tm_v, kvh, cv.next(j - 1) * kTileN, kv_seq, kTileBytes)) return;
+      if (!load_tile(tm_k, true, kvh, ck.next(j) * kTileN, kv_seq, kTileBytes)) return;
+      if (!kW && !load_tile(tm_v, true, kvh, cv.next(j - 1) * kTileN, kv_seq, kTileBytes)) return;
     }
-    if (!kW && !load_tile(tm_v, kvh, cv.next(it.n - 1) * kTileN, kv_seq, kTileBytes)) return;
+    if (!kW && !load_tile(tm_v, true, kvh, cv.next(it.n - 1) * kTileN, kv_seq, kTileBytes)) return;
   }
 }
 

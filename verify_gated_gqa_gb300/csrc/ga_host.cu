@@ -118,18 +118,25 @@ int get_encode(EncodeTiledFn* fn) {
   return g_encode ? GA_OK : GA_ERR_DEVICE;
 }
 
-// [n_outer][n_tok][2][256] bf16 keys or values as a TMA tensor: box = 64 dims x 1 head x
-// 128 tokens, 128-byte swizzle; tokens past the end read as zeros.
-int encode_kv_map(CUtensorMap* map, const void* base, long long n_tok, long long n_outer) {
+// [n_outer][n_tok][2][256] bf16 keys or values as a TMA tensor: box = 64 dims x 128 tokens
+// x 1 head x 4 blocks of 64 dims, 128-byte swizzle; tokens past the end read as zeros. With
+// seq_dim the sequence is the fifth coordinate (verify caches, n_outer >= 1 sequences);
+// without it the map has four dimensions (n_outer must be 1).
+int encode_kv_map(CUtensorMap* map, const void* base, long long n_tok, long long n_outer,
+                  bool seq_dim) {
   EncodeTiledFn enc;
   int st = get_encode(&enc);
   if (st != GA_OK) return st;
-  cuuint64_t dims[4] = {(cuuint64_t)kDim, (cuuint64_t)kKvHeads, (cuuint64_t)n_tok, (cuuint64_t)n_outer};
-  cuuint64_t strides[3] = {(cuuint64_t)kDim * 2, (cuuint64_t)kKvHeads * kDim * 2,
+  // dims (64 dims of a block, token, head, block of 64 dims[, sequence]): the block index
+  // is listed after the token so one box of 64 x 128 x 1 x 4 lands as four consecutive
+  // [128 keys][64 dims] blocks, the layout the tensor cores read
+  cuuint64_t dims[5] = {64, (cuuint64_t)n_tok, (cuuint64_t)kKvHeads, (cuuint64_t)(kDim / 64),
+                        (cuuint64_t)n_outer};
+  cuuint64_t strides[4] = {(cuuint64_t)kKvHeads * kDim * 2, (cuuint64_t)kDim * 2, 64 * 2,
                            (cuuint64_t)n_tok * kKvHeads * kDim * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTileN, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  const cuuint32_t rank = n_outer > 1 ? 4 : 3;
+  cuuint32_t box[5] = {64, (cuuint32_t)kTileN, 1, (cuuint32_t)(kDim / 64), 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  const cuuint32_t rank = seq_dim ? 5 : 4;
   CUresult r = GA_CUDA(enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
                            dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -245,9 +252,9 @@ int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const v
   CUtensorMap tm_q, tm_k, tm_v;
   int st = encode_q_map(&tm_q, q_prep, a0.rows);
   if (st != GA_OK) return st;
-  st = encode_kv_map(&tm_k, k_prep, n_tok, 1);
+  st = encode_kv_map(&tm_k, k_prep, n_tok, 1, false);
   if (st != GA_OK) return st;
-  st = encode_kv_map(&tm_v, v, n_tok, 1);
+  st = encode_kv_map(&tm_v, v, n_tok, 1, false);
   if (st != GA_OK) return st;
   AttnArgs a = a0;
   a.status = dev->status_word;
@@ -555,9 +562,9 @@ int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_c
     CUtensorMap tm_q, tm_k, tm_v;
     st = encode_q_map(&tm_q, a.out, (long long)n * rows, kVerifyHeadsPerTile, rows);
     if (st != GA_OK) return st;
-    st = encode_kv_map(&tm_k, k_cache + (size_t)g0 * seq_elems, cap, n);
+    st = encode_kv_map(&tm_k, k_cache + (size_t)g0 * seq_elems, cap, n, true);
     if (st != GA_OK) return st;
-    st = encode_kv_map(&tm_v, v_cache + (size_t)g0 * seq_elems, cap, n);
+    st = encode_kv_map(&tm_v, v_cache + (size_t)g0 * seq_elems, cap, n, true);
     if (st != GA_OK) return st;
     const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
     if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, a, grid, s))) != cudaSuccess) return fail_cuda(e);

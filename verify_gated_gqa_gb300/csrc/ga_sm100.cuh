@@ -147,6 +147,17 @@ __device__ __forceinline__ void tma_load_4d_warp(void* dst, const CUtensorMap* m
       "r"(c3)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_5d_warp(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                 int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];\n\t}\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(c4)
+      : "memory");
+}
 
 // ------------------------------------------------------------------ tcgen05: TMEM
 // Allocation and deallocation are warp-wide; the allocated base lands in *slot.
