@@ -18,9 +18,10 @@
 // not depend on which tile or window computes it.
 //
 // Structure (one CTA per SM, persistent, 512 threads in four warpgroups):
-//   warp 0     TMA producer: K and V tiles of 128 keys x 256 dims (64 KiB, four 16 KiB
-//              128-byte-swizzled column blocks) through three tile slots (the whole warp
-//              runs the loop, one elected lane issues the copies);
+//   warp 0     TMA producer: each item's prepared Q tile and gate tile (the gate halves of
+//              its fused rows), then its K and V tiles of 128 keys x 256 dims (64 KiB, four
+//              16 KiB 128-byte-swizzled column blocks), through three tile slots (the whole
+//              warp runs the loop, one elected lane issues the copies);
 //   warp 1     allocates the 512 TMEM columns and issues every S = Q K^T (M=128, N=128,
 //              K=256; Q read from TMEM);
 //   warp 2     issues every O += P V (M=128, N=256, K=128; P from shared memory, V
@@ -35,11 +36,11 @@
 //              goes to shared memory, each half its own 64 keys (and the tensor cores read
 //              each half as soon as it is written), and each half rescales its half of O
 //              when needed;
-//   warps 12-15 the edge of each work item: the gate sigmoids of the current item while
-//              its tiles run, the next item's prepared Q tile (normed and rotated by the
-//              query prologue, delivered through the tile ring) into TMEM as soon as the
-//              current item's last S = Q K^T has read Q, then the gated epilogue of the
-//              current item.
+//   warps 12-15 the edge of each work item: the current item's gate tile from its ring
+//              slot into registers and its bf16 sigmoids while the item's tiles run, the
+//              next item's prepared Q tile (normed and rotated by the query prologue) into
+//              TMEM as soon as the current item's last S = Q K^T has read Q, then the gated
+//              epilogue of the current item.
 // The edge code is kept in short loops: the four roles run different code at once and
 // share the SM's instruction cache, which long unrolled sequences would overflow.
 // Tensor memory (512 columns x 128 lanes, lane = query row): O [0, 256) fp32, Q
@@ -78,6 +79,11 @@ constexpr uint32_t kTmemS = 384;    // S: 128 columns (fp32)
 constexpr float kLog2eOver16 = 1.4426950408889634f / 16.0f;
 constexpr int kLazyRescale = 8;     // rescale when the tile maximum exceeds M by > 2^8
 
+// Items of the gated passes (causal, bidirectional, stored mask) carry a gate tile in the
+// ring; the weights pass and the verify partials have no gated epilogue.
+template <int kMode, bool kW>
+__host__ __device__ constexpr bool has_gate() { return !kW && kMode != kModeVerify; }
+
 static_assert(kTileN == 128, "this kernel is laid out for 128-key tiles");
 
 struct AttnSmem {
@@ -89,7 +95,7 @@ struct AttnSmem {
   uint64_t full[kSlots], empty[kSlots];
   uint64_t q_full, q_empty, s_full, s_free;
   uint64_t p_full[2], p_empty[2];     // per 64-key half of P
-  uint64_t o_done, o_free, st_full, st_empty, drain, drain_pv, q_read, mx_bar;
+  uint64_t o_done, o_free, st_full, st_empty, drain, drain_pv, q_read, g_read, mx_bar;
   uint32_t tmem_base;
   int abort;
 };
@@ -196,14 +202,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // ------------------------------------------------------------------ warp 0: producer
 template <int kMode, bool kW>
 __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                              const CUtensorMap* tm_v, const AttnArgs& a, volatile int* abort,
-                              uint32_t& cnt) {
+                              const CUtensorMap* tm_v, const CUtensorMap* tm_g, const AttnArgs& a,
+                              volatile int* abort, uint32_t& cnt) {
   // One tile into the next slot. A Q tile is four 64-dim boxes at (dim, head, row r0), a
-  // verify Q tile 6 heads x vrows rows per box; a K or V tile is one copy of all four
-  // 64-dim blocks (the key/value map lists the block index as its outermost dimension, so
-  // the box lands as four consecutive 16 KiB blocks) at (0, key r0, head, 0[, sequence]).
+  // verify Q tile 6 heads x vrows rows per box; a gate tile four 64-value boxes of the
+  // fused rows at (256 + dim, head, row r0); a K or V tile is one copy of all four 64-dim
+  // blocks (the key/value map lists the block index as its outermost dimension, so the box
+  // lands as four consecutive 16 KiB blocks) at (0, key r0, head, 0[, sequence]).
   auto load_tile = [&](const CUtensorMap* map, bool kv, int head, int r0, int seq,
-                       uint32_t bytes) -> bool {
+                       uint32_t bytes, int x0 = 0) -> bool {
     const uint32_t slot = cnt % kSlots;
     if (!warp_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
     mbar_expect_tx_warp(&sm.full[slot], bytes);
@@ -215,7 +222,8 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
     } else {
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        tma_load_3d_warp(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], c * 64, head, r0);
+        tma_load_3d_warp(sm.tile[slot] + c * kChunkBytes, map, &sm.full[slot], x0 + c * 64, head,
+                         r0);
     }
     ++cnt;
     return true;
@@ -226,7 +234,7 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
     const int kvh = it.h / kGroup;
     TileCursor<kMode> ck(it), cv(it);
     // Ring order: the item's prepared Q (for the edge warps), then in MMA order K0,
-    // (K_j, V_{j-1}) for j >= 1, V_{n-1}.
+    // (K_j, V_{j-1}) for j >= 1, V_{n-1}; the gate tile (gated passes) just before V_0.
     const int kv_seq = kMode == kModeVerify ? it.seq : -1;
     if (kMode == kModeVerify) {
       if (!load_tile(tm_q, false, it.h, it.seq * a.vrows, -1,
@@ -234,20 +242,27 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
     } else {
       if (!load_tile(tm_q, false, it.h, it.mt * kTileM, -1, kTileBytes)) return;
     }
+    auto load_gate = [&]() -> bool {
+      return !has_gate<kMode, kW>() ||
+             load_tile(tm_g, false, it.h, it.mt * kTileM, -1, kTileBytes, kDim);
+    };
     if (!load_tile(tm_k, true, kvh, ck.next(0) * kTileN, kv_seq, kTileBytes)) return;
     for (int j = 1; j < it.n; ++j) {
       if (!load_tile(tm_k, true, kvh, ck.next(j) * kTileN, kv_seq, kTileBytes)) return;
+      if (j == 1 && !load_gate()) return;
       if (!kW && !load_tile(tm_v, true, kvh, cv.next(j - 1) * kTileN, kv_seq, kTileBytes)) return;
     }
+    if (it.n == 1 && !load_gate()) return;
     if (!kW && !load_tile(tm_v, true, kvh, cv.next(it.n - 1) * kTileN, kv_seq, kTileBytes)) return;
   }
 }
 
 template <int kMode, bool kW>
 __device__ void producer(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                         const CUtensorMap* tm_v, const AttnArgs& a, volatile int* abort) {
+                         const CUtensorMap* tm_v, const CUtensorMap* tm_g, const AttnArgs& a,
+                         volatile int* abort) {
   uint32_t cnt = 0;
-  producer_loop<kMode, kW>(sm, tm_q, tm_k, tm_v, a, abort, cnt);
+  producer_loop<kMode, kW>(sm, tm_q, tm_k, tm_v, tm_g, a, abort, cnt);
   if (*abort) {
     // let the loads already issued into the slots land before exit
     const uint32_t first = cnt > (uint32_t)kSlots ? cnt - kSlots : 0;
@@ -266,8 +281,8 @@ __device__ void producer(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMa
 // once it has seen the fill) and its consumer has released it (tcgen05.commit for K and V,
 // the edge warps for Q), so no walker can miss a fill. A warp's commits track only its own
 // MMAs (a commit covers the MMAs its thread issued).
-// Ring order per item: Q, K0, then K_j, V_{j-1} for j >= 1, then V_{n-1} (Q and K only in
-// the weights pass).
+// Ring order per item: Q, K0, then K_j, V_{j-1} for j >= 1, then V_{n-1}, with the gate
+// tile of the gated passes right before V_0 (Q and K only in the weights pass).
 struct RingWalk {
   uint32_t cnt = 0;
   // wait for the next fill in ring order (its slot in `slot`) and count this warp as past it
@@ -293,11 +308,16 @@ __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
   uint32_t slot;
   ItemWalk<kMode> walk;
   Item it;
+  // V_idx, preceded by the gate tile when idx is 0
+  auto walk_v = [&](int idx) -> bool {
+    if (has_gate<kMode, kW>() && idx == 0 && !ring.next(sm, abort, slot)) return false;
+    return ring.next(sm, abort, slot);
+  };
   while (walk.next(a, it)) {
     if (!ring.next(sm, abort, slot)) return;            // the item's Q tile (edge warps)
     if (!warp_wait(&sm.q_full, it_done & 1, abort)) return;
     for (int j = 0; j < it.n; ++j, ++g) {
-      if (!kW && j >= 2 && !ring.next(sm, abort, slot)) return;   // V_{j-2}
+      if (!kW && j >= 2 && !walk_v(j - 2)) return;      // V_{j-2}
       if (!ring.next(sm, abort, slot)) return;          // K_j
       // S is free once the softmax warps have copied the previous tile's S out
       if (g > 0 && !warp_wait(&sm.s_free, (g - 1) & 1, abort)) return;
@@ -313,8 +333,8 @@ __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
       if (j == it.n - 1) umma_commit_warp(&sm.q_empty);
     }
     if (!kW) {
-      if (it.n >= 2 && !ring.next(sm, abort, slot)) return;   // V_{n-2}
-      if (!ring.next(sm, abort, slot)) return;                // V_{n-1}
+      if (it.n >= 2 && !walk_v(it.n - 2)) return;       // V_{n-2}
+      if (!walk_v(it.n - 1)) return;                    // V_{n-1}
     }
     ++it_done;
   }
@@ -336,6 +356,7 @@ __device__ void pv_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
     if (!ring.next(sm, abort, slot)) return;            // K0
     for (int j = 0; j < it.n; ++j, ++g) {
       if (j + 1 < it.n && !ring.next(sm, abort, slot)) return;   // K_{j+1}
+      if (has_gate<kMode, false>() && j == 0 && !ring.next(sm, abort, slot)) return;   // gate
       if (!ring.next(sm, abort, slot)) return;                   // V_j
       if (j == 0 && it_done > 0 && !warp_wait(&sm.o_free, (it_done - 1) & 1, abort)) return;
       const uint64_t bd0 = v_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
@@ -558,26 +579,27 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
       }
       M = newM;
       const float mf = hasM ? (float)M : 0.f;
-      // P = bf16(2^(t - M)), t = bf16(s) * log2(e) / 16, into this half's 64-key block of
-      // shared memory once the previous P.V has read it; l sums the rounded P
-      if (g > 0 && !warp_wait(&sm.p_empty[hf], (g - 1) & 1, abort)) return;
+      // P = bf16(2^(t - M)), t = bf16(s) * log2(e) / 16, computed in place over the scores
+      // (l sums the rounded P), then stored into this half's 64-key block of shared memory
+      // once the previous P.V has read it: the exponentials do not wait for the tensor cores
       float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
-      for (int cd = 0; cd < kHalfKeys / 8; ++cd) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t w = sb[cd * 4 + k];
-          const float t0 = fmaf(lo_f(w), kLog2eOver16, -mf);
-          const float t1 = fmaf(hi_f(w), kLog2eOver16, -mf);
-          pk[k] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
-          if (k & 1) add_bf16x2(l2, l3, pk[k]);
-          else add_bf16x2(l0, l1, pk[k]);
-        }
-        uint8_t* dst = sm.p[hf] + sw128_offset((uint32_t)r, (uint32_t)cd);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      for (int k = 0; k < kHalfKeys / 2; ++k) {
+        const uint32_t w = sb[k];
+        const float t0 = fmaf(lo_f(w), kLog2eOver16, -mf);
+        const float t1 = fmaf(hi_f(w), kLog2eOver16, -mf);
+        sb[k] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
+        if (k & 1) add_bf16x2(l2, l3, sb[k]);
+        else add_bf16x2(l0, l1, sb[k]);
       }
       l += (l0 + l2) + (l1 + l3);
+      if (g > 0 && !warp_wait(&sm.p_empty[hf], (g - 1) & 1, abort)) return;
+#pragma unroll
+      for (int cd = 0; cd < kHalfKeys / 8; ++cd) {
+        uint8_t* dst = sm.p[hf] + sw128_offset((uint32_t)r, (uint32_t)cd);
+        *reinterpret_cast<uint4*>(dst) =
+            make_uint4(sb[4 * cd], sb[4 * cd + 1], sb[4 * cd + 2], sb[4 * cd + 3]);
+      }
       fence_async_smem();
       mbar_arrive(&sm.p_full[hf]);
     }
@@ -643,21 +665,24 @@ __device__ __noinline__ uint4 sigmoid_patch8(uint4 g, uint4 o) {
   return make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
 
-// bf16(sigmoid(g)) of this thread's 256 gates, as bf16 pairs in registers (word c holds
-// dims 2c and 2c+1); zeros for rows past the end. The gates are read once and processed
-// 8 at a time through a rotating register queue: the loop body stays small, because this
-// code shares the instruction cache with the softmax loop running on the same SM
-// sub-partition, and a long unrolled body evicts it.
-__device__ void gate_sigmoid(const AttnArgs& a, const Item& it, int r, uint4 (&sg)[kDim / 8]) {
-  const int row = it.mt * kTileM + r;
-  if (row >= a.rows) {
+// This thread's 256 gates (row r of the item's gate tile in a ring slot: four 128-row x
+// 64-value blocks, 128-byte swizzled) into registers, word c holding dims 2c and 2c+1.
+// Rows past the end read as zeros; their outputs are never stored.
+__device__ __forceinline__ void gate_from_tile(const uint8_t* tile, int r, uint4 (&sg)[kDim / 8]) {
 #pragma unroll
-    for (int i = 0; i < kDim / 8; ++i) sg[i] = make_uint4(0, 0, 0, 0);
-    return;
+  for (int grp = 0; grp < 4; ++grp) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      sg[grp * 8 + j] = *reinterpret_cast<const uint4*>(tile + grp * kChunkBytes +
+                                                        sw128_offset((uint32_t)r, (uint32_t)j));
   }
-  const uint4* gp = reinterpret_cast<const uint4*>(a.qg + ((size_t)row * kHeads + it.h) * kQgStride + kDim);
-#pragma unroll
-  for (int i = 0; i < kDim / 8; ++i) sg[i] = __ldg(gp + i);
+}
+
+// bf16(sigmoid(g)) of the 256 gates in sg, in place. The gates are processed 8 at a time
+// through a rotating register queue: the loop body stays small, because this code shares
+// the instruction cache with the softmax loop running on the same SM sub-partition, and a
+// long unrolled body evicts it.
+__device__ void gate_sigmoid(uint4 (&sg)[kDim / 8]) {
 #pragma unroll 1
   for (int step = 0; step < kDim / 8; ++step) {
     const uint4 g = sg[0];
@@ -708,6 +733,7 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
   tc_fence_after();
   const float inv = l > 0.f ? 1.0f / l : 0.f;
   uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)(valid ? row : 0) * kOutRow + h * kDim);
+  const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;   // rows are 12 KiB apart
 #pragma unroll 1
   for (int c = 0; c < kDim / 64; ++c) {
 #pragma unroll
@@ -716,17 +742,27 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
       tmem_ld32(tmem + kTmemO + lane_off + c * 64 + 32 * half, o);
       tmem_wait_ld(o);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t sw[4] = {sg[4 * half + i].x, sg[4 * half + i].y, sg[4 * half + i].z,
-                                sg[4 * half + i].w};
-        uint32_t w[4];
+      for (int i2 = 0; i2 < 4; i2 += 2) {
+        uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t ob = pack_bf16x2(__uint_as_float(o[8 * i + 2 * k]) * inv,
-                                          __uint_as_float(o[8 * i + 2 * k + 1]) * inv);
-          w[k] = mul_bf16x2(ob, sw[k]);   // bf16(o * s), o and s already bf16
+        for (int i = i2; i < i2 + 2; ++i) {
+          const uint32_t sw[4] = {sg[4 * half + i].x, sg[4 * half + i].y, sg[4 * half + i].z,
+                                  sg[4 * half + i].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t ob = pack_bf16x2(__uint_as_float(o[8 * i + 2 * k]) * inv,
+                                            __uint_as_float(o[8 * i + 2 * k + 1]) * inv);
+            w[4 * (i - i2) + k] = mul_bf16x2(ob, sw[k]);   // bf16(o * s), o and s already bf16
+          }
         }
-        if (valid) op[8 * c + 4 * half + i] = make_uint4(w[0], w[1], w[2], w[3]);
+        // 32 bytes per store where the output allows it (32-byte aligned base)
+        uint4* dst = op + 8 * c + 4 * half + i2;
+        if (valid && out32) {
+          st_global_v8(dst, w);
+        } else if (valid) {
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
       }
     }
     uint4 none[8];
@@ -822,7 +858,25 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
       mbar_arrive(&sm.empty[slot]);
     }
     ++q_takes;
-    q_pos += 1 + (kW ? 1 : 2) * it.n;
+    q_pos += (has_gate<kMode, kW>() ? 2 : 1) + (kW ? 1 : 2) * it.n;
+    return true;
+  };
+  // The item's gate tile sits at ring position pos (after Q, K0 and, when the item has two
+  // key tiles or more, K1). Its slot's previous fill is the item's own Q tile or the
+  // previous item's last V tile, both known to have landed (the previous epilogue waited for
+  // its last P V), so the parity wait is safe. The slot is handed back once all 128 edge
+  // threads have copied their row.
+  uint32_t g_takes = 0;
+  auto take_gate = [&](uint32_t pos, uint4 (&sg)[kDim / 8]) -> bool {
+    const uint32_t slot = pos % kSlots;
+    if (!warp_wait(&sm.full[slot], (pos / kSlots) & 1, abort)) return false;
+    gate_from_tile(sm.tile[slot], r, sg);
+    mbar_arrive(&sm.g_read);
+    if (threadIdx.x == kEdgeThread0) {
+      if (!mbar_wait(&sm.g_read, g_takes & 1, abort)) return false;
+      mbar_arrive(&sm.empty[slot]);
+    }
+    ++g_takes;
     return true;
   };
   // Item i+1's Q goes into TMEM as soon as item i's last S = Q K^T has read Q; item i's
@@ -830,12 +884,17 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
   // is done.
   Item cur, nxt;
   if (!next_item(cur)) return;
+  uint32_t cur_q = q_pos;   // ring position of the current item's Q tile
   if (!take_q(cur, false, 0)) return;
   uint4 sg[kDim / 8];
   uint32_t it_done = 0;
   while (true) {
-    if (!kW && kMode != kModeVerify) gate_sigmoid(a, cur, r, sg);
+    if (has_gate<kMode, kW>()) {
+      if (!take_gate(cur_q + (cur.n >= 2 ? 3 : 2), sg)) return;
+      gate_sigmoid(sg);
+    }
     const bool have_next = next_item(nxt);
+    const uint32_t nxt_q = q_pos;
     if (have_next && !take_q(nxt, true, it_done)) return;
     if (kMode == kModeVerify) {
       if (!epilogue_partial(sm, a, cur, tmem, lane_off, r, it_done, abort)) return;
@@ -845,13 +904,15 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
     ++it_done;
     if (!have_next) break;
     cur = nxt;
+    cur_q = nxt_q;
   }
 }
 
 template <int kMode, bool kW>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnArgs a) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                const __grid_constant__ AttnArgs a) {
   // The dynamic shared memory is declared 1024-byte aligned (the 128-byte swizzle of TMA
   // and the MMA descriptors needs it); every thread checks it before using any of it.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -885,6 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.drain, 1);
     mbar_init(&sm.drain_pv, 1);
     mbar_init(&sm.q_read, 128);
+    mbar_init(&sm.g_read, 128);
     mbar_init(&sm.mx_bar, 256);
     mbar_fence_init();
   }
@@ -892,6 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    if (has_gate<kMode, kW>()) tma_prefetch_desc(&tm_g);
   }
   if (warp == 1) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -904,7 +967,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
-    if (warp == 0) producer<kMode, kW>(sm, &tm_q, &tm_k, &tm_v, a, abort);
+    if (warp == 0) producer<kMode, kW>(sm, &tm_q, &tm_k, &tm_v, &tm_g, a, abort);
     if (warp == 1 || warp == 2) mma_issuer<kMode, kW>(sm, a, tmem, abort, warp == 2);
   } else if (warp < 12) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
@@ -1029,19 +1092,19 @@ cudaError_t attn_set_smem_attribute() {
 }
 
 cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                        const AttnArgs& a, int grid, cudaStream_t s) {
+                        const CUtensorMap& tm_g, const AttnArgs& a, int grid, cudaStream_t s) {
   const size_t smem = attn_smem_bytes();
   if (a.weights_pass) {
     if (a.mode != kModeMask) return cudaErrorInvalidValue;
-    attn_kernel<kModeMask, true><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
+    attn_kernel<kModeMask, true><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else if (a.mode == kModeCausal) {
-    attn_kernel<kModeCausal, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
+    attn_kernel<kModeCausal, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else if (a.mode == kModeBidir) {
-    attn_kernel<kModeBidir, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
+    attn_kernel<kModeBidir, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else if (a.mode == kModeVerify) {
-    attn_kernel<kModeVerify, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
+    attn_kernel<kModeVerify, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else {
-    attn_kernel<kModeMask, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, a);
+    attn_kernel<kModeMask, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   }
   return cudaGetLastError();
 }

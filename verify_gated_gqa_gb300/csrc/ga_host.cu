@@ -171,6 +171,28 @@ int encode_q_map(CUtensorMap* map, const void* base, long long rows, int box_hea
   return GA_OK;
 }
 
+// [rows][24][512] bf16 fused q|gate rows as a TMA tensor, read for the gate halves: box =
+// 64 values x 1 head x 128 rows at x = 256 + 64c, 128-byte swizzle; rows past the end read
+// as zeros.
+int encode_gate_map(CUtensorMap* map, const void* base, long long rows) {
+  EncodeTiledFn enc;
+  int st = get_encode(&enc);
+  if (st != GA_OK) return st;
+  cuuint64_t dims[3] = {(cuuint64_t)kQgStride, (cuuint64_t)kHeads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)kQgStride * 2, (cuuint64_t)kHeads * kQgStride * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kTileM};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = GA_CUDA(enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = (int)r;
+    return GA_ERR_CUDA;
+  }
+  return GA_OK;
+}
+
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // bf16 (nearest, ties to even) of a double.
@@ -249,8 +271,10 @@ size_t verify_ws_bytes(const VerifyPlan& p) {
 // (row, head) slot is read by the work item that later writes its output there.
 int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const void* k_prep,
                      const void* v, long long n_tok, DeviceState* dev, cudaStream_t s) {
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v, tm_g;
   int st = encode_q_map(&tm_q, q_prep, a0.rows);
+  if (st != GA_OK) return st;
+  st = encode_gate_map(&tm_g, a0.qg, a0.rows);
   if (st != GA_OK) return st;
   st = encode_kv_map(&tm_k, k_prep, n_tok, 1, false);
   if (st != GA_OK) return st;
@@ -266,7 +290,7 @@ int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const v
                                      s))) != cudaSuccess)
     return fail_cuda(e);
   const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
-  e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, a, grid, s));
+  e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_g, a, grid, s));
   if (e != cudaSuccess) return fail_cuda(e);
   return GA_OK;
 }
@@ -567,7 +591,9 @@ int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_c
     st = encode_kv_map(&tm_v, v_cache + (size_t)g0 * seq_elems, cap, n, true);
     if (st != GA_OK) return st;
     const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
-    if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, a, grid, s))) != cudaSuccess) return fail_cuda(e);
+    // the verify partials have no gated epilogue: tm_q stands in for the unused gate map
+    if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_q, a, grid, s))) != cudaSuccess)
+      return fail_cuda(e);
     if ((e = GA_CUDA(launch_verify_combine(a, s))) != cudaSuccess) return fail_cuda(e);
   }
   return GA_OK;
