@@ -152,9 +152,9 @@ def test_single_key_and_single_row():
 
 def test_gate_every_bf16_value():
     """Every bf16 gate value but NaN (one per output element across 11 rows) with V = 1, so
-    that o = 1 and out = bf16(sigmoid(g)) itself: the gate's fast path and its exact
-    fallback, bit for bit against the oracle, including +-inf, subnormal gates and the
-    gates whose sigmoid is a bf16 subnormal."""
+    that o = 1 and out = bf16(sigmoid(g)) itself: the device's sigmoid table, bit for bit
+    against the oracle, including +-inf, subnormal gates and the gates whose sigmoid is a
+    bf16 subnormal."""
     bits = np.arange(65536, dtype=np.uint32)
     is_nan = (((bits >> 7) & 0xFF) == 0xFF) & ((bits & 0x7F) != 0)
     vals = (bits[~is_nan] << 16).view(np.float32).astype(np.float64)

@@ -646,23 +646,14 @@ __device__ __forceinline__ void rotate8(uint4 (&q)[kDim / 8], const uint4 (&in)[
 }
 
 // bf16(sigmoid(g)) for every bf16 g (index: g's bits), exact from the double definition;
-// filled once per device from the host. The gate's rare exact path reads it.
+// filled once per device from the host. Every gate of the epilogue and of the verify
+// combine is looked up here: the answer is the definition itself, and a lookup costs the
+// edge warps far less than computing it (exponential and reciprocal on the special-function
+// unit the softmax needs) while the item's tiles run.
 __device__ uint16_t g_sigmoid_bf16[1 << 16];
 
-// Rare path (this lane only): the 8 gates of g (bf16 pairs) whose fast sigmoid was not
-// certified take the exact table value, in the matching halves of o.
-__device__ __noinline__ uint4 sigmoid_patch8(uint4 g, uint4 o) {
-  uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-  uint32_t ow[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll 1
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t gb = (k & 1) ? (gw[k >> 1] >> 16) : (gw[k >> 1] & 0xFFFFu);
-    float y;
-    if (sigmoid_fast(__uint_as_float(gb << 16), y)) continue;
-    const uint32_t b = g_sigmoid_bf16[gb];
-    ow[k >> 1] = (k & 1) ? ((ow[k >> 1] & 0xFFFFu) | (b << 16)) : ((ow[k >> 1] & 0xFFFF0000u) | b);
-  }
-  return make_uint4(ow[0], ow[1], ow[2], ow[3]);
+__device__ __forceinline__ uint32_t sigmoid_pair(uint32_t g) {
+  return (uint32_t)g_sigmoid_bf16[g & 0xFFFFu] | ((uint32_t)g_sigmoid_bf16[g >> 16] << 16);
 }
 
 // This thread's 256 gates (row r of the item's gate tile in a ring slot: four 128-row x
@@ -678,26 +669,16 @@ __device__ __forceinline__ void gate_from_tile(const uint8_t* tile, int r, uint4
   }
 }
 
-// bf16(sigmoid(g)) of the 256 gates in sg, in place. The gates are processed 8 at a time
-// through a rotating register queue: the loop body stays small, because this code shares
-// the instruction cache with the softmax loop running on the same SM sub-partition, and a
-// long unrolled body evicts it.
+// bf16(sigmoid(g)) of the 256 gates in sg, in place, from the table. The gates are
+// processed 8 at a time through a rotating register queue: the loop body stays small,
+// because this code shares the instruction cache with the softmax loop running on the same
+// SM sub-partition, and a long unrolled body evicts it.
 __device__ void gate_sigmoid(uint4 (&sg)[kDim / 8]) {
 #pragma unroll 1
   for (int step = 0; step < kDim / 8; ++step) {
     const uint4 g = sg[0];
-    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-    uint32_t w[4];
-    bool ok = true;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float s0, s1;
-      ok &= sigmoid_fast(lo_f(gw[k]), s0);
-      ok &= sigmoid_fast(hi_f(gw[k]), s1);
-      w[k] = pack_bf16x2(s0, s1);
-    }
-    uint4 o = make_uint4(w[0], w[1], w[2], w[3]);
-    if (!ok) o = sigmoid_patch8(g, o);
+    const uint4 o = make_uint4(sigmoid_pair(g.x), sigmoid_pair(g.y), sigmoid_pair(g.z),
+                               sigmoid_pair(g.w));
 #pragma unroll
     for (int i = 0; i < kDim / 8 - 1; ++i) sg[i] = sg[i + 1];
     sg[kDim / 8 - 1] = o;
@@ -1030,12 +1011,8 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_consta
   uint32_t res[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    float s0, s1;
-    if (!sigmoid_fast(lo_f(gw[k]), s0)) s0 = __uint_as_float((uint32_t)g_sigmoid_bf16[gw[k] & 0xFFFFu] << 16);
-    if (!sigmoid_fast(hi_f(gw[k]), s1)) s1 = __uint_as_float((uint32_t)g_sigmoid_bf16[gw[k] >> 16] << 16);
     const uint32_t ob = pack_bf16x2(o[2 * k] * inv, o[2 * k + 1] * inv);
-    const uint32_t sp = pack_bf16x2(s0, s1);
-    res[k] = mul_bf16x2(ob, sp);
+    res[k] = mul_bf16x2(ob, sigmoid_pair(gw[k]));
   }
   reinterpret_cast<uint4*>(a.out + row * kOutRow + h * kDim)[lane] = make_uint4(res[0], res[1], res[2], res[3]);
 }

@@ -119,29 +119,4 @@ __device__ __forceinline__ void rope_pair(float a, float b, float c, float s, fl
   yb = bf16_round(bf16_round(b * c) + bf16_round(a * s));
 }
 
-// Fast sigmoid of a bf16 g for the epilogue: 1 / (1 + 2^(-g log2 e)) with the exponent
-// split exactly (g has 8 significant bits, kL2eHi 16, so -g * kL2eHi is exact in fp32; the
-// small remainder -g * kL2eLo is applied as a first-order factor), ex2.approx and
-// rcp.approx. Over every bf16 g whose sigmoid is a normal fp32 number the result is within
-// 2.7 fp32 ulps (checked exhaustively on the device against the double definition); the
-// caller rounds it to bf16 unless it lies within kSigmoidMargin ulps of a bf16 midpoint,
-// or g is outside that range, and then the exact table value is the answer: returns false
-// for those. Where 2^-g*log2e is below 2^-32 the sum 1 + e is exactly 1 and so is the bf16
-// result.
-constexpr int kSigmoidMargin = 4;
-constexpr float kL2eHi = 1.44268798828125f;          // 47274 / 2^15: log2(e) to 16 bits
-constexpr float kL2eLo = 7.05260771340736e-06f;      // log2(e) - kL2eHi
-__device__ __forceinline__ bool sigmoid_fast(float g, float& y) {
-  const float th = -g * kL2eHi;
-  // the remainder from a clamped g, so that an infinite g gives 0 * finite, not 0 * inf
-  // (a NaN g still gives NaN through th)
-  const float tl = -fminf(fmaxf(g, -256.0f), 256.0f) * kL2eLo;
-  float e0, r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(th));
-  const float e = fmaf(e0, tl * 0.6931471805599453f, e0);
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-  y = r;
-  return th <= 120.0f && !near_bf16_midpoint(r, kSigmoidMargin);
-}
-
 }  // namespace ga
