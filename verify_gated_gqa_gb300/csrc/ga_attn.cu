@@ -23,8 +23,8 @@
 //              16 KiB 128-byte-swizzled column blocks), through three tile slots (the whole
 //              warp runs the loop, one elected lane issues the copies);
 //   warp 1     allocates the 512 TMEM columns and issues every S = Q K^T (M=128, N=128,
-//              K=256; Q read from TMEM);
-//   warp 2     issues every O += P V (M=128, N=256, K=128; P from shared memory, V
+//              K=256; Q dims 0..127 read from TMEM, dims 128..255 from shared memory);
+//   warp 2     issues every O += P V (M=128, N=256, K=128; P from tensor memory, V
 //              MN-major), so a tile's P V need not wait behind the next tile's Q K^T
 //              issue. Both at full rate (N >= 128); in each, the whole warp runs the issue
 //              loop and one elected lane issues (a lone lane in a divergent branch issued
@@ -33,7 +33,7 @@
 //              per thread: S is copied to registers and its TMEM columns released at once
 //              (so the next S = Q K^T overlaps this softmax); the two halves exchange their
 //              row maxima through shared memory and take the same M; P = bf16(2^(t - M))
-//              goes to shared memory, each half its own 64 keys (and the tensor cores read
+//              goes to tensor memory, each half its own 64 keys (and the tensor cores read
 //              each half as soon as it is written), and each half rescales its half of O
 //              when needed;
 //   warps 12-15 the edge of each work item: the current item's gate tile from its ring
@@ -43,8 +43,10 @@
 //              epilogue of the current item.
 // The edge code is kept in short loops: the four roles run different code at once and
 // share the SM's instruction cache, which long unrolled sequences would overflow.
-// Tensor memory (512 columns x 128 lanes, lane = query row): O [0, 256) fp32, Q
-// [256, 384) bf16 pairs, S [384, 512) fp32.
+// Tensor memory (512 columns x 128 lanes, lane = query row): O [0, 256) fp32, S [256, 384)
+// fp32, Q dims 0..127 [384, 448) and P [448, 512) as bf16 pairs. Q dims 128..255 stay in
+// shared memory for the item, where P used to go: P is written to tensor memory with one
+// store per thread and read from there by the P V MMAs.
 // Work items are (query head, 128-row tile), longest first, dealt to the CTAs in a
 // serpentine order so each CTA's total work evens out. The kernel is compiled once per
 // visibility mode (causal, bidirectional, stored mask) and for the weights pass, so each
@@ -74,8 +76,9 @@ static_assert(128 * (kRegsIssue + 2 * kRegsSoftmax + kRegsEdge) == kThreads * kL
 constexpr int kHalfKeys = kTileN / 2;   // keys per softmax warpgroup in a tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;      // O accumulator: 256 columns (fp32)
-constexpr uint32_t kTmemQ = 256;    // Q: 128 columns of bf16 pairs (A operand of Q K^T)
-constexpr uint32_t kTmemS = 384;    // S: 128 columns (fp32)
+constexpr uint32_t kTmemS = 256;    // S: 128 columns (fp32)
+constexpr uint32_t kTmemQ = 384;    // Q dims 0..127: 64 columns of bf16 pairs (A of Q K^T)
+constexpr uint32_t kTmemP = 448;    // P: 64 columns of bf16 pairs, 32 per 64-key half (A of P V)
 constexpr float kLog2eOver16 = 1.4426950408889634f / 16.0f;
 constexpr int kLazyRescale = 8;     // rescale when the tile maximum exceeds M by > 2^8
 
@@ -88,7 +91,7 @@ static_assert(kTileN == 128, "this kernel is laid out for 128-key tiles");
 
 struct AttnSmem {
   uint8_t tile[kSlots][kTileBytes];   // K or V tiles (1024-byte aligned)
-  uint8_t p[2][kChunkBytes];          // P: 128 rows x 128 keys, two swizzled 64-key columns
+  uint8_t qhi[2][kChunkBytes];        // Q dims 128..255 of the item: two swizzled 64-dim blocks
   float stat_l[2][kTileM];            // softmax -> edge: each half's row sum l of the item
   float stat_m[kTileM];               // and the running maximum M
   uint16_t mx[2][2][kTileM];          // tile g: each half's row maximum (bf16 bits), by g % 2
@@ -302,6 +305,7 @@ template <int kMode, bool kW>
 __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
   constexpr uint32_t kIdQK = idesc_bf16(128, kTileN, false, false);
   const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), 16, 1024);
+  const uint64_t qhi_desc0 = sdesc_sw128(smem_u32(sm.qhi[0]), 16, 1024);
   RingWalk ring;
   uint32_t g = 0;         // global key-tile counter: S phases
   uint32_t it_done = 0;
@@ -323,10 +327,18 @@ __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
       if (g > 0 && !warp_wait(&sm.s_free, (g - 1) & 1, abort)) return;
       tc_fence_after();
       const uint64_t kd0 = k_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
+      // dims 0..127 with Q from tensor memory, dims 128..255 with Q from shared memory
 #pragma unroll
-      for (int kk = 0; kk < kDim / 16; ++kk) {
+      for (int kk = 0; kk < kDim / 32; ++kk) {
         const uint64_t bd = kd0 + (uint64_t)((kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2);
         umma_ts_warp(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, kIdQK, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = kDim / 32; kk < kDim / 16; ++kk) {
+        const uint32_t blk = (kk >> 2) - 2;
+        const uint64_t bd = kd0 + (uint64_t)((kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2);
+        const uint64_t ad = qhi_desc0 + (uint64_t)(blk * (kChunkBytes >> 4) + (kk & 3) * 2);
+        umma_ss_warp(tmem + kTmemS, ad, bd, kIdQK, 1u);
       }
       umma_commit_warp(&sm.empty[slot]);
       umma_commit_warp(&sm.s_full);
@@ -343,7 +355,6 @@ __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
 template <int kMode>
 __device__ void pv_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
   constexpr uint32_t kIdPV = idesc_bf16(128, kDim, false, true);
-  const uint64_t p_desc0 = sdesc_sw128(smem_u32(sm.p[0]), 16, 1024);
   const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), kChunkBytes, 1024);
   RingWalk ring;
   uint32_t g = 0;         // global key-tile counter: P and P V phases
@@ -369,8 +380,8 @@ __device__ void pv_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int kk = 4 * hb + k4;
-          const uint64_t ad = p_desc0 + (uint64_t)(hb * (kChunkBytes >> 4) + k4 * 2);
-          umma_ss_warp(tmem + kTmemO, ad, bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
+          umma_ts_warp(tmem + kTmemO, tmem + kTmemP + hb * (kHalfKeys / 2) + k4 * 8,
+                       bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
                        (j > 0 || kk > 0) ? 1u : 0u);
         }
         // p_empty[1] also tells the softmax that O holds every P V so far
@@ -593,14 +604,14 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
         else add_bf16x2(l0, l1, sb[k]);
       }
       l += (l0 + l2) + (l1 + l3);
+      // this half's P (word k: keys 2k, 2k+1) into its 32 columns of tensor memory once the
+      // previous P V has read them
       if (g > 0 && !warp_wait(&sm.p_empty[hf], (g - 1) & 1, abort)) return;
-#pragma unroll
-      for (int cd = 0; cd < kHalfKeys / 8; ++cd) {
-        uint8_t* dst = sm.p[hf] + sw128_offset((uint32_t)r, (uint32_t)cd);
-        *reinterpret_cast<uint4*>(dst) =
-            make_uint4(sb[4 * cd], sb[4 * cd + 1], sb[4 * cd + 2], sb[4 * cd + 3]);
-      }
-      fence_async_smem();
+      tc_fence_after();
+      tmem_st32(tmem + kTmemP + lane_off + (kHalfKeys / 2) * hf,
+                *reinterpret_cast<uint32_t(*)[32]>(sb));
+      tmem_wait_st();
+      tc_fence_before();
       mbar_arrive(&sm.p_full[hf]);
     }
     if (!kW) {
@@ -616,25 +627,35 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
 
 // ------------------------------------------------------------------ warps 12-15: edge
 // The item's prepared Q tile (a ring slot: four 128-row x 64-dim blocks, 128-byte
-// swizzled) into this thread's TMEM lane at Q: row r, dims 2c and 2c+1 in column c.
-// Every lane of the warp runs it (warp-collective stores).
-// Lanes with `have` false (verify padding) store zeros.
-__device__ __forceinline__ void q_copy_tmem(const uint8_t* tile, int r, bool have, uint32_t q_taddr) {
+// swizzled): dims 0..127 into this thread's TMEM lane at Q (row r, dims 2c and 2c+1 in
+// column c), dims 128..255 as they are into the item's Q blocks in shared memory (the same
+// swizzled layout, read by the tensor cores). Every lane of the warp runs it
+// (warp-collective stores). Lanes with `have` false (verify padding) store zeros.
+__device__ __forceinline__ void q_copy(const uint8_t* tile, int r, bool have, uint32_t q_taddr,
+                                       uint8_t (&qhi)[2][kChunkBytes]) {
 #pragma unroll
   for (int grp = 0; grp < 4; ++grp) {
 #pragma unroll
     for (int j = 0; j < 8; j += 2) {
       const uint8_t* base = tile + grp * kChunkBytes;
+      const uint32_t o0 = sw128_offset((uint32_t)r, (uint32_t)j);
+      const uint32_t o1 = sw128_offset((uint32_t)r, (uint32_t)j + 1);
       uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
       if (have) {
-        v0 = *reinterpret_cast<const uint4*>(base + sw128_offset((uint32_t)r, (uint32_t)j));
-        v1 = *reinterpret_cast<const uint4*>(base + sw128_offset((uint32_t)r, (uint32_t)j + 1));
+        v0 = *reinterpret_cast<const uint4*>(base + o0);
+        v1 = *reinterpret_cast<const uint4*>(base + o1);
       }
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      tmem_st8(q_taddr + 32 * grp + 4 * j, w);
+      if (grp < 2) {
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        tmem_st8(q_taddr + 32 * grp + 4 * j, w);
+      } else {
+        *reinterpret_cast<uint4*>(qhi[grp - 2] + o0) = v0;
+        *reinterpret_cast<uint4*>(qhi[grp - 2] + o1) = v1;
+      }
     }
   }
   tmem_wait_st();
+  fence_async_smem();   // the tensor cores read the shared-memory half
 }
 
 // Moves the 32-entry register queue on by 8: entries 8..31 to the front, `in` at the end.
@@ -829,8 +850,8 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
     if (wait_empty && !warp_wait(&sm.q_empty, it_done & 1, abort)) return false;
     if (!warp_wait(&sm.full[slot], (q_pos / kSlots) & 1, abort)) return false;
     tc_fence_after();
-    q_copy_tmem(sm.tile[slot], r, kMode != kModeVerify || r < kVerifyHeadsPerTile * a.vrows,
-                q_taddr);
+    q_copy(sm.tile[slot], r, kMode != kModeVerify || r < kVerifyHeadsPerTile * a.vrows, q_taddr,
+           sm.qhi);
     tc_fence_before();
     mbar_arrive(&sm.q_full);
     mbar_arrive(&sm.q_read);
