@@ -336,6 +336,37 @@ def verify(qg_seq, k_cache, v_cache, seq_len, w_q, cos, sin, mode="R1", rows=Non
     return np.stack(outs)
 
 
+def gather_pages(pool, table_row, n_tok, page_size):
+    """A sequence's cache rows 0 .. n_tok-1 from a page pool: position t lives on page
+    table_row[t // page_size], slot t % page_size. pool [n_pages, page_size, ...].
+    (Paged caches are named as the next step after the contiguous key array in [QSA]
+    §Summary and §Limits; the layout is this plain reading of a page table.)"""
+    pool = np.asarray(pool)
+    rows = []
+    for t in range(n_tok):
+        rows.append(pool[int(table_row[t // page_size]), t % page_size])
+    if not rows:
+        return np.zeros((0,) + pool.shape[2:], dtype=pool.dtype)
+    return np.stack(rows)
+
+
+def verify_paged(qg_seq, k_pages, v_pages, page_table, page_size, seq_len, w_q, cos, sin,
+                 mode="R1", rows=None, heads=None):
+    """verify() over paged caches: each sequence's prepared keys and values are gathered
+    from the page pools through its page-table row, then attended exactly as in verify().
+    Decode is the same with one row per sequence."""
+    qg_seq = np.asarray(qg_seq)
+    R = qg_seq.shape[1]
+    outs = []
+    for b in range(qg_seq.shape[0]):
+        L = int(seq_len[b])
+        kc = gather_pages(k_pages, page_table[b], L + R, page_size)
+        vc = gather_pages(v_pages, page_table[b], L + R, page_size)
+        outs.append(prefill(qg_seq[b], kc, vc, w_q, cos, sin, L, L + R, True, mode, rows,
+                            heads))
+    return np.stack(outs)
+
+
 def row_stats(q_hat_h, k_hat_kv, vis):
     """Diagnostics: per row the largest visible score s and the spread max-min (nats)."""
     dot = bf16(q_hat_h @ k_hat_kv.T) / 16.0

@@ -429,6 +429,48 @@ def test_verify_equals_prefill_rows():
     assert np.array_equal(out[0], full[L:])
 
 
+def test_gather_pages_indexing():
+    """Every gathered row carries its own (page, slot) label: position t comes from page
+    table[t // page_size], slot t % page_size, for page sizes of one and two tiles."""
+    rng = np.random.default_rng(5)
+    for page_size in (128, 256):
+        n_pages = 7
+        pool = np.zeros((n_pages, page_size, 2))
+        pool[:, :, 0] = np.arange(n_pages)[:, None]
+        pool[:, :, 1] = np.arange(page_size)[None, :]
+        table = rng.permutation(n_pages)
+        n_tok = 3 * page_size + 37
+        got = O.gather_pages(pool, table, n_tok, page_size)
+        t = np.arange(n_tok)
+        assert np.array_equal(got[:, 0], table[t // page_size])
+        assert np.array_equal(got[:, 1], t % page_size)
+    assert O.gather_pages(pool, table, 0, 256).shape == (0, 2)
+
+
+def test_verify_paged_equals_contiguous_and_decode_equals_prefill_row():
+    """Scattered pages give the contiguous cache's outputs bit for bit, and a one-row
+    decode at position L equals row L of the full causal pass."""
+    L, R, page_size = 300, 3, 128
+    qg_all, kp, v, w_q, c, s = _prepared(S=L + R, seed=27)
+    n_pages = 5
+    order = np.array([3, 0, 4, 1, 2])                 # page order[i] holds positions i*128..
+    kpool = np.zeros((n_pages, page_size, 2, 256))
+    vpool = np.zeros_like(kpool)
+    for i in range(-(-(L + R) // page_size)):
+        rows = slice(i * page_size, min((i + 1) * page_size, L + R))
+        n = rows.stop - rows.start
+        kpool[order[i], :n] = kp[rows]
+        vpool[order[i], :n] = v[rows]
+    qg = qg_all[L:][None]
+    paged = O.verify_paged(qg, kpool, vpool, order[None], page_size, [L], w_q, c, s)
+    cont = O.verify(qg, kp[None], v[None], [L], w_q, c, s)
+    assert np.array_equal(paged, cont)
+    dec = O.verify_paged(qg_all[L:L + 1][None], kpool, vpool, order[None], page_size, [L],
+                         w_q, c, s)
+    full = O.prefill(qg_all, kp, v, w_q, c, s, 0, L + R)
+    assert np.array_equal(dec[0, 0], full[L])
+
+
 # ---------------------------------------------------------------- planted mistakes
 def test_planted_unrounded_sigmoid_is_caught(monkeypatch):
     """[QSA] §Validation, mutation calibration: dropping the sigmoid's bf16 rounding
