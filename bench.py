@@ -297,6 +297,7 @@ def run_gpu(args, world, rank, local):
 # ---------------------------------------------------------------- verify windows (config 5)
 V_ROWS, V_L = 16, 65536
 V_CAP = V_L + V_ROWS
+V_PAGE = 256   # positions per page of the paged-cache workload
 
 
 def verify_bytes(n_seq):
@@ -307,9 +308,13 @@ def verify_bytes(n_seq):
 
 def run_verify(args, world, rank, local):
     """Config 5 on one GPU (per rank): ga_attn_verify over prepared caches resident in HBM
-    (--verify-seqs sequences; 8 is the configuration, fewer only for profiling)."""
+    (--verify-seqs sequences; 8 is the configuration, fewer only for profiling). With
+    --workload verify_paged the same caches sit in pages of 256 positions scattered over
+    two page pools in a seeded random order, read through ga_attn_verify_paged."""
     V_SEQ = args.verify_seqs
-    V_METRIC = f"verify windows: HBM GB/s ({V_SEQ} sequences x 16 rows over L=65536 cached keys)"
+    paged = args.workload == "verify_paged"
+    V_METRIC = (f"verify windows{' over paged caches' if paged else ''}: HBM GB/s ({V_SEQ} "
+                "sequences x 16 rows over L=65536 cached keys)")
     V_BYTES = verify_bytes(V_SEQ)
     from verify_gated_gqa_gb300 import binding as B
     from verify_gated_gqa_gb300 import synth
@@ -336,9 +341,27 @@ def run_verify(args, world, rank, local):
     lens = [V_L] * V_SEQ
     out = torch.empty(V_SEQ, V_ROWS, HEADS * DIM, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(B.ga_verify_workspace_bytes(V_SEQ, V_ROWS, V_L), dtype=torch.uint8, device=dev)
+    if paged:
+        pages_per_seq = -(-V_CAP // V_PAGE)
+        n_pages = V_SEQ * pages_per_seq
+        order = torch.randperm(n_pages, generator=torch.Generator().manual_seed(seed))
+        table = order.view(V_SEQ, pages_per_seq).to(torch.int32).to(dev)
+        k_pool = torch.zeros(n_pages, V_PAGE, KV_HEADS, DIM, dtype=torch.bfloat16, device=dev)
+        v_pool = torch.zeros_like(k_pool)
+        for b in range(V_SEQ):
+            for p in range(pages_per_seq):
+                lo, hi = p * V_PAGE, min((p + 1) * V_PAGE, V_CAP)
+                pg = int(order[b * pages_per_seq + p])
+                k_pool[pg, :hi - lo] = k_cache[b, lo:hi]
+                v_pool[pg, :hi - lo] = v_cache[b, lo:hi]
+        del k_cache, v_cache
 
     def step():
-        B.ga_attn_verify(qg, k_cache, v_cache, lens, w_q, cos, sin, out=out, workspace=ws)
+        if paged:
+            B.ga_attn_verify_paged(qg, k_pool, v_pool, table, lens, w_q, cos, sin, out=out,
+                                   workspace=ws)
+        else:
+            B.ga_attn_verify(qg, k_cache, v_cache, lens, w_q, cos, sin, out=out, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -371,14 +394,16 @@ def run_verify(args, world, rank, local):
         "data": "synthetic (seeded N(0,1) activations, N(0,0.1) norm weights)",
         "config": {"workload": f"verify: {V_SEQ} sequences x 16 rows at positions 65536..65551 over "
                                "prepared K/V caches [65552, 2, 256] bf16, split-key partials "
-                               "and combine",
+                               "and combine" + (f"; caches in pages of {V_PAGE} positions, "
+                                                "scattered over two page pools" if paged else ""),
                    "l2": f"K/V caches {2 * V_SEQ * V_CAP * KV_HEADS * DIM * 2 / 1e9:.2f} GB"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                      "frac": round(gbs / peak_hbm, 4),
-                     "traffic": VERIFY_ATTN_TRAFFIC_BYTES if V_SEQ == 8 else None,
+                     "traffic": VERIFY_ATTN_TRAFFIC_BYTES if V_SEQ == 8 and not paged else None,
                      "traffic_kernel": "attn_kernel (verify variant), the call's dominant launch",
                      "peak_kind": f"HBM copy ({peak_src})",
-                     "kernel": "ga_attn_verify (Q prologue + attn_kernel<verify> + combine)",
+                     "kernel": f"ga_attn_verify{'_paged' if paged else ''} (Q prologue + "
+                               "attn_kernel<verify> + combine)",
                      "algorithmic_bytes": V_BYTES},
         "gpu_launches": 3 * args.steps, "clocks": clk, "device_status": B.ga_device_status(),
     }
@@ -487,14 +512,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--workload", default="prefill", choices=["prefill", "verify"],
-                    help="prefill: the headline S=8192 causal step; verify: config 5")
+    ap.add_argument("--workload", default="prefill", choices=["prefill", "verify", "verify_paged"],
+                    help="prefill: the headline S=8192 causal step; verify: config 5; "
+                         "verify_paged: config 5 over paged caches")
     ap.add_argument("--verify-seqs", type=int, default=8)
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, world, rank)
-    elif args.workload == "verify":
+    elif args.workload in ("verify", "verify_paged"):
         line = run_verify(args, world, rank, local)
     else:
         line = run_gpu(args, world, rank, local)

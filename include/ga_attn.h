@@ -99,8 +99,9 @@ int ga_last_cuda_error(void);
 unsigned long long ga_debug_cuda_calls(void);
 
 /* Reads the current device's status word, written by kernels whose bounded waits gave
- * up (0 = no error, 1 = wait timeout). Synchronises the device. clear != 0 resets the
- * word afterwards. */
+ * up or whose inputs failed a device-side check (0 = no error, 1 = wait timeout, 2 = bad
+ * launch configuration, 3 = a page-table entry outside the page pool, see
+ * ga_attn_verify_paged). Synchronises the device. clear != 0 resets the word afterwards. */
 int ga_device_status(int* status_out, int clear);
 
 /* Test hook for failure detection (no counterpart in the pages): launches a one-thread
@@ -243,13 +244,42 @@ size_t ga_verify_workspace_bytes(int n_seq, int rows, int max_len);
  *   seq_len  HOST array of n_seq ints: L_b, with L_b >= 0 and L_b + rows <= cap
  *   out      [n_seq][rows][24 * 256] (scratch during the call, as in ga_attn_prefill)
  *   workspace >= ga_verify_workspace_bytes(n_seq, rows, max L_b), 256-byte aligned
- * Row r of sequence b sees keys 0 .. L_b + r.
+ * Row r of sequence b sees keys 0 .. L_b + r. Cache positions from L_b + rows up to the
+ * end of the 128-key tile that holds position L_b + rows - 1 are read and hidden, so they
+ * must hold finite values (a hidden value still meets the tensor cores with weight 0).
  * Rules: 1 <= rows <= 16, cap <= GA_MAX_TOKENS, table_rows >= max L_b + rows.
  * Errors: NULL, SHAPE, RANGE, TABLE, ALIGN, WORKSPACE, DEVICE, CUDA. */
 int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_cache,
                    int cap, const int* seq_len, int n_seq, int rows, const ga_bf16* w_q,
                    const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
                    ga_bf16* out, void* workspace, size_t ws_bytes, ga_stream stream);
+
+/* ga_attn_verify over PAGED caches, and decode (rows = 1). pegainfer PR #1151, "feat(qwen4):
+ * add the QSA sparse-attention kernel and its golden", §Summary and §Limits name paged KV
+ * and decode as the next steps after its contiguous key array; the layout is the plain
+ * reading of a page table. Each sequence's positions live in fixed-size pages of two pools:
+ *   k_pages   [n_pages][page_size][2][256] PREPARED keys (as ga_k_prologue writes them)
+ *   v_pages   [n_pages][page_size][2][256] values
+ *   page_table DEVICE int32 [n_seq][max_pages]: position t of sequence b lives on page
+ *             page_table[b * max_pages + t / page_size], slot t % page_size. Only the
+ *             entries that cover positions 0 .. L_b + rows - 1 are read; each must lie in
+ *             [0, n_pages). An entry outside that range is not a fault: the kernel records
+ *             status 3 in the device status word (ga_device_status) and reads zeros for
+ *             that tile, so the call's outputs are then meaningless.
+ *   page_size a multiple of 128 (one or more 128-key tiles per page)
+ * Everything else (qg, seq_len on the HOST, rows, the tables, out, the workspace from
+ * ga_verify_workspace_bytes, the finite-values rule for hidden positions) is as in
+ * ga_attn_verify, and so are the results: the same sequence gives the same bits whether
+ * its caches are contiguous or paged. Pages may be shared between sequences (a common
+ * prefix) and need not be in any order. Nothing is allocated; the call keeps no pointer.
+ * Rules: 1 <= rows <= 16, L_b + rows <= max_pages * page_size and <= GA_MAX_TOKENS,
+ * table_rows >= max L_b + rows, page_table 4-byte aligned.
+ * Errors: NULL, SHAPE, RANGE, TABLE, ALIGN, WORKSPACE, DEVICE, CUDA. */
+int ga_attn_verify_paged(const ga_bf16* qg, const ga_bf16* k_pages, const ga_bf16* v_pages,
+                         int n_pages, int page_size, const int* page_table, int max_pages,
+                         const int* seq_len, int n_seq, int rows, const ga_bf16* w_q,
+                         const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
+                         ga_bf16* out, void* workspace, size_t ws_bytes, ga_stream stream);
 
 #ifdef __cplusplus
 }

@@ -147,6 +147,38 @@ def test_verify_refusals_make_no_cuda_call(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def _verify_paged(L, lens=(1000, 2000), **kw):
+    n = len(lens)
+    arr = (ctypes.c_int * n)(*lens)
+    wsb = L.ga_verify_workspace_bytes(n, 16, max(lens, default=0))
+    args = dict(qg=A, k=A, v=A, n_pages=40, page_size=256, pt=A, max_pages=16, arr=arr, n=n,
+                rows=16, wq=A, cos=A, sin=A, table=4096, out=A, ws=0x100000, wsb=wsb)
+    args.update(kw)
+    return L.ga_attn_verify_paged(args["qg"], args["k"], args["v"], args["n_pages"],
+                                  args["page_size"], args["pt"], args["max_pages"], args["arr"],
+                                  args["n"], args["rows"], args["wq"], args["cos"], args["sin"],
+                                  args["table"], args["out"], args["ws"], args["wsb"], S)
+
+
+def test_verify_paged_refusals_make_no_cuda_call(L):
+    cases = [
+        (dict(pt=None), -1), (dict(k=None), -1), (dict(arr=None), -1),
+        (dict(n_pages=0), -2), (dict(page_size=0), -2), (dict(max_pages=0), -2),
+        (dict(rows=17), -4), (dict(page_size=200), -4), (dict(page_size=(1 << 20) + 128), -4),
+        (dict(max_pages=7), -4),                     # 2000 + 16 positions need 8 pages of 256
+        (dict(lens=(5, -1)), -4), (dict(table=1000), -5), (dict(pt=A + 2), -3),
+        (dict(v=MIS), -3), (dict(ws=None), -6), (dict(wsb=0), -6),
+    ]
+    for kw, want in cases:
+        before = L.ga_debug_cuda_calls()
+        assert _verify_paged(L, **kw) == want, kw
+        assert L.ga_debug_cuda_calls() == before
+    before = L.ga_debug_cuda_calls()
+    assert _verify_paged(L, rows=0, wsb=256) == 0        # an empty call is a no-op
+    assert _verify_paged(L, lens=()) == 0
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_k_prologue_refusals(L):
     before = L.ga_debug_cuda_calls()
     assert L.ga_k_prologue(None, A, A, A, 100, 10, 0, A, S) == -1

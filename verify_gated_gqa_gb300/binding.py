@@ -49,6 +49,8 @@ _SIGS = {
                             _SZ, _P]),
     "ga_verify_workspace_bytes": (_SZ, [_I, _I, _I]),
     "ga_attn_verify": (_I, [_P, _P, _P, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P, _SZ, _P]),
+    "ga_attn_verify_paged": (_I, [_P, _P, _P, _I, _I, _P, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P,
+                                  _SZ, _P]),
 }
 
 
@@ -273,4 +275,33 @@ def ga_attn_verify(qg, k_cache, v_cache, seq_len, w_q, cos_tab, sin_tab, out=Non
                                 _ptr(w_q), _ptr(cos_tab), _ptr(sin_tab), cos_tab.shape[0],
                                 _ptr(out), _ptr(workspace), workspace.numel(), _stream()),
            "ga_attn_verify")
+    return out
+
+
+def ga_attn_verify_paged(qg, k_pages, v_pages, page_table, seq_len, w_q, cos_tab, sin_tab,
+                         out=None, workspace=None):
+    """qg [n_seq, rows, 24, 512]; k_pages, v_pages [n_pages, page_size, 2, 256];
+    page_table int32 [n_seq, max_pages] on the device; seq_len: ints (host)."""
+    n_seq, rows = qg.shape[0], qg.shape[1]
+    n_pages, page_size = k_pages.shape[0], k_pages.shape[1]
+    if (page_table.dtype != torch.int32 or not page_table.is_cuda or page_table.dim() != 2
+            or not page_table.is_contiguous() or page_table.shape[0] != n_seq):
+        raise ValueError("page_table must be a contiguous int32 CUDA tensor [n_seq, max_pages]")
+    if tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages and v_pages must have the same shape")
+    lens = (ctypes.c_int * n_seq)(*[int(x) for x in seq_len])
+    dev = qg.device
+    if out is None:
+        out = torch.empty(n_seq, rows, N_Q_HEADS * HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    ws_bytes = ga_verify_workspace_bytes(n_seq, rows, max(int(x) for x in seq_len))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    for n, t in (("qg", qg), ("k_pages", k_pages), ("v_pages", v_pages), ("w_q", w_q),
+                 ("cos_tab", cos_tab), ("sin_tab", sin_tab), ("out", out)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_attn_verify_paged(_ptr(qg), _ptr(k_pages), _ptr(v_pages), n_pages, page_size,
+                                      _ptr(page_table), page_table.shape[1], lens, n_seq, rows,
+                                      _ptr(w_q), _ptr(cos_tab), _ptr(sin_tab), cos_tab.shape[0],
+                                      _ptr(out), _ptr(workspace), workspace.numel(), _stream()),
+           "ga_attn_verify_paged")
     return out

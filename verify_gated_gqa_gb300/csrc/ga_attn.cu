@@ -233,12 +233,51 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
   };
   ItemWalk<kMode> walk;
   Item it;
+  const int lane = threadIdx.x & 31;
   while (walk.next(a, it)) {
     const int kvh = it.h / kGroup;
     TileCursor<kMode> ck(it), cv(it);
+    // Coordinates of key tile kt: token r0 and outer index (verify: the sequence, or with
+    // paged caches the page; -1 for the four-dimensional prefill map). For paged caches
+    // the warp holds a window of 32 consecutive page-table entries, one per lane, so one
+    // coalesced read serves 32 entries. An entry outside the pool is recorded in the
+    // status word and its tile read past the pool's end, which yields zeros.
+    int win0 = -1, win_page = 0;
+    auto kv_at = [&](int kt, int& r0) -> int {
+      if (kMode != kModeVerify) {
+        r0 = kt * kTileN;
+        return -1;
+      }
+      if (a.page_table == nullptr) {
+        r0 = kt * kTileN;
+        return it.seq;
+      }
+      const int e = kt / a.page_tiles;
+      r0 = (kt - e * a.page_tiles) * kTileN;
+      if (win0 < 0 || e < win0 || e >= win0 + 32) {
+        win0 = e;
+        const int idx = e + lane;
+        win_page = idx < a.max_pages ? __ldg(a.page_table + (size_t)it.seq * a.max_pages + idx) : 0;
+      }
+      int page = __shfl_sync(0xffffffffu, win_page, e - win0);
+      if (page < 0 || page >= a.n_pages) {
+        if (lane == 0) record_abort(a.status, kDevBadPage);
+        page = a.n_pages;
+      }
+      return page;
+    };
+    auto load_k = [&](int kt) -> bool {
+      int r0;
+      const int outer = kv_at(kt, r0);
+      return load_tile(tm_k, true, kvh, r0, outer, kTileBytes);
+    };
+    auto load_v = [&](int kt) -> bool {
+      int r0;
+      const int outer = kv_at(kt, r0);
+      return load_tile(tm_v, true, kvh, r0, outer, kTileBytes);
+    };
     // Ring order: the item's prepared Q (for the edge warps), then in MMA order K0,
     // (K_j, V_{j-1}) for j >= 1, V_{n-1}; the gate tile (gated passes) just before V_0.
-    const int kv_seq = kMode == kModeVerify ? it.seq : -1;
     if (kMode == kModeVerify) {
       if (!load_tile(tm_q, false, it.h, it.seq * a.vrows, -1,
                      4u * kVerifyHeadsPerTile * a.vrows * 128u)) return;
@@ -249,14 +288,14 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
       return !has_gate<kMode, kW>() ||
              load_tile(tm_g, false, it.h, it.mt * kTileM, -1, kTileBytes, kDim);
     };
-    if (!load_tile(tm_k, true, kvh, ck.next(0) * kTileN, kv_seq, kTileBytes)) return;
+    if (!load_k(ck.next(0))) return;
     for (int j = 1; j < it.n; ++j) {
-      if (!load_tile(tm_k, true, kvh, ck.next(j) * kTileN, kv_seq, kTileBytes)) return;
+      if (!load_k(ck.next(j))) return;
       if (j == 1 && !load_gate()) return;
-      if (!kW && !load_tile(tm_v, true, kvh, cv.next(j - 1) * kTileN, kv_seq, kTileBytes)) return;
+      if (!kW && !load_v(cv.next(j - 1))) return;
     }
     if (it.n == 1 && !load_gate()) return;
-    if (!kW && !load_tile(tm_v, true, kvh, cv.next(it.n - 1) * kTileN, kv_seq, kTileBytes)) return;
+    if (!kW && !load_v(cv.next(it.n - 1))) return;
   }
 }
 

@@ -295,6 +295,106 @@ int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const v
   return GA_OK;
 }
 
+// The verify call over contiguous caches (one [cap][2][256] cache per sequence) or paged
+// caches (page pools and a page table); the callers have checked the arguments that differ.
+struct VerifyCaches {
+  const ga_bf16* k;
+  const ga_bf16* v;
+  int cap;                  // contiguous: positions per sequence's cache
+  const int* page_table;    // paged: [n_seq][max_pages] device array, else null
+  int page_size, max_pages, n_pages;
+};
+
+int verify_run(const ga_bf16* qg, const VerifyCaches& c, const int* seq_len, int n_seq, int rows,
+               const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+               int table_rows, ga_bf16* out, void* workspace, size_t ws_bytes, ga_stream stream) {
+  int max_len = 0;
+  for (int b = 0; b < n_seq; ++b)
+    if (seq_len[b] > max_len) max_len = seq_len[b];
+  if ((long long)table_rows < (long long)max_len + rows) return GA_ERR_TABLE;
+  if (!aligned(qg, 16) || !aligned(c.k, 16) || !aligned(c.v, 16) || !aligned(w_q, 16) ||
+      !aligned(cos_tab, 16) || !aligned(sin_tab, 16) || !aligned(out, 16))
+    return GA_ERR_ALIGN;
+  if (n_seq == 0 || rows == 0) return GA_OK;
+  if (!workspace || !aligned(workspace, 256) ||
+      ws_bytes < ga_verify_workspace_bytes(n_seq, rows, max_len))
+    return GA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const VerifyPlan plan = verify_plan(n_seq, rows, max_len);
+  const size_t seq_elems = (size_t)c.cap * kKvHeads * kDim;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  for (int g0 = 0; g0 < n_seq; g0 += kVerifyMaxSeq) {
+    const int n = n_seq - g0 < kVerifyMaxSeq ? n_seq - g0 : kVerifyMaxSeq;
+    AttnArgs a{};
+    a.qg = qg + (size_t)g0 * rows * kRowElems;
+    a.out = out + (size_t)g0 * rows * kOutRow;
+    a.mode = kModeVerify;
+    a.n_seq = n;
+    a.vrows = rows;
+    SeqPositions sp{};
+    sp.rows_per_seq = rows;
+    int tiles_max = 1;
+    for (int b = 0; b < n; ++b) {
+      a.seq_len[b] = seq_len[g0 + b];
+      sp.seq_base[b] = seq_len[g0 + b];
+      const int t = (seq_len[g0 + b] + rows + kTileN - 1) / kTileN;
+      if (t > tiles_max) tiles_max = t;
+    }
+    // The chunk count (at most the workspace's) that minimises the busiest SM's key tiles:
+    // ceil(items / SMs) items of chunk_tiles tiles each, ties to fewer chunks (fewer partials).
+    int best_nc = 1;
+    long long best_cost = -1;
+    for (int nc = 1; nc <= plan.n_chunks_cap && nc <= tiles_max; ++nc) {
+      const int ct = (tiles_max + nc - 1) / nc;
+      const long long items = 4LL * n * ((tiles_max + ct - 1) / ct);
+      const long long cost = (items + dev->sm_count - 1) / dev->sm_count * ct;
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_nc = nc;
+      }
+    }
+    a.chunk_tiles = (tiles_max + best_nc - 1) / best_nc;
+    a.n_chunks = (tiles_max + a.chunk_tiles - 1) / a.chunk_tiles;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_ml = reinterpret_cast<float*>(ws + verify_part_o_bytes(plan));
+    a.n_items = a.n_chunks * n * 4;
+    a.status = dev->status_word;
+    a.rows = n * rows;
+    cudaError_t e;
+    if ((e = GA_CUDA(launch_q_prologue_seq(a.qg, w_q, cos_tab, sin_tab, n * rows, sp, a.out, s))) !=
+        cudaSuccess)
+      return fail_cuda(e);
+    CUtensorMap tm_q, tm_k, tm_v;
+    st = encode_q_map(&tm_q, a.out, (long long)n * rows, kVerifyHeadsPerTile, rows);
+    if (st != GA_OK) return st;
+    if (c.page_table) {
+      // the whole pools, the page as the outer coordinate
+      st = encode_kv_map(&tm_k, c.k, c.page_size, c.n_pages, true);
+      if (st != GA_OK) return st;
+      st = encode_kv_map(&tm_v, c.v, c.page_size, c.n_pages, true);
+      if (st != GA_OK) return st;
+      a.page_table = c.page_table + (size_t)g0 * c.max_pages;
+      a.page_tiles = c.page_size / kTileN;
+      a.max_pages = c.max_pages;
+      a.n_pages = c.n_pages;
+    } else {
+      st = encode_kv_map(&tm_k, c.k + (size_t)g0 * seq_elems, c.cap, n, true);
+      if (st != GA_OK) return st;
+      st = encode_kv_map(&tm_v, c.v + (size_t)g0 * seq_elems, c.cap, n, true);
+      if (st != GA_OK) return st;
+    }
+    const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
+    // the verify partials have no gated epilogue: tm_q stands in for the unused gate map
+    if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_q, a, grid, s))) != cudaSuccess)
+      return fail_cuda(e);
+    if ((e = GA_CUDA(launch_verify_combine(a, s))) != cudaSuccess) return fail_cuda(e);
+  }
+  return GA_OK;
+}
+
 }  // namespace
 }  // namespace ga
 
@@ -522,81 +622,41 @@ int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_c
     return GA_ERR_NULL;
   if (n_seq < 0 || rows < 0 || cap < 1 || table_rows < 0) return GA_ERR_SHAPE;
   if (rows > 16 || cap > GA_MAX_TOKENS) return GA_ERR_RANGE;
-  int max_len = 0;
-  for (int b = 0; b < n_seq; ++b) {
+  for (int b = 0; b < n_seq; ++b)
     if (seq_len[b] < 0 || (long long)seq_len[b] + rows > cap) return GA_ERR_RANGE;
-    if (seq_len[b] > max_len) max_len = seq_len[b];
-  }
-  if ((long long)table_rows < (long long)max_len + rows) return GA_ERR_TABLE;
-  if (!aligned(qg, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(w_q, 16) ||
-      !aligned(cos_tab, 16) || !aligned(sin_tab, 16) || !aligned(out, 16))
-    return GA_ERR_ALIGN;
-  if (n_seq == 0 || rows == 0) return GA_OK;
-  if (!workspace || !aligned(workspace, 256) ||
-      ws_bytes < ga_verify_workspace_bytes(n_seq, rows, max_len))
-    return GA_ERR_WORKSPACE;
-  DeviceState* dev = nullptr;
-  int st = current_device(&dev);
-  if (st != GA_OK) return st;
-  cudaStream_t s = (cudaStream_t)stream;
-  const VerifyPlan plan = verify_plan(n_seq, rows, max_len);
-  const size_t seq_elems = (size_t)cap * kKvHeads * kDim;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  for (int g0 = 0; g0 < n_seq; g0 += kVerifyMaxSeq) {
-    const int n = n_seq - g0 < kVerifyMaxSeq ? n_seq - g0 : kVerifyMaxSeq;
-    AttnArgs a{};
-    a.qg = qg + (size_t)g0 * rows * kRowElems;
-    a.out = out + (size_t)g0 * rows * kOutRow;
-    a.mode = kModeVerify;
-    a.n_seq = n;
-    a.vrows = rows;
-    SeqPositions sp{};
-    sp.rows_per_seq = rows;
-    int tiles_max = 1;
-    for (int b = 0; b < n; ++b) {
-      a.seq_len[b] = seq_len[g0 + b];
-      sp.seq_base[b] = seq_len[g0 + b];
-      const int t = (seq_len[g0 + b] + rows + kTileN - 1) / kTileN;
-      if (t > tiles_max) tiles_max = t;
-    }
-    // The chunk count (at most the workspace's) that minimises the busiest SM's key tiles:
-    // ceil(items / SMs) items of chunk_tiles tiles each, ties to fewer chunks (fewer partials).
-    int best_nc = 1;
-    long long best_cost = -1;
-    for (int nc = 1; nc <= plan.n_chunks_cap && nc <= tiles_max; ++nc) {
-      const int ct = (tiles_max + nc - 1) / nc;
-      const long long items = 4LL * n * ((tiles_max + ct - 1) / ct);
-      const long long cost = (items + dev->sm_count - 1) / dev->sm_count * ct;
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
-        best_nc = nc;
-      }
-    }
-    a.chunk_tiles = (tiles_max + best_nc - 1) / best_nc;
-    a.n_chunks = (tiles_max + a.chunk_tiles - 1) / a.chunk_tiles;
-    a.part_o = reinterpret_cast<float*>(ws);
-    a.part_ml = reinterpret_cast<float*>(ws + verify_part_o_bytes(plan));
-    a.n_items = a.n_chunks * n * 4;
-    a.status = dev->status_word;
-    a.rows = n * rows;
-    cudaError_t e;
-    if ((e = GA_CUDA(launch_q_prologue_seq(a.qg, w_q, cos_tab, sin_tab, n * rows, sp, a.out, s))) !=
-        cudaSuccess)
-      return fail_cuda(e);
-    CUtensorMap tm_q, tm_k, tm_v;
-    st = encode_q_map(&tm_q, a.out, (long long)n * rows, kVerifyHeadsPerTile, rows);
-    if (st != GA_OK) return st;
-    st = encode_kv_map(&tm_k, k_cache + (size_t)g0 * seq_elems, cap, n, true);
-    if (st != GA_OK) return st;
-    st = encode_kv_map(&tm_v, v_cache + (size_t)g0 * seq_elems, cap, n, true);
-    if (st != GA_OK) return st;
-    const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
-    // the verify partials have no gated epilogue: tm_q stands in for the unused gate map
-    if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_q, a, grid, s))) != cudaSuccess)
-      return fail_cuda(e);
-    if ((e = GA_CUDA(launch_verify_combine(a, s))) != cudaSuccess) return fail_cuda(e);
-  }
-  return GA_OK;
+  VerifyCaches c{};
+  c.k = k_cache;
+  c.v = v_cache;
+  c.cap = cap;
+  return verify_run(qg, c, seq_len, n_seq, rows, w_q, cos_tab, sin_tab, table_rows, out,
+                    workspace, ws_bytes, stream);
+}
+
+int ga_attn_verify_paged(const ga_bf16* qg, const ga_bf16* k_pages, const ga_bf16* v_pages,
+                         int n_pages, int page_size, const int* page_table, int max_pages,
+                         const int* seq_len, int n_seq, int rows, const ga_bf16* w_q,
+                         const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
+                         ga_bf16* out, void* workspace, size_t ws_bytes, ga_stream stream) {
+  if (!qg || !k_pages || !v_pages || !page_table || !seq_len || !w_q || !cos_tab || !sin_tab ||
+      !out)
+    return GA_ERR_NULL;
+  if (n_seq < 0 || rows < 0 || n_pages < 1 || page_size < 1 || max_pages < 1 || table_rows < 0)
+    return GA_ERR_SHAPE;
+  if (rows > 16 || page_size % kTileN != 0 || page_size > GA_MAX_TOKENS) return GA_ERR_RANGE;
+  for (int b = 0; b < n_seq; ++b)
+    if (seq_len[b] < 0 || (long long)seq_len[b] + rows > (long long)max_pages * page_size ||
+        (long long)seq_len[b] + rows > GA_MAX_TOKENS)
+      return GA_ERR_RANGE;
+  if (!aligned(page_table, 4)) return GA_ERR_ALIGN;
+  VerifyCaches c{};
+  c.k = k_pages;
+  c.v = v_pages;
+  c.page_table = page_table;
+  c.page_size = page_size;
+  c.max_pages = max_pages;
+  c.n_pages = n_pages;
+  return verify_run(qg, c, seq_len, n_seq, rows, w_q, cos_tab, sin_tab, table_rows, out,
+                    workspace, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------ allocation-free masked call

@@ -61,6 +61,11 @@ struct AttnArgs {
   int seq_len[kVerifyMaxSeq];   // L per sequence: row rr sits at position L + rr
   float* part_o;                // [n_seq][2][2][n_chunks][96][256]
   float* part_ml;               // [n_seq][2][2][n_chunks][96][2]: M, l
+  // verify over paged caches (page_table null: contiguous caches, one per sequence):
+  // key tile kt of sequence b is slot (kt % page_tiles) * 128 of page
+  // page_table[b * max_pages + kt / page_tiles] of the page pools
+  const int* page_table;
+  int page_tiles, max_pages, n_pages;
 };
 
 // Launchers (defined next to their kernels). Return a cudaError_t.

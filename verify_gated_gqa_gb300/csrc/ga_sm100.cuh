@@ -19,6 +19,7 @@ enum DeviceStatus : int {
   kDevOk = 0,
   kDevWaitTimeout = 1,
   kDevBadLaunch = 2,
+  kDevBadPage = 3,   // a page-table entry outside the page pool (the tile reads zeros)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
