@@ -281,6 +281,38 @@ int ga_attn_verify_paged(const ga_bf16* qg, const ga_bf16* k_pages, const ga_bf1
                          const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
                          ga_bf16* out, void* workspace, size_t ws_bytes, ga_stream stream);
 
+/* Several causal prefills in one call: sequences (or branches) of different lengths, each a
+ * window of rows at its own q_base over its own paged cache. system1-omni PR #99, "run
+ * prompts that share prefixes once per prefix", and PR #196, "perf(open-jev): optimize 9B
+ * prefill while preserving native outputs" (its batched gated-attention entry points,
+ * checked bit for bit against the one-sequence path): prompts that share a prefix run the
+ * prefix once and continue each branch from it. Here a branch is a sequence whose page-table
+ * row lists the prefix's pages (whole pages, shared) and then its own; its rows are its
+ * positions after the prefix (q_base = the prefix length).
+ *   qg          [total_rows][24][512] fused rows of all sequences, packed: sequence b's row r
+ *               is packed row row_start[b] + r, at position q_base[b] + r
+ *   row_start   HOST int[n_seq + 1], ascending, row_start[0] >= 0; sequence b has
+ *               row_start[b + 1] - row_start[b] >= 0 rows
+ *   q_base      HOST int[n_seq], multiples of 64
+ *   k_pages, v_pages, n_pages, page_size, page_table, max_pages: as in ga_attn_verify_paged;
+ *               sequence b's keys 0 .. q_base[b] + rows_b - 1 are read through page-table
+ *               row b (they must be prepared and present, the window's own keys included)
+ *   out         [total_rows][24 * 256] (scratch during the call, as in ga_attn_prefill)
+ * Row r of sequence b sees keys 0 .. q_base[b] + r. Every sequence's rows come out with the
+ * same bits as ga_attn_prefill gives for them over the same keys (causal, window q_base[b],
+ * T = q_base[b] + rows_b). The kernels handle up to 64 sequences and 256 row tiles of 128
+ * rows per launch and the call launches as many times as needed; nothing is allocated and
+ * no pointer is kept. Hidden positions read inside a window's last key tile must be finite.
+ * Rules: page_size a multiple of 128, q_base[b] + rows_b <= max_pages * page_size and
+ * <= GA_MAX_TOKENS, row_start[n_seq] <= GA_MAX_TOKENS, table_rows >= max q_base[b] + rows_b,
+ * page_table 4-byte aligned. A call with no rows returns GA_OK without a CUDA call.
+ * Errors: NULL, SHAPE, RANGE, TABLE, ALIGN, DEVICE, CUDA. */
+int ga_attn_prefill_batch(const ga_bf16* qg, const int* row_start, const int* q_base, int n_seq,
+                          const ga_bf16* k_pages, const ga_bf16* v_pages, int n_pages,
+                          int page_size, const int* page_table, int max_pages,
+                          const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                          int table_rows, ga_bf16* out, ga_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

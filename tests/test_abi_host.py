@@ -179,6 +179,41 @@ def test_verify_paged_refusals_make_no_cuda_call(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def _batch(L, starts=(0, 300, 300, 1000), bases=(0, 64, 1024), **kw):
+    n = len(bases)
+    st = (ctypes.c_int * len(starts))(*starts)
+    qb = (ctypes.c_int * max(n, 1))(*bases)
+    args = dict(qg=A, st=st, qb=qb, n=n, k=A, v=A, n_pages=64, page_size=128, pt=A,
+                max_pages=16, wq=A, cos=A, sin=A, table=4096, out=A)
+    args.update(kw)
+    return L.ga_attn_prefill_batch(args["qg"], args["st"], args["qb"], args["n"], args["k"],
+                                   args["v"], args["n_pages"], args["page_size"], args["pt"],
+                                   args["max_pages"], args["wq"], args["cos"], args["sin"],
+                                   args["table"], args["out"], S)
+
+
+def test_prefill_batch_refusals_make_no_cuda_call(L):
+    cases = [
+        (dict(qg=None), -1), (dict(st=None), -1), (dict(pt=None), -1), (dict(out=None), -1),
+        (dict(n=-1), -2), (dict(n_pages=0), -2), (dict(max_pages=0), -2),
+        (dict(starts=(0, 300, 200, 1000)), -2),          # a sequence with -100 rows
+        (dict(starts=(-5, 300, 300, 1000)), -2),
+        (dict(bases=(0, 65, 1024)), -4), (dict(bases=(0, -64, 1024)), -4),
+        (dict(page_size=192), -4),
+        (dict(max_pages=13), -4),                         # 1024 + 700 keys need 14 pages
+        (dict(table=1700), -5),                           # the longest window ends at 1724
+        (dict(pt=A + 1), -3), (dict(k=MIS), -3), (dict(out=MIS), -3),
+    ]
+    for kw, want in cases:
+        before = L.ga_debug_cuda_calls()
+        assert _batch(L, **kw) == want, kw
+        assert L.ga_debug_cuda_calls() == before
+    before = L.ga_debug_cuda_calls()
+    assert _batch(L, starts=(0, 0, 0, 0)) == 0            # no rows: a no-op
+    assert _batch(L, starts=(7,), bases=()) == 0           # no sequences
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_k_prologue_refusals(L):
     before = L.ga_debug_cuda_calls()
     assert L.ga_k_prologue(None, A, A, A, 100, 10, 0, A, S) == -1

@@ -51,6 +51,8 @@ _SIGS = {
     "ga_attn_verify": (_I, [_P, _P, _P, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P, _SZ, _P]),
     "ga_attn_verify_paged": (_I, [_P, _P, _P, _I, _I, _P, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P,
                                   _SZ, _P]),
+    "ga_attn_prefill_batch": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _P, _I, _P, _P, _P, _I, _P,
+                                   _P]),
 }
 
 
@@ -304,4 +306,34 @@ def ga_attn_verify_paged(qg, k_pages, v_pages, page_table, seq_len, w_q, cos_tab
                                       _ptr(w_q), _ptr(cos_tab), _ptr(sin_tab), cos_tab.shape[0],
                                       _ptr(out), _ptr(workspace), workspace.numel(), _stream()),
            "ga_attn_verify_paged")
+    return out
+
+
+def ga_attn_prefill_batch(qg, row_start, q_base, k_pages, v_pages, page_table, w_q, cos_tab,
+                          sin_tab, out=None):
+    """qg [total_rows, 24, 512] packed; row_start: n_seq + 1 ints; q_base: n_seq ints (host);
+    k_pages, v_pages [n_pages, page_size, 2, 256]; page_table int32 [n_seq, max_pages] on the
+    device. Returns out [total_rows, 24*256]."""
+    n_seq = len(q_base)
+    if len(row_start) != n_seq + 1:
+        raise ValueError("row_start needs n_seq + 1 entries")
+    n_pages, page_size = k_pages.shape[0], k_pages.shape[1]
+    if (page_table.dtype != torch.int32 or not page_table.is_cuda or page_table.dim() != 2
+            or not page_table.is_contiguous() or page_table.shape[0] != n_seq):
+        raise ValueError("page_table must be a contiguous int32 CUDA tensor [n_seq, max_pages]")
+    if tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages and v_pages must have the same shape")
+    starts = (ctypes.c_int * (n_seq + 1))(*[int(x) for x in row_start])
+    bases = (ctypes.c_int * max(n_seq, 1))(*[int(x) for x in q_base])
+    total = qg.shape[0]
+    if out is None:
+        out = torch.empty(total, N_Q_HEADS * HEAD_DIM, dtype=torch.bfloat16, device=qg.device)
+    for n, t in (("qg", qg), ("k_pages", k_pages), ("v_pages", v_pages), ("w_q", w_q),
+                 ("cos_tab", cos_tab), ("sin_tab", sin_tab), ("out", out)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_attn_prefill_batch(_ptr(qg), starts, bases, n_seq, _ptr(k_pages),
+                                       _ptr(v_pages), n_pages, page_size, _ptr(page_table),
+                                       page_table.shape[1], _ptr(w_q), _ptr(cos_tab),
+                                       _ptr(sin_tab), cos_tab.shape[0], _ptr(out), _stream()),
+           "ga_attn_prefill_batch")
     return out

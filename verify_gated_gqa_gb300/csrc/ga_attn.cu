@@ -108,8 +108,15 @@ struct Item {
   int h, mt;          // query head (verify: the first query head of the half), 128-row tile
   int n;              // key tiles to visit
   int seq, half, kt0; // verify: sequence, half of the query group, first key tile of the chunk
+                      // (batch: seq is the item's sequence)
+  int row0, rows, qb, T;  // the item's sequence: first (packed) row, rows, position of its
+                          // row 0 (q_base), keys; the call's own values outside batch mode
   uint64_t tiles[2];  // mask mode: bit kt set for every key tile with a visible key
 };
+
+// Causal visibility (key j <= position of the row), for one sequence or a batch of them.
+template <int kMode>
+__host__ __device__ constexpr bool is_causal() { return kMode == kModeCausal || kMode == kModeBatch; }
 
 __device__ __forceinline__ int item_index(int round, int cta, int G) {
   return round * G + ((round & 1) ? (G - 1 - cta) : cta);
@@ -120,6 +127,24 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
   Item it;
   it.seq = it.half = it.kt0 = 0;
   it.tiles[0] = it.tiles[1] = 0;
+  it.row0 = 0;
+  it.rows = a.rows;
+  it.qb = a.q_base;
+  it.T = a.T;
+  if (kMode == kModeBatch) {
+    const uint32_t e = a.batch_entry[idx / kHeads];
+    const int piece = (int)(e >> 16);
+    it.h = idx % kHeads;
+    it.mt = (int)(e & 0xFFFFu);
+    it.seq = a.batch_seq[piece];
+    it.row0 = a.batch_row0[piece];
+    it.rows = a.batch_rows[piece];
+    it.qb = a.batch_qbase[piece];
+    it.T = it.qb + it.rows;
+    const int last_row = min(it.rows, (it.mt + 1) * kTileM) - 1;
+    it.n = (it.qb + last_row + 1 + kTileN - 1) / kTileN;
+    return it;
+  }
   if (kMode == kModeVerify) {
     // (chunk, sequence, KV head, half): the two halves of a query group are neighbours, so
     // the CTAs that run them read each K/V tile at about the same time (the second from L2)
@@ -244,7 +269,7 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
     // status word and its tile read past the pool's end, which yields zeros.
     int win0 = -1, win_page = 0;
     auto kv_at = [&](int kt, int& r0) -> int {
-      if (kMode != kModeVerify) {
+      if (kMode != kModeVerify && kMode != kModeBatch) {
         r0 = kt * kTileN;
         return -1;
       }
@@ -282,11 +307,11 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
       if (!load_tile(tm_q, false, it.h, it.seq * a.vrows, -1,
                      4u * kVerifyHeadsPerTile * a.vrows * 128u)) return;
     } else {
-      if (!load_tile(tm_q, false, it.h, it.mt * kTileM, -1, kTileBytes)) return;
+      if (!load_tile(tm_q, false, it.h, it.row0 + it.mt * kTileM, -1, kTileBytes)) return;
     }
     auto load_gate = [&]() -> bool {
       return !has_gate<kMode, kW>() ||
-             load_tile(tm_g, false, it.h, it.mt * kTileM, -1, kTileBytes, kDim);
+             load_tile(tm_g, false, it.h, it.row0 + it.mt * kTileM, -1, kTileBytes, kDim);
     };
     if (!load_k(ck.next(0))) return;
     for (int j = 1; j < it.n; ++j) {
@@ -477,8 +502,8 @@ template <int kMode>
 __device__ __forceinline__ bool tile_full(const AttnArgs& a, const Item& it, int kt) {
   if (kMode == kModeMask) return false;
   if (kMode == kModeVerify) return (kt + 1) * kTileN - 1 <= a.seq_len[it.seq];
-  if ((it.mt + 1) * kTileM > a.rows || (kt + 1) * kTileN > a.T) return false;
-  if (kMode == kModeCausal) return (kt + 1) * kTileN - 1 <= a.q_base + it.mt * kTileM;
+  if ((it.mt + 1) * kTileM > it.rows || (kt + 1) * kTileN > it.T) return false;
+  if (is_causal<kMode>()) return (kt + 1) * kTileN - 1 <= it.qb + it.mt * kTileM;
   return true;
 }
 
@@ -528,10 +553,10 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
   ItemWalk<kMode> walk;
   Item it;
   while (walk.next(a, it)) {
-    const int row = it.mt * kTileM + r;
-    const bool valid = kMode == kModeVerify ? r < kVerifyHeadsPerTile * a.vrows : row < a.rows;
+    const int row = it.mt * kTileM + r;   // the row within its sequence
+    const bool valid = kMode == kModeVerify ? r < kVerifyHeadsPerTile * a.vrows : row < it.rows;
     const int limit = kMode == kModeVerify ? a.seq_len[it.seq] + r / kVerifyHeadsPerTile
-                                           : a.q_base + row;
+                                           : it.qb + row;
     const int h = it.h;
     int M = 0;
     bool hasM = false;
@@ -764,8 +789,8 @@ __device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r, bool
 __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32_t tmem,
                          uint32_t lane_off, int r, uint32_t it_done, uint4 (&sg)[kDim / 8],
                          volatile int* abort) {
-  const int row = it.mt * kTileM + r;
-  const bool valid = row < a.rows;
+  const int row = it.mt * kTileM + r;   // the row within its sequence
+  const bool valid = row < it.rows;
   const int h = it.h;
   if (!warp_wait(&sm.st_full, it_done & 1, abort)) return false;
   const float l = sm.stat_l[0][r] + sm.stat_l[1][r];
@@ -773,7 +798,8 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
   if (!warp_wait(&sm.o_done, it_done & 1, abort)) return false;
   tc_fence_after();
   const float inv = l > 0.f ? 1.0f / l : 0.f;
-  uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)(valid ? row : 0) * kOutRow + h * kDim);
+  uint4* op =
+      reinterpret_cast<uint4*>(a.out + (size_t)(valid ? it.row0 + row : 0) * kOutRow + h * kDim);
   const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;   // rows are 12 KiB apart
 #pragma unroll 1
   for (int c = 0; c < kDim / 64; ++c) {
@@ -1124,6 +1150,9 @@ cudaError_t attn_set_smem_attribute() {
   if ((e = cudaFuncSetAttribute(attn_kernel<kModeVerify, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
+  if ((e = cudaFuncSetAttribute(attn_kernel<kModeBatch, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+    return e;
   return cudaFuncSetAttribute(attn_kernel<kModeMask, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
@@ -1140,6 +1169,8 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
     attn_kernel<kModeBidir, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else if (a.mode == kModeVerify) {
     attn_kernel<kModeVerify, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+  } else if (a.mode == kModeBatch) {
+    attn_kernel<kModeBatch, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else {
     attn_kernel<kModeMask, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   }

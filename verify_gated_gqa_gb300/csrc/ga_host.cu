@@ -3,7 +3,9 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "ga_internal.h"
 
@@ -395,6 +397,94 @@ int verify_run(const ga_bf16* qg, const VerifyCaches& c, const int* seq_len, int
   return GA_OK;
 }
 
+// Several causal prefills (each a window of rows at its own q_base over its own paged
+// cache) in as few launches as the per-launch tables allow. A sequence of more than
+// kBatchMaxEntries row tiles is cut into windows of that many tiles, each a piece of its own.
+struct BatchPiece {
+  int seq, row0, rows, qbase;
+};
+
+int batch_run(const ga_bf16* qg, const BatchPiece* pieces, int n_pieces, const ga_bf16* k_pages,
+              const ga_bf16* v_pages, int n_pages, int page_size, const int* page_table,
+              int max_pages, const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+              ga_bf16* out, ga_stream stream) {
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  CUtensorMap tm_k, tm_v;
+  st = encode_kv_map(&tm_k, k_pages, page_size, n_pages, true);
+  if (st != GA_OK) return st;
+  st = encode_kv_map(&tm_v, v_pages, page_size, n_pages, true);
+  if (st != GA_OK) return st;
+  int p0 = 0;
+  while (p0 < n_pieces) {
+    // the next group: consecutive pieces, at most kVerifyMaxSeq of them and kBatchMaxEntries
+    // row tiles in all (every piece has at most kBatchMaxEntries tiles)
+    int p1 = p0, entries = 0;
+    while (p1 < n_pieces && p1 - p0 < kVerifyMaxSeq) {
+      const int t = (pieces[p1].rows + kTileM - 1) / kTileM;
+      if (entries + t > kBatchMaxEntries) break;
+      entries += t;
+      ++p1;
+    }
+    AttnArgs a{};
+    const int grp_row0 = pieces[p0].row0;
+    const int grp_rows = pieces[p1 - 1].row0 + pieces[p1 - 1].rows - grp_row0;
+    a.qg = qg + (size_t)grp_row0 * kRowElems;
+    a.out = out + (size_t)grp_row0 * kOutRow;
+    a.mode = kModeBatch;
+    a.rows = grp_rows;
+    a.n_seq = p1 - p0;
+    a.page_table = page_table;
+    a.page_tiles = page_size / kTileN;
+    a.max_pages = max_pages;
+    a.n_pages = n_pages;
+    a.status = dev->status_word;
+    SeqPositions sp{};
+    sp.n_seq = p1 - p0;
+    std::vector<std::pair<int, uint32_t>> order;   // (key tiles, entry)
+    for (int p = p0; p < p1; ++p) {
+      const int i = p - p0;
+      a.batch_seq[i] = pieces[p].seq;
+      a.batch_row0[i] = pieces[p].row0 - grp_row0;
+      a.batch_rows[i] = pieces[p].rows;
+      a.batch_qbase[i] = pieces[p].qbase;
+      sp.row_start[i] = pieces[p].row0 - grp_row0;
+      sp.seq_base[i] = pieces[p].qbase;
+      const int tiles = (pieces[p].rows + kTileM - 1) / kTileM;
+      for (int mt = 0; mt < tiles; ++mt) {
+        const int last_row = std::min(pieces[p].rows, (mt + 1) * kTileM) - 1;
+        const int n = (pieces[p].qbase + last_row + 1 + kTileN - 1) / kTileN;
+        order.push_back({n, ((uint32_t)i << 16) | (uint32_t)mt});
+      }
+    }
+    sp.row_start[p1 - p0] = grp_rows;
+    // the tiles with the most keys first, so each CTA's share of the work evens out
+    std::stable_sort(order.begin(), order.end(),
+                     [](const std::pair<int, uint32_t>& x, const std::pair<int, uint32_t>& y) {
+                       return x.first > y.first;
+                     });
+    a.n_entries = (int)order.size();
+    for (int i = 0; i < a.n_entries; ++i) a.batch_entry[i] = order[i].second;
+    a.n_items = a.n_entries * kHeads;
+    cudaError_t e;
+    if ((e = GA_CUDA(launch_q_prologue_seq(a.qg, w_q, cos_tab, sin_tab, grp_rows, sp, a.out, s))) !=
+        cudaSuccess)
+      return fail_cuda(e);
+    CUtensorMap tm_q, tm_g;
+    st = encode_q_map(&tm_q, a.out, grp_rows);
+    if (st != GA_OK) return st;
+    st = encode_gate_map(&tm_g, a.qg, grp_rows);
+    if (st != GA_OK) return st;
+    const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
+    if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_g, a, grid, s))) != cudaSuccess)
+      return fail_cuda(e);
+    p0 = p1;
+  }
+  return GA_OK;
+}
+
 }  // namespace
 }  // namespace ga
 
@@ -657,6 +747,46 @@ int ga_attn_verify_paged(const ga_bf16* qg, const ga_bf16* k_pages, const ga_bf1
   c.n_pages = n_pages;
   return verify_run(qg, c, seq_len, n_seq, rows, w_q, cos_tab, sin_tab, table_rows, out,
                     workspace, ws_bytes, stream);
+}
+
+int ga_attn_prefill_batch(const ga_bf16* qg, const int* row_start, const int* q_base, int n_seq,
+                          const ga_bf16* k_pages, const ga_bf16* v_pages, int n_pages,
+                          int page_size, const int* page_table, int max_pages, const ga_bf16* w_q,
+                          const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
+                          ga_bf16* out, ga_stream stream) {
+  if (!qg || !row_start || !q_base || !k_pages || !v_pages || !page_table || !w_q || !cos_tab ||
+      !sin_tab || !out)
+    return GA_ERR_NULL;
+  if (n_seq < 0 || n_pages < 1 || page_size < 1 || max_pages < 1 || table_rows < 0 ||
+      row_start[0] < 0)
+    return GA_ERR_SHAPE;
+  if (page_size % kTileN != 0 || page_size > GA_MAX_TOKENS) return GA_ERR_RANGE;
+  long long max_T = 0;
+  for (int b = 0; b < n_seq; ++b) {
+    const long long rows = (long long)row_start[b + 1] - row_start[b];
+    if (rows < 0) return GA_ERR_SHAPE;
+    if (q_base[b] < 0 || q_base[b] % 64 != 0) return GA_ERR_RANGE;
+    const long long T = (long long)q_base[b] + rows;
+    if (T > (long long)max_pages * page_size || T > GA_MAX_TOKENS) return GA_ERR_RANGE;
+    if (T > max_T) max_T = T;
+  }
+  if (row_start[n_seq] > GA_MAX_TOKENS) return GA_ERR_RANGE;
+  if ((long long)table_rows < max_T) return GA_ERR_TABLE;
+  if (!aligned(qg, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(w_q, 16) ||
+      !aligned(cos_tab, 16) || !aligned(sin_tab, 16) || !aligned(out, 16) ||
+      !aligned(page_table, 4))
+    return GA_ERR_ALIGN;
+  std::vector<BatchPiece> pieces;
+  for (int b = 0; b < n_seq; ++b) {
+    const int rows = row_start[b + 1] - row_start[b];
+    for (int r0 = 0; r0 < rows; r0 += kBatchMaxEntries * kTileM) {
+      const int n = std::min(rows - r0, kBatchMaxEntries * kTileM);
+      pieces.push_back({b, row_start[b] + r0, n, q_base[b] + r0});
+    }
+  }
+  if (pieces.empty()) return GA_OK;
+  return batch_run(qg, pieces.data(), (int)pieces.size(), k_pages, v_pages, n_pages, page_size,
+                   page_table, max_pages, w_q, cos_tab, sin_tab, out, stream);
 }
 
 // ------------------------------------------------------------------ allocation-free masked call

@@ -30,7 +30,14 @@ enum AttnMode : int {
   kModeBidir = 1,    // every key j < T
   kModeMask = 2,     // stored bit mask (from the mask prepass)
   kModeVerify = 3,   // few-row windows over long caches: split-key partials (see below)
+  kModeBatch = 4,    // several causal prefills (windows) over paged caches in one launch
 };
+
+// Batch mode: sequence b's rows are packed rows batch_row0[b] .. + batch_rows[b] - 1 (row r
+// at position batch_qbase[b] + r, seeing keys 0 .. batch_qbase[b] + r of its own paged
+// cache). A work item is (row tile entry, query head); the entries, (b << 16) | mt, are
+// sorted by the host so that the tiles with the most keys come first.
+constexpr int kBatchMaxEntries = 256;   // 128-row tiles per launch (the host loops over groups)
 
 // Verify mode: a work item is (sequence, KV head, half of the query group, key chunk). Its
 // 128-lane row tile packs 6 query heads x vrows rows of one sequence (lane 6 rr + hh for
@@ -66,6 +73,11 @@ struct AttnArgs {
   // page_table[b * max_pages + kt / page_tiles] of the page pools
   const int* page_table;
   int page_tiles, max_pages, n_pages;
+  // batch mode (n_seq sequences, n_items = n_entries * 24)
+  int n_entries;
+  int batch_row0[kVerifyMaxSeq], batch_rows[kVerifyMaxSeq], batch_qbase[kVerifyMaxSeq];
+  int batch_seq[kVerifyMaxSeq];     // the page-table row of each sequence (piece) of the launch
+  uint32_t batch_entry[kBatchMaxEntries];
 };
 
 // Launchers (defined next to their kernels). Return a cudaError_t.
@@ -73,10 +85,14 @@ cudaError_t launch_k_prologue(const uint16_t* k_raw, const uint16_t* w_k, const 
                               const uint16_t* sin_tab, int n_tok, int pos_base, uint16_t* k_prep,
                               int* status, cudaStream_t s);
 // Prepared query rows of several sequences: token t of sequence t / rows_per_seq sits at
-// position seq_base[t / rows_per_seq] + t % rows_per_seq.
+// position seq_base[t / rows_per_seq] + t % rows_per_seq; or, with row_start set (n_seq
+// ascending starts, row_start[n_seq] = the total), token t of the sequence b with
+// row_start[b] <= t < row_start[b + 1] sits at seq_base[b] + t - row_start[b].
 struct SeqPositions {
   int rows_per_seq;
   int seq_base[kVerifyMaxSeq];
+  int n_seq;                        // 0: uniform rows_per_seq
+  int row_start[kVerifyMaxSeq + 1];
 };
 cudaError_t launch_q_prologue_seq(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
                                   const uint16_t* sin_tab, int n_tok, const SeqPositions& sp,

@@ -42,8 +42,21 @@ __global__ void __launch_bounds__(256) prologue_kernel(const uint16_t* __restric
   if (row >= n_rows) return;
   const unsigned gmask = 0xFFu << (lane & 24);
   const long long tok = row / heads_per_tok;
-  const int pos = kSeq ? sp.seq_base[tok / sp.rows_per_seq] + (int)(tok % sp.rows_per_seq)
-                       : pos_base + (int)tok;
+  int pos = pos_base + (int)tok;
+  if (kSeq) {
+    if (sp.n_seq > 0) {
+      // the sequence holding packed token tok: the last b with row_start[b] <= tok
+      int lo = 0, hi = sp.n_seq - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sp.row_start[mid] <= tok) lo = mid;
+        else hi = mid - 1;
+      }
+      pos = sp.seq_base[lo] + (int)(tok - sp.row_start[lo]);
+    } else {
+      pos = sp.seq_base[tok / sp.rows_per_seq] + (int)(tok % sp.rows_per_seq);
+    }
+  }
 
   const uint2* xs = reinterpret_cast<const uint2*>(src + row * src_stride) + j;
   const uint2* ws = reinterpret_cast<const uint2*>(w_norm) + j;
