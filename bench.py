@@ -409,6 +409,127 @@ def run_verify(args, world, rank, local):
     }
 
 
+B_LENS = [512 * (1 + b % 8) for b in range(16)]   # 16 prompts of 512 .. 4096 tokens
+B_PAGE = 256
+
+
+def run_batch(args, world, rank, local):
+    """Batched causal prefill: 16 prompts of 512 to 4096 tokens (36,864 rows in all) in one
+    ga_attn_prefill_batch call over prepared caches in 256-position pages scattered over two
+    page pools (seeded random order); the step is the call (query prologue + attention)."""
+    from verify_gated_gqa_gb300 import binding as B
+    from verify_gated_gqa_gb300 import synth
+    from verify_gated_gqa_gb300.build import build
+
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    seed = SEED + 7 + rank
+    tmax = max(B_LENS)
+    c, s = B.ga_rope_table_host(tmax)
+    cos, sin = c.to(dev), s.to(dev)
+    w_q = synth.normal_bf16(seed, "w_q", (DIM,), sigma=0.1, device=dev)
+    w_k = synth.normal_bf16(seed, "w_k", (DIM,), sigma=0.1, device=dev)
+    need = [-(-L // B_PAGE) for L in B_LENS]
+    order = torch.randperm(sum(need), generator=torch.Generator().manual_seed(seed))
+    k_pool = torch.zeros(sum(need), B_PAGE, KV_HEADS, DIM, dtype=torch.bfloat16, device=dev)
+    v_pool = torch.zeros_like(k_pool)
+    table = torch.full((len(B_LENS), max(need)), -1, dtype=torch.int32)
+    i = 0
+    seqs = []   # the same prompts as contiguous caches, for one-call-per-prompt timing
+    for b, L in enumerate(B_LENS):
+        k_raw = synth.normal_bf16(seed, "k", (L, KV_HEADS, DIM), sub=b, device=dev)
+        k_prep = torch.empty_like(k_raw)
+        B.ga_k_prologue(k_raw, w_k, cos, sin, k_prep=k_prep)
+        v = synth.normal_bf16(seed, "v", (L, KV_HEADS, DIM), sub=b, device=dev)
+        seqs.append((k_prep, v))
+        for p in range(need[b]):
+            pg = int(order[i])
+            i += 1
+            table[b, p] = pg
+            lo, hi = p * B_PAGE, min((p + 1) * B_PAGE, L)
+            k_pool[pg, :hi - lo] = k_prep[lo:hi]
+            v_pool[pg, :hi - lo] = v[lo:hi]
+    table = table.to(dev)
+    qg = torch.cat([synth.normal_bf16(seed, "qg", (L, HEADS, 2 * DIM), sub=b, device=dev)
+                    for b, L in enumerate(B_LENS)])
+    starts = [0]
+    for L in B_LENS:
+        starts.append(starts[-1] + L)
+    out = torch.empty(qg.shape[0], HEADS * DIM, dtype=torch.bfloat16, device=dev)
+    flops = sum(attention_flops(visible_pairs_causal(L, L)) for L in B_LENS)
+
+    def step():
+        B.ga_attn_prefill_batch(qg, starts, [0] * len(B_LENS), k_pool, v_pool, table, w_q, cos,
+                                sin, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / args.steps
+
+    # context: the same prompts as one ga_attn_prefill call each (not the metric)
+    def separate():
+        for b, L in enumerate(B_LENS):
+            B.ga_attn_prefill(qg[starts[b]:starts[b + 1]], seqs[b][0], seqs[b][1], w_q, cos, sin,
+                              0, L, out=out[starts[b]:starts[b + 1]])
+
+    for _ in range(3):
+        separate()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n_sep = max(3, min(args.steps, 20))
+    e0.record(stream)
+    for _ in range(n_sep):
+        separate()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_sep = e0.elapsed_time(e1) / n_sep
+    if rank != 0:
+        return None
+    peak_bf16, _, peak_src = measured_peaks()
+    tflops = flops / (ms * 1e-3) / 1e12
+    return {
+        "metric": "batched causal prefill attention TFLOP/s (16 prompts of 512..4096 tokens)",
+        "value": round(world * tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.1) norm weights)",
+        "config": {"workload": f"batched causal gated GQA prefill: {len(B_LENS)} prompts of "
+                               f"{min(B_LENS)}..{max(B_LENS)} tokens ({starts[-1]} rows), 24q/2kv "
+                               f"heads, d=256, caches in pages of {B_PAGE} positions scattered "
+                               "over two page pools",
+                   "l2": f"inputs larger than L2 (qg {qg.numel() * 2 / 2**20:.0f} MiB)"},
+        "tokens_per_s": round(world * starts[-1] / (ms * 1e-3), 1),
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak_bf16,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak_bf16, 4), "traffic": None,
+                     "peak_kind": f"dense bf16 burst ({peak_src})",
+                     "kernel": "ga_attn_prefill_batch (query prologue + attn_kernel<batch>)",
+                     "algorithmic_flops": flops},
+        "gpu_launches": 2 * args.steps, "clocks": clk, "device_status": B.ga_device_status(),
+        "one_call_per_prompt": {"ms": round(ms_sep, 4), "calls": len(B_LENS),
+                                "note": "the same prompts as contiguous caches, one "
+                                        "ga_attn_prefill each; context, not the metric"},
+    }
+
+
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
 # summarised in profiles/attn_kernel_causal_s8192.md (218,201,856 + 61,244,928) and
 # profiles/attn_kernel_verify_8x16_l65536.md (1,077,417,472 + 18,403,072, the verify
@@ -512,9 +633,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--workload", default="prefill", choices=["prefill", "verify", "verify_paged"],
+    ap.add_argument("--workload", default="prefill",
+                    choices=["prefill", "verify", "verify_paged", "batch"],
                     help="prefill: the headline S=8192 causal step; verify: config 5; "
-                         "verify_paged: config 5 over paged caches")
+                         "verify_paged: config 5 over paged caches; batch: 16 prompts of "
+                         "512..4096 tokens in one batched call")
     ap.add_argument("--verify-seqs", type=int, default=8)
     args = ap.parse_args()
     world, rank, local = dist_env()
@@ -522,6 +645,8 @@ def main():
         line = run_reference(args, world, rank)
     elif args.workload in ("verify", "verify_paged"):
         line = run_verify(args, world, rank, local)
+    elif args.workload == "batch":
+        line = run_batch(args, world, rank, local)
     else:
         line = run_gpu(args, world, rank, local)
     if line is not None:
