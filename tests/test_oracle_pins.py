@@ -471,6 +471,67 @@ def test_verify_paged_equals_contiguous_and_decode_equals_prefill_row():
     assert np.array_equal(dec[0, 0], full[L])
 
 
+def _e4m3_grid():
+    """Every finite OCP FP8 E4M3 value, decoded from its byte by the format's definition."""
+    vals = []
+    for byte in range(256):
+        sign = -1.0 if byte >> 7 else 1.0
+        e, m = (byte >> 3) & 15, byte & 7
+        if e == 15 and m == 7:
+            continue                                  # the NaN codes
+        vals.append(sign * (m / 8) * 2.0 ** -6 if e == 0 else sign * (1 + m / 8) * 2.0 ** (e - 7))
+    return np.array(sorted(set(vals)))
+
+
+def test_e4m3_grid_nearest_ties_to_even_and_saturation():
+    """e4m3() keeps every grid value, returns the nearest grid value for random inputs (ties
+    to the even mantissa, found by exhaustive search), and saturates at +-448."""
+    grid = _e4m3_grid()
+    assert grid.size == 253 and grid.max() == 448.0 and np.min(grid[grid > 0]) == 2.0 ** -9
+    assert np.array_equal(O.e4m3(grid), grid)
+    rng = np.random.default_rng(8)
+    v = np.concatenate([rng.normal(size=4000) * 2.0 ** rng.integers(-12, 9, 4000),
+                        (grid[1:] + grid[:-1]) / 2])  # includes every midpoint
+    v = v[np.abs(v) <= 448]
+    got = O.e4m3(v)
+    d = np.abs(v[:, None] - grid[None, :])
+    best = d.min(axis=1)
+    for i in range(v.size):
+        cand = grid[np.isclose(d[i], best[i], rtol=0, atol=0)]
+        if cand.size == 1:
+            assert got[i] == cand[0], v[i]
+        else:                                         # a tie: the even mantissa (code) wins
+            codes = [int(np.round(abs(c) / 2.0 ** (max(np.floor(np.log2(abs(c))), -6) - 3))) % 2
+                     if c != 0 else 0 for c in cand]
+            assert got[i] == cand[codes.index(0)], v[i]
+    assert O.e4m3(463.99) == 448 and O.e4m3(464.0) == 448 and O.e4m3(1e9) == 448
+    assert O.e4m3(-1e9) == -448 and O.e4m3(0.0) == 0
+
+
+def test_e4m3_rows_scale_and_round_trip():
+    """A row whose largest magnitude is 448 has scale 1, so its codes are e4m3 of the row
+    itself (1.0625 ties down to 1.0, 1.1875 up to 1.25); the largest element of any row
+    maps to +-448; a zero row gives scale 0 and zeros; the widened row is within 2^-4
+    relative (plus one bf16 rounding) of the row for elements above the subnormal range."""
+    row = np.zeros(256)
+    row[:5] = [448.0, 1.0625, 1.1875, -3.0, 0.5]
+    q, sc = O.quantize_e4m3_rows(row[None])
+    assert sc[0] == 1.0
+    assert list(q[0, :5]) == [448.0, 1.0, 1.25, -3.0, 0.5]
+    assert np.array_equal(O.dequantize_e4m3_rows(q, sc)[0, :5], [448.0, 1.0, 1.25, -3.0, 0.5])
+    rng = np.random.default_rng(9)
+    x = O.bf16(rng.normal(size=(64, 256)) * 2.0 ** rng.integers(-8, 8, (64, 1)))
+    q, sc = O.quantize_e4m3_rows(x)
+    assert np.all(np.abs(q).max(axis=1) == 448.0)
+    assert np.all(sc == O.fp32(np.abs(x).max(axis=1) / 448.0))
+    xh = O.dequantize_e4m3_rows(q, sc)
+    big = np.abs(x) >= 2.0 ** -6 * sc[:, None] * 1.0001
+    rel = np.abs(xh - x)[big] / np.abs(x)[big]
+    assert rel.max() <= 2.0 ** -4 * (1 + 2.0 ** -7) + 2.0 ** -8
+    q0, sc0 = O.quantize_e4m3_rows(np.zeros((2, 256)))
+    assert np.all(q0 == 0) and np.all(sc0 == 0) and np.all(O.dequantize_e4m3_rows(q0, sc0) == 0)
+
+
 # ---------------------------------------------------------------- planted mistakes
 def test_planted_unrounded_sigmoid_is_caught(monkeypatch):
     """[QSA] §Validation, mutation calibration: dropping the sigmoid's bf16 rounding
