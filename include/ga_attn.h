@@ -281,6 +281,23 @@ int ga_attn_verify_paged(const ga_bf16* qg, const ga_bf16* k_pages, const ga_bf1
                          const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
                          ga_bf16* out, void* workspace, size_t ws_bytes, ga_stream stream);
 
+/* e4m3 cache rows with one fp32 scale each (TensorFold PR #1080, "qwen CUDA: long-prompt
+ * prefill 5.4x faster": its prompt chain reads e4m3 cache rows with an fp32 scale each and
+ * widens them to bf16 in the shared-memory slot; its rope kernels compute the e4m3 scales by
+ * reductions over the row). For every (token, head) row of 256 bf16 values x:
+ *   scale = fp32(max|x| / 448),  q = e4m3(fp32(x / scale))
+ * with IEEE divisions rounded to nearest and the OCP FP8 E4M3 conversion rounding to nearest
+ * (ties to even) and saturating at +-448; a row of zeros gives scale 0 and q 0. The widened
+ * row that ga_attn_verify_e4m3 attends over is bf16(fp32(q * scale)).
+ *   x      [n_tok][2][256] bf16: prepared keys (as ga_k_prologue writes them) or values
+ *   q      [n_tok][2][256] uint8 e4m3 codes (byte d of a row is dim d)
+ *   scale  [n_tok][2] fp32
+ * Rules: x 8-byte aligned, q 4-byte aligned, scale 4-byte aligned, 0 <= n_tok <= GA_MAX_TOKENS
+ * x 64 (sequences laid end to end count as one long run). n_tok = 0 is a no-op.
+ * Errors: NULL, SHAPE, RANGE, ALIGN, DEVICE, CUDA. */
+int ga_kv_quantize_e4m3(const ga_bf16* x, long long n_tok, uint8_t* q, float* scale,
+                        ga_stream stream);
+
 /* Several causal prefills in one call: sequences (or branches) of different lengths, each a
  * window of rows at its own q_base over its own paged cache. system1-omni PR #99, "run
  * prompts that share prefixes once per prefix", and PR #196, "perf(open-jev): optimize 9B

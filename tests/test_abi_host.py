@@ -214,6 +214,19 @@ def test_prefill_batch_refusals_make_no_cuda_call(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def test_quantize_refusals_make_no_cuda_call(L):
+    before = L.ga_debug_cuda_calls()
+    assert L.ga_kv_quantize_e4m3(None, 10, A, A, S) == -1
+    assert L.ga_kv_quantize_e4m3(A, 10, None, A, S) == -1
+    assert L.ga_kv_quantize_e4m3(A, 10, A, None, S) == -1
+    assert L.ga_kv_quantize_e4m3(A, -1, A, A, S) == -2
+    assert L.ga_kv_quantize_e4m3(A, (1 << 26) + 1, A, A, S) == -4
+    assert L.ga_kv_quantize_e4m3(A + 4, 10, A, A, S) == -3
+    assert L.ga_kv_quantize_e4m3(A, 10, A + 2, A, S) == -3
+    assert L.ga_kv_quantize_e4m3(A, 0, A, A, S) == 0          # no rows: a no-op
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_k_prologue_refusals(L):
     before = L.ga_debug_cuda_calls()
     assert L.ga_k_prologue(None, A, A, A, 100, 10, 0, A, S) == -1

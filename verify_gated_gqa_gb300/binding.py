@@ -53,6 +53,7 @@ _SIGS = {
                                   _SZ, _P]),
     "ga_attn_prefill_batch": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _P, _I, _P, _P, _P, _I, _P,
                                    _P]),
+    "ga_kv_quantize_e4m3": (_I, [_P, _LL, _P, _P, _P]),
 }
 
 
@@ -337,3 +338,23 @@ def ga_attn_prefill_batch(qg, row_start, q_base, k_pages, v_pages, page_table, w
                                        _ptr(sin_tab), cos_tab.shape[0], _ptr(out), _stream()),
            "ga_attn_prefill_batch")
     return out
+
+
+def ga_kv_quantize_e4m3(x, q=None, scale=None):
+    """x [..., 2, 256] bf16 (rows of prepared keys or values) -> (q uint8 [..., 2, 256],
+    scale fp32 [..., 2])."""
+    _bf16_cuda("x", x)
+    if x.shape[-2:] != (N_KV_HEADS, HEAD_DIM):
+        raise ValueError("x must end in [2, 256]")
+    n_tok = x.numel() // (N_KV_HEADS * HEAD_DIM)
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    if q.dtype != torch.uint8 or not q.is_contiguous() or q.shape != x.shape:
+        raise ValueError("q must be a contiguous uint8 tensor shaped like x")
+    if scale.dtype != torch.float32 or not scale.is_contiguous() or scale.shape != x.shape[:-1]:
+        raise ValueError("scale must be a contiguous float32 tensor shaped like x[..., 0]")
+    _check(lib().ga_kv_quantize_e4m3(_ptr(x), n_tok, _ptr(q), _ptr(scale), _stream()),
+           "ga_kv_quantize_e4m3")
+    return q, scale

@@ -789,6 +789,21 @@ int ga_attn_prefill_batch(const ga_bf16* qg, const int* row_start, const int* q_
                    page_table, max_pages, w_q, cos_tab, sin_tab, out, stream);
 }
 
+int ga_kv_quantize_e4m3(const ga_bf16* x, long long n_tok, uint8_t* q, float* scale,
+                        ga_stream stream) {
+  if (!x || !q || !scale) return GA_ERR_NULL;
+  if (n_tok < 0) return GA_ERR_SHAPE;
+  if (n_tok > (long long)GA_MAX_TOKENS * 64) return GA_ERR_RANGE;
+  if (!aligned(x, 8) || !aligned(q, 4) || !aligned(scale, 4)) return GA_ERR_ALIGN;
+  if (n_tok == 0) return GA_OK;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaError_t e = GA_CUDA(launch_quantize_e4m3(x, n_tok * kKvHeads, q, scale, (cudaStream_t)stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return GA_OK;
+}
+
 // ------------------------------------------------------------------ allocation-free masked call
 // The scratch of ga_attn_masked_static: one static array per device, reserved at module
 // load, its address looked up once per device on the first call (with that device current).

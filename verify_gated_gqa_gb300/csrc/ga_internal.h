@@ -103,6 +103,9 @@ cudaError_t launch_verify_combine(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
                               const uint16_t* sin_tab, int rows, int q_base, uint16_t* q_prep,
                               cudaStream_t s);
+// e4m3 cache rows: q[row][0..255] and scale[row] for n_rows rows of 256 bf16 values.
+cudaError_t launch_quantize_e4m3(const uint16_t* x, long long n_rows, uint8_t* q, float* scale,
+                                 cudaStream_t s);
 cudaError_t attn_set_smem_attribute();
 // Test hook: a bounded wait on a barrier nothing arrives on (records a wait timeout).
 cudaError_t launch_wait_timeout(long long limit, int* status, cudaStream_t s);
