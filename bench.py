@@ -313,8 +313,10 @@ def run_verify(args, world, rank, local):
     two page pools in a seeded random order, read through ga_attn_verify_paged."""
     V_SEQ = args.verify_seqs
     paged = args.workload == "verify_paged"
-    V_METRIC = (f"verify windows{' over paged caches' if paged else ''}: HBM GB/s ({V_SEQ} "
-                "sequences x 16 rows over L=65536 cached keys)")
+    e4m3 = args.workload == "verify_e4m3"
+    kind = " over paged caches" if paged else (" over e4m3 caches" if e4m3 else "")
+    V_METRIC = (f"verify windows{kind}: HBM GB/s ({V_SEQ} sequences x 16 rows over L=65536 "
+                "cached keys)")
     V_BYTES = verify_bytes(V_SEQ)
     from verify_gated_gqa_gb300 import binding as B
     from verify_gated_gqa_gb300 import synth
@@ -341,6 +343,14 @@ def run_verify(args, world, rank, local):
     lens = [V_L] * V_SEQ
     out = torch.empty(V_SEQ, V_ROWS, HEADS * DIM, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(B.ga_verify_workspace_bytes(V_SEQ, V_ROWS, V_L), dtype=torch.uint8, device=dev)
+    if e4m3:
+        # the same caches as e4m3 rows with an fp32 scale each (algorithmic bytes: the codes
+        # and scales read once, the fused rows and the outputs)
+        k8, ksc = B.ga_kv_quantize_e4m3(k_cache)
+        v8, vsc = B.ga_kv_quantize_e4m3(v_cache)
+        del k_cache, v_cache
+        V_BYTES = (k8.numel() + v8.numel() + 4 * (ksc.numel() + vsc.numel())
+                   + qg.numel() * 2 + out.numel() * 2)
     if paged:
         pages_per_seq = -(-V_CAP // V_PAGE)
         n_pages = V_SEQ * pages_per_seq
@@ -360,6 +370,8 @@ def run_verify(args, world, rank, local):
         if paged:
             B.ga_attn_verify_paged(qg, k_pool, v_pool, table, lens, w_q, cos, sin, out=out,
                                    workspace=ws)
+        elif e4m3:
+            B.ga_attn_verify_e4m3(qg, k8, ksc, v8, vsc, lens, w_q, cos, sin, out=out, workspace=ws)
         else:
             B.ga_attn_verify(qg, k_cache, v_cache, lens, w_q, cos, sin, out=out, workspace=ws)
 
@@ -395,15 +407,18 @@ def run_verify(args, world, rank, local):
         "config": {"workload": f"verify: {V_SEQ} sequences x 16 rows at positions 65536..65551 over "
                                "prepared K/V caches [65552, 2, 256] bf16, split-key partials "
                                "and combine" + (f"; caches in pages of {V_PAGE} positions, "
-                                                "scattered over two page pools" if paged else ""),
+                                                "scattered over two page pools" if paged else "")
+                               + ("; caches as e4m3 rows with an fp32 scale each (half the "
+                                  "bytes), widened to bf16 in shared memory" if e4m3 else ""),
                    "l2": f"K/V caches {2 * V_SEQ * V_CAP * KV_HEADS * DIM * 2 / 1e9:.2f} GB"},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                      "frac": round(gbs / peak_hbm, 4),
-                     "traffic": VERIFY_ATTN_TRAFFIC_BYTES if V_SEQ == 8 and not paged else None,
+                     "traffic": (VERIFY_ATTN_TRAFFIC_BYTES if V_SEQ == 8 and not paged and not e4m3
+                                 else None),
                      "traffic_kernel": "attn_kernel (verify variant), the call's dominant launch",
                      "peak_kind": f"HBM copy ({peak_src})",
-                     "kernel": f"ga_attn_verify{'_paged' if paged else ''} (Q prologue + "
-                               "attn_kernel<verify> + combine)",
+                     "kernel": f"ga_attn_verify{'_paged' if paged else ('_e4m3' if e4m3 else '')} "
+                               "(Q prologue + attn_kernel<verify> + combine)",
                      "algorithmic_bytes": V_BYTES},
         "gpu_launches": 3 * args.steps, "clocks": clk, "device_status": B.ga_device_status(),
     }
@@ -634,16 +649,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", default="prefill",
-                    choices=["prefill", "verify", "verify_paged", "batch"],
+                    choices=["prefill", "verify", "verify_paged", "verify_e4m3", "batch"],
                     help="prefill: the headline S=8192 causal step; verify: config 5; "
-                         "verify_paged: config 5 over paged caches; batch: 16 prompts of "
+                         "verify_paged: config 5 over paged caches; verify_e4m3: config 5 "
+                         "over e4m3 caches; batch: 16 prompts of "
                          "512..4096 tokens in one batched call")
     ap.add_argument("--verify-seqs", type=int, default=8)
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, world, rank)
-    elif args.workload in ("verify", "verify_paged"):
+    elif args.workload in ("verify", "verify_paged", "verify_e4m3"):
         line = run_verify(args, world, rank, local)
     elif args.workload == "batch":
         line = run_batch(args, world, rank, local)

@@ -254,6 +254,22 @@ int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_c
                    const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
                    ga_bf16* out, void* workspace, size_t ws_bytes, ga_stream stream);
 
+/* ga_attn_verify over e4m3 caches (TensorFold PR #1080, "qwen CUDA: long-prompt prefill 5.4x
+ * faster": e4m3 cache rows with an fp32 scale each, staged a step ahead and widened to bf16
+ * in the shared-memory slot). The caches hold what ga_kv_quantize_e4m3 writes:
+ *   k_codes, v_codes  [n_seq][cap][2][256] uint8 e4m3 codes, 16-byte aligned
+ *   k_scale, v_scale  [n_seq][cap][2] fp32 row scales, 4-byte aligned
+ * Each row is widened to bf16(fp32(code * scale)) and the call then computes exactly what
+ * ga_attn_verify computes over those bf16 rows: the same bits. It reads half the cache bytes.
+ * Positions read but hidden (past L_b + rows inside the last 128-key tile, below cap) must
+ * hold codes other than NaN (0x7F, 0xFF) and finite scales. Everything else, the rules and
+ * the errors are those of ga_attn_verify, with the same workspace size. */
+int ga_attn_verify_e4m3(const ga_bf16* qg, const uint8_t* k_codes, const float* k_scale,
+                        const uint8_t* v_codes, const float* v_scale, int cap, const int* seq_len,
+                        int n_seq, int rows, const ga_bf16* w_q, const ga_bf16* cos_tab,
+                        const ga_bf16* sin_tab, int table_rows, ga_bf16* out, void* workspace,
+                        size_t ws_bytes, ga_stream stream);
+
 /* ga_attn_verify over PAGED caches, and decode (rows = 1). pegainfer PR #1151, "feat(qwen4):
  * add the QSA sparse-attention kernel and its golden", §Summary and §Limits name paged KV
  * and decode as the next steps after its contiguous key array; the layout is the plain

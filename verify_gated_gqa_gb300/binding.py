@@ -54,6 +54,8 @@ _SIGS = {
     "ga_attn_prefill_batch": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _P, _I, _P, _P, _P, _I, _P,
                                    _P]),
     "ga_kv_quantize_e4m3": (_I, [_P, _LL, _P, _P, _P]),
+    "ga_attn_verify_e4m3": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P, _SZ,
+                                 _P]),
 }
 
 
@@ -358,3 +360,31 @@ def ga_kv_quantize_e4m3(x, q=None, scale=None):
     _check(lib().ga_kv_quantize_e4m3(_ptr(x), n_tok, _ptr(q), _ptr(scale), _stream()),
            "ga_kv_quantize_e4m3")
     return q, scale
+
+
+def ga_attn_verify_e4m3(qg, k_codes, k_scale, v_codes, v_scale, seq_len, w_q, cos_tab, sin_tab,
+                        out=None, workspace=None):
+    """qg [n_seq, rows, 24, 512]; k_codes, v_codes uint8 [n_seq, cap, 2, 256]; k_scale,
+    v_scale fp32 [n_seq, cap, 2] (as ga_kv_quantize_e4m3 writes them); seq_len: ints."""
+    n_seq, rows = qg.shape[0], qg.shape[1]
+    cap = k_codes.shape[1]
+    for n, t, dt in (("k_codes", k_codes, torch.uint8), ("v_codes", v_codes, torch.uint8),
+                     ("k_scale", k_scale, torch.float32), ("v_scale", v_scale, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous() or t.shape[:2] != (n_seq, cap):
+            raise ValueError(f"{n} must be a contiguous {dt} CUDA tensor [n_seq, cap, ...]")
+    lens = (ctypes.c_int * n_seq)(*[int(x) for x in seq_len])
+    dev = qg.device
+    if out is None:
+        out = torch.empty(n_seq, rows, N_Q_HEADS * HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    ws_bytes = ga_verify_workspace_bytes(n_seq, rows, max(int(x) for x in seq_len))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    for n, t in (("qg", qg), ("w_q", w_q), ("cos_tab", cos_tab), ("sin_tab", sin_tab),
+                 ("out", out)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_attn_verify_e4m3(_ptr(qg), _ptr(k_codes), _ptr(k_scale), _ptr(v_codes),
+                                     _ptr(v_scale), cap, lens, n_seq, rows, _ptr(w_q),
+                                     _ptr(cos_tab), _ptr(sin_tab), cos_tab.shape[0], _ptr(out),
+                                     _ptr(workspace), workspace.numel(), _stream()),
+           "ga_attn_verify_e4m3")
+    return out

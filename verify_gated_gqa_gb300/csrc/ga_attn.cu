@@ -43,6 +43,9 @@
 //              epilogue of the current item.
 // The edge code is kept in short loops: the four roles run different code at once and
 // share the SM's instruction cache, which long unrolled sequences would overflow.
+// Over e4m3 caches (verify), the producer loads each K or V tile as e4m3 codes into the back
+// half of its slot, the edge warps widen it in place to bf16(fp32(code * scale)), and the
+// MMA warps wait for the widened tile instead of the copy.
 // Tensor memory (512 columns x 128 lanes, lane = query row): O [0, 256) fp32, S [256, 384)
 // fp32, Q dims 0..127 [384, 448) and P [448, 512) as bf16 pairs. Q dims 128..255 stay in
 // shared memory for the item, where P used to go: P is written to tensor memory with one
@@ -51,6 +54,8 @@
 // serpentine order so each CTA's total work evens out. The kernel is compiled once per
 // visibility mode (causal, bidirectional, stored mask) and for the weights pass, so each
 // variant carries only its own code.
+#include <cuda_fp8.h>
+
 #include "ga_internal.h"
 #include "ga_numerics.cuh"
 #include "ga_sm100.cuh"
@@ -84,8 +89,12 @@ constexpr int kLazyRescale = 8;     // rescale when the tile maximum exceeds M b
 
 // Items of the gated passes (causal, bidirectional, stored mask) carry a gate tile in the
 // ring; the weights pass and the verify partials have no gated epilogue.
+// Few-row verify windows, over bf16 or e4m3 caches: the same items, softmax and partials.
+template <int kMode>
+__host__ __device__ constexpr bool is_verify() { return kMode == kModeVerify || kMode == kModeVerify8; }
+
 template <int kMode, bool kW>
-__host__ __device__ constexpr bool has_gate() { return !kW && kMode != kModeVerify; }
+__host__ __device__ constexpr bool has_gate() { return !kW && !is_verify<kMode>(); }
 
 static_assert(kTileN == 128, "this kernel is laid out for 128-key tiles");
 
@@ -96,6 +105,8 @@ struct AttnSmem {
   float stat_m[kTileM];               // and the running maximum M
   uint16_t mx[2][2][kTileM];          // tile g: each half's row maximum (bf16 bits), by g % 2
   uint64_t full[kSlots], empty[kSlots];
+  uint64_t conv[kSlots];              // e4m3 caches: the slot's tile is widened (or seen: Q)
+  uint64_t wide_read;                 // e4m3 caches: every edge thread has read the raw tile
   uint64_t q_full, q_empty, s_full, s_free;
   uint64_t p_full[2], p_empty[2];     // per 64-key half of P
   uint64_t o_done, o_free, st_full, st_empty, drain, drain_pv, q_read, g_read, mx_bar;
@@ -145,7 +156,7 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
     it.n = (it.qb + last_row + 1 + kTileN - 1) / kTileN;
     return it;
   }
-  if (kMode == kModeVerify) {
+  if (is_verify<kMode>()) {
     // (chunk, sequence, KV head, half): the two halves of a query group are neighbours, so
     // the CTAs that run them read each K/V tile at about the same time (the second from L2)
     it.half = idx & 1;
@@ -269,7 +280,7 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
     // status word and its tile read past the pool's end, which yields zeros.
     int win0 = -1, win_page = 0;
     auto kv_at = [&](int kt, int& r0) -> int {
-      if (kMode != kModeVerify && kMode != kModeBatch) {
+      if (!is_verify<kMode>() && kMode != kModeBatch) {
         r0 = kt * kTileN;
         return -1;
       }
@@ -291,19 +302,32 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
       }
       return page;
     };
+    // e4m3 caches: one box of 128 keys x 256 bytes into the back half of the slot, where
+    // the edge warps widen it to the bf16 tile the tensor cores read
+    auto load_raw8 = [&](const CUtensorMap* map, int kt) -> bool {
+      const uint32_t slot = cnt % kSlots;
+      if (!warp_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
+      mbar_expect_tx_warp(&sm.full[slot], kTileBytes / 2);
+      tma_load_4d_warp(sm.tile[slot] + kTileBytes / 2, map, &sm.full[slot], 0, kvh, kt * kTileN,
+                       it.seq);
+      ++cnt;
+      return true;
+    };
     auto load_k = [&](int kt) -> bool {
+      if (kMode == kModeVerify8) return load_raw8(tm_k, kt);
       int r0;
       const int outer = kv_at(kt, r0);
       return load_tile(tm_k, true, kvh, r0, outer, kTileBytes);
     };
     auto load_v = [&](int kt) -> bool {
+      if (kMode == kModeVerify8) return load_raw8(tm_v, kt);
       int r0;
       const int outer = kv_at(kt, r0);
       return load_tile(tm_v, true, kvh, r0, outer, kTileBytes);
     };
     // Ring order: the item's prepared Q (for the edge warps), then in MMA order K0,
     // (K_j, V_{j-1}) for j >= 1, V_{n-1}; the gate tile (gated passes) just before V_0.
-    if (kMode == kModeVerify) {
+    if (is_verify<kMode>()) {
       if (!load_tile(tm_q, false, it.h, it.seq * a.vrows, -1,
                      4u * kVerifyHeadsPerTile * a.vrows * 128u)) return;
     } else {
@@ -350,12 +374,15 @@ __device__ void producer(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMa
 // MMAs (a commit covers the MMAs its thread issued).
 // Ring order per item: Q, K0, then K_j, V_{j-1} for j >= 1, then V_{n-1}, with the gate
 // tile of the gated passes right before V_0 (Q and K only in the weights pass).
+// With e4m3 caches a fill is ready once the edge warps have widened it (K, V) or seen it (Q).
+template <int kMode>
 struct RingWalk {
   uint32_t cnt = 0;
   // wait for the next fill in ring order (its slot in `slot`) and count this warp as past it
   __device__ __forceinline__ bool next(AttnSmem& sm, volatile int* abort, uint32_t& slot) {
     slot = cnt % kSlots;
-    const bool ok = warp_wait(&sm.full[slot], (cnt / kSlots) & 1, abort);
+    uint64_t* ready = kMode == kModeVerify8 ? &sm.conv[slot] : &sm.full[slot];
+    const bool ok = warp_wait(ready, (cnt / kSlots) & 1, abort);
     ++cnt;
     if (ok && (threadIdx.x & 31) == 0) mbar_arrive(&sm.empty[slot]);
     return ok;
@@ -370,7 +397,7 @@ __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
   constexpr uint32_t kIdQK = idesc_bf16(128, kTileN, false, false);
   const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), 16, 1024);
   const uint64_t qhi_desc0 = sdesc_sw128(smem_u32(sm.qhi[0]), 16, 1024);
-  RingWalk ring;
+  RingWalk<kMode> ring;
   uint32_t g = 0;         // global key-tile counter: S phases
   uint32_t it_done = 0;
   uint32_t slot;
@@ -420,7 +447,7 @@ template <int kMode>
 __device__ void pv_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
   constexpr uint32_t kIdPV = idesc_bf16(128, kDim, false, true);
   const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), kChunkBytes, 1024);
-  RingWalk ring;
+  RingWalk<kMode> ring;
   uint32_t g = 0;         // global key-tile counter: P and P V phases
   uint32_t it_done = 0;
   uint32_t slot;
@@ -501,7 +528,7 @@ __device__ __forceinline__ uint32_t chunk_visibility(const AttnArgs& a, int row,
 template <int kMode>
 __device__ __forceinline__ bool tile_full(const AttnArgs& a, const Item& it, int kt) {
   if (kMode == kModeMask) return false;
-  if (kMode == kModeVerify) return (kt + 1) * kTileN - 1 <= a.seq_len[it.seq];
+  if (is_verify<kMode>()) return (kt + 1) * kTileN - 1 <= a.seq_len[it.seq];
   if ((it.mt + 1) * kTileM > it.rows || (kt + 1) * kTileN > it.T) return false;
   if (is_causal<kMode>()) return (kt + 1) * kTileN - 1 <= it.qb + it.mt * kTileM;
   return true;
@@ -554,8 +581,8 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
   Item it;
   while (walk.next(a, it)) {
     const int row = it.mt * kTileM + r;   // the row within its sequence
-    const bool valid = kMode == kModeVerify ? r < kVerifyHeadsPerTile * a.vrows : row < it.rows;
-    const int limit = kMode == kModeVerify ? a.seq_len[it.seq] + r / kVerifyHeadsPerTile
+    const bool valid = is_verify<kMode>() ? r < kVerifyHeadsPerTile * a.vrows : row < it.rows;
+    const int limit = is_verify<kMode>() ? a.seq_len[it.seq] + r / kVerifyHeadsPerTile
                                            : it.qb + row;
     const int h = it.h;
     int M = 0;
@@ -882,6 +909,62 @@ __device__ bool epilogue_partial(AttnSmem& sm, const AttnArgs& a, const Item& it
   return true;
 }
 
+// Two e4m3 codes (low byte first) as floats; every e4m3 value is exact in f16 and f32.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+  const __half2_raw hr =
+      __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
+  return __half22float2(__half2(hr));
+}
+
+// e4m3 caches: the raw tile (128 keys x 256 codes, one 256-byte row per key) in the back half
+// of the fill's slot becomes the bf16 tile the tensor cores read, bf16(fp32(code * scale))
+// per element, in place. Edge thread t widens the 16 codes of column t % 16 in rows t / 16 +
+// 8k: it reads all of them (its rows' scales already in flight), waits until every edge
+// thread has read (the bf16 tile overwrites the raw one), then writes. The long-prompt
+// page's F8 rows are staged this way: loaded a step ahead, widened in the slot.
+__device__ bool widen_e4m3(AttnSmem& sm, const AttnArgs& a, uint32_t pos, const float* scale,
+                           int seq, int kvh, int kt, int t, uint32_t n_done, volatile int* abort) {
+  const uint32_t slot = pos % kSlots;
+  const int c = t & 15;
+  const int r0 = t >> 4;
+  float scv[16];
+  const float* srow = scale + (size_t)seq * a.cache_cap * kKvHeads + kvh;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int key = kt * kTileN + r0 + 8 * k;
+    scv[k] = key < a.cache_cap ? __ldg(srow + (size_t)key * kKvHeads) : 0.f;
+  }
+  if (!warp_wait(&sm.full[slot], (pos / kSlots) & 1, abort)) return false;
+  const uint8_t* raw = sm.tile[slot] + kTileBytes / 2;
+  uint4 v[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k)
+    v[k] = *reinterpret_cast<const uint4*>(raw + (r0 + 8 * k) * kDim + c * 16);
+  mbar_arrive(&sm.wide_read);
+  if (!warp_wait(&sm.wide_read, n_done & 1, abort)) return false;
+  uint8_t* blk = sm.tile[slot] + (c >> 2) * kChunkBytes;
+  const uint32_t j0 = (uint32_t)(c & 3) * 2;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t row = (uint32_t)(r0 + 8 * k);
+    const uint32_t wi[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+    uint32_t w[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      // codes of dims 4q .. 4q+3 of this chunk, lowest byte first; fp32(code * scale)
+      const float2 lo = e4m3x2_to_float2(wi[q]);
+      const float2 hi = e4m3x2_to_float2(wi[q] >> 16);
+      w[2 * q] = pack_bf16x2(lo.x * scv[k], lo.y * scv[k]);
+      w[2 * q + 1] = pack_bf16x2(hi.x * scv[k], hi.y * scv[k]);
+    }
+    *reinterpret_cast<uint4*>(blk + sw128_offset(row, j0)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(blk + sw128_offset(row, j0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  fence_async_smem();
+  mbar_arrive(&sm.conv[slot]);
+  return true;
+}
+
 template <int kMode, bool kW>
 __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -901,7 +984,7 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
         ++round;
         return true;
       }
-      if (kMode != kModeVerify) write_hidden_rows(a, out, r, kW);
+      if (!is_verify<kMode>()) write_hidden_rows(a, out, r, kW);
     }
   };
   // Ring position of each item's Q tile: the producer loads Q, then the item's K and V tiles.
@@ -914,8 +997,9 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
     const uint32_t slot = q_pos % kSlots;
     if (wait_empty && !warp_wait(&sm.q_empty, it_done & 1, abort)) return false;
     if (!warp_wait(&sm.full[slot], (q_pos / kSlots) & 1, abort)) return false;
+    if (kMode == kModeVerify8) mbar_arrive(&sm.conv[slot]);
     tc_fence_after();
-    q_copy(sm.tile[slot], r, kMode != kModeVerify || r < kVerifyHeadsPerTile * a.vrows, q_taddr,
+    q_copy(sm.tile[slot], r, !is_verify<kMode>() || r < kVerifyHeadsPerTile * a.vrows, q_taddr,
            sm.qhi);
     tc_fence_before();
     mbar_arrive(&sm.q_full);
@@ -955,7 +1039,36 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
   if (!take_q(cur, false, 0)) return;
   uint4 sg[kDim / 8];
   uint32_t it_done = 0;
+  // e4m3 caches: the edge warps walk every fill of the ring in order and widen each K and V
+  // tile of the item (ring order K0, then K_j, V_{j-1} for j >= 1, then V_{n-1})
+  uint32_t n_wide = 0;
+  auto widen_item = [&](const Item& it, uint32_t q_at) -> bool {
+    const int kvh = it.h / kGroup;
+    for (int f = 1; f <= 2 * it.n; ++f) {
+      bool is_v;
+      int tile;
+      if (f == 1) {
+        is_v = false;
+        tile = 0;
+      } else if (f == 2 * it.n) {
+        is_v = true;
+        tile = it.n - 1;
+      } else if ((f & 1) == 0) {
+        is_v = false;
+        tile = f / 2;
+      } else {
+        is_v = true;
+        tile = (f - 3) / 2;
+      }
+      if (!widen_e4m3(sm, a, q_at + f, is_v ? a.v_scale : a.k_scale, it.seq, kvh, it.kt0 + tile,
+                      r, n_wide, abort))
+        return false;
+      ++n_wide;
+    }
+    return true;
+  };
   while (true) {
+    if (kMode == kModeVerify8 && !widen_item(cur, cur_q)) return;
     if (has_gate<kMode, kW>()) {
       if (!take_gate(cur_q + (cur.n >= 2 ? 3 : 2), sg)) return;
       gate_sigmoid(sg);
@@ -963,7 +1076,7 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
     const bool have_next = next_item(nxt);
     const uint32_t nxt_q = q_pos;
     if (have_next && !take_q(nxt, true, it_done)) return;
-    if (kMode == kModeVerify) {
+    if (is_verify<kMode>()) {
       if (!epilogue_partial(sm, a, cur, tmem, lane_off, r, it_done, abort)) return;
     } else if (!kW && !epilogue(sm, a, cur, tmem, lane_off, r, it_done, sg, abort)) {
       return;
@@ -1013,6 +1126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.drain, 1);
     mbar_init(&sm.drain_pv, 1);
     mbar_init(&sm.q_read, 128);
+    for (int i = 0; i < kSlots; ++i) mbar_init(&sm.conv[i], 128);
+    mbar_init(&sm.wide_read, 128);
     mbar_init(&sm.g_read, 128);
     mbar_init(&sm.mx_bar, 256);
     mbar_fence_init();
@@ -1153,6 +1268,9 @@ cudaError_t attn_set_smem_attribute() {
   if ((e = cudaFuncSetAttribute(attn_kernel<kModeBatch, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
     return e;
+  if ((e = cudaFuncSetAttribute(attn_kernel<kModeVerify8, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+    return e;
   return cudaFuncSetAttribute(attn_kernel<kModeMask, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
@@ -1171,6 +1289,8 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
     attn_kernel<kModeVerify, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else if (a.mode == kModeBatch) {
     attn_kernel<kModeBatch, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+  } else if (a.mode == kModeVerify8) {
+    attn_kernel<kModeVerify8, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else {
     attn_kernel<kModeMask, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   }

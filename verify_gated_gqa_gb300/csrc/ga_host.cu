@@ -173,6 +173,29 @@ int encode_q_map(CUtensorMap* map, const void* base, long long rows, int box_hea
   return GA_OK;
 }
 
+// [n_seq][cap][2][256] e4m3 key or value rows as a TMA tensor: box = one head's 256 codes x
+// 128 tokens of one sequence, unswizzled (the edge warps widen it to the swizzled bf16 tile);
+// tokens past the cache read as zeros.
+int encode_kv8_map(CUtensorMap* map, const void* base, long long cap, long long n_seq) {
+  EncodeTiledFn enc;
+  int st = get_encode(&enc);
+  if (st != GA_OK) return st;
+  cuuint64_t dims[4] = {(cuuint64_t)kDim, (cuuint64_t)kKvHeads, (cuuint64_t)cap, (cuuint64_t)n_seq};
+  cuuint64_t strides[3] = {(cuuint64_t)kDim, (cuuint64_t)kKvHeads * kDim,
+                           (cuuint64_t)cap * kKvHeads * kDim};
+  cuuint32_t box[4] = {(cuuint32_t)kDim, 1, (cuuint32_t)kTileN, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = GA_CUDA(enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
+                           strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = (int)r;
+    return GA_ERR_CUDA;
+  }
+  return GA_OK;
+}
+
 // [rows][24][512] bf16 fused q|gate rows as a TMA tensor, read for the gate halves: box =
 // 64 values x 1 head x 128 rows at x = 256 + 64c, 128-byte swizzle; rows past the end read
 // as zeros.
@@ -302,6 +325,10 @@ int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const v
 struct VerifyCaches {
   const ga_bf16* k;
   const ga_bf16* v;
+  const uint8_t* k8;        // e4m3 caches (k, v null): [n_seq][cap][2][256] codes
+  const uint8_t* v8;
+  const float* k_scale;     // and their row scales [n_seq][cap][2]
+  const float* v_scale;
   int cap;                  // contiguous: positions per sequence's cache
   const int* page_table;    // paged: [n_seq][max_pages] device array, else null
   int page_size, max_pages, n_pages;
@@ -314,9 +341,12 @@ int verify_run(const ga_bf16* qg, const VerifyCaches& c, const int* seq_len, int
   for (int b = 0; b < n_seq; ++b)
     if (seq_len[b] > max_len) max_len = seq_len[b];
   if ((long long)table_rows < (long long)max_len + rows) return GA_ERR_TABLE;
-  if (!aligned(qg, 16) || !aligned(c.k, 16) || !aligned(c.v, 16) || !aligned(w_q, 16) ||
-      !aligned(cos_tab, 16) || !aligned(sin_tab, 16) || !aligned(out, 16))
+  const bool fp8 = c.k8 != nullptr;
+  if (!aligned(qg, 16) || !aligned(fp8 ? (const void*)c.k8 : c.k, 16) ||
+      !aligned(fp8 ? (const void*)c.v8 : c.v, 16) || !aligned(w_q, 16) || !aligned(cos_tab, 16) ||
+      !aligned(sin_tab, 16) || !aligned(out, 16))
     return GA_ERR_ALIGN;
+  if (fp8 && (!aligned(c.k_scale, 4) || !aligned(c.v_scale, 4))) return GA_ERR_ALIGN;
   if (n_seq == 0 || rows == 0) return GA_OK;
   if (!workspace || !aligned(workspace, 256) ||
       ws_bytes < ga_verify_workspace_bytes(n_seq, rows, max_len))
@@ -333,7 +363,7 @@ int verify_run(const ga_bf16* qg, const VerifyCaches& c, const int* seq_len, int
     AttnArgs a{};
     a.qg = qg + (size_t)g0 * rows * kRowElems;
     a.out = out + (size_t)g0 * rows * kOutRow;
-    a.mode = kModeVerify;
+    a.mode = fp8 ? kModeVerify8 : kModeVerify;
     a.n_seq = n;
     a.vrows = rows;
     SeqPositions sp{};
@@ -372,7 +402,16 @@ int verify_run(const ga_bf16* qg, const VerifyCaches& c, const int* seq_len, int
     CUtensorMap tm_q, tm_k, tm_v;
     st = encode_q_map(&tm_q, a.out, (long long)n * rows, kVerifyHeadsPerTile, rows);
     if (st != GA_OK) return st;
-    if (c.page_table) {
+    if (fp8) {
+      const size_t seq_codes = (size_t)c.cap * kKvHeads * kDim;
+      st = encode_kv8_map(&tm_k, c.k8 + (size_t)g0 * seq_codes, c.cap, n);
+      if (st != GA_OK) return st;
+      st = encode_kv8_map(&tm_v, c.v8 + (size_t)g0 * seq_codes, c.cap, n);
+      if (st != GA_OK) return st;
+      a.k_scale = c.k_scale + (size_t)g0 * c.cap * kKvHeads;
+      a.v_scale = c.v_scale + (size_t)g0 * c.cap * kKvHeads;
+      a.cache_cap = c.cap;
+    } else if (c.page_table) {
       // the whole pools, the page as the outer coordinate
       st = encode_kv_map(&tm_k, c.k, c.page_size, c.n_pages, true);
       if (st != GA_OK) return st;
@@ -717,6 +756,28 @@ int ga_attn_verify(const ga_bf16* qg, const ga_bf16* k_cache, const ga_bf16* v_c
   VerifyCaches c{};
   c.k = k_cache;
   c.v = v_cache;
+  c.cap = cap;
+  return verify_run(qg, c, seq_len, n_seq, rows, w_q, cos_tab, sin_tab, table_rows, out,
+                    workspace, ws_bytes, stream);
+}
+
+int ga_attn_verify_e4m3(const ga_bf16* qg, const uint8_t* k_codes, const float* k_scale,
+                        const uint8_t* v_codes, const float* v_scale, int cap, const int* seq_len,
+                        int n_seq, int rows, const ga_bf16* w_q, const ga_bf16* cos_tab,
+                        const ga_bf16* sin_tab, int table_rows, ga_bf16* out, void* workspace,
+                        size_t ws_bytes, ga_stream stream) {
+  if (!qg || !k_codes || !k_scale || !v_codes || !v_scale || !seq_len || !w_q || !cos_tab ||
+      !sin_tab || !out)
+    return GA_ERR_NULL;
+  if (n_seq < 0 || rows < 0 || cap < 1 || table_rows < 0) return GA_ERR_SHAPE;
+  if (rows > 16 || cap > GA_MAX_TOKENS) return GA_ERR_RANGE;
+  for (int b = 0; b < n_seq; ++b)
+    if (seq_len[b] < 0 || (long long)seq_len[b] + rows > cap) return GA_ERR_RANGE;
+  VerifyCaches c{};
+  c.k8 = k_codes;
+  c.v8 = v_codes;
+  c.k_scale = k_scale;
+  c.v_scale = v_scale;
   c.cap = cap;
   return verify_run(qg, c, seq_len, n_seq, rows, w_q, cos_tab, sin_tab, table_rows, out,
                     workspace, ws_bytes, stream);

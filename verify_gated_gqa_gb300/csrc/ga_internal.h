@@ -31,6 +31,7 @@ enum AttnMode : int {
   kModeMask = 2,     // stored bit mask (from the mask prepass)
   kModeVerify = 3,   // few-row windows over long caches: split-key partials (see below)
   kModeBatch = 4,    // several causal prefills (windows) over paged caches in one launch
+  kModeVerify8 = 5,  // verify over e4m3 caches, widened to bf16 in the shared-memory slot
 };
 
 // Batch mode: sequence b's rows are packed rows batch_row0[b] .. + batch_rows[b] - 1 (row r
@@ -73,6 +74,10 @@ struct AttnArgs {
   // page_table[b * max_pages + kt / page_tiles] of the page pools
   const int* page_table;
   int page_tiles, max_pages, n_pages;
+  // verify over e4m3 caches: scales [n_seq][cache_cap][2] fp32 of the key and value rows
+  const float* k_scale;
+  const float* v_scale;
+  int cache_cap;
   // batch mode (n_seq sequences, n_items = n_entries * 24)
   int n_entries;
   int batch_row0[kVerifyMaxSeq], batch_rows[kVerifyMaxSeq], batch_qbase[kVerifyMaxSeq];
