@@ -546,12 +546,12 @@ def run_batch(args, world, rank, local):
 
 
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
-# summarised in profiles/attn_kernel_causal_s8192.md (218,201,856 + 61,244,928) and
-# profiles/attn_kernel_verify_8x16_l65536.md (1,077,417,472 + 18,403,072, the verify
+# summarised in profiles/attn_kernel_causal_s8192.md (218,203,904 + 61,091,072) and
+# profiles/attn_kernel_verify_8x16_l65536.md (1,077,440,256 + 18,318,592, the verify
 # variant of attn_kernel); each is to be set to None whenever its kernel changes until it is
 # captured again.
-ATTN_TRAFFIC_BYTES = 279_446_784
-VERIFY_ATTN_TRAFFIC_BYTES = 1_095_820_544
+ATTN_TRAFFIC_BYTES = 279_294_976
+VERIFY_ATTN_TRAFFIC_BYTES = 1_095_758_848
 
 
 # ---------------------------------------------------------------- the oracle as baseline
