@@ -294,7 +294,7 @@ def run_gpu(args, world, rank, local):
     return line
 
 
-# ---------------------------------------------------------------- verify windows (config 5)
+# ---------------------------------------------------------------- verify windows (8 x 16 rows, L = 65,536)
 V_ROWS, V_L = 16, 65536
 V_CAP = V_L + V_ROWS
 V_PAGE = 256   # positions per page of the paged-cache workload
@@ -307,8 +307,9 @@ def verify_bytes(n_seq):
 
 
 def run_verify(args, world, rank, local):
-    """Config 5 on one GPU (per rank): ga_attn_verify over prepared caches resident in HBM
-    (--verify-seqs sequences; 8 is the configuration, fewer only for profiling). With
+    """Verify windows on one GPU (per rank): ga_attn_verify over prepared caches resident in
+    HBM, 16 rows over 65,536 cached keys per sequence (--verify-seqs sequences; 8 is the
+    workload, fewer only for profiling). With
     --workload verify_paged the same caches sit in pages of 256 positions scattered over
     two page pools in a seeded random order, read through ga_attn_verify_paged."""
     V_SEQ = args.verify_seqs
@@ -650,9 +651,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", default="prefill",
                     choices=["prefill", "verify", "verify_paged", "verify_e4m3", "batch"],
-                    help="prefill: the headline S=8192 causal step; verify: config 5; "
-                         "verify_paged: config 5 over paged caches; verify_e4m3: config 5 "
-                         "over e4m3 caches; batch: 16 prompts of "
+                    help="prefill: the headline S=8192 causal step; verify: 8 x 16 rows over "
+                         "65,536 cached keys; verify_paged: the same over paged caches; "
+                         "verify_e4m3: the same over e4m3 caches; batch: 16 prompts of "
                          "512..4096 tokens in one batched call")
     ap.add_argument("--verify-seqs", type=int, default=8)
     args = ap.parse_args()

@@ -52,7 +52,7 @@ extern "C" {
 #define GA_HEAD_DIM 256
 #define GA_ROPE_DIMS 64
 #define GA_MASKED_MAX_TOKENS 8192 /* pegainfer PR #1151, §Summary: the 8192-token cap */
-#define GA_MAX_TOKENS (1 << 20)   /* index-arithmetic limit of this build */
+#define GA_MAX_TOKENS (1 << 20)   /* index-arithmetic limit of the library */
 
 typedef uint16_t ga_bf16; /* bfloat16 bit pattern */
 typedef void* ga_stream;  /* cudaStream_t */
@@ -67,7 +67,7 @@ enum ga_status {
   GA_ERR_WORKSPACE = -6, /* workspace missing, misaligned or smaller than required */
   GA_ERR_DEVICE = -7,    /* current device is not sm_103 or refused the smem opt-in */
   GA_ERR_CUDA = -8,      /* a CUDA call failed; see ga_last_cuda_error() */
-  GA_ERR_GEOMETRY = -9   /* ga_check_geometry: not this build's compiled geometry */
+  GA_ERR_GEOMETRY = -9   /* ga_check_geometry: not the compiled geometry */
 };
 
 /* Geometry a caller expects; ga_check_geometry compares it with the compiled constants

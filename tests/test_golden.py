@@ -1,5 +1,5 @@
 """Values the pages print, kept as small text fixtures under tests/golden/ with their
-citations, checked against this build's conventions."""
+citations, checked against the library's conventions."""
 import os
 
 import pytest

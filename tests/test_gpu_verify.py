@@ -83,7 +83,7 @@ def test_verify_equals_prefill_rows():
 
 
 def test_verify_long_cache_sampled():
-    """Config-5 shape on two sequences: 16 rows at positions 65,536..65,551 over 65,536
+    """The long-cache verify shape on two sequences: 16 rows at positions 65,536..65,551 over 65,536
     cached keys (cap 65,552); sampled heads against the oracle."""
     lens, rows, cap = [65536, 65536], 16, 65552
     out, data, kd, _ = _run(SEED + 32, lens, rows, cap)
@@ -91,6 +91,36 @@ def test_verify_long_cache_sampled():
     refs = _refs(data, lens, cap, heads=heads)
     for b in range(2):
         refs[b].check(out[b], what=f"verify L=65536 seq {b} heads {heads}")
+
+
+def test_verify_8x16_l65536_launch_sampled():
+    """The benchmark's launch: 8 sequences x 16 rows at positions 65,536..65,551 over caches
+    of 65,552 positions (the chunking the bench times); three sequences' sampled heads
+    against the oracle. Inputs are generated on the device with the same seeded recipe."""
+    lens, rows, cap, n = [65536] * 8, 16, 65552, 8
+    seed = SEED + 35
+    dev = "cuda"
+    w_q = synth.normal_bf16(seed, "w_q", (256,), sigma=0.1, device=dev)
+    w_k = synth.normal_bf16(seed, "w_k", (256,), sigma=0.1, device=dev)
+    c, s = B.ga_rope_table_host(cap)
+    c, s = c.cuda(), s.cuda()
+    kd = torch.empty(n, cap, 2, 256, dtype=torch.bfloat16, device=dev)
+    vd = torch.empty_like(kd)
+    for b in range(n):
+        B.ga_k_prologue(synth.normal_bf16(seed, "k", (cap, 2, 256), sub=b, device=dev), w_k, c,
+                        s, k_prep=kd[b])
+        vd[b] = synth.normal_bf16(seed, "v", (cap, 2, 256), sub=b, device=dev)
+    qg = torch.stack([synth.normal_bf16(seed, "qg", (rows, 24, 512), sub=b, device=dev)
+                      for b in range(n)])
+    out = B.ga_attn_verify(qg, kd, vd, lens, w_q, c, s)
+    torch.cuda.synchronize()
+    oc, os_ = O.rope_tables(cap)
+    heads = [3, 12, 22]
+    for b in (0, 4, 7):
+        # the device's prepared keys are bit-exact to the oracle's (test_k_prologue_bit_exact)
+        AttnRef(np64(qg[b]), np64(kd[b]), np64(vd[b]), np64(w_q), oc, os_, lens[b],
+                lens[b] + rows, "causal", heads=heads).check(
+            out[b], what=f"8 x 16 rows at L=65536, seq {b}, heads {heads}")
 
 
 def test_verify_single_sequence():
