@@ -204,6 +204,51 @@ def visibility(kind, rows, T, q_base=0, mask=None):
 
 
 # ----------------------------------------------------------------------------------
+# Selection mask: the indexer's top-k blocks AND causality
+# ----------------------------------------------------------------------------------
+# [QSA], the commit moving the oracle to the real geometry: an indexer budget of 2048
+# tokens is 512 blocks, so a block holds 4 consecutive keys; its golden review: budget
+# 16 -> block_topk 4.
+BLOCK_TOKENS = 4
+
+
+def block_topk_for_budget(budget):
+    """Blocks a row keeps for a token budget: budget / BLOCK_TOKENS (2048 -> 512, 16 -> 4)."""
+    budget = int(budget)
+    if budget < BLOCK_TOKENS or budget % BLOCK_TOKENS:
+        raise ValueError("the budget is a positive multiple of the block size")
+    return budget // BLOCK_TOKENS
+
+
+def select_blocks_mask(block_scores, q_base, T, block_topk):
+    """uint8 [rows, T], 1 = visible: the mask the stored-mask pass reads, built from the
+    indexer's per-block scores ([QSA] the attention-reader commit: the mask is the
+    indexer's selection AND causality; the golden's effective mask is the same AND).
+
+    block_scores [rows, >= ceil(T / 4)]: row r (position p = q_base + r) scores block b,
+    the keys 4b .. 4b + 3. The row's candidates are the blocks holding a key j <= p, that
+    is b = 0 .. p // 4. It keeps the block_topk candidates with the highest scores, a tie
+    going to the lower block index (every candidate when there are fewer), and sees key j
+    iff j <= p and block j // 4 is kept. Scores may be +-inf, never NaN; -0 equals +0."""
+    s = np.asarray(block_scores, np.float64)
+    rows = s.shape[0]
+    nb = -(-T // BLOCK_TOKENS)
+    assert block_topk >= 1 and q_base >= 0 and q_base + rows <= T
+    assert not np.isnan(s[:, :nb]).any(), "scores must not be NaN"
+    j = np.arange(T)
+    out = np.zeros((rows, T), np.uint8)
+    for r in range(rows):
+        p = q_base + r
+        nc = min(nb, p // BLOCK_TOKENS + 1)
+        cand = np.arange(nc)
+        order = np.lexsort((cand, -s[r, :nc]))      # score descending, then index ascending
+        kept = np.zeros(nb, dtype=bool)
+        kept[order[:block_topk]] = True
+        out[r] = (j <= p) & kept[j // BLOCK_TOKENS]
+    return out
+
+
+# ----------------------------------------------------------------------------------
 # The attention core
 # ----------------------------------------------------------------------------------
 def sigmoid_gate(g, mode="R1"):

@@ -32,3 +32,34 @@ def test_causal_pair_count():
     """The causal pass at S = 8192 has S (S + 1) / 2 visible pairs per head."""
     assert bench.visible_pairs_causal(8192, 8192) == 8192 * 8193 // 2
     assert bench.FLOPS_STEP == 4.0 * 256 * 24 * 33_558_528
+
+
+def _budget_rows(kind):
+    return [r[1:] for r in _rows("qsa_indexer_budget.txt") if r[0] == kind]
+
+
+@pytest.mark.parametrize("row", _budget_rows("budget"))
+def test_indexer_budget_gives_block_topk(row):
+    """The two budget -> block_topk pairs the pages print fix a block of 4 tokens."""
+    from oracle import ga_oracle as O
+    budget, topk = int(row[0]), int(row[1])
+    assert O.block_topk_for_budget(budget) == topk
+    assert O.BLOCK_TOKENS == budget // topk
+
+
+@pytest.mark.parametrize("row", _budget_rows("drop"))
+def test_budget_truncation_drops_one_block(row):
+    """A row whose causal prefix is exactly `complete` whole blocks, under block_topk one
+    fewer, loses one block: the printed count of dropped causally visible keys. Scores
+    are distinct, so the lowest-scoring block is the one dropped."""
+    import numpy as np
+    from oracle import ga_oracle as O
+    complete, topk, dropped = (int(x) for x in row)
+    T = complete * O.BLOCK_TOKENS
+    p = T - 1                                         # the row sees keys 0 .. T - 1
+    scores = np.array([[3.0, 1.0, 4.0, 1.5, 9.0]])[:, :complete]
+    m = O.select_blocks_mask(scores, p, T, topk)
+    causal = np.arange(T) <= p
+    assert int((causal & (m[0] == 0)).sum()) == dropped
+    low = int(np.argmin(scores[0]))
+    assert not m[0, low * O.BLOCK_TOKENS:(low + 1) * O.BLOCK_TOKENS].any()

@@ -578,3 +578,91 @@ def test_planted_eps_outside_sqrt_is_caught(monkeypatch):
     monkeypatch.setattr(O, "rms_norm_1pw", wrong)
     with pytest.raises(AssertionError):
         test_norm_constant_vector_closed_form()
+
+
+# ---------------------------------------------------------------- selection mask
+def _kept_blocks(mask_row, p):
+    """Blocks kept in a mask row: every candidate block b has its first key 4b <= p."""
+    nc = p // O.BLOCK_TOKENS + 1
+    return {b for b in range(nc) if b * O.BLOCK_TOKENS < mask_row.shape[0]
+            and mask_row[b * O.BLOCK_TOKENS]}
+
+
+def test_select_brute_force_tiny():
+    """Brute force over every subset: among the candidate subsets of size min(k, nc),
+    exactly one is closed under 'beats' (higher score, or equal score and lower index)
+    against every left-out candidate, and it is the oracle's. Scores are drawn from a
+    handful of values (with -0, +0 and +-inf) so ties are everywhere."""
+    import itertools
+    rng = np.random.default_rng(81)
+    vals = np.array([-np.inf, -1.0, -0.0, 0.0, 0.5, 1.0, np.inf])
+    for trial in range(60):
+        T = int(rng.integers(1, 27))
+        nb = -(-T // O.BLOCK_TOKENS)
+        q_base = int(rng.integers(0, T))
+        rows = T - q_base
+        k = int(rng.integers(1, 8))
+        s = vals[rng.integers(0, len(vals), (rows, nb))]
+        m = O.select_blocks_mask(s, q_base, T, k)
+        for r in range(rows):
+            p = q_base + r
+            nc = min(nb, p // O.BLOCK_TOKENS + 1)
+            beats = lambda a, b: s[r, a] > s[r, b] or (s[r, a] == s[r, b] and a < b)
+            ok = [set(c) for c in itertools.combinations(range(nc), min(k, nc))
+                  if all(beats(a, b) for a in c for b in set(range(nc)) - set(c))]
+            assert len(ok) == 1, (trial, r)
+            assert _kept_blocks(m[r], p) == ok[0], (trial, r)
+            assert np.array_equal(m[r] != 0, (np.arange(T) <= p) &
+                                  np.isin(np.arange(T) // O.BLOCK_TOKENS, list(ok[0])))
+
+
+def test_select_invariants_and_special_cases():
+    """N(0,1) scores, a ragged T: the mask lies inside causality, keeps min(k, nc) blocks,
+    never hides a whole row; k >= nc gives the causal row; k = 1 keeps numpy's argmax
+    (its first maximum, i.e. the lower index on a tie); constant scores keep the k lowest
+    blocks; raising a kept block's score or lowering a dropped one changes nothing."""
+    rng = np.random.default_rng(82)
+    T, q_base, k = 1203, 5, 37
+    rows = T - q_base
+    nb = -(-T // 4)
+    s = rng.standard_normal((rows, nb))
+    m = O.select_blocks_mask(s, q_base, T, k)
+    causal = O.visibility("causal", np.arange(rows), T, q_base)
+    assert not np.any((m != 0) & ~causal)
+    for r in range(0, rows, 7):
+        p = q_base + r
+        nc = min(nb, p // 4 + 1)
+        kept = _kept_blocks(m[r], p)
+        assert len(kept) == min(k, nc) and m[r].any()
+        if k >= nc:
+            assert np.array_equal(m[r] != 0, causal[r])
+        else:
+            lowest_kept = min(s[r, b] for b in kept)
+            assert all(s[r, b] <= lowest_kept for b in set(range(nc)) - kept)
+    one = O.select_blocks_mask(s, q_base, T, 1)
+    for r in range(0, rows, 11):
+        p = q_base + r
+        assert _kept_blocks(one[r], p) == {int(np.argmax(s[r, :min(nb, p // 4 + 1)]))}
+    const = O.select_blocks_mask(np.full((rows, nb), 0.25), q_base, T, k)
+    j = np.arange(T)
+    assert np.array_equal(const != 0, causal & (j < 4 * k)[None, :])
+    assert np.array_equal(O.select_blocks_mask(s, q_base, T, nb) != 0, causal)
+    s2 = s.copy()
+    r = rows - 1
+    kept = sorted(_kept_blocks(m[r], q_base + r))
+    dropped = sorted(set(range(nb)) - set(kept))
+    s2[r, kept[0]] += 5.0
+    s2[r, dropped[0]] -= 5.0
+    assert np.array_equal(O.select_blocks_mask(s2[r:], q_base + r, T, k), m[r:])
+
+
+def test_planted_reversed_tie_rule_is_caught():
+    """An oracle that breaks ties toward the higher block index fails the constant-score
+    special case (the k lowest blocks)."""
+    T, k = 40, 3
+    s = np.zeros((1, 10))
+    m = O.select_blocks_mask(s, T - 1, T, k)
+    order_hi = np.lexsort((-np.arange(10), -s[0]))[:k]      # the planted rule
+    planted = np.isin(np.arange(T) // 4, order_hi)
+    assert not np.array_equal(m[0] != 0, planted)
+    assert np.array_equal(m[0] != 0, np.arange(T) < 4 * k)
