@@ -425,6 +425,86 @@ def run_verify(args, world, rank, local):
     }
 
 
+SEL_T, SEL_BUDGET, SEL_SETS = 8192, 2048, 4
+
+
+def select_bytes(T=SEL_T, budget=SEL_BUDGET):
+    """Algorithmic bytes of one selection-mask call over rows at positions 0 .. T-1: the
+    candidate scores of every row that must select (more candidate blocks than it keeps;
+    the others keep all of theirs and need no score), read once, and the T x T mask
+    written once."""
+    k = budget // 4
+    read = sum(4 * (p // 4 + 1) for p in range(T) if p // 4 + 1 > k)
+    return read + T * T
+
+
+def run_select(args, world, rank, local):
+    """The selection-mask producer: ga_select_mask over 8192 query rows and 8192 keys (2048
+    blocks of 4 keys, N(0,1) fp32 scores), block_topk 512 (a budget of 2048 tokens). Each
+    step takes the next of four input sets (scores 64 MiB + mask 64 MiB each), so the
+    set a step touches has left L2 since its last use."""
+    from verify_gated_gqa_gb300 import binding as B
+    from verify_gated_gqa_gb300 import synth
+    from verify_gated_gqa_gb300.build import build
+
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    seed = SEED + 9 + rank
+    k = SEL_BUDGET // 4
+    scores = [synth.block_scores(seed + i, SEL_T, SEL_T // 4, device=dev) for i in range(SEL_SETS)]
+    masks = [torch.empty(SEL_T, SEL_T, dtype=torch.uint8, device=dev) for _ in range(SEL_SETS)]
+    n_bytes = select_bytes()
+    it = [0]
+
+    def step():
+        i = it[0] % SEL_SETS
+        it[0] += 1
+        B.ga_select_mask(scores[i], SEL_T, k, mask=masks[i])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / args.steps
+    if rank != 0:
+        return None
+    _, peak_hbm, peak_src = measured_peaks()
+    gbs = n_bytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": "selection mask: HBM GB/s (8192 rows x 8192 keys, block_topk 512)",
+        "value": round(world * gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) fp32 block scores)",
+        "config": {"workload": "selection mask: scores [8192, 2048] fp32 -> mask [8192, 8192] "
+                               "uint8, blocks of 4 keys, top 512 blocks per row AND causal",
+                   "l2": f"{SEL_SETS} input sets of 128 MiB in rotation"},
+        "rows_per_s": round(world * SEL_T / (ms * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                     "frac": round(gbs / peak_hbm, 4), "traffic": None,
+                     "peak_kind": f"HBM copy ({peak_src})", "kernel": "select_mask_kernel",
+                     "algorithmic_bytes": n_bytes},
+        "gpu_launches": args.steps, "clocks": clk, "device_status": B.ga_device_status(),
+    }
+
+
 B_LENS = [512 * (1 + b % 8) for b in range(16)]   # 16 prompts of 512 .. 4096 tokens
 B_PAGE = 256
 
@@ -650,11 +730,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", default="prefill",
-                    choices=["prefill", "verify", "verify_paged", "verify_e4m3", "batch"],
+                    choices=["prefill", "verify", "verify_paged", "verify_e4m3", "batch",
+                             "select"],
                     help="prefill: the headline S=8192 causal step; verify: 8 x 16 rows over "
                          "65,536 cached keys; verify_paged: the same over paged caches; "
                          "verify_e4m3: the same over e4m3 caches; batch: 16 prompts of "
-                         "512..4096 tokens in one batched call")
+                         "512..4096 tokens in one batched call; select: the selection-mask "
+                         "producer at 8192 x 8192, block_topk 512")
     ap.add_argument("--verify-seqs", type=int, default=8)
     args = ap.parse_args()
     world, rank, local = dist_env()
@@ -664,6 +746,8 @@ def main():
         line = run_verify(args, world, rank, local)
     elif args.workload == "batch":
         line = run_batch(args, world, rank, local)
+    elif args.workload == "select":
+        line = run_select(args, world, rank, local)
     else:
         line = run_gpu(args, world, rank, local)
     if line is not None:

@@ -53,6 +53,8 @@ extern "C" {
 #define GA_ROPE_DIMS 64
 #define GA_MASKED_MAX_TOKENS 8192 /* pegainfer PR #1151, §Summary: the 8192-token cap */
 #define GA_MAX_TOKENS (1 << 20)   /* index-arithmetic limit of the library */
+/* Keys per indexer block (pegainfer PR #1151: a budget of 2048 tokens is 512 blocks). */
+#define GA_INDEX_BLOCK_TOKENS 4
 
 typedef uint16_t ga_bf16; /* bfloat16 bit pattern */
 typedef void* ga_stream;  /* cudaStream_t */
@@ -230,6 +232,27 @@ int ga_attn_masked_static(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf1
                           int table_rows, int rows, int T, int q_base, const uint8_t* mask,
                           long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
                           ga_stream stream);
+
+/* The selection mask ga_attn_masked reads, from the indexer's per-block scores (pegainfer
+ * PR #1151, "feat(qwen4): add the QSA sparse-attention kernel and its golden": the mask is
+ * the indexer's selection AND causality; a budget of 2048 tokens keeps 512 blocks of 4 keys,
+ * a budget of 16 keeps 4). The scores themselves come from the indexer, which the pages
+ * do not specify; this call does the selection and writes the mask.
+ *   block_scores [rows][ld_scores] fp32, 4-byte aligned: row r scores block b (keys
+ *           4b .. 4b+3) at r * ld_scores + b for b < ceil(T / 4). Scores may be +-inf
+ *           and -0 equals +0; a NaN score gives an unspecified selection for its row.
+ *   rows, T, q_base: row r is query position p = q_base + r; the keys are 0 .. T-1
+ *   block_topk  blocks kept per row (budget / GA_INDEX_BLOCK_TOKENS)
+ *   mask    [rows][ld_mask] uint8, written for columns 0 .. T-1 (later columns untouched):
+ *           1 iff j <= p and block j / 4 is among the row's block_topk highest-scoring
+ *           candidates (the blocks b <= p / 4), a tie going to the lower block index;
+ *           every candidate when there are fewer. A row always sees at least one key.
+ * Rules: T <= GA_MASKED_MAX_TOKENS, q_base + rows <= T, ld_scores >= ceil(T / 4),
+ * ld_mask >= T, ld_mask % 16 == 0, mask 16-byte aligned, both leading dimensions <= 2^31.
+ * Nothing is allocated; the call keeps no pointer. rows == 0 is a no-op.
+ * Errors: NULL, SHAPE, RANGE, ALIGN, DEVICE, CUDA. */
+int ga_select_mask(const float* block_scores, long long ld_scores, int rows, int T, int q_base,
+                   int block_topk, uint8_t* mask, long long ld_mask, ga_stream stream);
 
 /* Bytes of workspace ga_attn_verify needs; max_len is the largest L over the sequences. */
 size_t ga_verify_workspace_bytes(int n_seq, int rows, int max_len);

@@ -227,6 +227,28 @@ def test_quantize_refusals_make_no_cuda_call(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def test_select_mask_refusals_make_no_cuda_call(L):
+    before = L.ga_debug_cuda_calls()
+    f = L.ga_select_mask
+    assert f(None, 2048, 10, 8192, 0, 512, A, 8192, S) == -1
+    assert f(A, 2048, 10, 8192, 0, 512, None, 8192, S) == -1
+    assert f(A, 2048, -1, 8192, 0, 512, A, 8192, S) == -2
+    assert f(A, 2048, 10, 0, 0, 512, A, 8192, S) == -2
+    assert f(A, 2048, 10, 8192, -1, 512, A, 8192, S) == -2
+    assert f(A, 2048, 10, 8192, 0, 0, A, 8192, S) == -2
+    assert f(A, 2049, 10, 8196, 0, 512, A, 8208, S) == -4       # T over the masked cap
+    assert f(A, 2048, 10, 8192, 8183, 512, A, 8192, S) == -4    # q_base + rows > T
+    assert f(A, 2047, 10, 8192, 0, 512, A, 8192, S) == -4       # ld_scores < ceil(T / 4)
+    assert f(A, 26, 10, 101, 0, 4, A, 96, S) == -4              # ld_mask < T
+    assert f(A, 1 << 32, 10, 8192, 0, 4, A, 8192, S) == -4
+    assert f(A, 2048, 10, 8192, 0, 512, A, 8200, S) == -3       # ld_mask % 16
+    assert f(A, 2048, 10, 8192, 0, 512, A + 8, 8192, S) == -3
+    assert f(A + 2, 2048, 10, 8192, 0, 512, A, 8192, S) == -3
+    assert f(A, 2048, 0, 8192, 0, 512, A, 8192, S) == 0         # no rows: a no-op
+    assert f(A, 26, 10, 101, 91, 4, A + 4, 112, S) == -3
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_k_prologue_refusals(L):
     before = L.ga_debug_cuda_calls()
     assert L.ga_k_prologue(None, A, A, A, 100, 10, 0, A, S) == -1

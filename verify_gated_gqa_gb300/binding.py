@@ -56,6 +56,7 @@ _SIGS = {
     "ga_kv_quantize_e4m3": (_I, [_P, _LL, _P, _P, _P]),
     "ga_attn_verify_e4m3": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P, _SZ,
                                  _P]),
+    "ga_select_mask": (_I, [_P, _LL, _I, _I, _I, _I, _P, _LL, _P]),
 }
 
 
@@ -236,6 +237,26 @@ def ga_attn_masked(qg, k_prep, v, w_q, cos_tab, sin_tab, mask, q_base=0, T=None,
                                 _ptr(workspace), workspace.numel(), _stream()),
            "ga_attn_masked")
     return out, weights, hidden_rows
+
+
+def ga_select_mask(block_scores, T, block_topk, q_base=0, mask=None):
+    """block_scores float32 [rows, >= ceil(T / 4)] (unit column stride) -> the selection
+    mask uint8 [rows, ld] that ga_attn_masked reads (ld = T rounded up to 16 when the mask is
+    allocated here; its columns from T on stay 0)."""
+    if (block_scores.dtype != torch.float32 or not block_scores.is_cuda or
+            block_scores.dim() != 2 or block_scores.stride(1) != 1):
+        raise ValueError("block_scores must be a 2-D float32 CUDA tensor with unit column stride")
+    rows = block_scores.shape[0]
+    if mask is None:
+        mask = torch.zeros(rows, (T + 15) // 16 * 16, dtype=torch.uint8,
+                           device=block_scores.device)
+    if (mask.dtype != torch.uint8 or not mask.is_cuda or mask.dim() != 2 or
+            mask.shape[0] != rows or mask.stride(1) != 1):
+        raise ValueError("mask must be a uint8 CUDA tensor [rows, ld] with unit column stride")
+    _check(lib().ga_select_mask(_ptr(block_scores), block_scores.stride(0), rows, T, q_base,
+                                block_topk, _ptr(mask), mask.stride(0), _stream()),
+           "ga_select_mask")
+    return mask
 
 
 def ga_attn_masked_static(qg, k_prep, v, w_q, cos_tab, sin_tab, mask, out, hidden_rows,

@@ -865,6 +865,25 @@ int ga_kv_quantize_e4m3(const ga_bf16* x, long long n_tok, uint8_t* q, float* sc
   return GA_OK;
 }
 
+int ga_select_mask(const float* block_scores, long long ld_scores, int rows, int T, int q_base,
+                   int block_topk, uint8_t* mask, long long ld_mask, ga_stream stream) {
+  if (!block_scores || !mask) return GA_ERR_NULL;
+  if (rows < 0 || T < 1 || q_base < 0 || block_topk < 1) return GA_ERR_SHAPE;
+  if (T > GA_MASKED_MAX_TOKENS || (long long)q_base + rows > T) return GA_ERR_RANGE;
+  const long long n_blocks = (T + GA_INDEX_BLOCK_TOKENS - 1) / GA_INDEX_BLOCK_TOKENS;
+  if (ld_scores < n_blocks || ld_mask < T || ld_scores > (1LL << 31) || ld_mask > (1LL << 31))
+    return GA_ERR_RANGE;
+  if (!aligned(block_scores, 4) || !aligned(mask, 16) || ld_mask % 16 != 0) return GA_ERR_ALIGN;
+  if (rows == 0) return GA_OK;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaError_t e = GA_CUDA(launch_select_mask(block_scores, ld_scores, rows, T, q_base, block_topk,
+                                             mask, ld_mask, (cudaStream_t)stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return GA_OK;
+}
+
 // ------------------------------------------------------------------ allocation-free masked call
 // The scratch of ga_attn_masked_static: one static array per device, reserved at module
 // load, its address looked up once per device on the first call (with that device current).

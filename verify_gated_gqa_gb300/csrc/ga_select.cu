@@ -1,0 +1,173 @@
+// Selection mask from the indexer's block scores (pegainfer PR #1151, "feat(qwen4): add the
+// QSA sparse-attention kernel and its golden": the attention reads the indexer's selection
+// AND causality as its mask; the commit moving to the real geometry keeps 512 blocks for a
+// budget of 2048 tokens, so a block is 4 consecutive keys).
+//
+// One CTA of 256 threads per query row r at position p = q_base + r. The row's candidates
+// are the blocks b = 0 .. nc-1 holding a key j <= p, nc = min(ceil(T / 4), p / 4 + 1); it
+// keeps the top_k highest scores, a tie going to the lower block index. Thread t holds
+// blocks t + 256 i (i < 8) as order-preserving unsigned keys. A radix select (four passes of
+// 8 bits over a shared 256-bin histogram; lanes with the same digit add once, through
+// __match_any_sync) gives the top_k-th largest key tau and the number `need` of keys equal
+// to tau that are kept: those with the lowest block indices, ranked by a block-wide count
+// in index order. The row's T mask bytes (1 = visible) then go out as 16-byte stores.
+#include "ga_internal.h"
+
+namespace ga {
+namespace {
+
+constexpr int kBlockTokens = GA_INDEX_BLOCK_TOKENS;   // 4
+constexpr int kSelThreads = 256;
+constexpr int kSelMaxBlocks = GA_MASKED_MAX_TOKENS / kBlockTokens;   // 2048
+constexpr int kSelKeys = kSelMaxBlocks / kSelThreads;            // 8 per thread
+constexpr int kSelWarps = kSelThreads / 32;
+static_assert(kSelKeys * kSelThreads == kSelMaxBlocks, "blocks per row");
+static_assert(kSelKeys * kSelWarps == 64, "the tie scan gives two entries to each lane");
+
+// IEEE order as unsigned order. -0 becomes +0 first, so the two tie as the values do.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_mask_kernel(
+    const float* __restrict__ scores, long long ld_scores, int T, int q_base, int top_k,
+    uint8_t* __restrict__ mask, long long ld_mask) {
+  __shared__ uint32_t sel_words[kSelMaxBlocks / 4];   // byte b: 1 if block b is kept
+  __shared__ int hist[256];
+  __shared__ int tie_base[kSelKeys * kSelWarps];      // entry i * 8 + warp
+  __shared__ int s_digit, s_need;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = blockIdx.x;
+  const int p = q_base + r;
+  const int nb = (T + kBlockTokens - 1) / kBlockTokens;
+  const int nc = min(nb, p / kBlockTokens + 1);
+  uint8_t* sel = reinterpret_cast<uint8_t*>(sel_words);
+
+  if (top_k >= nc) {
+    // every candidate is kept: the causal row
+#pragma unroll
+    for (int i = 0; i < kSelKeys; ++i) sel[tid + i * kSelThreads] = (tid + i * kSelThreads) < nc;
+  } else {
+    const float* row = scores + (long long)r * ld_scores;
+    uint32_t key[kSelKeys];
+#pragma unroll
+    for (int i = 0; i < kSelKeys; ++i) {
+      const int b = tid + i * kSelThreads;
+      key[i] = b < nc ? order_key(__ldg(row + b)) : 0u;
+    }
+    uint32_t prefix = 0, pmask = 0;
+    int need = top_k;   // keys still to take among those that match the prefix
+#pragma unroll 1
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      hist[tid] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < kSelKeys; ++i) {
+        const int b = tid + i * kSelThreads;
+        const bool act = b < nc && (key[i] & pmask) == prefix;
+        const uint32_t d = act ? (key[i] >> shift) & 255u : 256u;
+        const unsigned same = __match_any_sync(0xFFFFFFFFu, d);
+        if (act && lane == __ffs(same) - 1) atomicAdd(&hist[d], __popc(same));
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l holds bins 8l .. 8l+7; the digit is in the lane where the keys in higher
+        // bins are fewer than `need` and those in its bins and higher are at least `need`
+        int c[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = hist[8 * lane + j];
+          sum += c[j];
+        }
+        int incl = sum;   // keys in the bins of lanes lane .. 31
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_down_sync(0xFFFFFFFFu, incl, off);
+          if (lane + off < 32) incl += v;
+        }
+        const int above = incl - sum;
+        if (above < need && need <= incl) {
+          int acc = above;
+#pragma unroll
+          for (int j = 7; j >= 0; --j) {
+            if (acc < need && acc + c[j] >= need) {
+              s_digit = 8 * lane + j;
+              s_need = need - acc;
+            }
+            acc += c[j];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= (uint32_t)s_digit << shift;
+      pmask |= 255u << shift;
+      need = s_need;
+    }
+    // keys above tau are kept; of the keys equal to tau, the `need` lowest block indices.
+    // Index order is (i, warp, lane), so the rank of a tie is the ties in earlier
+    // (i, warp) groups plus those in lower lanes of its own warp.
+    unsigned tie[kSelKeys];
+#pragma unroll
+    for (int i = 0; i < kSelKeys; ++i) {
+      const int b = tid + i * kSelThreads;
+      tie[i] = __ballot_sync(0xFFFFFFFFu, b < nc && key[i] == prefix);
+      if (lane == 0) tie_base[i * kSelWarps + warp] = __popc(tie[i]);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int a0 = tie_base[2 * lane], a1 = tie_base[2 * lane + 1];
+      int incl = a0 + a1;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      const int excl = incl - a0 - a1;
+      tie_base[2 * lane] = excl;
+      tie_base[2 * lane + 1] = excl + a0;
+    }
+    __syncthreads();
+    const unsigned lower = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < kSelKeys; ++i) {
+      const int b = tid + i * kSelThreads;
+      const bool is_tie = (tie[i] >> lane) & 1u;
+      const int rank = tie_base[i * kSelWarps + warp] + __popc(tie[i] & lower);
+      sel[b] = (b < nc && key[i] > prefix) || (is_tie && rank < need);
+    }
+  }
+  __syncthreads();
+
+  // key j is visible iff j <= p and block j / 4 is kept
+  uint8_t* out = mask + (long long)r * ld_mask;
+  const int nvec = T / 16;
+  for (int v = tid; v < nvec; v += kSelThreads) {
+    const uint32_t w = sel_words[v];   // blocks 4v .. 4v+3
+    uint32_t word[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int vis = p - (16 * v + 4 * q) + 1;   // keys of the block at or before p
+      const uint32_t causal =
+          vis >= 4 ? 0xFFFFFFFFu : (vis <= 0 ? 0u : (1u << (8 * vis)) - 1u);
+      word[q] = ((w >> (8 * q)) & 1u) * 0x01010101u & causal;
+    }
+    *reinterpret_cast<uint4*>(out + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
+  }
+  for (int j = nvec * 16 + tid; j < T; j += kSelThreads)
+    out[j] = (j <= p && sel[j / kBlockTokens]) ? 1 : 0;
+}
+
+}  // namespace
+
+cudaError_t launch_select_mask(const float* scores, long long ld_scores, int rows, int T,
+                               int q_base, int top_k, uint8_t* mask, long long ld_mask,
+                               cudaStream_t s) {
+  select_mask_kernel<<<rows, kSelThreads, 0, s>>>(scores, ld_scores, T, q_base, top_k, mask,
+                                                  ld_mask);
+  return cudaGetLastError();
+}
+
+}  // namespace ga

@@ -28,7 +28,7 @@ _M2 = 0x94D049BB133111EB
 _MASK64 = (1 << 64) - 1
 
 # Tensor ids: part of the counter, so that tensors drawn with one seed are independent.
-TENSOR_IDS = {"qg": 1, "k": 2, "v": 3, "w_q": 4, "w_k": 5, "mask": 6}
+TENSOR_IDS = {"qg": 1, "k": 2, "v": 3, "w_q": 4, "w_k": 5, "mask": 6, "block_scores": 7}
 
 
 def _to_i64(u: int) -> int:
@@ -98,6 +98,18 @@ def normal_bf16(seed: int, tensor: str, shape, sigma: float = 1.0, sub: int = 0,
         z = _bits_to_normal(random_bits(key, s, c, device))
         out[s:s + c] = _double_to_bf16(z * sigma)
     return out.view(*shape)
+
+
+def block_scores(seed: int, rows: int, n_blocks: int, device="cpu", chunk: int = 1 << 24):
+    """float32 [rows, n_blocks] N(0, 1) indexer block scores from the counter stream (each
+    double rounded once to float32), standing in for the indexer's output."""
+    n = rows * n_blocks
+    key = stream_key(seed, "block_scores")
+    out = torch.empty(n, dtype=torch.float32, device=device)
+    for s in range(0, n, chunk):
+        c = min(chunk, n - s)
+        out[s:s + c] = _bits_to_normal(random_bits(key, s, c, device)).to(torch.float32)
+    return out.view(rows, n_blocks)
 
 
 def attention_inputs(seed: int, rows: int, T: int, device="cpu"):
