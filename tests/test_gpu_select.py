@@ -84,8 +84,12 @@ def test_select_strided_scores_and_wide_mask():
 
 
 def test_select_empty_rows_is_a_noop():
-    mask = torch.full((0, 16), 7, dtype=torch.uint8, device="cuda")
-    B.ga_select_mask(torch.empty(0, 4, device="cuda"), 16, 2, q_base=16, mask=mask)
+    """rows = 0 (views of real allocations: a zero-size tensor of its own has no pointer,
+    which the entry point refuses) leaves the mask untouched."""
+    mask = torch.full((4, 16), 7, dtype=torch.uint8, device="cuda")
+    B.ga_select_mask(torch.zeros(4, 4, device="cuda")[:0], 16, 2, q_base=16, mask=mask[:0])
+    torch.cuda.synchronize()
+    assert bool((mask == 7).all())
 
 
 def test_selected_mask_feeds_masked_attention():
