@@ -83,15 +83,6 @@ def test_select_strided_scores_and_wide_mask():
     assert np.all(got[:, T:] == 7)
 
 
-def test_select_empty_rows_is_a_noop():
-    """rows = 0 (views of real allocations: a zero-size tensor of its own has no pointer,
-    which the entry point refuses) leaves the mask untouched."""
-    mask = torch.full((4, 16), 7, dtype=torch.uint8, device="cuda")
-    B.ga_select_mask(torch.zeros(4, 4, device="cuda")[:0], 16, 2, q_base=16, mask=mask[:0])
-    torch.cuda.synchronize()
-    assert bool((mask == 7).all())
-
-
 def test_selected_mask_feeds_masked_attention():
     """Block scores -> ga_select_mask -> ga_attn_masked, against the oracle's selection and
     the oracle's masked attention (sampled heads), at S = 512 with a 64-token budget."""
