@@ -3,26 +3,35 @@
 // AND causality as its mask; the commit moving to the real geometry keeps 512 blocks for a
 // budget of 2048 tokens, so a block is 4 consecutive keys).
 //
-// One CTA of 256 threads per query row r at position p = q_base + r. The row's candidates
+// One CTA of 128 threads per query row r at position p = q_base + r. The row's candidates
 // are the blocks b = 0 .. nc-1 holding a key j <= p, nc = min(ceil(T / 4), p / 4 + 1); it
 // keeps the top_k highest scores, a tie going to the lower block index. Thread t holds
-// blocks t + 256 i (i < 8) as order-preserving unsigned keys. A radix select (four passes of
-// 8 bits over a shared 256-bin histogram; lanes with the same digit add once, through
-// __match_any_sync) gives the top_k-th largest key tau and the number `need` of keys equal
-// to tau that are kept: those with the lowest block indices, ranked by a block-wide count
-// in index order. The row's T mask bytes (1 = visible) then go out as 16-byte stores.
+// blocks t + 128 i (i < 16) as order-preserving unsigned keys, and 0 for b >= nc: below
+// every score's key, so padding never outranks a candidate, and any padding block that
+// does get marked is hidden by causality (its keys lie after p).
+//
+// A radix select over four 8-bit digits finds the top_k-th largest key tau. Each warp
+// counts its keys that match the prefix so far into a histogram of its own (shared-memory
+// atomics; no same-address contention between warps), and warp 0 sums the four and finds
+// the digit. When the digit's bin is taken whole the select stops early: the kept keys are
+// then those whose prefix is at least tau's, with no tie to break. Otherwise the `need`
+// keys equal to tau with the lowest block indices are kept, ranked by a block-wide count in
+// index order. Kept blocks become a bitmask (one ballot per 32 blocks), and the row's T
+// mask bytes (1 = visible) go out as 16-byte stores; only the store that straddles p
+// computes causality byte by byte.
 #include "ga_internal.h"
 
 namespace ga {
 namespace {
 
 constexpr int kBlockTokens = GA_INDEX_BLOCK_TOKENS;   // 4
-constexpr int kSelThreads = 256;
+constexpr int kSelThreads = 128;
 constexpr int kSelMaxBlocks = GA_MASKED_MAX_TOKENS / kBlockTokens;   // 2048
-constexpr int kSelKeys = kSelMaxBlocks / kSelThreads;            // 8 per thread
+constexpr int kSelKeys = kSelMaxBlocks / kSelThreads;                // 16 per thread
 constexpr int kSelWarps = kSelThreads / 32;
 static_assert(kSelKeys * kSelThreads == kSelMaxBlocks, "blocks per row");
-static_assert(kSelKeys * kSelWarps == 64, "the tie scan gives two entries to each lane");
+static_assert(kSelKeys * kSelWarps == kSelMaxBlocks / 32,
+              "one bitmask word and one tie count per (key slot, warp); two per lane");
 
 // IEEE order as unsigned order. -0 becomes +0 first, so the two tie as the values do.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -31,25 +40,24 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_mask_kernel(
+__global__ void __launch_bounds__(kSelThreads, 10) select_mask_kernel(
     const float* __restrict__ scores, long long ld_scores, int T, int q_base, int top_k,
     uint8_t* __restrict__ mask, long long ld_mask) {
-  __shared__ uint32_t sel_words[kSelMaxBlocks / 4];   // byte b: 1 if block b is kept
-  __shared__ int hist[256];
-  __shared__ int tie_base[kSelKeys * kSelWarps];      // entry i * 8 + warp
-  __shared__ int s_digit, s_need;
+  __shared__ uint32_t bits[kSelMaxBlocks / 32];   // bit b % 32 of word b / 32: block b kept
+  __shared__ int whist[kSelWarps][256];
+  __shared__ int tie_base[kSelKeys * kSelWarps];   // entry i * 4 + warp
+  __shared__ int s_digit, s_need, s_all;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = blockIdx.x;
   const int p = q_base + r;
   const int nb = (T + kBlockTokens - 1) / kBlockTokens;
   const int nc = min(nb, p / kBlockTokens + 1);
-  uint8_t* sel = reinterpret_cast<uint8_t*>(sel_words);
 
   if (top_k >= nc) {
     // every candidate is kept: the causal row
-#pragma unroll
-    for (int i = 0; i < kSelKeys; ++i) sel[tid + i * kSelThreads] = (tid + i * kSelThreads) < nc;
+    for (int w = tid; w < kSelMaxBlocks / 32; w += kSelThreads)
+      bits[w] = 32 * w + 32 <= nc ? 0xFFFFFFFFu : (32 * w >= nc ? 0u : (1u << (nc - 32 * w)) - 1u);
   } else {
     const float* row = scores + (long long)r * ld_scores;
     uint32_t key[kSelKeys];
@@ -60,27 +68,28 @@ __global__ void __launch_bounds__(kSelThreads) select_mask_kernel(
     }
     uint32_t prefix = 0, pmask = 0;
     int need = top_k;   // keys still to take among those that match the prefix
+    bool whole = false;
 #pragma unroll 1
     for (int shift = 24; shift >= 0; shift -= 8) {
-      hist[tid] = 0;
-      __syncthreads();
 #pragma unroll
-      for (int i = 0; i < kSelKeys; ++i) {
-        const int b = tid + i * kSelThreads;
-        const bool act = b < nc && (key[i] & pmask) == prefix;
-        const uint32_t d = act ? (key[i] >> shift) & 255u : 256u;
-        const unsigned same = __match_any_sync(0xFFFFFFFFu, d);
-        if (act && lane == __ffs(same) - 1) atomicAdd(&hist[d], __popc(same));
-      }
+      for (int j = 0; j < 8; ++j) whist[warp][lane + 32 * j] = 0;
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < kSelKeys; ++i)
+        if ((key[i] & pmask) == prefix) atomicAdd(&whist[warp][(key[i] >> shift) & 255u], 1);
       __syncthreads();
       if (warp == 0) {
-        // lane l holds bins 8l .. 8l+7; the digit is in the lane where the keys in higher
-        // bins are fewer than `need` and those in its bins and higher are at least `need`
+        // lane l sums bins 8l .. 8l+7 over the warps; the digit is in the lane where the
+        // keys in higher bins are fewer than `need` and those in its bins and higher are
+        // at least `need`
         int c[8], sum = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          c[j] = hist[8 * lane + j];
-          sum += c[j];
+          int t = 0;
+#pragma unroll
+          for (int w = 0; w < kSelWarps; ++w) t += whist[w][8 * lane + j];
+          c[j] = t;
+          sum += t;
         }
         int incl = sum;   // keys in the bins of lanes lane .. 31
 #pragma unroll
@@ -96,6 +105,7 @@ __global__ void __launch_bounds__(kSelThreads) select_mask_kernel(
             if (acc < need && acc + c[j] >= need) {
               s_digit = 8 * lane + j;
               s_need = need - acc;
+              s_all = (need - acc) == c[j];
             }
             acc += c[j];
           }
@@ -105,38 +115,49 @@ __global__ void __launch_bounds__(kSelThreads) select_mask_kernel(
       prefix |= (uint32_t)s_digit << shift;
       pmask |= 255u << shift;
       need = s_need;
-    }
-    // keys above tau are kept; of the keys equal to tau, the `need` lowest block indices.
-    // Index order is (i, warp, lane), so the rank of a tie is the ties in earlier
-    // (i, warp) groups plus those in lower lanes of its own warp.
-    unsigned tie[kSelKeys];
-#pragma unroll
-    for (int i = 0; i < kSelKeys; ++i) {
-      const int b = tid + i * kSelThreads;
-      tie[i] = __ballot_sync(0xFFFFFFFFu, b < nc && key[i] == prefix);
-      if (lane == 0) tie_base[i * kSelWarps + warp] = __popc(tie[i]);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int a0 = tie_base[2 * lane], a1 = tie_base[2 * lane + 1];
-      int incl = a0 + a1;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += v;
+      if (s_all) {   // the digit's bin is taken whole
+        whole = true;
+        break;
       }
-      const int excl = incl - a0 - a1;
-      tie_base[2 * lane] = excl;
-      tie_base[2 * lane + 1] = excl + a0;
     }
-    __syncthreads();
-    const unsigned lower = (1u << lane) - 1u;
+    if (whole) {
 #pragma unroll
-    for (int i = 0; i < kSelKeys; ++i) {
-      const int b = tid + i * kSelThreads;
-      const bool is_tie = (tie[i] >> lane) & 1u;
-      const int rank = tie_base[i * kSelWarps + warp] + __popc(tie[i] & lower);
-      sel[b] = (b < nc && key[i] > prefix) || (is_tie && rank < need);
+      for (int i = 0; i < kSelKeys; ++i) {
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, (key[i] & pmask) >= prefix);
+        if (lane == 0) bits[i * kSelWarps + warp] = m;
+      }
+    } else {
+      // keys above tau are kept; of the keys equal to tau, the `need` lowest block indices.
+      // Index order is (i, warp, lane), so the rank of a tie is the ties in earlier
+      // (i, warp) groups plus those in lower lanes of its own warp.
+      unsigned tie[kSelKeys];
+#pragma unroll
+      for (int i = 0; i < kSelKeys; ++i) {
+        tie[i] = __ballot_sync(0xFFFFFFFFu, key[i] == prefix);
+        if (lane == 0) tie_base[i * kSelWarps + warp] = __popc(tie[i]);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const int a0 = tie_base[2 * lane], a1 = tie_base[2 * lane + 1];
+        int incl = a0 + a1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        const int excl = incl - a0 - a1;
+        tie_base[2 * lane] = excl;
+        tie_base[2 * lane + 1] = excl + a0;
+      }
+      __syncthreads();
+      const unsigned lower = (1u << lane) - 1u;
+#pragma unroll
+      for (int i = 0; i < kSelKeys; ++i) {
+        const bool is_tie = (tie[i] >> lane) & 1u;
+        const int rank = tie_base[i * kSelWarps + warp] + __popc(tie[i] & lower);
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, key[i] > prefix || (is_tie && rank < need));
+        if (lane == 0) bits[i * kSelWarps + warp] = m;
+      }
     }
   }
   __syncthreads();
@@ -145,19 +166,21 @@ __global__ void __launch_bounds__(kSelThreads) select_mask_kernel(
   uint8_t* out = mask + (long long)r * ld_mask;
   const int nvec = T / 16;
   for (int v = tid; v < nvec; v += kSelThreads) {
-    const uint32_t w = sel_words[v];   // blocks 4v .. 4v+3
+    const uint32_t nib = (bits[v >> 3] >> (4 * (v & 7))) & 0xFu;   // blocks 4v .. 4v+3
     uint32_t word[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int vis = p - (16 * v + 4 * q) + 1;   // keys of the block at or before p
-      const uint32_t causal =
-          vis >= 4 ? 0xFFFFFFFFu : (vis <= 0 ? 0u : (1u << (8 * vis)) - 1u);
-      word[q] = ((w >> (8 * q)) & 1u) * 0x01010101u & causal;
+    for (int q = 0; q < 4; ++q) word[q] = ((nib >> q) & 1u) * 0x01010101u;
+    if (16 * v + 15 > p) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int vis = p - (16 * v + 4 * q) + 1;   // keys of block 4v + q at or before p
+        word[q] &= vis >= 4 ? 0xFFFFFFFFu : (vis <= 0 ? 0u : (1u << (8 * vis)) - 1u);
+      }
     }
     *reinterpret_cast<uint4*>(out + 16 * v) = make_uint4(word[0], word[1], word[2], word[3]);
   }
   for (int j = nvec * 16 + tid; j < T; j += kSelThreads)
-    out[j] = (j <= p && sel[j / kBlockTokens]) ? 1 : 0;
+    out[j] = (j <= p && ((bits[j >> 7] >> ((j >> 2) & 31)) & 1u)) ? 1 : 0;
 }
 
 }  // namespace
