@@ -426,6 +426,9 @@ def run_verify(args, world, rank, local):
 
 
 SEL_T, SEL_BUDGET, SEL_SETS = 8192, 2048, 4
+# dram__bytes_read.sum + dram__bytes_write.sum of one select_mask_kernel launch at this
+# size (ncu); L2 still holds most of the mask's writes when the launch ends
+SELECT_TRAFFIC_BYTES = 44_877_568
 
 
 def select_bytes(T=SEL_T, budget=SEL_BUDGET):
@@ -498,7 +501,7 @@ def run_select(args, world, rank, local):
                    "l2": f"{SEL_SETS} input sets of 128 MiB in rotation"},
         "rows_per_s": round(world * SEL_T / (ms * 1e-3), 1),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
-                     "frac": round(gbs / peak_hbm, 4), "traffic": None,
+                     "frac": round(gbs / peak_hbm, 4), "traffic": SELECT_TRAFFIC_BYTES,
                      "peak_kind": f"HBM copy ({peak_src})", "kernel": "select_mask_kernel",
                      "algorithmic_bytes": n_bytes},
         "gpu_launches": args.steps, "clocks": clk, "device_status": B.ga_device_status(),
