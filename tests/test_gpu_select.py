@@ -103,3 +103,38 @@ def test_selected_mask_feeds_masked_attention():
     kp = O.prep_keys(np64(kr), np64(w_k), oc, os_)
     AttnRef(np64(qg), kp, np64(v), np64(w_q), oc, os_, 0, S, "mask", mask=want_mask,
             heads=[0, 13, 23]).check(out, what="selected mask through ga_attn_masked")
+
+
+def test_select_windows_equal_full_pass_rows():
+    """Windows at several q_base (rows of the same score array) give the full pass's rows
+    byte for byte, and the full pass equals the oracle."""
+    T, k = 4096, 256
+    scores = synth.block_scores(SEED + 94, T, T // 4).cuda()
+    full = B.ga_select_mask(scores, T, k)
+    for q_base, rows in ((0, 128), (1000, 77), (4095, 1)):
+        win = B.ga_select_mask(scores[q_base:q_base + rows], T, k, q_base=q_base)
+        assert torch.equal(win, full[q_base:q_base + rows]), q_base
+    want = O.select_blocks_mask(scores.cpu().double().numpy(), 0, T, k)
+    assert np.array_equal(full.cpu().numpy()[:, :T], want)
+
+
+def test_select_nan_row_stays_in_its_row():
+    """NaN scores are outside the contract: the call still completes, writes only the NaN
+    rows' own mask bytes (inside causality), and every other row equals the oracle's."""
+    T, k = 2048, 64
+    scores = synth.block_scores(SEED + 95, T, T // 4)
+    bad = [100, 1500, 2047]
+    for r in bad:
+        scores[r, ::3] = float("nan")
+    mask = torch.full((T, T + 16), 7, dtype=torch.uint8, device="cuda")
+    B.ga_select_mask(scores.cuda(), T, k, mask=mask)
+    torch.cuda.synchronize()
+    got = mask.cpu().numpy()
+    assert np.all(got[:, T:] == 7)
+    ok = [r for r in range(T) if r not in bad]
+    clean = scores.clone()
+    clean[bad] = 0.0
+    want = O.select_blocks_mask(clean.double().numpy(), 0, T, k)
+    assert np.array_equal(got[ok, :T], want[ok])
+    causal = np.arange(T)[None, :] <= np.array(bad)[:, None]
+    assert np.all(got[bad, :T] <= causal)

@@ -666,3 +666,15 @@ def test_planted_reversed_tie_rule_is_caught():
     planted = np.isin(np.arange(T) // 4, order_hi)
     assert not np.array_equal(m[0] != 0, planted)
     assert np.array_equal(m[0] != 0, np.arange(T) < 4 * k)
+
+
+def test_select_window_rows_equal_full_pass():
+    """A row's selection depends only on its own scores and position: the rows of a window
+    at q_base equal the same positions' rows of the full pass."""
+    rng = np.random.default_rng(83)
+    T, k = 700, 20
+    s = rng.standard_normal((T, -(-T // 4)))
+    full = O.select_blocks_mask(s, 0, T, k)
+    for q_base, rows in ((0, 1), (64, 100), (333, 367), (699, 1)):
+        win = O.select_blocks_mask(s[q_base:q_base + rows], q_base, T, k)
+        assert np.array_equal(win, full[q_base:q_base + rows]), q_base
