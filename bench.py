@@ -428,7 +428,7 @@ def run_verify(args, world, rank, local):
 SEL_T, SEL_BUDGET, SEL_SETS = 8192, 2048, 4
 # dram__bytes_read.sum + dram__bytes_write.sum of one select_mask_kernel launch at this
 # size (ncu); L2 still holds most of the mask's writes when the launch ends
-SELECT_TRAFFIC_BYTES = 44_877_568
+SELECT_TRAFFIC_BYTES = 48_163_840
 
 
 def select_bytes(T=SEL_T, budget=SEL_BUDGET):
