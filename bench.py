@@ -508,6 +508,75 @@ def run_select(args, world, rank, local):
     }
 
 
+def run_prefill_e4m3(args, world, rank, local):
+    """Causal prefill at S = 8192 over e4m3 caches (prepared keys and values as e4m3 rows
+    with an fp32 scale each, resident in HBM): the step is one ga_attn_prefill_e4m3 call,
+    which widens both caches into its workspace, prepares the queries and attends."""
+    from verify_gated_gqa_gb300 import binding as B
+    from verify_gated_gqa_gb300.build import build
+
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    qg, kraw, v, w_q, w_k = make_inputs(dev, SEED + rank)
+    c, s_ = B.ga_rope_table_host(S)
+    cos, sin = c.to(dev), s_.to(dev)
+    k_prep = B.ga_k_prologue(kraw, w_k, cos, sin)
+    kq, ksc = B.ga_kv_quantize_e4m3(k_prep)
+    vq, vsc = B.ga_kv_quantize_e4m3(v)
+    del k_prep, kraw, v
+    out = torch.empty(S, HEADS * DIM, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(B.ga_prefill_e4m3_workspace_bytes(S), dtype=torch.uint8, device=dev)
+
+    def step():
+        B.ga_attn_prefill_e4m3(qg, kq, ksc, vq, vsc, w_q, cos, sin, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / args.steps
+    if rank != 0:
+        return None
+    peak_tf, _, peak_src = measured_peaks()
+    tf = FLOPS_STEP / (ms * 1e-3) / 1e12
+    return {
+        "metric": "causal prefill over e4m3 K/V caches: TFLOP/s at S=8192",
+        "value": round(world * tf, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.1) norm weights)",
+        "config": {"workload": "causal gated GQA prefill, S=8192, over e4m3 caches of the "
+                               "prepared keys and the values (fp32 scale per row); the call "
+                               "widens them once into its workspace, then attends",
+                   "l2": "inputs larger than L2 (qg 192 MiB read + out 96 MiB written per step)"},
+        "tokens_per_s": round(world * S / (ms * 1e-3), 1),
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(tf / peak_tf, 4), "traffic": None,
+                     "peak_kind": f"dense bf16 burst ({peak_src})",
+                     "kernel": "ga_attn_prefill_e4m3 (2 widening launches + Q prologue + "
+                               "attn_kernel), the whole call",
+                     "algorithmic_flops": FLOPS_STEP},
+        "gpu_launches": 4 * args.steps, "clocks": clk, "device_status": B.ga_device_status(),
+    }
+
+
 B_LENS = [512 * (1 + b % 8) for b in range(16)]   # 16 prompts of 512 .. 4096 tokens
 B_PAGE = 256
 
@@ -734,12 +803,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", default="prefill",
                     choices=["prefill", "verify", "verify_paged", "verify_e4m3", "batch",
-                             "select"],
+                             "select", "prefill_e4m3"],
                     help="prefill: the headline S=8192 causal step; verify: 8 x 16 rows over "
                          "65,536 cached keys; verify_paged: the same over paged caches; "
                          "verify_e4m3: the same over e4m3 caches; batch: 16 prompts of "
                          "512..4096 tokens in one batched call; select: the selection-mask "
-                         "producer at 8192 x 8192, block_topk 512")
+                         "producer at 8192 x 8192, block_topk 512; prefill_e4m3: the "
+                         "headline causal step over e4m3 caches")
     ap.add_argument("--verify-seqs", type=int, default=8)
     args = ap.parse_args()
     world, rank, local = dist_env()
@@ -751,6 +821,8 @@ def main():
         line = run_batch(args, world, rank, local)
     elif args.workload == "select":
         line = run_select(args, world, rank, local)
+    elif args.workload == "prefill_e4m3":
+        line = run_prefill_e4m3(args, world, rank, local)
     else:
         line = run_gpu(args, world, rank, local)
     if line is not None:

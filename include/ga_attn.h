@@ -233,6 +233,38 @@ int ga_attn_masked_static(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf1
                           long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
                           ga_stream stream);
 
+/* The widened rows of e4m3 cache rows: out = bf16(fp32(code * scale)) per element, the
+ * values ga_attn_verify_e4m3 attends over (TensorFold PR #1080: e4m3 cache rows with an
+ * fp32 scale each, widened to bf16).
+ *   q      [n_tok][2][256] uint8 e4m3 codes, as ga_kv_quantize_e4m3 writes them, 8-byte aligned
+ *   scale  [n_tok][2] fp32, 4-byte aligned
+ *   out    [n_tok][2][256] bf16, 16-byte aligned
+ * Rules: 0 <= n_tok <= 64 * GA_MAX_TOKENS; n_tok == 0 is a no-op.
+ * Errors: NULL, SHAPE, RANGE, ALIGN, DEVICE, CUDA. */
+int ga_kv_dequantize_e4m3(const uint8_t* q, const float* scale, long long n_tok, ga_bf16* out,
+                          ga_stream stream);
+
+/* Bytes of workspace ga_attn_prefill_e4m3 needs for T keys (the widened K and V); 0 for
+ * T outside 1 .. GA_MAX_TOKENS. */
+size_t ga_prefill_e4m3_workspace_bytes(int T);
+
+/* ga_attn_prefill over e4m3 caches of prepared keys and values (TensorFold PR #1080: e4m3
+ * cache rows with an fp32 scale each, read by the prompt chain). Prefill reads every key
+ * tile once per 128-row tile of queries, so the rows are widened once, into the workspace,
+ * by ga_kv_dequantize_e4m3's kernel, and the bf16 pass then runs over them: the results
+ * are the bits of ga_attn_prefill over the widened rows.
+ *   k_codes, v_codes [T][2][256] uint8, 16-byte aligned; k_scale, v_scale [T][2] fp32
+ *   qg, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base, causal, out, row_stats: as in
+ *           ga_attn_prefill
+ *   workspace >= ga_prefill_e4m3_workspace_bytes(T) bytes, 256-byte aligned, owned by the
+ *           caller and not shared with a concurrent call; it holds the widened K then V
+ * Errors: NULL, SHAPE, RANGE, TABLE, ALIGN, WORKSPACE, DEVICE, CUDA. */
+int ga_attn_prefill_e4m3(const ga_bf16* qg, const uint8_t* k_codes, const float* k_scale,
+                         const uint8_t* v_codes, const float* v_scale, const ga_bf16* w_q,
+                         const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
+                         int rows, int T, int q_base, int causal, ga_bf16* out,
+                         float* row_stats, void* workspace, size_t ws_bytes, ga_stream stream);
+
 /* The selection mask ga_attn_masked reads, from the indexer's per-block scores (pegainfer
  * PR #1151, "feat(qwen4): add the QSA sparse-attention kernel and its golden": the mask is
  * the indexer's selection AND causality; a budget of 2048 tokens keeps 512 blocks of 4 keys,

@@ -249,6 +249,45 @@ def test_select_mask_refusals_make_no_cuda_call(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def test_dequantize_and_prefill_e4m3_refusals_make_no_cuda_call(L):
+    before = L.ga_debug_cuda_calls()
+    f = L.ga_kv_dequantize_e4m3
+    assert f(None, A, 10, A, S) == -1
+    assert f(A, None, 10, A, S) == -1
+    assert f(A, A, 10, None, S) == -1
+    assert f(A, A, -1, A, S) == -2
+    assert f(A, A, (1 << 26) + 1, A, S) == -4
+    assert f(A + 4, A, 10, A, S) == -3
+    assert f(A, A + 2, 10, A, S) == -3
+    assert f(A, A, 10, A + 8, S) == -3
+    assert f(A, A, 0, A, S) == 0                       # no rows: a no-op
+    assert L.ga_prefill_e4m3_workspace_bytes(0) == 0
+    assert L.ga_prefill_e4m3_workspace_bytes(1000) == 2 * 1000 * 2 * 256 * 2
+    ws = L.ga_prefill_e4m3_workspace_bytes(512)
+    g = L.ga_attn_prefill_e4m3
+    ok = (A, A, A, A, A, A, A, A, 512, 128, 512, 0, 1, A, None, A, ws, S)
+    def call(**kw):
+        names = ["qg", "kc", "ks", "vc", "vs", "wq", "cos", "sin", "tr", "rows", "T", "qb",
+                 "causal", "out", "rs", "ws", "wsb", "s"]
+        args = dict(zip(names, ok))
+        args.update(kw)
+        return g(*[args[n] for n in names])
+    assert call(kc=None) == -1
+    assert call(vs=None) == -1
+    assert call(rows=-1) == -2
+    assert call(qb=32) == -4                           # q_base not a multiple of 64
+    assert call(causal=2) == -4
+    assert call(qb=64, rows=64, causal=0) == -4        # bidirectional starts at 0
+    assert call(tr=100) == -5
+    assert call(kc=A + 8) == -3                        # codes 16-byte aligned
+    assert call(ks=A + 2) == -3
+    assert call(ws=None) == -6
+    assert call(ws=A + 16) == -6
+    assert call(wsb=ws - 1) == -6
+    assert call(rows=0) == 0                           # no rows: a no-op
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_k_prologue_refusals(L):
     before = L.ga_debug_cuda_calls()
     assert L.ga_k_prologue(None, A, A, A, 100, 10, 0, A, S) == -1

@@ -57,6 +57,10 @@ _SIGS = {
     "ga_attn_verify_e4m3": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P, _SZ,
                                  _P]),
     "ga_select_mask": (_I, [_P, _LL, _I, _I, _I, _I, _P, _LL, _P]),
+    "ga_kv_dequantize_e4m3": (_I, [_P, _P, _LL, _P, _P]),
+    "ga_prefill_e4m3_workspace_bytes": (_SZ, [_I]),
+    "ga_attn_prefill_e4m3": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P,
+                                  _SZ, _P]),
 }
 
 
@@ -381,6 +385,56 @@ def ga_kv_quantize_e4m3(x, q=None, scale=None):
     _check(lib().ga_kv_quantize_e4m3(_ptr(x), n_tok, _ptr(q), _ptr(scale), _stream()),
            "ga_kv_quantize_e4m3")
     return q, scale
+
+
+def ga_kv_dequantize_e4m3(q, scale, out=None):
+    """q uint8 [..., 2, 256] e4m3 codes, scale fp32 [..., 2] -> the widened rows, bf16 shaped
+    like q: bf16(fp32(code * scale))."""
+    if q.dtype != torch.uint8 or not q.is_cuda or not q.is_contiguous() or q.shape[-2:] != (
+            N_KV_HEADS, HEAD_DIM):
+        raise ValueError("q must be a contiguous uint8 CUDA tensor ending in [2, 256]")
+    if (scale.dtype != torch.float32 or not scale.is_contiguous() or
+            scale.shape != q.shape[:-1]):
+        raise ValueError("scale must be a contiguous float32 tensor shaped like q[..., 0]")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    _bf16_cuda("out", out, q.shape)
+    n_tok = q.numel() // (N_KV_HEADS * HEAD_DIM)
+    _check(lib().ga_kv_dequantize_e4m3(_ptr(q), _ptr(scale), n_tok, _ptr(out), _stream()),
+           "ga_kv_dequantize_e4m3")
+    return out
+
+
+def ga_prefill_e4m3_workspace_bytes(T: int) -> int:
+    return lib().ga_prefill_e4m3_workspace_bytes(T)
+
+
+def ga_attn_prefill_e4m3(qg, k_codes, k_scale, v_codes, v_scale, w_q, cos_tab, sin_tab,
+                         q_base=0, T=None, causal=True, out=None, row_stats=None,
+                         workspace=None):
+    """ga_attn_prefill over e4m3 caches: k_codes, v_codes uint8 [T, 2, 256], k_scale,
+    v_scale fp32 [T, 2] (as ga_kv_quantize_e4m3 writes them)."""
+    rows = qg.shape[0]
+    T = k_codes.shape[0] if T is None else T
+    for n, t, dt in (("k_codes", k_codes, torch.uint8), ("v_codes", v_codes, torch.uint8),
+                     ("k_scale", k_scale, torch.float32), ("v_scale", v_scale, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous() or t.shape[0] < T:
+            raise ValueError(f"{n} must be a contiguous {dt} CUDA tensor with >= T rows")
+    if out is None:
+        out = torch.empty(rows, N_Q_HEADS * HEAD_DIM, dtype=torch.bfloat16, device=qg.device)
+    if workspace is None:
+        workspace = torch.empty(max(ga_prefill_e4m3_workspace_bytes(T), 1), dtype=torch.uint8,
+                                device=qg.device)
+    for n, t in (("qg", qg), ("w_q", w_q), ("cos_tab", cos_tab), ("sin_tab", sin_tab),
+                 ("out", out)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_attn_prefill_e4m3(_ptr(qg), _ptr(k_codes), _ptr(k_scale), _ptr(v_codes),
+                                      _ptr(v_scale), _ptr(w_q), _ptr(cos_tab), _ptr(sin_tab),
+                                      cos_tab.shape[0], rows, T, q_base, 1 if causal else 0,
+                                      _ptr(out), _ptr(row_stats), _ptr(workspace),
+                                      workspace.numel(), _stream()),
+           "ga_attn_prefill_e4m3")
+    return out
 
 
 def ga_attn_verify_e4m3(qg, k_codes, k_scale, v_codes, v_scale, seq_len, w_q, cos_tab, sin_tab,

@@ -909,13 +909,6 @@ __device__ bool epilogue_partial(AttnSmem& sm, const AttnArgs& a, const Item& it
   return true;
 }
 
-// Two e4m3 codes (low byte first) as floats; every e4m3 value is exact in f16 and f32.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
-  const __half2_raw hr =
-      __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
-  return __half22float2(__half2(hr));
-}
-
 // e4m3 caches: the raw tile (128 keys x 256 codes, one 256-byte row per key) in the back half
 // of the fill's slot becomes the bf16 tile the tensor cores read, bf16(fp32(code * scale))
 // per element, in place. Edge thread t widens the 16 codes of column t % 16 in rows t / 16 +

@@ -865,6 +865,67 @@ int ga_kv_quantize_e4m3(const ga_bf16* x, long long n_tok, uint8_t* q, float* sc
   return GA_OK;
 }
 
+int ga_kv_dequantize_e4m3(const uint8_t* q, const float* scale, long long n_tok, ga_bf16* out,
+                          ga_stream stream) {
+  if (!q || !scale || !out) return GA_ERR_NULL;
+  if (n_tok < 0) return GA_ERR_SHAPE;
+  if (n_tok > (long long)GA_MAX_TOKENS * 64) return GA_ERR_RANGE;
+  if (!aligned(q, 8) || !aligned(scale, 4) || !aligned(out, 16)) return GA_ERR_ALIGN;
+  if (n_tok == 0) return GA_OK;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaError_t e = GA_CUDA(launch_dequantize_e4m3(q, scale, n_tok * kKvHeads,
+                                                 reinterpret_cast<uint16_t*>(out),
+                                                 (cudaStream_t)stream));
+  if (e != cudaSuccess) return fail_cuda(e);
+  return GA_OK;
+}
+
+size_t ga_prefill_e4m3_workspace_bytes(int T) {
+  if (T < 1 || T > GA_MAX_TOKENS) return 0;
+  return 2 * (size_t)T * kKvHeads * kDim * sizeof(uint16_t);
+}
+
+int ga_attn_prefill_e4m3(const ga_bf16* qg, const uint8_t* k_codes, const float* k_scale,
+                         const uint8_t* v_codes, const float* v_scale, const ga_bf16* w_q,
+                         const ga_bf16* cos_tab, const ga_bf16* sin_tab, int table_rows,
+                         int rows, int T, int q_base, int causal, ga_bf16* out,
+                         float* row_stats, void* workspace, size_t ws_bytes, ga_stream stream) {
+  // the code arrays stand in for the bf16 caches in the shared checks (16-byte aligned)
+  int st = check_attention_args(qg, k_codes, v_codes, w_q, cos_tab, sin_tab, table_rows, rows,
+                                T, q_base, out);
+  if (st != GA_OK) return st;
+  if (!k_scale || !v_scale) return GA_ERR_NULL;
+  if (causal != 0 && causal != 1) return GA_ERR_RANGE;
+  if (!causal && q_base != 0) return GA_ERR_RANGE;   // bidirectional passes start at 0
+  if (!aligned(k_scale, 4) || !aligned(v_scale, 4) || (row_stats && !aligned(row_stats, 4)))
+    return GA_ERR_ALIGN;
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < ga_prefill_e4m3_workspace_bytes(T))
+    return GA_ERR_WORKSPACE;
+  if (rows == 0) return GA_OK;
+  // the widened K and V live in the workspace: [T][2][256] bf16 each
+  ga_bf16* k_wide = static_cast<ga_bf16*>(workspace);
+  ga_bf16* v_wide = k_wide + (size_t)T * kKvHeads * kDim;
+  DeviceState* dev = nullptr;
+  st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  if ((e = GA_CUDA(launch_dequantize_e4m3(k_codes, k_scale, (long long)T * kKvHeads,
+                                          reinterpret_cast<uint16_t*>(k_wide), s))) != cudaSuccess)
+    return fail_cuda(e);
+  if ((e = GA_CUDA(launch_dequantize_e4m3(v_codes, v_scale, (long long)T * kKvHeads,
+                                          reinterpret_cast<uint16_t*>(v_wide), s))) != cudaSuccess)
+    return fail_cuda(e);
+  AttnArgs a{};
+  a.qg = qg; a.w_q = w_q; a.cos_tab = cos_tab; a.sin_tab = sin_tab;
+  a.out = out; a.row_stats = row_stats;
+  a.rows = rows; a.T = T; a.q_base = q_base;
+  a.mode = causal ? kModeCausal : kModeBidir;
+  return launch_attention(a, out, false, k_wide, v_wide, T, dev, s);
+}
+
 int ga_select_mask(const float* block_scores, long long ld_scores, int rows, int T, int q_base,
                    int block_topk, uint8_t* mask, long long ld_mask, ga_stream stream) {
   if (!block_scores || !mask) return GA_ERR_NULL;

@@ -111,6 +111,9 @@ cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uin
 // e4m3 cache rows: q[row][0..255] and scale[row] for n_rows rows of 256 bf16 values.
 cudaError_t launch_quantize_e4m3(const uint16_t* x, long long n_rows, uint8_t* q, float* scale,
                                  cudaStream_t s);
+// The widened bf16 rows out[row][0..255] of n_rows e4m3 rows and their scales.
+cudaError_t launch_dequantize_e4m3(const uint8_t* q, const float* scale, long long n_rows,
+                                   uint16_t* out, cudaStream_t s);
 // Selection mask: mask[r][0..T-1] for rows r < rows from block_scores[r][0..ceil(T/4)-1].
 cudaError_t launch_select_mask(const float* scores, long long ld_scores, int rows, int T,
                                int q_base, int top_k, uint8_t* mask, long long ld_mask,

@@ -11,6 +11,8 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 namespace ga {
 
@@ -109,6 +111,13 @@ __device__ __forceinline__ float norm_elem(float x, float w, InvRms r) {
   const float y = norm_fast(x, w, r);
   if (!near_bf16_midpoint(y, 3)) return bf16_round(y);
   return norm_elem_exact(x, w, r.h, r.l);
+}
+
+// Two e4m3 codes (low byte first) as floats; every e4m3 value is exact in f16 and f32.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+  const __half2_raw hr =
+      __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
+  return __half22float2(__half2(hr));
 }
 
 // Rotate-half RoPE of one pair with bf16 rounding after each product and after the sum;

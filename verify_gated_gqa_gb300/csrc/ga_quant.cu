@@ -7,9 +7,13 @@
 //
 // Eight lanes per row, four rows per warp; lane j holds dims 32k + 4j .. +3 (k = 0..7), as in
 // the prologue, so the row maximum reduces over the row's 8 lanes in three shuffle steps.
+// The inverse, widening rows back to bf16(fp32(code * scale)), serves prefill over e4m3
+// caches: prefill reads every key tile once per row tile, so its rows are widened once in
+// HBM rather than at every visit.
 #include <cuda_fp8.h>
 
 #include "ga_internal.h"
+#include "ga_numerics.cuh"
 #include "ga_sm100.cuh"
 
 namespace ga {
@@ -58,7 +62,34 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(const uint16_t* __re
   if (j == 0) scale[row] = sc;
 }
 
+// The widened rows: bf16(fp32(code * scale)) per element, the value the attention reads
+// from an e4m3 cache row. One thread per 8 codes (an 8-byte load, a 16-byte store); the 32
+// threads of a row share its scale.
+__global__ void __launch_bounds__(256) dequantize_e4m3_kernel(const uint8_t* __restrict__ q,
+                                                              const float* __restrict__ scale,
+                                                              long long n_rows,
+                                                              uint16_t* __restrict__ out) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_rows * (kDim / 8)) return;
+  const float sc = __ldg(scale + i / (kDim / 8));
+  const uint2 c = __ldg(reinterpret_cast<const uint2*>(q) + i);
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = e4m3x2_to_float2((k < 2 ? c.x : c.y) >> (16 * (k & 1)));
+    w[k] = pack_bf16x2(f.x * sc, f.y * sc);
+  }
+  reinterpret_cast<uint4*>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 }  // namespace
+
+cudaError_t launch_dequantize_e4m3(const uint8_t* q, const float* scale, long long n_rows,
+                                   uint16_t* out, cudaStream_t s) {
+  const long long n = n_rows * (kDim / 8);
+  dequantize_e4m3_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(q, scale, n_rows, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_e4m3(const uint16_t* x, long long n_rows, uint8_t* q, float* scale,
                                  cudaStream_t s) {
