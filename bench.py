@@ -508,6 +508,91 @@ def run_select(args, world, rank, local):
     }
 
 
+SMALL_CASES = [("S=64 causal", 64, True), ("S=2048 causal", 2048, True),
+               ("S=2048 bidirectional", 2048, False)]
+
+
+def run_small(args, world, rank, local):
+    """The small prefill configurations: S = 64 causal (latency), S = 2048 causal and S = 2048
+    bidirectional, each step ga_k_prologue + ga_attn_prefill (query prologue and attention)
+    as in the headline step. Their inputs fit in L2, so every timed call follows a 256 MiB
+    write that flushes it, and CUDA events bracket the call alone. The line's value is the
+    S = 2048 causal TFLOP/s; `cases` holds all three."""
+    import statistics
+
+    from verify_gated_gqa_gb300 import binding as B
+    from verify_gated_gqa_gb300 import synth
+    from verify_gated_gqa_gb300.build import build
+
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    cases = {}
+    for name, n, causal in SMALL_CASES:
+        qg, kraw, v, w_q, w_k = synth.attention_inputs(SEED + rank + n, n, n, device=dev)
+        c, s_ = B.ga_rope_table_host(n)
+        cos, sin = c.to(dev), s_.to(dev)
+        k_prep = torch.empty_like(kraw)
+        out = torch.empty(n, HEADS * DIM, dtype=torch.bfloat16, device=dev)
+
+        def step():
+            B.ga_k_prologue(kraw, w_k, cos, sin, k_prep=k_prep)
+            B.ga_attn_prefill(qg, k_prep, v, w_q, cos, sin, 0, n, causal=causal, out=out)
+
+        for _ in range(args.warmup):
+            step()
+        barrier(world)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        barrier(world)
+        ms = max_over_ranks(statistics.median(ts), world, dev)
+        pairs = visible_pairs_causal(n, n) if causal else n * n
+        flops = attention_flops(pairs)
+        cases[name] = {"us_per_call": round(ms * 1e3, 2),
+                       "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+                       "algorithmic_gflop": round(flops / 1e9, 3)}
+    clk = clocks.stop() if clocks else None
+    if rank != 0:
+        return None
+    peak_tf, _, peak_src = measured_peaks()
+    head = cases["S=2048 causal"]
+    return {
+        "metric": "causal prefill TFLOP/s at S=2048 (S=64 latency and S=2048 bidirectional in cases)",
+        "value": round(world * head["tflops"], 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(head["us_per_call"] / 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.1) norm weights)",
+        "config": {"workload": "small prefill configurations: S=64 causal, S=2048 causal, S=2048 "
+                               "bidirectional; step = ga_k_prologue + ga_attn_prefill",
+                   "l2": "flushed before every timed call (256 MiB write); median of the steps"},
+        "cases": cases,
+        "roofline": {"bound": "tensor", "achieved": head["tflops"], "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(head["tflops"] / peak_tf, 4),
+                     "traffic": None, "peak_kind": f"dense bf16 burst ({peak_src})",
+                     "kernel": "the S=2048 causal step (K prologue + Q prologue + attention)",
+                     "algorithmic_flops": attention_flops(visible_pairs_causal(2048, 2048))},
+        "gpu_launches": 3 * args.steps * len(SMALL_CASES), "clocks": clk,
+        "device_status": B.ga_device_status(),
+    }
+
+
 def run_prefill_e4m3(args, world, rank, local):
     """Causal prefill at S = 8192 over e4m3 caches (prepared keys and values as e4m3 rows
     with an fp32 scale each, resident in HBM): the step is one ga_attn_prefill_e4m3 call,
@@ -803,13 +888,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", default="prefill",
                     choices=["prefill", "verify", "verify_paged", "verify_e4m3", "batch",
-                             "select", "prefill_e4m3"],
+                             "select", "prefill_e4m3", "small"],
                     help="prefill: the headline S=8192 causal step; verify: 8 x 16 rows over "
                          "65,536 cached keys; verify_paged: the same over paged caches; "
                          "verify_e4m3: the same over e4m3 caches; batch: 16 prompts of "
                          "512..4096 tokens in one batched call; select: the selection-mask "
                          "producer at 8192 x 8192, block_topk 512; prefill_e4m3: the "
-                         "headline causal step over e4m3 caches")
+                         "headline causal step over e4m3 caches; small: S=64 and S=2048 "
+                         "(causal and bidirectional) with L2 flushed before each call")
     ap.add_argument("--verify-seqs", type=int, default=8)
     args = ap.parse_args()
     world, rank, local = dist_env()
@@ -823,6 +909,8 @@ def main():
         line = run_select(args, world, rank, local)
     elif args.workload == "prefill_e4m3":
         line = run_prefill_e4m3(args, world, rank, local)
+    elif args.workload == "small":
+        line = run_small(args, world, rank, local)
     else:
         line = run_gpu(args, world, rank, local)
     if line is not None:
