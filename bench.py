@@ -560,12 +560,32 @@ def run_small(args, world, rank, local):
             e1.record(stream)
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1))
+        # the same step captured once in a CUDA graph and replayed: the device's own time
+        # without the host's per-call work
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(args.warmup):
+            graph.replay()
+        tg = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            tg.append(e0.elapsed_time(e1))
         barrier(world)
         ms = max_over_ranks(statistics.median(ts), world, dev)
+        ms_g = max_over_ranks(statistics.median(tg), world, dev)
         pairs = visible_pairs_causal(n, n) if causal else n * n
         flops = attention_flops(pairs)
         cases[name] = {"us_per_call": round(ms * 1e3, 2),
                        "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+                       "us_per_graph_replay": round(ms_g * 1e3, 2),
+                       "tflops_graph": round(flops / (ms_g * 1e-3) / 1e12, 2),
                        "algorithmic_gflop": round(flops / 1e9, 3)}
     clk = clocks.stop() if clocks else None
     if rank != 0:
@@ -588,7 +608,7 @@ def run_small(args, world, rank, local):
                      "traffic": None, "peak_kind": f"dense bf16 burst ({peak_src})",
                      "kernel": "the S=2048 causal step (K prologue + Q prologue + attention)",
                      "algorithmic_flops": attention_flops(visible_pairs_causal(2048, 2048))},
-        "gpu_launches": 3 * args.steps * len(SMALL_CASES), "clocks": clk,
+        "gpu_launches": 6 * args.steps * len(SMALL_CASES), "clocks": clk,
         "device_status": B.ga_device_status(),
     }
 
