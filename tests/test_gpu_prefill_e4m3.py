@@ -88,3 +88,15 @@ def test_prefill_e4m3_against_oracle():
     vc = O.dequantize_e4m3_rows(*O.quantize_e4m3_rows(np64(v)))
     AttnRef(np64(qg), kc, vc, np64(w_q), oc, os_, 0, S, "causal",
             heads=[0, 11, 12, 23]).check(got, what="e4m3 prefill S=1024")
+
+
+def test_prefill_e4m3_s8192_full_output():
+    """The benchmark's size, causal S = 8192: every output of the e4m3 call equals the bf16
+    prefill's over the rows widened on the host."""
+    S = 8192
+    qg, w_q, (c, s), (kq, ksc, vq, vsc), _ = _case(SEED + 87, S)
+    kw, vw = _host_widen(kq, ksc).cuda(), _host_widen(vq, vsc).cuda()
+    got = B.ga_attn_prefill_e4m3(qg, kq, ksc, vq, vsc, w_q, c, s)
+    want = B.ga_attn_prefill(qg, kw, vw, w_q, c, s, 0, S)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want), int((got != want).sum())
