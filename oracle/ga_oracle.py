@@ -252,8 +252,10 @@ def select_blocks_mask(block_scores, q_base, T, block_topk):
 # The attention core
 # ----------------------------------------------------------------------------------
 def sigmoid_gate(g, mode="R1"):
-    """sigmoid(g) = 1 / (1 + e^{-g}); rounded to bf16 except in F64 ([QSA] §Semantics)."""
-    s = 1.0 / (1.0 + np.exp(-np.asarray(g, dtype=np.float64)))
+    """sigmoid(g) = 1 / (1 + e^{-g}); rounded to bf16 except in F64 ([QSA] §Semantics).
+    For g below about -709, e^{-g} overflows to inf and the quotient is the exact limit 0."""
+    with np.errstate(over="ignore"):
+        s = 1.0 / (1.0 + np.exp(-np.asarray(g, dtype=np.float64)))
     return s if mode == "F64" else bf16(s)
 
 
