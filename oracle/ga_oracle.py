@@ -458,10 +458,3 @@ def verify_paged(qg_seq, k_pages, v_pages, page_table, page_size, seq_len, w_q, 
                             heads))
     return np.stack(outs)
 
-
-def row_stats(q_hat_h, k_hat_kv, vis):
-    """Diagnostics: per row the largest visible score s and the spread max-min (nats)."""
-    dot = bf16(q_hat_h @ k_hat_kv.T) / 16.0
-    mx = np.max(np.where(vis, dot, -np.inf), axis=1)
-    mn = np.min(np.where(vis, dot, np.inf), axis=1)
-    return mx, mx - mn

@@ -166,6 +166,39 @@ def test_rope_identity_norm_and_inverse():
     assert np.allclose(back, x, atol=1e-12)
 
 
+def test_rope_rounding_points_hand_worked():
+    """[QSA], the attention-reader commit: cos/sin are bf16 and the rotation rounds in
+    bf16, each product and then the sum. Hand-worked values where that differs from one
+    rounding of the exact a*c - b*s (and of b*c + a*s):
+
+    pair 0: a = 1 + 2^-6, b = -2^-9, c = 1 - 2^-8, s = 2^-4.
+      a*c = 1 + 3*2^-8 - 2^-14, just below the midpoint 1 + 3*2^-8 of 1 + 2^-7 and
+      1 + 2^-6, so bf16(a*c) = 1 + 2^-7; bf16(b*s) = -2^-13 (exact);
+      bf16(1 + 2^-7 + 2^-13) = 1 + 2^-7.  One rounding of the exact value
+      1 + 3*2^-8 + 2^-14 (above the midpoint) would give 1 + 2^-6.
+      y_32 = bf16(bf16(b*c) + bf16(a*s)) = bf16(-(2^-9 - 2^-17) + (2^-4 + 2^-10))
+           = 252 * 2^-12 (the step there is 2^-12).
+    pair 1 mirrors it in the second formula: a = 2^-9, b = 1 + 2^-6:
+      y_33 = bf16(bf16(b*c) + bf16(a*s)) = 1 + 2^-7 (one rounding: 1 + 2^-6),
+      y_1 = -252 * 2^-12."""
+    x = np.zeros(256)
+    cos_row, sin_row = np.ones(32), np.zeros(32)
+    x[0], x[32] = 1 + 2.0 ** -6, -(2.0 ** -9)
+    x[1], x[33] = 2.0 ** -9, 1 + 2.0 ** -6
+    cos_row[:2], sin_row[:2] = 1 - 2.0 ** -8, 2.0 ** -4
+    x[2:32] = x[34:64] = 0.5
+    x[100] = 3.0
+    y = O.rope_partial(x, cos_row, sin_row)
+    assert y[0] == 1 + 2.0 ** -7 and y[33] == 1 + 2.0 ** -7
+    assert y[32] == 252 * 2.0 ** -12 and y[1] == -252 * 2.0 ** -12
+    assert np.all(y[2:32] == 0.5) and np.all(y[34:64] == 0.5) and y[100] == 3.0
+    # the single-rounding reading of the same pair, worked with exact rationals: the
+    # values above are where the two readings part
+    from fractions import Fraction as F
+    exact = F(1) + F(1, 64) - F(1, 256) - F(1, 2 ** 14) + F(1, 2 ** 13)
+    assert exact > F(1) + F(3, 256) and O.bf16(float(exact)) == 1 + 2.0 ** -6
+
+
 # ---------------------------------------------------------------- brute force attention
 def _mp_attention(qg, k, v, w_q, w_k, q_base, T, kind, mask=None, heads=(0, 12)):
     """Textbook gated GQA attention at 200 bits, written directly from the pages'
@@ -559,6 +592,35 @@ def test_planted_interleaved_rope_is_caught(monkeypatch):
     monkeypatch.setattr(O, "rope_partial", interleaved)
     with pytest.raises(AssertionError):
         test_rope_pairing_closed_form()
+
+
+def test_planted_single_rounding_rope_is_caught(monkeypatch):
+    """Rotating with one rounding of the exact a*c - b*s (and b*c + a*s) instead of
+    rounding each product and then the sum must fail the hand-worked rounding pin."""
+    def fused(x, cos_rows, sin_rows, rounded=True):
+        x = np.asarray(x, dtype=np.float64)
+        a, b = x[..., :32], x[..., 32:64]
+        y = x.copy()
+        y[..., :32] = a * cos_rows - b * sin_rows
+        y[..., 32:64] = b * cos_rows + a * sin_rows
+        return O.bf16(y) if rounded else y
+    monkeypatch.setattr(O, "rope_partial", fused)
+    with pytest.raises(AssertionError):
+        test_rope_rounding_points_hand_worked()
+
+
+def test_planted_unrounded_products_rope_is_caught(monkeypatch):
+    """Rounding only the sum (products kept exact) must fail the same pin."""
+    def sum_only(x, cos_rows, sin_rows, rounded=True):
+        x = np.asarray(x, dtype=np.float64)
+        a, b = x[..., :32], x[..., 32:64]
+        y = x.copy()
+        y[..., :32] = O.bf16(a * cos_rows - O.bf16(b * sin_rows))
+        y[..., 32:64] = O.bf16(O.bf16(b * cos_rows) + a * sin_rows)
+        return y
+    monkeypatch.setattr(O, "rope_partial", sum_only)
+    with pytest.raises(AssertionError):
+        test_rope_rounding_points_hand_worked()
 
 
 def test_planted_causal_for_sparse_mask_is_caught(monkeypatch):
