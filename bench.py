@@ -227,50 +227,15 @@ def run_gpu(args, world, rank, local):
     # streams with double-buffered device inputs and outputs, as a serving loop would run
     # them: step i+1's inputs travel while step i computes and step i-1's output returns.
     host_in = [t.cpu().pin_memory() for t in (qg, k, v, w_q, w_k, cos, sin)]
-    dev_in = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(2)]
-    outs = [out, torch.empty_like(out)]
-    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+
+    def compute(d, o):
+        qg_d, k_d, v_d, wq_d, wk_d, cos_d, sin_d = d
+        B.ga_k_prologue(k_d, wk_d, cos_d, sin_d, k_prep=k_prep)
+        B.ga_attn_prefill(qg_d, k_prep, v_d, wq_d, cos_d, sin_d, 0, S, out=o)
+
     e2e_steps = max(3, min(args.steps, 20))
-    h_stream, c_stream, d_stream = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-
-    def e2e_run(n):
-        h_done = [torch.cuda.Event() for _ in range(n)]
-        c_done = [torch.cuda.Event() for _ in range(n)]
-        d_done = [torch.cuda.Event() for _ in range(n)]
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        h_stream.wait_event(start)
-        for i in range(n):
-            b = i % 2
-            with torch.cuda.stream(h_stream):
-                if i >= 2:
-                    h_stream.wait_event(c_done[i - 2])   # buffer b's inputs are consumed
-                for h, d in zip(host_in, dev_in[b]):
-                    d.copy_(h, non_blocking=True)
-                h_done[i].record(h_stream)
-            with torch.cuda.stream(c_stream):
-                c_stream.wait_event(h_done[i])
-                if i >= 2:
-                    c_stream.wait_event(d_done[i - 2])   # buffer b's output was read back
-                qg_d, k_d, v_d, wq_d, wk_d, cos_d, sin_d = dev_in[b]
-                B.ga_k_prologue(k_d, wk_d, cos_d, sin_d, k_prep=k_prep)
-                B.ga_attn_prefill(qg_d, k_prep, v_d, wq_d, cos_d, sin_d, 0, S, out=outs[b])
-                c_done[i].record(c_stream)
-            with torch.cuda.stream(d_stream):
-                d_stream.wait_event(c_done[i])
-                host_out[b].copy_(outs[b], non_blocking=True)
-                d_done[i].record(d_stream)
-        stream.wait_event(d_done[n - 1])
-        end.record(stream)
-        torch.cuda.synchronize()
-        return start.elapsed_time(end)
-
-    e2e_run(2)
-    barrier(world)
-    e2e_ms = max_over_ranks(e2e_run(e2e_steps), world, dev) / e2e_steps
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = host_out[0].numel() * host_out[0].element_size()
+    e2e_ms, h2d, d2h = e2e_pipelined(host_in, compute, out, e2e_steps, world, dev)
+    secondary = secondary_measurements(dev, rank, max(3, min(args.steps, 20)))
 
     if rank != 0:
         return None
@@ -308,10 +273,63 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "device_status": status,
+        "secondary": secondary,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
+
+
+def e2e_pipelined(host_in, compute, out, n, world, dev):
+    """End to end through the C ABI with host buffers: every step copies its inputs from
+    pinned host memory (H2D), runs `compute(device inputs, device output)` (the public
+    calls) and reads its output back into pinned host memory (D2H). Steps are pipelined on
+    three streams with double-buffered device inputs and outputs, as a serving loop would
+    run them: step i+1's inputs travel while step i computes and step i-1's output returns.
+    Returns (ms per step, max over ranks; H2D bytes per step; D2H bytes per step)."""
+    stream = torch.cuda.current_stream()
+    dev_in = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(2)]
+    outs = [out, torch.empty_like(out)]
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    h_stream, c_stream, d_stream = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(n):
+        h_done = [torch.cuda.Event() for _ in range(n)]
+        c_done = [torch.cuda.Event() for _ in range(n)]
+        d_done = [torch.cuda.Event() for _ in range(n)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        h_stream.wait_event(start)
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(h_stream):
+                if i >= 2:
+                    h_stream.wait_event(c_done[i - 2])   # buffer b's inputs are consumed
+                for h, d in zip(host_in, dev_in[b]):
+                    d.copy_(h, non_blocking=True)
+                h_done[i].record(h_stream)
+            with torch.cuda.stream(c_stream):
+                c_stream.wait_event(h_done[i])
+                if i >= 2:
+                    c_stream.wait_event(d_done[i - 2])   # buffer b's output was read back
+                compute(dev_in[b], outs[b])
+                c_done[i].record(c_stream)
+            with torch.cuda.stream(d_stream):
+                d_stream.wait_event(c_done[i])
+                host_out[b].copy_(outs[b], non_blocking=True)
+                d_done[i].record(d_stream)
+        stream.wait_event(d_done[n - 1])
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
+
+    run(2)
+    barrier(world)
+    ms = max_over_ranks(run(n), world, dev) / n
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    return ms, h2d, d2h
 
 
 # ---------------------------------------------------------------- verify windows (8 x 16 rows, L = 65,536)
@@ -326,6 +344,81 @@ def verify_bytes(n_seq):
             + n_seq * V_ROWS * HEADS * DIM * 2)        # output rows
 
 
+def verify_setup(dev, seed, n_seq, paged=False, e4m3=False):
+    """Prepared K/V caches of n_seq sequences (65,552 positions each) resident in HBM, the
+    fused rows of their 16 new rows, and one step: the verify call over them. Returns
+    (step, algorithmic bytes per step)."""
+    from verify_gated_gqa_gb300 import binding as B
+    from verify_gated_gqa_gb300 import synth
+    c, s = B.ga_rope_table_host(V_CAP)
+    cos, sin = c.to(dev), s.to(dev)
+    w_q = synth.normal_bf16(seed, "w_q", (DIM,), sigma=0.1, device=dev)
+    w_k = synth.normal_bf16(seed, "w_k", (DIM,), sigma=0.1, device=dev)
+    k_cache = torch.empty(n_seq, V_CAP, KV_HEADS, DIM, dtype=torch.bfloat16, device=dev)
+    v_cache = torch.empty_like(k_cache)
+    for b in range(n_seq):
+        k_raw = synth.normal_bf16(seed, "k", (V_CAP, KV_HEADS, DIM), sub=b, device=dev)
+        B.ga_k_prologue(k_raw, w_k, cos, sin, k_prep=k_cache[b])
+        v_cache[b] = synth.normal_bf16(seed, "v", (V_CAP, KV_HEADS, DIM), sub=b, device=dev)
+        del k_raw
+    qg = torch.stack([synth.normal_bf16(seed, "qg", (V_ROWS, HEADS, 2 * DIM), sub=b, device=dev)
+                      for b in range(n_seq)])
+    lens = [V_L] * n_seq
+    out = torch.empty(n_seq, V_ROWS, HEADS * DIM, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(B.ga_verify_workspace_bytes(n_seq, V_ROWS, V_L), dtype=torch.uint8,
+                     device=dev)
+    n_bytes = verify_bytes(n_seq)
+    if e4m3:
+        # the same caches as e4m3 rows with an fp32 scale each (algorithmic bytes: the codes
+        # and scales read once, the fused rows and the outputs)
+        k8, ksc = B.ga_kv_quantize_e4m3(k_cache)
+        v8, vsc = B.ga_kv_quantize_e4m3(v_cache)
+        del k_cache, v_cache
+        n_bytes = (k8.numel() + v8.numel() + 4 * (ksc.numel() + vsc.numel())
+                   + qg.numel() * 2 + out.numel() * 2)
+
+        def step():
+            B.ga_attn_verify_e4m3(qg, k8, ksc, v8, vsc, lens, w_q, cos, sin, out=out, workspace=ws)
+    elif paged:
+        pages_per_seq = -(-V_CAP // V_PAGE)
+        n_pages = n_seq * pages_per_seq
+        order = torch.randperm(n_pages, generator=torch.Generator().manual_seed(seed))
+        table = order.view(n_seq, pages_per_seq).to(torch.int32).to(dev)
+        k_pool = torch.zeros(n_pages, V_PAGE, KV_HEADS, DIM, dtype=torch.bfloat16, device=dev)
+        v_pool = torch.zeros_like(k_pool)
+        for b in range(n_seq):
+            for p in range(pages_per_seq):
+                lo, hi = p * V_PAGE, min((p + 1) * V_PAGE, V_CAP)
+                pg = int(order[b * pages_per_seq + p])
+                k_pool[pg, :hi - lo] = k_cache[b, lo:hi]
+                v_pool[pg, :hi - lo] = v_cache[b, lo:hi]
+        del k_cache, v_cache
+
+        def step():
+            B.ga_attn_verify_paged(qg, k_pool, v_pool, table, lens, w_q, cos, sin, out=out,
+                                   workspace=ws)
+    else:
+        def step():
+            B.ga_attn_verify(qg, k_cache, v_cache, lens, w_q, cos, sin, out=out, workspace=ws)
+    return step, n_bytes
+
+
+def timed_steps(step, steps, warmup, stream):
+    """ms per step of `steps` back-to-back steps after `warmup` untimed ones (CUDA events
+    on the launching stream, synchronised on both sides)."""
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
 def run_verify(args, world, rank, local):
     """Verify windows on one GPU (per rank): ga_attn_verify over prepared caches resident in
     HBM, 16 rows over 65,536 cached keys per sequence (--verify-seqs sequences; 8 is the
@@ -338,64 +431,14 @@ def run_verify(args, world, rank, local):
     kind = " over paged caches" if paged else (" over e4m3 caches" if e4m3 else "")
     V_METRIC = (f"verify windows{kind}: HBM GB/s ({V_SEQ} sequences x 16 rows over L=65536 "
                 "cached keys)")
-    V_BYTES = verify_bytes(V_SEQ)
     from verify_gated_gqa_gb300 import binding as B
-    from verify_gated_gqa_gb300 import synth
     from verify_gated_gqa_gb300.build import build
 
     build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
-    seed = SEED + 5 + rank
-    c, s = B.ga_rope_table_host(V_CAP)
-    cos, sin = c.to(dev), s.to(dev)
-    w_q = synth.normal_bf16(seed, "w_q", (DIM,), sigma=0.1, device=dev)
-    w_k = synth.normal_bf16(seed, "w_k", (DIM,), sigma=0.1, device=dev)
-    k_cache = torch.empty(V_SEQ, V_CAP, KV_HEADS, DIM, dtype=torch.bfloat16, device=dev)
-    v_cache = torch.empty_like(k_cache)
-    for b in range(V_SEQ):
-        k_raw = synth.normal_bf16(seed, "k", (V_CAP, KV_HEADS, DIM), sub=b, device=dev)
-        B.ga_k_prologue(k_raw, w_k, cos, sin, k_prep=k_cache[b])
-        v_cache[b] = synth.normal_bf16(seed, "v", (V_CAP, KV_HEADS, DIM), sub=b, device=dev)
-        del k_raw
-    qg = torch.stack([synth.normal_bf16(seed, "qg", (V_ROWS, HEADS, 2 * DIM), sub=b, device=dev)
-                      for b in range(V_SEQ)])
-    lens = [V_L] * V_SEQ
-    out = torch.empty(V_SEQ, V_ROWS, HEADS * DIM, dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(B.ga_verify_workspace_bytes(V_SEQ, V_ROWS, V_L), dtype=torch.uint8, device=dev)
-    if e4m3:
-        # the same caches as e4m3 rows with an fp32 scale each (algorithmic bytes: the codes
-        # and scales read once, the fused rows and the outputs)
-        k8, ksc = B.ga_kv_quantize_e4m3(k_cache)
-        v8, vsc = B.ga_kv_quantize_e4m3(v_cache)
-        del k_cache, v_cache
-        V_BYTES = (k8.numel() + v8.numel() + 4 * (ksc.numel() + vsc.numel())
-                   + qg.numel() * 2 + out.numel() * 2)
-    if paged:
-        pages_per_seq = -(-V_CAP // V_PAGE)
-        n_pages = V_SEQ * pages_per_seq
-        order = torch.randperm(n_pages, generator=torch.Generator().manual_seed(seed))
-        table = order.view(V_SEQ, pages_per_seq).to(torch.int32).to(dev)
-        k_pool = torch.zeros(n_pages, V_PAGE, KV_HEADS, DIM, dtype=torch.bfloat16, device=dev)
-        v_pool = torch.zeros_like(k_pool)
-        for b in range(V_SEQ):
-            for p in range(pages_per_seq):
-                lo, hi = p * V_PAGE, min((p + 1) * V_PAGE, V_CAP)
-                pg = int(order[b * pages_per_seq + p])
-                k_pool[pg, :hi - lo] = k_cache[b, lo:hi]
-                v_pool[pg, :hi - lo] = v_cache[b, lo:hi]
-        del k_cache, v_cache
-
-    def step():
-        if paged:
-            B.ga_attn_verify_paged(qg, k_pool, v_pool, table, lens, w_q, cos, sin, out=out,
-                                   workspace=ws)
-        elif e4m3:
-            B.ga_attn_verify_e4m3(qg, k8, ksc, v8, vsc, lens, w_q, cos, sin, out=out, workspace=ws)
-        else:
-            B.ga_attn_verify(qg, k_cache, v_cache, lens, w_q, cos, sin, out=out, workspace=ws)
-
+    step, V_BYTES = verify_setup(dev, SEED + 5 + rank, V_SEQ, paged, e4m3)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -443,6 +486,194 @@ def run_verify(args, world, rank, local):
                      "algorithmic_bytes": V_BYTES},
         "gpu_launches": 3 * args.steps, "clocks": clk, "device_status": B.ga_device_status(),
     }
+
+
+# ---------------------------------------------------------------- sparse-selection masked attention (S = 8192)
+M_WINDOW, M_RANDOM = 128, 1024
+
+
+def masked_setup(dev, seed):
+    """The stored-mask workload at the 8192-token cap: seeded inputs, the selection mask
+    (each row's causal window of 128 keys plus 1024 random earlier keys) resident in HBM,
+    the prepared keys, and the counts of its work: visible (query, key) pairs and the
+    128 x 128 tiles with a visible key (the tiles the kernel executes)."""
+    from verify_gated_gqa_gb300 import binding as B
+    from verify_gated_gqa_gb300 import synth
+    qg, kraw, v, w_q, w_k = synth.attention_inputs(seed, S, S, device=dev)
+    mask = synth.selection_mask(seed, S, window=M_WINDOW, n_random=M_RANDOM, device=dev)
+    c, s_ = B.ga_rope_table_host(S)
+    cos, sin = c.to(dev), s_.to(dev)
+    k_prep = B.ga_k_prologue(kraw, w_k, cos, sin)
+    pairs = int(mask.sum(dtype=torch.int64).item())
+    tiles = int((mask.view(S // 128, 128, S // 128, 128).amax(dim=(1, 3)) != 0).sum().item())
+    return dict(qg=qg, kraw=kraw, v=v, w_q=w_q, w_k=w_k, mask=mask, cos=cos, sin=sin,
+                k_prep=k_prep, pairs=pairs, flops=attention_flops(pairs),
+                exec_flops=4.0 * DIM * HEADS * tiles * 128 * 128, tiles=tiles)
+
+
+def run_masked(args, world, rank, local):
+    """Sparse-selection masked attention at S = 8192: each step runs the key prologue, the
+    query prologue and ga_attn_masked_prepared (the mask prepass and the attention), the
+    pieces ga_attn_masked runs, each timed on the stream. TFLOP/s both on the algorithmic
+    work (visible pairs) and on the executed 128 x 128 tiles."""
+    from verify_gated_gqa_gb300 import binding as B
+    from verify_gated_gqa_gb300.build import build
+
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    m = masked_setup(dev, SEED + 7 + rank)
+    qg, kraw, v, w_q, w_k, mask, cos, sin = (m[n] for n in ("qg", "kraw", "v", "w_q", "w_k",
+                                                             "mask", "cos", "sin"))
+    k_prep = torch.empty_like(kraw)
+    q_prep = torch.empty(S, HEADS, DIM, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(S, HEADS * DIM, dtype=torch.bfloat16, device=dev)
+    hid = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(B.ga_masked_workspace_bytes(S, S), dtype=torch.uint8, device=dev)
+
+    def step():
+        B.ga_k_prologue(kraw, w_k, cos, sin, k_prep=k_prep)
+        B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
+        B.ga_attn_masked_prepared(q_prep, qg, k_prep, v, mask, out=out, hidden_rows=hid,
+                                  workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        B.ga_k_prologue(kraw, w_k, cos, sin, k_prep=k_prep)
+        ev[i][1].record(stream)
+        B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
+        ev[i][2].record(stream)
+        B.ga_attn_masked_prepared(q_prep, qg, k_prep, v, mask, out=out, hidden_rows=hid,
+                                  workspace=ws)
+        ev[i][3].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / args.steps
+    span = lambda a, b: statistics.mean(ev[i][a].elapsed_time(ev[i][b]) for i in range(args.steps))
+    kpro_ms, qpro_ms, attn_ms = span(0, 1), span(1, 2), span(2, 3)
+    status = B.ga_device_status()
+    hidden = int(hid.item())
+
+    host_in = [t.cpu().pin_memory() for t in (qg, kraw, v, w_q, w_k, cos, sin, mask)]
+    ws2 = torch.empty_like(ws)
+
+    def compute(d, o):
+        qg_d, k_d, v_d, wq_d, wk_d, cos_d, sin_d, m_d = d
+        B.ga_k_prologue(k_d, wk_d, cos_d, sin_d, k_prep=k_prep)
+        B.ga_attn_masked(qg_d, k_prep, v_d, wq_d, cos_d, sin_d, m_d, out=o, hidden_rows=hid,
+                         workspace=ws2)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_ms, h2d, d2h = e2e_pipelined(host_in, compute, out, e2e_steps, world, dev)
+    if rank != 0:
+        return None
+    peak_tf, _, peak_src = measured_peaks()
+    flops, exec_flops = m["flops"], m["exec_flops"]
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    line = {
+        "metric": "sparse-selection masked attention TFLOP/s at S=8192 (algorithmic: visible "
+                  "pairs)",
+        "value": round(world * flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.1) norm weights, seeded selection "
+                "mask)",
+        "config": {"workload": f"masked gated GQA, S=8192 (the cap), 24q/2kv heads, d=256, "
+                               f"stored uint8 mask [8192, 8192]: each row's causal window of "
+                               f"{M_WINDOW} keys plus {M_RANDOM} random earlier keys",
+                   "global_batch": world, "seq_len": S,
+                   "parallelism": f"independent sequence per GPU x{world}",
+                   "l2": "inputs larger than L2 (qg 192 MiB + mask 64 MiB read, out 96 MiB "
+                         "written per step)",
+                   "step": "ga_k_prologue + ga_q_prologue + ga_attn_masked_prepared (mask "
+                           "prepass + attention), the pieces of ga_attn_masked"},
+        "visible_pairs_per_head": m["pairs"], "algorithmic_gflop": round(flops / 1e9, 2),
+        "executed_tiles": {"tiles_per_head": m["tiles"],
+                           "gflop": round(exec_flops / 1e9, 2),
+                           "tflops_attention": round(exec_flops / (attn_ms * 1e-3) / 1e12, 2),
+                           "note": "128 x 128 tiles with a visible key, each a dense QK^T and "
+                                   "P.V on the tensor cores"},
+        "tokens_per_s": round(world * S / (ms * 1e-3), 1),
+        "kernel_ms": {"mask_prepass_and_attn_kernel": round(attn_ms, 4),
+                      "k_prologue": round(kpro_ms, 4), "q_prologue": round(qpro_ms, 4)},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": None,
+                     "peak_kind": f"dense bf16 burst ({peak_src})",
+                     "kernel": "ga_attn_masked_prepared (mask_prepass_kernel + "
+                               "attn_kernel<mask>), algorithmic flops",
+                     "algorithmic_flops": flops},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "schedule": "H2D, compute (ga_k_prologue + ga_attn_masked) and D2H on three "
+                            "streams, device inputs and outputs double-buffered"},
+        "gpu_launches": 4 * args.steps, "clocks": clk, "device_status": status,
+        "hidden_rows": hidden,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_masked(args.cpu_seconds)
+    return line
+
+
+def secondary_measurements(dev, rank, steps):
+    """The two other long-context configurations, timed after the headline for a few steps
+    each: the verify call (8 sequences x 16 rows over 65,536 cached keys, HBM-bound) and the
+    sparse-selection masked call at S = 8192 (ga_attn_masked: mask prepass, query prologue,
+    attention; keys prepared beforehand)."""
+    from verify_gated_gqa_gb300 import binding as B
+    if rank != 0:
+        return None
+    stream = torch.cuda.current_stream()
+    peak_tf, peak_hbm, peak_src = measured_peaks()
+    res = {}
+    step, n_bytes = verify_setup(dev, SEED + 5, 8)
+    ms = timed_steps(step, steps, 3, stream)
+    gbs = n_bytes / (ms * 1e-3) / 1e9
+    res["verify"] = {"workload": "ga_attn_verify, 8 sequences x 16 rows at positions "
+                                 "65536..65551 over prepared K/V caches [65552, 2, 256] bf16",
+                     "ms": round(ms, 4), "value": round(gbs, 1), "unit": "GB/s",
+                     "algorithmic_bytes": n_bytes, "roofline_frac": round(gbs / peak_hbm, 4),
+                     "peak": peak_hbm, "peak_kind": f"HBM copy ({peak_src})", "steps": steps}
+    del step
+    torch.cuda.empty_cache()
+    m = masked_setup(dev, SEED + 7)
+    out = torch.empty(S, HEADS * DIM, dtype=torch.bfloat16, device=dev)
+    hid = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(B.ga_masked_workspace_bytes(S, S), dtype=torch.uint8, device=dev)
+
+    def mstep():
+        B.ga_attn_masked(m["qg"], m["k_prep"], m["v"], m["w_q"], m["cos"], m["sin"], m["mask"],
+                         out=out, hidden_rows=hid, workspace=ws)
+
+    ms = timed_steps(mstep, steps, 3, stream)
+    tf = m["flops"] / (ms * 1e-3) / 1e12
+    res["masked"] = {"workload": "ga_attn_masked at S=8192, stored mask: causal window of 128 "
+                                 "keys plus 1024 random earlier keys per row",
+                     "ms": round(ms, 4), "value": round(tf, 2), "unit": "TFLOP/s",
+                     "algorithmic_gflop": round(m["flops"] / 1e9, 2),
+                     "executed_tile_gflop": round(m["exec_flops"] / 1e9, 2),
+                     "executed_tile_tflops": round(m["exec_flops"] / (ms * 1e-3) / 1e12, 2),
+                     "roofline_frac": round(tf / peak_tf, 4), "peak": peak_tf,
+                     "peak_kind": f"dense bf16 burst ({peak_src})", "steps": steps,
+                     "device_status": B.ga_device_status()}
+    return res
 
 
 SEL_T, SEL_BUDGET, SEL_SETS = 8192, 2048, 4
@@ -879,6 +1110,33 @@ def cpu_baseline(seconds: float):
                       f"16-row batch with the K prologue over all 8192 keys; {dt:.1f} s"}
 
 
+def cpu_baseline_masked(seconds: float):
+    """The oracle on the masked workload: the key prologue over all 8192 keys and the
+    stored-mask attention of 16 random query rows (all 24 heads) per batch."""
+    import numpy as np
+    from oracle import ga_oracle as O
+    from verify_gated_gqa_gb300 import synth
+    qg, k, v, w_q, w_k = synth.attention_inputs(SEED + 7, S, S)
+    mask = synth.selection_mask(SEED + 7, S, window=M_WINDOW, n_random=M_RANDOM).numpy()
+    f = lambda t: t.double().numpy()
+    qg, k, v, w_q, w_k = f(qg), f(k), f(v), f(w_q), f(w_k)
+    cos, sin = O.rope_tables(S)
+    rng = np.random.default_rng(0)
+    pairs = n_rows = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        rows = np.sort(rng.choice(S, 16, replace=False))
+        kp = O.prep_keys(k, w_k, cos, sin)
+        O.masked(qg, kp, v, w_q, cos, sin, 0, S, mask, rows=rows)
+        pairs += int((mask[rows] != 0).sum())
+        n_rows += 16
+    dt = time.perf_counter() - t0
+    return {"value": round(attention_flops(pairs) / dt / 1e12, 6), "unit": UNIT,
+            "cores": _threads_used(), "kind": "oracle",
+            "sample": f"{n_rows} random query rows x 24 heads of the S=8192 masked pass, each "
+                      f"16-row batch with the K prologue over all 8192 keys; {dt:.1f} s"}
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle, as it stands, on this machine's host cores."""
     if rank != 0:
@@ -928,14 +1186,16 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--workload", default="prefill",
                     choices=["prefill", "verify", "verify_paged", "verify_e4m3", "batch",
-                             "select", "prefill_e4m3", "small"],
+                             "select", "prefill_e4m3", "small", "masked"],
                     help="prefill: the headline S=8192 causal step; verify: 8 x 16 rows over "
                          "65,536 cached keys; verify_paged: the same over paged caches; "
                          "verify_e4m3: the same over e4m3 caches; batch: 16 prompts of "
                          "512..4096 tokens in one batched call; select: the selection-mask "
                          "producer at 8192 x 8192, block_topk 512; prefill_e4m3: the "
                          "headline causal step over e4m3 caches; small: S=64 and S=2048 "
-                         "(causal and bidirectional) with L2 flushed before each call")
+                         "(causal and bidirectional) with L2 flushed before each call; masked: "
+                         "sparse-selection masked attention at S=8192 (window 128 + 1024 "
+                         "random keys per row)")
     ap.add_argument("--verify-seqs", type=int, default=8)
     ap.add_argument("--serial-prologues", action="store_true",
                     help="prefill: run the key prologue on the main stream, not beside the "
@@ -954,6 +1214,8 @@ def main():
         line = run_prefill_e4m3(args, world, rank, local)
     elif args.workload == "small":
         line = run_small(args, world, rank, local)
+    elif args.workload == "masked":
+        line = run_masked(args, world, rank, local)
     else:
         line = run_gpu(args, world, rank, local)
     if line is not None:

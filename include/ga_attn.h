@@ -208,6 +208,21 @@ int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
                    long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
                    void* workspace, size_t ws_bytes, ga_stream stream);
 
+/* ga_attn_masked from prepared queries (ga_q_prologue's output): the mask prepass and the
+ * attention kernel (and the weights pass) without the query prologue, exposed so that a
+ * caller can time or reuse the prepared queries, as ga_attn_prefill_prepared does for the
+ * causal pass.
+ *   q_prep  [rows][24][256]  prepared queries of positions q_base .. q_base+rows-1, 16-byte
+ *                            aligned; may not overlap out
+ *   qg, k_prep, v, rows, T, q_base, mask, ld_mask, out, weights, hidden_rows, workspace,
+ *           ws_bytes: as in ga_attn_masked (the workspace's query area is not used)
+ * Rules and errors: as ga_attn_masked (NULL also for q_prep), without the table checks. */
+int ga_attn_masked_prepared(const ga_bf16* q_prep, const ga_bf16* qg, const ga_bf16* k_prep,
+                            const ga_bf16* v, int rows, int T, int q_base, const uint8_t* mask,
+                            long long ld_mask, ga_bf16* out, ga_bf16* weights,
+                            int* hidden_rows, void* workspace, size_t ws_bytes,
+                            ga_stream stream);
+
 /* Allocation-free variant of ga_attn_masked. The pages have no counterpart: this is an
  * addition of the library for callers that may not allocate device memory at call time,
  * such as a server step that runs under a fixed memory budget, or a framework that
@@ -216,12 +231,16 @@ int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
  * comes instead from one static device array of GA_STATIC_SCRATCH_BYTES per device,
  * reserved when the library is loaded; nothing is allocated by the call.
  *   Arguments, layouts and results: as in ga_attn_masked, without workspace/ws_bytes.
- *   Limit: ga_masked_workspace_bytes(rows, T) <= GA_STATIC_SCRATCH_BYTES (about 1,100
- *           rows at T = 8192); larger calls are refused with GA_ERR_WORKSPACE before any
+ *   Limit: the call runs when ga_masked_workspace_bytes(rows, T) <=
+ *           GA_STATIC_SCRATCH_BYTES: up to 1,239 rows at T = 8192, 1,286 at T = 4096,
+ *           1,315 at T = 2048. Larger calls are refused with GA_ERR_WORKSPACE before any
  *           CUDA call.
  *   The first call on a device looks up the array's address (one CUDA runtime query,
  *           once per device, with that device current); make a first call before any
- *           stream capture.
+ *           stream capture. The address is kept per device index for the life of the
+ *           process: the library assumes each device's primary context (the runtime's
+ *           default) and no cudaDeviceReset between calls, the same assumption as its
+ *           other per-device set-up.
  *   The scratch needs no initial contents (every call writes all of it that it reads).
  *   The array is shared by all calls on a device: calls that may overlap in time (other
  *           streams, other host threads) race on it and must be serialised by the caller.

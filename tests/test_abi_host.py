@@ -317,6 +317,25 @@ def test_q_prologue_and_prepared_refusals(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def test_masked_prepared_refusals(L):
+    before = L.ga_debug_cuda_calls()
+    P = L.ga_attn_masked_prepared
+    wsb = L.ga_masked_workspace_bytes(10, 100)
+    W = 0x20000                                             # 256-byte aligned fake workspace
+    assert P(None, A, A, A, 10, 100, 0, A, 112, A, None, None, W, wsb, S) == -1
+    assert P(A, A, A, A, 10, 100, 0, None, 112, A, None, None, W, wsb, S) == -1
+    assert P(A, A, A, A, -1, 100, 0, A, 112, A, None, None, W, wsb, S) == -2
+    assert P(A, A, A, A, 10, 100, 32, A, 112, A, None, None, W, wsb, S) == -4
+    assert P(A, A, A, A, 10, 9000, 0, A, 9008, A, None, None, W, wsb, S) == -4   # masked cap
+    assert P(A, A, A, A, 10, 100, 0, A, 96, A, None, None, W, wsb, S) == -4      # ld < T
+    assert P(MIS, A, A, A, 10, 100, 0, A, 112, A, None, None, W, wsb, S) == -3
+    assert P(A, A, A, A, 10, 100, 0, A, 104, A, None, None, W, wsb, S) == -3     # ld % 16
+    assert P(A, A, A, A, 10, 100, 0, A, 112, A, None, None, W, wsb - 1, S) == -6
+    assert P(A, A, A, A, 10, 100, 0, A, 112, A, None, None, W + 16, wsb, S) == -6
+    assert P(A, A, A, A, 0, 100, 0, A, 112, A, None, None, W, wsb, S) == 0        # no-op
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_wait_timeout_hook_refuses_bad_limits(L):
     before = L.ga_debug_cuda_calls()
     assert L.ga_debug_wait_timeout(0, S) == -4

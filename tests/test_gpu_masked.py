@@ -118,3 +118,23 @@ def test_negative_control_causal_for_sparse_mask_fails():
     c_out = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, S)
     with pytest.raises(AssertionError):
         inp.ref(0, S, "mask", mask=mask.numpy()).check(c_out, what="causal for sparse (must fail)")
+
+
+def test_masked_prepared_equals_masked_call():
+    """ga_q_prologue then ga_attn_masked_prepared gives ga_attn_masked's bits (outputs,
+    weights and hidden rows), on a window with a hidden row."""
+    S, qb = 384, 128
+    inp = Inputs(SEED + 25, S, S)
+    d = inp.dev()
+    mask = synth.selection_mask(SEED + 25, S, window=16, n_random=48)[qb:].contiguous()
+    mask[5] = 0
+    mcu = mask.cuda()
+    qg = d["qg"][qb:]
+    ref = B.ga_attn_masked(qg, d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], mcu, q_base=qb,
+                           want_weights=True)
+    q_prep = B.ga_q_prologue(qg, d["w_q"], d["cos"], d["sin"], q_base=qb)
+    got = B.ga_attn_masked_prepared(q_prep, qg, d["k_prep"], d["v"], mcu, q_base=qb,
+                                    want_weights=True)
+    torch.cuda.synchronize()
+    assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+    assert int(got[2].item()) == int(ref[2].item()) == 1

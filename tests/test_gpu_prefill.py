@@ -208,6 +208,9 @@ def test_prefill_s8192_full_and_chunks():
                                      rng.integers(0, S, 22)]))
     inp.ref(0, S, "causal", rows=rows).check(full[torch.as_tensor(rows)],
                                               what=f"S=8192 causal, {len(rows)} sampled rows")
+    r2 = rows[rows >= 4096] - 4096
+    inp.ref(4096, S, "causal", rows=r2, qg=inp.np["qg"][4096:]).check(
+        c2[torch.as_tensor(r2)], what=f"S=8192 chunk q_base=4096, {len(r2)} sampled rows")
 
 
 # ------------------------------------------------------------------ negative controls

@@ -67,3 +67,30 @@ def test_static_matches_workspace_call_two_calls_in_a_row():
         assert torch.equal(w, ref_w)
         assert int(hid.item()) == int(ref_h.item())
     assert B.ga_device_status() == 0
+
+
+@pytest.mark.gpu
+def test_static_at_the_size_limit():
+    """The largest call the static scratch takes at T = 8192 (1,239 rows: the scratch's
+    last rows in use) against the workspace call, bit for bit, so the layout's end stays
+    inside the array; one row more is refused."""
+    T, rows, q_base = 8192, 1239, 6912
+    assert B.ga_masked_workspace_bytes(rows, T) <= 16 << 20 < B.ga_masked_workspace_bytes(rows + 1, T)
+    d, mask, q_base, T = _case(SEED + 42, rows, T, q_base, 128, 1024)
+    qg = d["qg"][q_base:q_base + rows]
+    ref_out, _, ref_h = B.ga_attn_masked(qg, d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"],
+                                         mask, q_base=q_base, T=T)
+    out = torch.empty_like(ref_out)
+    hid = torch.zeros(1, dtype=torch.int32, device=out.device)
+    B.ga_attn_masked_static(qg, d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], mask, out,
+                            hid, q_base=q_base, T=T)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+    assert int(hid.item()) == int(ref_h.item()) == 0
+    big = torch.zeros(rows + 1, T, dtype=torch.uint8, device=out.device)
+    with pytest.raises(B.GaError, match="WORKSPACE"):
+        B.ga_attn_masked_static(d["qg"][q_base - 64:q_base + rows], d["k_prep"], d["v"], d["w_q"],
+                                d["cos"], d["sin"], big,
+                                torch.empty(rows + 1, 6144, dtype=torch.bfloat16,
+                                            device=out.device), hid, q_base=q_base - 64, T=T)
+    assert B.ga_device_status() == 0

@@ -45,6 +45,8 @@ _SIGS = {
     "ga_attn_masked_static": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _LL, _P, _P, _P,
                                    _P]),
     "ga_masked_workspace_bytes": (_SZ, [_I, _I]),
+    "ga_attn_masked_prepared": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _LL, _P, _P, _P, _P, _SZ,
+                                     _P]),
     "ga_attn_masked": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _LL, _P, _P, _P, _P,
                             _SZ, _P]),
     "ga_verify_workspace_bytes": (_SZ, [_I, _I, _I]),
@@ -240,6 +242,34 @@ def ga_attn_masked(qg, k_prep, v, w_q, cos_tab, sin_tab, mask, q_base=0, T=None,
                                 mask.stride(0), _ptr(out), _ptr(weights), _ptr(hidden_rows),
                                 _ptr(workspace), workspace.numel(), _stream()),
            "ga_attn_masked")
+    return out, weights, hidden_rows
+
+
+def ga_attn_masked_prepared(q_prep, qg, k_prep, v, mask, q_base=0, T=None, want_weights=False,
+                            out=None, weights=None, hidden_rows=None, workspace=None):
+    """ga_attn_masked from prepared queries q_prep [rows, 24, 256] (ga_q_prologue's output):
+    the mask prepass and the attention only. Returns (out, weights or None, hidden_rows)."""
+    rows = qg.shape[0]
+    T = k_prep.shape[0] if T is None else T
+    dev = qg.device
+    if out is None:
+        out = torch.empty(rows, N_Q_HEADS * HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    if want_weights and weights is None:
+        weights = torch.empty(N_Q_HEADS, rows, T, dtype=torch.bfloat16, device=dev)
+    if hidden_rows is None:
+        hidden_rows = torch.zeros(1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(ga_masked_workspace_bytes(rows, T), 1), dtype=torch.uint8,
+                                device=dev)
+    if mask.dtype != torch.uint8 or not mask.is_cuda or mask.stride(1) != 1:
+        raise ValueError("mask must be a uint8 CUDA tensor with unit column stride")
+    for n, t in (("q_prep", q_prep), ("qg", qg), ("k_prep", k_prep), ("v", v), ("out", out)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_attn_masked_prepared(_ptr(q_prep), _ptr(qg), _ptr(k_prep), _ptr(v), rows, T,
+                                         q_base, _ptr(mask), mask.stride(0), _ptr(out),
+                                         _ptr(weights), _ptr(hidden_rows), _ptr(workspace),
+                                         workspace.numel(), _stream()),
+           "ga_attn_masked_prepared")
     return out, weights, hidden_rows
 
 

@@ -690,11 +690,17 @@ size_t ga_masked_workspace_bytes(int rows, int T) {
   return masked_layout(rows, T).total;
 }
 
-int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
-                   const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
-                   int table_rows, int rows, int T, int q_base, const uint8_t* mask,
-                   long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
-                   void* workspace, size_t ws_bytes, ga_stream stream) {
+}  // extern "C"
+
+namespace ga {
+namespace {
+// Every check of a stored-mask call except the workspace's (no CUDA call); shared by
+// ga_attn_masked and ga_attn_masked_static.
+int masked_check_args(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                      const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                      int table_rows, int rows, int T, int q_base, const uint8_t* mask,
+                      long long ld_mask, const ga_bf16* out, const ga_bf16* weights,
+                      const int* hidden_rows) {
   int st = check_attention_args(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T,
                                 q_base, out);
   if (st != GA_OK) return st;
@@ -703,18 +709,36 @@ int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
   if (!aligned(mask, 16) || ld_mask % 16 != 0) return GA_ERR_ALIGN;
   if ((weights && !aligned(weights, 16)) || (hidden_rows && !aligned(hidden_rows, 4)))
     return GA_ERR_ALIGN;
-  const MaskedLayout L = masked_layout(rows, T);
-  if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return GA_ERR_WORKSPACE;
-  if (rows == 0) return GA_OK;
+  return GA_OK;
+}
+}  // namespace
+}  // namespace ga
+
+extern "C" {
+
+}  // extern "C"
+
+namespace ga {
+namespace {
+// The stored-mask call after its checks: zero hidden_rows, the mask prepass into the
+// workspace, the query prologue into the workspace (unless q_prep already holds the
+// prepared queries), the attention, and the weights pass when weights are wanted.
+int masked_run(const ga_bf16* q_prep_in, const ga_bf16* qg, const ga_bf16* k_prep,
+               const ga_bf16* v, const ga_bf16* w_q, const ga_bf16* cos_tab,
+               const ga_bf16* sin_tab, int rows, int T, int q_base, const uint8_t* mask,
+               long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
+               void* workspace, ga_stream stream) {
   DeviceState* dev = nullptr;
-  st = current_device(&dev);
+  int st = current_device(&dev);
   if (st != GA_OK) return st;
+  const MaskedLayout L = masked_layout(rows, T);
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* bits = reinterpret_cast<uint32_t*>(ws + L.bits_off);
   uint8_t* flags = ws + L.flags_off;
   float* stats = reinterpret_cast<float*>(ws + L.stats_off);
-  uint16_t* q_prep = reinterpret_cast<uint16_t*>(ws + L.q_off);
+  uint16_t* q_prep = q_prep_in ? const_cast<uint16_t*>(q_prep_in)
+                               : reinterpret_cast<uint16_t*>(ws + L.q_off);
   cudaError_t e;
   if (hidden_rows && (e = GA_CUDA(cudaMemsetAsync(hidden_rows, 0, sizeof(int), s))) != cudaSuccess)
     return fail_cuda(e);
@@ -727,7 +751,7 @@ int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
   a.mask_bits = bits; a.tile_flags = flags;
   a.key_tiles = L.key_tiles; a.mask_words = L.mask_words;
   a.rows = rows; a.T = T; a.q_base = q_base; a.mode = kModeMask;
-  st = launch_attention(a, q_prep, false, k_prep, v, T, dev, s);
+  st = launch_attention(a, q_prep, q_prep_in != nullptr, k_prep, v, T, dev, s);
   if (st != GA_OK || !weights) return st;
   if ((e = GA_CUDA(cudaMemsetAsync(weights, 0, (size_t)kHeads * rows * T * sizeof(uint16_t), s))) != cudaSuccess)
     return fail_cuda(e);
@@ -735,6 +759,43 @@ int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
   a.weights_pass = 1;
   a.hidden_rows = nullptr;
   return launch_attention(a, q_prep, true, k_prep, v, T, dev, s);
+}
+}  // namespace
+}  // namespace ga
+
+extern "C" {
+
+int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                   const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                   int table_rows, int rows, int T, int q_base, const uint8_t* mask,
+                   long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
+                   void* workspace, size_t ws_bytes, ga_stream stream) {
+  int st = masked_check_args(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base,
+                             mask, ld_mask, out, weights, hidden_rows);
+  if (st != GA_OK) return st;
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < masked_layout(rows, T).total)
+    return GA_ERR_WORKSPACE;
+  if (rows == 0) return GA_OK;
+  return masked_run(nullptr, qg, k_prep, v, w_q, cos_tab, sin_tab, rows, T, q_base, mask,
+                    ld_mask, out, weights, hidden_rows, workspace, stream);
+}
+
+int ga_attn_masked_prepared(const ga_bf16* q_prep, const ga_bf16* qg, const ga_bf16* k_prep,
+                            const ga_bf16* v, int rows, int T, int q_base, const uint8_t* mask,
+                            long long ld_mask, ga_bf16* out, ga_bf16* weights,
+                            int* hidden_rows, void* workspace, size_t ws_bytes,
+                            ga_stream stream) {
+  if (!q_prep) return GA_ERR_NULL;
+  // the prepared queries stand in for w_q and the tables in the shared checks (no
+  // table is read; table_rows is the largest position + 1)
+  int st = masked_check_args(qg, k_prep, v, q_prep, q_prep, q_prep, q_base + rows, rows, T,
+                             q_base, mask, ld_mask, out, weights, hidden_rows);
+  if (st != GA_OK) return st;
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < masked_layout(rows, T).total)
+    return GA_ERR_WORKSPACE;
+  if (rows == 0) return GA_OK;
+  return masked_run(q_prep, qg, k_prep, v, nullptr, nullptr, nullptr, rows, T, q_base, mask,
+                    ld_mask, out, weights, hidden_rows, workspace, stream);
 }
 
 size_t ga_verify_workspace_bytes(int n_seq, int rows, int max_len) {
@@ -965,15 +1026,13 @@ int ga_attn_masked_static(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf1
                           int table_rows, int rows, int T, int q_base, const uint8_t* mask,
                           long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
                           ga_stream stream) {
-  // Every argument check first, with no CUDA call: ga_attn_masked validates all arguments
-  // before it looks at the workspace, and a valid call with an empty (never dereferenced)
-  // workspace answers GA_ERR_WORKSPACE, or GA_OK when there is nothing to do.
-  void* const probe = reinterpret_cast<void*>(uintptr_t(256));
-  int st = ga_attn_masked(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base,
-                          mask, ld_mask, out, weights, hidden_rows, probe, 0, stream);
-  if (st != GA_ERR_WORKSPACE) return st;
-  const size_t need = masked_layout(rows, T).total;
-  if (need > GA_STATIC_SCRATCH_BYTES) return GA_ERR_WORKSPACE;
+  // Every argument check first, with no CUDA call (the same checks as ga_attn_masked),
+  // then the size limit of the static scratch.
+  int st = masked_check_args(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base,
+                             mask, ld_mask, out, weights, hidden_rows);
+  if (st != GA_OK) return st;
+  if (masked_layout(rows, T).total > GA_STATIC_SCRATCH_BYTES) return GA_ERR_WORKSPACE;
+  if (rows == 0) return GA_OK;
   int dev = 0;
   cudaError_t e = GA_CUDA(cudaGetDevice(&dev));
   if (e != cudaSuccess) return fail_cuda(e);
@@ -989,9 +1048,8 @@ int ga_attn_masked_static(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf1
     }
     scratch = g_static_scratch_ptr[dev];
   }
-  return ga_attn_masked(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base, mask,
-                        ld_mask, out, weights, hidden_rows, scratch, GA_STATIC_SCRATCH_BYTES,
-                        stream);
+  return masked_run(nullptr, qg, k_prep, v, w_q, cos_tab, sin_tab, rows, T, q_base, mask,
+                    ld_mask, out, weights, hidden_rows, scratch, stream);
 }
 
 }  // extern "C"
