@@ -57,7 +57,7 @@ def test_genuine_error_is_rejected():
     got[i, h * 256:(h + 1) * 256] = row
     assert not np.array_equal(row, ref.out[i, h * 256:(h + 1) * 256])
     with pytest.raises(AssertionError):
-        ref.check(torch.from_numpy(got), None, "genuine error")
+        ref.check(torch.from_numpy(got), None, "planted genuine error (must fail)")
 
 
 def test_wrong_kv_head_is_rejected():
@@ -65,4 +65,4 @@ def test_wrong_kv_head_is_rejected():
     got = ref.out.copy()
     got[:, :256] = ref.out[:, 12 * 256:13 * 256]    # head 0 answered with head 12's output
     with pytest.raises(AssertionError):
-        ref.check(torch.from_numpy(got), None, "swapped head")
+        ref.check(torch.from_numpy(got), None, "planted swapped head (must fail)")
