@@ -114,6 +114,21 @@ int ga_device_status(int* status_out, int clear);
  * ga_device_status. Errors: RANGE, DEVICE, CUDA. */
 int ga_debug_wait_timeout(long long limit_cycles, ga_stream stream);
 
+/* Test hook: the fp32 dot products the tensor cores form for the scores, before any
+ * rounding. For each of n_tiles tiles, s[n][i][j] = q[n][i] . k[n][j] over 256 dims, computed
+ * exactly as the attention kernel computes S = Q K^T (tcgen05.mma kind::f16, M128 N128,
+ * sixteen K16 steps accumulating in fp32 in tensor memory, operands in shared memory in the
+ * kernel's 128-byte-swizzled layout). The score is the bf16 rounding of this value (pegainfer
+ * PR #1151, the commit that adds the attention reader: "the bf16 GEMM result"); the fp32
+ * reduction order inside the tensor core is the hardware's, and the tests use this hook to
+ * bound its distance from the exact dot product.
+ *   q, k   [n_tiles][128][256] bf16, 16-byte aligned
+ *   s      [n_tiles][128][128] fp32, 16-byte aligned
+ * Rules: 0 <= n_tiles <= 65535 (0 is a no-op).
+ * Errors: NULL, SHAPE, RANGE, ALIGN, DEVICE, CUDA. */
+int ga_debug_qk_fp32(const ga_bf16* q, const ga_bf16* k, int n_tiles, float* s,
+                     ga_stream stream);
+
 /* HOST helper. Fills cos_out and sin_out (HOST arrays of n_pos * 32 values each,
  * [position][pair]) with cos and sin of p * 1e7^(-2i/64) for positions p < n_pos and
  * pairs i < 32, each computed in double and rounded once to bf16 (pegainfer PR #1151,

@@ -112,9 +112,13 @@ TC_BAND_ULP32 = 16.0
 MAX_ALTERNATIVES = 10
 # At most this fraction of a check's (row, head) pairs may miss the tolerance and still be
 # explained by ambiguous roundings (never fewer than MIN_OFF_CAP pairs); beyond it the check
-# fails without a search.
+# fails without a search. Calibration (every GPU parity check of the suite on GB300): the
+# explained pairs were 0.26 % of all pairs checked, at most 0.42 % in a check of more than
+# 10,000 pairs (S = 2048 bidirectional) and at most 5 pairs in a check of fewer than 1,000
+# (S = 8192 sampled rows, 768 pairs): the cap is about 2.4 times the largest large-sample
+# rate, with a floor for the small samples.
 MAX_OFF_FRACTION = 0.01
-MIN_OFF_CAP = 4
+MIN_OFF_CAP = 8
 
 
 def off_cap(pairs):

@@ -336,6 +336,16 @@ def test_masked_prepared_refusals(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def test_qk_probe_refusals(L):
+    before = L.ga_debug_cuda_calls()
+    assert L.ga_debug_qk_fp32(None, A, 1, A, S) == -1
+    assert L.ga_debug_qk_fp32(A, A, -1, A, S) == -2
+    assert L.ga_debug_qk_fp32(A, A, 70000, A, S) == -4
+    assert L.ga_debug_qk_fp32(A, MIS, 1, A, S) == -3
+    assert L.ga_debug_qk_fp32(A, A, 0, A, S) == 0
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_wait_timeout_hook_refuses_bad_limits(L):
     before = L.ga_debug_cuda_calls()
     assert L.ga_debug_wait_timeout(0, S) == -4

@@ -40,6 +40,7 @@ _SIGS = {
     "ga_k_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "ga_q_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "ga_debug_wait_timeout": (_I, [_LL, _P]),
+    "ga_debug_qk_fp32": (_I, [_P, _P, _I, _P, _P]),
     "ga_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "ga_attn_prefill_prepared": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "ga_attn_masked_static": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _LL, _P, _P, _P,
@@ -271,6 +272,19 @@ def ga_attn_masked_prepared(q_prep, qg, k_prep, v, mask, q_base=0, T=None, want_
                                          workspace.numel(), _stream()),
            "ga_attn_masked_prepared")
     return out, weights, hidden_rows
+
+
+def ga_debug_qk_fp32(q, k):
+    """Test hook: the tensor cores' fp32 dot products s[n, i, j] = q[n, i] . k[n, j] of bf16
+    tiles q, k [n, 128, 256], formed as the attention kernel forms its scores."""
+    for n, t in (("q", q), ("k", k)):
+        _bf16_cuda(n, t)
+    if q.dim() != 3 or tuple(q.shape[1:]) != (128, HEAD_DIM) or q.shape != k.shape:
+        raise ValueError("q and k must both be [n, 128, 256]")
+    s = torch.empty(q.shape[0], 128, 128, dtype=torch.float32, device=q.device)
+    _check(lib().ga_debug_qk_fp32(_ptr(q), _ptr(k), q.shape[0], _ptr(s), _stream()),
+           "ga_debug_qk_fp32")
+    return s
 
 
 def ga_select_mask(block_scores, T, block_topk, q_base=0, mask=None):

@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libga_attn.so")
 SOURCES = ["ga_host.cu", "ga_prologue.cu", "ga_attn.cu", "ga_mask.cu", "ga_quant.cu",
-           "ga_select.cu"]
+           "ga_select.cu", "ga_debug.cu"]
 HEADERS = ["ga_internal.h", "ga_numerics.cuh", "ga_sm100.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

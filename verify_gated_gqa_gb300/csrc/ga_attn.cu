@@ -180,10 +180,23 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
   } else if (kMode == kModeBidir) {
     it.n = (a.T + kTileN - 1) / kTileN;
   } else {
-    const uint8_t* f = a.tile_flags + (size_t)it.mt * a.key_tiles;
-    for (int kt = 0; kt < a.key_tiles; ++kt)
-      if (f[kt]) it.tiles[kt >> 6] |= (1ull << (kt & 63));
-    it.n = __popcll(it.tiles[0]) + __popcll(it.tiles[1]);
+    // the row tile's 64 flag bytes (0 or 1 each) in four 16-byte loads; each word's four
+    // flags become four bits by one multiply (the products land on distinct bits, so no
+    // carry joins them)
+    static_assert(kMaskFlagStride == 64, "one 64-bit tile map per row tile");
+    const uint4* f = reinterpret_cast<const uint4*>(a.tile_flags + (size_t)it.mt * kMaskFlagStride);
+    uint64_t m = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = __ldg(f + q);
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        m |= (uint64_t)((((wd[i] & 0x01010101u) * 0x00204081u) >> 21) & 0xFu) << (16 * q + 4 * i);
+    }
+    if (a.key_tiles < 64) m &= (1ull << a.key_tiles) - 1ull;
+    it.tiles[0] = m;
+    it.n = __popcll(m);
   }
   return it;
 }
@@ -514,12 +527,40 @@ template <int kMode>
 __device__ __forceinline__ uint32_t chunk_visibility(const AttnArgs& a, int row, int limit, int kt,
                                                      int ch, bool valid) {
   if (!valid) return 0u;
-  if (kMode == kModeMask)
-    return __ldg(a.mask_bits + (size_t)row * a.mask_words + kt * (kTileN / 32) + ch);
   const int first = kt * kTileN + ch * 32;
   int n = (kMode == kModeBidir) ? (a.T - first) : (limit - first + 1);
   n = max(0, min(32, n));
   return n >= 32 ? 0xFFFFFFFFu : ((1u << n) - 1u);
+}
+
+// Stored mask: this row's visibility words of one 64-key half of tile kt (keys 32 apart,
+// in the prepass's bit order). Rows past the end of the call lie inside the prepass's
+// padded row tile, whose words are zero.
+__device__ __forceinline__ uint2 mask_words_half(const AttnArgs& a, int row, int kt, int hf) {
+  return __ldg(reinterpret_cast<const uint2*>(a.mask_bits + (size_t)row * a.mask_words +
+                                              kt * (kTileN / 32) + 2 * hf));
+}
+
+// The bf16 score pairs sb[0..31] of a 64-key half with every hidden key set to -inf, from
+// the half's two visibility words. For s = 0..7, word << s holds keys 4s .. 4s+3 in the top
+// bits of its bytes (the prepass's bit order), and a byte permute that replicates those
+// bits gives each pair's keep mask (0xFFFF per visible key); one three-input logic op then
+// keeps the score or puts -inf (0xFF80) in its place.
+__device__ __forceinline__ void apply_mask_half(uint32_t (&sb)[kHalfKeys], uint2 vis) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t word = c ? vis.y : vis.x;
+#pragma unroll
+    for (int s4 = 0; s4 < 8; ++s4) {
+      const uint32_t w = word << s4;
+      const uint32_t k0 = prmt_b32(w, 0u, 0x9988u);   // keys 4s, 4s+1
+      const uint32_t k1 = prmt_b32(w, 0u, 0xBBAAu);   // keys 4s+2, 4s+3
+      uint32_t& p0 = sb[16 * c + 2 * s4];
+      uint32_t& p1 = sb[16 * c + 2 * s4 + 1];
+      p0 = (p0 & k0) | (0xFF80FF80u & ~k0);
+      p1 = (p1 & k1) | (0xFF80FF80u & ~k1);
+    }
+  }
 }
 
 // Every key of tile kt visible to every row of row tile mt (no per-key selects needed).
@@ -595,8 +636,18 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
       hasM = l_final > 0.f;
     }
     TileCursor<kMode> cursor(it);
+    // stored mask: the next tile's visibility words are loaded a tile ahead, so their
+    // latency hides behind this tile's work
+    int kt_next = cursor.next(0);
+    uint2 vis_next = make_uint2(0u, 0u);
+    if (kMode == kModeMask) vis_next = mask_words_half(a, it.mt * kTileM + r, kt_next, hf);
     for (int j = 0; j < it.n; ++j, ++g) {
-      const int kt = cursor.next(j);
+      const int kt = kt_next;
+      const uint2 vis = vis_next;
+      if (j + 1 < it.n) {
+        kt_next = cursor.next(j + 1);
+        if (kMode == kModeMask) vis_next = mask_words_half(a, it.mt * kTileM + r, kt_next, hf);
+      }
       if (!warp_wait(&sm.s_full, g & 1, abort)) return;
       tc_fence_after();
       // this half's 64 S columns -> registers, packed in place as bf16 pairs (the score's
@@ -607,7 +658,12 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
       tmem_wait_ld(sb);
       tc_fence_before();
       mbar_arrive(&sm.s_free);   // the next S = Q K^T may overwrite S once both halves are out
-      if (tile_full<kMode>(a, it, kt)) {
+      if (kMode == kModeMask) {
+#pragma unroll
+        for (int k = 0; k < kHalfKeys / 2; ++k)
+          sb[k] = pack_bf16x2(__uint_as_float(sb[2 * k]), __uint_as_float(sb[2 * k + 1]));
+        if (!__all_sync(0xffffffffu, (vis.x & vis.y) == 0xFFFFFFFFu)) apply_mask_half(sb, vis);
+      } else if (tile_full<kMode>(a, it, kt)) {
 #pragma unroll
         for (int k = 0; k < kHalfKeys / 2; ++k)
           sb[k] = pack_bf16x2(__uint_as_float(sb[2 * k]), __uint_as_float(sb[2 * k + 1]));

@@ -86,6 +86,7 @@ int current_device(DeviceState** out) {
     } else {
       void* sw = nullptr;
       if ((e = GA_CUDA(attn_set_smem_attribute())) != cudaSuccess) return fail_cuda(e);
+      if ((e = GA_CUDA(probe_set_smem_attribute())) != cudaSuccess) return fail_cuda(e);
       if ((e = GA_CUDA(attn_upload_sigmoid_table(sigmoid_table()))) != cudaSuccess)
         return fail_cuda(e);
       if ((e = GA_CUDA(cudaGetSymbolAddress(&sw, g_device_status))) != cudaSuccess) return fail_cuda(e);
@@ -260,7 +261,7 @@ MaskedLayout masked_layout(int rows, int T) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   L.bits_off = 0;
   L.flags_off = up(L.bits_off + (size_t)L.row_tiles * kTileM * L.mask_words * 4);
-  L.stats_off = up(L.flags_off + (size_t)L.row_tiles * L.key_tiles);
+  L.stats_off = up(L.flags_off + (size_t)L.row_tiles * kMaskFlagStride);
   L.q_off = up(L.stats_off + (size_t)kHeads * rows * 2 * sizeof(float));
   L.total = up(L.q_off + (size_t)rows * kOutRow * sizeof(uint16_t));
   return L;
@@ -311,8 +312,8 @@ int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const v
   a.n_items = a.row_tiles * kHeads;
   cudaError_t e;
   if (!q_ready &&
-      (e = GA_CUDA(launch_q_prologue(a.qg, a.w_q, a.cos_tab, a.sin_tab, a.rows, a.q_base, q_prep,
-                                     s))) != cudaSuccess)
+      (e = GA_CUDA(launch_q_prologue(a.qg, a.w_q, a.cos_tab, a.sin_tab, a.rows, a.q_base, 0,
+                                     kHeads, q_prep, dev->sm_count, s))) != cudaSuccess)
     return fail_cuda(e);
   const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
   e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_g, a, grid, s));
@@ -396,7 +397,8 @@ int verify_run(const ga_bf16* qg, const VerifyCaches& c, const int* seq_len, int
     a.status = dev->status_word;
     a.rows = n * rows;
     cudaError_t e;
-    if ((e = GA_CUDA(launch_q_prologue_seq(a.qg, w_q, cos_tab, sin_tab, n * rows, sp, a.out, s))) !=
+    if ((e = GA_CUDA(launch_q_prologue_seq(a.qg, w_q, cos_tab, sin_tab, n * rows, sp, a.out,
+                                           dev->sm_count, s))) !=
         cudaSuccess)
       return fail_cuda(e);
     CUtensorMap tm_q, tm_k, tm_v;
@@ -508,7 +510,8 @@ int batch_run(const ga_bf16* qg, const BatchPiece* pieces, int n_pieces, const g
     for (int i = 0; i < a.n_entries; ++i) a.batch_entry[i] = order[i].second;
     a.n_items = a.n_entries * kHeads;
     cudaError_t e;
-    if ((e = GA_CUDA(launch_q_prologue_seq(a.qg, w_q, cos_tab, sin_tab, grp_rows, sp, a.out, s))) !=
+    if ((e = GA_CUDA(launch_q_prologue_seq(a.qg, w_q, cos_tab, sin_tab, grp_rows, sp, a.out,
+                                           dev->sm_count, s))) !=
         cudaSuccess)
       return fail_cuda(e);
     CUtensorMap tm_q, tm_g;
@@ -585,6 +588,20 @@ int ga_debug_wait_timeout(long long limit_cycles, ga_stream stream) {
   return e == cudaSuccess ? GA_OK : fail_cuda(e);
 }
 
+int ga_debug_qk_fp32(const ga_bf16* q, const ga_bf16* k, int n_tiles, float* s,
+                     ga_stream stream) {
+  if (!q || !k || !s) return GA_ERR_NULL;
+  if (n_tiles < 0) return GA_ERR_SHAPE;
+  if (n_tiles > 65535) return GA_ERR_RANGE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(s, 16)) return GA_ERR_ALIGN;
+  if (n_tiles == 0) return GA_OK;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaError_t e = GA_CUDA(launch_qk_probe(q, k, n_tiles, s, dev->status_word, (cudaStream_t)stream));
+  return e == cudaSuccess ? GA_OK : fail_cuda(e);
+}
+
 int ga_rope_table_host(int n_pos, ga_bf16* cos_out, ga_bf16* sin_out) {
   if (!cos_out || !sin_out) return GA_ERR_NULL;
   if (n_pos < 0) return GA_ERR_SHAPE;
@@ -615,7 +632,7 @@ int ga_k_prologue(const ga_bf16* k_raw, const ga_bf16* w_k, const ga_bf16* cos_t
   int st = current_device(&dev);
   if (st != GA_OK) return st;
   cudaError_t e = GA_CUDA(launch_k_prologue(k_raw, w_k, cos_tab, sin_tab, n_tok, pos_base, k_prep,
-                                            dev->status_word, (cudaStream_t)stream));
+                                            dev->sm_count, (cudaStream_t)stream));
   return e == cudaSuccess ? GA_OK : fail_cuda(e);
 }
 
@@ -633,8 +650,8 @@ int ga_q_prologue(const ga_bf16* qg, const ga_bf16* w_q, const ga_bf16* cos_tab,
   DeviceState* dev = nullptr;
   int st = current_device(&dev);
   if (st != GA_OK) return st;
-  cudaError_t e = GA_CUDA(launch_q_prologue(qg, w_q, cos_tab, sin_tab, rows, q_base, q_prep,
-                                            (cudaStream_t)stream));
+  cudaError_t e = GA_CUDA(launch_q_prologue(qg, w_q, cos_tab, sin_tab, rows, q_base, 0, kHeads,
+                                            q_prep, dev->sm_count, (cudaStream_t)stream));
   return e == cudaSuccess ? GA_OK : fail_cuda(e);
 }
 

@@ -49,6 +49,15 @@ constexpr int kVerifyMaxRows = 16;
 constexpr int kVerifyLanes = kVerifyHeadsPerTile * kVerifyMaxRows;   // 96
 constexpr int kVerifyMaxSeq = 64;       // sequences per launch (the host loops over groups)
 
+// Stored-mask bits, as the mask prepass writes them for the attention kernel. Key j of a
+// 32-key word sits at bit 8 (j % 4) + 7 - j / 4: shifted left by s = 0..7, the word holds
+// keys 4s .. 4s+3 in the top bits of its four bytes, from which one byte permute with sign
+// replication builds the 16-bit keep masks of the bf16 score pairs (4s, 4s+1) and
+// (4s+2, 4s+3).
+__host__ __device__ constexpr int mask_bit_pos(int j) { return 8 * (j & 3) + 7 - (j >> 2); }
+// Tile flags: one byte per (128-row tile, 128-key tile), rows of this many bytes.
+constexpr int kMaskFlagStride = GA_MASKED_MAX_TOKENS / kTileN;   // 64
+
 struct AttnArgs {
   const uint16_t* qg;       // [rows][24][512]
   const uint16_t* w_q;      // [256]
@@ -58,8 +67,10 @@ struct AttnArgs {
   float* row_stats;         // nullable [24][rows][2]
   uint16_t* weights;        // weights pass: [24][rows][T]
   int* hidden_rows;         // nullable
-  const uint32_t* mask_bits;  // [rows_pad][mask_words], bit j of word w <-> key 32w + j
-  const uint8_t* tile_flags;  // [row_tiles][key_tiles] (128 rows x 128 keys), 1 = a visible key
+  const uint32_t* mask_bits;  // [rows_pad][mask_words]: word w holds keys 32w .. 32w+31, key
+                              // 32w + j at bit mask_bit_pos(j)
+  const uint8_t* tile_flags;  // [row_tiles][kMaskFlagStride] (128 rows x 128 keys), 1 = a
+                              // visible key
   int* status;              // device status word
   int rows, T, q_base, mode, weights_pass;
   int row_tiles, key_tiles, mask_words;
@@ -86,9 +97,10 @@ struct AttnArgs {
 };
 
 // Launchers (defined next to their kernels). Return a cudaError_t.
+// Launchers of the prologue kernel (ga_prologue.cu); sm_count sizes its persistent grid.
 cudaError_t launch_k_prologue(const uint16_t* k_raw, const uint16_t* w_k, const uint16_t* cos_tab,
                               const uint16_t* sin_tab, int n_tok, int pos_base, uint16_t* k_prep,
-                              int* status, cudaStream_t s);
+                              int sm_count, cudaStream_t s);
 // Prepared query rows of several sequences: token t of sequence t / rows_per_seq sits at
 // position seq_base[t / rows_per_seq] + t % rows_per_seq; or, with row_start set (n_seq
 // ascending starts, row_start[n_seq] = the total), token t of the sequence b with
@@ -101,13 +113,14 @@ struct SeqPositions {
 };
 cudaError_t launch_q_prologue_seq(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
                                   const uint16_t* sin_tab, int n_tok, const SeqPositions& sp,
-                                  uint16_t* q_prep, cudaStream_t s);
+                                  uint16_t* q_prep, int sm_count, cudaStream_t s);
 // Merges the verify partials and applies the gate: out[b][rr][h*256 ..].
 cudaError_t launch_verify_combine(const AttnArgs& a, cudaStream_t s);
-// Prepared query rows: q_prep[r][h][0..255] = rope(norm(qg[r][h][0..255])) at q_base + r.
+// Prepared query rows: q_prep[r][h][0..255] = rope(norm(qg[r][h][0..255])) at q_base + r,
+// for the heads head0 .. head0+n_heads-1 (the other heads' slots are not written).
 cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
-                              const uint16_t* sin_tab, int rows, int q_base, uint16_t* q_prep,
-                              cudaStream_t s);
+                              const uint16_t* sin_tab, int rows, int q_base, int head0,
+                              int n_heads, uint16_t* q_prep, int sm_count, cudaStream_t s);
 // e4m3 cache rows: q[row][0..255] and scale[row] for n_rows rows of 256 bf16 values.
 cudaError_t launch_quantize_e4m3(const uint16_t* x, long long n_rows, uint8_t* q, float* scale,
                                  cudaStream_t s);
@@ -119,6 +132,11 @@ cudaError_t launch_select_mask(const float* scores, long long ld_scores, int row
                                int q_base, int top_k, uint8_t* mask, long long ld_mask,
                                cudaStream_t s);
 cudaError_t attn_set_smem_attribute();
+// Test hook (ga_debug.cu): fp32 tensor-core dot products of n_tiles pairs of 128 x 256 bf16
+// tiles, s[n][i][j] = q[n][i] . k[n][j].
+cudaError_t probe_set_smem_attribute();
+cudaError_t launch_qk_probe(const uint16_t* q, const uint16_t* k, int n_tiles, float* s,
+                            int* status, cudaStream_t st);
 // Test hook: a bounded wait on a barrier nothing arrives on (records a wait timeout).
 cudaError_t launch_wait_timeout(long long limit, int* status, cudaStream_t s);
 // Fills the device's table of bf16(sigmoid(g)) for every bf16 g (65536 entries, by bits).

@@ -2,10 +2,12 @@
 // sparse-attention kernel and its golden", §Semantics: the kernel consumes the selection
 // mask as given, non-zero = visible).
 //
-// Reads the uint8 mask once and writes (a) one bit per (row, key) -- bit j of word w is
-// key 32w + j -- and (b) one flag per (128-row tile, 128-key tile) that says whether any
-// key of the tile is visible to any row of the tile, so the attention kernel skips
-// all-hidden tiles without loading them. Rows >= rows and keys >= T read as hidden.
+// Reads the uint8 mask once and writes (a) one bit per (row, key) -- word w of a row holds
+// keys 32w .. 32w+31, key 32w + j at bit mask_bit_pos(j), the order in which the attention
+// kernel's softmax turns bits into score masks -- and (b) one flag per (128-row tile,
+// 128-key tile) that says whether any key of the tile is visible to any row of the tile,
+// so the attention kernel skips all-hidden tiles without loading them. Rows >= rows and
+// keys >= T read as hidden.
 #include "ga_internal.h"
 
 namespace ga {
@@ -40,8 +42,8 @@ __global__ void __launch_bounds__(128) mask_prepass_kernel(const uint8_t* __rest
       }
       uint32_t m = 0;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) m |= (b[e] != 0 ? 1u : 0u) << e;
-      w[c >> 1] |= m << (16 * (c & 1));
+      for (int e = 0; e < 16; ++e) m |= (b[e] != 0 ? 1u : 0u) << mask_bit_pos(16 * (c & 1) + e);
+      w[c >> 1] |= m;
     }
   }
   uint32_t any_bit = 0u;
@@ -52,7 +54,7 @@ __global__ void __launch_bounds__(128) mask_prepass_kernel(const uint8_t* __rest
     any_bit |= w[i];
   }
   const int any = __syncthreads_or(any_bit != 0u);
-  if (r == 0) flags[(size_t)mt * key_tiles + kt] = any ? 1 : 0;
+  if (r == 0) flags[(size_t)mt * kMaskFlagStride + kt] = any ? 1 : 0;
 }
 
 }  // namespace

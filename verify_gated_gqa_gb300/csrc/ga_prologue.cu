@@ -3,12 +3,24 @@
 // all twelve query heads of a KV head read the same prepared key; the query rows take
 // the same norm with w_q at their own positions).
 //
-// Eight lanes per (token, head) row of 256 bf16, four rows per warp. Lane j of a row holds
-// dims 32k + 4j .. 32k + 4j + 3 for k = 0..7 (eight 8-byte loads and stores; the eight
-// lanes of a row read 64 contiguous bytes per k). The rotated pairs (d, d + 32), d < 32,
-// then sit in one lane (k = 0 and k = 1), so every lane takes part in the rotation and the
-// row's sum of squares needs three shuffle steps. Keys: [T][2][256] -> [T][2][256].
-// Queries: the q halves of the fused rows [rows][24][512] -> [rows][24][256].
+// Sixteen lanes (a half-warp) per (token, head) row of 256 bf16. Lane l holds the rotated
+// pair dims 2l, 2l+1 and 32+2l, 33+2l (so both members of every RoPE pair (d, d+32) sit in
+// one lane) and the pass-through dims 64 + 64k + 4l .. +3 for k = 0..2: 16 values in five
+// loads, every load instruction of the half-warp one contiguous 64- or 128-byte run. The
+// kernel is persistent: each half-warp walks rows with a stride of all half-warps, the
+// next row's values in flight while the current one is computed.
+//
+// Exact rounding at low cost. The result must be the bf16 rounding of the exact
+// x (1 + w) / sqrt(mean(x^2) + eps). The fast path sums the squares in plain fp32 (each
+// square of a bf16 value is exact; a pairwise tree of depth 4 in the lane, then 4 shuffle
+// levels: relative error at most 8u, u = 2^-24), adds eps (u), takes rsqrtf (at most 2 ulp
+// = 4u) and forms fma(x, w, x) * r (two roundings): in all at most 10.5u relative, which is
+// under 10.5 fp32 ulps of the result. A result whose low 16 bits lie more than 12 ulps from
+// the bf16 midpoint 0x8000 therefore rounds to the bf16 value of the exact result. Rows
+// with an element inside that margin (about one in ten) take the exact path for those
+// elements: the sum of squares as a TwoSum pair, the inverse RMS as a double-float, and a
+// double-float product (ga_numerics.cuh), the same arithmetic as before this kernel took
+// the fast path first.
 #include "ga_internal.h"
 #include "ga_numerics.cuh"
 #include "ga_sm100.cuh"
@@ -18,32 +30,66 @@ namespace {
 
 __device__ __forceinline__ float lo_f(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float hi_f(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-  return (uint32_t)bf16_bits(a) | ((uint32_t)bf16_bits(b) << 16);
+
+constexpr int kThreads = 256;          // 16 half-warps, one row each at a time
+constexpr int kBlocksPerSm = 3;
+constexpr int kFastMargin = 12;        // fp32 ulps around a bf16 midpoint (see above)
+
+// The 16 values of a lane: words 0 and 1 hold dims (2l, 2l+1) and (32+2l, 33+2l); words
+// 2..7 the pass-through dims, two bf16 per word, in the order of the loads.
+struct RowVals {
+  uint32_t w[8];
+};
+
+__device__ __forceinline__ void load_row(const uint16_t* p, int l, RowVals& v) {
+  v.w[0] = __ldg(reinterpret_cast<const uint32_t*>(p) + l);
+  v.w[1] = __ldg(reinterpret_cast<const uint32_t*>(p + 32) + l);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const uint2 t = __ldg(reinterpret_cast<const uint2*>(p + 64 + 64 * k) + l);
+    v.w[2 + 2 * k] = t.x;
+    v.w[3 + 2 * k] = t.y;
+  }
 }
 
-// rows are (token, head) pairs, heads_per_tok heads per token; row `row` reads 256 values
-// at src + row * src_stride and writes 256 at dst + row * 256. Token t sits at position
-// pos_base + t, or, with kSeq, at sp.seq_base[t / sp.rows_per_seq] + t % sp.rows_per_seq.
-constexpr int kRowsPerBlock = 32;   // 8 warps x 4 rows
+// Rows are (token, head) pairs over n_heads heads head0 .. head0+n_heads-1 of a token that
+// has heads_per_tok heads: row r is token r / n_heads, head head0 + r % n_heads; it reads 256
+// values at src + (token * heads_per_tok + head) * src_stride and writes 256 at dst +
+// (token * heads_per_tok + head) * 256. Token t sits at position pos_base + t, or, with kSeq,
+// at the position its sequence gives (SeqPositions).
 template <bool kSeq>
-__global__ void __launch_bounds__(256) prologue_kernel(const uint16_t* __restrict__ src,
-                                                       int src_stride, int heads_per_tok,
-                                                       const uint16_t* __restrict__ w_norm,
-                                                       const uint16_t* __restrict__ cos_tab,
-                                                       const uint16_t* __restrict__ sin_tab,
-                                                       long long n_rows, int pos_base,
-                                                       const __grid_constant__ SeqPositions sp,
-                                                       uint16_t* __restrict__ dst) {
-  const int lane = threadIdx.x & 31;
-  const int j = lane & 7;
-  const long long row = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 3);
-  // whole row groups leave together: the shuffles below stay within a group of 8 lanes
-  if (row >= n_rows) return;
-  const unsigned gmask = 0xFFu << (lane & 24);
-  const long long tok = row / heads_per_tok;
-  int pos = pos_base + (int)tok;
-  if (kSeq) {
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm)
+    prologue_kernel(const uint16_t* __restrict__ src, int src_stride, int heads_per_tok,
+                    int head0, int n_heads, const uint16_t* __restrict__ w_norm,
+                    const uint16_t* __restrict__ cos_tab, const uint16_t* __restrict__ sin_tab,
+                    long long n_rows, int pos_base, const __grid_constant__ SeqPositions sp,
+                    uint16_t* __restrict__ dst) {
+  const int l = threadIdx.x & 15;
+  const unsigned hmask = 0xFFFFu << (threadIdx.x & 16);   // this half-warp's lanes
+  const long long stride = (long long)gridDim.x * (kThreads / 16);
+  long long row = (long long)blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
+  if (row >= n_rows) return;   // whole half-warps leave together
+
+  // this lane's norm weights, in the value order of RowVals
+  float w[16];
+  {
+    RowVals wv;
+    load_row(w_norm, l, wv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      w[2 * i] = lo_f(wv.w[i]);
+      w[2 * i + 1] = hi_f(wv.w[i]);
+    }
+  }
+  // element offset of row r in an array of rows stride_el values apart
+  auto row_off = [&](long long r, int stride_el) -> long long {
+    const long long tok = r / n_heads;
+    const int head = head0 + (int)(r - tok * n_heads);
+    return (tok * heads_per_tok + head) * (long long)stride_el;
+  };
+  auto position = [&](long long r) -> int {
+    const long long tok = r / n_heads;
+    if (!kSeq) return pos_base + (int)tok;
     if (sp.n_seq > 0) {
       // the sequence holding packed token tok: the last b with row_start[b] <= tok
       int lo = 0, hi = sp.n_seq - 1;
@@ -52,116 +98,129 @@ __global__ void __launch_bounds__(256) prologue_kernel(const uint16_t* __restric
         if (sp.row_start[mid] <= tok) lo = mid;
         else hi = mid - 1;
       }
-      pos = sp.seq_base[lo] + (int)(tok - sp.row_start[lo]);
-    } else {
-      pos = sp.seq_base[tok / sp.rows_per_seq] + (int)(tok % sp.rows_per_seq);
+      return sp.seq_base[lo] + (int)(tok - sp.row_start[lo]);
     }
-  }
-
-  const uint2* xs = reinterpret_cast<const uint2*>(src + row * src_stride) + j;
-  const uint2* ws = reinterpret_cast<const uint2*>(w_norm) + j;
-  uint2 xv[8], wv[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    xv[k] = __ldg(xs + 8 * k);
-    wv[k] = __ldg(ws + 8 * k);
-  }
-  // sum of squares: two independent TwoSum chains per lane, then the row's 8 lanes in a
-  // fixed order (lower lane first) so every lane of the row holds the same pair
-  SumSq s0, s1;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    s0.add(lo_f(xv[k].x));
-    s1.add(hi_f(xv[k].x));
-    s0.add(lo_f(xv[k].y));
-    s1.add(hi_f(xv[k].y));
-  }
-  s0.merge(s1);
-  SumSq ss = s0;
-#pragma unroll
-  for (int off = 1; off < 8; off <<= 1) {
-    SumSq o;
-    o.hi = __shfl_xor_sync(gmask, ss.hi, off, 8);
-    o.lo = __shfl_xor_sync(gmask, ss.lo, off, 8);
-    if (j & off) {
-      SumSq t = o;
-      t.merge(ss);
-      ss = t;
-    } else {
-      ss.merge(o);
-    }
-  }
-  const InvRms r = inv_rms_df(ss);
-
-  // normed values (fp32 values whose bf16 rounding is the exact one: the fast result when
-  // it is clear of a bf16 midpoint, else the exact bf16 value itself)
-  auto norm4 = [&](int k, float (&y)[4]) {
-    const float xk[4] = {lo_f(xv[k].x), hi_f(xv[k].x), lo_f(xv[k].y), hi_f(xv[k].y)};
-    const float wk[4] = {lo_f(wv[k].x), hi_f(wv[k].x), lo_f(wv[k].y), hi_f(wv[k].y)};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      y[i] = norm_fast(xk[i], wk[i], r);
-      if (near_bf16_midpoint(y[i], 3)) y[i] = norm_elem_exact(xk[i], wk[i], r.h, r.l);
-    }
+    return sp.seq_base[tok / sp.rows_per_seq] + (int)(tok % sp.rows_per_seq);
   };
-  uint2* out = reinterpret_cast<uint2*>(dst + row * kDim) + j;
-  {
-    // Partial RoPE on dims 0..63: pair p = 4j + i is (dim p, dim p + 32), both in this lane.
-    float ya[4], yb[4];
-    norm4(0, ya);
-    norm4(1, yb);
-    const uint2 cv = __ldg(reinterpret_cast<const uint2*>(cos_tab + (long long)pos * kHalfRot) + j);
-    const uint2 sv = __ldg(reinterpret_cast<const uint2*>(sin_tab + (long long)pos * kHalfRot) + j);
-    const float c[4] = {lo_f(cv.x), hi_f(cv.x), lo_f(cv.y), hi_f(cv.y)};
-    const float sn[4] = {lo_f(sv.x), hi_f(sv.x), lo_f(sv.y), hi_f(sv.y)};
+
+  RowVals cur;
+  load_row(src + row_off(row, src_stride), l, cur);
+  while (true) {
+    const long long next = row + stride;
+    RowVals nxt;
+    if (next < n_rows) load_row(src + row_off(next, src_stride), l, nxt);
+    const int pos = position(row);
+    const uint32_t cw = __ldg(reinterpret_cast<const uint32_t*>(cos_tab + (long long)pos * kHalfRot) + l);
+    const uint32_t sw = __ldg(reinterpret_cast<const uint32_t*>(sin_tab + (long long)pos * kHalfRot) + l);
+
+    float x[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float oa, ob;
-      rope_pair(bf16_round(ya[i]), bf16_round(yb[i]), c[i], sn[i], oa, ob);
-      ya[i] = oa;
-      yb[i] = ob;
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = lo_f(cur.w[i]);
+      x[2 * i + 1] = hi_f(cur.w[i]);
     }
-    out[0] = make_uint2(pack2(ya[0], ya[1]), pack2(ya[2], ya[3]));
-    out[8] = make_uint2(pack2(yb[0], yb[1]), pack2(yb[2], yb[3]));
-  }
+    // fast sum of squares: pairs by one fma (the second square is exact), then a tree
+    float t8[8];
 #pragma unroll
-  for (int k = 2; k < 8; ++k) {
-    float y[4];
-    norm4(k, y);
-    out[8 * k] = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+    for (int i = 0; i < 8; ++i) t8[i] = fmaf(x[2 * i], x[2 * i], x[2 * i + 1] * x[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) t8[i] = t8[2 * i] + t8[2 * i + 1];
+    t8[0] = t8[0] + t8[1];
+    t8[2] = t8[2] + t8[3];
+    float ssum = t8[0] + t8[2];
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) ssum += __shfl_xor_sync(hmask, ssum, off, 16);
+    const float rf = rsqrtf(fmaf(ssum, 1.0f / 256.0f, kEps));
+
+    float y[16];
+    uint32_t near = 0u;   // bit i: value i lies within the margin of a bf16 midpoint
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      y[i] = fmaf(x[i], w[i], x[i]) * rf;
+      if (near_bf16_midpoint(y[i], kFastMargin)) near |= 1u << i;
+    }
+    if (__any_sync(hmask, near != 0u)) {
+      // exact path for this row: the sum of squares as a TwoSum pair, combined over the
+      // row's 16 lanes in a fixed order (lower lane first) so every lane holds the same pair
+      SumSq s0, s1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        s0.add(x[2 * i]);
+        s1.add(x[2 * i + 1]);
+      }
+      s0.merge(s1);
+      SumSq ss = s0;
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) {
+        SumSq o;
+        o.hi = __shfl_xor_sync(hmask, ss.hi, off, 16);
+        o.lo = __shfl_xor_sync(hmask, ss.lo, off, 16);
+        if (l & off) {
+          SumSq t = o;
+          t.merge(ss);
+          ss = t;
+        } else {
+          ss.merge(o);
+        }
+      }
+      const InvRms r = inv_rms_df(ss);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if ((near >> i) & 1u) y[i] = norm_elem_exact(x[i], w[i], r.h, r.l);
+    }
+
+    // partial RoPE: values 0, 1 are dims 2l, 2l+1 (a) and 2, 3 are dims 32+2l, 33+2l (b)
+    float oa0, ob0, oa1, ob1;
+    rope_pair(bf16_round(y[0]), bf16_round(y[2]), lo_f(cw), lo_f(sw), oa0, ob0);
+    rope_pair(bf16_round(y[1]), bf16_round(y[3]), hi_f(cw), hi_f(sw), oa1, ob1);
+    uint16_t* out = dst + row_off(row, kDim);
+    reinterpret_cast<uint32_t*>(out)[l] = pack_bf16x2(oa0, oa1);
+    reinterpret_cast<uint32_t*>(out + 32)[l] = pack_bf16x2(ob0, ob1);
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+      reinterpret_cast<uint2*>(out + 64 + 64 * k)[l] =
+          make_uint2(pack_bf16x2(y[4 + 4 * k], y[5 + 4 * k]), pack_bf16x2(y[6 + 4 * k], y[7 + 4 * k]));
+
+    if (next >= n_rows) break;
+    row = next;
+    cur = nxt;
   }
+}
+
+unsigned prologue_grid(long long n_rows, int sm_count) {
+  const long long need = (n_rows + kThreads / 16 - 1) / (kThreads / 16);
+  const long long cap = (long long)(sm_count > 0 ? sm_count : 1) * kBlocksPerSm;
+  return (unsigned)(need < cap ? need : cap);
 }
 
 }  // namespace
 
 cudaError_t launch_k_prologue(const uint16_t* k_raw, const uint16_t* w_k, const uint16_t* cos_tab,
                               const uint16_t* sin_tab, int n_tok, int pos_base, uint16_t* k_prep,
-                              int* status, cudaStream_t s) {
-  (void)status;
+                              int sm_count, cudaStream_t s) {
   const long long n_rows = (long long)n_tok * kKvHeads;
-  const unsigned grid = (unsigned)((n_rows + kRowsPerBlock - 1) / kRowsPerBlock);
-  prologue_kernel<false><<<grid, 256, 0, s>>>(k_raw, kDim, kKvHeads, w_k, cos_tab, sin_tab,
-                                              n_rows, pos_base, SeqPositions{}, k_prep);
+  prologue_kernel<false><<<prologue_grid(n_rows, sm_count), kThreads, 0, s>>>(
+      k_raw, kDim, kKvHeads, 0, kKvHeads, w_k, cos_tab, sin_tab, n_rows, pos_base,
+      SeqPositions{}, k_prep);
   return cudaGetLastError();
 }
 
 cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
-                              const uint16_t* sin_tab, int rows, int q_base, uint16_t* q_prep,
-                              cudaStream_t s) {
-  const long long n_rows = (long long)rows * kHeads;
-  const unsigned grid = (unsigned)((n_rows + kRowsPerBlock - 1) / kRowsPerBlock);
-  prologue_kernel<false><<<grid, 256, 0, s>>>(qg, kQgStride, kHeads, w_q, cos_tab, sin_tab,
-                                              n_rows, q_base, SeqPositions{}, q_prep);
+                              const uint16_t* sin_tab, int rows, int q_base, int head0,
+                              int n_heads, uint16_t* q_prep, int sm_count, cudaStream_t s) {
+  const long long n_rows = (long long)rows * n_heads;
+  prologue_kernel<false><<<prologue_grid(n_rows, sm_count), kThreads, 0, s>>>(
+      qg, kQgStride, kHeads, head0, n_heads, w_q, cos_tab, sin_tab, n_rows, q_base,
+      SeqPositions{}, q_prep);
   return cudaGetLastError();
 }
 
 cudaError_t launch_q_prologue_seq(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
                                   const uint16_t* sin_tab, int n_tok, const SeqPositions& sp,
-                                  uint16_t* q_prep, cudaStream_t s) {
+                                  uint16_t* q_prep, int sm_count, cudaStream_t s) {
   const long long n_rows = (long long)n_tok * kHeads;
-  const unsigned grid = (unsigned)((n_rows + kRowsPerBlock - 1) / kRowsPerBlock);
-  prologue_kernel<true><<<grid, 256, 0, s>>>(qg, kQgStride, kHeads, w_q, cos_tab, sin_tab, n_rows,
-                                             0, sp, q_prep);
+  prologue_kernel<true><<<prologue_grid(n_rows, sm_count), kThreads, 0, s>>>(
+      qg, kQgStride, kHeads, 0, kHeads, w_q, cos_tab, sin_tab, n_rows, 0, sp, q_prep);
   return cudaGetLastError();
 }
 
