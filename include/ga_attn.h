@@ -189,6 +189,22 @@ int ga_attn_prefill(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
                     int table_rows, int rows, int T, int q_base, int causal, ga_bf16* out,
                     float* row_stats, ga_stream stream);
 
+/* ga_attn_prefill for one group of KV heads: the query heads 12 * kv_first ..
+ * 12 * (kv_first + kv_count) - 1 (each KV head with the 12 query heads that read it) and
+ * nothing else. This is how the pass shards over GPUs with no exchange between them: GPU g
+ * takes KV head g, reads only that head's keys and values and its query heads' halves of the
+ * fused rows, and writes only their output columns h * 256 .. h * 256 + 255; the other
+ * columns of out (and of row_stats) are left as they were. The results are the bits of
+ * ga_attn_prefill in those columns.
+ *   kv_first, kv_count: 0 <= kv_first, 1 <= kv_count, kv_first + kv_count <= 2
+ *   every other argument as in ga_attn_prefill (out doubles as scratch only in the columns
+ *   of the heads processed)
+ * Errors: as ga_attn_prefill (RANGE also for the KV-head group). */
+int ga_attn_prefill_kv(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                       const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                       int table_rows, int rows, int T, int q_base, int causal, int kv_first,
+                       int kv_count, ga_bf16* out, float* row_stats, ga_stream stream);
+
 /* ga_attn_prefill from prepared queries (ga_q_prologue's output): the attention kernel
  * alone. qg still supplies the gates (its last 256 values per head).
  *   q_prep  [rows][24][256]  prepared queries; may be the same buffer as out (each
@@ -222,6 +238,20 @@ int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
                    int table_rows, int rows, int T, int q_base, const uint8_t* mask,
                    long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
                    void* workspace, size_t ws_bytes, ga_stream stream);
+
+/* ga_attn_masked for one group of KV heads (see ga_attn_prefill_kv): the query heads
+ * 12 * kv_first .. 12 * (kv_first + kv_count) - 1 only. Their output columns (and, when
+ * weights is given, their [12 * kv_count][rows][T] slice of weights, zeroed first) are
+ * written; everything else is left as it was. hidden_rows counts each hidden row once.
+ *   kv_first, kv_count: 0 <= kv_first, 1 <= kv_count, kv_first + kv_count <= 2
+ *   every other argument as in ga_attn_masked
+ * Errors: as ga_attn_masked (RANGE also for the KV-head group). */
+int ga_attn_masked_kv(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                      const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                      int table_rows, int rows, int T, int q_base, const uint8_t* mask,
+                      long long ld_mask, int kv_first, int kv_count, ga_bf16* out,
+                      ga_bf16* weights, int* hidden_rows, void* workspace, size_t ws_bytes,
+                      ga_stream stream);
 
 /* ga_attn_masked from prepared queries (ga_q_prologue's output): the mask prepass and the
  * attention kernel (and the weights pass) without the query prologue, exposed so that a

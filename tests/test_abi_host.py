@@ -336,6 +336,24 @@ def test_masked_prepared_refusals(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def test_kv_group_refusals(L):
+    before = L.ga_debug_cuda_calls()
+    P = L.ga_attn_prefill_kv
+    for first, count in [(-1, 1), (0, 0), (1, 2), (2, 1), (0, 3)]:
+        assert P(A, A, A, A, A, A, 100, 10, 100, 0, 1, first, count, A, None, S) == -4
+    assert P(None, A, A, A, A, A, 100, 10, 100, 0, 1, 0, 1, A, None, S) == -1
+    assert P(A, A, A, A, A, A, 100, 0, 100, 0, 1, 1, 1, A, None, S) == 0          # no-op
+    M = L.ga_attn_masked_kv
+    wsb = L.ga_masked_workspace_bytes(10, 100)
+    W = 0x20000
+    for first, count in [(-1, 1), (0, 0), (1, 2)]:
+        assert M(A, A, A, A, A, A, 100, 10, 100, 0, A, 112, first, count, A, None, None, W, wsb,
+                 S) == -4
+    assert M(A, A, A, A, A, A, 100, 10, 100, 0, A, 112, 1, 1, A, None, None, W, wsb - 1, S) == -6
+    assert M(A, A, A, A, A, A, 100, 0, 100, 0, A, 112, 1, 1, A, None, None, W, wsb, S) == 0
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_qk_probe_refusals(L):
     before = L.ga_debug_cuda_calls()
     assert L.ga_debug_qk_fp32(None, A, 1, A, S) == -1

@@ -43,6 +43,9 @@ _SIGS = {
     "ga_debug_qk_fp32": (_I, [_P, _P, _I, _P, _P]),
     "ga_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "ga_attn_prefill_prepared": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "ga_attn_prefill_kv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "ga_attn_masked_kv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _LL, _I, _I, _P, _P,
+                               _P, _P, _SZ, _P]),
     "ga_attn_masked_static": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _LL, _P, _P, _P,
                                    _P]),
     "ga_masked_workspace_bytes": (_SZ, [_I, _I]),
@@ -198,7 +201,9 @@ def ga_attn_prefill_prepared(q_prep, qg, k_prep, v, q_base=0, T=None, causal=Tru
 
 
 def ga_attn_prefill(qg, k_prep, v, w_q, cos_tab, sin_tab, q_base=0, T=None, causal=True,
-                    out=None, row_stats=None):
+                    out=None, row_stats=None, kv=None):
+    """kv = (kv_first, kv_count) runs ga_attn_prefill_kv: only the query heads of those KV
+    heads, whose output columns alone are written."""
     rows = qg.shape[0]
     T = k_prep.shape[0] if T is None else T
     if out is None:
@@ -206,10 +211,14 @@ def ga_attn_prefill(qg, k_prep, v, w_q, cos_tab, sin_tab, q_base=0, T=None, caus
     for n, t in (("qg", qg), ("k_prep", k_prep), ("v", v), ("w_q", w_q), ("cos_tab", cos_tab),
                  ("sin_tab", sin_tab), ("out", out)):
         _bf16_cuda(n, t)
-    _check(lib().ga_attn_prefill(_ptr(qg), _ptr(k_prep), _ptr(v), _ptr(w_q), _ptr(cos_tab),
-                                 _ptr(sin_tab), cos_tab.shape[0], rows, T, q_base,
-                                 1 if causal else 0, _ptr(out), _ptr(row_stats), _stream()),
-           "ga_attn_prefill")
+    args = (_ptr(qg), _ptr(k_prep), _ptr(v), _ptr(w_q), _ptr(cos_tab), _ptr(sin_tab),
+            cos_tab.shape[0], rows, T, q_base, 1 if causal else 0)
+    tail = (_ptr(out), _ptr(row_stats), _stream())
+    if kv is None:
+        _check(lib().ga_attn_prefill(*args, *tail), "ga_attn_prefill")
+    else:
+        _check(lib().ga_attn_prefill_kv(*args, int(kv[0]), int(kv[1]), *tail),
+               "ga_attn_prefill_kv")
     return out
 
 
@@ -219,8 +228,9 @@ def ga_masked_workspace_bytes(rows: int, T: int) -> int:
 
 def ga_attn_masked(qg, k_prep, v, w_q, cos_tab, sin_tab, mask, q_base=0, T=None,
                    want_weights=False, out=None, weights=None, hidden_rows=None,
-                   workspace=None):
-    """Returns (out, weights or None, hidden_rows int32 device tensor [1])."""
+                   workspace=None, kv=None):
+    """Returns (out, weights or None, hidden_rows int32 device tensor [1]). kv =
+    (kv_first, kv_count) runs ga_attn_masked_kv (those KV heads' query heads only)."""
     rows = qg.shape[0]
     T = k_prep.shape[0] if T is None else T
     dev = qg.device
@@ -238,11 +248,14 @@ def ga_attn_masked(qg, k_prep, v, w_q, cos_tab, sin_tab, mask, q_base=0, T=None,
     for n, t in (("qg", qg), ("k_prep", k_prep), ("v", v), ("w_q", w_q), ("cos_tab", cos_tab),
                  ("sin_tab", sin_tab), ("out", out)):
         _bf16_cuda(n, t)
-    _check(lib().ga_attn_masked(_ptr(qg), _ptr(k_prep), _ptr(v), _ptr(w_q), _ptr(cos_tab),
-                                _ptr(sin_tab), cos_tab.shape[0], rows, T, q_base, _ptr(mask),
-                                mask.stride(0), _ptr(out), _ptr(weights), _ptr(hidden_rows),
-                                _ptr(workspace), workspace.numel(), _stream()),
-           "ga_attn_masked")
+    head = (_ptr(qg), _ptr(k_prep), _ptr(v), _ptr(w_q), _ptr(cos_tab), _ptr(sin_tab),
+            cos_tab.shape[0], rows, T, q_base, _ptr(mask), mask.stride(0))
+    tail = (_ptr(out), _ptr(weights), _ptr(hidden_rows), _ptr(workspace), workspace.numel(),
+            _stream())
+    if kv is None:
+        _check(lib().ga_attn_masked(*head, *tail), "ga_attn_masked")
+    else:
+        _check(lib().ga_attn_masked_kv(*head, int(kv[0]), int(kv[1]), *tail), "ga_attn_masked_kv")
     return out, weights, hidden_rows
 
 

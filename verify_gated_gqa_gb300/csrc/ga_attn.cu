@@ -171,8 +171,8 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
     it.n = max(0, min(a.chunk_tiles, tiles - it.kt0));
     return it;
   }
-  it.mt = a.row_tiles - 1 - idx / kHeads;  // later row tiles see more keys: longest first
-  it.h = idx % kHeads;
+  it.mt = a.row_tiles - 1 - idx / a.n_heads;  // later row tiles see more keys: longest first
+  it.h = a.head0 + idx % a.n_heads;
   if (kMode == kModeCausal) {
     const int last_row = min(a.rows, (it.mt + 1) * kTileM) - 1;
     const int key_end = min(a.T, a.q_base + last_row + 1);
@@ -864,7 +864,7 @@ __device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r, bool
     a.row_stats[((size_t)it.h * a.rows + row) * 2] = 0.f;
     a.row_stats[((size_t)it.h * a.rows + row) * 2 + 1] = 0.f;
   }
-  if (a.hidden_rows && it.h == 0) atomicAdd(a.hidden_rows, 1);
+  if (a.hidden_rows && it.h == a.head0) atomicAdd(a.hidden_rows, 1);
 }
 
 // Gated epilogue of one finished item: out = bf16(bf16(O / l) * s) with s = bf16(sigmoid(
@@ -928,7 +928,7 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
     a.row_stats[((size_t)h * a.rows + row) * 2] = M;
     a.row_stats[((size_t)h * a.rows + row) * 2 + 1] = l;
   }
-  if (a.hidden_rows && h == 0 && l == 0.f) atomicAdd(a.hidden_rows, 1);
+  if (a.hidden_rows && h == a.head0 && l == 0.f) atomicAdd(a.hidden_rows, 1);
   return true;
 }
 

@@ -308,12 +308,16 @@ int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const v
   if (st != GA_OK) return st;
   AttnArgs a = a0;
   a.status = dev->status_word;
+  if (a.n_heads == 0) {   // every query head unless the caller chose a KV-head group
+    a.head0 = 0;
+    a.n_heads = kHeads;
+  }
   a.row_tiles = (a.rows + kTileM - 1) / kTileM;
-  a.n_items = a.row_tiles * kHeads;
+  a.n_items = a.row_tiles * a.n_heads;
   cudaError_t e;
   if (!q_ready &&
-      (e = GA_CUDA(launch_q_prologue(a.qg, a.w_q, a.cos_tab, a.sin_tab, a.rows, a.q_base, 0,
-                                     kHeads, q_prep, dev->sm_count, s))) != cudaSuccess)
+      (e = GA_CUDA(launch_q_prologue(a.qg, a.w_q, a.cos_tab, a.sin_tab, a.rows, a.q_base, a.head0,
+                                     a.n_heads, q_prep, dev->sm_count, s))) != cudaSuccess)
     return fail_cuda(e);
   const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
   e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_g, a, grid, s));
@@ -680,15 +684,16 @@ int ga_attn_prefill_prepared(const ga_bf16* q_prep, const ga_bf16* qg, const ga_
                           (cudaStream_t)stream);
 }
 
-int ga_attn_prefill(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
-                    const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
-                    int table_rows, int rows, int T, int q_base, int causal, ga_bf16* out,
-                    float* row_stats, ga_stream stream) {
+int ga_attn_prefill_kv(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                       const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                       int table_rows, int rows, int T, int q_base, int causal, int kv_first,
+                       int kv_count, ga_bf16* out, float* row_stats, ga_stream stream) {
   int st = check_attention_args(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T,
                                 q_base, out);
   if (st != GA_OK) return st;
   if (causal != 0 && causal != 1) return GA_ERR_RANGE;
   if (!causal && q_base != 0) return GA_ERR_RANGE;  // bidirectional passes start at 0
+  if (kv_first < 0 || kv_count < 1 || kv_first + kv_count > kKvHeads) return GA_ERR_RANGE;
   if (row_stats && !aligned(row_stats, 4)) return GA_ERR_ALIGN;
   if (rows == 0) return GA_OK;
   DeviceState* dev = nullptr;
@@ -699,7 +704,17 @@ int ga_attn_prefill(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
   a.out = out; a.row_stats = row_stats;
   a.rows = rows; a.T = T; a.q_base = q_base;
   a.mode = causal ? kModeCausal : kModeBidir;
+  a.head0 = kv_first * kGroup;
+  a.n_heads = kv_count * kGroup;
   return launch_attention(a, out, false, k_prep, v, T, dev, (cudaStream_t)stream);
+}
+
+int ga_attn_prefill(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                    const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                    int table_rows, int rows, int T, int q_base, int causal, ga_bf16* out,
+                    float* row_stats, ga_stream stream) {
+  return ga_attn_prefill_kv(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base,
+                            causal, 0, kKvHeads, out, row_stats, stream);
 }
 
 size_t ga_masked_workspace_bytes(int rows, int T) {
@@ -743,8 +758,8 @@ namespace {
 int masked_run(const ga_bf16* q_prep_in, const ga_bf16* qg, const ga_bf16* k_prep,
                const ga_bf16* v, const ga_bf16* w_q, const ga_bf16* cos_tab,
                const ga_bf16* sin_tab, int rows, int T, int q_base, const uint8_t* mask,
-               long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
-               void* workspace, ga_stream stream) {
+               long long ld_mask, int kv_first, int kv_count, ga_bf16* out, ga_bf16* weights,
+               int* hidden_rows, void* workspace, ga_stream stream) {
   DeviceState* dev = nullptr;
   int st = current_device(&dev);
   if (st != GA_OK) return st;
@@ -768,9 +783,14 @@ int masked_run(const ga_bf16* q_prep_in, const ga_bf16* qg, const ga_bf16* k_pre
   a.mask_bits = bits; a.tile_flags = flags;
   a.key_tiles = L.key_tiles; a.mask_words = L.mask_words;
   a.rows = rows; a.T = T; a.q_base = q_base; a.mode = kModeMask;
+  a.head0 = kv_first * kGroup;
+  a.n_heads = kv_count * kGroup;
   st = launch_attention(a, q_prep, q_prep_in != nullptr, k_prep, v, T, dev, s);
   if (st != GA_OK || !weights) return st;
-  if ((e = GA_CUDA(cudaMemsetAsync(weights, 0, (size_t)kHeads * rows * T * sizeof(uint16_t), s))) != cudaSuccess)
+  // the weights of the heads processed: zero first (hidden keys stay 0), then the pass
+  const size_t head_elems = (size_t)rows * T;
+  if ((e = GA_CUDA(cudaMemsetAsync(weights + (size_t)a.head0 * head_elems, 0,
+                                   (size_t)a.n_heads * head_elems * sizeof(uint16_t), s))) != cudaSuccess)
     return fail_cuda(e);
   a.weights = weights;
   a.weights_pass = 1;
@@ -782,19 +802,31 @@ int masked_run(const ga_bf16* q_prep_in, const ga_bf16* qg, const ga_bf16* k_pre
 
 extern "C" {
 
+int ga_attn_masked_kv(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
+                      const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                      int table_rows, int rows, int T, int q_base, const uint8_t* mask,
+                      long long ld_mask, int kv_first, int kv_count, ga_bf16* out,
+                      ga_bf16* weights, int* hidden_rows, void* workspace, size_t ws_bytes,
+                      ga_stream stream) {
+  int st = masked_check_args(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base,
+                             mask, ld_mask, out, weights, hidden_rows);
+  if (st != GA_OK) return st;
+  if (kv_first < 0 || kv_count < 1 || kv_first + kv_count > kKvHeads) return GA_ERR_RANGE;
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < masked_layout(rows, T).total)
+    return GA_ERR_WORKSPACE;
+  if (rows == 0) return GA_OK;
+  return masked_run(nullptr, qg, k_prep, v, w_q, cos_tab, sin_tab, rows, T, q_base, mask,
+                    ld_mask, kv_first, kv_count, out, weights, hidden_rows, workspace, stream);
+}
+
 int ga_attn_masked(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf16* v,
                    const ga_bf16* w_q, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
                    int table_rows, int rows, int T, int q_base, const uint8_t* mask,
                    long long ld_mask, ga_bf16* out, ga_bf16* weights, int* hidden_rows,
                    void* workspace, size_t ws_bytes, ga_stream stream) {
-  int st = masked_check_args(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base,
-                             mask, ld_mask, out, weights, hidden_rows);
-  if (st != GA_OK) return st;
-  if (!workspace || !aligned(workspace, 256) || ws_bytes < masked_layout(rows, T).total)
-    return GA_ERR_WORKSPACE;
-  if (rows == 0) return GA_OK;
-  return masked_run(nullptr, qg, k_prep, v, w_q, cos_tab, sin_tab, rows, T, q_base, mask,
-                    ld_mask, out, weights, hidden_rows, workspace, stream);
+  return ga_attn_masked_kv(qg, k_prep, v, w_q, cos_tab, sin_tab, table_rows, rows, T, q_base,
+                           mask, ld_mask, 0, kKvHeads, out, weights, hidden_rows, workspace,
+                           ws_bytes, stream);
 }
 
 int ga_attn_masked_prepared(const ga_bf16* q_prep, const ga_bf16* qg, const ga_bf16* k_prep,
@@ -812,7 +844,7 @@ int ga_attn_masked_prepared(const ga_bf16* q_prep, const ga_bf16* qg, const ga_b
     return GA_ERR_WORKSPACE;
   if (rows == 0) return GA_OK;
   return masked_run(q_prep, qg, k_prep, v, nullptr, nullptr, nullptr, rows, T, q_base, mask,
-                    ld_mask, out, weights, hidden_rows, workspace, stream);
+                    ld_mask, 0, kKvHeads, out, weights, hidden_rows, workspace, stream);
 }
 
 size_t ga_verify_workspace_bytes(int n_seq, int rows, int max_len) {
@@ -1066,7 +1098,7 @@ int ga_attn_masked_static(const ga_bf16* qg, const ga_bf16* k_prep, const ga_bf1
     scratch = g_static_scratch_ptr[dev];
   }
   return masked_run(nullptr, qg, k_prep, v, w_q, cos_tab, sin_tab, rows, T, q_base, mask,
-                    ld_mask, out, weights, hidden_rows, scratch, stream);
+                    ld_mask, 0, kKvHeads, out, weights, hidden_rows, scratch, stream);
 }
 
 }  // extern "C"

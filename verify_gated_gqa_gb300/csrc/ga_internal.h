@@ -73,6 +73,7 @@ struct AttnArgs {
                               // visible key
   int* status;              // device status word
   int rows, T, q_base, mode, weights_pass;
+  int head0, n_heads;       // causal, bidirectional, stored mask: the query heads processed
   int row_tiles, key_tiles, mask_words;
   int n_items;
   // verify mode
