@@ -338,6 +338,28 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
       const int outer = kv_at(kt, r0);
       return load_tile(tm_v, true, kvh, r0, outer, kTileBytes);
     };
+    // The next item's prepared Q tile and gate tile go into L2 a few key tiles before this
+    // item ends (the ring can take the Q tile only once this item's last K tile is used,
+    // and from DRAM it would arrive late): its first Q K^T then waits for an L2 read.
+    Item nx;
+    bool prefetch_next = false;
+    if (!is_verify<kMode>() && kMode != kModeBatch) {
+      ItemWalk<kMode> peek = walk;
+      prefetch_next = peek.next(a, nx);
+    }
+    const int prefetch_at = it.n > 4 ? it.n - 4 : 1;
+    auto prefetch = [&](int j) {
+      if (!prefetch_next || j != prefetch_at) return;
+      if (lane == 0) {
+        const int r0 = nx.row0 + nx.mt * kTileM;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tma_prefetch_l2_3d(tm_q, c * 64, nx.h, r0);
+          if (has_gate<kMode, kW>()) tma_prefetch_l2_3d(tm_g, kDim + c * 64, nx.h, r0);
+        }
+      }
+      __syncwarp();
+    };
     // Ring order: the item's prepared Q (for the edge warps), then in MMA order K0,
     // (K_j, V_{j-1}) for j >= 1, V_{n-1}; the gate tile (gated passes) just before V_0.
     if (is_verify<kMode>()) {
@@ -351,7 +373,9 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
              load_tile(tm_g, false, it.h, it.row0 + it.mt * kTileM, -1, kTileBytes, kDim);
     };
     if (!load_k(ck.next(0))) return;
+    if (it.n == 1) prefetch(1);
     for (int j = 1; j < it.n; ++j) {
+      prefetch(j);
       if (!load_k(ck.next(j))) return;
       if (j == 1 && !load_gate()) return;
       if (!kW && !load_v(cv.next(j - 1))) return;
@@ -805,14 +829,6 @@ __device__ __forceinline__ void q_copy(const uint8_t* tile, int r, bool have, ui
   fence_async_smem();   // the tensor cores read the shared-memory half
 }
 
-// Moves the 32-entry register queue on by 8: entries 8..31 to the front, `in` at the end.
-__device__ __forceinline__ void rotate8(uint4 (&q)[kDim / 8], const uint4 (&in)[8]) {
-#pragma unroll
-  for (int i = 0; i < kDim / 8 - 8; ++i) q[i] = q[i + 8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) q[kDim / 8 - 8 + i] = in[i];
-}
-
 // bf16(sigmoid(g)) for every bf16 g (index: g's bits), exact from the double definition;
 // filled once per device from the host. Every gate of the epilogue and of the verify
 // combine is looked up here: the answer is the definition itself, and a lookup costs the
@@ -868,7 +884,10 @@ __device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r, bool
 }
 
 // Gated epilogue of one finished item: out = bf16(bf16(O / l) * s) with s = bf16(sigmoid(
-// gate)) already in registers; O is read 32 columns at a time and released at the end.
+// gate)) already in registers. All of O is read first (16 columns at a time, each gated pair
+// of bf16 kept in a register: 128 words for the row, the gate registers freed as they are
+// used) and released at once, so the next item's first P V waits only for the reads; the
+// row's 512 bytes of stores follow while the next item runs.
 __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32_t tmem,
                          uint32_t lane_off, int r, uint32_t it_done, uint4 (&sg)[kDim / 8],
                          volatile int* abort) {
@@ -881,49 +900,41 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
   if (!warp_wait(&sm.o_done, it_done & 1, abort)) return false;
   tc_fence_after();
   const float inv = l > 0.f ? 1.0f / l : 0.f;
-  uint4* op =
-      reinterpret_cast<uint4*>(a.out + (size_t)(valid ? it.row0 + row : 0) * kOutRow + h * kDim);
-  const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0;   // rows are 12 KiB apart
-#pragma unroll 1
-  for (int c = 0; c < kDim / 64; ++c) {
+  uint32_t res[kDim / 2];   // word j: the gated outputs of columns 2j, 2j+1
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t o[32];
-      tmem_ld32(tmem + kTmemO + lane_off + c * 64 + 32 * half, o);
-      tmem_wait_ld(o);
+  for (int c16 = 0; c16 < kDim / 16; ++c16) {
+    uint32_t o[16];
+    tmem_ld16(tmem + kTmemO + lane_off + 16 * c16, o);
+    tmem_wait_ld(o);
 #pragma unroll
-      for (int i2 = 0; i2 < 4; i2 += 2) {
-        uint32_t w[8];
+    for (int i = 0; i < 2; ++i) {
+      const uint4 g4 = sg[2 * c16 + i];   // the sigmoids of columns 16 c16 + 8 i .. + 7
+      const uint32_t sw[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
-        for (int i = i2; i < i2 + 2; ++i) {
-          const uint32_t sw[4] = {sg[4 * half + i].x, sg[4 * half + i].y, sg[4 * half + i].z,
-                                  sg[4 * half + i].w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t ob = pack_bf16x2(__uint_as_float(o[8 * i + 2 * k]) * inv,
-                                            __uint_as_float(o[8 * i + 2 * k + 1]) * inv);
-            w[4 * (i - i2) + k] = mul_bf16x2(ob, sw[k]);   // bf16(o * s), o and s already bf16
-          }
-        }
-        // 32 bytes per store where the output allows it (32-byte aligned base)
-        uint4* dst = op + 8 * c + 4 * half + i2;
-        if (valid && out32) {
-          st_global_v8(dst, w);
-        } else if (valid) {
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t ob = pack_bf16x2(__uint_as_float(o[8 * i + 2 * k]) * inv,
+                                        __uint_as_float(o[8 * i + 2 * k + 1]) * inv);
+        res[8 * c16 + 4 * i + k] = mul_bf16x2(ob, sw[k]);   // bf16(o * s), both bf16
       }
     }
-    uint4 none[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) none[i] = make_uint4(0, 0, 0, 0);
-    rotate8(sg, none);
   }
   tc_fence_before();
   mbar_arrive(&sm.o_free);
   mbar_arrive(&sm.st_empty);
   if (!valid) return true;
+  uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)(it.row0 + row) * kOutRow + h * kDim);
+  if ((reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) {   // rows are 12 KiB apart
+#pragma unroll
+    for (int q = 0; q < kDim / 16; ++q) {
+      const uint32_t w[8] = {res[8 * q], res[8 * q + 1], res[8 * q + 2], res[8 * q + 3],
+                             res[8 * q + 4], res[8 * q + 5], res[8 * q + 6], res[8 * q + 7]};
+      st_global_v8(op + 2 * q, w);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < kDim / 8; ++q)
+      op[q] = make_uint4(res[4 * q], res[4 * q + 1], res[4 * q + 2], res[4 * q + 3]);
+  }
   if (a.row_stats) {
     a.row_stats[((size_t)h * a.rows + row) * 2] = M;
     a.row_stats[((size_t)h * a.rows + row) * 2 + 1] = l;

@@ -13,14 +13,13 @@
 // Exact rounding at low cost. The result must be the bf16 rounding of the exact
 // x (1 + w) / sqrt(mean(x^2) + eps). The fast path sums the squares in plain fp32 (each
 // square of a bf16 value is exact; a pairwise tree of depth 4 in the lane, then 4 shuffle
-// levels: relative error at most 8u, u = 2^-24), adds eps (u), takes rsqrtf (at most 2 ulp
-// = 4u) and forms fma(x, w, x) * r (two roundings): in all at most 10.5u relative, which is
-// under 10.5 fp32 ulps of the result. A result whose low 16 bits lie more than 12 ulps from
-// the bf16 midpoint 0x8000 therefore rounds to the bf16 value of the exact result. Rows
-// with an element inside that margin (about one in ten) take the exact path for those
-// elements: the sum of squares as a TwoSum pair, the inverse RMS as a double-float, and a
-// double-float product (ga_numerics.cuh), the same arithmetic as before this kernel took
-// the fast path first.
+// levels: relative error at most 8u, u = 2^-24), adds eps (u), takes rsqrtf and one Newton
+// step (about 1.5u), and forms fma(x, w, x) * r (two roundings): in all under 8u relative,
+// which is under 8 fp32 ulps of the result. A result whose low 16 bits lie more than 9 ulps
+// from the bf16 midpoint 0x8000 therefore rounds to the bf16 value of the exact result.
+// Rows with an element inside that margin (about one in fourteen) take the exact path for
+// those elements: the sum of squares as a TwoSum pair, the inverse RMS as a double-float,
+// and a double-float product (ga_numerics.cuh).
 #include "ga_internal.h"
 #include "ga_numerics.cuh"
 #include "ga_sm100.cuh"
@@ -33,7 +32,7 @@ __device__ __forceinline__ float hi_f(uint32_t u) { return __uint_as_float(u & 0
 
 constexpr int kThreads = 256;          // 16 half-warps, one row each at a time
 constexpr int kBlocksPerSm = 3;
-constexpr int kFastMargin = 12;        // fp32 ulps around a bf16 midpoint (see above)
+constexpr int kFastMargin = 9;         // fp32 ulps around a bf16 midpoint (see above)
 
 // The 16 values of a lane: words 0 and 1 hold dims (2l, 2l+1) and (32+2l, 33+2l); words
 // 2..7 the pass-through dims, two bf16 per word, in the order of the loads.
@@ -66,9 +65,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
                     uint16_t* __restrict__ dst) {
   const int l = threadIdx.x & 15;
   const unsigned hmask = 0xFFFFu << (threadIdx.x & 16);   // this half-warp's lanes
-  const long long stride = (long long)gridDim.x * (kThreads / 16);
-  long long row = (long long)blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
-  if (row >= n_rows) return;   // whole half-warps leave together
+  // rows are walked as (token, head) pairs: no division inside the loop
+  const int n_rows32 = (int)n_rows;                          // callers keep it below 2^31
+  const int stride = gridDim.x * (kThreads / 16);
+  int row = blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
+  if (row >= n_rows32) return;   // whole half-warps leave together
+  const int stride_tok = stride / n_heads, stride_head = stride - stride_tok * n_heads;
+  int tok = row / n_heads, head = row - tok * n_heads;
 
   // this lane's norm weights, in the value order of RowVals
   float w[16];
@@ -81,35 +84,37 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
       w[2 * i + 1] = hi_f(wv.w[i]);
     }
   }
-  // element offset of row r in an array of rows stride_el values apart
-  auto row_off = [&](long long r, int stride_el) -> long long {
-    const long long tok = r / n_heads;
-    const int head = head0 + (int)(r - tok * n_heads);
-    return (tok * heads_per_tok + head) * (long long)stride_el;
+  // element offset of the row (token t, head hd) in an array of rows stride_el values apart
+  auto row_off = [&](int t, int hd, int stride_el) -> long long {
+    return ((long long)t * heads_per_tok + head0 + hd) * stride_el;
   };
-  auto position = [&](long long r) -> int {
-    const long long tok = r / n_heads;
-    if (!kSeq) return pos_base + (int)tok;
+  auto position = [&](int t) -> int {
+    if (!kSeq) return pos_base + t;
     if (sp.n_seq > 0) {
-      // the sequence holding packed token tok: the last b with row_start[b] <= tok
+      // the sequence holding packed token t: the last b with row_start[b] <= t
       int lo = 0, hi = sp.n_seq - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (sp.row_start[mid] <= tok) lo = mid;
+        if (sp.row_start[mid] <= t) lo = mid;
         else hi = mid - 1;
       }
-      return sp.seq_base[lo] + (int)(tok - sp.row_start[lo]);
+      return sp.seq_base[lo] + (t - sp.row_start[lo]);
     }
-    return sp.seq_base[tok / sp.rows_per_seq] + (int)(tok % sp.rows_per_seq);
+    return sp.seq_base[t / sp.rows_per_seq] + t % sp.rows_per_seq;
   };
 
   RowVals cur;
-  load_row(src + row_off(row, src_stride), l, cur);
+  load_row(src + row_off(tok, head, src_stride), l, cur);
   while (true) {
-    const long long next = row + stride;
+    int ntok = tok + stride_tok, nhead = head + stride_head;
+    if (nhead >= n_heads) {
+      nhead -= n_heads;
+      ++ntok;
+    }
+    const bool more = row + stride < n_rows32;
     RowVals nxt;
-    if (next < n_rows) load_row(src + row_off(next, src_stride), l, nxt);
-    const int pos = position(row);
+    if (more) load_row(src + row_off(ntok, nhead, src_stride), l, nxt);
+    const int pos = position(tok);
     const uint32_t cw = __ldg(reinterpret_cast<const uint32_t*>(cos_tab + (long long)pos * kHalfRot) + l);
     const uint32_t sw = __ldg(reinterpret_cast<const uint32_t*>(sin_tab + (long long)pos * kHalfRot) + l);
 
@@ -130,16 +135,21 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
     float ssum = t8[0] + t8[2];
 #pragma unroll
     for (int off = 1; off < 16; off <<= 1) ssum += __shfl_xor_sync(hmask, ssum, off, 16);
-    const float rf = rsqrtf(fmaf(ssum, 1.0f / 256.0f, kEps));
+    const float a = fmaf(ssum, 1.0f / 256.0f, kEps);
+    const float r0 = rsqrtf(a);
+    const float rf = fmaf(0.5f * r0, fmaf(-(a * r0), r0, 1.0f), r0);   // one Newton step
 
+    // distance of each result's low 16 bits from the bf16 midpoint, shifted so that
+    // "within the margin" reads d <= 2 * margin; the smallest decides the exact path
     float y[16];
-    uint32_t near = 0u;   // bit i: value i lies within the margin of a bf16 midpoint
+    uint32_t dmin = 0xFFFFu;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       y[i] = fmaf(x[i], w[i], x[i]) * rf;
-      if (near_bf16_midpoint(y[i], kFastMargin)) near |= 1u << i;
+      dmin = min(dmin, (__float_as_uint(y[i]) + (uint32_t)(kFastMargin - 0x8000)) & 0xFFFFu);
     }
-    if (__any_sync(hmask, near != 0u)) {
+    const bool near_any = dmin <= 2u * kFastMargin;
+    if (__any_sync(hmask, near_any)) {
       // exact path for this row: the sum of squares as a TwoSum pair, combined over the
       // row's 16 lanes in a fixed order (lower lane first) so every lane holds the same pair
       SumSq s0, s1;
@@ -166,14 +176,14 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
       const InvRms r = inv_rms_df(ss);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if ((near >> i) & 1u) y[i] = norm_elem_exact(x[i], w[i], r.h, r.l);
+        if (near_bf16_midpoint(y[i], kFastMargin)) y[i] = norm_elem_exact(x[i], w[i], r.h, r.l);
     }
 
     // partial RoPE: values 0, 1 are dims 2l, 2l+1 (a) and 2, 3 are dims 32+2l, 33+2l (b)
     float oa0, ob0, oa1, ob1;
     rope_pair(bf16_round(y[0]), bf16_round(y[2]), lo_f(cw), lo_f(sw), oa0, ob0);
     rope_pair(bf16_round(y[1]), bf16_round(y[3]), hi_f(cw), hi_f(sw), oa1, ob1);
-    uint16_t* out = dst + row_off(row, kDim);
+    uint16_t* out = dst + row_off(tok, head, kDim);
     reinterpret_cast<uint32_t*>(out)[l] = pack_bf16x2(oa0, oa1);
     reinterpret_cast<uint32_t*>(out + 32)[l] = pack_bf16x2(ob0, ob1);
 #pragma unroll
@@ -181,8 +191,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
       reinterpret_cast<uint2*>(out + 64 + 64 * k)[l] =
           make_uint2(pack_bf16x2(y[4 + 4 * k], y[5 + 4 * k]), pack_bf16x2(y[6 + 4 * k], y[7 + 4 * k]));
 
-    if (next >= n_rows) break;
-    row = next;
+    if (!more) break;
+    row += stride;
+    tok = ntok;
+    head = nhead;
     cur = nxt;
   }
 }
