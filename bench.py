@@ -276,7 +276,7 @@ def run_gpu(args, world, rank, local):
         "secondary": secondary,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, gpu_out=out)
     return line
 
 
@@ -628,7 +628,7 @@ def run_masked(args, world, rank, local):
         "hidden_rows": hidden,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_masked(args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline_masked(args.cpu_seconds, gpu_out=out)
     return line
 
 
@@ -1091,30 +1091,82 @@ def _threads_used():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(seconds: float):
-    import numpy as np
-    data = _oracle_inputs()
-    rng = np.random.default_rng(0)
-    pairs = 0
-    t0 = time.perf_counter()
-    n_rows = 0
-    while time.perf_counter() - t0 < seconds:
-        rows = np.sort(rng.choice(S, 16, replace=False))
-        oracle_sample_step(*data, rows)
-        pairs += int((rows + 1).sum())
-        n_rows += 16
-    dt = time.perf_counter() - t0
-    return {"value": round(attention_flops(pairs) / dt / 1e12, 6), "unit": UNIT,
-            "cores": _threads_used(), "kind": "oracle",
-            "sample": f"{n_rows} random query rows x 24 heads of the S=8192 causal pass, each "
-                      f"16-row batch with the K prologue over all 8192 keys; {dt:.1f} s"}
+class _ParityTally:
+    """Parity of the GPU output on the oracle's sampled rows (the tests' element-wise check:
+    2 bf16 ulp + 1e-5, with its ambiguous-rounding rule), summed over the samples."""
+
+    def __init__(self):
+        self.n = self.bad = self.pairs = self.off = self.explained = 0
+        self.over = 0.0
+        self.max_ulp = 0.0
+        self.passed = True
+
+    def add(self, ref, got):
+        import contextlib
+        import io
+        with contextlib.redirect_stdout(io.StringIO()):
+            try:
+                st = ref.check(got)
+            except AssertionError:
+                self.passed = False
+                return
+        self.n += st["n"]
+        self.bad += st["bad"]
+        self.over += st["over_1ulp"] * st["n"]
+        self.max_ulp = max(self.max_ulp, st["max_ulp"])
+        self.pairs += len(ref.rows) * len(ref.heads)
+        self.off += st["rows_off_oracle"]
+        self.explained += st["explained_by_ambiguous_rounding"]
+
+    def summary(self, what):
+        return {"what": what, "elements": self.n, "bad": self.bad,
+                "over_1ulp": round(self.over / max(self.n, 1), 6),
+                "max_ulp": round(self.max_ulp, 2), "pairs": self.pairs,
+                "pairs_off_oracle": self.off, "explained_by_ambiguous_rounding": self.explained,
+                "passed": self.passed,
+                "tolerance": "|gpu - oracle| <= 2 bf16 ulp(oracle) + 1e-5 per element"}
 
 
-def cpu_baseline_masked(seconds: float):
-    """The oracle on the masked workload: the key prologue over all 8192 keys and the
-    stored-mask attention of 16 random query rows (all 24 heads) per batch."""
+def cpu_baseline(seconds: float, gpu_out=None):
+    """The oracle on a bounded sample of the headline workload (random query rows, all 24
+    heads, with the K prologue over all keys), timed on the host cores. When the GPU output
+    of the same inputs is given, each sampled row is also checked against it (untimed)."""
     import numpy as np
     from oracle import ga_oracle as O
+    from tests.parity import AttnRef
+    qg, kraw, v, w_q, w_k, cos, sin = _oracle_inputs()
+    rng = np.random.default_rng(0)
+    pairs = 0
+    spent = 0.0
+    n_rows = 0
+    tally = _ParityTally()
+    got = gpu_out.cpu() if gpu_out is not None else None
+    while spent < seconds:
+        rows = np.sort(rng.choice(S, 16, replace=False))
+        t0 = time.perf_counter()
+        kp = O.prep_keys(kraw, w_k, cos, sin)
+        ref = AttnRef(qg, kp, v, w_q, cos, sin, 0, S, "causal", rows=rows)
+        spent += time.perf_counter() - t0
+        if got is not None:
+            tally.add(ref, got[torch.as_tensor(rows)])
+        pairs += int((rows + 1).sum())
+        n_rows += 16
+    res = {"value": round(attention_flops(pairs) / spent / 1e12, 6), "unit": UNIT,
+           "cores": _threads_used(), "kind": "oracle",
+           "sample": f"{n_rows} random query rows x 24 heads of the S=8192 causal pass, each "
+                     f"16-row batch with the K prologue over all 8192 keys; {spent:.1f} s"}
+    if got is not None:
+        res["parity"] = tally.summary("the timed launch's output on the sampled rows")
+    return res
+
+
+def cpu_baseline_masked(seconds: float, gpu_out=None):
+    """The oracle on the masked workload: the key prologue over all 8192 keys and the
+    stored-mask attention of 16 random query rows (all 24 heads) per batch; with the GPU
+    output given, each sampled row is also checked against it (untimed)."""
+    import numpy as np
+    from oracle import ga_oracle as O
+    from tests.parity import AttnRef
     from verify_gated_gqa_gb300 import synth
     qg, k, v, w_q, w_k = synth.attention_inputs(SEED + 7, S, S)
     mask = synth.selection_mask(SEED + 7, S, window=M_WINDOW, n_random=M_RANDOM).numpy()
@@ -1123,18 +1175,26 @@ def cpu_baseline_masked(seconds: float):
     cos, sin = O.rope_tables(S)
     rng = np.random.default_rng(0)
     pairs = n_rows = 0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds:
+    spent = 0.0
+    tally = _ParityTally()
+    got = gpu_out.cpu() if gpu_out is not None else None
+    while spent < seconds:
         rows = np.sort(rng.choice(S, 16, replace=False))
+        t0 = time.perf_counter()
         kp = O.prep_keys(k, w_k, cos, sin)
-        O.masked(qg, kp, v, w_q, cos, sin, 0, S, mask, rows=rows)
+        ref = AttnRef(qg, kp, v, w_q, cos, sin, 0, S, "mask", mask=mask, rows=rows)
+        spent += time.perf_counter() - t0
+        if got is not None:
+            tally.add(ref, got[torch.as_tensor(rows)])
         pairs += int((mask[rows] != 0).sum())
         n_rows += 16
-    dt = time.perf_counter() - t0
-    return {"value": round(attention_flops(pairs) / dt / 1e12, 6), "unit": UNIT,
-            "cores": _threads_used(), "kind": "oracle",
-            "sample": f"{n_rows} random query rows x 24 heads of the S=8192 masked pass, each "
-                      f"16-row batch with the K prologue over all 8192 keys; {dt:.1f} s"}
+    res = {"value": round(attention_flops(pairs) / spent / 1e12, 6), "unit": UNIT,
+           "cores": _threads_used(), "kind": "oracle",
+           "sample": f"{n_rows} random query rows x 24 heads of the S=8192 masked pass, each "
+                     f"16-row batch with the K prologue over all 8192 keys; {spent:.1f} s"}
+    if got is not None:
+        res["parity"] = tally.summary("the timed launch's output on the sampled rows")
+    return res
 
 
 def run_reference(args, world, rank):
