@@ -338,28 +338,6 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
       const int outer = kv_at(kt, r0);
       return load_tile(tm_v, true, kvh, r0, outer, kTileBytes);
     };
-    // The next item's prepared Q tile and gate tile go into L2 a few key tiles before this
-    // item ends (the ring can take the Q tile only once this item's last K tile is used,
-    // and from DRAM it would arrive late): its first Q K^T then waits for an L2 read.
-    Item nx;
-    bool prefetch_next = false;
-    if (!is_verify<kMode>() && kMode != kModeBatch) {
-      ItemWalk<kMode> peek = walk;
-      prefetch_next = peek.next(a, nx);
-    }
-    const int prefetch_at = it.n > 4 ? it.n - 4 : 1;
-    auto prefetch = [&](int j) {
-      if (!prefetch_next || j != prefetch_at) return;
-      if (lane == 0) {
-        const int r0 = nx.row0 + nx.mt * kTileM;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tma_prefetch_l2_3d(tm_q, c * 64, nx.h, r0);
-          if (has_gate<kMode, kW>()) tma_prefetch_l2_3d(tm_g, kDim + c * 64, nx.h, r0);
-        }
-      }
-      __syncwarp();
-    };
     // Ring order: the item's prepared Q (for the edge warps), then in MMA order K0,
     // (K_j, V_{j-1}) for j >= 1, V_{n-1}; the gate tile (gated passes) just before V_0.
     if (is_verify<kMode>()) {
@@ -373,9 +351,7 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
              load_tile(tm_g, false, it.h, it.row0 + it.mt * kTileM, -1, kTileBytes, kDim);
     };
     if (!load_k(ck.next(0))) return;
-    if (it.n == 1) prefetch(1);
     for (int j = 1; j < it.n; ++j) {
-      prefetch(j);
       if (!load_k(ck.next(j))) return;
       if (j == 1 && !load_gate()) return;
       if (!kW && !load_v(cv.next(j - 1))) return;

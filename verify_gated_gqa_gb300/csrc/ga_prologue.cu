@@ -141,14 +141,15 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
 
     // distance of each result's low 16 bits from the bf16 midpoint, shifted so that
     // "within the margin" reads d <= 2 * margin; the smallest decides the exact path
+    // (one multiply-add per value: the low 16 bits moved to the top, the offset added there)
     float y[16];
-    uint32_t dmin = 0xFFFFu;
+    uint32_t dmin = 0xFFFFFFFFu;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       y[i] = fmaf(x[i], w[i], x[i]) * rf;
-      dmin = min(dmin, (__float_as_uint(y[i]) + (uint32_t)(kFastMargin - 0x8000)) & 0xFFFFu);
+      dmin = min(dmin, __float_as_uint(y[i]) * 65536u + ((uint32_t)(kFastMargin - 0x8000) << 16));
     }
-    const bool near_any = dmin <= 2u * kFastMargin;
+    const bool near_any = dmin <= (2u * kFastMargin) << 16;
     if (__any_sync(hmask, near_any)) {
       // exact path for this row: the sum of squares as a TwoSum pair, combined over the
       // row's 16 lanes in a fixed order (lower lane first) so every lane holds the same pair

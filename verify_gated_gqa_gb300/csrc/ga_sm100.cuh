@@ -130,14 +130,6 @@ __device__ __forceinline__ void tma_load_5d_warp(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// A tile of a 3-D tensor map into L2 only (no shared memory, no barrier): the box at
-// coordinates (x, y, z) is fetched from global memory into the L2 cache.
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-
 // ------------------------------------------------------------------ tcgen05: TMEM
 // Allocation and deallocation are warp-wide; the allocated base lands in *slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
