@@ -26,6 +26,11 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
     tr.write_sep("-", "parity against the oracle (tolerance 2 bf16 ulp + 1e-5 per element)")
     tr.write_line("check | elements | bad | over 1 ulp | max ulp | pairs off/checked (cap) | "
                   "explained | result")
+    # the named configurations last, so that the end of the log always holds them
+    named = ("S=64 causal", "S=2048 causal", "S=2048 bidirectional", "S=8192 causal",
+             "S=8192 chunk", "masked S=8192", "verify 8 x 16")
+    key = lambda r: any(r["what"].startswith(n) for n in named)
+    recs = [r for r in recs if not key(r)] + [r for r in recs if key(r)]
     for r in recs:
         pairs = r["pairs"]
         po = (f"{r['off']}/{pairs} ({mod.off_cap(pairs)})" if pairs else "-")

@@ -43,9 +43,11 @@
 //              epilogue of the current item.
 // The edge code is kept in short loops: the four roles run different code at once and
 // share the SM's instruction cache, which long unrolled sequences would overflow.
-// Over e4m3 caches (verify), the producer loads each K or V tile as e4m3 codes into the back
-// half of its slot, the edge warps widen it in place to bf16(fp32(code * scale)), and the
-// MMA warps wait for the widened tile instead of the copy.
+// Over e4m3 caches (verify), the kernel runs as clusters of two CTAs, one per half of a
+// query group, that walk the same key tiles: each CTA loads the e4m3 codes of its 64 keys of
+// a K or V tile into the back of its slot, widens them to bf16(fp32(code * scale)) and
+// writes the bf16 rows into its own slot and into its peer's (distributed shared memory),
+// so every code is widened once; the MMA warps wait until both halves are in.
 // Tensor memory (512 columns x 128 lanes, lane = query row): O [0, 256) fp32, S [256, 384)
 // fp32, Q dims 0..127 [384, 448) and P [448, 512) as bf16 pairs. Q dims 128..255 stay in
 // shared memory for the item, where P used to go: P is written to tensor memory with one
@@ -64,6 +66,16 @@ namespace ga {
 namespace {
 
 constexpr int kSlots = 3;
+// e4m3 caches: each CTA of a pair holds the codes of its 64 keys of a tile (64 x 256 bytes)
+// until they are widened, in eight 2 KiB pieces of 8 keys, each inside rows that only one
+// edge warp writes: edge warp w widens keys 16w .. 16w+15 of the CTA's half into bf16 rows
+// 64 rank + 16w .. + 15 of the four 64-dim blocks, and its keys 16w + 8s .. + 7 wait in its
+// rows of block 2 + s. A warp's writes then only ever cover its own codes.
+constexpr int kRawKeys = 64;
+constexpr int kRawBytes = kRawKeys * 256;
+__device__ __forceinline__ uint32_t raw_piece_offset(int w, int s, uint32_t rank) {
+  return (uint32_t)(2 + s) * 16384u + (rank * (uint32_t)kRawKeys + 16u * (uint32_t)w) * 128u;
+}
 constexpr int kChunkBytes = kTileN * 128;     // 128 keys x 64 dims of bf16
 constexpr int kTileBytes = 4 * kChunkBytes;   // 128 keys x 256 dims
 constexpr int kThreads = 512;     // four warpgroups
@@ -106,7 +118,7 @@ struct AttnSmem {
   uint16_t mx[2][2][kTileM];          // tile g: each half's row maximum (bf16 bits), by g % 2
   uint64_t full[kSlots], empty[kSlots];
   uint64_t conv[kSlots];              // e4m3 caches: the slot's tile is widened (or seen: Q)
-  uint64_t wide_read;                 // e4m3 caches: every edge thread has read the raw tile
+  uint64_t peer_free[kSlots];         // e4m3 caches: the peer's slot is free for the next fill
   uint64_t q_full, q_empty, s_full, s_free;
   uint64_t p_full[2], p_empty[2];     // per 64-key half of P
   uint64_t o_done, o_free, st_full, st_empty, drain, drain_pv, q_read, g_read, mx_bar;
@@ -131,6 +143,16 @@ __host__ __device__ constexpr bool is_causal() { return kMode == kModeCausal || 
 
 __device__ __forceinline__ int item_index(int round, int cta, int G) {
   return round * G + ((round & 1) ? (G - 1 - cta) : cta);
+}
+
+// The item a CTA takes in a round. Over e4m3 caches the CTAs run in clusters of two (ranks
+// blockIdx.x % 2): the pair takes the items 2p and 2p + 1, the two halves of one query
+// group over the same key chunk, the pairs dealt like single items.
+template <int kMode>
+__device__ __forceinline__ int walk_index(int round) {
+  if (kMode == kModeVerify8)
+    return 2 * item_index(round, blockIdx.x >> 1, gridDim.x >> 1) + (blockIdx.x & 1);
+  return item_index(round, blockIdx.x, gridDim.x);
 }
 
 template <int kMode>
@@ -227,9 +249,8 @@ template <int kMode>
 struct ItemWalk {
   int round = 0;
   __device__ __forceinline__ bool next(const AttnArgs& a, Item& out) {
-    const int G = gridDim.x;
     for (;; ++round) {
-      const int idx = item_index(round, blockIdx.x, G);
+      const int idx = walk_index<kMode>(round);
       if (idx >= a.n_items) return false;
       out = make_item<kMode>(a, idx);
       if (out.n > 0) {
@@ -261,10 +282,13 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
   // fused rows at (256 + dim, head, row r0); a K or V tile is one copy of all four 64-dim
   // blocks (the key/value map lists the block index as its outermost dimension, so the box
   // lands as four consecutive 16 KiB blocks) at (0, key r0, head, 0[, sequence]).
+  const int lane = threadIdx.x & 31;
   auto load_tile = [&](const CUtensorMap* map, bool kv, int head, int r0, int seq,
                        uint32_t bytes, int x0 = 0) -> bool {
     const uint32_t slot = cnt % kSlots;
     if (!warp_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
+    if (kMode == kModeVerify8 && lane == 0)   // the peer may copy into this slot's next fill
+      mbar_arrive_remote(mapa_shared(smem_u32(&sm.peer_free[slot]), (blockIdx.x & 1) ^ 1u));
     mbar_expect_tx_warp(&sm.full[slot], bytes);
     if (kv) {
       if (seq < 0)
@@ -282,7 +306,6 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
   };
   ItemWalk<kMode> walk;
   Item it;
-  const int lane = threadIdx.x & 31;
   while (walk.next(a, it)) {
     const int kvh = it.h / kGroup;
     TileCursor<kMode> ck(it), cv(it);
@@ -315,14 +338,21 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
       }
       return page;
     };
-    // e4m3 caches: one box of 128 keys x 256 bytes into the back half of the slot, where
-    // the edge warps widen it to the bf16 tile the tensor cores read
+    // e4m3 caches: this CTA's 64 keys of the tile (eight boxes of 8 keys x 256 bytes) into
+    // its edge warps' rows of the slot, where they widen them (and copy them to the peer)
     auto load_raw8 = [&](const CUtensorMap* map, int kt) -> bool {
       const uint32_t slot = cnt % kSlots;
+      const uint32_t rank = blockIdx.x & 1;
       if (!warp_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
-      mbar_expect_tx_warp(&sm.full[slot], kTileBytes / 2);
-      tma_load_4d_warp(sm.tile[slot] + kTileBytes / 2, map, &sm.full[slot], 0, kvh, kt * kTileN,
-                       it.seq);
+      if (lane == 0)   // the peer may copy into this slot's next fill
+        mbar_arrive_remote(mapa_shared(smem_u32(&sm.peer_free[slot]), rank ^ 1u));
+      mbar_expect_tx_warp(&sm.full[slot], kRawBytes);
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+#pragma unroll
+        for (int piece = 0; piece < 2; ++piece)
+          tma_load_4d_warp(sm.tile[slot] + raw_piece_offset(w, piece, rank), map, &sm.full[slot],
+                           0, kvh, kt * kTileN + kRawKeys * (int)rank + 16 * w + 8 * piece, it.seq);
       ++cnt;
       return true;
     };
@@ -394,8 +424,9 @@ struct RingWalk {
   // wait for the next fill in ring order (its slot in `slot`) and count this warp as past it
   __device__ __forceinline__ bool next(AttnSmem& sm, volatile int* abort, uint32_t& slot) {
     slot = cnt % kSlots;
-    uint64_t* ready = kMode == kModeVerify8 ? &sm.conv[slot] : &sm.full[slot];
-    const bool ok = warp_wait(ready, (cnt / kSlots) & 1, abort);
+    const bool ok = kMode == kModeVerify8
+                        ? __all_sync(0xffffffffu, mbar_wait<true>(&sm.conv[slot], (cnt / kSlots) & 1, abort))
+                        : warp_wait(&sm.full[slot], (cnt / kSlots) & 1, abort);
     ++cnt;
     if (ok && (threadIdx.x & 31) == 0) mbar_arrive(&sm.empty[slot]);
     return ok;
@@ -860,7 +891,7 @@ __device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r, bool
 }
 
 // Gated epilogue of one finished item: out = bf16(bf16(O / l) * s) with s = bf16(sigmoid(
-// gate)) already in registers. All of O is read first (16 columns at a time, each gated pair
+// gate)) already in registers. All of O is read first (64 columns at a time, each gated pair
 // of bf16 kept in a register: 128 words for the row, the gate registers freed as they are
 // used) and released at once, so the next item's first P V waits only for the reads; the
 // row's 512 bytes of stores follow while the next item runs.
@@ -877,20 +908,22 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
   tc_fence_after();
   const float inv = l > 0.f ? 1.0f / l : 0.f;
   uint32_t res[kDim / 2];   // word j: the gated outputs of columns 2j, 2j+1
+  // 64 columns per round: two 32-column loads in flight, one wait
 #pragma unroll
-  for (int c16 = 0; c16 < kDim / 16; ++c16) {
-    uint32_t o[16];
-    tmem_ld16(tmem + kTmemO + lane_off + 16 * c16, o);
+  for (int c64 = 0; c64 < kDim / 64; ++c64) {
+    uint32_t o[64];
+    tmem_ld32(tmem + kTmemO + lane_off + 64 * c64, *reinterpret_cast<uint32_t(*)[32]>(o));
+    tmem_ld32(tmem + kTmemO + lane_off + 64 * c64 + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
     tmem_wait_ld(o);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint4 g4 = sg[2 * c16 + i];   // the sigmoids of columns 16 c16 + 8 i .. + 7
+    for (int i = 0; i < 8; ++i) {
+      const uint4 g4 = sg[8 * c64 + i];   // the sigmoids of columns 64 c64 + 8 i .. + 7
       const uint32_t sw[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t ob = pack_bf16x2(__uint_as_float(o[8 * i + 2 * k]) * inv,
                                         __uint_as_float(o[8 * i + 2 * k + 1]) * inv);
-        res[8 * c16 + 4 * i + k] = mul_bf16x2(ob, sw[k]);   // bf16(o * s), both bf16
+        res[32 * c64 + 4 * i + k] = mul_bf16x2(ob, sw[k]);   // bf16(o * s), both bf16
       }
     }
   }
@@ -952,52 +985,83 @@ __device__ bool epilogue_partial(AttnSmem& sm, const AttnArgs& a, const Item& it
   return true;
 }
 
-// e4m3 caches: the raw tile (128 keys x 256 codes, one 256-byte row per key) in the back half
-// of the fill's slot becomes the bf16 tile the tensor cores read, bf16(fp32(code * scale))
-// per element, in place. Edge thread t widens the 16 codes of column t % 16 in rows t / 16 +
-// 8k: it reads all of them (its rows' scales already in flight), waits until every edge
-// thread has read (the bf16 tile overwrites the raw one), then writes. The long-prompt
-// page's F8 rows are staged this way: loaded a step ahead, widened in the slot.
-__device__ bool widen_e4m3(AttnSmem& sm, const AttnArgs& a, uint32_t pos, const float* scale,
-                           int seq, int kvh, int kt, int t, uint32_t n_done, volatile int* abort) {
-  const uint32_t slot = pos % kSlots;
-  const int c = t & 15;
-  const int r0 = t >> 4;
-  float scv[16];
+// e4m3 caches: this CTA's 64 keys of the fill's tile (their codes in eight pieces, each in
+// the rows of the edge warp that widens it) become rows 64 rank .. 64 rank + 63 of the bf16
+// tile the tensor cores read, bf16(fp32(code * scale)) per element, in this CTA's slot; the
+// copy engine then copies them into the same rows of the peer's slot (the peer supplies the
+// other 64). Edge warp w widens rows 16w .. 16w+15 of the half, lane l the 16 codes of column
+// l % 16 in rows l / 16 + 2k. Each thread reads its codes (its rows' scales loaded during the
+// previous fill); once the warp has read (its rows overwrite its own codes, and nothing else
+// does) it writes its rows and arrives on this CTA's conv barrier of the slot, which also
+// waits for the 32 KiB the peer copies in. Lane 0 of each warp then waits until the peer's
+// slot is free for this fill (its producer's signal, normally long given) and copies the
+// warp's 16 rows of each 64-dim block (2 KiB, rows contiguous) to the peer. The MMA warps of
+// each CTA wait on their conv barrier. The long-prompt page's F8 rows are staged this way:
+// loaded a step ahead, widened in the slot.
+constexpr uint32_t kPeerCopyBytes = kRawKeys * 128 * 4;   // the peer's 64 rows of 4 blocks
+constexpr int kWideRows = 8;   // rows each edge thread widens per fill
+// The scales of an edge thread's rows of key tile kt (this CTA's half), for the fill after the
+// current one: loaded while the current fill is widened.
+__device__ __forceinline__ void load_row_scales(const AttnArgs& a, const float* scale, int seq,
+                                                int kvh, int kt, int t, float (&scv)[kWideRows]) {
+  const uint32_t rank = blockIdx.x & 1;
+  const int rbase = 16 * (t >> 5) + ((t & 31) >> 4);
   const float* srow = scale + (size_t)seq * a.cache_cap * kKvHeads + kvh;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const int key = kt * kTileN + r0 + 8 * k;
+  for (int k = 0; k < kWideRows; ++k) {
+    const int key = kt * kTileN + kRawKeys * (int)rank + rbase + 2 * k;
     scv[k] = key < a.cache_cap ? __ldg(srow + (size_t)key * kKvHeads) : 0.f;
   }
+}
+__device__ bool widen_e4m3(AttnSmem& sm, uint32_t pos, const float (&scv)[kWideRows], int t,
+                           volatile int* abort) {
+  const uint32_t slot = pos % kSlots;
+  const uint32_t rank = blockIdx.x & 1, peer = rank ^ 1u;
+  const int w = t >> 5, l = t & 31;
+  const int c = l & 15;
+  const int rbase = 16 * w + (l >> 4);   // this thread's rows: rbase + 2k of the half
+  constexpr int kRows = kWideRows;
   if (!warp_wait(&sm.full[slot], (pos / kSlots) & 1, abort)) return false;
-  const uint8_t* raw = sm.tile[slot] + kTileBytes / 2;
-  uint4 v[16];
+  uint4 v[kRows];
 #pragma unroll
-  for (int k = 0; k < 16; ++k)
-    v[k] = *reinterpret_cast<const uint4*>(raw + (r0 + 8 * k) * kDim + c * 16);
-  mbar_arrive(&sm.wide_read);
-  if (!warp_wait(&sm.wide_read, n_done & 1, abort)) return false;
+  for (int k = 0; k < kRows; ++k) {
+    const int kk = (l >> 4) + 2 * k;   // the warp's key 0 .. 15: piece kk / 8, row kk % 8
+    v[k] = *reinterpret_cast<const uint4*>(sm.tile[slot] + raw_piece_offset(w, kk >> 3, rank) +
+                                           (kk & 7) * kDim + c * 16);
+  }
+  __syncwarp();   // the warp's codes are read before its rows overwrite them
   uint8_t* blk = sm.tile[slot] + (c >> 2) * kChunkBytes;
   const uint32_t j0 = (uint32_t)(c & 3) * 2;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const uint32_t row = (uint32_t)(r0 + 8 * k);
+  for (int k = 0; k < kRows; ++k) {
+    const uint32_t row = (uint32_t)(kRawKeys * rank + rbase + 2 * k);
     const uint32_t wi[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-    uint32_t w[8];
+    uint32_t wd[8];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       // codes of dims 4q .. 4q+3 of this chunk, lowest byte first; fp32(code * scale)
       const float2 lo = e4m3x2_to_float2(wi[q]);
       const float2 hi = e4m3x2_to_float2(wi[q] >> 16);
-      w[2 * q] = pack_bf16x2(lo.x * scv[k], lo.y * scv[k]);
-      w[2 * q + 1] = pack_bf16x2(hi.x * scv[k], hi.y * scv[k]);
+      wd[2 * q] = pack_bf16x2(lo.x * scv[k], lo.y * scv[k]);
+      wd[2 * q + 1] = pack_bf16x2(hi.x * scv[k], hi.y * scv[k]);
     }
-    *reinterpret_cast<uint4*>(blk + sw128_offset(row, j0)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(blk + sw128_offset(row, j0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+    *reinterpret_cast<uint4*>(blk + sw128_offset(row, j0)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    *reinterpret_cast<uint4*>(blk + sw128_offset(row, j0 + 1)) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
   }
-  fence_async_smem();
-  mbar_arrive(&sm.conv[slot]);
+  fence_async_smem();   // this CTA's tensor cores and copy engine read what the threads wrote
+  if (t == 0) mbar_arrive_expect_tx(&sm.conv[slot], kPeerCopyBytes);   // the peer's rows
+  else mbar_arrive(&sm.conv[slot]);
+  __syncwarp();
+  if (!__all_sync(0xffffffffu, mbar_wait<true>(&sm.peer_free[slot], (pos / kSlots) & 1, abort)))
+    return false;
+  if (l == 0) {
+    const uint32_t bar_peer = mapa_shared(smem_u32(&sm.conv[slot]), peer);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint8_t* src = sm.tile[slot] + b * kChunkBytes + (kRawKeys * rank + 16 * w) * 128;
+      bulk_copy_to_peer(mapa_shared(smem_u32(src), peer), src, 16 * 128, bar_peer);
+    }
+  }
   return true;
 }
 
@@ -1008,12 +1072,11 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
   const int r = quad * 32 + lane;
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const uint32_t q_taddr = tmem + kTmemQ + lane_off;
-  const int G = gridDim.x;
   int round = 0;
   // the CTA's next item with key tiles; items without any are answered on the way
   auto next_item = [&](Item& out) -> bool {
     for (;; ++round) {
-      const int idx = item_index(round, blockIdx.x, G);
+      const int idx = walk_index<kMode>(round);
       if (idx >= a.n_items) return false;
       out = make_item<kMode>(a, idx);
       if (out.n > 0) {
@@ -1077,29 +1140,27 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
   uint32_t it_done = 0;
   // e4m3 caches: the edge warps walk every fill of the ring in order and widen each K and V
   // tile of the item (ring order K0, then K_j, V_{j-1} for j >= 1, then V_{n-1})
-  uint32_t n_wide = 0;
   auto widen_item = [&](const Item& it, uint32_t q_at) -> bool {
     const int kvh = it.h / kGroup;
+    // fill f (1 .. 2n) after the item's Q: K0, then K_j, V_{j-1} for j >= 1, then V_{n-1}
+    auto fill_tile = [&](int f, bool& is_v) -> int {
+      if (f == 1) { is_v = false; return 0; }
+      if (f == 2 * it.n) { is_v = true; return it.n - 1; }
+      is_v = (f & 1) != 0;
+      return is_v ? (f - 3) / 2 : f / 2;
+    };
+    float scv[kWideRows], scv_next[kWideRows];
+    bool is_v;
+    int tile = fill_tile(1, is_v);
+    load_row_scales(a, is_v ? a.v_scale : a.k_scale, it.seq, kvh, it.kt0 + tile, r, scv_next);
     for (int f = 1; f <= 2 * it.n; ++f) {
-      bool is_v;
-      int tile;
-      if (f == 1) {
-        is_v = false;
-        tile = 0;
-      } else if (f == 2 * it.n) {
-        is_v = true;
-        tile = it.n - 1;
-      } else if ((f & 1) == 0) {
-        is_v = false;
-        tile = f / 2;
-      } else {
-        is_v = true;
-        tile = (f - 3) / 2;
+#pragma unroll
+      for (int k = 0; k < kWideRows; ++k) scv[k] = scv_next[k];
+      if (f < 2 * it.n) {
+        tile = fill_tile(f + 1, is_v);
+        load_row_scales(a, is_v ? a.v_scale : a.k_scale, it.seq, kvh, it.kt0 + tile, r, scv_next);
       }
-      if (!widen_e4m3(sm, a, q_at + f, is_v ? a.v_scale : a.k_scale, it.seq, kvh, it.kt0 + tile,
-                      r, n_wide, abort))
-        return false;
-      ++n_wide;
+      if (!widen_e4m3(sm, q_at + f, scv, r, abort)) return false;
     }
     return true;
   };
@@ -1134,6 +1195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((smem_u32(smem_raw) & 1023u) != 0u) {
     if (threadIdx.x == 0) record_abort(a.status, kDevBadLaunch);
+    if (kMode == kModeVerify8) {   // the peer's two cluster barriers (after set-up, at exit)
+      cluster_sync_all();
+      cluster_sync_all();
+    }
     return;
   }
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
@@ -1162,8 +1227,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.drain, 1);
     mbar_init(&sm.drain_pv, 1);
     mbar_init(&sm.q_read, 128);
-    for (int i = 0; i < kSlots; ++i) mbar_init(&sm.conv[i], 128);
-    mbar_init(&sm.wide_read, 128);
+    // e4m3 caches: conv counts this CTA's 128 edge threads (and, for a K or V fill, the 32 KiB
+    // the peer copies in); peer_free the peer's producer, once per fill of the slot
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&sm.conv[i], 128);
+      mbar_init(&sm.peer_free[i], 1);
+    }
     mbar_init(&sm.g_read, 128);
     mbar_init(&sm.mx_bar, 256);
     mbar_fence_init();
@@ -1180,6 +1249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // over e4m3 caches the peer arrives on this CTA's barriers: both CTAs' barriers are
+  // initialised before either runs
+  if (kMode == kModeVerify8) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
@@ -1202,6 +1274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
   if (threadIdx.x == 0 && sm.abort) record_abort(a.status, sm.abort);
+  // a CTA of a pair leaves only when its peer no longer writes into its shared memory or
+  // arrives on its barriers (every wait before this point is bounded)
+  if (kMode == kModeVerify8) cluster_sync_all();
 }
 
 // Verify combine (TensorFold PR #1080, "qwen CUDA: long-prompt prefill 5.4x faster", the
@@ -1311,6 +1386,21 @@ cudaError_t attn_set_smem_attribute() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+cudaError_t attn_max_pair_clusters(int* n) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = attn_smem_bytes();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(n, attn_kernel<kModeVerify8, false>, &cfg);
+}
+
 cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                         const CUtensorMap& tm_g, const AttnArgs& a, int grid, cudaStream_t s) {
   const size_t smem = attn_smem_bytes();
@@ -1326,7 +1416,21 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
   } else if (a.mode == kModeBatch) {
     attn_kernel<kModeBatch, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else if (a.mode == kModeVerify8) {
-    attn_kernel<kModeVerify8, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    // clusters of two CTAs (grid even): the pair shares the widening of each e4m3 tile
+    if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_kernel<kModeVerify8, false>, tm_q, tm_k, tm_v, tm_g, a);
   } else {
     attn_kernel<kModeMask, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   }

@@ -30,6 +30,7 @@ struct DeviceState {
   bool ready = false;
   int status = GA_OK;  // GA_OK or GA_ERR_DEVICE / GA_ERR_CUDA from set-up
   int sm_count = 0;
+  int pair_clusters = 0;  // clusters of two attention CTAs that fit at once (e4m3 verify)
   int* status_word = nullptr;
 };
 DeviceState g_devices[kMaxDevices];
@@ -87,6 +88,13 @@ int current_device(DeviceState** out) {
       void* sw = nullptr;
       if ((e = GA_CUDA(attn_set_smem_attribute())) != cudaSuccess) return fail_cuda(e);
       if ((e = GA_CUDA(probe_set_smem_attribute())) != cudaSuccess) return fail_cuda(e);
+      if ((e = GA_CUDA(attn_max_pair_clusters(&d.pair_clusters))) != cudaSuccess) return fail_cuda(e);
+      if (d.pair_clusters < 1) {
+        d.ready = true;
+        d.status = GA_ERR_DEVICE;
+        *out = &d;
+        return d.status;
+      }
       if ((e = GA_CUDA(attn_upload_sigmoid_table(sigmoid_table()))) != cudaSuccess)
         return fail_cuda(e);
       if ((e = GA_CUDA(cudaGetSymbolAddress(&sw, g_device_status))) != cudaSuccess) return fail_cuda(e);
@@ -175,8 +183,8 @@ int encode_q_map(CUtensorMap* map, const void* base, long long rows, int box_hea
 }
 
 // [n_seq][cap][2][256] e4m3 key or value rows as a TMA tensor: box = one head's 256 codes x
-// 128 tokens of one sequence, unswizzled (the edge warps widen it to the swizzled bf16 tile);
-// tokens past the cache read as zeros.
+// 8 tokens of one sequence (an eighth of one CTA's 64 keys of a 128-key tile), unswizzled
+// (the edge warps widen it to the swizzled bf16 tile); tokens past the cache read as zeros.
 int encode_kv8_map(CUtensorMap* map, const void* base, long long cap, long long n_seq) {
   EncodeTiledFn enc;
   int st = get_encode(&enc);
@@ -184,7 +192,7 @@ int encode_kv8_map(CUtensorMap* map, const void* base, long long cap, long long 
   cuuint64_t dims[4] = {(cuuint64_t)kDim, (cuuint64_t)kKvHeads, (cuuint64_t)cap, (cuuint64_t)n_seq};
   cuuint64_t strides[3] = {(cuuint64_t)kDim, (cuuint64_t)kKvHeads * kDim,
                            (cuuint64_t)cap * kKvHeads * kDim};
-  cuuint32_t box[4] = {(cuuint32_t)kDim, 1, (cuuint32_t)kTileN, 1};
+  cuuint32_t box[4] = {(cuuint32_t)kDim, 1, 8, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = GA_CUDA(enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
                            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -433,7 +441,11 @@ int verify_run(const ga_bf16* qg, const VerifyCaches& c, const int* seq_len, int
       st = encode_kv_map(&tm_v, c.v + (size_t)g0 * seq_elems, c.cap, n, true);
       if (st != GA_OK) return st;
     }
-    const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
+    int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
+    if (fp8) {   // clusters of two CTAs (the two halves of a query group), as many as fit
+      const int pairs = a.n_items / 2;
+      grid = 2 * (pairs < dev->pair_clusters ? pairs : dev->pair_clusters);
+    }
     // the verify partials have no gated epilogue: tm_q stands in for the unused gate map
     if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_q, a, grid, s))) != cudaSuccess)
       return fail_cuda(e);

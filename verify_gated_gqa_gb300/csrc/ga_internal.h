@@ -133,6 +133,8 @@ cudaError_t launch_select_mask(const float* scores, long long ld_scores, int row
                                int q_base, int top_k, uint8_t* mask, long long ld_mask,
                                cudaStream_t s);
 cudaError_t attn_set_smem_attribute();
+// Clusters of two attention CTAs (the e4m3 verify variant) that can run at once.
+cudaError_t attn_max_pair_clusters(int* n);
 // Test hook (ga_debug.cu): fp32 tensor-core dot products of n_tiles pairs of 128 x 256 bf16
 // tiles, s[n][i][j] = q[n][i] . k[n][j].
 cudaError_t probe_set_smem_attribute();

@@ -50,14 +50,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same try with acquire at cluster scope: for barriers that a peer CTA of the cluster
+// completes (release.cluster arrivals) after writing into this CTA's shared memory.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase with the given parity to complete. Returns false (and
 // raises *abort) on timeout, or at once if another thread of the CTA raised *abort.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           long long limit = kWaitCycles) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto try_once = [&]() {
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (try_once()) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_once()) return true;
     if (*abort) return false;
     if (clock64() - t0 > limit) {
       *abort = kDevWaitTimeout;
@@ -76,9 +93,71 @@ __device__ __forceinline__ bool mbar_wait_quiet(uint64_t* bar, uint32_t parity, 
   return true;
 }
 
+// ------------------------------------------------------------------ clusters (pairs of CTAs)
+// The CTA's rank in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address, in the cluster's shared-memory window, of the same offset in CTA `rank`'s
+// shared memory as the local address `saddr`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+// 16-byte store into (possibly another CTA's) shared memory by a cluster address.
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t caddr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+// Arrive, with release at cluster scope, on an mbarrier of another CTA of the cluster
+// (caddr from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
+               : "memory");
+}
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's
+// shared memory to another CTA's of the cluster (dst and the completion barrier as cluster
+// addresses from mapa_shared); the copy engine reports the bytes on that barrier
+// (complete_tx), as a TMA load does.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_caddr, const void* src,
+                                                  uint32_t bytes, uint32_t bar_caddr) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_caddr),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar_caddr)
+      : "memory");
+}
+// Arrive on a local mbarrier and raise its expected transaction bytes in one step.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Arrive `count` times at once on a local mbarrier.
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+// Every thread of both CTAs of the cluster: arrive (release) and wait (acquire). Used once,
+// on the way out of a paired kernel, so that no CTA leaves while its peer may still write
+// into its shared memory or arrive on its barriers.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 // ------------------------------------------------------------------ proxies and fences
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// The same for shared memory of the whole cluster: generic-proxy writes (also into a peer
+// CTA's shared memory) ordered before async-proxy reads of it (the peer's tensor cores).
+__device__ __forceinline__ void fence_async_smem_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ TMA
