@@ -860,19 +860,25 @@ __device__ __forceinline__ void gate_from_tile(const uint8_t* tile, int r, uint4
   }
 }
 
-// bf16(sigmoid(g)) of the 256 gates in sg, in place, from the table. The gates are
-// processed 8 at a time through a rotating register queue: the loop body stays small,
-// because this code shares the instruction cache with the softmax loop running on the same
-// SM sub-partition, and a long unrolled body evicts it.
+// bf16(sigmoid(g)) of the 256 gates in sg, in place, from the table. The table (128 KB) does
+// not fit in the L1 left beside the shared memory, so each lookup is an L2 read: the gates
+// go 32 at a time (64 independent lookups in flight), through a register queue that moves on
+// by 4 entries per round. The loop body stays short: this code shares the instruction cache
+// with the softmax loop on the same SM sub-partition.
 __device__ void gate_sigmoid(uint4 (&sg)[kDim / 8]) {
+  constexpr int kPer = 4;   // queue entries (8 gates each) per round
 #pragma unroll 1
-  for (int step = 0; step < kDim / 8; ++step) {
-    const uint4 g = sg[0];
-    const uint4 o = make_uint4(sigmoid_pair(g.x), sigmoid_pair(g.y), sigmoid_pair(g.z),
-                               sigmoid_pair(g.w));
+  for (int round = 0; round < kDim / 8 / kPer; ++round) {
+    uint4 o[kPer];
 #pragma unroll
-    for (int i = 0; i < kDim / 8 - 1; ++i) sg[i] = sg[i + 1];
-    sg[kDim / 8 - 1] = o;
+    for (int i = 0; i < kPer; ++i) {
+      const uint4 g = sg[i];
+      o[i] = make_uint4(sigmoid_pair(g.x), sigmoid_pair(g.y), sigmoid_pair(g.z), sigmoid_pair(g.w));
+    }
+#pragma unroll
+    for (int i = 0; i < kDim / 8 - kPer; ++i) sg[i] = sg[i + kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) sg[kDim / 8 - kPer + i] = o[i];
   }
 }
 
