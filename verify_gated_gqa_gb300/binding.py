@@ -41,6 +41,7 @@ _SIGS = {
     "ga_q_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "ga_debug_wait_timeout": (_I, [_LL, _P]),
     "ga_debug_qk_fp32": (_I, [_P, _P, _I, _P, _P]),
+    "ga_debug_set_cta_pairs": (_I, [_I]),
     "ga_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "ga_attn_prefill_prepared": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "ga_attn_prefill_kv": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
@@ -141,6 +142,12 @@ def ga_status_string(status: int) -> str:
 
 def ga_debug_cuda_calls() -> int:
     return lib().ga_debug_cuda_calls()
+
+
+def ga_debug_set_cta_pairs(enable: bool) -> bool:
+    """Run the causal, bidirectional and stored-mask passes as CTA pairs (the default) or as
+    single CTAs; the same bits either way. Returns the previous setting."""
+    return bool(lib().ga_debug_set_cta_pairs(1 if enable else 0))
 
 
 def ga_device_status(clear: bool = True) -> int:

@@ -78,6 +78,7 @@ __device__ __forceinline__ uint32_t raw_piece_offset(int w, int s, uint32_t rank
 }
 constexpr int kChunkBytes = kTileN * 128;     // 128 keys x 64 dims of bf16
 constexpr int kTileBytes = 4 * kChunkBytes;   // 128 keys x 256 dims
+constexpr int kHalfTileBytes = kTileBytes / 2;   // a CTA pair: each CTA's half of a K or V tile
 constexpr int kThreads = 512;     // four warpgroups
 constexpr int kEdgeThread0 = 384; // first thread of the edge warpgroup (warps 12-15)
 // Register split (setmaxnreg): the kernel is launched at kLaunchRegs per thread; the
@@ -147,15 +148,20 @@ __device__ __forceinline__ int item_index(int round, int cta, int G) {
 
 // The item a CTA takes in a round. Over e4m3 caches the CTAs run in clusters of two (ranks
 // blockIdx.x % 2): the pair takes the items 2p and 2p + 1, the two halves of one query
-// group over the same key chunk, the pairs dealt like single items.
-template <int kMode>
+// group over the same key chunk, the pairs dealt like single items. CTA pairs of the
+// gated passes (kPair) deal pair items to the clusters; both CTAs take the same one.
+template <int kMode, bool kPair = false>
 __device__ __forceinline__ int walk_index(int round) {
   if (kMode == kModeVerify8)
     return 2 * item_index(round, blockIdx.x >> 1, gridDim.x >> 1) + (blockIdx.x & 1);
+  if (kPair) return item_index(round, blockIdx.x >> 1, gridDim.x >> 1);
   return item_index(round, blockIdx.x, gridDim.x);
 }
 
-template <int kMode>
+// CTA pairs (kPair): item idx is (row tile, pair of neighbouring query heads of one KV
+// group); the even CTA of the cluster takes the first head, the odd one the second, so
+// both walk the same key tiles under the same visibility.
+template <int kMode, bool kPair = false>
 __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
   Item it;
   it.seq = it.half = it.kt0 = 0;
@@ -193,8 +199,9 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
     it.n = max(0, min(a.chunk_tiles, tiles - it.kt0));
     return it;
   }
-  it.mt = a.row_tiles - 1 - idx / a.n_heads;  // later row tiles see more keys: longest first
-  it.h = a.head0 + idx % a.n_heads;
+  const int per_tile = kPair ? a.n_heads / 2 : a.n_heads;
+  it.mt = a.row_tiles - 1 - idx / per_tile;  // later row tiles see more keys: longest first
+  it.h = a.head0 + (kPair ? 2 * (idx % per_tile) + (int)(blockIdx.x & 1) : idx % per_tile);
   if (kMode == kModeCausal) {
     const int last_row = min(a.rows, (it.mt + 1) * kTileM) - 1;
     const int key_end = min(a.T, a.q_base + last_row + 1);
@@ -245,14 +252,14 @@ struct TileCursor {
 
 // The CTA's sequence of work items that have key tiles (items without any, in mask
 // mode, are skipped here and answered by the edge warps).
-template <int kMode>
+template <int kMode, bool kPair = false>
 struct ItemWalk {
   int round = 0;
   __device__ __forceinline__ bool next(const AttnArgs& a, Item& out) {
     for (;; ++round) {
-      const int idx = walk_index<kMode>(round);
+      const int idx = walk_index<kMode, kPair>(round);
       if (idx >= a.n_items) return false;
-      out = make_item<kMode>(a, idx);
+      out = make_item<kMode, kPair>(a, idx);
       if (out.n > 0) {
         ++round;
         return true;
@@ -267,13 +274,41 @@ __device__ __forceinline__ void record_abort(int* status, int code) {
 
 // Wait in all 32 lanes and agree on the outcome, so that the warp-collective TMEM loads and
 // stores (and elected MMA issues) that follow always run with the whole warp (or the whole warp leaves).
+// kCluster: acquire at cluster scope, for barriers that the peer CTA of a pair arrives on.
+template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  const bool ok = mbar_wait(bar, parity, abort);
+  const bool ok = mbar_wait<kCluster>(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
 }
 
+// The MMA issue and commit forms of a single CTA or of a CTA pair (cta_group::2).
+template <bool kPair>
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if (kPair) umma_ts_pair_warp(d, a, b, id, acc);
+  else umma_ts_warp(d, a, b, id, acc);
+}
+template <bool kPair>
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if (kPair) umma_ss_pair_warp(d, a, b, id, acc);
+  else umma_ss_warp(d, a, b, id, acc);
+}
+// A pair's commit arrives on the barrier of both CTAs.
+template <bool kPair>
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  if (kPair) umma_commit_pair_both_warp(bar);
+  else umma_commit_warp(bar);
+}
+// One arrival of a consumer warp (or thread) on a barrier the MMA warps wait on: per thread
+// in a single CTA; per warp, on the even CTA's barrier, in a pair (kRelease: at cluster
+// scope, after generic shared-memory writes the pair's MMAs read).
+template <bool kPair, bool kRelease = false>
+__device__ __forceinline__ void arrive_for_mma(uint64_t* bar) {
+  if (kPair) mbar_arrive_warp_at<kRelease>(bar, 0);
+  else mbar_arrive(bar);
+}
+
 // ------------------------------------------------------------------ warp 0: producer
-template <int kMode, bool kW>
+template <int kMode, bool kW, bool kPair>
 __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                               const CUtensorMap* tm_v, const CUtensorMap* tm_g, const AttnArgs& a,
                               volatile int* abort, uint32_t& cnt) {
@@ -304,7 +339,7 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
     ++cnt;
     return true;
   };
-  ItemWalk<kMode> walk;
+  ItemWalk<kMode, kPair> walk;
   Item it;
   while (walk.next(a, it)) {
     const int kvh = it.h / kGroup;
@@ -356,13 +391,35 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
       ++cnt;
       return true;
     };
+    // CTA pairs: this CTA's half of a K or V tile into the front of the slot (K: keys
+    // 64 rank .. + 63 of the tile, four 8 KiB blocks of 64 dims; V: dims 128 rank .. + 127,
+    // two 16 KiB blocks of 128 keys). Its bytes complete on the even CTA's full barrier,
+    // which expects both halves; the odd CTA's own barrier only counts the fill, so that
+    // its phases keep step with the ring (its edge warps wait there for Q and gate tiles).
+    auto load_half = [&](const CUtensorMap* map, bool is_v, int kt) -> bool {
+      const uint32_t slot = cnt % kSlots;
+      const uint32_t rank = blockIdx.x & 1;
+      if (!warp_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
+      if (rank == 0) mbar_expect_tx_warp(&sm.full[slot], 2 * kHalfTileBytes);
+      else mbar_arrive_elect_warp(&sm.full[slot]);
+      const uint32_t bar = mapa_shared(smem_u32(&sm.full[slot]), 0);
+      if (is_v)
+        tma_load_4d_pair_warp(sm.tile[slot], map, bar, 0, kt * kTileN, kvh, 2 * (int)rank);
+      else
+        tma_load_4d_pair_warp(sm.tile[slot], map, bar, 0, kt * kTileN + kHalfKeys * (int)rank,
+                              kvh, 0);
+      ++cnt;
+      return true;
+    };
     auto load_k = [&](int kt) -> bool {
+      if (kPair) return load_half(tm_k, false, kt);
       if (kMode == kModeVerify8) return load_raw8(tm_k, kt);
       int r0;
       const int outer = kv_at(kt, r0);
       return load_tile(tm_k, true, kvh, r0, outer, kTileBytes);
     };
     auto load_v = [&](int kt) -> bool {
+      if (kPair) return load_half(tm_v, true, kt);
       if (kMode == kModeVerify8) return load_raw8(tm_v, kt);
       int r0;
       const int outer = kv_at(kt, r0);
@@ -391,13 +448,20 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
   }
 }
 
-template <int kMode, bool kW>
+template <int kMode, bool kW, bool kPair>
 __device__ void producer(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                          const CUtensorMap* tm_v, const CUtensorMap* tm_g, const AttnArgs& a,
                          volatile int* abort) {
   uint32_t cnt = 0;
-  producer_loop<kMode, kW>(sm, tm_q, tm_k, tm_v, tm_g, a, abort, cnt);
+  producer_loop<kMode, kW, kPair>(sm, tm_q, tm_k, tm_v, tm_g, a, abort, cnt);
   if (*abort) {
+    if (kPair && (blockIdx.x & 1) && cnt > 0) {
+      // this CTA's K and V halves complete on the peer's barriers, not on its own: give the
+      // copies in flight (from memory: microseconds) about a millisecond to land
+      const long long t0 = clock64();
+      while (clock64() - t0 < (1LL << 21)) {
+      }
+    }
     // let the loads already issued into the slots land before exit
     const uint32_t first = cnt > (uint32_t)kSlots ? cnt - kSlots : 0;
     for (uint32_t c = first; c < cnt; ++c)
@@ -436,16 +500,19 @@ struct RingWalk {
 // descriptors advance by constants (addresses in 16-byte units in the low field): K by
 // 32 bytes per k-step inside a 64-dim block and 16 KiB per block; P by 32 bytes per k-step
 // inside a 64-key block and 16 KiB per block; V by 2 KiB per k-step; a slot is 64 KiB.
-template <int kMode, bool kW>
+template <int kMode, bool kW, bool kPair>
 __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
-  constexpr uint32_t kIdQK = idesc_bf16(128, kTileN, false, false);
+  // a pair: M = 256 (both CTAs' rows), each CTA holding 64 of the tile's keys, so a 64-dim
+  // block of this CTA's K is 8 KiB
+  constexpr uint32_t kIdQK = idesc_bf16(kPair ? 256 : 128, kTileN, false, false);
+  constexpr uint32_t kKBlock = kPair ? kChunkBytes / 2 : kChunkBytes;
   const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), 16, 1024);
   const uint64_t qhi_desc0 = sdesc_sw128(smem_u32(sm.qhi[0]), 16, 1024);
   RingWalk<kMode> ring;
   uint32_t g = 0;         // global key-tile counter: S phases
   uint32_t it_done = 0;
   uint32_t slot;
-  ItemWalk<kMode> walk;
+  ItemWalk<kMode, kPair> walk;
   Item it;
   // V_idx, preceded by the gate tile when idx is 0
   auto walk_v = [&](int idx) -> bool {
@@ -454,30 +521,30 @@ __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
   };
   while (walk.next(a, it)) {
     if (!ring.next(sm, abort, slot)) return;            // the item's Q tile (edge warps)
-    if (!warp_wait(&sm.q_full, it_done & 1, abort)) return;
+    if (!warp_wait<kPair>(&sm.q_full, it_done & 1, abort)) return;
     for (int j = 0; j < it.n; ++j, ++g) {
       if (!kW && j >= 2 && !walk_v(j - 2)) return;      // V_{j-2}
       if (!ring.next(sm, abort, slot)) return;          // K_j
       // S is free once the softmax warps have copied the previous tile's S out
-      if (g > 0 && !warp_wait(&sm.s_free, (g - 1) & 1, abort)) return;
+      if (g > 0 && !warp_wait<kPair>(&sm.s_free, (g - 1) & 1, abort)) return;
       tc_fence_after();
       const uint64_t kd0 = k_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
       // dims 0..127 with Q from tensor memory, dims 128..255 with Q from shared memory
 #pragma unroll
       for (int kk = 0; kk < kDim / 32; ++kk) {
-        const uint64_t bd = kd0 + (uint64_t)((kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2);
-        umma_ts_warp(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, kIdQK, kk > 0 ? 1u : 0u);
+        const uint64_t bd = kd0 + (uint64_t)((kk >> 2) * (kKBlock >> 4) + (kk & 3) * 2);
+        mma_ts<kPair>(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, kIdQK, kk > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = kDim / 32; kk < kDim / 16; ++kk) {
         const uint32_t blk = (kk >> 2) - 2;
-        const uint64_t bd = kd0 + (uint64_t)((kk >> 2) * (kChunkBytes >> 4) + (kk & 3) * 2);
+        const uint64_t bd = kd0 + (uint64_t)((kk >> 2) * (kKBlock >> 4) + (kk & 3) * 2);
         const uint64_t ad = qhi_desc0 + (uint64_t)(blk * (kChunkBytes >> 4) + (kk & 3) * 2);
-        umma_ss_warp(tmem + kTmemS, ad, bd, kIdQK, 1u);
+        mma_ss<kPair>(tmem + kTmemS, ad, bd, kIdQK, 1u);
       }
-      umma_commit_warp(&sm.empty[slot]);
-      umma_commit_warp(&sm.s_full);
-      if (j == it.n - 1) umma_commit_warp(&sm.q_empty);
+      mma_commit<kPair>(&sm.empty[slot]);
+      mma_commit<kPair>(&sm.s_full);
+      if (j == it.n - 1) mma_commit<kPair>(&sm.q_empty);
     }
     if (!kW) {
       if (it.n >= 2 && !walk_v(it.n - 2)) return;       // V_{n-2}
@@ -487,15 +554,17 @@ __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
   }
 }
 
-template <int kMode>
+// A pair's V half is its two 64-dim blocks of 128 keys (N = 256 over the pair), at the same
+// block stride as a whole tile's.
+template <int kMode, bool kPair>
 __device__ void pv_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
-  constexpr uint32_t kIdPV = idesc_bf16(128, kDim, false, true);
+  constexpr uint32_t kIdPV = idesc_bf16(kPair ? 256 : 128, kDim, false, true);
   const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), kChunkBytes, 1024);
   RingWalk<kMode> ring;
   uint32_t g = 0;         // global key-tile counter: P and P V phases
   uint32_t it_done = 0;
   uint32_t slot;
-  ItemWalk<kMode> walk;
+  ItemWalk<kMode, kPair> walk;
   Item it;
   while (walk.next(a, it)) {
     if (!ring.next(sm, abort, slot)) return;            // Q
@@ -504,44 +573,45 @@ __device__ void pv_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
       if (j + 1 < it.n && !ring.next(sm, abort, slot)) return;   // K_{j+1}
       if (has_gate<kMode, false>() && j == 0 && !ring.next(sm, abort, slot)) return;   // gate
       if (!ring.next(sm, abort, slot)) return;                   // V_j
-      if (j == 0 && it_done > 0 && !warp_wait(&sm.o_free, (it_done - 1) & 1, abort)) return;
+      if (j == 0 && it_done > 0 && !warp_wait<kPair>(&sm.o_free, (it_done - 1) & 1, abort)) return;
       const uint64_t bd0 = v_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
       // The two 64-key halves of P go separately: each softmax warpgroup writes its half
       // of the next tile as soon as this tile's P V has read that half.
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
-        if (!warp_wait(&sm.p_full[hb], g & 1, abort)) return;
+        if (!warp_wait<kPair>(&sm.p_full[hb], g & 1, abort)) return;
         tc_fence_after();
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           const int kk = 4 * hb + k4;
-          umma_ts_warp(tmem + kTmemO, tmem + kTmemP + hb * (kHalfKeys / 2) + k4 * 8,
-                       bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
-                       (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts<kPair>(tmem + kTmemO, tmem + kTmemP + hb * (kHalfKeys / 2) + k4 * 8,
+                        bd0 + (uint64_t)(kk * (2048 >> 4)), kIdPV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
         }
         // p_empty[1] also tells the softmax that O holds every P V so far
-        umma_commit_warp(&sm.p_empty[hb]);
+        mma_commit<kPair>(&sm.p_empty[hb]);
       }
-      umma_commit_warp(&sm.empty[slot]);
+      mma_commit<kPair>(&sm.empty[slot]);
     }
-    umma_commit_warp(&sm.o_done);
+    mma_commit<kPair>(&sm.o_done);
     ++it_done;
   }
 }
 
 // Issue every MMA, then wait (bounded) until all of them completed, so that tensor
 // memory is never released under an MMA in flight.
-template <int kMode, bool kW>
+template <int kMode, bool kW, bool kPair>
 __device__ void mma_issuer(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort,
                            bool pv_warp) {
   uint64_t* drain = pv_warp ? &sm.drain_pv : &sm.drain;
   if (pv_warp) {
     if (kW) return;   // the weights pass has no P V
-    pv_loop<kMode>(sm, a, tmem, abort);
+    pv_loop<kMode, kPair>(sm, a, tmem, abort);
   } else {
-    qk_loop<kMode, kW>(sm, a, tmem, abort);
+    qk_loop<kMode, kW, kPair>(sm, a, tmem, abort);
   }
-  umma_commit_warp(drain);
+  if (kPair) umma_commit_pair_local_warp(drain);
+  else umma_commit_warp(drain);
   mbar_wait_quiet(drain, 0, 100000000LL);
 }
 
@@ -640,7 +710,7 @@ __device__ __forceinline__ void weights_half(const AttnArgs& a, const uint32_t (
 }
 
 // Softmax of one 64-key half (hf) of every S tile, one query row per thread.
-template <int kMode, bool kW>
+template <int kMode, bool kW, bool kPair>
 __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, int hf,
                                volatile int* abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -649,7 +719,7 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
   const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
   const uint32_t s_taddr = tmem + kTmemS + lane_off + kHalfKeys * hf;
   uint32_t g = 0, it_done = 0;
-  ItemWalk<kMode> walk;
+  ItemWalk<kMode, kPair> walk;
   Item it;
   while (walk.next(a, it)) {
     const int row = it.mt * kTileM + r;   // the row within its sequence
@@ -688,7 +758,7 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
       tmem_ld32(s_taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(sb + 32));
       tmem_wait_ld(sb);
       tc_fence_before();
-      mbar_arrive(&sm.s_free);   // the next S = Q K^T may overwrite S once both halves are out
+      arrive_for_mma<kPair>(&sm.s_free);   // the next S = Q K^T may overwrite S once both halves are out
       if (kMode == kModeMask) {
 #pragma unroll
         for (int k = 0; k < kHalfKeys / 2; ++k)
@@ -790,7 +860,7 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
                 *reinterpret_cast<uint32_t(*)[32]>(sb));
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&sm.p_full[hf]);
+      arrive_for_mma<kPair>(&sm.p_full[hf]);
     }
     if (!kW) {
       // hand this half's l (and M) of the item to the edge warps
@@ -809,6 +879,7 @@ __device__ void softmax_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, i
 // column c), dims 128..255 as they are into the item's Q blocks in shared memory (the same
 // swizzled layout, read by the tensor cores). Every lane of the warp runs it
 // (warp-collective stores). Lanes with `have` false (verify padding) store zeros.
+template <bool kPair>
 __device__ __forceinline__ void q_copy(const uint8_t* tile, int r, bool have, uint32_t q_taddr,
                                        uint8_t (&qhi)[2][kChunkBytes]) {
 #pragma unroll
@@ -833,7 +904,9 @@ __device__ __forceinline__ void q_copy(const uint8_t* tile, int r, bool have, ui
     }
   }
   tmem_wait_st();
-  fence_async_smem();   // the tensor cores read the shared-memory half
+  // the tensor cores read the shared-memory half (a pair's: MMAs the peer CTA issues)
+  if (kPair) fence_async_smem_cluster();
+  else fence_async_smem();
 }
 
 // bf16(sigmoid(g)) for every bf16 g (index: g's bits), exact from the double definition;
@@ -901,6 +974,7 @@ __device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r, bool
 // of bf16 kept in a register: 128 words for the row, the gate registers freed as they are
 // used) and released at once, so the next item's first P V waits only for the reads; the
 // row's 512 bytes of stores follow while the next item runs.
+template <bool kPair>
 __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32_t tmem,
                          uint32_t lane_off, int r, uint32_t it_done, uint4 (&sg)[kDim / 8],
                          volatile int* abort) {
@@ -934,7 +1008,7 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
     }
   }
   tc_fence_before();
-  mbar_arrive(&sm.o_free);
+  arrive_for_mma<kPair>(&sm.o_free);
   mbar_arrive(&sm.st_empty);
   if (!valid) return true;
   uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)(it.row0 + row) * kOutRow + h * kDim);
@@ -1071,7 +1145,7 @@ __device__ bool widen_e4m3(AttnSmem& sm, uint32_t pos, const float (&scv)[kWideR
   return true;
 }
 
-template <int kMode, bool kW>
+template <int kMode, bool kW, bool kPair>
 __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -1082,9 +1156,9 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
   // the CTA's next item with key tiles; items without any are answered on the way
   auto next_item = [&](Item& out) -> bool {
     for (;; ++round) {
-      const int idx = walk_index<kMode>(round);
+      const int idx = walk_index<kMode, kPair>(round);
       if (idx >= a.n_items) return false;
-      out = make_item<kMode>(a, idx);
+      out = make_item<kMode, kPair>(a, idx);
       if (out.n > 0) {
         ++round;
         return true;
@@ -1104,10 +1178,10 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
     if (!warp_wait(&sm.full[slot], (q_pos / kSlots) & 1, abort)) return false;
     if (kMode == kModeVerify8) mbar_arrive(&sm.conv[slot]);
     tc_fence_after();
-    q_copy(sm.tile[slot], r, !is_verify<kMode>() || r < kVerifyHeadsPerTile * a.vrows, q_taddr,
-           sm.qhi);
+    q_copy<kPair>(sm.tile[slot], r, !is_verify<kMode>() || r < kVerifyHeadsPerTile * a.vrows,
+                  q_taddr, sm.qhi);
     tc_fence_before();
-    mbar_arrive(&sm.q_full);
+    arrive_for_mma<kPair, true>(&sm.q_full);
     mbar_arrive(&sm.q_read);
     if (threadIdx.x == kEdgeThread0) {
       if (!mbar_wait(&sm.q_read, q_takes & 1, abort)) return false;
@@ -1181,7 +1255,7 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
     if (have_next && !take_q(nxt, true, it_done)) return;
     if (is_verify<kMode>()) {
       if (!epilogue_partial(sm, a, cur, tmem, lane_off, r, it_done, abort)) return;
-    } else if (!kW && !epilogue(sm, a, cur, tmem, lane_off, r, it_done, sg, abort)) {
+    } else if (!kW && !epilogue<kPair>(sm, a, cur, tmem, lane_off, r, it_done, sg, abort)) {
       return;
     }
     ++it_done;
@@ -1191,43 +1265,57 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
   }
 }
 
-template <int kMode, bool kW>
+// kPair (causal, bidirectional and stored-mask passes): the kernel runs as clusters of two
+// CTAs that share each K and V tile. A pair item is one row tile of two neighbouring query
+// heads of a KV group (the even CTA's head first); the even CTA issues every MMA for both
+// (cta_group::2, M = 256: each CTA's 128 rows of Q, S, P and O stay in its own shared and
+// tensor memory), and each CTA loads only its half of every K and V tile, so each SM's
+// shared memory carries half the key and value traffic of a single CTA's. The tensor
+// cores' commits arrive on the barriers of both CTAs; the odd CTA's softmax and edge warps
+// arrive on the even CTA's barriers (one arrival per warp) for the MMA warps there.
+template <int kMode, bool kW, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                 const __grid_constant__ AttnArgs a) {
+  constexpr bool kCluster = kPair || kMode == kModeVerify8;
   // The dynamic shared memory is declared 1024-byte aligned (the 128-byte swizzle of TMA
   // and the MMA descriptors needs it); every thread checks it before using any of it.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((smem_u32(smem_raw) & 1023u) != 0u) {
     if (threadIdx.x == 0) record_abort(a.status, kDevBadLaunch);
-    if (kMode == kModeVerify8) {   // the peer's two cluster barriers (after set-up, at exit)
+    if (kCluster) {   // the peer's cluster barriers (after set-up, [before the release,] at exit)
       cluster_sync_all();
+      if (kPair) cluster_sync_all();
       cluster_sync_all();
     }
     return;
   }
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool leader = !kPair || (blockIdx.x & 1) == 0;   // a pair's MMA-issuing CTA
   volatile int* abort = &sm.abort;
   if (threadIdx.x == 0) {
     sm.abort = 0;
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&sm.full[i], 1);
       // refilled once both MMA warps have passed the fill and its consumer released it
-      // (weights pass: the score warp alone walks the ring)
-      mbar_init(&sm.empty[i], kW ? 2 : 3);
+      // (weights pass: the score warp alone walks the ring); in a pair's odd CTA, once its
+      // consumer released it (the pair's commit for K and V, its edge warps for Q and gate)
+      mbar_init(&sm.empty[i], !leader ? 1 : kW ? 2 : 3);
     }
-    mbar_init(&sm.q_full, 128);
+    // barriers the MMA warps wait on: per thread in a single CTA, per warp of both CTAs in
+    // a pair
+    mbar_init(&sm.q_full, kPair ? 8 : 128);
     mbar_init(&sm.q_empty, 1);
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, 256);       // both softmax warpgroups
+    mbar_init(&sm.s_free, kPair ? 16 : 256);       // both softmax warpgroups
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.p_full[i], 128);
+      mbar_init(&sm.p_full[i], kPair ? 8 : 128);
       mbar_init(&sm.p_empty[i], 1);
     }
     mbar_init(&sm.o_done, 1);
-    mbar_init(&sm.o_free, 128);
+    mbar_init(&sm.o_free, kPair ? 8 : 128);
     mbar_init(&sm.st_full, 256);
     mbar_init(&sm.st_empty, 128);
     mbar_init(&sm.drain, 1);
@@ -1250,39 +1338,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (has_gate<kMode, kW>()) tma_prefetch_desc(&tm_g);
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, kTmemCols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(&sm.tmem_base, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&sm.tmem_base, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
-  // over e4m3 caches the peer arrives on this CTA's barriers: both CTAs' barriers are
-  // initialised before either runs
-  if (kMode == kModeVerify8) cluster_sync_all();
+  // the peer arrives on this CTA's barriers (and, in a pair, its MMAs use this CTA's tensor
+  // memory): both CTAs' barriers are initialised and their columns allocated before either runs
+  if (kCluster) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // a pair's MMAs address both CTAs' tensor memory at the even CTA's column: both CTAs
+  // check that the allocation gave the same columns in each (else neither runs)
+  bool run = true;
+  if (kPair) {
+    const uint32_t other =
+        ld_shared_cluster_u32(mapa_shared(smem_u32(&sm.tmem_base), (blockIdx.x & 1) ^ 1u));
+    if (other != tmem) {
+      run = false;
+      if (threadIdx.x == 0) record_abort(a.status, kDevBadLaunch);
+    }
+  }
 
-  if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
-    if (warp == 0) producer<kMode, kW>(sm, &tm_q, &tm_k, &tm_v, &tm_g, a, abort);
-    if (warp == 1 || warp == 2) mma_issuer<kMode, kW>(sm, a, tmem, abort, warp == 2);
-  } else if (warp < 12) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    softmax_worker<kMode, kW>(sm, a, tmem, (warp - 4) >> 2, abort);
-  } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEdge));
-    edge_worker<kMode, kW>(sm, a, tmem, abort);
+  if (run) {
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
+      if (warp == 0) producer<kMode, kW, kPair>(sm, &tm_q, &tm_k, &tm_v, &tm_g, a, abort);
+      if ((warp == 1 || warp == 2) && leader)
+        mma_issuer<kMode, kW, kPair>(sm, a, tmem, abort, warp == 2);
+    } else if (warp < 12) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+      softmax_worker<kMode, kW, kPair>(sm, a, tmem, (warp - 4) >> 2, abort);
+    } else {
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEdge));
+      edge_worker<kMode, kW, kPair>(sm, a, tmem, abort);
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // a pair: the even CTA's MMAs into this CTA's tensor memory have completed (its MMA warps
+  // waited for their last commits) and neither CTA arrives on the other's barriers any more
+  if (kPair) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if (kPair) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
   }
   if (threadIdx.x == 0 && sm.abort) record_abort(a.status, sm.abort);
   // a CTA of a pair leaves only when its peer no longer writes into its shared memory or
   // arrives on its barriers (every wait before this point is bounded)
-  if (kMode == kModeVerify8) cluster_sync_all();
+  if (kCluster) cluster_sync_all();
 }
 
 // Verify combine (TensorFold PR #1080, "qwen CUDA: long-prompt prefill 5.4x faster", the
@@ -1369,76 +1480,92 @@ cudaError_t attn_upload_sigmoid_table(const uint16_t* host_table) {
 
 cudaError_t attn_set_smem_attribute() {
   const int bytes = (int)attn_smem_bytes();
-  cudaError_t e;
-  if ((e = cudaFuncSetAttribute(attn_kernel<kModeCausal, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(attn_kernel<kModeBidir, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(attn_kernel<kModeMask, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(attn_kernel<kModeVerify, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(attn_kernel<kModeBatch, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(attn_kernel<kModeVerify8, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(attn_kernel<kModeMask, true>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  const void* kernels[] = {
+      (const void*)attn_kernel<kModeCausal, false, false>,
+      (const void*)attn_kernel<kModeBidir, false, false>,
+      (const void*)attn_kernel<kModeMask, false, false>,
+      (const void*)attn_kernel<kModeVerify, false, false>,
+      (const void*)attn_kernel<kModeBatch, false, false>,
+      (const void*)attn_kernel<kModeVerify8, false, false>,
+      (const void*)attn_kernel<kModeMask, true, false>,
+      (const void*)attn_kernel<kModeCausal, false, true>,
+      (const void*)attn_kernel<kModeBidir, false, true>,
+      (const void*)attn_kernel<kModeMask, false, true>,
+  };
+  for (const void* k : kernels) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
-cudaError_t attn_max_pair_clusters(int* n) {
+namespace {
+cudaLaunchConfig_t pair_config(unsigned grid, size_t smem, cudaStream_t s,
+                               cudaLaunchAttribute (&attr)[1]) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = attn_smem_bytes();
-  cudaLaunchAttribute attr[1];
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, attn_kernel<kModeVerify8, false>, &cfg);
+  return cfg;
+}
+}  // namespace
+
+cudaError_t attn_max_pair_clusters(int* n) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config(2, attn_smem_bytes(), nullptr, attr);
+  return cudaOccupancyMaxActiveClusters(n, attn_kernel<kModeVerify8, false, false>, &cfg);
+}
+
+cudaError_t attn_max_gated_pair_clusters(int* n) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config(2, attn_smem_bytes(), nullptr, attr);
+  return cudaOccupancyMaxActiveClusters(n, attn_kernel<kModeCausal, false, true>, &cfg);
 }
 
 cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                         const CUtensorMap& tm_g, const AttnArgs& a, int grid, cudaStream_t s) {
   const size_t smem = attn_smem_bytes();
+  if (a.pair || a.mode == kModeVerify8) {
+    // clusters of two CTAs (grid even)
+    if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config((unsigned)grid, smem, s, attr);
+    if (a.mode == kModeVerify8)
+      return cudaLaunchKernelEx(&cfg, attn_kernel<kModeVerify8, false, false>, tm_q, tm_k, tm_v,
+                                tm_g, a);
+    if (a.weights_pass) return cudaErrorInvalidValue;
+    if (a.mode == kModeCausal)
+      return cudaLaunchKernelEx(&cfg, attn_kernel<kModeCausal, false, true>, tm_q, tm_k, tm_v,
+                                tm_g, a);
+    if (a.mode == kModeBidir)
+      return cudaLaunchKernelEx(&cfg, attn_kernel<kModeBidir, false, true>, tm_q, tm_k, tm_v,
+                                tm_g, a);
+    if (a.mode == kModeMask)
+      return cudaLaunchKernelEx(&cfg, attn_kernel<kModeMask, false, true>, tm_q, tm_k, tm_v,
+                                tm_g, a);
+    return cudaErrorInvalidValue;
+  }
   if (a.weights_pass) {
     if (a.mode != kModeMask) return cudaErrorInvalidValue;
-    attn_kernel<kModeMask, true><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeMask, true, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else if (a.mode == kModeCausal) {
-    attn_kernel<kModeCausal, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeCausal, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else if (a.mode == kModeBidir) {
-    attn_kernel<kModeBidir, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeBidir, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else if (a.mode == kModeVerify) {
-    attn_kernel<kModeVerify, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeVerify, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else if (a.mode == kModeBatch) {
-    attn_kernel<kModeBatch, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
-  } else if (a.mode == kModeVerify8) {
-    // clusters of two CTAs (grid even): the pair shares the widening of each e4m3 tile
-    if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<kModeVerify8, false>, tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeBatch, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   } else {
-    attn_kernel<kModeMask, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeMask, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
   }
   return cudaGetLastError();
 }

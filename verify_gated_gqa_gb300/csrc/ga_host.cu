@@ -31,6 +31,7 @@ struct DeviceState {
   int status = GA_OK;  // GA_OK or GA_ERR_DEVICE / GA_ERR_CUDA from set-up
   int sm_count = 0;
   int pair_clusters = 0;  // clusters of two attention CTAs that fit at once (e4m3 verify)
+  int gated_pair_clusters = 0;  // the same for the CTA-pair gated passes
   int* status_word = nullptr;
 };
 DeviceState g_devices[kMaxDevices];
@@ -89,7 +90,9 @@ int current_device(DeviceState** out) {
       if ((e = GA_CUDA(attn_set_smem_attribute())) != cudaSuccess) return fail_cuda(e);
       if ((e = GA_CUDA(probe_set_smem_attribute())) != cudaSuccess) return fail_cuda(e);
       if ((e = GA_CUDA(attn_max_pair_clusters(&d.pair_clusters))) != cudaSuccess) return fail_cuda(e);
-      if (d.pair_clusters < 1) {
+      if ((e = GA_CUDA(attn_max_gated_pair_clusters(&d.gated_pair_clusters))) != cudaSuccess)
+        return fail_cuda(e);
+      if (d.pair_clusters < 1 || d.gated_pair_clusters < 1) {
         d.ready = true;
         d.status = GA_ERR_DEVICE;
         *out = &d;
@@ -129,12 +132,13 @@ int get_encode(EncodeTiledFn* fn) {
   return g_encode ? GA_OK : GA_ERR_DEVICE;
 }
 
-// [n_outer][n_tok][2][256] bf16 keys or values as a TMA tensor: box = 64 dims x 128 tokens
-// x 1 head x 4 blocks of 64 dims, 128-byte swizzle; tokens past the end read as zeros. With
-// seq_dim the sequence is the fifth coordinate (verify caches, n_outer >= 1 sequences);
+// [n_outer][n_tok][2][256] bf16 keys or values as a TMA tensor: box = 64 dims x box_tok
+// tokens x 1 head x box_blocks blocks of 64 dims (a whole tile: 128 x 4; a CTA pair's
+// halves: 64 x 4 for K, 128 x 2 for V), 128-byte swizzle; tokens past the end read as zeros.
+// With seq_dim the sequence is the fifth coordinate (verify caches, n_outer >= 1 sequences);
 // without it the map has four dimensions (n_outer must be 1).
 int encode_kv_map(CUtensorMap* map, const void* base, long long n_tok, long long n_outer,
-                  bool seq_dim) {
+                  bool seq_dim, int box_tok = kTileN, int box_blocks = kDim / 64) {
   EncodeTiledFn enc;
   int st = get_encode(&enc);
   if (st != GA_OK) return st;
@@ -145,7 +149,7 @@ int encode_kv_map(CUtensorMap* map, const void* base, long long n_tok, long long
                         (cuuint64_t)n_outer};
   cuuint64_t strides[4] = {(cuuint64_t)kKvHeads * kDim * 2, (cuuint64_t)kDim * 2, 64 * 2,
                            (cuuint64_t)n_tok * kKvHeads * kDim * 2};
-  cuuint32_t box[5] = {64, (cuuint32_t)kTileN, 1, (cuuint32_t)(kDim / 64), 1};
+  cuuint32_t box[5] = {64, (cuuint32_t)box_tok, 1, (cuuint32_t)box_blocks, 1};
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
   const cuuint32_t rank = seq_dim ? 5 : 4;
   CUresult r = GA_CUDA(enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
@@ -303,31 +307,44 @@ size_t verify_ws_bytes(const VerifyPlan& p) {
 // The query prologue (unless q_ready: q_prep already holds this call's prepared queries)
 // and the attention kernel. q_prep [rows][24][256] may be the output buffer itself: each
 // (row, head) slot is read by the work item that later writes its output there.
+std::atomic<bool> g_cta_pairs{true};   // ga_debug_set_cta_pairs
+
 int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const void* k_prep,
                      const void* v, long long n_tok, DeviceState* dev, cudaStream_t s) {
-  CUtensorMap tm_q, tm_k, tm_v, tm_g;
-  int st = encode_q_map(&tm_q, q_prep, a0.rows);
-  if (st != GA_OK) return st;
-  st = encode_gate_map(&tm_g, a0.qg, a0.rows);
-  if (st != GA_OK) return st;
-  st = encode_kv_map(&tm_k, k_prep, n_tok, 1, false);
-  if (st != GA_OK) return st;
-  st = encode_kv_map(&tm_v, v, n_tok, 1, false);
-  if (st != GA_OK) return st;
   AttnArgs a = a0;
   a.status = dev->status_word;
   if (a.n_heads == 0) {   // every query head unless the caller chose a KV-head group
     a.head0 = 0;
     a.n_heads = kHeads;
   }
+  // The causal and bidirectional passes run as CTA pairs (two query heads of one KV group
+  // per pair item) whenever the heads come in such pairs. The stored-mask pass (slower as
+  // pairs: its longer softmax puts the pair's extra synchronisation on the critical path)
+  // and the weights pass run on single CTAs.
+  const bool pair = g_cta_pairs.load() && !a.weights_pass &&
+                    (a.mode == kModeCausal || a.mode == kModeBidir) && a.head0 % 2 == 0 &&
+                    a.n_heads % 2 == 0;
+  a.pair = pair ? 1 : 0;
+  CUtensorMap tm_q, tm_k, tm_v, tm_g;
+  int st = encode_q_map(&tm_q, q_prep, a0.rows);
+  if (st != GA_OK) return st;
+  st = encode_gate_map(&tm_g, a0.qg, a0.rows);
+  if (st != GA_OK) return st;
+  st = pair ? encode_kv_map(&tm_k, k_prep, n_tok, 1, false, kTileN / 2, kDim / 64)
+            : encode_kv_map(&tm_k, k_prep, n_tok, 1, false);
+  if (st != GA_OK) return st;
+  st = pair ? encode_kv_map(&tm_v, v, n_tok, 1, false, kTileN, kDim / 128)
+            : encode_kv_map(&tm_v, v, n_tok, 1, false);
+  if (st != GA_OK) return st;
   a.row_tiles = (a.rows + kTileM - 1) / kTileM;
-  a.n_items = a.row_tiles * a.n_heads;
+  a.n_items = a.row_tiles * (pair ? a.n_heads / 2 : a.n_heads);
   cudaError_t e;
   if (!q_ready &&
       (e = GA_CUDA(launch_q_prologue(a.qg, a.w_q, a.cos_tab, a.sin_tab, a.rows, a.q_base, a.head0,
                                      a.n_heads, q_prep, dev->sm_count, s))) != cudaSuccess)
     return fail_cuda(e);
-  const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
+  const int cap = pair ? dev->gated_pair_clusters : dev->sm_count;
+  const int grid = (pair ? 2 : 1) * (a.n_items < cap ? a.n_items : cap);
   e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_g, a, grid, s));
   if (e != cudaSuccess) return fail_cuda(e);
   return GA_OK;
@@ -603,6 +620,8 @@ int ga_debug_wait_timeout(long long limit_cycles, ga_stream stream) {
   cudaError_t e = GA_CUDA(launch_wait_timeout(limit_cycles, dev->status_word, (cudaStream_t)stream));
   return e == cudaSuccess ? GA_OK : fail_cuda(e);
 }
+
+int ga_debug_set_cta_pairs(int enable) { return g_cta_pairs.exchange(enable != 0) ? 1 : 0; }
 
 int ga_debug_qk_fp32(const ga_bf16* q, const ga_bf16* k, int n_tiles, float* s,
                      ga_stream stream) {

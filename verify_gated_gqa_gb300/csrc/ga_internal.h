@@ -74,6 +74,9 @@ struct AttnArgs {
   int* status;              // device status word
   int rows, T, q_base, mode, weights_pass;
   int head0, n_heads;       // causal, bidirectional, stored mask: the query heads processed
+  int pair;                 // causal, bidirectional, stored mask: clusters of two CTAs that
+                            // share each K/V tile (n_items counts row tiles x head pairs;
+                            // tm_k / tm_v hold half tiles: box 64 x 64 x 1 x 4, 64 x 128 x 1 x 2)
   int row_tiles, key_tiles, mask_words;
   int n_items;
   // verify mode
@@ -135,6 +138,8 @@ cudaError_t launch_select_mask(const float* scores, long long ld_scores, int row
 cudaError_t attn_set_smem_attribute();
 // Clusters of two attention CTAs (the e4m3 verify variant) that can run at once.
 cudaError_t attn_max_pair_clusters(int* n);
+// The same for the CTA-pair variants of the causal, bidirectional and stored-mask passes.
+cudaError_t attn_max_gated_pair_clusters(int* n);
 // Test hook (ga_debug.cu): fp32 tensor-core dot products of n_tiles pairs of 128 x 256 bf16
 // tiles, s[n][i][j] = q[n][i] . k[n][j].
 cudaError_t probe_set_smem_attribute();

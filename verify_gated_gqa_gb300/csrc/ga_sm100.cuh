@@ -231,6 +231,22 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// CTA pairs (cta_group::2): one warp of each CTA of the pair allocates (and later frees)
+// the same columns of both CTAs' tensor memory, collectively.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05: MMA
 // D[tmem] (+)= A * B^T, kind::f16 (bf16 in, fp32 accumulate), with A from shared memory
 // (umma_ss_warp: two smem descriptors) or from tensor memory (umma_ts_warp: one row per
@@ -266,6 +282,101 @@ __device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
           smem_u32(bar))
       : "memory");
+}
+
+// The same MMAs for a CTA pair (cta_group::2), issued by the pair's even CTA only: M = 256,
+// rows 0..127 of A and D in the even CTA (its shared and tensor memory), rows 128..255 in
+// the odd CTA at the same addresses; B's N rows split the same way, the first half in the
+// even CTA's shared memory and the second in the odd CTA's, at the same address.
+__device__ __forceinline__ void umma_ss_pair_warp(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_pair_warp(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Commit of the pair's MMAs issued so far by this thread: one arrival on the barrier at the
+// same shared-memory offset in both CTAs of the pair (multicast), or on this CTA's only.
+__device__ __forceinline__ void umma_commit_pair_both_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}\n" ::"r"(smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair_local_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// Tensor load into this CTA's shared memory whose bytes complete on an mbarrier of either CTA
+// of the pair (bar_caddr: a cluster address from mapa_shared), elected lane of a warp.
+__device__ __forceinline__ void tma_load_4d_pair_warp(void* dst, const CUtensorMap* map,
+                                                      uint32_t bar_caddr, int c0, int c1, int c2,
+                                                      int c3) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_caddr), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster with the default semantics (release at
+// CTA scope): enough where the arrival only orders the thread's completed tensor-memory
+// accesses (tcgen05.wait::ld / ::st, then tcgen05.fence::before_thread_sync) before the
+// peer's next MMA. A release at cluster scope also waits until the thread's earlier memory
+// operations are visible to the cluster, which cost the arriving warp 1,000 to 1,600 cycles
+// per arrival in the attention kernel's softmax.
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+// One arrival of the warp, after every lane got here, on an mbarrier of CTA `rank` of the
+// cluster: a plain local arrival when that is this CTA, else a remote one (kRelease: with
+// release at cluster scope, for generic shared-memory writes the peer's tensor cores read;
+// otherwise as mbar_arrive_remote_cta).
+template <bool kRelease = false>
+__device__ __forceinline__ void mbar_arrive_warp_at(uint64_t* bar, uint32_t rank) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (rank == cluster_ctarank()) mbar_arrive(bar);
+    else if (kRelease) mbar_arrive_remote(mapa_shared(smem_u32(bar), rank));
+    else mbar_arrive_remote_cta(mapa_shared(smem_u32(bar), rank));
+  }
+}
+// A plain arrival (no transaction bytes) by the elected lane of a warp.
+__device__ __forceinline__ void mbar_arrive_elect_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}\n" ::"r"(smem_u32(bar))
+      : "memory");
+}
+// A 32-bit load from (possibly another CTA's) shared memory by a cluster address.
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t caddr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+  return v;
 }
 
 // Instruction descriptor, kind::f16 with bf16 A and B and an fp32 accumulator.
