@@ -65,7 +65,10 @@
 namespace ga {
 namespace {
 
-constexpr int kSlots = 3;
+constexpr int kSlots = 3;       // single CTAs: a ring of three 64 KiB slots (Q, gate, K, V tiles)
+constexpr int kPairSlots = 4;   // CTA pairs: four 32 KiB slots for K and V halves, then a
+                                // 64 KiB staging buffer (Q tiles, gate tiles, output tiles)
+constexpr int kMaxSlots = 4;
 // e4m3 caches: each CTA of a pair holds the codes of its 64 keys of a tile (64 x 256 bytes)
 // until they are widened, in eight 2 KiB pieces of 8 keys, each inside rows that only one
 // edge warp writes: edge warp w widens keys 16w .. 16w+15 of the CTA's half into bf16 rows
@@ -79,6 +82,10 @@ __device__ __forceinline__ uint32_t raw_piece_offset(int w, int s, uint32_t rank
 constexpr int kChunkBytes = kTileN * 128;     // 128 keys x 64 dims of bf16
 constexpr int kTileBytes = 4 * kChunkBytes;   // 128 keys x 256 dims
 constexpr int kHalfTileBytes = kTileBytes / 2;   // a CTA pair: each CTA's half of a K or V tile
+static_assert(kPairSlots * kHalfTileBytes + kTileBytes == kSlots * kTileBytes,
+              "a pair's ring and staging buffer take the single ring's bytes");
+template <bool kPair>
+__host__ __device__ constexpr int ring_slots() { return kPair ? kPairSlots : kSlots; }
 constexpr int kThreads = 512;     // four warpgroups
 constexpr int kEdgeThread0 = 384; // first thread of the edge warpgroup (warps 12-15)
 // Register split (setmaxnreg): the kernel is launched at kLaunchRegs per thread; the
@@ -117,15 +124,26 @@ struct AttnSmem {
   float stat_l[2][kTileM];            // softmax -> edge: each half's row sum l of the item
   float stat_m[kTileM];               // and the running maximum M
   uint16_t mx[2][2][kTileM];          // tile g: each half's row maximum (bf16 bits), by g % 2
-  uint64_t full[kSlots], empty[kSlots];
+  uint64_t full[kMaxSlots], empty[kMaxSlots];
   uint64_t conv[kSlots];              // e4m3 caches: the slot's tile is widened (or seen: Q)
   uint64_t peer_free[kSlots];         // e4m3 caches: the peer's slot is free for the next fill
   uint64_t q_full, q_empty, s_full, s_free;
   uint64_t p_full[2], p_empty[2];     // per 64-key half of P
   uint64_t o_done, o_free, st_full, st_empty, drain, drain_pv, q_read, g_read, mx_bar;
+  uint64_t stg_full, stg_empty, o_st;   // CTA pairs: the staging buffer, the output tile in it
   uint32_t tmem_base;
   int abort;
 };
+
+// A ring slot's bytes: slot s of the single ring, or of a pair's ring of half tiles; a pair's
+// staging buffer follows its ring.
+template <bool kPair>
+__device__ __forceinline__ uint8_t* slot_ptr(AttnSmem& sm, uint32_t s) {
+  return reinterpret_cast<uint8_t*>(sm.tile) + s * (uint32_t)(kPair ? kHalfTileBytes : kTileBytes);
+}
+__device__ __forceinline__ uint8_t* staging_ptr(AttnSmem& sm) {
+  return reinterpret_cast<uint8_t*>(sm.tile) + kPairSlots * kHalfTileBytes;
+}
 
 // ------------------------------------------------------------------ work items
 struct Item {
@@ -391,23 +409,22 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
       ++cnt;
       return true;
     };
-    // CTA pairs: this CTA's half of a K or V tile into the front of the slot (K: keys
-    // 64 rank .. + 63 of the tile, four 8 KiB blocks of 64 dims; V: dims 128 rank .. + 127,
-    // two 16 KiB blocks of 128 keys). Its bytes complete on the even CTA's full barrier,
-    // which expects both halves; the odd CTA's own barrier only counts the fill, so that
-    // its phases keep step with the ring (its edge warps wait there for Q and gate tiles).
+    // CTA pairs: this CTA's half of a K or V tile into a 32 KiB slot of the pair ring (K:
+    // keys 64 rank .. + 63 of the tile, four 8 KiB blocks of 64 dims; V: dims 128 rank ..
+    // + 127, two 16 KiB blocks of 128 keys). Its bytes complete on the even CTA's full
+    // barrier, which expects both halves; the odd CTA's own barrier only counts the fill.
     auto load_half = [&](const CUtensorMap* map, bool is_v, int kt) -> bool {
-      const uint32_t slot = cnt % kSlots;
+      const uint32_t slot = cnt % kPairSlots;
       const uint32_t rank = blockIdx.x & 1;
-      if (!warp_wait(&sm.empty[slot], ((cnt / kSlots) & 1) ^ 1, abort)) return false;
+      if (!warp_wait(&sm.empty[slot], ((cnt / kPairSlots) & 1) ^ 1, abort)) return false;
       if (rank == 0) mbar_expect_tx_warp(&sm.full[slot], 2 * kHalfTileBytes);
       else mbar_arrive_elect_warp(&sm.full[slot]);
       const uint32_t bar = mapa_shared(smem_u32(&sm.full[slot]), 0);
+      uint8_t* dst = slot_ptr<true>(sm, slot);
       if (is_v)
-        tma_load_4d_pair_warp(sm.tile[slot], map, bar, 0, kt * kTileN, kvh, 2 * (int)rank);
+        tma_load_4d_pair_warp(dst, map, bar, 0, kt * kTileN, kvh, 2 * (int)rank);
       else
-        tma_load_4d_pair_warp(sm.tile[slot], map, bar, 0, kt * kTileN + kHalfKeys * (int)rank,
-                              kvh, 0);
+        tma_load_4d_pair_warp(dst, map, bar, 0, kt * kTileN + kHalfKeys * (int)rank, kvh, 0);
       ++cnt;
       return true;
     };
@@ -427,14 +444,17 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
     };
     // Ring order: the item's prepared Q (for the edge warps), then in MMA order K0,
     // (K_j, V_{j-1}) for j >= 1, V_{n-1}; the gate tile (gated passes) just before V_0.
-    if (is_verify<kMode>()) {
+    // A pair's ring holds only the K and V halves (Q and gate tiles go through the staging
+    // buffer, loaded by warp 3).
+    if (kPair) {
+    } else if (is_verify<kMode>()) {
       if (!load_tile(tm_q, false, it.h, it.seq * a.vrows, -1,
                      4u * kVerifyHeadsPerTile * a.vrows * 128u)) return;
     } else {
       if (!load_tile(tm_q, false, it.h, it.row0 + it.mt * kTileM, -1, kTileBytes)) return;
     }
     auto load_gate = [&]() -> bool {
-      return !has_gate<kMode, kW>() ||
+      return kPair || !has_gate<kMode, kW>() ||
              load_tile(tm_g, false, it.h, it.row0 + it.mt * kTileM, -1, kTileBytes, kDim);
     };
     if (!load_k(ck.next(0))) return;
@@ -463,10 +483,43 @@ __device__ void producer(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMa
       }
     }
     // let the loads already issued into the slots land before exit
-    const uint32_t first = cnt > (uint32_t)kSlots ? cnt - kSlots : 0;
+    constexpr uint32_t kRing = (uint32_t)ring_slots<kPair>();
+    const uint32_t first = cnt > kRing ? cnt - kRing : 0;
     for (uint32_t c = first; c < cnt; ++c)
-      mbar_wait_quiet(&sm.full[c % kSlots], (c / kSlots) & 1, 100000000LL);
+      mbar_wait_quiet(&sm.full[c % kRing], (c / kRing) & 1, 100000000LL);
   }
+}
+
+// ------------------------------------------------------------------ warp 3: staging (pairs)
+// A pair CTA's staging buffer takes, in turn, each item's prepared Q tile and its gate tile
+// (fill 2i and 2i + 1 for the CTA's i-th item), each four 64-dim boxes of 128 rows. The edge
+// warps hand a Q fill back only after the previous item's output tile, written into the
+// same buffer after they copied Q out, has been read by its tensor stores; so the next item's
+// Q is in shared memory long before the current item ends, and its gate tile follows once
+// the output is out.
+template <int kMode, bool kPair>
+__device__ void stage_producer(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_g,
+                               const AttnArgs& a, volatile int* abort) {
+  uint8_t* stg = staging_ptr(sm);
+  uint32_t f = 0;   // fills issued
+  auto load = [&](const CUtensorMap* map, int head, int r0, int x0) -> bool {
+    if (f > 0 && !warp_wait(&sm.stg_empty, (f - 1) & 1, abort)) return false;
+    mbar_expect_tx_warp(&sm.stg_full, kTileBytes);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      tma_load_3d_warp(stg + c * kChunkBytes, map, &sm.stg_full, x0 + c * 64, head, r0);
+    ++f;
+    return true;
+  };
+  ItemWalk<kMode, kPair> walk;
+  Item it;
+  while (walk.next(a, it)) {
+    const int r0 = it.row0 + it.mt * kTileM;
+    if (!load(tm_q, it.h, r0, 0)) break;
+    if (!load(tm_g, it.h, r0, kDim)) break;
+  }
+  // on the way out after an abort, the last fill (never waited for by a consumer) lands first
+  if (*abort && f > 0) mbar_wait_quiet(&sm.stg_full, (f - 1) & 1, 100000000LL);
 }
 
 // ------------------------------------------------------------------ warps 1-2: MMA issuers
@@ -482,15 +535,16 @@ __device__ void producer(AttnSmem& sm, const CUtensorMap* tm_q, const CUtensorMa
 // Ring order per item: Q, K0, then K_j, V_{j-1} for j >= 1, then V_{n-1}, with the gate
 // tile of the gated passes right before V_0 (Q and K only in the weights pass).
 // With e4m3 caches a fill is ready once the edge warps have widened it (K, V) or seen it (Q).
-template <int kMode>
+template <int kMode, bool kPair = false>
 struct RingWalk {
   uint32_t cnt = 0;
   // wait for the next fill in ring order (its slot in `slot`) and count this warp as past it
   __device__ __forceinline__ bool next(AttnSmem& sm, volatile int* abort, uint32_t& slot) {
-    slot = cnt % kSlots;
+    constexpr uint32_t kRing = (uint32_t)ring_slots<kPair>();
+    slot = cnt % kRing;
     const bool ok = kMode == kModeVerify8
-                        ? __all_sync(0xffffffffu, mbar_wait<true>(&sm.conv[slot], (cnt / kSlots) & 1, abort))
-                        : warp_wait(&sm.full[slot], (cnt / kSlots) & 1, abort);
+                        ? __all_sync(0xffffffffu, mbar_wait<true>(&sm.conv[slot], (cnt / kRing) & 1, abort))
+                        : warp_wait(&sm.full[slot], (cnt / kRing) & 1, abort);
     ++cnt;
     if (ok && (threadIdx.x & 31) == 0) mbar_arrive(&sm.empty[slot]);
     return ok;
@@ -506,21 +560,22 @@ __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
   // block of this CTA's K is 8 KiB
   constexpr uint32_t kIdQK = idesc_bf16(kPair ? 256 : 128, kTileN, false, false);
   constexpr uint32_t kKBlock = kPair ? kChunkBytes / 2 : kChunkBytes;
+  constexpr uint32_t kSlotBytes = kPair ? kHalfTileBytes : kTileBytes;
   const uint64_t k_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), 16, 1024);
   const uint64_t qhi_desc0 = sdesc_sw128(smem_u32(sm.qhi[0]), 16, 1024);
-  RingWalk<kMode> ring;
+  RingWalk<kMode, kPair> ring;
   uint32_t g = 0;         // global key-tile counter: S phases
   uint32_t it_done = 0;
   uint32_t slot;
   ItemWalk<kMode, kPair> walk;
   Item it;
-  // V_idx, preceded by the gate tile when idx is 0
+  // V_idx, preceded by the gate tile when idx is 0 (not in a pair's ring)
   auto walk_v = [&](int idx) -> bool {
-    if (has_gate<kMode, kW>() && idx == 0 && !ring.next(sm, abort, slot)) return false;
+    if (!kPair && has_gate<kMode, kW>() && idx == 0 && !ring.next(sm, abort, slot)) return false;
     return ring.next(sm, abort, slot);
   };
   while (walk.next(a, it)) {
-    if (!ring.next(sm, abort, slot)) return;            // the item's Q tile (edge warps)
+    if (!kPair && !ring.next(sm, abort, slot)) return;  // the item's Q tile (edge warps)
     if (!warp_wait<kPair>(&sm.q_full, it_done & 1, abort)) return;
     for (int j = 0; j < it.n; ++j, ++g) {
       if (!kW && j >= 2 && !walk_v(j - 2)) return;      // V_{j-2}
@@ -528,7 +583,7 @@ __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
       // S is free once the softmax warps have copied the previous tile's S out
       if (g > 0 && !warp_wait<kPair>(&sm.s_free, (g - 1) & 1, abort)) return;
       tc_fence_after();
-      const uint64_t kd0 = k_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
+      const uint64_t kd0 = k_desc0 + (uint64_t)(slot * (kSlotBytes >> 4));
       // dims 0..127 with Q from tensor memory, dims 128..255 with Q from shared memory
 #pragma unroll
       for (int kk = 0; kk < kDim / 32; ++kk) {
@@ -559,22 +614,23 @@ __device__ void qk_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile
 template <int kMode, bool kPair>
 __device__ void pv_loop(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
   constexpr uint32_t kIdPV = idesc_bf16(kPair ? 256 : 128, kDim, false, true);
+  constexpr uint32_t kSlotBytes = kPair ? kHalfTileBytes : kTileBytes;
   const uint64_t v_desc0 = sdesc_sw128(smem_u32(sm.tile[0]), kChunkBytes, 1024);
-  RingWalk<kMode> ring;
+  RingWalk<kMode, kPair> ring;
   uint32_t g = 0;         // global key-tile counter: P and P V phases
   uint32_t it_done = 0;
   uint32_t slot;
   ItemWalk<kMode, kPair> walk;
   Item it;
   while (walk.next(a, it)) {
-    if (!ring.next(sm, abort, slot)) return;            // Q
+    if (!kPair && !ring.next(sm, abort, slot)) return;  // Q
     if (!ring.next(sm, abort, slot)) return;            // K0
     for (int j = 0; j < it.n; ++j, ++g) {
       if (j + 1 < it.n && !ring.next(sm, abort, slot)) return;   // K_{j+1}
-      if (has_gate<kMode, false>() && j == 0 && !ring.next(sm, abort, slot)) return;   // gate
+      if (!kPair && has_gate<kMode, false>() && j == 0 && !ring.next(sm, abort, slot)) return;   // gate
       if (!ring.next(sm, abort, slot)) return;                   // V_j
       if (j == 0 && it_done > 0 && !warp_wait<kPair>(&sm.o_free, (it_done - 1) & 1, abort)) return;
-      const uint64_t bd0 = v_desc0 + (uint64_t)(slot * (kTileBytes >> 4));
+      const uint64_t bd0 = v_desc0 + (uint64_t)(slot * (kSlotBytes >> 4));
       // The two 64-key halves of P go separately: each softmax warpgroup writes its half
       // of the next tile as soon as this tile's P V has read that half.
 #pragma unroll
@@ -974,10 +1030,15 @@ __device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r, bool
 // of bf16 kept in a register: 128 words for the row, the gate registers freed as they are
 // used) and released at once, so the next item's first P V waits only for the reads; the
 // row's 512 bytes of stores follow while the next item runs.
+// A pair CTA writes its output tile into the staging buffer instead (row r of each 64-dim
+// block, in the 128-byte-swizzled layout of the output map's boxes) and one thread stores it
+// with four tensor stores: whole 128-byte lines, where each thread's own row stores (32 rows
+// 12 KiB apart per warp instruction) hold up the tensor cores' shared-memory reads for their
+// whole duration.
 template <bool kPair>
-__device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32_t tmem,
-                         uint32_t lane_off, int r, uint32_t it_done, uint4 (&sg)[kDim / 8],
-                         volatile int* abort) {
+__device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const CUtensorMap* tm_o, const Item& it,
+                         uint32_t tmem, uint32_t lane_off, int r, uint32_t it_done,
+                         uint4 (&sg)[kDim / 8], volatile int* abort) {
   const int row = it.mt * kTileM + r;   // the row within its sequence
   const bool valid = row < it.rows;
   const int h = it.h;
@@ -1010,9 +1071,32 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const Item& it, uint32
   tc_fence_before();
   arrive_for_mma<kPair>(&sm.o_free);
   mbar_arrive(&sm.st_empty);
+  if (kPair) {
+    uint8_t* stg = staging_ptr(sm);
+#pragma unroll
+    for (int c64 = 0; c64 < kDim / 64; ++c64)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(stg + c64 * kChunkBytes + sw128_offset((uint32_t)r, (uint32_t)j)) =
+            make_uint4(res[32 * c64 + 4 * j], res[32 * c64 + 4 * j + 1], res[32 * c64 + 4 * j + 2],
+                       res[32 * c64 + 4 * j + 3]);
+    fence_async_smem();   // the tensor stores read what the threads wrote
+    mbar_arrive(&sm.o_st);
+    if (threadIdx.x == kEdgeThread0) {
+      if (!mbar_wait(&sm.o_st, it_done & 1, abort)) return false;
+      // rows past the call's end lie outside the map and are not written
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tma_store_3d(tm_o, stg + c * kChunkBytes, c * 64, h, it.row0 + it.mt * kTileM);
+      bulk_commit_group();
+      bulk_wait_group_read0();
+      mbar_arrive(&sm.stg_empty);   // the buffer may take the next gate tile
+    }
+  }
   if (!valid) return true;
   uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)(it.row0 + row) * kOutRow + h * kDim);
-  if ((reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) {   // rows are 12 KiB apart
+  if (kPair) {
+  } else if ((reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) {   // rows are 12 KiB apart
 #pragma unroll
     for (int q = 0; q < kDim / 16; ++q) {
       const uint32_t w[8] = {res[8 * q], res[8 * q + 1], res[8 * q + 2], res[8 * q + 3],
@@ -1146,7 +1230,8 @@ __device__ bool widen_e4m3(AttnSmem& sm, uint32_t pos, const float (&scv)[kWideR
 }
 
 template <int kMode, bool kW, bool kPair>
-__device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, volatile int* abort) {
+__device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, const CUtensorMap* tm_o, uint32_t tmem,
+                            volatile int* abort) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
   const int r = quad * 32 + lane;
@@ -1172,7 +1257,30 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
   // slot's previous fill, so the slot's full barrier is at most one phase behind the
   // awaited one (a parity wait cannot tell a phase from the one two before it).
   uint32_t q_pos = 0, q_takes = 0;
+  uint32_t stg_f = 0;   // pairs: staging fills taken (the CTA's item i: Q 2i, gate tile 2i + 1)
+  // A pair's Q comes from the staging buffer, which the item's output tile takes next (it
+  // is handed back after the output's tensor stores); only the first item's Q, which no
+  // output follows, is handed back at once.
+  auto take_q_pair = [&](bool wait_empty, uint32_t it_done) -> bool {
+    if (wait_empty && !warp_wait(&sm.q_empty, it_done & 1, abort)) return false;
+    if (!warp_wait(&sm.stg_full, stg_f & 1, abort)) return false;
+    tc_fence_after();
+    q_copy<true>(staging_ptr(sm), r, true, q_taddr, sm.qhi);
+    tc_fence_before();
+    arrive_for_mma<true, true>(&sm.q_full);
+    ++stg_f;
+    if (!wait_empty) {
+      mbar_arrive(&sm.q_read);
+      if (threadIdx.x == kEdgeThread0) {
+        if (!mbar_wait(&sm.q_read, q_takes & 1, abort)) return false;
+        mbar_arrive(&sm.stg_empty);
+      }
+      ++q_takes;
+    }
+    return true;
+  };
   auto take_q = [&](const Item& it, bool wait_empty, uint32_t it_done) -> bool {
+    if (kPair) return take_q_pair(wait_empty, it_done);
     const uint32_t slot = q_pos % kSlots;
     if (wait_empty && !warp_wait(&sm.q_empty, it_done & 1, abort)) return false;
     if (!warp_wait(&sm.full[slot], (q_pos / kSlots) & 1, abort)) return false;
@@ -1198,6 +1306,18 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
   // threads have copied their row.
   uint32_t g_takes = 0;
   auto take_gate = [&](uint32_t pos, uint4 (&sg)[kDim / 8]) -> bool {
+    if (kPair) {   // from the staging buffer, handed back once all 128 rows are read
+      if (!warp_wait(&sm.stg_full, stg_f & 1, abort)) return false;
+      gate_from_tile(staging_ptr(sm), r, sg);
+      ++stg_f;
+      mbar_arrive(&sm.g_read);
+      if (threadIdx.x == kEdgeThread0) {
+        if (!mbar_wait(&sm.g_read, g_takes & 1, abort)) return false;
+        mbar_arrive(&sm.stg_empty);
+      }
+      ++g_takes;
+      return true;
+    }
     const uint32_t slot = pos % kSlots;
     if (!warp_wait(&sm.full[slot], (pos / kSlots) & 1, abort)) return false;
     gate_from_tile(sm.tile[slot], r, sg);
@@ -1255,7 +1375,7 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, uint32_t tmem, vola
     if (have_next && !take_q(nxt, true, it_done)) return;
     if (is_verify<kMode>()) {
       if (!epilogue_partial(sm, a, cur, tmem, lane_off, r, it_done, abort)) return;
-    } else if (!kW && !epilogue<kPair>(sm, a, cur, tmem, lane_off, r, it_done, sg, abort)) {
+    } else if (!kW && !epilogue<kPair>(sm, a, tm_o, cur, tmem, lane_off, r, it_done, sg, abort)) {
       return;
     }
     ++it_done;
@@ -1277,7 +1397,7 @@ template <int kMode, bool kW, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                const __grid_constant__ AttnArgs a) {
+                const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ AttnArgs a) {
   constexpr bool kCluster = kPair || kMode == kModeVerify8;
   // The dynamic shared memory is declared 1024-byte aligned (the 128-byte swizzle of TMA
   // and the MMA descriptors needs it); every thread checks it before using any of it.
@@ -1297,11 +1417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &sm.abort;
   if (threadIdx.x == 0) {
     sm.abort = 0;
-    for (int i = 0; i < kSlots; ++i) {
+    for (int i = 0; i < kMaxSlots; ++i) {   // a pair's ring has four slots
       mbar_init(&sm.full[i], 1);
       // refilled once both MMA warps have passed the fill and its consumer released it
-      // (weights pass: the score warp alone walks the ring); in a pair's odd CTA, once its
-      // consumer released it (the pair's commit for K and V, its edge warps for Q and gate)
+      // (weights pass: the score warp alone walks the ring); in a pair's odd CTA, once the
+      // pair's commit released it
       mbar_init(&sm.empty[i], !leader ? 1 : kW ? 2 : 3);
     }
     // barriers the MMA warps wait on: per thread in a single CTA, per warp of both CTAs in
@@ -1329,6 +1449,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sm.g_read, 128);
     mbar_init(&sm.mx_bar, 256);
+    mbar_init(&sm.stg_full, 1);
+    mbar_init(&sm.stg_empty, 1);
+    mbar_init(&sm.o_st, 128);
     mbar_fence_init();
   }
   if (warp == 0 && lane == 0) {
@@ -1336,6 +1459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     if (has_gate<kMode, kW>()) tma_prefetch_desc(&tm_g);
+    if (kPair) tma_prefetch_desc(&tm_o);
   }
   if (warp == 1) {
     if (kPair) {
@@ -1371,12 +1495,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 0) producer<kMode, kW, kPair>(sm, &tm_q, &tm_k, &tm_v, &tm_g, a, abort);
       if ((warp == 1 || warp == 2) && leader)
         mma_issuer<kMode, kW, kPair>(sm, a, tmem, abort, warp == 2);
+      if (kPair && warp == 3) stage_producer<kMode, kPair>(sm, &tm_q, &tm_g, a, abort);
     } else if (warp < 12) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
       softmax_worker<kMode, kW, kPair>(sm, a, tmem, (warp - 4) >> 2, abort);
     } else {
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEdge));
-      edge_worker<kMode, kW, kPair>(sm, a, tmem, abort);
+      edge_worker<kMode, kW, kPair>(sm, a, &tm_o, tmem, abort);
+      // the output tiles' tensor stores complete before the CTA leaves
+      if (kPair && threadIdx.x == kEdgeThread0) bulk_wait_group0();
     }
   }
   tc_fence_before();
@@ -1531,7 +1658,8 @@ cudaError_t attn_max_gated_pair_clusters(int* n) {
 }
 
 cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                        const CUtensorMap& tm_g, const AttnArgs& a, int grid, cudaStream_t s) {
+                        const CUtensorMap& tm_g, const CUtensorMap& tm_o, const AttnArgs& a,
+                        int grid, cudaStream_t s) {
   const size_t smem = attn_smem_bytes();
   if (a.pair || a.mode == kModeVerify8) {
     // clusters of two CTAs (grid even)
@@ -1540,32 +1668,32 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
     const cudaLaunchConfig_t cfg = pair_config((unsigned)grid, smem, s, attr);
     if (a.mode == kModeVerify8)
       return cudaLaunchKernelEx(&cfg, attn_kernel<kModeVerify8, false, false>, tm_q, tm_k, tm_v,
-                                tm_g, a);
+                                tm_g, tm_o, a);
     if (a.weights_pass) return cudaErrorInvalidValue;
     if (a.mode == kModeCausal)
       return cudaLaunchKernelEx(&cfg, attn_kernel<kModeCausal, false, true>, tm_q, tm_k, tm_v,
-                                tm_g, a);
+                                tm_g, tm_o, a);
     if (a.mode == kModeBidir)
       return cudaLaunchKernelEx(&cfg, attn_kernel<kModeBidir, false, true>, tm_q, tm_k, tm_v,
-                                tm_g, a);
+                                tm_g, tm_o, a);
     if (a.mode == kModeMask)
       return cudaLaunchKernelEx(&cfg, attn_kernel<kModeMask, false, true>, tm_q, tm_k, tm_v,
-                                tm_g, a);
+                                tm_g, tm_o, a);
     return cudaErrorInvalidValue;
   }
   if (a.weights_pass) {
     if (a.mode != kModeMask) return cudaErrorInvalidValue;
-    attn_kernel<kModeMask, true, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeMask, true, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, tm_o, a);
   } else if (a.mode == kModeCausal) {
-    attn_kernel<kModeCausal, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeCausal, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, tm_o, a);
   } else if (a.mode == kModeBidir) {
-    attn_kernel<kModeBidir, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeBidir, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, tm_o, a);
   } else if (a.mode == kModeVerify) {
-    attn_kernel<kModeVerify, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeVerify, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, tm_o, a);
   } else if (a.mode == kModeBatch) {
-    attn_kernel<kModeBatch, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeBatch, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, tm_o, a);
   } else {
-    attn_kernel<kModeMask, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, a);
+    attn_kernel<kModeMask, false, false><<<grid, kThreads, smem, s>>>(tm_q, tm_k, tm_v, tm_g, tm_o, a);
   }
   return cudaGetLastError();
 }

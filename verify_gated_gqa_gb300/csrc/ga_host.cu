@@ -325,10 +325,12 @@ int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const v
                     (a.mode == kModeCausal || a.mode == kModeBidir) && a.head0 % 2 == 0 &&
                     a.n_heads % 2 == 0;
   a.pair = pair ? 1 : 0;
-  CUtensorMap tm_q, tm_k, tm_v, tm_g;
+  CUtensorMap tm_q, tm_k, tm_v, tm_g, tm_o;
   int st = encode_q_map(&tm_q, q_prep, a0.rows);
   if (st != GA_OK) return st;
   st = encode_gate_map(&tm_g, a0.qg, a0.rows);
+  if (st != GA_OK) return st;
+  st = pair ? encode_q_map(&tm_o, a0.out, a0.rows) : encode_q_map(&tm_o, q_prep, a0.rows);
   if (st != GA_OK) return st;
   st = pair ? encode_kv_map(&tm_k, k_prep, n_tok, 1, false, kTileN / 2, kDim / 64)
             : encode_kv_map(&tm_k, k_prep, n_tok, 1, false);
@@ -345,7 +347,7 @@ int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const v
     return fail_cuda(e);
   const int cap = pair ? dev->gated_pair_clusters : dev->sm_count;
   const int grid = (pair ? 2 : 1) * (a.n_items < cap ? a.n_items : cap);
-  e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_g, a, grid, s));
+  e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_g, tm_o, a, grid, s));
   if (e != cudaSuccess) return fail_cuda(e);
   return GA_OK;
 }
@@ -464,7 +466,7 @@ int verify_run(const ga_bf16* qg, const VerifyCaches& c, const int* seq_len, int
       grid = 2 * (pairs < dev->pair_clusters ? pairs : dev->pair_clusters);
     }
     // the verify partials have no gated epilogue: tm_q stands in for the unused gate map
-    if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_q, a, grid, s))) != cudaSuccess)
+    if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_q, tm_q, a, grid, s))) != cudaSuccess)
       return fail_cuda(e);
     if ((e = GA_CUDA(launch_verify_combine(a, s))) != cudaSuccess) return fail_cuda(e);
   }
@@ -553,7 +555,7 @@ int batch_run(const ga_bf16* qg, const BatchPiece* pieces, int n_pieces, const g
     st = encode_gate_map(&tm_g, a.qg, grp_rows);
     if (st != GA_OK) return st;
     const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
-    if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_g, a, grid, s))) != cudaSuccess)
+    if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_g, tm_q, a, grid, s))) != cudaSuccess)
       return fail_cuda(e);
     p0 = p1;
   }

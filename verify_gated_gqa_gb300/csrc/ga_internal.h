@@ -152,9 +152,11 @@ cudaError_t attn_upload_sigmoid_table(const uint16_t* host_table);
 size_t attn_smem_bytes();
 // tm_q: the prepared queries [rows][24][256] (box 64 dims x 1 head x 128 rows); tm_g: the
 // fused rows [rows][24][512], read for their gate halves (box 64 values x 1 head x 128 rows;
-// used by the causal, bidirectional and stored-mask passes).
+// used by the causal, bidirectional and stored-mask passes); tm_o: the output [rows][24][256]
+// as a.out (box as tm_q), written by tensor stores in the CTA-pair passes (a.pair).
 cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                        const CUtensorMap& tm_g, const AttnArgs& a, int grid, cudaStream_t s);
+                        const CUtensorMap& tm_g, const CUtensorMap& tm_o, const AttnArgs& a,
+                        int grid, cudaStream_t s);
 cudaError_t launch_mask_prepass(const uint8_t* mask, long long ld_mask, int rows, int T,
                                 uint32_t* bits, int mask_words, uint8_t* flags, int key_tiles,
                                 cudaStream_t s);
