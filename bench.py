@@ -1056,12 +1056,11 @@ def run_batch(args, world, rank, local):
 
 
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
-# summarised in profiles/attn_kernel_causal_s8192.md (218,213,376 + 60,994,816) and
-# profiles/attn_kernel_verify_8x16_l65536.md (1,077,404,160 + 18,152,192, the verify
-# variant of attn_kernel); each is to be set to None whenever its kernel changes until it is
-# captured again. The causal capture precedes the 32-at-a-time gate lookups of its epilogue
-# (279,208,192 B per launch then); the verify variant looks up no gate and is unchanged.
-ATTN_TRAFFIC_BYTES = None
+# summarised in profiles/attn_kernel_causal_s8192.md (218,662,400 + 61,944,320, the causal
+# variant as CTA pairs) and profiles/attn_kernel_verify_8x16_l65536.md (1,077,404,160 +
+# 18,152,192, the verify variant of attn_kernel); each is to be set to None whenever its
+# kernel changes until it is captured again.
+ATTN_TRAFFIC_BYTES = 280_606_720
 VERIFY_ATTN_TRAFFIC_BYTES = 1_095_556_352
 
 

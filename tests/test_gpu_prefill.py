@@ -166,11 +166,13 @@ def test_single_key_and_single_row():
     assert np.array_equal(np64(got)[0], want)
 
 
-def test_gate_every_bf16_value():
+@pytest.mark.parametrize("pairs", [True, False])
+def test_gate_every_bf16_value(pairs):
     """Every bf16 gate value but NaN (one per output element across 11 rows) with V = 1, so
     that o = 1 and out = bf16(sigmoid(g)) itself: the device's sigmoid table, bit for bit
     against the oracle, including +-inf, subnormal gates and the gates whose sigmoid is a
-    bf16 subnormal."""
+    bf16 subnormal. Both forms of the kernel: CTA pairs (their gate tiles through the
+    staging buffer) and single CTAs (through the ring)."""
     bits = np.arange(65536, dtype=np.uint32)
     is_nan = (((bits >> 7) & 0xFF) == 0xFF) & ((bits & 0x7F) != 0)
     vals = (bits[~is_nan] << 16).view(np.float32).astype(np.float64)
@@ -184,7 +186,13 @@ def test_gate_every_bf16_value():
     inp.cpu["v"] = torch.ones_like(inp.cpu["v"])
     inp.np["v"] = np64(inp.cpu["v"])
     d = inp.dev()
-    got = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0, rows)
+    prev = B.ga_debug_set_cta_pairs(pairs)
+    try:
+        got = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0,
+                                rows)
+        torch.cuda.synchronize()
+    finally:
+        B.ga_debug_set_cta_pairs(prev)
     want = inp.ref(0, rows, "causal").out
     assert np.array_equal(want.reshape(-1)[:vals.size], O.sigmoid_gate(vals))
     g_np = np64(got)
