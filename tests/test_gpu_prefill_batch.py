@@ -169,3 +169,27 @@ def test_batch_against_oracle():
         vc = O.gather_pages(vp_np, table[b], T, page)
         AttnRef(np64(qgs[b]), kc, vc, wq_np, oc, os_, qb, T, "causal", heads=heads).check(
             got[starts[b]:starts[b + 1]], what=f"batch seq {b} (q_base {qb}, {rows} rows)")
+
+
+@pytest.mark.parametrize("page_size", [128, 256])
+def test_batch_pairs_equal_single(page_size):
+    """The batched pass as CTA pairs (half K/V tiles per CTA from the paged pools, output tiles
+    by TMA stores where a sequence fills them, the rows' own stores where it ends inside one)
+    against single CTAs: the same bits, on windows at several positions, an empty sequence,
+    one row and tiles that end mid-sequence."""
+    spec = [(0, 300), (64, 129), (1024, 700), (0, 1), (128, 0), (256, 128), (0, 256)]
+    w_q, (c, s), caches, qgs, starts = _setup(SEED + 52, spec, 2048)
+    kpool, vpool, table = _pages(caches, page_size, 53 + page_size)
+    qg = torch.cat(qgs)
+    tab = torch.from_numpy(table).cuda()
+    outs = []
+    for pairs in (False, True):
+        prev = B.ga_debug_set_cta_pairs(pairs)
+        try:
+            outs.append(B.ga_attn_prefill_batch(qg, starts, [qb for qb, _ in spec], kpool, vpool,
+                                                tab, w_q, c, s))
+            torch.cuda.synchronize()
+        finally:
+            B.ga_debug_set_cta_pairs(prev)
+    assert B.ga_device_status() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))

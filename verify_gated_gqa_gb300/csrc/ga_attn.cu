@@ -189,9 +189,10 @@ __device__ __forceinline__ Item make_item(const AttnArgs& a, int idx) {
   it.qb = a.q_base;
   it.T = a.T;
   if (kMode == kModeBatch) {
-    const uint32_t e = a.batch_entry[idx / kHeads];
+    const int per_entry = kPair ? kHeads / 2 : kHeads;
+    const uint32_t e = a.batch_entry[idx / per_entry];
     const int piece = (int)(e >> 16);
-    it.h = idx % kHeads;
+    it.h = kPair ? 2 * (idx % per_entry) + (int)(blockIdx.x & 1) : idx % kHeads;
     it.mt = (int)(e & 0xFFFFu);
     it.seq = a.batch_seq[piece];
     it.row0 = a.batch_row0[piece];
@@ -421,10 +422,14 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
       else mbar_arrive_elect_warp(&sm.full[slot]);
       const uint32_t bar = mapa_shared(smem_u32(&sm.full[slot]), 0);
       uint8_t* dst = slot_ptr<true>(sm, slot);
-      if (is_v)
-        tma_load_4d_pair_warp(dst, map, bar, 0, kt * kTileN, kvh, 2 * (int)rank);
+      int r0;
+      const int outer = kv_at(kt, r0);   // batch mode: the page, r0 within it
+      const int key0 = is_v ? r0 : r0 + kHalfKeys * (int)rank;
+      const int blk0 = is_v ? 2 * (int)rank : 0;
+      if (outer < 0)
+        tma_load_4d_pair_warp(dst, map, bar, 0, key0, kvh, blk0);
       else
-        tma_load_4d_pair_warp(dst, map, bar, 0, kt * kTileN + kHalfKeys * (int)rank, kvh, 0);
+        tma_load_5d_pair_warp(dst, map, bar, 0, key0, kvh, blk0, outer);
       ++cnt;
       return true;
     };
@@ -1035,7 +1040,7 @@ __device__ void write_hidden_rows(const AttnArgs& a, const Item& it, int r, bool
 // with four tensor stores: whole 128-byte lines, where each thread's own row stores (32 rows
 // 12 KiB apart per warp instruction) hold up the tensor cores' shared-memory reads for their
 // whole duration.
-template <bool kPair>
+template <int kMode, bool kPair>
 __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const CUtensorMap* tm_o, const Item& it,
                          uint32_t tmem, uint32_t lane_off, int r, uint32_t it_done,
                          uint4 (&sg)[kDim / 8], volatile int* abort) {
@@ -1071,7 +1076,16 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const CUtensorMap* tm_
   tc_fence_before();
   arrive_for_mma<kPair>(&sm.o_free);
   mbar_arrive(&sm.st_empty);
-  if (kPair) {
+  // batch mode: a tile that ends inside its sequence leaves by the rows' own stores (the
+  // box's remaining rows belong to the next sequence)
+  const bool tma_out = kMode != kModeBatch || (it.mt + 1) * kTileM <= it.rows;
+  if (kPair && !tma_out) {
+    mbar_arrive(&sm.o_st);   // every row has read the staged Q: the buffer may refill
+    if (threadIdx.x == kEdgeThread0) {
+      if (!mbar_wait(&sm.o_st, it_done & 1, abort)) return false;
+      mbar_arrive(&sm.stg_empty);
+    }
+  } else if (kPair) {
     uint8_t* stg = staging_ptr(sm);
 #pragma unroll
     for (int c64 = 0; c64 < kDim / 64; ++c64)
@@ -1095,7 +1109,7 @@ __device__ bool epilogue(AttnSmem& sm, const AttnArgs& a, const CUtensorMap* tm_
   }
   if (!valid) return true;
   uint4* op = reinterpret_cast<uint4*>(a.out + (size_t)(it.row0 + row) * kOutRow + h * kDim);
-  if (kPair) {
+  if (kPair && tma_out) {
   } else if ((reinterpret_cast<uintptr_t>(a.out) & 31u) == 0) {   // rows are 12 KiB apart
 #pragma unroll
     for (int q = 0; q < kDim / 16; ++q) {
@@ -1375,7 +1389,7 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, const CUtensorMap* 
     if (have_next && !take_q(nxt, true, it_done)) return;
     if (is_verify<kMode>()) {
       if (!epilogue_partial(sm, a, cur, tmem, lane_off, r, it_done, abort)) return;
-    } else if (!kW && !epilogue<kPair>(sm, a, tm_o, cur, tmem, lane_off, r, it_done, sg, abort)) {
+    } else if (!kW && !epilogue<kMode, kPair>(sm, a, tm_o, cur, tmem, lane_off, r, it_done, sg, abort)) {
       return;
     }
     ++it_done;
@@ -1618,6 +1632,7 @@ cudaError_t attn_set_smem_attribute() {
       (const void*)attn_kernel<kModeCausal, false, true>,
       (const void*)attn_kernel<kModeBidir, false, true>,
       (const void*)attn_kernel<kModeMask, false, true>,
+      (const void*)attn_kernel<kModeBatch, false, true>,
   };
   for (const void* k : kernels) {
     const cudaError_t e =
@@ -1678,6 +1693,9 @@ cudaError_t launch_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const 
                                 tm_g, tm_o, a);
     if (a.mode == kModeMask)
       return cudaLaunchKernelEx(&cfg, attn_kernel<kModeMask, false, true>, tm_q, tm_k, tm_v,
+                                tm_g, tm_o, a);
+    if (a.mode == kModeBatch)
+      return cudaLaunchKernelEx(&cfg, attn_kernel<kModeBatch, false, true>, tm_q, tm_k, tm_v,
                                 tm_g, tm_o, a);
     return cudaErrorInvalidValue;
   }

@@ -488,10 +488,15 @@ int batch_run(const ga_bf16* qg, const BatchPiece* pieces, int n_pieces, const g
   int st = current_device(&dev);
   if (st != GA_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
+  // CTA pairs (two query heads of a KV group per pair item, each CTA holding half of every
+  // K and V tile: maps of half boxes) unless switched off
+  const bool pair = g_cta_pairs.load();
   CUtensorMap tm_k, tm_v;
-  st = encode_kv_map(&tm_k, k_pages, page_size, n_pages, true);
+  st = pair ? encode_kv_map(&tm_k, k_pages, page_size, n_pages, true, kTileN / 2, kDim / 64)
+            : encode_kv_map(&tm_k, k_pages, page_size, n_pages, true);
   if (st != GA_OK) return st;
-  st = encode_kv_map(&tm_v, v_pages, page_size, n_pages, true);
+  st = pair ? encode_kv_map(&tm_v, v_pages, page_size, n_pages, true, kTileN, kDim / 128)
+            : encode_kv_map(&tm_v, v_pages, page_size, n_pages, true);
   if (st != GA_OK) return st;
   int p0 = 0;
   while (p0 < n_pieces) {
@@ -543,7 +548,8 @@ int batch_run(const ga_bf16* qg, const BatchPiece* pieces, int n_pieces, const g
                      });
     a.n_entries = (int)order.size();
     for (int i = 0; i < a.n_entries; ++i) a.batch_entry[i] = order[i].second;
-    a.n_items = a.n_entries * kHeads;
+    a.pair = pair ? 1 : 0;
+    a.n_items = a.n_entries * (pair ? kHeads / 2 : kHeads);
     cudaError_t e;
     if ((e = GA_CUDA(launch_q_prologue_seq(a.qg, w_q, cos_tab, sin_tab, grp_rows, sp, a.out,
                                            dev->sm_count, s))) !=
@@ -554,7 +560,10 @@ int batch_run(const ga_bf16* qg, const BatchPiece* pieces, int n_pieces, const g
     if (st != GA_OK) return st;
     st = encode_gate_map(&tm_g, a.qg, grp_rows);
     if (st != GA_OK) return st;
-    const int grid = a.n_items < dev->sm_count ? a.n_items : dev->sm_count;
+    // the output map is the prepared-query map: the attention writes each row tile over the
+    // queries it has read
+    const int cap = pair ? dev->gated_pair_clusters : dev->sm_count;
+    const int grid = (pair ? 2 : 1) * (a.n_items < cap ? a.n_items : cap);
     if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_g, tm_q, a, grid, s))) != cudaSuccess)
       return fail_cuda(e);
     p0 = p1;

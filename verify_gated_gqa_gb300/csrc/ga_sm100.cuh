@@ -373,6 +373,18 @@ __device__ __forceinline__ void tma_load_4d_pair_warp(void* dst, const CUtensorM
 __device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t caddr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
+__device__ __forceinline__ void tma_load_5d_pair_warp(void* dst, const CUtensorMap* map,
+                                                      uint32_t bar_caddr, int c0, int c1, int c2,
+                                                      int c3, int c4) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];\n\t}\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_caddr), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(c4)
+      : "memory");
+}
 // One arrival of the warp, after every lane got here, on an mbarrier of CTA `rank` of the
 // cluster: a plain local arrival when that is this CTA, else a remote one (kRelease: with
 // release at cluster scope, for generic shared-memory writes the peer's tensor cores read;
