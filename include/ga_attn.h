@@ -114,15 +114,15 @@ int ga_device_status(int* status_out, int clear);
  * ga_device_status. Errors: RANGE, DEVICE, CUDA. */
 int ga_debug_wait_timeout(long long limit_cycles, ga_stream stream);
 
-/* Selects how the causal and bidirectional passes run (no counterpart in the pages; the
- * results are the same bits either way). enable != 0 (the default): as clusters of two CTAs
- * that share each key and value tile, two query heads of one KV group per pair item,
- * whenever the call's heads come in such pairs (every call through the ABI does: the
- * KV-group entry points take whole groups of 12). enable == 0: one CTA per 128-row tile
- * and head. The stored-mask pass always runs on single CTAs. Process-wide; takes effect
- * from the next call. Returns the previous setting (0 or 1). Makes no CUDA call; never
- * fails. */
-int ga_debug_set_cta_pairs(int enable);
+/* Selects how the attention passes run (no counterpart in the pages; the results are the
+ * same bits either way). mode 1 (the default): the causal, bidirectional, stored-mask and
+ * batched passes as clusters of two CTAs that share each key and value tile, two query heads
+ * of one KV group per pair item, whenever the call's heads come in such pairs (every call
+ * through the ABI does: the KV-group entry points take whole groups of 12); the weights pass
+ * and the verify passes on single CTAs. mode 0: every pass on single CTAs (one CTA per
+ * 128-row tile and head). Process-wide; takes effect from the next call. Returns the
+ * previous mode (0 or 1). Errors: RANGE (mode outside 0 .. 1). Makes no CUDA call. */
+int ga_debug_set_cta_pairs(int mode);
 
 /* Test hook: the fp32 dot products the tensor cores form for the scores, before any
  * rounding. For each of n_tiles tiles, s[n][i][j] = q[n][i] . k[n][j] over 256 dims, computed

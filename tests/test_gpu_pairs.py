@@ -1,10 +1,10 @@
 """The causal, bidirectional and stored-mask passes run as clusters of two CTAs that share
 each key and value tile (two query heads of one KV group per pair item, cta_group::2 MMAs
 issued by the even CTA). Every output, statistic and weight must be the same bits as the
-single-CTA kernel's: the pair changes only which SM's shared memory holds which half of a
-tile, not any arithmetic. The oracle checks of the other GPU tests run through the pairs
-(the default); these tests pin the two forms to each other on ragged sizes, windows, KV
-groups and masks with hidden rows."""
+single-CTA kernel's: the pair changes only which
+SM's shared memory holds which half of a tile, not any arithmetic. The oracle checks of the
+other GPU tests run through the default forms; these tests pin the two forms to each other
+on ragged sizes, windows, KV groups and masks with hidden rows."""
 import contextlib
 
 import pytest
@@ -35,12 +35,12 @@ def _pairs(enable):
         B.ga_debug_set_cta_pairs(prev)
 
 
-def _both(fn):
+def _both(fn, mode=1):
     """fn() under single CTAs and under CTA pairs; both results (tuples of tensors)."""
-    with _pairs(False):
+    with _pairs(0):
         single = fn()
         torch.cuda.synchronize()
-    with _pairs(True):
+    with _pairs(mode):
         paired = fn()
         torch.cuda.synchronize()
     assert B.ga_device_status() == 0
@@ -55,9 +55,9 @@ def _equal(single, paired):
 
 
 def test_switch_round_trips():
-    prev = B.ga_debug_set_cta_pairs(True)
-    assert B.ga_debug_set_cta_pairs(False) is True
-    assert B.ga_debug_set_cta_pairs(prev) is False
+    prev = B.ga_debug_set_cta_pairs(1)
+    assert B.ga_debug_set_cta_pairs(0) == 1
+    assert B.ga_debug_set_cta_pairs(prev) == 0
 
 
 @pytest.mark.parametrize("S,causal", [(64, True), (333, True), (333, False), (2048, True),

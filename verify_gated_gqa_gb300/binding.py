@@ -144,10 +144,14 @@ def ga_debug_cuda_calls() -> int:
     return lib().ga_debug_cuda_calls()
 
 
-def ga_debug_set_cta_pairs(enable: bool) -> bool:
-    """Run the causal, bidirectional and stored-mask passes as CTA pairs (the default) or as
-    single CTAs; the same bits either way. Returns the previous setting."""
-    return bool(lib().ga_debug_set_cta_pairs(1 if enable else 0))
+def ga_debug_set_cta_pairs(mode) -> int:
+    """0 (or False): every pass on single CTAs; 1 (or True, the default): the causal,
+    bidirectional, stored-mask and batched passes as CTA pairs. The same bits either way.
+    Returns the previous mode."""
+    st = lib().ga_debug_set_cta_pairs(int(mode))
+    if st < 0:
+        _check(st, "ga_debug_set_cta_pairs")
+    return st
 
 
 def ga_device_status(clear: bool = True) -> int:

@@ -317,13 +317,20 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   if (kPair) umma_commit_pair_both_warp(bar);
   else umma_commit_warp(bar);
 }
-// One arrival of a consumer warp (or thread) on a barrier the MMA warps wait on: per thread
-// in a single CTA; per warp, on the even CTA's barrier, in a pair (kRelease: at cluster
-// scope, after generic shared-memory writes the pair's MMAs read).
+// One arrival on a barrier the MMA warps wait on: per thread in a single CTA and in a
+// pair's even CTA (whose barriers they are); per warp, remotely, from a pair's odd CTA
+// (kRelease: at cluster scope, after generic shared-memory writes the pair's MMAs read).
 template <bool kPair, bool kRelease = false>
 __device__ __forceinline__ void arrive_for_mma(uint64_t* bar) {
-  if (kPair) mbar_arrive_warp_at<kRelease>(bar, 0);
-  else mbar_arrive(bar);
+  if (!kPair || (blockIdx.x & 1) == 0) {
+    mbar_arrive(bar);
+    return;
+  }
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (kRelease) mbar_arrive_remote(mapa_shared(smem_u32(bar), 0));
+    else mbar_arrive_remote_cta(mapa_shared(smem_u32(bar), 0));
+  }
 }
 
 // ------------------------------------------------------------------ warp 0: producer
@@ -1438,18 +1445,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pair's commit released it
       mbar_init(&sm.empty[i], !leader ? 1 : kW ? 2 : 3);
     }
-    // barriers the MMA warps wait on: per thread in a single CTA, per warp of both CTAs in
-    // a pair
-    mbar_init(&sm.q_full, kPair ? 8 : 128);
+    // barriers the MMA warps wait on: per thread of this CTA, plus in a pair one arrival per
+    // warp of the odd CTA
+    mbar_init(&sm.q_full, kPair ? 128 + 4 : 128);
     mbar_init(&sm.q_empty, 1);
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, kPair ? 16 : 256);       // both softmax warpgroups
+    mbar_init(&sm.s_free, kPair ? 256 + 8 : 256);       // both softmax warpgroups
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.p_full[i], kPair ? 8 : 128);
+      mbar_init(&sm.p_full[i], kPair ? 128 + 4 : 128);
       mbar_init(&sm.p_empty[i], 1);
     }
     mbar_init(&sm.o_done, 1);
-    mbar_init(&sm.o_free, kPair ? 8 : 128);
+    mbar_init(&sm.o_free, kPair ? 128 + 4 : 128);
     mbar_init(&sm.st_full, 256);
     mbar_init(&sm.st_empty, 128);
     mbar_init(&sm.drain, 1);

@@ -307,7 +307,7 @@ size_t verify_ws_bytes(const VerifyPlan& p) {
 // The query prologue (unless q_ready: q_prep already holds this call's prepared queries)
 // and the attention kernel. q_prep [rows][24][256] may be the output buffer itself: each
 // (row, head) slot is read by the work item that later writes its output there.
-std::atomic<bool> g_cta_pairs{true};   // ga_debug_set_cta_pairs
+std::atomic<int> g_cta_pairs{1};   // ga_debug_set_cta_pairs: 0 single CTAs, 1 CTA pairs
 
 int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const void* k_prep,
                      const void* v, long long n_tok, DeviceState* dev, cudaStream_t s) {
@@ -317,13 +317,12 @@ int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const v
     a.head0 = 0;
     a.n_heads = kHeads;
   }
-  // The causal and bidirectional passes run as CTA pairs (two query heads of one KV group
-  // per pair item) whenever the heads come in such pairs. The stored-mask pass (slower as
-  // pairs: its longer softmax puts the pair's extra synchronisation on the critical path)
-  // and the weights pass run on single CTAs.
-  const bool pair = g_cta_pairs.load() && !a.weights_pass &&
-                    (a.mode == kModeCausal || a.mode == kModeBidir) && a.head0 % 2 == 0 &&
-                    a.n_heads % 2 == 0;
+  // The causal, bidirectional and stored-mask passes run as CTA pairs (two query heads of
+  // one KV group per pair item) whenever the heads come in such pairs; the weights pass
+  // runs on single CTAs.
+  const bool pair = g_cta_pairs.load() > 0 && !a.weights_pass &&
+                    (a.mode == kModeCausal || a.mode == kModeBidir || a.mode == kModeMask) &&
+                    a.head0 % 2 == 0 && a.n_heads % 2 == 0;
   a.pair = pair ? 1 : 0;
   CUtensorMap tm_q, tm_k, tm_v, tm_g, tm_o;
   int st = encode_q_map(&tm_q, q_prep, a0.rows);
@@ -490,7 +489,7 @@ int batch_run(const ga_bf16* qg, const BatchPiece* pieces, int n_pieces, const g
   cudaStream_t s = (cudaStream_t)stream;
   // CTA pairs (two query heads of a KV group per pair item, each CTA holding half of every
   // K and V tile: maps of half boxes) unless switched off
-  const bool pair = g_cta_pairs.load();
+  const bool pair = g_cta_pairs.load() > 0;
   CUtensorMap tm_k, tm_v;
   st = pair ? encode_kv_map(&tm_k, k_pages, page_size, n_pages, true, kTileN / 2, kDim / 64)
             : encode_kv_map(&tm_k, k_pages, page_size, n_pages, true);
@@ -632,7 +631,10 @@ int ga_debug_wait_timeout(long long limit_cycles, ga_stream stream) {
   return e == cudaSuccess ? GA_OK : fail_cuda(e);
 }
 
-int ga_debug_set_cta_pairs(int enable) { return g_cta_pairs.exchange(enable != 0) ? 1 : 0; }
+int ga_debug_set_cta_pairs(int mode) {
+  if (mode < 0 || mode > 1) return GA_ERR_RANGE;
+  return g_cta_pairs.exchange(mode);
+}
 
 int ga_debug_qk_fp32(const ga_bf16* q, const ga_bf16* k, int n_tiles, float* s,
                      ga_stream stream) {

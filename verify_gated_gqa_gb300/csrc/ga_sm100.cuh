@@ -385,19 +385,6 @@ __device__ __forceinline__ void tma_load_5d_pair_warp(void* dst, const CUtensorM
       "r"(c4)
       : "memory");
 }
-// One arrival of the warp, after every lane got here, on an mbarrier of CTA `rank` of the
-// cluster: a plain local arrival when that is this CTA, else a remote one (kRelease: with
-// release at cluster scope, for generic shared-memory writes the peer's tensor cores read;
-// otherwise as mbar_arrive_remote_cta).
-template <bool kRelease = false>
-__device__ __forceinline__ void mbar_arrive_warp_at(uint64_t* bar, uint32_t rank) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) {
-    if (rank == cluster_ctarank()) mbar_arrive(bar);
-    else if (kRelease) mbar_arrive_remote(mapa_shared(smem_u32(bar), rank));
-    else mbar_arrive_remote_cta(mapa_shared(smem_u32(bar), rank));
-  }
-}
 // A plain arrival (no transaction bytes) by the elected lane of a warp.
 __device__ __forceinline__ void mbar_arrive_elect_warp(uint64_t* bar) {
   asm volatile(
