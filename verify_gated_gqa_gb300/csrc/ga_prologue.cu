@@ -30,6 +30,31 @@ namespace {
 __device__ __forceinline__ float lo_f(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float hi_f(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
+// Straight from a word of two bf16 values by mixed-precision FMAs (bf16 operands widened
+// exactly, fp32 addend, one rounding), so the values need no unpacking on the integer pipe:
+// lo^2 + hi^2 rounded once (hi^2 is exact), as fmaf(lo, lo, hi * hi).
+__device__ __forceinline__ float sumsq2(uint32_t xw) {
+  float t;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "fma.rn.f32.bf16 %0, hi, hi, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 %0, lo, lo, %0;\n\t}"
+      : "=f"(t)
+      : "r"(xw));
+  return t;
+}
+// fl(x + x w) of the two halves, as fmaf(x, w, x): x w is exact (-0 as the addend keeps its
+// sign), then x is added with one rounding.
+__device__ __forceinline__ void xw_plus_x2(uint32_t xw, uint32_t ww, float& p0, float& p1) {
+  asm("{\n\t.reg .b16 xl, xh, wl, wh, one;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\tmov.b16 one, 0x3F80;\n\t"
+      "fma.rn.f32.bf16 %0, xl, wl, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 %0, xl, one, %0;\n\t"
+      "fma.rn.f32.bf16 %1, xh, wh, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 %1, xh, one, %1;\n\t}"
+      : "=f"(p0), "=f"(p1)
+      : "r"(xw), "r"(ww));
+}
+
 constexpr int kThreads = 256;          // 16 half-warps, one row each at a time
 constexpr int kBlocksPerSm = 3;
 constexpr int kFastMargin = 9;         // fp32 ulps around a bf16 midpoint (see above)
@@ -73,17 +98,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
   const int stride_tok = stride / n_heads, stride_head = stride - stride_tok * n_heads;
   int tok = row / n_heads, head = row - tok * n_heads;
 
-  // this lane's norm weights, in the value order of RowVals
-  float w[16];
-  {
-    RowVals wv;
-    load_row(w_norm, l, wv);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      w[2 * i] = lo_f(wv.w[i]);
-      w[2 * i + 1] = hi_f(wv.w[i]);
-    }
-  }
+  // this lane's norm weights, in the value order of RowVals (two bf16 per word)
+  RowVals wv;
+  load_row(w_norm, l, wv);
   // element offset of the row (token t, head hd) in an array of rows stride_el values apart
   auto row_off = [&](int t, int hd, int stride_el) -> long long {
     return ((long long)t * heads_per_tok + head0 + hd) * stride_el;
@@ -118,16 +135,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
     const uint32_t cw = __ldg(reinterpret_cast<const uint32_t*>(cos_tab + (long long)pos * kHalfRot) + l);
     const uint32_t sw = __ldg(reinterpret_cast<const uint32_t*>(sin_tab + (long long)pos * kHalfRot) + l);
 
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[2 * i] = lo_f(cur.w[i]);
-      x[2 * i + 1] = hi_f(cur.w[i]);
-    }
     // fast sum of squares: pairs by one fma (the second square is exact), then a tree
     float t8[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) t8[i] = fmaf(x[2 * i], x[2 * i], x[2 * i + 1] * x[2 * i + 1]);
+    for (int i = 0; i < 8; ++i) t8[i] = sumsq2(cur.w[i]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) t8[i] = t8[2 * i] + t8[2 * i + 1];
     t8[0] = t8[0] + t8[1];
@@ -145,14 +156,27 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
     float y[16];
     uint32_t dmin = 0xFFFFFFFFu;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      y[i] = fmaf(x[i], w[i], x[i]) * rf;
-      dmin = min(dmin, __float_as_uint(y[i]) * 65536u + ((uint32_t)(kFastMargin - 0x8000) << 16));
+    for (int i = 0; i < 8; ++i) {
+      float p0, p1;
+      xw_plus_x2(cur.w[i], wv.w[i], p0, p1);
+      y[2 * i] = p0 * rf;
+      y[2 * i + 1] = p1 * rf;
     }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      dmin = min(dmin, __float_as_uint(y[i]) * 65536u + ((uint32_t)(kFastMargin - 0x8000) << 16));
     const bool near_any = dmin <= (2u * kFastMargin) << 16;
     if (__any_sync(hmask, near_any)) {
       // exact path for this row: the sum of squares as a TwoSum pair, combined over the
       // row's 16 lanes in a fixed order (lower lane first) so every lane holds the same pair
+      float x[16], w[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = lo_f(cur.w[i]);
+        x[2 * i + 1] = hi_f(cur.w[i]);
+        w[2 * i] = lo_f(wv.w[i]);
+        w[2 * i + 1] = hi_f(wv.w[i]);
+      }
       SumSq s0, s1;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
