@@ -354,6 +354,8 @@ __device__ void producer_loop(AttnSmem& sm, const CUtensorMap* tm_q, const CUten
     if (kv) {
       if (seq < 0)
         tma_load_4d_warp(sm.tile[slot], map, &sm.full[slot], 0, r0, head, 0);
+      else if (kMode == kModeVerify)   // read by this query group's two CTAs only: evicted first
+        tma_load_5d_warp_evict_first(sm.tile[slot], map, &sm.full[slot], 0, r0, head, 0, seq);
       else
         tma_load_5d_warp(sm.tile[slot], map, &sm.full[slot], 0, r0, head, 0, seq);
     } else {

@@ -231,6 +231,22 @@ __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// The same five-dimensional load with an L2 policy that evicts the lines first (for data
+// streamed through once: the verify caches, so that L2 keeps what is read again).
+__device__ __forceinline__ void tma_load_5d_warp_evict_first(void* dst, const CUtensorMap* map,
+                                                             uint64_t* bar, int c0, int c1,
+                                                             int c2, int c3, int c4) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b64 pol;\n\t"
+      "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], pol;\n\t}\n" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(c4)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05: TMEM
 // Allocation and deallocation are warp-wide; the allocated base lands in *slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
