@@ -13,48 +13,67 @@
 namespace ga {
 namespace {
 
-__global__ void __launch_bounds__(128) mask_prepass_kernel(const uint8_t* __restrict__ mask,
-                                                           long long ld_mask, int rows, int T,
-                                                           uint32_t* __restrict__ bits,
-                                                           int mask_words,
-                                                           uint8_t* __restrict__ flags,
-                                                           int key_tiles) {
-  const int kt = blockIdx.x, mt = blockIdx.y;
-  const int r = threadIdx.x;
-  const int row = mt * kTileM + r;
-  const int k0 = kt * kTileN;
-  constexpr int kWords = kTileN / 32;
-  uint32_t w[kWords];
+// One CTA of 256 threads per (128-row tile, four 128-key tiles): warp w takes rows 16w ..
+// 16w+15 of the tile, one row per instruction, lane l the 16 keys 16l .. 16l+15 of the 512
+// (a 16-byte load; the warp reads 512 contiguous bytes of the row). A byte is visible when
+// it is non-zero: ((x & 0x7F..) + 0x7F..) | x has bit 7 of each byte set exactly then (no
+// carry crosses a byte). Key j of a 32-key word belongs at bit 8 (j % 4) + 7 - j / 4: for the
+// lane's bytes 4i .. 4i+3 of word half h that is bit 7 - (4h + i) of the byte's own
+// position, one shift of those top bits. The two lanes of a word combine by one shuffle; a
+// tile's flag is the OR over its 8 lanes and the 8 warps. At most 32 registers a thread, so
+// eight CTAs fit an SM and the 1,024 CTAs of an 8192 x 8192 mask run as one wave.
+constexpr int kPrepThreads = 256;
+constexpr int kPrepKeyTiles = 4;
+
+__global__ void __launch_bounds__(kPrepThreads, 8) mask_prepass_kernel(
+    const uint8_t* __restrict__ mask, long long ld_mask, int rows, int T,
+    uint32_t* __restrict__ bits, int mask_words, uint8_t* __restrict__ flags, int key_tiles) {
+  const int kt0 = blockIdx.x * kPrepKeyTiles, mt = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int key = kt0 * kTileN + 16 * lane;   // this lane's first key
+  const bool tile_ok = kt0 + (lane >> 3) < key_tiles;
+  const uint32_t h = (uint32_t)(lane & 1);     // the lane's half of its 32-key word
+  uint32_t any = 0u;
+#pragma unroll 2
+  for (int i = 0; i < 16; ++i) {
+    const int row = mt * kTileM + warp * 16 + i;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row < rows && key < T) {
+      const uint8_t* src = mask + (long long)row * ld_mask + key;
+      if (key + 16 <= T) {
+        v = __ldg(reinterpret_cast<const uint4*>(src));
+      } else {   // the row's last keys: byte by byte, the rest hidden
+        uint32_t w4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int i = 0; i < kWords; ++i) w[i] = 0u;
-  if (row < rows) {
-    const uint8_t* src = mask + (long long)row * ld_mask + k0;
-#pragma unroll
-    for (int c = 0; c < kTileN / 16; ++c) {  // 16-byte chunks of the row's keys
-      const int j0 = k0 + 16 * c;
-      uint8_t b[16];
-      if (j0 + 16 <= T) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + 16 * c));
-        *reinterpret_cast<uint4*>(b) = v;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) b[e] = (j0 + e < T) ? src[16 * c + e] : 0;
+        for (int e = 0; e < 16; ++e)
+          if (key + e < T) w4[e >> 2] |= (uint32_t)src[e] << (8 * (e & 3));
+        v = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
-      uint32_t m = 0;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) m |= (b[e] != 0 ? 1u : 0u) << mask_bit_pos(16 * (c & 1) + e);
-      w[c >> 1] |= m;
     }
-  }
-  uint32_t any_bit = 0u;
-  uint32_t* dst = bits + (size_t)row * mask_words + (size_t)kt * kWords;
+    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0u;
 #pragma unroll
-  for (int i = 0; i < kWords; ++i) {
-    dst[i] = w[i];
-    any_bit |= w[i];
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t nz = (((x[q] & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x[q]) & 0x80808080u;
+      m |= nz >> (4u * h + (uint32_t)q);
+    }
+    any |= m;
+    const uint32_t word = m | __shfl_xor_sync(0xffffffffu, m, 1);
+    if ((lane & 1) == 0 && tile_ok)   // rows past the call's end get zero words
+      bits[(size_t)row * mask_words + (size_t)kt0 * (kTileN / 32) + (lane >> 1)] = word;
   }
-  const int any = __syncthreads_or(any_bit != 0u);
-  if (r == 0) flags[(size_t)mt * kMaskFlagStride + kt] = any ? 1 : 0;
+  any |= __shfl_xor_sync(0xffffffffu, any, 1);
+  any |= __shfl_xor_sync(0xffffffffu, any, 2);
+  any |= __shfl_xor_sync(0xffffffffu, any, 4);
+  __shared__ uint32_t tile_any[kPrepThreads / 32][kPrepKeyTiles];
+  if ((lane & 7) == 0) tile_any[warp][lane >> 3] = any;
+  __syncthreads();
+  if (threadIdx.x < kPrepKeyTiles && kt0 + (int)threadIdx.x < key_tiles) {
+    uint32_t o = 0u;
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) o |= tile_any[w][threadIdx.x];
+    flags[(size_t)mt * kMaskFlagStride + kt0 + threadIdx.x] = o ? 1 : 0;
+  }
 }
 
 }  // namespace
@@ -63,9 +82,9 @@ cudaError_t launch_mask_prepass(const uint8_t* mask, long long ld_mask, int rows
                                 uint32_t* bits, int mask_words, uint8_t* flags, int key_tiles,
                                 cudaStream_t s) {
   const int row_tiles = (rows + kTileM - 1) / kTileM;
-  dim3 grid((unsigned)key_tiles, (unsigned)row_tiles);
-  mask_prepass_kernel<<<grid, 128, 0, s>>>(mask, ld_mask, rows, T, bits, mask_words, flags,
-                                           key_tiles);
+  dim3 grid((unsigned)((key_tiles + kPrepKeyTiles - 1) / kPrepKeyTiles), (unsigned)row_tiles);
+  mask_prepass_kernel<<<grid, kPrepThreads, 0, s>>>(mask, ld_mask, rows, T, bits, mask_words,
+                                                    flags, key_tiles);
   return cudaGetLastError();
 }
 
