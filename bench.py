@@ -1057,11 +1057,11 @@ def run_batch(args, world, rank, local):
 
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
 # summarised in profiles/attn_kernel_causal_s8192.md (218,614,272 + 61,802,752, the causal
-# variant as CTA pairs) and profiles/attn_kernel_verify_8x16_l65536.md (1,077,404,160 +
-# 18,152,192, the verify variant of attn_kernel); each is to be set to None whenever its
+# variant as CTA pairs) and profiles/attn_kernel_verify_8x16_l65536.md (1,075,817,472 +
+# 7,236,352, the verify variant of attn_kernel); each is to be set to None whenever its
 # kernel changes until it is captured again.
 ATTN_TRAFFIC_BYTES = 280_417_024
-VERIFY_ATTN_TRAFFIC_BYTES = 1_095_556_352
+VERIFY_ATTN_TRAFFIC_BYTES = 1_083_053_824
 
 
 # ---------------------------------------------------------------- the oracle as baseline
