@@ -3,8 +3,9 @@
 Workload (one step): long causal prefill at S = 8192, batch 1, 24 query heads over 2 KV
 heads, head_dim 256, 64-dim partial RoPE, (1+w) RMSNorm: the K prologue over all 8192
 keys, the Q prologue over all 8192 x 24 query rows, then the full causal pass (Q.K^T,
-online softmax, P.V, gated epilogue). The three kernels are the ones ga_attn_prefill runs;
-the step calls the two prologues and ga_attn_prefill_prepared so that each is timed alone.
+online softmax, P.V, gated epilogue). The step runs both prologues in one launch
+(ga_qk_prologue; --prologues side or serial runs them as two) and then
+ga_attn_prefill_prepared, so that the prologues and the attention are each timed alone.
 Inputs are seeded synthetic bf16 N(0,1) activations and N(0,0.1) norm weights.
 
 Metric: algorithmic TFLOP/s, 4 * head_dim * heads per visible (query, key) pair (the
@@ -165,10 +166,14 @@ def run_gpu(args, world, rank, local):
     out = torch.empty(S, HEADS * DIM, dtype=torch.bfloat16, device=dev)
 
     q_prep = out.view(S, HEADS, DIM)   # as in ga_attn_prefill: the output buffer holds Q first
+    joint = args.prologues == "joint"
 
     def step():
-        B.ga_k_prologue(k, w_k, cos, sin, k_prep=k_prep)
-        B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
+        if joint:
+            B.ga_qk_prologue(k, w_k, qg, w_q, cos, sin, k_prep=k_prep, q_prep=q_prep)
+        else:
+            B.ga_k_prologue(k, w_k, cos, sin, k_prep=k_prep)
+            B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
         B.ga_attn_prefill_prepared(out, qg, k_prep, v, out=out)
 
     for _ in range(args.warmup):
@@ -186,15 +191,20 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    # the key prologue (half a wave of blocks) runs on a side stream beside the query
-    # prologue's waves, after the previous step's attention has read k_prep; the attention
-    # waits for both. --serial-prologues puts all three on one stream.
+    # --prologues joint (the default): both prologues in one launch (ga_qk_prologue);
+    # side: the key prologue on a side stream beside the query prologue, after the previous
+    # step's attention has read k_prep, the attention waiting for both; serial: all three
+    # on one stream.
     side = torch.cuda.Stream(device=dev)
     k_done = [torch.cuda.Event() for _ in range(args.steps)]
+    serial, side_mode = args.prologues == "serial", args.prologues == "side"
     t0.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
-        if args.serial_prologues:
+        if joint:
+            B.ga_qk_prologue(k, w_k, qg, w_q, cos, sin, k_prep=k_prep, q_prep=q_prep)
+            ev[i][1].record(stream)
+        elif serial:
             B.ga_k_prologue(k, w_k, cos, sin, k_prep=k_prep)
             ev[i][1].record(stream)
         else:
@@ -203,9 +213,10 @@ def run_gpu(args, world, rank, local):
                 B.ga_k_prologue(k, w_k, cos, sin, k_prep=k_prep)
                 ev[i][1].record(side)
                 k_done[i].record(side)
-        B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
+        if not joint:
+            B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
         ev[i][2].record(stream)
-        if not args.serial_prologues:
+        if side_mode:
             stream.wait_event(k_done[i])
         B.ga_attn_prefill_prepared(out, qg, k_prep, v, out=out)
         ev[i][3].record(stream)
@@ -216,7 +227,7 @@ def run_gpu(args, world, rank, local):
     total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_step = total_ms / args.steps
     pro_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
-    qpro_ms = statistics.mean((ev[i][1] if args.serial_prologues else ev[i][0]).elapsed_time(
+    qpro_ms = statistics.mean((ev[i][1] if serial else ev[i][0]).elapsed_time(
         ev[i][2]) for i in range(args.steps))
     attn_ms = statistics.mean(ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps))
     status = B.ga_device_status()
@@ -230,8 +241,13 @@ def run_gpu(args, world, rank, local):
 
     def compute(d, o):
         qg_d, k_d, v_d, wq_d, wk_d, cos_d, sin_d = d
-        B.ga_k_prologue(k_d, wk_d, cos_d, sin_d, k_prep=k_prep)
-        B.ga_attn_prefill(qg_d, k_prep, v_d, wq_d, cos_d, sin_d, 0, S, out=o)
+        if joint:
+            B.ga_qk_prologue(k_d, wk_d, qg_d, wq_d, cos_d, sin_d, k_prep=k_prep,
+                             q_prep=o.view(S, HEADS, DIM))
+            B.ga_attn_prefill_prepared(o, qg_d, k_prep, v_d, out=o)
+        else:
+            B.ga_k_prologue(k_d, wk_d, cos_d, sin_d, k_prep=k_prep)
+            B.ga_attn_prefill(qg_d, k_prep, v_d, wq_d, cos_d, sin_d, 0, S, out=o)
 
     e2e_steps = max(3, min(args.steps, 20))
     e2e_ms, h2d, d2h = e2e_pipelined(host_in, compute, out, e2e_steps, world, dev)
@@ -251,16 +267,19 @@ def run_gpu(args, world, rank, local):
         "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": S,
                    "parallelism": f"independent sequence per GPU x{world}",
                    "l2": "inputs larger than L2 (qg 192 MiB read + out 96 MiB written per step)",
-                   "step": ("ga_k_prologue (8192 keys) + ga_q_prologue (8192 x 24 rows) + "
-                            "ga_attn_prefill_prepared (8192 rows, causal)"
-                            + ("" if args.serial_prologues else
-                               "; the key prologue on a side stream beside the query "
-                               "prologue, joined before the attention"))},
+                   "step": (("ga_qk_prologue (8192 keys and 8192 x 24 query rows in one "
+                             "launch)" if joint else
+                             "ga_k_prologue (8192 keys) + ga_q_prologue (8192 x 24 rows)")
+                            + " + ga_attn_prefill_prepared (8192 rows, causal)"
+                            + ("; the key prologue on a side stream beside the query "
+                               "prologue, joined before the attention" if side_mode else ""))},
         "tokens_per_s": round(world * S / (ms_step * 1e-3), 1),
-        "kernel_ms": {"attn_kernel": round(attn_ms, 4), "k_prologue": round(pro_ms, 4),
-                      "q_prologue": round(qpro_ms, 4),
-                      "prologues": "serial" if args.serial_prologues else
-                                   "concurrent (each span includes the other's overlap)"},
+        "kernel_ms": ({"attn_kernel": round(attn_ms, 4), "qk_prologue": round(pro_ms, 4)}
+                      if joint else
+                      {"attn_kernel": round(attn_ms, 4), "k_prologue": round(pro_ms, 4),
+                       "q_prologue": round(qpro_ms, 4),
+                       "prologues": "serial" if serial else
+                                    "concurrent (each span includes the other's overlap)"}),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
                      "traffic": ATTN_TRAFFIC_BYTES,
@@ -269,9 +288,12 @@ def run_gpu(args, world, rank, local):
         "e2e": {"value": round(world * FLOPS_STEP / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
-                "schedule": "H2D, compute (ga_k_prologue + ga_attn_prefill) and D2H on three "
-                            "streams, device inputs and outputs double-buffered"},
-        "gpu_launches": 3 * args.steps,
+                "schedule": "H2D, compute ("
+                            + ("ga_qk_prologue + ga_attn_prefill_prepared" if joint else
+                               "ga_k_prologue + ga_attn_prefill")
+                            + ") and D2H on three streams, device inputs and outputs "
+                              "double-buffered"},
+        "gpu_launches": (2 if joint else 3) * args.steps,
         "clocks": clk,
         "device_status": status,
         "secondary": secondary,
@@ -513,8 +535,9 @@ def masked_setup(dev, seed):
 
 
 def run_masked(args, world, rank, local):
-    """Sparse-selection masked attention at S = 8192: each step runs the key prologue, the
-    query prologue and ga_attn_masked_prepared (the mask prepass and the attention), the
+    """Sparse-selection masked attention at S = 8192: each step runs the key and query
+    prologues (one ga_qk_prologue launch; with --prologues side or serial, ga_k_prologue then
+    ga_q_prologue) and ga_attn_masked_prepared (the mask prepass and the attention), the
     pieces ga_attn_masked runs, each timed on the stream. TFLOP/s both on the algorithmic
     work (visible pairs) and on the executed 128 x 128 tiles."""
     from verify_gated_gqa_gb300 import binding as B
@@ -533,9 +556,17 @@ def run_masked(args, world, rank, local):
     hid = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = torch.empty(B.ga_masked_workspace_bytes(S, S), dtype=torch.uint8, device=dev)
 
+    joint = args.prologues == "joint"
+
+    def prologues():
+        if joint:
+            B.ga_qk_prologue(kraw, w_k, qg, w_q, cos, sin, k_prep=k_prep, q_prep=q_prep)
+        else:
+            B.ga_k_prologue(kraw, w_k, cos, sin, k_prep=k_prep)
+            B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
+
     def step():
-        B.ga_k_prologue(kraw, w_k, cos, sin, k_prep=k_prep)
-        B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
+        prologues()
         B.ga_attn_masked_prepared(q_prep, qg, k_prep, v, mask, out=out, hidden_rows=hid,
                                   workspace=ws)
 
@@ -555,9 +586,13 @@ def run_masked(args, world, rank, local):
     t0.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
-        B.ga_k_prologue(kraw, w_k, cos, sin, k_prep=k_prep)
-        ev[i][1].record(stream)
-        B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
+        if joint:
+            B.ga_qk_prologue(kraw, w_k, qg, w_q, cos, sin, k_prep=k_prep, q_prep=q_prep)
+            ev[i][1].record(stream)
+        else:
+            B.ga_k_prologue(kraw, w_k, cos, sin, k_prep=k_prep)
+            ev[i][1].record(stream)
+            B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
         ev[i][2].record(stream)
         B.ga_attn_masked_prepared(q_prep, qg, k_prep, v, mask, out=out, hidden_rows=hid,
                                   workspace=ws)
@@ -603,8 +638,10 @@ def run_masked(args, world, rank, local):
                    "parallelism": f"independent sequence per GPU x{world}",
                    "l2": "inputs larger than L2 (qg 192 MiB + mask 64 MiB read, out 96 MiB "
                          "written per step)",
-                   "step": "ga_k_prologue + ga_q_prologue + ga_attn_masked_prepared (mask "
-                           "prepass + attention), the pieces of ga_attn_masked"},
+                   "step": ("ga_qk_prologue (both prologues, one launch)" if joint else
+                            "ga_k_prologue + ga_q_prologue")
+                           + " + ga_attn_masked_prepared (mask prepass + attention), the "
+                             "pieces of ga_attn_masked"},
         "visible_pairs_per_head": m["pairs"], "algorithmic_gflop": round(flops / 1e9, 2),
         "executed_tiles": {"tiles_per_head": m["tiles"],
                            "gflop": round(exec_flops / 1e9, 2),
@@ -612,8 +649,10 @@ def run_masked(args, world, rank, local):
                            "note": "128 x 128 tiles with a visible key, each a dense QK^T and "
                                    "P.V on the tensor cores"},
         "tokens_per_s": round(world * S / (ms * 1e-3), 1),
-        "kernel_ms": {"mask_prepass_and_attn_kernel": round(attn_ms, 4),
-                      "k_prologue": round(kpro_ms, 4), "q_prologue": round(qpro_ms, 4)},
+        "kernel_ms": ({"mask_prepass_and_attn_kernel": round(attn_ms, 4),
+                       "qk_prologue": round(kpro_ms + qpro_ms, 4)} if joint else
+                      {"mask_prepass_and_attn_kernel": round(attn_ms, 4),
+                       "k_prologue": round(kpro_ms, 4), "q_prologue": round(qpro_ms, 4)}),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tf,
                      "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4), "traffic": None,
                      "peak_kind": f"dense bf16 burst ({peak_src})",
@@ -625,8 +664,8 @@ def run_masked(args, world, rank, local):
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
                 "schedule": "H2D, compute (ga_k_prologue + ga_attn_masked) and D2H on three "
                             "streams, device inputs and outputs double-buffered"},
-        "gpu_launches": 4 * args.steps, "clocks": clk, "device_status": status,
-        "hidden_rows": hidden,
+        "gpu_launches": (3 if joint else 4) * args.steps, "clocks": clk,
+        "device_status": status, "hidden_rows": hidden,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_masked(args.cpu_seconds, gpu_out=out)
@@ -766,12 +805,12 @@ SMALL_CASES = [("S=64 causal", 64, True), ("S=2048 causal", 2048, True),
 
 def run_small(args, world, rank, local):
     """The small prefill configurations: S = 64 causal (latency), S = 2048 causal and S = 2048
-    bidirectional, each step the headline step's three calls: ga_k_prologue on a side stream
-    beside ga_q_prologue, then ga_attn_prefill_prepared once both are done. Their inputs fit
-    in L2, so every timed call follows a 256 MiB write that flushes it, and CUDA events
-    bracket the step alone. The line's value is the S = 2048 causal TFLOP/s; `cases` holds
-    all three, each with the attention call's own time beside the step's (also from a
-    flushed L2)."""
+    bidirectional, each step the headline step's calls: both prologues (one ga_qk_prologue
+    launch, or with --prologues side ga_k_prologue on a side stream beside ga_q_prologue,
+    or serial), then ga_attn_prefill_prepared. Their inputs fit in L2, so every timed call
+    follows a 256 MiB write that flushes it, and CUDA events bracket the step alone. The
+    line's value is the S = 2048 causal TFLOP/s; `cases` holds all three, each with the
+    attention call's own time beside the step's (also from a flushed L2)."""
     import statistics
 
     from verify_gated_gqa_gb300 import binding as B
@@ -799,12 +838,18 @@ def run_small(args, world, rank, local):
         side = torch.cuda.Stream(device=dev)
 
         def step():
-            # the key prologue beside the query prologue; the attention waits for both
-            side.wait_stream(stream)
-            with torch.cuda.stream(side):
+            if args.prologues == "joint":
+                B.ga_qk_prologue(kraw, w_k, qg, w_q, cos, sin, k_prep=k_prep, q_prep=q_prep)
+            elif args.prologues == "serial":
                 B.ga_k_prologue(kraw, w_k, cos, sin, k_prep=k_prep)
-            B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
-            stream.wait_stream(side)
+                B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
+            else:
+                # the key prologue beside the query prologue; the attention waits for both
+                side.wait_stream(stream)
+                with torch.cuda.stream(side):
+                    B.ga_k_prologue(kraw, w_k, cos, sin, k_prep=k_prep)
+                B.ga_q_prologue(qg, w_q, cos, sin, q_prep=q_prep)
+                stream.wait_stream(side)
             B.ga_attn_prefill_prepared(q_prep, qg, k_prep, v, 0, n, causal=causal, out=out)
 
         for _ in range(args.warmup):
@@ -875,8 +920,11 @@ def run_small(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.1) norm weights)",
         "config": {"workload": "small prefill configurations: S=64 causal, S=2048 causal, S=2048 "
-                               "bidirectional; step = ga_k_prologue (side stream) beside "
-                               "ga_q_prologue, then ga_attn_prefill_prepared",
+                               "bidirectional; step = "
+                               + {"joint": "ga_qk_prologue (both prologues, one launch)",
+                                  "side": "ga_k_prologue (side stream) beside ga_q_prologue",
+                                  "serial": "ga_k_prologue, ga_q_prologue"}[args.prologues]
+                               + ", then ga_attn_prefill_prepared",
                    "l2": "flushed before every timed call (256 MiB write); median of the steps"},
         "cases": cases,
         "roofline": {"bound": "tensor", "achieved": head["tflops"], "peak": peak_tf,
@@ -884,7 +932,8 @@ def run_small(args, world, rank, local):
                      "traffic": None, "peak_kind": f"dense bf16 burst ({peak_src})",
                      "kernel": "the S=2048 causal step (K prologue + Q prologue + attention)",
                      "algorithmic_flops": attention_flops(visible_pairs_causal(2048, 2048))},
-        "gpu_launches": 7 * args.steps * len(SMALL_CASES), "clocks": clk,
+        "gpu_launches": ((5 if args.prologues == "joint" else 7) * args.steps
+                         * len(SMALL_CASES)), "clocks": clk,
         "device_status": B.ga_device_status(),
     }
 
@@ -1285,9 +1334,10 @@ def main():
     ap.add_argument("--no-secondary", action="store_true",
                     help="prefill: skip the verify and masked measurements after the headline "
                          "(for profiling runs)")
-    ap.add_argument("--serial-prologues", action="store_true",
-                    help="prefill: run the key prologue on the main stream, not beside the "
-                         "query prologue")
+    ap.add_argument("--prologues", choices=("joint", "side", "serial"), default="joint",
+                    help="prefill and small: both prologues in one launch (joint), the key "
+                         "prologue on a side stream beside the query prologue (side), or "
+                         "one after the other (serial)")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

@@ -173,6 +173,25 @@ int ga_q_prologue(const ga_bf16* qg, const ga_bf16* w_q, const ga_bf16* cos_tab,
                   const ga_bf16* sin_tab, int table_rows, int rows, int q_base,
                   ga_bf16* q_prep, ga_stream stream);
 
+/* Both prologues in one launch (pegainfer PR #1151, §What changed and §Semantics: the key
+ * pass and the query pass take the same (1+w) norm and partial rotation):
+ * ga_k_prologue over n_tok key tokens and ga_q_prologue over rows fused query rows, with
+ * the same results bit for bit. One persistent grid walks the
+ * key rows and then the query rows, so the two share every SM instead of competing as two
+ * launches on two streams would.
+ *   k_raw, w_k, n_tok, k_pos_base, k_prep: as ga_k_prologue's k_raw, w_k, n_tok, pos_base
+ *                            and k_prep
+ *   qg, w_q, rows, q_base, q_prep: as ga_q_prologue's; q_prep may not overlap qg, and no
+ *                            output may overlap the other call's inputs or output
+ *   cos_tab, sin_tab [table_rows][32]; table_rows >= k_pos_base + n_tok and
+ *                            table_rows >= q_base + rows
+ * Errors: NULL, SHAPE (n_tok < 0 or rows < 0), RANGE, TABLE, ALIGN (every pointer),
+ * DEVICE, CUDA; all checked before anything is launched. */
+int ga_qk_prologue(const ga_bf16* k_raw, const ga_bf16* w_k, int n_tok, int k_pos_base,
+                   ga_bf16* k_prep, const ga_bf16* qg, const ga_bf16* w_q, int rows, int q_base,
+                   ga_bf16* q_prep, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                   int table_rows, ga_stream stream);
+
 /* Causal / prefix-window / bidirectional gated GQA attention (system1-omni PR #202,
  * §Scope: full pass, causal or bidirectional, and causal prefix windows at q_base).
  *   qg      [rows][24][512]  fused rows of query positions q_base .. q_base+rows-1; per

@@ -298,6 +298,27 @@ def test_k_prologue_refusals(L):
     assert L.ga_debug_cuda_calls() == before
 
 
+def test_qk_prologue_refusals(L):
+    """Both prologues in one launch: every argument check of the two single calls, before any
+    CUDA call. Arguments: k_raw, w_k, n_tok, k_pos_base, k_prep, qg, w_q, rows, q_base,
+    q_prep, cos, sin, table_rows, stream."""
+    before = L.ga_debug_cuda_calls()
+    Q = L.ga_qk_prologue
+    assert Q(None, A, 10, 0, A, A, A, 10, 0, A, A, A, 100, S) == -1
+    assert Q(A, A, 10, 0, A, A, A, 10, 0, None, A, A, 100, S) == -1
+    assert Q(A, A, -1, 0, A, A, A, 10, 0, A, A, A, 100, S) == -2
+    assert Q(A, A, 10, 0, A, A, A, -1, 0, A, A, A, 100, S) == -2
+    assert Q(A, A, 10, -1, A, A, A, 10, 0, A, A, A, 100, S) == -4
+    assert Q(A, A, 10, 0, A, A, A, 10, -1, A, A, A, 100, S) == -4
+    assert Q(A, A, 10, 95, A, A, A, 10, 0, A, A, A, 100, S) == -5   # key positions past the table
+    assert Q(A, A, 10, 0, A, A, A, 10, 95, A, A, A, 100, S) == -5   # query positions past it
+    assert Q(MIS, A, 10, 0, A, A, A, 10, 0, A, A, A, 100, S) == -3
+    assert Q(A, A, 10, 0, A, A, A, 10, 0, MIS, A, A, 100, S) == -3
+    assert Q(A, A, 10, 0, A, A, MIS, 10, 0, A, A, A, 100, S) == -3
+    assert Q(A, A, 0, 0, A, A, A, 0, 0, A, A, A, 100, S) == 0      # nothing to do
+    assert L.ga_debug_cuda_calls() == before
+
+
 def test_q_prologue_and_prepared_refusals(L):
     before = L.ga_debug_cuda_calls()
     assert L.ga_q_prologue(None, A, A, A, 100, 10, 0, A, S) == -1

@@ -70,6 +70,65 @@ def test_q_prologue_bit_exact_s8192():
     assert np.array_equal(g, want), f"{int((g != want).sum())} of {g.size} differ"
 
 
+@pytest.mark.parametrize("n_tok,k_pos,rows,q_base", [(2048, 0, 333, 0), (333, 777, 200, 704),
+                                                    (0, 0, 100, 0), (50, 3, 0, 0),
+                                                    (8192, 0, 8192, 0)])
+def test_qk_prologue_equals_single_calls(n_tok, k_pos, rows, q_base):
+    """Both prologues in one launch: the same bits as ga_k_prologue and ga_q_prologue, with
+    the runs of key and query rows dealt over one grid (an empty run, whose output stays
+    untouched; a key run shorter than the grid's half-warps; the full S = 8192 pass); the
+    oracle fixes the small cases."""
+    T = max(k_pos + n_tok, q_base + rows, 1)
+    c, s = B.ga_rope_table_host(T)
+    cos, sin = c.cuda(), s.cuda()
+    w_k = synth.normal_bf16(SEED + 13, "w_k", (256,), sigma=0.1).cuda()
+    w_q = synth.normal_bf16(SEED + 13, "w_q", (256,), sigma=0.1).cuda()
+    # buffers of at least one row, so that an empty run still passes valid pointers
+    k = synth.normal_bf16(SEED + 13, "k", (max(n_tok, 1), 2, 256)).cuda()
+    qg = synth.normal_bf16(SEED + 13, "qg", (max(rows, 1), 24, 512)).cuda()
+    kp = torch.full_like(k, 7.0)
+    qp = torch.full((max(rows, 1), 24, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    st = B.lib().ga_qk_prologue(k.data_ptr(), w_k.data_ptr(), n_tok, k_pos, kp.data_ptr(),
+                                qg.data_ptr(), w_q.data_ptr(), rows, q_base, qp.data_ptr(),
+                                cos.data_ptr(), sin.data_ptr(), T, B._stream())
+    assert st == 0
+    torch.cuda.synchronize()
+    assert B.ga_device_status() == 0
+    if n_tok:
+        want_k = B.ga_k_prologue(k, w_k, cos, sin, pos_base=k_pos)
+        assert torch.equal(kp.view(torch.int16), want_k.view(torch.int16))
+    else:
+        assert bool((kp == 7.0).all())
+    if rows:
+        want_q = B.ga_q_prologue(qg, w_q, cos, sin, q_base=q_base)
+        assert torch.equal(qp.view(torch.int16), want_q.view(torch.int16))
+    else:
+        assert bool((qp == 7.0).all())
+    if T <= 4096:
+        oc, os_ = O.rope_tables(T)
+        if n_tok:
+            wk = O.prep_keys(np64(k.cpu()), np64(w_k.cpu()), oc, os_, pos0=k_pos)
+            assert np.array_equal(np64(kp), wk)
+        if rows:
+            wq, _ = O.prep_queries(np64(qg.cpu()), np64(w_q.cpu()), oc, os_, q_base)
+            assert np.array_equal(np64(qp), wq)
+
+
+def test_qk_prologue_binding():
+    """The binding's form allocates both outputs and returns them."""
+    T = 640
+    c, s = B.ga_rope_table_host(T)
+    k = synth.normal_bf16(SEED + 14, "k", (T, 2, 256)).cuda()
+    qg = synth.normal_bf16(SEED + 14, "qg", (128, 24, 512)).cuda()
+    w = synth.normal_bf16(SEED + 14, "w_q", (256,), sigma=0.1).cuda()
+    kp, qp = B.ga_qk_prologue(k, w, qg, w, c.cuda(), s.cuda(), q_base=512)
+    assert kp.shape == k.shape and qp.shape == (128, 24, 256)
+    assert torch.equal(kp.view(torch.int16),
+                       B.ga_k_prologue(k, w, c.cuda(), s.cuda()).view(torch.int16))
+    assert torch.equal(qp.view(torch.int16),
+                       B.ga_q_prologue(qg, w, c.cuda(), s.cuda(), q_base=512).view(torch.int16))
+
+
 def test_prepared_path_matches_fused_call():
     """ga_q_prologue + ga_attn_prefill_prepared equals ga_attn_prefill bit for bit, with the
     prepared queries in their own buffer and in the output buffer itself."""

@@ -39,6 +39,7 @@ _SIGS = {
     "ga_rope_table_host": (_I, [_I, _P, _P]),
     "ga_k_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "ga_q_prologue": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "ga_qk_prologue": (_I, [_P, _P, _I, _I, _P, _P, _P, _I, _I, _P, _P, _P, _I, _P]),
     "ga_debug_wait_timeout": (_I, [_LL, _P]),
     "ga_debug_qk_fp32": (_I, [_P, _P, _I, _P, _P]),
     "ga_debug_set_cta_pairs": (_I, [_I]),
@@ -194,6 +195,27 @@ def ga_q_prologue(qg, w_q, cos_tab, sin_tab, q_base=0, q_prep=None):
                                cos_tab.shape[0], rows, q_base, _ptr(q_prep), _stream()),
            "ga_q_prologue")
     return q_prep
+
+
+def ga_qk_prologue(k_raw, w_k, qg, w_q, cos_tab, sin_tab, k_pos_base=0, q_base=0, k_prep=None,
+                   q_prep=None):
+    """Both prologues in one launch: (k_prep [n_tok, 2, 256], q_prep [rows, 24, 256]), the
+    same bits as ga_k_prologue and ga_q_prologue."""
+    _bf16_cuda("k_raw", k_raw)
+    _bf16_cuda("qg", qg)
+    n_tok, rows = k_raw.shape[0], qg.shape[0]
+    if k_prep is None:
+        k_prep = torch.empty_like(k_raw)
+    if q_prep is None:
+        q_prep = torch.empty(rows, N_Q_HEADS, HEAD_DIM, dtype=torch.bfloat16, device=qg.device)
+    for n, t in (("w_k", w_k), ("w_q", w_q), ("cos_tab", cos_tab), ("sin_tab", sin_tab),
+                 ("k_prep", k_prep), ("q_prep", q_prep)):
+        _bf16_cuda(n, t)
+    _check(lib().ga_qk_prologue(_ptr(k_raw), _ptr(w_k), n_tok, k_pos_base, _ptr(k_prep), _ptr(qg),
+                                _ptr(w_q), rows, q_base, _ptr(q_prep), _ptr(cos_tab),
+                                _ptr(sin_tab), cos_tab.shape[0], _stream()),
+           "ga_qk_prologue")
+    return k_prep, q_prep
 
 
 def ga_attn_prefill_prepared(q_prep, qg, k_prep, v, q_base=0, T=None, causal=True, out=None,

@@ -703,6 +703,32 @@ int ga_q_prologue(const ga_bf16* qg, const ga_bf16* w_q, const ga_bf16* cos_tab,
   return e == cudaSuccess ? GA_OK : fail_cuda(e);
 }
 
+int ga_qk_prologue(const ga_bf16* k_raw, const ga_bf16* w_k, int n_tok, int k_pos_base,
+                   ga_bf16* k_prep, const ga_bf16* qg, const ga_bf16* w_q, int rows, int q_base,
+                   ga_bf16* q_prep, const ga_bf16* cos_tab, const ga_bf16* sin_tab,
+                   int table_rows, ga_stream stream) {
+  if (!k_raw || !w_k || !k_prep || !qg || !w_q || !q_prep || !cos_tab || !sin_tab)
+    return GA_ERR_NULL;
+  if (n_tok < 0 || rows < 0 || table_rows < 0) return GA_ERR_SHAPE;
+  if (k_pos_base < 0 || n_tok > GA_MAX_TOKENS || k_pos_base > GA_MAX_TOKENS || q_base < 0 ||
+      rows > GA_MAX_TOKENS || q_base > GA_MAX_TOKENS)
+    return GA_ERR_RANGE;
+  if ((long long)table_rows < (long long)k_pos_base + n_tok ||
+      (long long)table_rows < (long long)q_base + rows)
+    return GA_ERR_TABLE;
+  if (!aligned(k_raw, 16) || !aligned(k_prep, 16) || !aligned(w_k, 16) || !aligned(qg, 16) ||
+      !aligned(q_prep, 16) || !aligned(w_q, 16) || !aligned(cos_tab, 16) || !aligned(sin_tab, 16))
+    return GA_ERR_ALIGN;
+  if (n_tok == 0 && rows == 0) return GA_OK;
+  DeviceState* dev = nullptr;
+  int st = current_device(&dev);
+  if (st != GA_OK) return st;
+  cudaError_t e = GA_CUDA(launch_qk_prologue(k_raw, w_k, n_tok, k_pos_base, k_prep, qg, w_q, rows,
+                                             q_base, q_prep, cos_tab, sin_tab, dev->sm_count,
+                                             (cudaStream_t)stream));
+  return e == cudaSuccess ? GA_OK : fail_cuda(e);
+}
+
 int ga_attn_prefill_prepared(const ga_bf16* q_prep, const ga_bf16* qg, const ga_bf16* k_prep,
                              const ga_bf16* v, int rows, int T, int q_base, int causal,
                              ga_bf16* out, float* row_stats, ga_stream stream) {

@@ -125,6 +125,13 @@ cudaError_t launch_verify_combine(const AttnArgs& a, cudaStream_t s);
 cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
                               const uint16_t* sin_tab, int rows, int q_base, int head0,
                               int n_heads, uint16_t* q_prep, int sm_count, cudaStream_t s);
+// Both prologues in one launch: the key rows of n_tok tokens at positions k_pos_base.., then
+// the query rows of all 24 heads at q_base.., each with the single launches' results.
+cudaError_t launch_qk_prologue(const uint16_t* k_raw, const uint16_t* w_k, int n_tok,
+                               int k_pos_base, uint16_t* k_prep, const uint16_t* qg,
+                               const uint16_t* w_q, int rows, int q_base, uint16_t* q_prep,
+                               const uint16_t* cos_tab, const uint16_t* sin_tab, int sm_count,
+                               cudaStream_t s);
 // e4m3 cache rows: q[row][0..255] and scale[row] for n_rows rows of 256 bf16 values.
 cudaError_t launch_quantize_e4m3(const uint16_t* x, long long n_rows, uint8_t* q, float* scale,
                                  cudaStream_t s);

@@ -76,31 +76,41 @@ __device__ __forceinline__ void load_row(const uint16_t* p, int l, RowVals& v) {
   }
 }
 
-// Rows are (token, head) pairs over n_heads heads head0 .. head0+n_heads-1 of a token that
-// has heads_per_tok heads: row r is token r / n_heads, head head0 + r % n_heads; it reads 256
-// values at src + (token * heads_per_tok + head) * src_stride and writes 256 at dst +
-// (token * heads_per_tok + head) * 256. Token t sits at position pos_base + t, or, with kSeq,
-// at the position its sequence gives (SeqPositions).
+// One run of rows: (token, head) pairs over n_heads heads head0 .. head0+n_heads-1 of a
+// token that has heads_per_tok heads. Row r is token r / n_heads, head head0 + r % n_heads;
+// it reads 256 values at src + (token * heads_per_tok + head) * src_stride and writes 256 at
+// dst + (token * heads_per_tok + head) * 256, normed with w_norm. Token t sits at position
+// pos_base + t, or, with kSeq, at the position its sequence gives (SeqPositions).
+struct PrologueRows {
+  const uint16_t* src;
+  uint16_t* dst;
+  const uint16_t* w_norm;
+  long long n_rows;   // callers keep it below 2^31
+  int src_stride, heads_per_tok, head0, n_heads, pos_base;
+};
+
+// The rows first, first + stride, ... of one run, by this half-warp.
 template <bool kSeq>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSm)
-    prologue_kernel(const uint16_t* __restrict__ src, int src_stride, int heads_per_tok,
-                    int head0, int n_heads, const uint16_t* __restrict__ w_norm,
-                    const uint16_t* __restrict__ cos_tab, const uint16_t* __restrict__ sin_tab,
-                    long long n_rows, int pos_base, const __grid_constant__ SeqPositions sp,
-                    uint16_t* __restrict__ dst) {
+__device__ __forceinline__ void prologue_walk(const PrologueRows& run, int first, int stride,
+                                              const uint16_t* __restrict__ cos_tab,
+                                              const uint16_t* __restrict__ sin_tab,
+                                              const SeqPositions& sp) {
+  const uint16_t* __restrict__ src = run.src;
+  uint16_t* __restrict__ dst = run.dst;
+  const int src_stride = run.src_stride, heads_per_tok = run.heads_per_tok;
+  const int head0 = run.head0, n_heads = run.n_heads, pos_base = run.pos_base;
   const int l = threadIdx.x & 15;
   const unsigned hmask = 0xFFFFu << (threadIdx.x & 16);   // this half-warp's lanes
   // rows are walked as (token, head) pairs: no division inside the loop
-  const int n_rows32 = (int)n_rows;                          // callers keep it below 2^31
-  const int stride = gridDim.x * (kThreads / 16);
-  int row = blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
+  const int n_rows32 = (int)run.n_rows;
+  int row = first;
   if (row >= n_rows32) return;   // whole half-warps leave together
   const int stride_tok = stride / n_heads, stride_head = stride - stride_tok * n_heads;
   int tok = row / n_heads, head = row - tok * n_heads;
 
   // this lane's norm weights, in the value order of RowVals (two bf16 per word)
   RowVals wv;
-  load_row(w_norm, l, wv);
+  load_row(run.w_norm, l, wv);
   // element offset of the row (token t, head hd) in an array of rows stride_el values apart
   auto row_off = [&](int t, int hd, int stride_el) -> long long {
     return ((long long)t * heads_per_tok + head0 + hd) * stride_el;
@@ -224,40 +234,81 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSm)
   }
 }
 
+// One persistent grid over up to two runs of rows: every half-warp walks its rows of run0,
+// then its rows of run1 (n_rows 0: none), the two runs dealt as one sequence of rows so that
+// the half-warps' shares differ by one row at most.
+template <bool kSeq>
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm)
+    prologue_kernel(const __grid_constant__ PrologueRows run0,
+                    const __grid_constant__ PrologueRows run1,
+                    const uint16_t* __restrict__ cos_tab, const uint16_t* __restrict__ sin_tab,
+                    const __grid_constant__ SeqPositions sp) {
+  const int stride = gridDim.x * (kThreads / 16);
+  const int hw = blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
+  prologue_walk<kSeq>(run0, hw, stride, cos_tab, sin_tab, sp);
+  if (run1.n_rows > 0) {
+    // the first row of run1 in this half-warp's share of the joined sequence
+    const int first = (int)((((long long)hw - run0.n_rows) % stride + stride) % stride);
+    prologue_walk<kSeq>(run1, first, stride, cos_tab, sin_tab, sp);
+  }
+}
+
 unsigned prologue_grid(long long n_rows, int sm_count) {
   const long long need = (n_rows + kThreads / 16 - 1) / (kThreads / 16);
   const long long cap = (long long)(sm_count > 0 ? sm_count : 1) * kBlocksPerSm;
   return (unsigned)(need < cap ? need : cap);
 }
 
+PrologueRows k_rows(const uint16_t* k_raw, const uint16_t* w_k, int n_tok, int pos_base,
+                    uint16_t* k_prep) {
+  return PrologueRows{k_raw, k_prep, w_k, (long long)n_tok * kKvHeads, kDim, kKvHeads, 0,
+                      kKvHeads, pos_base};
+}
+PrologueRows q_rows(const uint16_t* qg, const uint16_t* w_q, int rows, int q_base, int head0,
+                    int n_heads, uint16_t* q_prep) {
+  return PrologueRows{qg, q_prep, w_q, (long long)rows * n_heads, kQgStride, kHeads, head0,
+                      n_heads, q_base};
+}
+PrologueRows no_rows() { return PrologueRows{nullptr, nullptr, nullptr, 0, 0, 1, 0, 1, 0}; }
+
 }  // namespace
 
 cudaError_t launch_k_prologue(const uint16_t* k_raw, const uint16_t* w_k, const uint16_t* cos_tab,
                               const uint16_t* sin_tab, int n_tok, int pos_base, uint16_t* k_prep,
                               int sm_count, cudaStream_t s) {
-  const long long n_rows = (long long)n_tok * kKvHeads;
-  prologue_kernel<false><<<prologue_grid(n_rows, sm_count), kThreads, 0, s>>>(
-      k_raw, kDim, kKvHeads, 0, kKvHeads, w_k, cos_tab, sin_tab, n_rows, pos_base,
-      SeqPositions{}, k_prep);
+  const PrologueRows run = k_rows(k_raw, w_k, n_tok, pos_base, k_prep);
+  prologue_kernel<false><<<prologue_grid(run.n_rows, sm_count), kThreads, 0, s>>>(
+      run, no_rows(), cos_tab, sin_tab, SeqPositions{});
   return cudaGetLastError();
 }
 
 cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
                               const uint16_t* sin_tab, int rows, int q_base, int head0,
                               int n_heads, uint16_t* q_prep, int sm_count, cudaStream_t s) {
-  const long long n_rows = (long long)rows * n_heads;
-  prologue_kernel<false><<<prologue_grid(n_rows, sm_count), kThreads, 0, s>>>(
-      qg, kQgStride, kHeads, head0, n_heads, w_q, cos_tab, sin_tab, n_rows, q_base,
-      SeqPositions{}, q_prep);
+  const PrologueRows run = q_rows(qg, w_q, rows, q_base, head0, n_heads, q_prep);
+  prologue_kernel<false><<<prologue_grid(run.n_rows, sm_count), kThreads, 0, s>>>(
+      run, no_rows(), cos_tab, sin_tab, SeqPositions{});
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qk_prologue(const uint16_t* k_raw, const uint16_t* w_k, int n_tok,
+                               int k_pos_base, uint16_t* k_prep, const uint16_t* qg,
+                               const uint16_t* w_q, int rows, int q_base, uint16_t* q_prep,
+                               const uint16_t* cos_tab, const uint16_t* sin_tab, int sm_count,
+                               cudaStream_t s) {
+  const PrologueRows rk = k_rows(k_raw, w_k, n_tok, k_pos_base, k_prep);
+  const PrologueRows rq = q_rows(qg, w_q, rows, q_base, 0, kHeads, q_prep);
+  prologue_kernel<false><<<prologue_grid(rk.n_rows + rq.n_rows, sm_count), kThreads, 0, s>>>(
+      rk, rq, cos_tab, sin_tab, SeqPositions{});
   return cudaGetLastError();
 }
 
 cudaError_t launch_q_prologue_seq(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
                                   const uint16_t* sin_tab, int n_tok, const SeqPositions& sp,
                                   uint16_t* q_prep, int sm_count, cudaStream_t s) {
-  const long long n_rows = (long long)n_tok * kHeads;
-  prologue_kernel<true><<<prologue_grid(n_rows, sm_count), kThreads, 0, s>>>(
-      qg, kQgStride, kHeads, 0, kHeads, w_q, cos_tab, sin_tab, n_rows, 0, sp, q_prep);
+  const PrologueRows run = q_rows(qg, w_q, n_tok, 0, 0, kHeads, q_prep);
+  prologue_kernel<true><<<prologue_grid(run.n_rows, sm_count), kThreads, 0, s>>>(
+      run, no_rows(), cos_tab, sin_tab, sp);
   return cudaGetLastError();
 }
 
