@@ -93,6 +93,18 @@ def test_verify_long_cache_sampled():
         refs[b].check(out[b], what=f"verify L=65536 seq {b} heads {heads}")
 
 
+def test_verify_one_sequence_l65536_many_chunks():
+    """One sequence of 16 rows over 65,536 cached keys: the launch splits its keys into 37
+    chunks (more than one warp's lanes), so the combine reads its (M, l) pairs from two lanes
+    per row and sums the partial rows four chunks at a time; sampled heads against the
+    oracle."""
+    lens, rows, cap = [65536], 16, 65552
+    out, data, kd, _ = _run(SEED + 35, lens, rows, cap)
+    heads = [0, 13, 23]
+    _refs(data, lens, cap, heads=heads)[0].check(out[0], what=f"verify L=65536, one sequence, "
+                                                             f"heads {heads}")
+
+
 def test_verify_8x16_l65536_launch_sampled():
     """The benchmark's launch: 8 sequences x 16 rows at positions 65,536..65,551 over caches
     of 65,552 positions (the chunking the bench times); two sequences' sampled heads

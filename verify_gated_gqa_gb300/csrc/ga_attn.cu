@@ -1546,12 +1546,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (kCluster) cluster_sync_all();
 }
 
+constexpr int kCombineChunkSlots = 3;   // (M, l) pairs per lane: up to 96 chunks
+constexpr int kCombineBatch = 4;        // partial rows loaded ahead of their sums
+static_assert(kVerifyChunkCap / 4 <= 32 * kCombineChunkSlots, "a verify row has at most 96 chunks");
+
 // Verify combine (TensorFold PR #1080, "qwen CUDA: long-prompt prefill 5.4x faster", the
 // attn_partial commit: key chunks processed apart, then merged per row). One warp per
 // (sequence, query head, row); lane l holds dims 8l .. 8l+7. With M = max_c M_c over the
 // chunks the row saw keys in, O = sum_c 2^(M_c - M) O_c and L = sum_c 2^(M_c - M) l_c (exact
 // power-of-two scales, chunks in order), o = bf16(O / L), out = bf16(o * bf16(sigmoid(g))).
-__global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_constant__ AttnArgs a) {
+// The loads do not wait on one another: all (M_c, l_c) are read at once, the partial rows
+// four chunks at a time, and only the sums run in chunk order.
+__global__ void __launch_bounds__(256, 3) verify_combine_kernel(const __grid_constant__ AttnArgs a) {
   const int lane = threadIdx.x & 31;
   const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (w >= a.n_seq * kHeads * a.vrows) return;
@@ -1564,24 +1570,48 @@ __global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_consta
   const int chunks = (tiles + a.chunk_tiles - 1) / a.chunk_tiles;
   const size_t slot0 = (((size_t)b * kKvHeads + kvh) * 2 + half) * a.n_chunks;
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+  // every chunk's (M_c, l_c) at once: lane l holds chunks l, l + 32 and l + 64
+  float2 mlv[kCombineChunkSlots];
   float M = -INFINITY;
-  for (int c = 0; c < chunks; ++c) {
-    const float2 v = ml[(slot0 + c) * kVerifyLanes + lanep];
-    if (v.y > 0.f) M = fmaxf(M, v.x);
+#pragma unroll
+  for (int k = 0; k < kCombineChunkSlots; ++k) {
+    const int c = lane + 32 * k;
+    mlv[k] = c < chunks ? ml[(slot0 + c) * kVerifyLanes + lanep] : make_float2(0.f, 0.f);
+    if (mlv[k].y > 0.f) M = fmaxf(M, mlv[k].x);
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  // the chunks in order, four chunks' partial rows in flight at a time; chunk c's scale
+  // and sum come from lane c % 32
   float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float L = 0.f;
-  for (int c = 0; c < chunks; ++c) {
-    const size_t prow = (slot0 + c) * kVerifyLanes + lanep;
-    const float2 v = ml[prow];
-    if (!(v.y > 0.f)) continue;
-    const float f = ldexpf(1.0f, (int)(v.x - M));   // an exact power of two
-    L = fmaf(f, v.y, L);
-    const float4* op = reinterpret_cast<const float4*>(a.part_o + prow * kDim) + 2 * lane;
-    const float4 p0 = op[0], p1 = op[1];
-    o[0] = fmaf(f, p0.x, o[0]); o[1] = fmaf(f, p0.y, o[1]); o[2] = fmaf(f, p0.z, o[2]);
-    o[3] = fmaf(f, p0.w, o[3]); o[4] = fmaf(f, p1.x, o[4]); o[5] = fmaf(f, p1.y, o[5]);
-    o[6] = fmaf(f, p1.z, o[6]); o[7] = fmaf(f, p1.w, o[7]);
+  for (int c0 = 0; c0 < chunks; c0 += kCombineBatch) {
+    float4 p[kCombineBatch][2];
+#pragma unroll
+    for (int j = 0; j < kCombineBatch; ++j) {
+      if (c0 + j < chunks) {
+        const float4* op = reinterpret_cast<const float4*>(
+                               a.part_o + ((slot0 + c0 + j) * kVerifyLanes + lanep) * kDim) + 2 * lane;
+        p[j][0] = op[0];
+        p[j][1] = op[1];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kCombineBatch; ++j) {
+      const int c = c0 + j;
+      if (c >= chunks) break;
+      const int k = c >> 5;   // the same for every lane
+      const float2 mine = k == 0 ? mlv[0] : (k == 1 ? mlv[1] : mlv[2]);
+      const float mc = __shfl_sync(0xFFFFFFFFu, mine.x, c & 31);
+      const float lc = __shfl_sync(0xFFFFFFFFu, mine.y, c & 31);
+      if (!(lc > 0.f)) continue;
+      const float f = ldexpf(1.0f, (int)(mc - M));   // an exact power of two
+      L = fmaf(f, lc, L);
+      const float4 p0 = p[j][0], p1 = p[j][1];
+      o[0] = fmaf(f, p0.x, o[0]); o[1] = fmaf(f, p0.y, o[1]); o[2] = fmaf(f, p0.z, o[2]);
+      o[3] = fmaf(f, p0.w, o[3]); o[4] = fmaf(f, p1.x, o[4]); o[5] = fmaf(f, p1.y, o[5]);
+      o[6] = fmaf(f, p1.z, o[6]); o[7] = fmaf(f, p1.w, o[7]);
+    }
   }
   const float inv = L > 0.f ? 1.0f / L : 0.f;
   const size_t row = (size_t)b * a.vrows + rr;

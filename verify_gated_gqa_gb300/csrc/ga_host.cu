@@ -283,7 +283,6 @@ MaskedLayout masked_layout(int rows, int T) {
 // of each sequence in n_chunks chunks of chunk_tiles 128-key tiles, with about two work
 // items (chunk x sequence x KV head x half group) per SM. The workspace holds one group's
 // partials; its size does not depend on the device (at most kVerifyChunkCap / n_seq chunks).
-constexpr int kVerifyChunkCap = 320;
 struct VerifyPlan {
   int n_seq_group, n_tiles_max, n_chunks_cap;
 };

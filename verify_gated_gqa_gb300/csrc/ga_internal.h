@@ -48,6 +48,9 @@ constexpr int kVerifyHeadsPerTile = 6;
 constexpr int kVerifyMaxRows = 16;
 constexpr int kVerifyLanes = kVerifyHeadsPerTile * kVerifyMaxRows;   // 96
 constexpr int kVerifyMaxSeq = 64;       // sequences per launch (the host loops over groups)
+// Work items (chunk x sequence x KV head x half group) of one verify launch at most: the
+// partial workspace holds kVerifyChunkCap / (4 n_seq) chunks per sequence, 80 at n_seq = 1.
+constexpr int kVerifyChunkCap = 320;
 
 // Stored-mask bits, as the mask prepass writes them for the attention kernel. Key j of a
 // 32-key word sits at bit 8 (j % 4) + 7 - j / 4: shifted left by s = 0..7, the word holds
