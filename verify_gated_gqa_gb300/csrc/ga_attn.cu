@@ -1547,19 +1547,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 constexpr int kCombineChunkSlots = 3;   // (M, l) pairs per lane: up to 96 chunks
-constexpr int kCombineBatch = 4;        // partial rows loaded ahead of their sums
 static_assert(kVerifyChunkCap / 4 <= 32 * kCombineChunkSlots, "a verify row has at most 96 chunks");
 
+// kDpl consecutive floats (8 bytes aligned; 16 when kDpl is a multiple of 4) into v.
+template <int kDpl>
+__device__ __forceinline__ void load_dims(const float* p, float (&v)[kDpl]) {
+  if constexpr (kDpl % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < kDpl / 4; ++i) {
+      const float4 t = reinterpret_cast<const float4*>(p)[i];
+      v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kDpl / 2; ++i) {
+      const float2 t = reinterpret_cast<const float2*>(p)[i];
+      v[2 * i] = t.x; v[2 * i + 1] = t.y;
+    }
+  }
+}
+
 // Verify combine (TensorFold PR #1080, "qwen CUDA: long-prompt prefill 5.4x faster", the
-// attn_partial commit: key chunks processed apart, then merged per row). One warp per
-// (sequence, query head, row); lane l holds dims 8l .. 8l+7. With M = max_c M_c over the
-// chunks the row saw keys in, O = sum_c 2^(M_c - M) O_c and L = sum_c 2^(M_c - M) l_c (exact
-// power-of-two scales, chunks in order), o = bf16(O / L), out = bf16(o * bf16(sigmoid(g))).
-// The loads do not wait on one another: all (M_c, l_c) are read at once, the partial rows
-// four chunks at a time, and only the sums run in chunk order.
-__global__ void __launch_bounds__(256, 3) verify_combine_kernel(const __grid_constant__ AttnArgs a) {
+// attn_partial commit: key chunks processed apart, then merged per row). kSplit warps per
+// (sequence, query head, row), warp q taking dims (256 / kSplit) q .. , lane l kDpl = 8 /
+// kSplit consecutive dims of them. With M = max_c M_c over the chunks the row saw keys in,
+// O = sum_c 2^(M_c - M) O_c and L = sum_c 2^(M_c - M) l_c (exact power-of-two scales, chunks
+// in order), o = bf16(O / L), out = bf16(o * bf16(sigmoid(g))). The loads do not wait on one
+// another: all (M_c, l_c) are read at once, the partial rows several chunks ahead, and only
+// the sums run in chunk order; calls with few rows split each row over more warps so that
+// the grid still covers the SMs (the bits do not depend on the split).
+template <int kSplit>
+__global__ void __launch_bounds__(256) verify_combine_kernel(const __grid_constant__ AttnArgs a) {
+  constexpr int kDpl = 8 / kSplit;                 // dims per lane
+  constexpr int kBatch = kDpl == 8 ? 4 : 8;        // chunks' partial values in flight
   const int lane = threadIdx.x & 31;
-  const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int wg = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int w = wg / kSplit, part = wg % kSplit;
   if (w >= a.n_seq * kHeads * a.vrows) return;
   const int rr = w % a.vrows;
   const int h = (w / a.vrows) % kHeads;
@@ -1569,6 +1592,7 @@ __global__ void __launch_bounds__(256, 3) verify_combine_kernel(const __grid_con
   const int tiles = (a.seq_len[b] + a.vrows + kTileN - 1) / kTileN;
   const int chunks = (tiles + a.chunk_tiles - 1) / a.chunk_tiles;
   const size_t slot0 = (((size_t)b * kKvHeads + kvh) * 2 + half) * a.n_chunks;
+  const int d0 = (kDim / kSplit) * part + kDpl * lane;   // this lane's first dim
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
   // every chunk's (M_c, l_c) at once: lane l holds chunks l, l + 32 and l + 64
   float2 mlv[kCombineChunkSlots];
@@ -1581,23 +1605,20 @@ __global__ void __launch_bounds__(256, 3) verify_combine_kernel(const __grid_con
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
-  // the chunks in order, four chunks' partial rows in flight at a time; chunk c's scale
+  // the chunks in order, kBatch chunks' partial values in flight at a time; chunk c's scale
   // and sum come from lane c % 32
-  float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float o[kDpl];
+#pragma unroll
+  for (int i = 0; i < kDpl; ++i) o[i] = 0.f;
   float L = 0.f;
-  for (int c0 = 0; c0 < chunks; c0 += kCombineBatch) {
-    float4 p[kCombineBatch][2];
+  for (int c0 = 0; c0 < chunks; c0 += kBatch) {
+    float p[kBatch][kDpl];
 #pragma unroll
-    for (int j = 0; j < kCombineBatch; ++j) {
-      if (c0 + j < chunks) {
-        const float4* op = reinterpret_cast<const float4*>(
-                               a.part_o + ((slot0 + c0 + j) * kVerifyLanes + lanep) * kDim) + 2 * lane;
-        p[j][0] = op[0];
-        p[j][1] = op[1];
-      }
-    }
+    for (int j = 0; j < kBatch; ++j)
+      if (c0 + j < chunks)
+        load_dims<kDpl>(a.part_o + ((slot0 + c0 + j) * kVerifyLanes + lanep) * kDim + d0, p[j]);
 #pragma unroll
-    for (int j = 0; j < kCombineBatch; ++j) {
+    for (int j = 0; j < kBatch; ++j) {
       const int c = c0 + j;
       if (c >= chunks) break;
       const int k = c >> 5;   // the same for every lane
@@ -1607,23 +1628,27 @@ __global__ void __launch_bounds__(256, 3) verify_combine_kernel(const __grid_con
       if (!(lc > 0.f)) continue;
       const float f = ldexpf(1.0f, (int)(mc - M));   // an exact power of two
       L = fmaf(f, lc, L);
-      const float4 p0 = p[j][0], p1 = p[j][1];
-      o[0] = fmaf(f, p0.x, o[0]); o[1] = fmaf(f, p0.y, o[1]); o[2] = fmaf(f, p0.z, o[2]);
-      o[3] = fmaf(f, p0.w, o[3]); o[4] = fmaf(f, p1.x, o[4]); o[5] = fmaf(f, p1.y, o[5]);
-      o[6] = fmaf(f, p1.z, o[6]); o[7] = fmaf(f, p1.w, o[7]);
+#pragma unroll
+      for (int i = 0; i < kDpl; ++i) o[i] = fmaf(f, p[j][i], o[i]);
     }
   }
   const float inv = L > 0.f ? 1.0f / L : 0.f;
   const size_t row = (size_t)b * a.vrows + rr;
-  const uint4 gv = __ldg(reinterpret_cast<const uint4*>(a.qg + (row * kHeads + h) * kQgStride + kDim) + lane);
-  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-  uint32_t res[4];
+  const uint32_t* gp = reinterpret_cast<const uint32_t*>(a.qg + (row * kHeads + h) * kQgStride + kDim + d0);
+  uint32_t* op = reinterpret_cast<uint32_t*>(a.out + row * kOutRow + h * kDim + d0);
+  uint32_t res[kDpl / 2];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < kDpl / 2; ++k) {
     const uint32_t ob = pack_bf16x2(o[2 * k] * inv, o[2 * k + 1] * inv);
-    res[k] = mul_bf16x2(ob, sigmoid_pair(gw[k]));
+    res[k] = mul_bf16x2(ob, sigmoid_pair(__ldg(gp + k)));
   }
-  reinterpret_cast<uint4*>(a.out + row * kOutRow + h * kDim)[lane] = make_uint4(res[0], res[1], res[2], res[3]);
+  if constexpr (kDpl == 8) {
+    *reinterpret_cast<uint4*>(op) = make_uint4(res[0], res[1], res[2], res[3]);
+  } else if constexpr (kDpl == 4) {
+    *reinterpret_cast<uint2*>(op) = make_uint2(res[0], res[1]);
+  } else {
+    op[0] = res[0];
+  }
 }
 
 // Test hook: one thread waits, with a bound of `limit` cycles, on an mbarrier that nothing
@@ -1648,9 +1673,18 @@ cudaError_t launch_wait_timeout(long long limit, int* status, cudaStream_t s) {
 
 size_t attn_smem_bytes() { return sizeof(AttnSmem); }
 
-cudaError_t launch_verify_combine(const AttnArgs& a, cudaStream_t s) {
-  const int warps = a.n_seq * kHeads * a.vrows;
-  verify_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(a);
+cudaError_t launch_verify_combine(const AttnArgs& a, int sm_count, cudaStream_t s) {
+  // one warp per row when the rows alone fill the SMs (about 24 warps resident per SM),
+  // else the row split over 2 or 4 warps
+  const int rows = a.n_seq * kHeads * a.vrows;
+  const int fill = 24 * (sm_count > 0 ? sm_count : 1);
+  if (rows * 2 > fill) {
+    verify_combine_kernel<1><<<(rows + 7) / 8, 256, 0, s>>>(a);
+  } else if (rows * 4 > fill) {
+    verify_combine_kernel<2><<<(rows * 2 + 7) / 8, 256, 0, s>>>(a);
+  } else {
+    verify_combine_kernel<4><<<(rows * 4 + 7) / 8, 256, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

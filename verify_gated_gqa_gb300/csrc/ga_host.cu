@@ -466,7 +466,7 @@ int verify_run(const ga_bf16* qg, const VerifyCaches& c, const int* seq_len, int
     // the verify partials have no gated epilogue: tm_q stands in for the unused gate map
     if ((e = GA_CUDA(launch_attn(tm_q, tm_k, tm_v, tm_q, tm_q, a, grid, s))) != cudaSuccess)
       return fail_cuda(e);
-    if ((e = GA_CUDA(launch_verify_combine(a, s))) != cudaSuccess) return fail_cuda(e);
+    if ((e = GA_CUDA(launch_verify_combine(a, dev->sm_count, s))) != cudaSuccess) return fail_cuda(e);
   }
   return GA_OK;
 }

@@ -122,7 +122,7 @@ cudaError_t launch_q_prologue_seq(const uint16_t* qg, const uint16_t* w_q, const
                                   const uint16_t* sin_tab, int n_tok, const SeqPositions& sp,
                                   uint16_t* q_prep, int sm_count, cudaStream_t s);
 // Merges the verify partials and applies the gate: out[b][rr][h*256 ..].
-cudaError_t launch_verify_combine(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_verify_combine(const AttnArgs& a, int sm_count, cudaStream_t s);
 // Prepared query rows: q_prep[r][h][0..255] = rope(norm(qg[r][h][0..255])) at q_base + r,
 // for the heads head0 .. head0+n_heads-1 (the other heads' slots are not written).
 cudaError_t launch_q_prologue(const uint16_t* qg, const uint16_t* w_q, const uint16_t* cos_tab,
