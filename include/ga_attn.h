@@ -115,13 +115,15 @@ int ga_device_status(int* status_out, int clear);
 int ga_debug_wait_timeout(long long limit_cycles, ga_stream stream);
 
 /* Selects how the attention passes run (no counterpart in the pages; the results are the
- * same bits either way). mode 1 (the default): the causal, bidirectional, stored-mask and
- * batched passes as clusters of two CTAs that share each key and value tile, two query heads
- * of one KV group per pair item, whenever the call's heads come in such pairs (every call
- * through the ABI does: the KV-group entry points take whole groups of 12); the weights pass
- * and the verify passes on single CTAs. mode 0: every pass on single CTAs (one CTA per
- * 128-row tile and head). Process-wide; takes effect from the next call. Returns the
- * previous mode (0 or 1). Errors: RANGE (mode outside 0 .. 1). Makes no CUDA call. */
+ * same bits either way). mode 2: the causal, bidirectional, stored-mask and batched passes
+ * as clusters of two CTAs that share each key and value tile, two query heads of one KV
+ * group per pair item, whenever the call's heads come in such pairs (every call through the
+ * ABI does: the KV-group entry points take whole groups of 12); the weights pass and the
+ * verify passes on single CTAs. mode 1 (the default): the same, except that causal,
+ * bidirectional and stored-mask calls over fewer than 2,048 keys run on single CTAs, which
+ * are faster there. mode 0: every pass on single CTAs (one CTA per 128-row tile and head).
+ * Process-wide; takes effect from the next call. Returns the previous mode (0, 1 or 2).
+ * Errors: RANGE (mode outside 0 .. 2). Makes no CUDA call. */
 int ga_debug_set_cta_pairs(int mode);
 
 /* Test hook: the fp32 dot products the tensor cores form for the scores, before any

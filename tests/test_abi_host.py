@@ -386,13 +386,14 @@ def test_qk_probe_refusals(L):
 
 
 def test_pair_switch(L):
-    """The form switch makes no CUDA call: modes 0 and 1 round-trip, the rest are refused
-    with RANGE and leave the mode as it was."""
+    """The form switch makes no CUDA call: modes 0, 1 and 2 round-trip, the rest are
+    refused with RANGE and leave the mode as it was."""
     before = L.ga_debug_cuda_calls()
     mode = L.ga_debug_set_cta_pairs(0)
-    assert mode in (0, 1)
-    assert L.ga_debug_set_cta_pairs(2) == -4 and L.ga_debug_set_cta_pairs(-1) == -4
-    assert L.ga_debug_set_cta_pairs(mode) == 0
+    assert mode in (0, 1, 2)
+    assert L.ga_debug_set_cta_pairs(3) == -4 and L.ga_debug_set_cta_pairs(-1) == -4
+    assert L.ga_debug_set_cta_pairs(2) == 0
+    assert L.ga_debug_set_cta_pairs(mode) == 2
     assert L.ga_debug_cuda_calls() == before
 
 

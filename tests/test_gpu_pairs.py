@@ -35,8 +35,9 @@ def _pairs(enable):
         B.ga_debug_set_cta_pairs(prev)
 
 
-def _both(fn, mode=1):
-    """fn() under single CTAs and under CTA pairs; both results (tuples of tensors)."""
+def _both(fn, mode=2):
+    """fn() under single CTAs and under CTA pairs (mode 2: wherever the heads allow them,
+    whatever the size); both results (tuples of tensors)."""
     with _pairs(0):
         single = fn()
         torch.cuda.synchronize()
@@ -56,8 +57,28 @@ def _equal(single, paired):
 
 def test_switch_round_trips():
     prev = B.ga_debug_set_cta_pairs(1)
-    assert B.ga_debug_set_cta_pairs(0) == 1
+    assert B.ga_debug_set_cta_pairs(2) == 1
+    assert B.ga_debug_set_cta_pairs(0) == 2
     assert B.ga_debug_set_cta_pairs(prev) == 0
+
+
+def test_default_mode_picks_by_keys():
+    """Mode 1 (the default) runs a call over 1,024 keys on single CTAs and one over 2,048
+    keys as pairs; at both sizes its output is the same bits as modes 0 and 2 give."""
+    for S in (1024, 2048):
+        inp = Inputs(SEED + 91, S, S)
+        d = inp.dev()
+
+        def run():
+            return (B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"],
+                                      d["sin"], 0, S),)
+
+        with _pairs(1):
+            default = run()
+            torch.cuda.synchronize()
+        single, paired = _both(run)
+        _equal(single, default)
+        _equal(paired, default)
 
 
 @pytest.mark.parametrize("S,causal", [(64, True), (333, True), (333, False), (2048, True),

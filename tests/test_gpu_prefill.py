@@ -245,7 +245,7 @@ def test_gate_every_bf16_value(pairs):
     inp.cpu["v"] = torch.ones_like(inp.cpu["v"])
     inp.np["v"] = np64(inp.cpu["v"])
     d = inp.dev()
-    prev = B.ga_debug_set_cta_pairs(pairs)
+    prev = B.ga_debug_set_cta_pairs(2 if pairs else 0)
     try:
         got = B.ga_attn_prefill(d["qg"], d["k_prep"], d["v"], d["w_q"], d["cos"], d["sin"], 0,
                                 rows)

@@ -184,7 +184,7 @@ def test_batch_pairs_equal_single(page_size):
     tab = torch.from_numpy(table).cuda()
     outs = []
     for pairs in (False, True):
-        prev = B.ga_debug_set_cta_pairs(pairs)
+        prev = B.ga_debug_set_cta_pairs(2 if pairs else 0)
         try:
             outs.append(B.ga_attn_prefill_batch(qg, starts, [qb for qb, _ in spec], kpool, vpool,
                                                 tab, w_q, c, s))

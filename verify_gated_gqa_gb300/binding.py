@@ -146,9 +146,10 @@ def ga_debug_cuda_calls() -> int:
 
 
 def ga_debug_set_cta_pairs(mode) -> int:
-    """0 (or False): every pass on single CTAs; 1 (or True, the default): the causal,
-    bidirectional, stored-mask and batched passes as CTA pairs. The same bits either way.
-    Returns the previous mode."""
+    """0 (or False): every pass on single CTAs; 2: the causal, bidirectional, stored-mask
+    and batched passes as CTA pairs; 1 (or True, the default): the same, but single CTAs for
+    calls over fewer than 2,048 keys (batches excepted). The same bits either way. Returns
+    the previous mode."""
     st = lib().ga_debug_set_cta_pairs(int(mode))
     if st < 0:
         _check(st, "ga_debug_set_cta_pairs")

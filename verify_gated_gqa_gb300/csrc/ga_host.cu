@@ -306,7 +306,15 @@ size_t verify_ws_bytes(const VerifyPlan& p) {
 // The query prologue (unless q_ready: q_prep already holds this call's prepared queries)
 // and the attention kernel. q_prep [rows][24][256] may be the output buffer itself: each
 // (row, head) slot is read by the work item that later writes its output there.
-std::atomic<int> g_cta_pairs{1};   // ga_debug_set_cta_pairs: 0 single CTAs, 1 CTA pairs
+// ga_debug_set_cta_pairs: 0 single CTAs; 1 CTA pairs where they pay (below); 2 CTA pairs
+// wherever the heads allow them
+std::atomic<int> g_cta_pairs{1};
+// Keys below which a single-sequence pass runs on single CTAs under mode 1: measured on one
+// box from a flushed L2, causal and bidirectional, the pairs' cluster set-up and staging
+// chain cost about 2 us per call up to 1,024 keys (S = 64: 17.1 against 15.0 us; S = 1024
+// causal: 31.4 against 29.3 us) and win from 2,048 keys on (53.9 against 55.9 us; at
+// 4,096: 135.8 against 144.1 us).
+constexpr int kPairMinKeys = 2048;
 
 int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const void* k_prep,
                      const void* v, long long n_tok, DeviceState* dev, cudaStream_t s) {
@@ -317,9 +325,11 @@ int launch_attention(const AttnArgs& a0, uint16_t* q_prep, bool q_ready, const v
     a.n_heads = kHeads;
   }
   // The causal, bidirectional and stored-mask passes run as CTA pairs (two query heads of
-  // one KV group per pair item) whenever the heads come in such pairs; the weights pass
-  // runs on single CTAs.
-  const bool pair = g_cta_pairs.load() > 0 && !a.weights_pass &&
+  // one KV group per pair item) whenever the heads come in such pairs and the keys are
+  // many enough for the pairs to pay (kPairMinKeys); the weights pass runs on single CTAs.
+  const int pair_mode = g_cta_pairs.load();
+  const bool pair = (pair_mode == 2 || (pair_mode == 1 && a.T >= kPairMinKeys)) &&
+                    !a.weights_pass &&
                     (a.mode == kModeCausal || a.mode == kModeBidir || a.mode == kModeMask) &&
                     a.head0 % 2 == 0 && a.n_heads % 2 == 0;
   a.pair = pair ? 1 : 0;
@@ -487,7 +497,9 @@ int batch_run(const ga_bf16* qg, const BatchPiece* pieces, int n_pieces, const g
   if (st != GA_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   // CTA pairs (two query heads of a KV group per pair item, each CTA holding half of every
-  // K and V tile: maps of half boxes) unless switched off
+  // K and V tile: maps of half boxes) unless switched off: a batch of prompts walks enough
+  // key tiles for them in every size measured (16 prompts of 512 to 4,096 tokens: 1.09
+  // against 1.29 ms)
   const bool pair = g_cta_pairs.load() > 0;
   CUtensorMap tm_k, tm_v;
   st = pair ? encode_kv_map(&tm_k, k_pages, page_size, n_pages, true, kTileN / 2, kDim / 64)
@@ -631,7 +643,7 @@ int ga_debug_wait_timeout(long long limit_cycles, ga_stream stream) {
 }
 
 int ga_debug_set_cta_pairs(int mode) {
-  if (mode < 0 || mode > 1) return GA_ERR_RANGE;
+  if (mode < 0 || mode > 2) return GA_ERR_RANGE;
   return g_cta_pairs.exchange(mode);
 }
 
