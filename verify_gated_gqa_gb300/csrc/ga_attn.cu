@@ -1391,7 +1391,9 @@ __device__ void edge_worker(AttnSmem& sm, const AttnArgs& a, const CUtensorMap* 
     if (kMode == kModeVerify8 && !widen_item(cur, cur_q)) return;
     if (has_gate<kMode, kW>()) {
       if (!take_gate(cur_q + (cur.n >= 2 ? 3 : 2), sg)) return;
-      gate_sigmoid(sg);
+      // rows past the sequence's end are never stored: their lookups are skipped (whole
+      // warps in a ragged last tile, which frees the L1 for the rows that count)
+      if (cur.mt * kTileM + r < cur.rows) gate_sigmoid(sg);
     }
     const bool have_next = next_item(nxt);
     const uint32_t nxt_q = q_pos;
