@@ -1129,12 +1129,12 @@ def run_batch(args, world, rank, local):
 
 
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
-# summarised in profiles/attn_kernel_causal_s8192.md (218,614,272 + 61,802,752, the causal
-# variant as CTA pairs) and profiles/attn_kernel_verify_8x16_l65536.md (1,075,817,472 +
-# 7,236,352, the verify variant of attn_kernel); each is to be set to None whenever its
+# summarised in profiles/attn_kernel_causal_s8192.md (218,658,048 + 62,062,080, the causal
+# variant as CTA pairs) and profiles/attn_kernel_verify_8x16_l65536.md (1,075,831,040 +
+# 7,228,672, the verify variant of attn_kernel); each is to be set to None whenever its
 # kernel changes until it is captured again.
-ATTN_TRAFFIC_BYTES = 280_417_024
-VERIFY_ATTN_TRAFFIC_BYTES = 1_083_053_824
+ATTN_TRAFFIC_BYTES = 280_720_128
+VERIFY_ATTN_TRAFFIC_BYTES = 1_083_059_712
 
 
 # ---------------------------------------------------------------- the oracle as baseline
